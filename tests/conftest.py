@@ -1,0 +1,22 @@
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def pytest_configure(config):
+    config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
+    config.addinivalue_line("markers", "slow: long CPU test")
+
+
+@pytest.fixture(scope="session")
+def lib():
+    """The C-ABI library, built in-tree on first use."""
+    from mixed_lora_projection_gb300 import build as _build
+    _build.ensure_built()
+    from mixed_lora_projection_gb300 import _lib
+    return _lib.load()
