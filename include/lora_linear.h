@@ -1,0 +1,191 @@
+/*
+ * lora_linear.h -- shared-base, per-request LoRA projection on one GB300 (sm_103a).
+ *
+ * For a batch of token rows grouped into request segments, one call computes
+ *
+ *     Y[t,:] = X[t,:] W^T + s_a (X[t,:] A_a^T) B_a^T    rows of a segment naming adapter a >= 1
+ *     Y[t,:] = X[t,:] W^T                              rows of a segment naming no adapter (0)
+ *
+ * Source: "Two 27B models on a single RTX 5090", section 3 (each changed matrix of the
+ * fine-tuned model equals the base matrix plus B.A, rank 256) and section 4 (a request
+ * that names the adapter runs the adapter's two thin matrices beside each changed matrix
+ * and adds their output; every other request in the same batch uses the base weights).
+ *
+ * Layouts (all row-major, bf16 = IEEE binary32 upper half, little endian):
+ *   X   [T, d_in]        W   [d_out, d_in]  (nn.Linear layout: row n is output feature n)
+ *   A_a [rank, d_in]     B_a [d_out, rank]  Y   [T, d_out]
+ * Arithmetic: bf16 operands, fp32 accumulation on the tensor cores. The shrink output
+ * U = s_a X A_a^T is rounded to bf16 (round to nearest even) before the expand; Y is
+ * rounded from fp32 to bf16 (round to nearest even). The summation order is not
+ * specified, so results are not bitwise equal to any other implementation.
+ *
+ * Errors: every function returns LORA_OK (0) or a negative code below. Argument checks
+ * run on the host before any launch; a failed check launches nothing and leaves every
+ * output buffer untouched. The library never prints, never aborts the process and never
+ * falls back to another implementation.
+ */
+#ifndef LORA_LINEAR_H
+#define LORA_LINEAR_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct lora_linear lora_linear; /* opaque handle */
+
+enum {
+    LORA_OK = 0,
+    LORA_EINVAL = -1,       /* bad argument (sizes, segments, ids, pointers, alignment, aliasing) */
+    LORA_ENOMEM = -2,       /* a device or pinned-host allocation failed in lora_linear_create */
+    LORA_ECUDA = -3,        /* a CUDA runtime/driver call failed */
+    LORA_ETIMEOUT = -4,     /* a kernel's bounded wait ran out (read by lora_linear_status) */
+    LORA_EUNSUPPORTED = -5, /* valid request this build does not run (no sm_103a device, rank > 256) */
+    LORA_ENODEV = -6        /* the device is not an sm_103 GPU or cannot be used */
+};
+
+/* Limits of this build. */
+#define LORA_MAX_RANK 256   /* adapter rank: the shrink writes at most one 256-column tile */
+#define LORA_TILE_ROWS 128  /* rows per tile of the planner (the tensor-core tile height) */
+
+/*
+ * lora_linear_create -- make a handle for one projection shape on one device.
+ *   out          receives the handle (set to NULL on failure).
+ *   d_in, d_out  input / output features; each a positive multiple of 8 (16-byte rows).
+ *   rank         adapter rank r, a multiple of 8 in [8, LORA_MAX_RANK].
+ *   max_tokens   largest T a forward call will pass (>= 1).
+ *   max_segments largest n_seg a forward call will pass (>= 1).
+ *   device       CUDA device ordinal; it must be an sm_103 GPU.
+ * The handle owns its workspace: the shrink output U (bf16 [max_tokens + 128, rank]),
+ * a ring of work-list buffers (device and pinned host), a device status word and CUDA
+ * events. The caller keeps the current device unchanged across the call.
+ * Returns LORA_OK, LORA_EINVAL, LORA_ENODEV, LORA_ENOMEM or LORA_ECUDA.
+ * Source: the shapes of "Two 27B models on a single RTX 5090", sections 2-3 (hidden
+ * size 5,120, rank 256).
+ */
+int lora_linear_create(lora_linear** out, int d_in, int d_out, int rank,
+                       int max_tokens, int max_segments, int device);
+
+/*
+ * lora_linear_forward -- Y for one batch, enqueued on `stream`; returns without waiting.
+ *   x               device bf16 [T, d_in], 16-byte aligned.
+ *   T               rows (0 <= T <= max_tokens). T = 0 returns LORA_OK and launches nothing.
+ *   seg_offsets     HOST int32 [n_seg + 1]: seg_offsets[0] = 0, seg_offsets[n_seg] = T,
+ *                   nondecreasing. Segment i is rows [seg_offsets[i], seg_offsets[i+1]),
+ *                   one request; empty segments are allowed.
+ *   seg_adapter_ids HOST int32 [n_seg]: 0 = no adapter, k >= 1 = adapter k (A[k-1], ...).
+ *   n_seg           1 <= n_seg <= max_segments (0 allowed only when T = 0).
+ *   W               device bf16 [d_out, d_in], 16-byte aligned.
+ *   A, B            HOST arrays [n_adapters] of device pointers: A[k] bf16 [rank, d_in],
+ *                   B[k] bf16 [d_out, rank], each 16-byte aligned. Only adapters named
+ *                   by a segment are read; the others may be NULL.
+ *   scale           HOST float [n_adapters]: s for each adapter (finite).
+ *   n_adapters      >= 0; every id must be <= n_adapters.
+ *   y               device bf16 [T, d_out], 16-byte aligned; fully overwritten. It must
+ *                   not overlap x, W or any named A/B.
+ *   stream          a cudaStream_t (NULL = the legacy default stream).
+ * Host arrays are read before the call returns. Device buffers must stay valid until
+ * the stream reaches the end of the call. Calls on one handle must be ordered on one
+ * stream (they share the handle's workspace); the handle is not thread-safe.
+ * Returns LORA_OK, LORA_EINVAL (nothing launched) or LORA_ECUDA. A bounded wait that
+ * ran out inside a kernel is reported later by lora_linear_status.
+ * Source: "Two 27B models on a single RTX 5090", section 4 (per-request adapter in a
+ * shared batch) and section 3 (W + B.A).
+ */
+int lora_linear_forward(lora_linear* h, const void* x, int T,
+                        const int32_t* seg_offsets, const int32_t* seg_adapter_ids, int n_seg,
+                        const void* W, const void* const* A, const void* const* B,
+                        const float* scale, int n_adapters, void* y, void* stream);
+
+/*
+ * lora_linear_forward_host -- the same projection from and to HOST memory.
+ *   x_host [T, d_in] and y_host [T, d_out] are host bf16 buffers (pinned memory gives the
+ *   fastest copies); W, A, B stay device pointers (resident weights). The call copies X
+ *   to a device staging buffer owned by the handle, runs lora_linear_forward, copies Y
+ *   back and waits for the stream before returning. The staging buffers are allocated on
+ *   the first call and grow to max_tokens rows. Returns as lora_linear_forward, plus
+ *   LORA_ENOMEM if staging cannot be allocated and LORA_ETIMEOUT if a kernel's bounded
+ *   wait ran out.
+ * Source: as lora_linear_forward.
+ */
+int lora_linear_forward_host(lora_linear* h, const void* x_host, int T,
+                             const int32_t* seg_offsets, const int32_t* seg_adapter_ids, int n_seg,
+                             const void* W, const void* const* A, const void* const* B,
+                             const float* scale, int n_adapters, void* y_host, void* stream);
+
+/* lora_linear_destroy -- wait for the handle's work, free everything it owns. NULL-safe. */
+int lora_linear_destroy(lora_linear* h);
+
+/*
+ * lora_linear_status -- LORA_OK, or LORA_ETIMEOUT if any kernel launched by this handle
+ * gave up a bounded wait (it then stopped early and its output is incomplete). Waits for
+ * the device first. reset != 0 clears the status word afterwards.
+ */
+int lora_linear_status(lora_linear* h, int reset);
+
+/*
+ * lora_linear_plan -- the token-segment planner, on the host (no GPU needed).
+ *   Tiles for the fused base+expand pass: walk the rows in order; a new tile starts when
+ *   the current one holds LORA_TILE_ROWS rows or when the next row names an adapter that
+ *   differs from one already in the tile. Rows with id 0 join the tile they fall in.
+ *   Shrink tiles: the fused tiles with a nonzero id, stably ordered by id.
+ *   fused_tiles / shrink_tiles receive int32 triples (row0, nrows, adapter_id); their
+ *   capacity in triples is *n_fused / *n_shrink on entry, the count written on return.
+ * Returns LORA_EINVAL for bad segments or too small a capacity.
+ * Source: "Two 27B models on a single RTX 5090", section 4 (requests that name the
+ * adapter and requests that do not share batches).
+ */
+int lora_linear_plan(const int32_t* seg_offsets, const int32_t* seg_adapter_ids, int n_seg, int T,
+                     int32_t* fused_tiles, int* n_fused, int32_t* shrink_tiles, int* n_shrink);
+
+/*
+ * lora_linear_validate -- the host checks lora_linear_forward runs first, without a
+ * handle or a GPU: the handle's shape (d_in, d_out, rank, max_tokens, max_segments) and
+ * the call's arguments. Pointers are checked for NULL, 16-byte alignment and overlap only.
+ * Returns LORA_OK or LORA_EINVAL.
+ */
+int lora_linear_validate(int d_in, int d_out, int rank, int max_tokens, int max_segments,
+                         const void* x, int T, const int32_t* seg_offsets,
+                         const int32_t* seg_adapter_ids, int n_seg, const void* W,
+                         const void* const* A, const void* const* B, const float* scale,
+                         int n_adapters, const void* y);
+
+/* Tunables and diagnostics (tests, benchmarks). */
+enum {
+    LORA_OPT_TILE_N = 1,        /* force the output-tile width (multiple of 16, 16..256); 0 = auto */
+    LORA_OPT_WAIT_LIMIT_US = 2, /* bound of every in-kernel wait, microseconds (default 4,000,000) */
+    LORA_OPT_DEBUG_STALL = 3,   /* 1 = the load warp never issues: every wait runs out (tests only) */
+    LORA_OPT_TIMING = 4,        /* 1 = record CUDA events around each kernel launch */
+    LORA_OPT_RASTER = 5         /* 0 = auto, 1 = row tiles fastest, 2 = column tiles fastest */
+};
+
+/* lora_linear_set_option -- set one option above. Returns LORA_OK or LORA_EINVAL. */
+int lora_linear_set_option(lora_linear* h, int option, long long value);
+
+/*
+ * lora_linear_timing -- with LORA_OPT_TIMING on: synchronises on the recorded events and
+ * returns, per kernel kind, the summed device time in milliseconds and the launch count
+ * since the option was last set. kind 0 = shrink, 1 = fused base+expand. Also returns
+ * the total number of kernels this handle has launched (any option state).
+ */
+int lora_linear_timing(lora_linear* h, int kind, double* total_ms, long long* launches,
+                       long long* all_launches);
+
+/*
+ * lora_linear_describe -- the launch shape forward would use for T rows and these
+ * segments, without launching: output-tile width, number of fused tiles, fused work
+ * units, grid size, pipeline stages, and whether a shrink runs. Any pointer may be NULL.
+ */
+int lora_linear_describe(lora_linear* h, int T, const int32_t* seg_offsets,
+                         const int32_t* seg_adapter_ids, int n_seg, int* tile_n, int* n_tiles,
+                         int* n_units, int* grid, int* stages, int* has_shrink);
+
+/* lora_linear_error_string -- a short static description of a return code. */
+const char* lora_linear_error_string(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LORA_LINEAR_H */

@@ -1,0 +1,56 @@
+"""ctypes loader for ``liblora_linear.so``: declares every exported C function's signature.
+
+Raises if the library has not been built; there is no other implementation to fall back to.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "liblora_linear.so")
+
+_lib = None
+
+P = C.c_void_p
+I32P = C.POINTER(C.c_int32)
+IP = C.POINTER(C.c_int)
+
+SIGNATURES = {
+    "lora_linear_create": (C.c_int, [C.POINTER(P), C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int]),
+    "lora_linear_forward": (C.c_int, [P, P, C.c_int, I32P, I32P, C.c_int, P, C.POINTER(P), C.POINTER(P),
+                                      C.POINTER(C.c_float), C.c_int, P, P]),
+    "lora_linear_forward_host": (C.c_int, [P, P, C.c_int, I32P, I32P, C.c_int, P, C.POINTER(P), C.POINTER(P),
+                                           C.POINTER(C.c_float), C.c_int, P, P]),
+    "lora_linear_destroy": (C.c_int, [P]),
+    "lora_linear_status": (C.c_int, [P, C.c_int]),
+    "lora_linear_plan": (C.c_int, [I32P, I32P, C.c_int, C.c_int, I32P, IP, I32P, IP]),
+    "lora_linear_validate": (C.c_int, [C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, P, C.c_int, I32P, I32P,
+                                       C.c_int, P, C.POINTER(P), C.POINTER(P), C.POINTER(C.c_float), C.c_int, P]),
+    "lora_linear_set_option": (C.c_int, [P, C.c_int, C.c_longlong]),
+    "lora_linear_timing": (C.c_int, [P, C.c_int, C.POINTER(C.c_double), C.POINTER(C.c_longlong),
+                                     C.POINTER(C.c_longlong)]),
+    "lora_linear_describe": (C.c_int, [P, C.c_int, I32P, I32P, C.c_int, IP, IP, IP, IP, IP, IP]),
+    "lora_linear_error_string": (C.c_char_p, [C.c_int]),
+}
+
+# return codes and options, as in include/lora_linear.h
+LORA_OK, LORA_EINVAL, LORA_ENOMEM, LORA_ECUDA, LORA_ETIMEOUT, LORA_EUNSUPPORTED, LORA_ENODEV = 0, -1, -2, -3, -4, -5, -6
+OPT_TILE_N, OPT_WAIT_LIMIT_US, OPT_DEBUG_STALL, OPT_TIMING, OPT_RASTER = 1, 2, 3, 4, 5
+
+
+def load():
+    """The loaded library (once per process)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is not built: run __graft_entry__.build() "
+                           "(or python -m mixed_lora_projection_gb300.build)")
+    lib = C.CDLL(LIB_PATH)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib

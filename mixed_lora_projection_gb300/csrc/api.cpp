@@ -1,0 +1,578 @@
+// C-ABI of the shared-base, per-request LoRA projection: handle, argument checks,
+// work-list upload and the two launches per call (shrink, then fused base+expand).
+//
+// Source: "Two 27B models on a single RTX 5090", sections 3-4 (W + B.A per changed
+// matrix; the adapter's two thin matrices run only for the requests that name it, in
+// the same batches as base requests).
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <algorithm>
+#include <cmath>
+#include <vector>
+
+#include "../../include/lora_linear.h"
+#include "lora_internal.h"
+
+using namespace lora;
+
+namespace {
+
+constexpr int kRing = 4;  // work-list slots in flight per handle
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+struct Slot {
+    uint8_t* host = nullptr;   // pinned
+    uint8_t* dev = nullptr;
+    cudaEvent_t done = nullptr;
+    bool pending = false;
+};
+
+struct TimingRec {
+    cudaEvent_t ev[3];
+    bool has_shrink;
+};
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+    if (!a || !b || na == 0 || nb == 0) return false;
+    uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + nb && b0 < a0 + na;
+}
+
+int check_shape(int d_in, int d_out, int rank, int max_tokens, int max_segments) {
+    if (d_in <= 0 || d_out <= 0 || (d_in % 8) || (d_out % 8)) return LORA_EINVAL;
+    if (rank < 8 || rank > LORA_MAX_RANK || (rank % 8)) return LORA_EINVAL;
+    if (max_tokens < 1 || max_segments < 1) return LORA_EINVAL;
+    return LORA_OK;
+}
+
+}  // namespace
+
+struct lora_linear {
+    int device = 0, d_in = 0, d_out = 0, rank = 0, max_tokens = 0, max_segments = 0;
+    int num_sms = 0;
+    void* u_ws = nullptr;       // bf16 [u_rows, rank]: shrink output, read by the fused pass
+    int u_rows = 0;
+    int* status = nullptr;      // device status word
+    int* status_host = nullptr; // pinned copy for forward_host
+    Slot slots[kRing];
+    size_t slot_bytes = 0;
+    int next_slot = 0;
+    int max_fused = 0;
+    EncodeTiledFn encode = nullptr;
+    // options
+    int force_tile_n = 0, raster = 0, debug_stall = 0, timing = 0;
+    unsigned long long wait_limit_ns = 4000000000ull;
+    std::vector<TimingRec> trec;
+    std::vector<cudaEvent_t> ev_pool;
+    long long launches = 0;
+    // staging for forward_host
+    void* x_stage = nullptr;
+    void* y_stage = nullptr;
+};
+
+namespace {
+
+struct DeviceGuard {
+    int prev = -1;
+    bool changed = false;
+    explicit DeviceGuard(int dev) {
+        if (cudaGetDevice(&prev) == cudaSuccess && prev != dev) {
+            changed = cudaSetDevice(dev) == cudaSuccess;
+        }
+    }
+    ~DeviceGuard() {
+        if (changed) cudaSetDevice(prev);
+    }
+};
+
+void free_handle(lora_linear* h) {
+    if (!h) return;
+    for (Slot& s : h->slots) {
+        if (s.host) cudaFreeHost(s.host);
+        if (s.dev) cudaFree(s.dev);
+        if (s.done) cudaEventDestroy(s.done);
+    }
+    for (TimingRec& r : h->trec)
+        for (cudaEvent_t e : r.ev) h->ev_pool.push_back(e);
+    for (cudaEvent_t e : h->ev_pool) cudaEventDestroy(e);
+    if (h->u_ws) cudaFree(h->u_ws);
+    if (h->status) cudaFree(h->status);
+    if (h->status_host) cudaFreeHost(h->status_host);
+    if (h->x_stage) cudaFree(h->x_stage);
+    if (h->y_stage) cudaFree(h->y_stage);
+    delete h;
+}
+
+cudaEvent_t take_event(lora_linear* h) {
+    if (!h->ev_pool.empty()) {
+        cudaEvent_t e = h->ev_pool.back();
+        h->ev_pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    return e;
+}
+
+CUresult encode_2d(lora_linear* h, CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer,
+                   uint32_t box_inner, uint32_t box_outer) {
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {inner * 2};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    return h->encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+int stages_for(int tile_n) {
+    int per = kStageBytesA + tile_n * kTileK * 2;
+    int s = (kSmemBudget - 1024 - 256) / per;
+    return std::max(2, std::min(kMaxStages, s));
+}
+
+// Output-tile width: the per-SM critical path is (waves x (tile_n + fixed cost)); narrow
+// tiles only where the row count is small enough that the pass streams W from memory.
+int choose_tile_n(const lora_linear* h, int n_fused) {
+    if (h->force_tile_n) return h->force_tile_n;
+    const bool small_batch = (long long)n_fused * kTileM <= 384;
+    long long best_cost = -1;
+    int best = kMaxTileN;
+    for (int tn = kMaxTileN; tn >= 16; tn -= 16) {
+        if (!small_batch && tn < 128) break;
+        long long units = (long long)n_fused * ceil_div(h->d_out, tn);
+        long long waves = (units + h->num_sms - 1) / h->num_sms;
+        long long cost = waves * (tn + 16);
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best = tn;
+        }
+    }
+    return best;
+}
+
+// Rasterisation: consecutive work units run at the same time on different SMs (a
+// "wave"). Walking output-column tiles fastest re-reads all of W every wave; walking row
+// tiles fastest re-reads all of X. Pick the order whose per-wave DRAM bytes are smaller,
+// counting an operand as L2-resident across waves when it fits in ~96 MB of the 129 MB L2.
+int choose_m_fastest(const lora_linear* h, int n_tiles, int n_ntiles, int tile_n) {
+    if (h->raster == 1) return 1;
+    if (h->raster == 2) return 0;
+    const double l2_budget = 96e6;
+    const long long units = (long long)n_tiles * n_ntiles;
+    const long long g = std::min<long long>(units, h->num_sms);
+    const double xb = (double)kTileM * h->d_in * 2, wb = (double)tile_n * h->d_in * 2;
+    const double total_x = (double)n_tiles * xb, total_w = (double)n_ntiles * wb;
+    const double rows_n = ceil_div(g, n_ntiles), cols_n = (double)std::min<long long>(g, n_ntiles);
+    const double rows_m = (double)std::min<long long>(g, n_tiles), cols_m = ceil_div(g, n_tiles);
+    const double cost_n = rows_n * xb + (total_w > l2_budget ? cols_n * wb : 0.0);
+    const double cost_m = cols_m * wb + (total_x > l2_budget ? rows_m * xb : 0.0);
+    return cost_m < cost_n ? 1 : 0;
+}
+
+Slot* acquire_slot(lora_linear* h) {
+    Slot* s = &h->slots[h->next_slot];
+    h->next_slot = (h->next_slot + 1) % kRing;
+    if (s->pending) {
+        if (cudaEventSynchronize(s->done) != cudaSuccess) return nullptr;
+        s->pending = false;
+    }
+    return s;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* lora_linear_error_string(int code) {
+    switch (code) {
+        case LORA_OK: return "ok";
+        case LORA_EINVAL: return "invalid argument";
+        case LORA_ENOMEM: return "out of memory";
+        case LORA_ECUDA: return "CUDA call failed";
+        case LORA_ETIMEOUT: return "a kernel's bounded wait ran out";
+        case LORA_EUNSUPPORTED: return "unsupported by this build";
+        case LORA_ENODEV: return "no usable sm_103 device";
+        default: return "unknown error";
+    }
+}
+
+int lora_linear_validate(int d_in, int d_out, int rank, int max_tokens, int max_segments,
+                         const void* x, int T, const int32_t* seg_offsets,
+                         const int32_t* seg_adapter_ids, int n_seg, const void* W,
+                         const void* const* A, const void* const* B, const float* scale,
+                         int n_adapters, const void* y) {
+    int rc = check_shape(d_in, d_out, rank, max_tokens, max_segments);
+    if (rc != LORA_OK) return rc;
+    if (T < 0 || T > max_tokens || n_seg < 0 || n_seg > max_segments || n_adapters < 0)
+        return LORA_EINVAL;
+    if (T == 0) {
+        if (n_seg == 0) return LORA_OK;
+        if (!seg_offsets || !seg_adapter_ids) return LORA_EINVAL;
+        for (int i = 0; i <= n_seg; ++i)
+            if (seg_offsets[i] != 0) return LORA_EINVAL;
+        for (int i = 0; i < n_seg; ++i)
+            if (seg_adapter_ids[i] < 0 || seg_adapter_ids[i] > n_adapters) return LORA_EINVAL;
+        return LORA_OK;
+    }
+    if (n_seg < 1 || !seg_offsets || !seg_adapter_ids) return LORA_EINVAL;
+    if (!x || !y || !W || !aligned16(x) || !aligned16(y) || !aligned16(W)) return LORA_EINVAL;
+    if (seg_offsets[0] != 0 || seg_offsets[n_seg] != T) return LORA_EINVAL;
+    const size_t xb = (size_t)T * d_in * 2, yb = (size_t)T * d_out * 2, wb = (size_t)d_out * d_in * 2;
+    const size_t ab = (size_t)rank * d_in * 2, bb = (size_t)d_out * rank * 2;
+    if (overlaps(y, yb, x, xb) || overlaps(y, yb, W, wb)) return LORA_EINVAL;
+    for (int i = 0; i < n_seg; ++i) {
+        if (seg_offsets[i + 1] < seg_offsets[i]) return LORA_EINVAL;
+        int a = seg_adapter_ids[i];
+        if (a < 0 || a > n_adapters) return LORA_EINVAL;
+        if (a == 0 || seg_offsets[i + 1] == seg_offsets[i]) continue;
+        if (!A || !B || !scale) return LORA_EINVAL;
+        const void* pa = A[a - 1];
+        const void* pb = B[a - 1];
+        if (!pa || !pb || !aligned16(pa) || !aligned16(pb)) return LORA_EINVAL;
+        if (!std::isfinite(scale[a - 1])) return LORA_EINVAL;
+        if (overlaps(y, yb, pa, ab) || overlaps(y, yb, pb, bb)) return LORA_EINVAL;
+    }
+    return LORA_OK;
+}
+
+int lora_linear_create(lora_linear** out, int d_in, int d_out, int rank, int max_tokens,
+                       int max_segments, int device) {
+    if (!out) return LORA_EINVAL;
+    *out = nullptr;
+    int rc = check_shape(d_in, d_out, rank, max_tokens, max_segments);
+    if (rc != LORA_OK) return rc;
+    int count = 0;
+    if (cudaGetDeviceCount(&count) != cudaSuccess || device < 0 || device >= count) {
+        cudaGetLastError();
+        return LORA_ENODEV;
+    }
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, device) != cudaSuccess) return LORA_ECUDA;
+    if (prop.major != 10 || prop.minor != 3) return LORA_ENODEV;
+
+    DeviceGuard guard(device);
+    lora_linear* h = new lora_linear();
+    h->device = device;
+    h->d_in = d_in;
+    h->d_out = d_out;
+    h->rank = rank;
+    h->max_tokens = max_tokens;
+    h->max_segments = max_segments;
+    h->num_sms = prop.multiProcessorCount;
+
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn) {
+        free_handle(h);
+        return LORA_ECUDA;
+    }
+    h->encode = reinterpret_cast<EncodeTiledFn>(fn);
+    if (gemm_prepare_device() != cudaSuccess) {
+        free_handle(h);
+        return LORA_ECUDA;
+    }
+
+    h->u_rows = ceil_div(max_tokens, kTileM) * kTileM + kTileM;
+    h->max_fused = ceil_div(max_tokens, kTileM) + max_segments + 1;
+    h->slot_bytes = align_up(2 * (size_t)max_segments * sizeof(CUtensorMap), 128) +
+                    2 * (size_t)h->max_fused * sizeof(Tile) +
+                    align_up(4 * (2 * (size_t)max_segments + 1), 16) +
+                    align_up(4 * (size_t)max_segments, 16) + 256;
+    if (cudaMalloc(&h->u_ws, (size_t)h->u_rows * rank * 2) != cudaSuccess ||
+        cudaMalloc((void**)&h->status, sizeof(int)) != cudaSuccess ||
+        cudaHostAlloc((void**)&h->status_host, sizeof(int), cudaHostAllocDefault) != cudaSuccess) {
+        cudaGetLastError();
+        free_handle(h);
+        return LORA_ENOMEM;
+    }
+    for (Slot& s : h->slots) {
+        if (cudaHostAlloc((void**)&s.host, h->slot_bytes, cudaHostAllocDefault) != cudaSuccess ||
+            cudaMalloc((void**)&s.dev, h->slot_bytes) != cudaSuccess) {
+            cudaGetLastError();
+            free_handle(h);
+            return LORA_ENOMEM;
+        }
+        if (cudaEventCreateWithFlags(&s.done, cudaEventDisableTiming) != cudaSuccess) {
+            free_handle(h);
+            return LORA_ECUDA;
+        }
+    }
+    if (cudaMemset(h->status, 0, sizeof(int)) != cudaSuccess ||
+        cudaMemset(h->u_ws, 0, (size_t)h->u_rows * rank * 2) != cudaSuccess) {
+        free_handle(h);
+        return LORA_ECUDA;
+    }
+    if (cudaDeviceSynchronize() != cudaSuccess) {
+        free_handle(h);
+        return LORA_ECUDA;
+    }
+    *out = h;
+    return LORA_OK;
+}
+
+int lora_linear_destroy(lora_linear* h) {
+    if (!h) return LORA_OK;
+    DeviceGuard guard(h->device);
+    cudaDeviceSynchronize();
+    free_handle(h);
+    return LORA_OK;
+}
+
+int lora_linear_set_option(lora_linear* h, int option, long long value) {
+    if (!h) return LORA_EINVAL;
+    switch (option) {
+        case LORA_OPT_TILE_N:
+            if (value != 0 && (value < 16 || value > kMaxTileN || value % 16)) return LORA_EINVAL;
+            h->force_tile_n = (int)value;
+            return LORA_OK;
+        case LORA_OPT_WAIT_LIMIT_US:
+            if (value < 1000 || value > 60000000) return LORA_EINVAL;
+            h->wait_limit_ns = (unsigned long long)value * 1000ull;
+            return LORA_OK;
+        case LORA_OPT_DEBUG_STALL:
+            h->debug_stall = value ? 1 : 0;
+            return LORA_OK;
+        case LORA_OPT_TIMING: {
+            DeviceGuard guard(h->device);
+            for (TimingRec& r : h->trec)
+                for (cudaEvent_t e : r.ev) h->ev_pool.push_back(e);
+            h->trec.clear();
+            h->timing = value ? 1 : 0;
+            return LORA_OK;
+        }
+        case LORA_OPT_RASTER:
+            if (value < 0 || value > 2) return LORA_EINVAL;
+            h->raster = (int)value;
+            return LORA_OK;
+        default:
+            return LORA_EINVAL;
+    }
+}
+
+int lora_linear_timing(lora_linear* h, int kind, double* total_ms, long long* launches,
+                       long long* all_launches) {
+    if (!h || kind < 0 || kind > 1) return LORA_EINVAL;
+    DeviceGuard guard(h->device);
+    double sum = 0;
+    long long n = 0;
+    for (TimingRec& r : h->trec) {
+        if (kind == 0 && !r.has_shrink) continue;
+        if (cudaEventSynchronize(r.ev[2]) != cudaSuccess) return LORA_ECUDA;
+        float ms = 0;
+        cudaEvent_t a = kind == 0 ? r.ev[0] : r.ev[1];
+        cudaEvent_t b = kind == 0 ? r.ev[1] : r.ev[2];
+        if (cudaEventElapsedTime(&ms, a, b) != cudaSuccess) return LORA_ECUDA;
+        sum += ms;
+        ++n;
+    }
+    if (total_ms) *total_ms = sum;
+    if (launches) *launches = n;
+    if (all_launches) *all_launches = h->launches;
+    return LORA_OK;
+}
+
+int lora_linear_status(lora_linear* h, int reset) {
+    if (!h) return LORA_EINVAL;
+    DeviceGuard guard(h->device);
+    if (cudaDeviceSynchronize() != cudaSuccess) return LORA_ECUDA;
+    int v = 0;
+    if (cudaMemcpy(&v, h->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return LORA_ECUDA;
+    if (reset && cudaMemset(h->status, 0, sizeof(int)) != cudaSuccess) return LORA_ECUDA;
+    if (reset && cudaDeviceSynchronize() != cudaSuccess) return LORA_ECUDA;
+    return v ? LORA_ETIMEOUT : LORA_OK;
+}
+
+int lora_linear_describe(lora_linear* h, int T, const int32_t* seg_offsets,
+                         const int32_t* seg_adapter_ids, int n_seg, int* tile_n, int* n_tiles,
+                         int* n_units, int* grid, int* stages, int* has_shrink) {
+    if (!h) return LORA_EINVAL;
+    Plan plan;
+    int rc = plan_segments(seg_offsets, seg_adapter_ids, n_seg, T, -1, &plan);
+    if (rc != LORA_OK) return rc;
+    int nf = (int)plan.fused.size();
+    int tn = nf ? choose_tile_n(h, nf) : 0;
+    int units = nf ? nf * ceil_div(h->d_out, tn) : 0;
+    if (tile_n) *tile_n = tn;
+    if (n_tiles) *n_tiles = nf;
+    if (n_units) *n_units = units;
+    if (grid) *grid = std::min(units, h->num_sms);
+    if (stages) *stages = tn ? stages_for(tn) : 0;
+    if (has_shrink) *has_shrink = plan.shrink.empty() ? 0 : 1;
+    return LORA_OK;
+}
+
+int lora_linear_forward(lora_linear* h, const void* x, int T, const int32_t* seg_offsets,
+                        const int32_t* seg_adapter_ids, int n_seg, const void* W,
+                        const void* const* A, const void* const* B, const float* scale,
+                        int n_adapters, void* y, void* stream_) {
+    if (!h) return LORA_EINVAL;
+    int rc = lora_linear_validate(h->d_in, h->d_out, h->rank, h->max_tokens, h->max_segments, x, T,
+                                  seg_offsets, seg_adapter_ids, n_seg, W, A, B, scale, n_adapters, y);
+    if (rc != LORA_OK) return rc;
+    if (T == 0) return LORA_OK;
+    Plan plan;
+    rc = plan_segments(seg_offsets, seg_adapter_ids, n_seg, T, n_adapters, &plan);
+    if (rc != LORA_OK) return rc;
+    if ((int)plan.fused.size() > h->max_fused) return LORA_EINVAL;
+
+    // caller's adapter index -> compact slot (1-based) for the device work list
+    const int n_used = (int)plan.used_adapters.size();
+    std::vector<int> compact(n_adapters + 1, 0);
+    for (int k = 0; k < n_used; ++k) compact[plan.used_adapters[k] + 1] = k + 1;
+    for (Tile& t : plan.fused) t.adapter = compact[t.adapter];
+    for (Tile& t : plan.shrink) t.adapter = compact[t.adapter];
+    for (int32_t& a : plan.seg_id) a = compact[a];
+
+    DeviceGuard guard(h->device);
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    const int nf = (int)plan.fused.size(), ns = (int)plan.shrink.size();
+    const int n_m = (int)plan.seg_id.size();
+    const int tile_n = choose_tile_n(h, nf);
+    const int n_ntiles = ceil_div(h->d_out, tile_n);
+    const int shrink_n = ceil_div(h->rank, 16) * 16;
+
+    Slot* slot = acquire_slot(h);
+    if (!slot) return LORA_ECUDA;
+    // work list: [B_a maps][A_a maps][fused tiles][shrink tiles][seg_off][seg_id][scales]
+    size_t off_bmaps = 0;
+    size_t off_amaps = off_bmaps + (size_t)n_used * sizeof(CUtensorMap);
+    size_t off_fused = align_up(off_amaps + (size_t)n_used * sizeof(CUtensorMap), 128);
+    size_t off_shrink = off_fused + (size_t)nf * sizeof(Tile);
+    size_t off_segoff = align_up(off_shrink + (size_t)ns * sizeof(Tile), 16);
+    size_t off_segid = off_segoff + 4 * (size_t)(n_m + 1);
+    size_t off_scale = align_up(off_segid + 4 * (size_t)n_m, 16);
+    size_t used_bytes = off_scale + 4 * (size_t)n_used;
+    if (used_bytes > h->slot_bytes) return LORA_EINVAL;
+
+    uint8_t* hb = slot->host;
+    CUtensorMap* bmaps = reinterpret_cast<CUtensorMap*>(hb + off_bmaps);
+    CUtensorMap* amaps = reinterpret_cast<CUtensorMap*>(hb + off_amaps);
+    for (int k = 0; k < n_used; ++k) {
+        int a = plan.used_adapters[k];
+        if (encode_2d(h, &bmaps[k], B[a], h->rank, h->d_out, kTileK, tile_n) != CUDA_SUCCESS) return LORA_ECUDA;
+        if (encode_2d(h, &amaps[k], A[a], h->d_in, h->rank, kTileK, shrink_n) != CUDA_SUCCESS) return LORA_ECUDA;
+    }
+    memcpy(hb + off_fused, plan.fused.data(), (size_t)nf * sizeof(Tile));
+    memcpy(hb + off_shrink, plan.shrink.data(), (size_t)ns * sizeof(Tile));
+    memcpy(hb + off_segoff, plan.seg_off.data(), 4 * (size_t)(n_m + 1));
+    memcpy(hb + off_segid, plan.seg_id.data(), 4 * (size_t)n_m);
+    float* sc = reinterpret_cast<float*>(hb + off_scale);
+    for (int k = 0; k < n_used; ++k) sc[k] = scale[plan.used_adapters[k]];
+    if (cudaMemcpyAsync(slot->dev, hb, used_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess)
+        return LORA_ECUDA;
+
+    GemmParams p;
+    memset(&p, 0, sizeof(p));
+    if (encode_2d(h, &p.tm_x, x, h->d_in, T, kTileK, kTileM) != CUDA_SUCCESS) return LORA_ECUDA;
+    p.seg_off = reinterpret_cast<const int32_t*>(slot->dev + off_segoff);
+    p.seg_id = reinterpret_cast<const int32_t*>(slot->dev + off_segid);
+    p.scales = reinterpret_cast<const float*>(slot->dev + off_scale);
+    p.n_seg = n_m;
+    p.status = h->status;
+    p.wait_limit_ns = h->wait_limit_ns;
+    p.k_main_blocks = ceil_div(h->d_in, kTileK);
+    p.debug_stall = h->debug_stall;
+
+    TimingRec rec{};
+    if (h->timing) {
+        for (int i = 0; i < 3; ++i) {
+            rec.ev[i] = take_event(h);
+            if (!rec.ev[i]) return LORA_ECUDA;
+        }
+        rec.has_shrink = ns > 0;
+        cudaEventRecord(rec.ev[0], stream);
+    }
+    if (ns > 0) {
+        GemmParams s = p;
+        s.tm_adapter = reinterpret_cast<const CUtensorMap*>(slot->dev + off_amaps);
+        s.tiles = reinterpret_cast<const Tile*>(slot->dev + off_shrink);
+        s.n_tiles = ns;
+        s.n_ntiles = 1;
+        s.tile_n = shrink_n;
+        s.stages = stages_for(shrink_n);
+        s.m_fastest = 1;
+        s.k_lora_blocks = 0;
+        s.out = h->u_ws;
+        s.ld_out = h->rank;
+        s.n_out = h->rank;
+        if (launch_gemm(kShrink, s, std::min(ns, h->num_sms), stream) != cudaSuccess) return LORA_ECUDA;
+        ++h->launches;
+    }
+    if (h->timing) cudaEventRecord(rec.ev[1], stream);
+    {
+        GemmParams f = p;
+        if (encode_2d(h, &f.tm_w, W, h->d_in, h->d_out, kTileK, tile_n) != CUDA_SUCCESS) return LORA_ECUDA;
+        if (encode_2d(h, &f.tm_u, h->u_ws, h->rank, h->u_rows, kTileK, kTileM) != CUDA_SUCCESS)
+            return LORA_ECUDA;
+        f.tm_adapter = reinterpret_cast<const CUtensorMap*>(slot->dev + off_bmaps);
+        f.tiles = reinterpret_cast<const Tile*>(slot->dev + off_fused);
+        f.n_tiles = nf;
+        f.n_ntiles = n_ntiles;
+        f.tile_n = tile_n;
+        f.stages = stages_for(tile_n);
+        f.m_fastest = choose_m_fastest(h, nf, n_ntiles, tile_n);
+        f.k_lora_blocks = ceil_div(h->rank, kTileK);
+        f.out = y;
+        f.ld_out = h->d_out;
+        f.n_out = h->d_out;
+        const int units = nf * n_ntiles;
+        if (launch_gemm(kFused, f, std::min(units, h->num_sms), stream) != cudaSuccess) return LORA_ECUDA;
+        ++h->launches;
+    }
+    if (h->timing) {
+        cudaEventRecord(rec.ev[2], stream);
+        h->trec.push_back(rec);
+    }
+    if (cudaEventRecord(slot->done, stream) != cudaSuccess) return LORA_ECUDA;
+    slot->pending = true;
+    return LORA_OK;
+}
+
+int lora_linear_forward_host(lora_linear* h, const void* x_host, int T, const int32_t* seg_offsets,
+                             const int32_t* seg_adapter_ids, int n_seg, const void* W,
+                             const void* const* A, const void* const* B, const float* scale,
+                             int n_adapters, void* y_host, void* stream_) {
+    if (!h) return LORA_EINVAL;
+    if (T < 0 || T > h->max_tokens) return LORA_EINVAL;
+    if (T > 0 && (!x_host || !y_host)) return LORA_EINVAL;
+    DeviceGuard guard(h->device);
+    if (!h->x_stage) {
+        if (cudaMalloc(&h->x_stage, (size_t)h->max_tokens * h->d_in * 2) != cudaSuccess ||
+            cudaMalloc(&h->y_stage, (size_t)h->max_tokens * h->d_out * 2) != cudaSuccess) {
+            cudaGetLastError();
+            if (h->x_stage) cudaFree(h->x_stage);
+            h->x_stage = nullptr;
+            h->y_stage = nullptr;
+            return LORA_ENOMEM;
+        }
+    }
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    const size_t xb = (size_t)T * h->d_in * 2, yb = (size_t)T * h->d_out * 2;
+    if (T > 0 && cudaMemcpyAsync(h->x_stage, x_host, xb, cudaMemcpyHostToDevice, stream) != cudaSuccess)
+        return LORA_ECUDA;
+    int rc = lora_linear_forward(h, h->x_stage, T, seg_offsets, seg_adapter_ids, n_seg, W, A, B, scale,
+                                 n_adapters, h->y_stage, stream_);
+    if (rc != LORA_OK) return rc;
+    if (T > 0 && cudaMemcpyAsync(y_host, h->y_stage, yb, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+        return LORA_ECUDA;
+    if (cudaMemcpyAsync(h->status_host, h->status, sizeof(int), cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+        return LORA_ECUDA;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return LORA_ECUDA;
+    return *h->status_host ? LORA_ETIMEOUT : LORA_OK;
+}
+
+}  // extern "C"

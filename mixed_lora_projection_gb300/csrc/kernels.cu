@@ -1,0 +1,409 @@
+// sm_103a kernels of the shared-base, per-request LoRA projection.
+//
+// One persistent, warp-specialised tile GEMM serves both passes of the method ("Two 27B
+// models on a single RTX 5090", section 4: the adapter's two thin matrices run beside
+// the changed matrix and their output is added):
+//
+//   shrink (Mode kShrink):  U[t, 0:r]   = bf16( s_a * X[t,:] A_a^T )  for the rows of adapter
+//                           tiles; rows of the tile that name no adapter get U = 0.
+//   fused  (Mode kFused):   acc[t, n]   = X[t,:] W[n,:]^T           (K = d_in)
+//                           acc[t, n]  += U[t,:] B_a[n,:]^T         (K = r, adapter tiles only,
+//                                                                    same TMEM accumulator)
+//                           Y[t, n]     = bf16(acc[t, n])
+//
+// Per CTA (one per SM, persistent over work units = planner tile x output-column tile):
+//   warp 0      one thread issues TMA loads (cp.async.bulk.tensor, 128-byte swizzle) of a
+//               128x64 A tile and a tile_n x 64 B tile per stage into a shared-memory ring;
+//   warp 1      owns 512 TMEM columns (two 128x256 fp32 accumulators); one thread issues
+//               tcgen05.mma kind::f16 (M=128, N=tile_n, K=16) and commits each stage back
+//               to the producer and each finished accumulator to the epilogue;
+//   warps 2..5  epilogue: tcgen05.ld the accumulator (warp w reads TMEM lanes 32*(w%4)..),
+//               round to bf16 and store the tile's rows with 16-byte stores.
+// Two accumulators let the epilogue of one tile overlap the mainloop of the next.
+//
+// Every mbarrier wait is bounded by a wall-clock limit; a wait that runs out sets bit 0
+// of the status word and a CTA-wide abort flag, and all roles leave their loops, wait
+// (bounded) for their own copies and MMAs in flight, free TMEM and return.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "lora_internal.h"
+
+namespace lora {
+namespace dev {
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// ---------------------------------------------------------------- mbarrier
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Waits for the phase with the given parity to complete. Gives up (returns false) when
+// another role has aborted or when `limit_ns` of wall time pass; in the latter case it
+// records the timeout in the status word and raises the CTA's abort flag.
+__device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          int* status, uint64_t limit_ns, bool honour_abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (honour_abort && *abort_flag) return false;
+        if (global_timer_ns() - t0 > limit_ns) {
+            atomicOr(status, 1);
+            *abort_flag = 1;
+            return false;
+        }
+    }
+}
+
+// ---------------------------------------------------------------- TMA
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int c_inner, int c_outer) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c_inner), "r"(c_outer)
+        : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+// Tensor maps written to global memory by the host: make the tensormap proxy see them.
+__device__ __forceinline__ void tensormap_acquire(const CUtensorMap* map) {
+    asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(
+                     reinterpret_cast<uint64_t>(map))
+                 : "memory");
+}
+
+// ---------------------------------------------------------------- tcgen05
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+// D[tmem] (+)= A[smem] * B[smem]^T, bf16 inputs, fp32 accumulate; one thread issues.
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Arrive once on `bar` when every tcgen05 op this thread issued so far has completed.
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+}
+// 32 lanes x 32 bits x 16 columns: thread i of the warp gets 16 consecutive columns of lane
+// (taddr.lane + i).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32"
+        " {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+          "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]),
+          "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor: K-major tile written by TMA with 128-byte swizzle.
+// Rows are 128 bytes (64 bf16), groups of 8 rows are 1024 bytes apart (stride byte
+// offset); the leading byte offset is unused for this layout; version 1; layout 2 =
+// 128-byte swizzle. The tile base must be 1024-byte aligned.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((addr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)1 << 16;
+    d |= (uint64_t)(1024 >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+// Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major, shape M x N.
+__device__ __forceinline__ uint32_t instr_desc_bf16(int m, int n) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) |
+           ((uint32_t)(m >> 4) << 24);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Adapter id of row t among the merged segments (binary search over offsets).
+__device__ __forceinline__ int row_adapter(const int32_t* off, const int32_t* ids, int n, int t) {
+    int lo = 0, hi = n - 1;
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (off[mid] <= t) lo = mid; else hi = mid - 1;
+    }
+    return ids[lo];
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_constant__ GemmParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // carve: rings (1024-aligned), then barriers, then the TMEM slot and the abort flag
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~static_cast<uintptr_t>(1023));
+    const int stages = p.stages;
+    const uint32_t b_stage_bytes = (uint32_t)p.tile_n * kTileK * 2;
+    uint8_t* a_ring = base;
+    uint8_t* b_ring = a_ring + (size_t)stages * kStageBytesA;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(b_ring + (size_t)stages * b_stage_bytes);
+    uint64_t* full = bars;
+    uint64_t* empty = full + stages;
+    uint64_t* tfull = empty + stages;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* drain = tempty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < stages; ++s) {
+            mbar_init(smem_addr(&full[s]), 1);
+            mbar_init(smem_addr(&empty[s]), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(smem_addr(&tfull[a]), 1);
+            mbar_init(smem_addr(&tempty[a]), kEpilogueThreads);
+        }
+        mbar_init(smem_addr(drain), 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) tmem_alloc(smem_addr(tmem_slot), 2 * kAccCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int n_units = p.n_tiles * p.n_ntiles;
+    const uint64_t limit = p.wait_limit_ns;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0 && !p.debug_stall) {
+            tma_prefetch_desc(&p.tm_x);
+            if (MODE == kFused) { tma_prefetch_desc(&p.tm_w); tma_prefetch_desc(&p.tm_u); }
+            int stage = 0;
+            uint32_t phase = 0;
+            long long issued = 0;
+            int acquired = -1;  // compact adapter whose global tensor map was last acquired
+            bool ok = true;
+            for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+                const int ti = p.m_fastest ? (u % p.n_tiles) : (u / p.n_ntiles);
+                const int nt = p.m_fastest ? (u / p.n_tiles) : (u % p.n_ntiles);
+                const Tile tile = p.tiles[ti];
+                const int n0 = nt * p.tile_n;
+                const CUtensorMap* ad = tile.adapter ? &p.tm_adapter[tile.adapter - 1] : nullptr;
+                if (ad && acquired != tile.adapter) { tensormap_acquire(ad); acquired = tile.adapter; }
+                const CUtensorMap* bmain = (MODE == kFused) ? &p.tm_w : ad;
+                const int nk = p.k_main_blocks + ((MODE == kFused && tile.adapter) ? p.k_lora_blocks : 0);
+                for (int kb = 0; kb < nk; ++kb) {
+                    if (!wait_bounded(smem_addr(&empty[stage]), phase ^ 1, abort_flag, p.status, limit, true)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = smem_addr(&full[stage]);
+                    mbar_arrive_expect_tx(fb, kStageBytesA + b_stage_bytes);
+                    const uint32_t sa = smem_addr(a_ring + (size_t)stage * kStageBytesA);
+                    const uint32_t sb = smem_addr(b_ring + (size_t)stage * b_stage_bytes);
+                    if (kb < p.k_main_blocks) {
+                        tma_load_2d(sa, &p.tm_x, fb, kb * kTileK, tile.row0);
+                        tma_load_2d(sb, bmain, fb, kb * kTileK, n0);
+                    } else {
+                        const int k = (kb - p.k_main_blocks) * kTileK;
+                        tma_load_2d(sa, &p.tm_u, fb, k, tile.row0);
+                        tma_load_2d(sb, ad, fb, k, n0);
+                    }
+                    ++issued;
+                    if (++stage == stages) { stage = 0; phase ^= 1; }
+                }
+            }
+            if (!ok) {
+                // wait (bounded, ignoring the abort flag) for the copies still in flight
+                long long first = issued > stages ? issued - stages : 0;
+                for (long long j = first; j < issued; ++j)
+                    wait_bounded(smem_addr(&full[j % stages]), (uint32_t)((j / stages) & 1), abort_flag,
+                                 p.status, limit, false);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc = instr_desc_bf16(kTileM, p.tile_n);
+            int stage = 0;
+            uint32_t phase = 0;
+            int it = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++it) {
+                const int ti = p.m_fastest ? (u % p.n_tiles) : (u / p.n_ntiles);
+                const Tile tile = p.tiles[ti];
+                const int nk = p.k_main_blocks + ((MODE == kFused && tile.adapter) ? p.k_lora_blocks : 0);
+                const int acc = it & 1;
+                if (!wait_bounded(smem_addr(&tempty[acc]), ((it >> 1) & 1) ^ 1, abort_flag, p.status, limit, true)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d = tmem_base + (uint32_t)(acc * kAccCols);
+                for (int kb = 0; kb < nk; ++kb) {
+                    if (!wait_bounded(smem_addr(&full[stage]), phase, abort_flag, p.status, limit, true)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t ad = smem_desc_sw128(smem_addr(a_ring + (size_t)stage * kStageBytesA));
+                    const uint64_t bd = smem_desc_sw128(smem_addr(b_ring + (size_t)stage * b_stage_bytes));
+#pragma unroll
+                    for (int k = 0; k < kTileK / 16; ++k) {
+                        // advance 16 bf16 = 32 bytes along K inside the swizzled rows
+                        mma_bf16(d, ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), idesc,
+                                 (kb > 0 || k > 0) ? 1u : 0u);
+                    }
+                    mma_commit(smem_addr(&empty[stage]));
+                    if (++stage == stages) { stage = 0; phase ^= 1; }
+                }
+                if (!ok) break;
+                mma_commit(smem_addr(&tfull[acc]));
+            }
+            // every MMA this thread issued has completed before TMEM is released
+            mma_commit(smem_addr(drain));
+            wait_bounded(smem_addr(drain), 0, abort_flag, p.status, limit, false);
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue (warps 2..5)
+        const int q = warp & 3;                      // TMEM lane quadrant this warp may read
+        const int r_local = q * 32 + lane;           // tile row held by this thread
+        const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+        int it = 0;
+        for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++it) {
+            const int ti = p.m_fastest ? (u % p.n_tiles) : (u / p.n_ntiles);
+            const int nt = p.m_fastest ? (u / p.n_tiles) : (u % p.n_ntiles);
+            const Tile tile = p.tiles[ti];
+            const int acc = it & 1;
+            int ok = 1;
+            if (lane == 0)
+                ok = wait_bounded(smem_addr(&tfull[acc]), (it >> 1) & 1, abort_flag, p.status, limit, true);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            tc_fence_after();
+            const int row = tile.row0 + r_local;
+            const bool row_ok = r_local < tile.nrows;
+            float scale = 1.0f;
+            if (MODE == kShrink) {
+                int a = row_ok ? row_adapter(p.seg_off, p.seg_id, p.n_seg, row) : 0;
+                scale = (a == tile.adapter) ? p.scales[tile.adapter - 1] : 0.0f;
+            }
+            const int n0 = nt * p.tile_n;
+            __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out) + (size_t)row * p.ld_out + n0;
+            const uint32_t taddr = tmem_base + (uint32_t)(acc * kAccCols) + lane_off;
+            for (int c = 0; c < p.tile_n; c += 16) {
+                uint32_t v[16];
+                tmem_ld16(taddr + (uint32_t)c, v);
+                tmem_ld_wait();
+                if (row_ok) {
+                    uint4 lo, hi;
+                    lo.x = pack_bf16x2(__uint_as_float(v[0]) * scale, __uint_as_float(v[1]) * scale);
+                    lo.y = pack_bf16x2(__uint_as_float(v[2]) * scale, __uint_as_float(v[3]) * scale);
+                    lo.z = pack_bf16x2(__uint_as_float(v[4]) * scale, __uint_as_float(v[5]) * scale);
+                    lo.w = pack_bf16x2(__uint_as_float(v[6]) * scale, __uint_as_float(v[7]) * scale);
+                    hi.x = pack_bf16x2(__uint_as_float(v[8]) * scale, __uint_as_float(v[9]) * scale);
+                    hi.y = pack_bf16x2(__uint_as_float(v[10]) * scale, __uint_as_float(v[11]) * scale);
+                    hi.z = pack_bf16x2(__uint_as_float(v[12]) * scale, __uint_as_float(v[13]) * scale);
+                    hi.w = pack_bf16x2(__uint_as_float(v[14]) * scale, __uint_as_float(v[15]) * scale);
+                    const int col = n0 + c;
+                    if (col < p.n_out) *reinterpret_cast<uint4*>(out + c) = lo;
+                    if (col + 8 < p.n_out) *reinterpret_cast<uint4*>(out + c + 8) = hi;
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(smem_addr(&tempty[acc]));
+        }
+    }
+
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, 2 * kAccCols);
+    }
+}
+
+}  // namespace dev
+
+size_t gemm_smem_bytes(int tile_n, int stages) {
+    return 1024 + (size_t)stages * (kStageBytesA + (size_t)tile_n * kTileK * 2) +
+           8 * (2 * (size_t)stages + 5) + 16;
+}
+
+cudaError_t gemm_prepare_device() {
+    cudaError_t e = cudaFuncSetAttribute(dev::lora_gemm_kernel<kFused>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget + 2048);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(dev::lora_gemm_kernel<kShrink>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget + 2048);
+}
+
+cudaError_t launch_gemm(int mode, const GemmParams& p, int grid, cudaStream_t stream) {
+    const size_t smem = gemm_smem_bytes(p.tile_n, p.stages);
+    if (mode == kFused)
+        dev::lora_gemm_kernel<kFused><<<grid, kThreads, smem, stream>>>(p);
+    else
+        dev::lora_gemm_kernel<kShrink><<<grid, kThreads, smem, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace lora

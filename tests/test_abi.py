@@ -1,0 +1,137 @@
+"""The C-ABI library builds, loads without a GPU and exports what include/*.h declares;
+its planner equals the oracle's bit for bit; its host-side checks reject bad arguments.
+No compute call here needs a GPU."""
+import glob
+import itertools
+import os
+import re
+
+import numpy as np
+import pytest
+
+from oracle import plan_ref
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = open(h).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        names |= set(re.findall(r"\b(lora_linear_\w+)\s*\(", src))
+    return names
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for n in ("lora_linear_create", "lora_linear_forward", "lora_linear_destroy", "lora_linear_plan"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    import ctypes
+    for name in sorted(_declared()):
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_binding_declares_every_export(lib):
+    from mixed_lora_projection_gb300 import _lib
+    assert set(_lib.SIGNATURES) == _declared()
+
+
+def test_error_strings(lib):
+    for code in (0, -1, -2, -3, -4, -5, -6, 7):
+        assert lib.lora_linear_error_string(code)
+
+
+# --------------------------------------------------------------------------- planner parity
+
+def _lib_plan(off, ids, T):
+    from mixed_lora_projection_gb300.lora_linear import plan
+    return plan(off, ids, T)
+
+
+LENGTHS = (0, 1, 2, 127, 128, 129, 255, 300)
+
+
+@pytest.mark.parametrize("nseg", [1, 2, 3])
+def test_planner_equals_plan_ref_exhaustive(lib, nseg):
+    for lens in itertools.product(LENGTHS, repeat=nseg):
+        off = [0] + np.cumsum(lens).tolist()
+        for ids in itertools.product((0, 1, 2), repeat=nseg):
+            T = off[-1]
+            assert _lib_plan(off, ids, T) == plan_ref(off, list(ids), T)
+
+
+@pytest.mark.parametrize("seed", range(30))
+def test_planner_equals_plan_ref_random(lib, seed):
+    rng = np.random.default_rng(1000 + seed)
+    nseg = int(rng.integers(1, 64))
+    lens = rng.integers(0, int(rng.choice([4, 64, 400, 3000])), nseg)
+    off = [0] + np.cumsum(lens).tolist()
+    ids = rng.integers(0, int(rng.integers(1, 6)), nseg).tolist()
+    T = int(off[-1])
+    assert _lib_plan(off, ids, T) == plan_ref(off, ids, T)
+
+
+def test_planner_workloads(lib):
+    from mixed_lora_projection_gb300.synth import WORKLOADS
+    for w in WORKLOADS.values():
+        assert _lib_plan(w.seg_offsets, w.seg_ids, w.T) == plan_ref(list(w.seg_offsets), list(w.seg_ids), w.T)
+
+
+@pytest.mark.parametrize("off,ids,T", [([0, 5], [0], 6), ([1, 6], [0], 6), ([0, 4, 3, 6], [0, 1, 0], 6),
+                                       ([0, 6], [-1], 6)])
+def test_planner_rejects_bad_segments(lib, off, ids, T):
+    from mixed_lora_projection_gb300.lora_linear import LoraError
+    with pytest.raises(LoraError):
+        _lib_plan(off, ids, T)
+
+
+# --------------------------------------------------------------------------- host-side checks
+
+def _v(**kw):
+    from mixed_lora_projection_gb300.lora_linear import validate
+    base = dict(d_in=256, d_out=512, rank=16, max_tokens=64, max_segments=4, x_ptr=0x10000000, T=64,
+                seg_offsets=[0, 32, 64], seg_ids=[0, 1], w_ptr=0x20000000, a_ptrs=[0x30000000],
+                b_ptrs=[0x40000000], scales=[1.0], y_ptr=0x50000000)
+    base.update(kw)
+    return validate(**base)
+
+
+def test_validate_accepts_good_arguments(lib):
+    assert _v() == 0
+    assert _v(T=0, seg_offsets=[0], seg_ids=[]) == 0
+    assert _v(T=0, seg_offsets=[0, 0], seg_ids=[1]) == 0
+    # unnamed adapters may be NULL
+    assert _v(a_ptrs=[0x30000000, None], b_ptrs=[0x40000000, None], scales=[1.0, 1.0]) == 0
+
+
+@pytest.mark.parametrize("kw", [
+    dict(d_in=250), dict(d_out=0), dict(rank=4), dict(rank=264), dict(rank=12),
+    dict(max_tokens=0), dict(T=65), dict(T=-1),
+    dict(seg_offsets=[0, 32, 63]), dict(seg_offsets=[1, 32, 64]), dict(seg_offsets=[0, 40, 32, 64], seg_ids=[0, 1, 0]),
+    dict(seg_ids=[0, 2]), dict(seg_ids=[-1, 1]),
+    dict(seg_offsets=[0, 8, 16, 32, 48, 64], seg_ids=[0, 1, 0, 1, 0]),   # n_seg > max_segments
+    dict(x_ptr=0x10000008), dict(y_ptr=0x50000004), dict(w_ptr=0x20000002), dict(a_ptrs=[0x30000001]),
+    dict(x_ptr=0), dict(y_ptr=0), dict(a_ptrs=[None]), dict(b_ptrs=[None]),
+    dict(scales=[float("nan")]), dict(scales=[float("inf")]),
+    dict(y_ptr=0x10000000 + 64 * 256 * 2 - 16),                         # y overlaps x
+    dict(y_ptr=0x20000000),                                              # y overlaps W
+    dict(a_ptrs=[0x50000000 + 32]),                                      # y overlaps A_1
+])
+def test_validate_rejects(lib, kw):
+    assert _v(**kw) == -1
+
+
+def test_create_without_a_gpu_reports_no_device(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    import ctypes
+    h = ctypes.c_void_p()
+    assert lib.lora_linear_create(ctypes.byref(h), 256, 512, 16, 64, 4, 0) == -6
+    assert not h.value
+    assert lib.lora_linear_destroy(None) == 0

@@ -1,0 +1,238 @@
+"""GPU parity: the CUDA path through the C-ABI against the fp64 oracle on the same seeded
+bf16 inputs (max|dY| / max|Y_ref| <= 5e-3), plus bit-exact routing invariants, odd
+shapes, guard rows and determinism."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import row_adapter_ids
+from mixed_lora_projection_gb300.synth import WORKLOADS, Workload, make_inputs
+
+from gpu_util import TOL, f64, oracle_full, oracle_rows, rel_err, run, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from mixed_lora_projection_gb300 import build
+    build.ensure_built()
+    return torch.device("cuda", 0)
+
+
+def _ll(w, max_segments=64, max_tokens=None):
+    from mixed_lora_projection_gb300 import LoraLinear
+    return LoraLinear(w.d_in, w.d_out, w.rank, max_tokens or max(w.T, 1), max_segments, 0)
+
+
+# --------------------------------------------------------------------------- layout pins
+
+def test_one_hot_rows_give_columns_of_w_exactly(dev):
+    # X row t = e_{k(t)}: every output is a single product W[n,k] * 1, exact in fp32 and bf16
+    T, d_in, d_out = 256, 384, 512
+    w = Workload("onehot", 9, T, d_in, d_out, 16, (0, T), (0,))
+    inp = make_inputs(w, dev)
+    k = torch.arange(T, device=dev) * 7 % d_in
+    inp.x.zero_()
+    inp.x[torch.arange(T, device=dev), k] = 1.0
+    with _ll(w) as ll:
+        y = run(ll, inp, [0, T], [0])
+    torch.cuda.synchronize()
+    want = inp.w[:, k].t().contiguous()
+    assert torch.equal(y, want)
+
+
+def test_one_hot_adapter_lands_in_one_column(dev):
+    # W = 0, A[j0,k0] = 1, B[n0,j0] = 1, s = 2: Y[t,n] = 2 X[t,k0] at n = n0, else 0
+    T, d_in, d_out, r = 200, 256, 384, 32
+    w = Workload("onehot_ad", 9, T, d_in, d_out, r, (0, T), (1,), scales=(2.0,))
+    inp = make_inputs(w, dev)
+    j0, k0, n0 = 5, 77, 301
+    inp.w.zero_()
+    inp.a[0].zero_(); inp.a[0][j0, k0] = 1.0
+    inp.b[0].zero_(); inp.b[0][n0, j0] = 1.0
+    with _ll(w) as ll:
+        y = run(ll, inp, [0, T], [1])
+    torch.cuda.synchronize()
+    want = torch.zeros_like(y)
+    want[:, n0] = (2.0 * inp.x[:, k0].float()).to(torch.bfloat16)
+    assert torch.equal(y, want)
+
+
+# --------------------------------------------------------------------------- tiny config, full compare
+
+def test_tiny_matches_oracle(dev):
+    w = WORKLOADS["tiny"]
+    inp = make_inputs(w, dev)
+    with _ll(w) as ll:
+        y = run(ll, inp, w.seg_offsets, w.seg_ids)
+    torch.cuda.synchronize()
+    ref = oracle_full(inp, list(w.seg_offsets), list(w.seg_ids))
+    assert rel_err(y, ref) <= TOL
+    # the delta is not negligible: adapter rows differ from base rows by O(1)
+    base = oracle_full(inp, list(w.seg_offsets), [0] * len(w.seg_ids))
+    assert np.abs(ref[32:] - base[32:]).max() > 0.5
+
+
+# --------------------------------------------------------------------------- odd shapes
+
+ODD = [
+    # (T, d_in, d_out, r, lengths, ids, n_adapters)
+    (1, 256, 512, 16, [1], [1], 1),
+    (7, 128, 256, 16, [3, 4], [0, 1], 1),
+    (127, 192, 320, 32, [127], [1], 1),
+    (129, 256, 512, 64, [64, 65], [1, 0], 1),
+    (300, 520, 264, 24, [0, 100, 1, 0, 199], [1, 0, 2, 2, 1], 2),
+    (517, 136, 1000, 128, [10, 5, 10, 3, 200, 289], [1, 0, 2, 2, 0, 3], 3),
+    (1024, 1024, 768, 256, [128, 256, 1, 639], [2, 1, 0, 2], 2),
+    (260, 4096, 4096, 256, [260], [0], 1),
+]
+
+
+@pytest.mark.parametrize("case", ODD, ids=[f"T{c[0]}_{c[1]}x{c[2]}_r{c[3]}" for c in ODD])
+def test_odd_shapes_match_oracle(dev, case):
+    T, d_in, d_out, r, lens, ids, na = case
+    off = [0] + np.cumsum(lens).tolist()
+    w = Workload("odd", 7, T, d_in, d_out, r, tuple(off), tuple(ids), n_adapters=na,
+                 scales=tuple(0.5 + 0.75 * k for k in range(na)))
+    inp = make_inputs(w, dev)
+    with _ll(w) as ll:
+        y = run(ll, inp, off, ids)
+    torch.cuda.synchronize()
+    ref = oracle_full(inp, off, ids)
+    assert rel_err(y, ref) <= TOL
+
+
+@pytest.mark.parametrize("tile_n", [16, 48, 128, 240, 256])
+def test_forced_tile_widths_match_oracle(dev, tile_n):
+    from mixed_lora_projection_gb300 import _lib as L
+    T, d_in, d_out, r = 300, 512, 1008, 32
+    off, ids = [0, 100, 180, 300], [1, 0, 1]
+    w = Workload("tilen", 8, T, d_in, d_out, r, tuple(off), tuple(ids))
+    inp = make_inputs(w, dev)
+    with _ll(w) as ll:
+        ll.set_option(L.OPT_TILE_N, tile_n)
+        y = run(ll, inp, off, ids)
+    torch.cuda.synchronize()
+    assert rel_err(y, oracle_full(inp, off, ids)) <= TOL
+
+
+# --------------------------------------------------------------------------- bit-exact invariants
+
+def test_base_rows_bit_identical_to_all_base_run(dev):
+    w = WORKLOADS["sweep_qkv_multi"]
+    inp = make_inputs(w, dev)
+    off, ids = list(w.seg_offsets), list(w.seg_ids)
+    with _ll(w) as ll:
+        y = run(ll, inp, off, ids)
+        y0 = run(ll, inp, off, [0] * len(ids))
+    torch.cuda.synchronize()
+    base = torch.as_tensor(row_adapter_ids(off, ids, w.T) == 0, device=dev)
+    assert torch.equal(y[base], y0[base])
+    assert not torch.equal(y[~base], y0[~base])
+
+
+def test_zero_b_adapter_rows_bit_identical_to_base(dev):
+    w = WORKLOADS["sweep_o"]
+    inp = make_inputs(w, dev)
+    off, ids = list(w.seg_offsets), list(w.seg_ids)
+    for b in inp.b:
+        b.zero_()
+    with _ll(w) as ll:
+        y = run(ll, inp, off, ids)
+        y0 = run(ll, inp, off, [0] * len(ids))
+    torch.cuda.synchronize()
+    assert torch.equal(y, y0)
+
+
+def test_deterministic(dev):
+    w = WORKLOADS["sweep_down"]
+    inp = make_inputs(w, dev)
+    with _ll(w) as ll:
+        y1 = run(ll, inp, w.seg_offsets, w.seg_ids).clone()
+        y2 = run(ll, inp, w.seg_offsets, w.seg_ids)
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2)
+
+
+def test_guard_rows_untouched(dev):
+    T, d_in, d_out, r, G = 333, 256, 520, 16, 3
+    off, ids = [0, 100, 101, 333], [1, 0, 1]
+    w = Workload("guard", 6, T, d_in, d_out, r, tuple(off), tuple(ids))
+    inp = make_inputs(w, dev)
+    full = torch.full((T + 2 * G, d_out), -77.0, dtype=torch.bfloat16, device=dev)
+    with _ll(w) as ll:
+        run(ll, inp, off, ids, y=full[G:G + T])
+    torch.cuda.synchronize()
+    assert bool((full[:G] == -77.0).all()) and bool((full[G + T:] == -77.0).all())
+    assert rel_err(full[G:G + T], oracle_full(inp, off, ids)) <= TOL
+
+
+def test_empty_batch_launches_nothing(dev):
+    w = WORKLOADS["tiny"]
+    inp = make_inputs(w, dev)
+    with _ll(w) as ll:
+        y = torch.empty((0, w.d_out), dtype=torch.bfloat16, device=dev)
+        ll.forward(inp.x[:0], [0], [], inp.w, inp.a, inp.b, inp.scales, y=y)
+        _, _, launched = ll.timing(1)
+        assert launched == 0
+
+
+def test_invalid_call_leaves_output_untouched(dev):
+    from mixed_lora_projection_gb300 import LoraError
+    w = WORKLOADS["tiny"]
+    inp = make_inputs(w, dev)
+    y = torch.full((w.T, w.d_out), 3.0, dtype=torch.bfloat16, device=dev)
+    with _ll(w) as ll:
+        with pytest.raises(LoraError):
+            run(ll, inp, [0, 32, 63], [0, 1], y=y)        # offsets do not end at T
+        with pytest.raises(LoraError):
+            run(ll, inp, [0, 32, 64], [0, 2], y=y)        # adapter 2 does not exist
+        torch.cuda.synchronize()
+        assert bool((y == 3.0).all())
+        assert ll.timing(1)[2] == 0
+
+
+def test_host_buffers_path_matches_device_path(dev):
+    w = WORKLOADS["tiny"]
+    inp = make_inputs(w, dev)
+    x_host = inp.x.cpu().pin_memory()
+    y_host = torch.empty((w.T, w.d_out), dtype=torch.bfloat16).pin_memory()
+    with _ll(w) as ll:
+        y = run(ll, inp, w.seg_offsets, w.seg_ids)
+        ll.forward_host(x_host, w.seg_offsets, w.seg_ids, inp.w, inp.a, inp.b, inp.scales, y_host)
+    torch.cuda.synchronize()
+    assert torch.equal(y.cpu(), y_host)
+
+
+# --------------------------------------------------------------------------- full-size workloads
+
+FULL = ["prefill_16k", "mixed_batch", "mixed_decode", "mixed_near_ridge", "prefill_32k"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_workload_sampled_rows(dev, name):
+    w = WORKLOADS[name]
+    inp = make_inputs(w, dev)
+    off, ids = list(w.seg_offsets), list(w.seg_ids)
+    with _ll(w) as ll:
+        y = run(ll, inp, off, ids)
+    torch.cuda.synchronize()
+    rows = sample_rows(w.T, off, ids, n_random=256, seed=w.index)
+    ref = oracle_rows(inp, off, ids, rows)
+    assert rel_err(y[torch.as_tensor(rows, device=dev)], ref) <= TOL
+
+
+@pytest.mark.parametrize("proj", ["qkv", "o", "gate_up", "down", "qkv_multi", "down_multi"])
+def test_sweep_layer_sampled_rows(dev, proj):
+    w = WORKLOADS[f"sweep_{proj}"]
+    inp = make_inputs(w, dev, layer=23)
+    off, ids = list(w.seg_offsets), list(w.seg_ids)
+    with _ll(w) as ll:
+        y = run(ll, inp, off, ids)
+    torch.cuda.synchronize()
+    rows = sample_rows(w.T, off, ids, n_random=128, seed=3)
+    ref = oracle_rows(inp, off, ids, rows)
+    assert rel_err(y[torch.as_tensor(rows, device=dev)], ref) <= TOL
