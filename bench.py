@@ -1,0 +1,416 @@
+"""Benchmark of the shared-base, per-request LoRA projection on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one pass of the whole hot path (planner, shrink, fused base+expand) over one
+batch of the workload: one lora_linear_forward call (for the 24-layer sweep, 96 calls: 4
+projections x 24 layers). Inputs are seeded synthetic bf16 tensors already resident in
+HBM; three copies of the weights rotate between steps so that W is not L2-resident, and
+X alone is larger than the 129 MB L2 for the prefill workloads.
+
+Prints one JSON line (rank 0). `value` is useful TFLOP/s of the whole job (all ranks);
+`e2e` is the same metric through the host-buffer entry point (X copied in, Y copied
+out every step); `roofline` is the fused kernel's achieved TFLOP/s (CUDA events around
+each launch, on the launch stream) against the measured bf16 peak; `cpu_baseline` is the
+fp64 oracle timed on a bounded sample on the host cores.
+
+Multi-GPU: launched under torchrun, every rank runs an independent replica (the
+projection's rows need no exchange); the timed region is bracketed by barriers and the
+slowest rank's time is used.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "LoRA-linear TFLOP/s & tokens/s at 1 GB300; % of bf16 tensor peak / HBM BW"
+SWEEP = "sweep_24_layers"
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d["bf16_tflops"], d.get("bf16_tflops_sustained"), d["hbm_gbs"], "measured"
+    return 1900.0, 1700.0, 6800.0, "fallback"
+
+
+def _kernel_hash():
+    h = hashlib.sha256()
+    for f in ("kernels.cu", "lora_internal.h"):
+        with open(os.path.join(ROOT, "mixed_lora_projection_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def _profiled_traffic(workload: str):
+    """dram bytes per fused launch from the committed ncu summary, if it was taken on the
+    current kernel source (else None)."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(p):
+        return None
+    kh = _kernel_hash()
+    with open(p) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) >= 4 and not line.startswith("#") and parts[0] == workload and parts[1] == kh:
+                return float(parts[3])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi SM clock / throttle samples in the background."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.samples = []
+        self.proc = None
+        self.index = index
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+
+    def summary(self, t0: float, t1: float):
+        rows = []
+        for ts, line in self.samples:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                rows.append((ts, float(parts[0]), float(parts[1]), parts[3:7]))
+            except ValueError:
+                continue
+        inside = [r for r in rows if t0 <= r[0] <= t1]
+        window = "timed"
+        if not inside:
+            inside, window = rows, "whole run"
+        if not inside:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in inside for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": max(r[2] for r in inside),
+                "reasons": reasons, "samples": len(inside), "window": window}
+
+
+# --------------------------------------------------------------------------- workloads
+
+def _workloads(name):
+    from mixed_lora_projection_gb300.synth import SWEEP_LAYERS, SWEEP_PROJECTIONS, WORKLOADS, sweep_workload
+    if name == SWEEP:
+        return [(sweep_workload(p), layer, i) for layer in range(SWEEP_LAYERS)
+                for i, (p, _, _) in enumerate(SWEEP_PROJECTIONS)]
+    return [(WORKLOADS[name], 0, 0)]
+
+
+def _flops_of(items):
+    return sum(w.useful_flops() for w, _, _ in items)
+
+
+def _tokens_of(items):
+    return items[0][0].T
+
+
+def _fused_flops(w):
+    """Algorithmic FLOPs of the fused base+expand kernel: 2 T d_in d_out + 2 T_a r d_out."""
+    return 2.0 * w.T * w.d_in * w.d_out + 2.0 * w.adapter_rows * w.rank * w.d_out
+
+
+# --------------------------------------------------------------------------- our arm
+
+def run_ours(args, rank, world, dist):
+    import torch
+    from mixed_lora_projection_gb300 import LoraLinear, _lib as L
+    from mixed_lora_projection_gb300.synth import make_inputs
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    items = _workloads(args.workload)
+    n_copies = 1 if args.workload == SWEEP else 3
+    setups = []
+    handles = {}
+    for (w, layer, pi) in items:
+        key = (w.d_in, w.d_out, w.rank)
+        if key not in handles:
+            handles[key] = LoraLinear(w.d_in, w.d_out, w.rank, w.T, max(8, len(w.seg_ids)), dev)
+        copies = [make_inputs(w, dev, layer=layer, proj_index=pi + 4 * c, with_x=(c == 0)) for c in range(n_copies)]
+        y = torch.empty((w.T, w.d_out), dtype=torch.bfloat16, device=dev)
+        setups.append((w, handles[key], copies, y))
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i):
+        for (w, ll, copies, y) in setups:
+            c = copies[i % len(copies)]
+            ll.forward(copies[0].x, w.seg_offsets, w.seg_ids, c.w, c.a, c.b, c.scales, y=y, stream=stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    for ll in handles.values():
+        assert ll.status() == 0
+        ll.set_option(L.OPT_TIMING, 1)
+    launches0 = sum(ll.timing(1)[2] for ll in handles.values())
+
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    time.sleep(0.2)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.time()
+    ev0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    if dist:
+        dist.barrier()
+    time.sleep(0.1)
+    sampler.stop()
+    elapsed_ms = ev0.elapsed_time(ev1)
+    launches = sum(ll.timing(1)[2] for ll in handles.values()) - launches0
+    fused_ms = sum(ll.timing(1)[0] for ll in handles.values())
+    fused_n = sum(ll.timing(1)[1] for ll in handles.values())
+    shrink_ms = sum(ll.timing(0)[0] for ll in handles.values())
+    shrink_n = sum(ll.timing(0)[1] for ll in handles.values())
+    for ll in handles.values():
+        ll.set_option(L.OPT_TIMING, 0)
+        assert ll.status() == 0, "a kernel's bounded wait ran out"
+
+    # e2e: the host-buffer entry point, X in and Y out every step
+    x_host = [s[2][0].x.cpu().pin_memory() for s in setups]
+    y_host = [torch.empty((s[0].T, s[0].d_out), dtype=torch.bfloat16).pin_memory() for s in setups]
+
+    def e2e_step(i):
+        for j, (w, ll, copies, y) in enumerate(setups):
+            c = copies[i % len(copies)]
+            ll.forward_host(x_host[j], w.seg_offsets, w.seg_ids, c.w, c.a, c.b, c.scales, y_host[j], stream=stream)
+
+    for i in range(min(args.warmup, 3)):
+        e2e_step(i)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e2e_steps = max(1, min(args.steps, args.e2e_steps))
+    te0 = time.perf_counter()
+    for i in range(e2e_steps):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    e2e_ms = (time.perf_counter() - te0) * 1e3 / e2e_steps
+    if dist:
+        dist.barrier()
+
+    if dist:
+        import torch.distributed as D
+        t = torch.tensor([elapsed_ms, e2e_ms], dtype=torch.float64)
+        D.all_reduce(t, op=D.ReduceOp.MAX)
+        elapsed_ms, e2e_ms = float(t[0]), float(t[1])
+
+    ms_per_step = elapsed_ms / args.steps
+    flops = _flops_of(items)
+    value = world * flops * args.steps / (elapsed_ms * 1e-3) / 1e12
+    e2e_value = world * flops / (e2e_ms * 1e-3) / 1e12
+    peak_burst, peak_sust, hbm, src = _peaks()
+    fused_flops = sum(_fused_flops(w) for w, _, _ in items)
+    avg_fused_ms = fused_ms / args.steps if fused_n else None  # device time of the fused launches per step
+    achieved = fused_flops / (avg_fused_ms * 1e-3) / 1e12 if avg_fused_ms else None
+    traffic = _profiled_traffic(args.workload)
+    w0 = items[0][0]
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded Gaussian bf16; no checkpoint)",
+        "config": {"workload": args.workload, "T": w0.T, "d_in": w0.d_in if len(items) == 1 else "per projection",
+                   "d_out": w0.d_out if len(items) == 1 else "per projection", "rank": w0.rank,
+                   "segments": len(w0.seg_ids), "adapter_rows": w0.adapter_rows, "calls_per_step": len(items),
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "X larger than L2; 3 rotating weight copies" if n_copies > 1 else "96 distinct weight sets per step (17 GB)"},
+        "tokens_per_s": round(world * _tokens_of(items) * args.steps / (elapsed_ms * 1e-3), 1),
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2) if achieved else None,
+                     "peak": peak_burst, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak_burst, 4) if achieved else None,
+                     "traffic": traffic, "peak_source": f"{src} bf16 burst",
+                     "kernel": "lora_gemm_kernel<fused>", "algorithmic_flops_per_step": fused_flops},
+        "kernel_ms": {"fused": round(fused_ms / max(1, args.steps), 5), "shrink": round(shrink_ms / max(1, args.steps), 5),
+                      "fused_launches": fused_n, "shrink_launches": shrink_n},
+        "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": sum(2 * w.T * w.d_in for w, _, _ in items),
+                "d2h_bytes_per_step": sum(2 * w.T * w.d_out for w, _, _ in items),
+                "ms_per_step": round(e2e_ms, 4), "steps": e2e_steps},
+        "gpu_launches": launches,
+        "clocks": sampler.summary(t0, t1),
+    }
+    if w0.T <= 512 and len(items) == 1:
+        gbs = w0.algorithmic_bytes() / (avg_fused_ms * 1e-3) / 1e9 if avg_fused_ms else None
+        out["roofline_hbm"] = {"bound": "hbm", "achieved": round(gbs, 1) if gbs else None, "peak": hbm,
+                               "unit": "GB/s", "frac": round(gbs / hbm, 4) if gbs else None,
+                               "algorithmic_bytes": w0.algorithmic_bytes()}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(items, args.cpu_seconds)
+    for ll in handles.values():
+        ll.close()
+    return out
+
+
+# --------------------------------------------------------------------------- oracle timing
+
+def _oracle_block(w, layer, pi, rows, seed_rows=0):
+    """Inputs for a contiguous block of `rows` rows of workload w (starting at row 0), as
+    exact fp64 values, and the segments restricted to the block."""
+    import numpy as np
+    from mixed_lora_projection_gb300.synth import bf16_bits, make_inputs
+    from oracle import bf16_bits_to_f64
+    inp = make_inputs(w, "cpu", layer=layer, proj_index=pi, x_rows=rows)
+    f = lambda t: bf16_bits_to_f64(bf16_bits(t))  # noqa: E731
+    off, ids = [0], []
+    for i, a in enumerate(w.seg_ids):
+        lo, hi = min(w.seg_offsets[i], rows), min(w.seg_offsets[i + 1], rows)
+        if hi > lo:
+            off.append(hi)
+            ids.append(a)
+    return f(inp.x), off, ids, f(inp.w), [f(a) for a in inp.a], [f(b) for b in inp.b], inp.scales
+
+
+def _block_flops(w, off, ids):
+    rows = off[-1]
+    ta = sum(off[i + 1] - off[i] for i, a in enumerate(ids) if a)
+    return 2.0 * rows * w.d_in * w.d_out + 2.0 * ta * w.rank * (w.d_in + w.d_out)
+
+
+def cpu_baseline(items, seconds):
+    """The fp64 oracle, as it stands, on a contiguous block of the workload's rows, sized
+    to about `seconds` of host time."""
+    from oracle import lora_linear_fp64
+    w, layer, pi = items[0]
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    rows = min(w.T, 64)
+    data = _oracle_block(w, layer, pi, rows)
+    t = time.perf_counter()
+    lora_linear_fp64(*data)
+    dt = time.perf_counter() - t
+    rate = _block_flops(w, data[1], data[2]) / max(dt, 1e-6)
+    rows = int(min(w.T, max(64, rows * seconds / max(dt, 1e-6) * 0.8)))
+    data = _oracle_block(w, layer, pi, rows)
+    t = time.perf_counter()
+    lora_linear_fp64(*data)
+    dt = time.perf_counter() - t
+    fl = _block_flops(w, data[1], data[2])
+    return {"value": round(fl / dt / 1e12, 5), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"rows [0,{rows}) of {w.name} ({w.T} rows), layer 0, all {w.d_out} outputs: "
+                      f"{fl / 1e9:.1f} GFLOP fp64 in {dt:.1f} s (numpy/OpenBLAS, {cores} threads)"}
+
+
+def run_reference(args, rank, world):
+    """The oracle as the reference arm: every step is a bounded sample of the workload."""
+    from oracle import lora_linear_fp64
+    items = _workloads(args.workload)
+    w, layer, pi = items[0]
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    budget = max(0.05, args.cpu_seconds * 4 / max(1, args.steps + args.warmup))  # ~a few minutes in all
+    rows = min(w.T, 32)
+    data = _oracle_block(w, layer, pi, rows)
+    t = time.perf_counter()
+    lora_linear_fp64(*data)
+    dt = time.perf_counter() - t
+    rows = int(min(w.T, max(8, rows * budget / max(dt, 1e-6))))
+    data = _oracle_block(w, layer, pi, rows)
+    fl = _block_flops(w, data[1], data[2])
+    for _ in range(args.warmup):
+        lora_linear_fp64(*data)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        lora_linear_fp64(*data)
+    dt = (time.perf_counter() - t) / args.steps
+    value = fl / dt / 1e12
+    sample = f"rows [0,{rows}) of {w.name} per step ({w.T} rows in the full batch), all {w.d_out} outputs, fp64"
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world,
+            "host": "rank 0 only, host cores",
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded Gaussian bf16 values, exact in fp64)",
+            "config": {"workload": args.workload, "T": w.T, "d_in": w.d_in, "d_out": w.d_out, "rank": w.rank,
+                       "sample_rows": rows},
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="prefill_16k")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--e2e-steps", type=int, default=100)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as D
+        if args.impl == "reference":
+            if rank != 0:
+                return
+        else:
+            import torch
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+            D.init_process_group("nccl")
+            dist = D
+    if args.impl == "reference":
+        out = run_reference(args, rank, world)
+    else:
+        out = run_ours(args, rank, world, dist)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
