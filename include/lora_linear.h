@@ -181,6 +181,40 @@ int lora_linear_describe(lora_linear* h, int T, const int32_t* seg_offsets,
                          const int32_t* seg_adapter_ids, int n_seg, int* tile_n, int* n_tiles,
                          int* n_units, int* grid, int* stages, int* has_shrink);
 
+/*
+ * lora_linear_forward_noalloc -- the same projection without a handle and without
+ * allocating any memory, for callers that cannot call cudaMalloc: code that runs while
+ * another component owns all device memory (a serving engine whose pools were reserved
+ * up front, so a raw allocation fails or fragments them), code on a latency-critical
+ * path where cudaMalloc's implicit device-wide synchronisation would stall other
+ * streams, and plugins whose host process forbids allocations after start-up.
+ * The source pages describe no such entry point; it exists for these callers.
+ *
+ * Scratch: the shrink output U, the work list and a status word live in one file-scope
+ * __device__ array of LORA_NOALLOC_SCRATCH_BYTES (about 2.2 MB), which every GPU that
+ * loads this library holds until the process exits. Limits: T <= LORA_NOALLOC_MAX_TOKENS,
+ * n_seg <= LORA_NOALLOC_MAX_SEGMENTS, rank <= LORA_MAX_RANK; larger requests return
+ * LORA_EINVAL and launch nothing.
+ * Arguments are those of lora_linear_forward plus the shape (d_in, d_out, rank), with the
+ * same layouts, alignment rules and checks; the caller still owns x, W, A, B and y.
+ * The first call on a device looks up the scratch array's device address there
+ * (cudaGetSymbolAddress) and sets the kernels' shared-memory limit; make that first call
+ * before any stream capture. Every call shares the one scratch array and leaves its
+ * contents behind: calls that overlap on the GPU (on different streams, or from several
+ * threads) race and give wrong results; order them on one stream. The work list is copied
+ * from host memory with cudaMemcpyAsync before the launches. A kernel wait that runs out
+ * stops that kernel early; this entry point cannot report it afterwards.
+ * Returns LORA_OK, LORA_EINVAL, LORA_ENODEV or LORA_ECUDA.
+ */
+#define LORA_NOALLOC_MAX_TOKENS 4096
+#define LORA_NOALLOC_MAX_SEGMENTS 64
+#define LORA_NOALLOC_SCRATCH_BYTES (((LORA_NOALLOC_MAX_TOKENS + 128) * LORA_MAX_RANK * 2) + 65536)
+int lora_linear_forward_noalloc(const void* x, int T, const int32_t* seg_offsets,
+                                const int32_t* seg_adapter_ids, int n_seg, int d_in, int d_out,
+                                int rank, const void* W, const void* const* A,
+                                const void* const* B, const float* scale, int n_adapters,
+                                void* y, void* stream);
+
 /* lora_linear_error_string -- a short static description of a return code. */
 const char* lora_linear_error_string(int code);
 
