@@ -157,7 +157,8 @@ enum {
     LORA_OPT_WAIT_LIMIT_US = 2, /* bound of every in-kernel wait, microseconds (default 4,000,000) */
     LORA_OPT_DEBUG_STALL = 3,   /* 1 = the load warp never issues: every wait runs out (tests only) */
     LORA_OPT_TIMING = 4,        /* 1 = record CUDA events around each kernel launch */
-    LORA_OPT_RASTER = 5         /* 0 = auto, 1 = row tiles fastest, 2 = column tiles fastest */
+    LORA_OPT_RASTER = 5,        /* 0 = auto, 1 = row tiles fastest, 2 = column tiles fastest */
+    LORA_OPT_TWO_LAUNCH = 6     /* 1 = shrink and fused pass as two launches (default 0: one launch) */
 };
 
 /* lora_linear_set_option -- set one option above. Returns LORA_OK or LORA_EINVAL. */
@@ -166,7 +167,9 @@ int lora_linear_set_option(lora_linear* h, int option, long long value);
 /*
  * lora_linear_timing -- with LORA_OPT_TIMING on: synchronises on the recorded events and
  * returns, per kernel kind, the summed device time in milliseconds and the launch count
- * since the option was last set. kind 0 = shrink, 1 = fused base+expand. Also returns
+ * since the option was last set. kind 0 = a separate shrink launch (two-launch mode
+ * only), 1 = the launch that computes Y (in the default one-launch mode it also runs the
+ * shrink). Also returns
  * the total number of kernels this handle has launched (any option state).
  */
 int lora_linear_timing(lora_linear* h, int kind, double* total_ms, long long* launches,

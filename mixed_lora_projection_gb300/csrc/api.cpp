@@ -64,6 +64,8 @@ struct lora_linear {
     void* u_ws = nullptr;       // bf16 [u_rows, rank]: shrink output, read by the fused pass
     int u_rows = 0;
     int* status = nullptr;      // device status word
+    int* flags = nullptr;       // per fused tile: epoch of the call whose U rows are ready
+    int epoch = 0;
     int* status_host = nullptr; // pinned copy for forward_host
     Slot slots[kRing];
     size_t slot_bytes = 0;
@@ -71,7 +73,7 @@ struct lora_linear {
     int max_fused = 0;
     EncodeTiledFn encode = nullptr;
     // options
-    int force_tile_n = 0, raster = 0, debug_stall = 0, timing = 0;
+    int force_tile_n = 0, raster = 0, debug_stall = 0, timing = 0, two_launch = 0;
     unsigned long long wait_limit_ns = 4000000000ull;
     std::vector<TimingRec> trec;
     std::vector<cudaEvent_t> ev_pool;
@@ -108,6 +110,7 @@ void free_handle(lora_linear* h) {
     for (cudaEvent_t e : h->ev_pool) cudaEventDestroy(e);
     if (h->u_ws) cudaFree(h->u_ws);
     if (h->status) cudaFree(h->status);
+    if (h->flags) cudaFree(h->flags);
     if (h->status_host) cudaFreeHost(h->status_host);
     if (h->x_stage) cudaFree(h->x_stage);
     if (h->y_stage) cudaFree(h->y_stage);
@@ -294,6 +297,7 @@ int lora_linear_create(lora_linear** out, int d_in, int d_out, int rank, int max
                     align_up(4 * (size_t)max_segments, 16) + 256;
     if (cudaMalloc(&h->u_ws, (size_t)h->u_rows * rank * 2) != cudaSuccess ||
         cudaMalloc((void**)&h->status, sizeof(int)) != cudaSuccess ||
+        cudaMalloc((void**)&h->flags, sizeof(int) * (size_t)h->max_fused) != cudaSuccess ||
         cudaHostAlloc((void**)&h->status_host, sizeof(int), cudaHostAllocDefault) != cudaSuccess) {
         cudaGetLastError();
         free_handle(h);
@@ -312,6 +316,7 @@ int lora_linear_create(lora_linear** out, int d_in, int d_out, int rank, int max
         }
     }
     if (cudaMemset(h->status, 0, sizeof(int)) != cudaSuccess ||
+        cudaMemset(h->flags, 0, sizeof(int) * (size_t)h->max_fused) != cudaSuccess ||
         cudaMemset(h->u_ws, 0, (size_t)h->u_rows * rank * 2) != cudaSuccess) {
         free_handle(h);
         return LORA_ECUDA;
@@ -357,6 +362,9 @@ int lora_linear_set_option(lora_linear* h, int option, long long value) {
         case LORA_OPT_RASTER:
             if (value < 0 || value > 2) return LORA_EINVAL;
             h->raster = (int)value;
+            return LORA_OK;
+        case LORA_OPT_TWO_LAUNCH:
+            h->two_launch = value ? 1 : 0;
             return LORA_OK;
         default:
             return LORA_EINVAL;
@@ -409,8 +417,8 @@ int lora_linear_describe(lora_linear* h, int T, const int32_t* seg_offsets,
     if (tile_n) *tile_n = tn;
     if (n_tiles) *n_tiles = nf;
     if (n_units) *n_units = units;
-    if (grid) *grid = std::min(units, h->num_sms);
-    if (stages) *stages = tn ? stages_for(tn) : 0;
+    if (grid) *grid = std::min(units + (int)plan.shrink.size(), h->num_sms);
+    if (stages) *stages = tn ? stages_for(std::max(tn, ceil_div(h->rank, 16) * 16)) : 0;
     if (has_shrink) *has_shrink = plan.shrink.empty() ? 0 : 1;
     return LORA_OK;
 }
@@ -478,13 +486,31 @@ int lora_linear_forward(lora_linear* h, const void* x, int T, const int32_t* seg
     GemmParams p;
     memset(&p, 0, sizeof(p));
     if (encode_2d(h, &p.tm_x, x, h->d_in, T, kTileK, kTileM) != CUDA_SUCCESS) return LORA_ECUDA;
+    if (encode_2d(h, &p.tm_w, W, h->d_in, h->d_out, kTileK, tile_n) != CUDA_SUCCESS) return LORA_ECUDA;
+    if (encode_2d(h, &p.tm_u, h->u_ws, h->rank, h->u_rows, kTileK, kTileM) != CUDA_SUCCESS) return LORA_ECUDA;
+    p.tm_b = reinterpret_cast<const CUtensorMap*>(slot->dev + off_bmaps);
+    p.tm_a = reinterpret_cast<const CUtensorMap*>(slot->dev + off_amaps);
+    p.shrink_tiles = reinterpret_cast<const Tile*>(slot->dev + off_shrink);
+    p.fused_tiles = reinterpret_cast<const Tile*>(slot->dev + off_fused);
     p.seg_off = reinterpret_cast<const int32_t*>(slot->dev + off_segoff);
     p.seg_id = reinterpret_cast<const int32_t*>(slot->dev + off_segid);
     p.scales = reinterpret_cast<const float*>(slot->dev + off_scale);
-    p.n_seg = n_m;
+    p.y = y;
+    p.u = h->u_ws;
     p.status = h->status;
     p.wait_limit_ns = h->wait_limit_ns;
+    p.n_seg = n_m;
+    p.n_shrink = ns;
+    p.n_fused = nf;
+    p.n_ntiles = n_ntiles;
+    p.tile_n = tile_n;
+    p.shrink_n = shrink_n;
+    p.stages = stages_for(std::max(tile_n, shrink_n));
+    p.m_fastest = choose_m_fastest(h, nf, n_ntiles, tile_n);
     p.k_main_blocks = ceil_div(h->d_in, kTileK);
+    p.k_lora_blocks = ceil_div(h->rank, kTileK);
+    p.d_out = h->d_out;
+    p.rank = h->rank;
     p.debug_stall = h->debug_stall;
 
     TimingRec rec{};
@@ -493,44 +519,30 @@ int lora_linear_forward(lora_linear* h, const void* x, int T, const int32_t* seg
             rec.ev[i] = take_event(h);
             if (!rec.ev[i]) return LORA_ECUDA;
         }
-        rec.has_shrink = ns > 0;
         cudaEventRecord(rec.ev[0], stream);
     }
-    if (ns > 0) {
+    const int fused_units = nf * n_ntiles;
+    if (h->two_launch && ns > 0) {
+        // shrink, then fused base+expand ordered by the stream
         GemmParams s = p;
-        s.tm_adapter = reinterpret_cast<const CUtensorMap*>(slot->dev + off_amaps);
-        s.tiles = reinterpret_cast<const Tile*>(slot->dev + off_shrink);
-        s.n_tiles = ns;
-        s.n_ntiles = 1;
-        s.tile_n = shrink_n;
-        s.stages = stages_for(shrink_n);
-        s.m_fastest = 1;
-        s.k_lora_blocks = 0;
-        s.out = h->u_ws;
-        s.ld_out = h->rank;
-        s.n_out = h->rank;
-        if (launch_gemm(kShrink, s, std::min(ns, h->num_sms), stream) != cudaSuccess) return LORA_ECUDA;
+        s.n_fused = 0;
+        if (launch_gemm(s, std::min(ns, h->num_sms), stream) != cudaSuccess) return LORA_ECUDA;
         ++h->launches;
-    }
-    if (h->timing) cudaEventRecord(rec.ev[1], stream);
-    {
+        rec.has_shrink = true;
+        if (h->timing) cudaEventRecord(rec.ev[1], stream);
         GemmParams f = p;
-        if (encode_2d(h, &f.tm_w, W, h->d_in, h->d_out, kTileK, tile_n) != CUDA_SUCCESS) return LORA_ECUDA;
-        if (encode_2d(h, &f.tm_u, h->u_ws, h->rank, h->u_rows, kTileK, kTileM) != CUDA_SUCCESS)
-            return LORA_ECUDA;
-        f.tm_adapter = reinterpret_cast<const CUtensorMap*>(slot->dev + off_bmaps);
-        f.tiles = reinterpret_cast<const Tile*>(slot->dev + off_fused);
-        f.n_tiles = nf;
-        f.n_ntiles = n_ntiles;
-        f.tile_n = tile_n;
-        f.stages = stages_for(tile_n);
-        f.m_fastest = choose_m_fastest(h, nf, n_ntiles, tile_n);
-        f.k_lora_blocks = ceil_div(h->rank, kTileK);
-        f.out = y;
-        f.ld_out = h->d_out;
-        f.n_out = h->d_out;
-        const int units = nf * n_ntiles;
-        if (launch_gemm(kFused, f, std::min(units, h->num_sms), stream) != cudaSuccess) return LORA_ECUDA;
+        f.n_shrink = 0;
+        if (launch_gemm(f, std::min(fused_units, h->num_sms), stream) != cudaSuccess) return LORA_ECUDA;
+        ++h->launches;
+    } else {
+        // one launch: shrink units first, fused units wait on the per-tile ready flags
+        if (h->timing) cudaEventRecord(rec.ev[1], stream);
+        if (ns > 0) {
+            h->epoch = h->epoch == 0x7fffffff ? 1 : h->epoch + 1;
+            p.flags = h->flags;
+            p.epoch = h->epoch;
+        }
+        if (launch_gemm(p, std::min(ns + fused_units, h->num_sms), stream) != cudaSuccess) return LORA_ECUDA;
         ++h->launches;
     }
     if (h->timing) {

@@ -2,16 +2,22 @@
 //
 // One persistent, warp-specialised tile GEMM serves both passes of the method ("Two 27B
 // models on a single RTX 5090", section 4: the adapter's two thin matrices run beside
-// the changed matrix and their output is added):
+// the changed matrix and their output is added), as two kinds of work unit of one launch:
 //
-//   shrink (Mode kShrink):  U[t, 0:r]   = bf16( s_a * X[t,:] A_a^T )  for the rows of adapter
-//                           tiles; rows of the tile that name no adapter get U = 0.
-//   fused  (Mode kFused):   acc[t, n]   = X[t,:] W[n,:]^T           (K = d_in)
-//                           acc[t, n]  += U[t,:] B_a[n,:]^T         (K = r, adapter tiles only,
-//                                                                    same TMEM accumulator)
-//                           Y[t, n]     = bf16(acc[t, n])
+//   shrink unit:  U[t, 0:r]   = bf16( s_a * X[t,:] A_a^T )  for the rows of one adapter tile;
+//                 rows of the tile that name no adapter get U = 0.
+//   fused unit:   acc[t, n]   = X[t,:] W[n,:]^T           (K = d_in)
+//                 acc[t, n]  += U[t,:] B_a[n,:]^T         (K = r, adapter tiles only, same
+//                                                          TMEM accumulator)
+//                 Y[t, n]     = bf16(acc[t, n])
 //
-// Per CTA (one per SM, persistent over work units = planner tile x output-column tile):
+// Shrink units come first in the unit order. A fused unit of an adapter tile waits, before
+// its expand k-blocks, for a ready flag that the tile's shrink unit publishes (release /
+// acquire at GPU scope, plus async-proxy fences because U is written with plain stores and
+// read by TMA). A CTA only ever waits for units earlier in the order, which every other
+// CTA reaches without waiting, so the dependency cannot cycle.
+//
+// Per CTA (one per SM, persistent over the work units):
 //   warp 0      one thread issues TMA loads (cp.async.bulk.tensor, 128-byte swizzle) of a
 //               128x64 A tile and a tile_n x 64 B tile per stage into a shared-memory ring;
 //   warp 1      owns 512 TMEM columns (two 128x256 fp32 accumulators); one thread issues
@@ -187,14 +193,80 @@ __device__ __forceinline__ int row_adapter(const int32_t* off, const int32_t* id
     return ids[lo];
 }
 
-template <int MODE>
+// ---------------------------------------------------------------- cross-CTA flags
+__device__ __forceinline__ int ld_acquire(const int* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release(int* p, int v) {
+    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Generic-proxy global writes / reads ordered against the async proxy (TMA).
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+__device__ __forceinline__ void epilogue_bar_sync() {
+    asm volatile("bar.sync 1, %0;" ::"n"(kEpilogueThreads) : "memory");
+}
+// Waits until *flag == epoch (bounded like wait_bounded).
+__device__ __noinline__ bool wait_flag(const int* flag, int epoch, volatile int* abort_flag, int* status,
+                                       uint64_t limit_ns) {
+    if (ld_acquire(flag) == epoch) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        __nanosleep(64);
+        if (ld_acquire(flag) == epoch) return true;
+        if (*abort_flag) return false;
+        if (global_timer_ns() - t0 > limit_ns) {
+            atomicOr(status, 1);
+            *abort_flag = 1;
+            return false;
+        }
+    }
+}
+
+// One work unit, as every role decodes it.
+struct Unit {
+    Tile tile;
+    int shrink;      // 1: shrink unit (U rows), 0: fused unit (Y block)
+    int tile_index;  // fused tile index (flag slot)
+    int n0;          // first output column
+    int n;           // MMA N of this unit
+    int nk;          // k-blocks of 64
+};
+
+__device__ __forceinline__ Unit decode_unit(const GemmParams& p, int u) {
+    Unit r;
+    if (u < p.n_shrink) {
+        r.tile = p.shrink_tiles[u];
+        r.shrink = 1;
+        r.tile_index = r.tile.fused_index;
+        r.n0 = 0;
+        r.n = p.shrink_n;
+        r.nk = p.k_main_blocks;
+    } else {
+        const int v = u - p.n_shrink;
+        const int ti = p.m_fastest ? (v % p.n_fused) : (v / p.n_ntiles);
+        const int nt = p.m_fastest ? (v / p.n_fused) : (v % p.n_ntiles);
+        r.tile = p.fused_tiles[ti];
+        r.shrink = 0;
+        r.tile_index = ti;
+        r.n0 = nt * p.tile_n;
+        r.n = p.tile_n;
+        r.nk = p.k_main_blocks + (r.tile.adapter ? p.k_lora_blocks : 0);
+    }
+    return r;
+}
+
 __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_constant__ GemmParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // carve: rings (1024-aligned), then barriers, then the TMEM slot and the abort flag
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
     const int stages = p.stages;
-    const uint32_t b_stage_bytes = (uint32_t)p.tile_n * kTileK * 2;
+    const int b_rows = p.tile_n > p.shrink_n ? p.tile_n : p.shrink_n;  // B stage sized for either kind
+    const uint32_t b_stage_bytes = (uint32_t)b_rows * kTileK * 2;
     uint8_t* a_ring = base;
     uint8_t* b_ring = a_ring + (size_t)stages * kStageBytesA;
     uint64_t* bars = reinterpret_cast<uint64_t*>(b_ring + (size_t)stages * b_stage_bytes);
@@ -228,44 +300,55 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    const int n_units = p.n_tiles * p.n_ntiles;
+    const int n_units = p.n_shrink + p.n_fused * p.n_ntiles;
     const uint64_t limit = p.wait_limit_ns;
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0 && !p.debug_stall) {
             tma_prefetch_desc(&p.tm_x);
-            if (MODE == kFused) { tma_prefetch_desc(&p.tm_w); tma_prefetch_desc(&p.tm_u); }
+            if (p.n_fused) { tma_prefetch_desc(&p.tm_w); tma_prefetch_desc(&p.tm_u); }
             int stage = 0;
             uint32_t phase = 0;
             long long issued = 0;
-            int acquired = -1;  // compact adapter whose global tensor map was last acquired
+            int acquired_a = -1, acquired_b = -1;  // adapters whose global tensor maps were acquired
             bool ok = true;
             for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-                const int ti = p.m_fastest ? (u % p.n_tiles) : (u / p.n_ntiles);
-                const int nt = p.m_fastest ? (u / p.n_tiles) : (u % p.n_ntiles);
-                const Tile tile = p.tiles[ti];
-                const int n0 = nt * p.tile_n;
-                const CUtensorMap* ad = tile.adapter ? &p.tm_adapter[tile.adapter - 1] : nullptr;
-                if (ad && acquired != tile.adapter) { tensormap_acquire(ad); acquired = tile.adapter; }
-                const CUtensorMap* bmain = (MODE == kFused) ? &p.tm_w : ad;
-                const int nk = p.k_main_blocks + ((MODE == kFused && tile.adapter) ? p.k_lora_blocks : 0);
-                for (int kb = 0; kb < nk; ++kb) {
+                const Unit w = decode_unit(p, u);
+                const int ad = w.tile.adapter;
+                const CUtensorMap* bmain = &p.tm_w;
+                if (w.shrink) {
+                    bmain = &p.tm_a[ad - 1];
+                    if (acquired_a != ad) { tensormap_acquire(bmain); acquired_a = ad; }
+                } else if (ad && acquired_b != ad) {
+                    tensormap_acquire(&p.tm_b[ad - 1]);
+                    acquired_b = ad;
+                }
+                const uint32_t tx = kStageBytesA + (uint32_t)w.n * kTileK * 2;
+                for (int kb = 0; kb < w.nk; ++kb) {
+                    if (kb == p.k_main_blocks && p.flags) {
+                        // the expand reads U rows written by this tile's shrink unit
+                        if (!wait_flag(&p.flags[w.tile_index], p.epoch, abort_flag, p.status, limit)) {
+                            ok = false;
+                            break;
+                        }
+                        fence_proxy_async_global();
+                    }
                     if (!wait_bounded(smem_addr(&empty[stage]), phase ^ 1, abort_flag, p.status, limit, true)) {
                         ok = false;
                         break;
                     }
                     const uint32_t fb = smem_addr(&full[stage]);
-                    mbar_arrive_expect_tx(fb, kStageBytesA + b_stage_bytes);
+                    mbar_arrive_expect_tx(fb, tx);
                     const uint32_t sa = smem_addr(a_ring + (size_t)stage * kStageBytesA);
                     const uint32_t sb = smem_addr(b_ring + (size_t)stage * b_stage_bytes);
                     if (kb < p.k_main_blocks) {
-                        tma_load_2d(sa, &p.tm_x, fb, kb * kTileK, tile.row0);
-                        tma_load_2d(sb, bmain, fb, kb * kTileK, n0);
+                        tma_load_2d(sa, &p.tm_x, fb, kb * kTileK, w.tile.row0);
+                        tma_load_2d(sb, bmain, fb, kb * kTileK, w.n0);
                     } else {
                         const int k = (kb - p.k_main_blocks) * kTileK;
-                        tma_load_2d(sa, &p.tm_u, fb, k, tile.row0);
-                        tma_load_2d(sb, ad, fb, k, n0);
+                        tma_load_2d(sa, &p.tm_u, fb, k, w.tile.row0);
+                        tma_load_2d(sb, &p.tm_b[ad - 1], fb, k, w.n0);
                     }
                     ++issued;
                     if (++stage == stages) { stage = 0; phase ^= 1; }
@@ -282,15 +365,13 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            const uint32_t idesc = instr_desc_bf16(kTileM, p.tile_n);
             int stage = 0;
             uint32_t phase = 0;
             int it = 0;
             bool ok = true;
             for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++it) {
-                const int ti = p.m_fastest ? (u % p.n_tiles) : (u / p.n_ntiles);
-                const Tile tile = p.tiles[ti];
-                const int nk = p.k_main_blocks + ((MODE == kFused && tile.adapter) ? p.k_lora_blocks : 0);
+                const Unit w = decode_unit(p, u);
+                const uint32_t idesc = instr_desc_bf16(kTileM, w.n);
                 const int acc = it & 1;
                 if (!wait_bounded(smem_addr(&tempty[acc]), ((it >> 1) & 1) ^ 1, abort_flag, p.status, limit, true)) {
                     ok = false;
@@ -298,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
                 }
                 tc_fence_after();
                 const uint32_t d = tmem_base + (uint32_t)(acc * kAccCols);
-                for (int kb = 0; kb < nk; ++kb) {
+                for (int kb = 0; kb < w.nk; ++kb) {
                     if (!wait_bounded(smem_addr(&full[stage]), phase, abort_flag, p.status, limit, true)) {
                         ok = false;
                         break;
@@ -329,9 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
         int it = 0;
         for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++it) {
-            const int ti = p.m_fastest ? (u % p.n_tiles) : (u / p.n_ntiles);
-            const int nt = p.m_fastest ? (u / p.n_tiles) : (u % p.n_ntiles);
-            const Tile tile = p.tiles[ti];
+            const Unit w = decode_unit(p, u);
             const int acc = it & 1;
             int ok = 1;
             if (lane == 0)
@@ -339,37 +418,70 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             tc_fence_after();
-            const int row = tile.row0 + r_local;
-            const bool row_ok = r_local < tile.nrows;
+            const int row = w.tile.row0 + r_local;
+            const bool row_ok = r_local < w.tile.nrows;
             float scale = 1.0f;
-            if (MODE == kShrink) {
-                int a = row_ok ? row_adapter(p.seg_off, p.seg_id, p.n_seg, row) : 0;
-                scale = (a == tile.adapter) ? p.scales[tile.adapter - 1] : 0.0f;
+            __nv_bfloat16* out;
+            int n_out;
+            if (w.shrink) {
+                const int a = row_ok ? row_adapter(p.seg_off, p.seg_id, p.n_seg, row) : 0;
+                scale = (a == w.tile.adapter) ? p.scales[w.tile.adapter - 1] : 0.0f;
+                out = reinterpret_cast<__nv_bfloat16*>(p.u) + (size_t)row * p.rank;
+                n_out = p.rank;
+            } else {
+                out = reinterpret_cast<__nv_bfloat16*>(p.y) + (size_t)row * p.d_out + w.n0;
+                n_out = p.d_out - w.n0;
             }
-            const int n0 = nt * p.tile_n;
-            __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out) + (size_t)row * p.ld_out + n0;
             const uint32_t taddr = tmem_base + (uint32_t)(acc * kAccCols) + lane_off;
-            for (int c = 0; c < p.tile_n; c += 16) {
+            int c = 0;
+            for (; c + 32 <= w.n; c += 32) {
+                uint32_t v[32];
+                tmem_ld16(taddr + (uint32_t)c, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
+                tmem_ld16(taddr + (uint32_t)c + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
+                tmem_ld_wait();
+                if (row_ok) {
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        if (c + 8 * h < n_out) {
+                            uint4 o;
+                            o.x = pack_bf16x2(__uint_as_float(v[8 * h + 0]) * scale, __uint_as_float(v[8 * h + 1]) * scale);
+                            o.y = pack_bf16x2(__uint_as_float(v[8 * h + 2]) * scale, __uint_as_float(v[8 * h + 3]) * scale);
+                            o.z = pack_bf16x2(__uint_as_float(v[8 * h + 4]) * scale, __uint_as_float(v[8 * h + 5]) * scale);
+                            o.w = pack_bf16x2(__uint_as_float(v[8 * h + 6]) * scale, __uint_as_float(v[8 * h + 7]) * scale);
+                            *reinterpret_cast<uint4*>(out + c + 8 * h) = o;
+                        }
+                    }
+                }
+            }
+            if (c < w.n) {  // a last 16 columns
                 uint32_t v[16];
                 tmem_ld16(taddr + (uint32_t)c, v);
                 tmem_ld_wait();
                 if (row_ok) {
-                    uint4 lo, hi;
-                    lo.x = pack_bf16x2(__uint_as_float(v[0]) * scale, __uint_as_float(v[1]) * scale);
-                    lo.y = pack_bf16x2(__uint_as_float(v[2]) * scale, __uint_as_float(v[3]) * scale);
-                    lo.z = pack_bf16x2(__uint_as_float(v[4]) * scale, __uint_as_float(v[5]) * scale);
-                    lo.w = pack_bf16x2(__uint_as_float(v[6]) * scale, __uint_as_float(v[7]) * scale);
-                    hi.x = pack_bf16x2(__uint_as_float(v[8]) * scale, __uint_as_float(v[9]) * scale);
-                    hi.y = pack_bf16x2(__uint_as_float(v[10]) * scale, __uint_as_float(v[11]) * scale);
-                    hi.z = pack_bf16x2(__uint_as_float(v[12]) * scale, __uint_as_float(v[13]) * scale);
-                    hi.w = pack_bf16x2(__uint_as_float(v[14]) * scale, __uint_as_float(v[15]) * scale);
-                    const int col = n0 + c;
-                    if (col < p.n_out) *reinterpret_cast<uint4*>(out + c) = lo;
-                    if (col + 8 < p.n_out) *reinterpret_cast<uint4*>(out + c + 8) = hi;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        if (c + 8 * h < n_out) {
+                            uint4 o;
+                            o.x = pack_bf16x2(__uint_as_float(v[8 * h + 0]) * scale, __uint_as_float(v[8 * h + 1]) * scale);
+                            o.y = pack_bf16x2(__uint_as_float(v[8 * h + 2]) * scale, __uint_as_float(v[8 * h + 3]) * scale);
+                            o.z = pack_bf16x2(__uint_as_float(v[8 * h + 4]) * scale, __uint_as_float(v[8 * h + 5]) * scale);
+                            o.w = pack_bf16x2(__uint_as_float(v[8 * h + 6]) * scale, __uint_as_float(v[8 * h + 7]) * scale);
+                            *reinterpret_cast<uint4*>(out + c + 8 * h) = o;
+                        }
+                    }
                 }
             }
             tc_fence_before();
             mbar_arrive(smem_addr(&tempty[acc]));
+            if (w.shrink && p.flags) {
+                // publish this tile's U rows to the fused units that wait for them
+                fence_proxy_async_global();
+                epilogue_bar_sync();
+                if (warp == 2 && lane == 0) {
+                    __threadfence();
+                    st_release(&p.flags[w.tile_index], p.epoch);
+                }
+            }
         }
     }
 
@@ -384,25 +496,20 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
 
 }  // namespace dev
 
-size_t gemm_smem_bytes(int tile_n, int stages) {
-    return 1024 + (size_t)stages * (kStageBytesA + (size_t)tile_n * kTileK * 2) +
+size_t gemm_smem_bytes(int b_tile_rows, int stages) {
+    return 1024 + (size_t)stages * (kStageBytesA + (size_t)b_tile_rows * kTileK * 2) +
            8 * (2 * (size_t)stages + 5) + 16;
 }
 
 cudaError_t gemm_prepare_device() {
-    cudaError_t e = cudaFuncSetAttribute(dev::lora_gemm_kernel<kFused>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget + 2048);
-    if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(dev::lora_gemm_kernel<kShrink>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget + 2048);
+    return cudaFuncSetAttribute(dev::lora_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kSmemBudget + 2048);
 }
 
-cudaError_t launch_gemm(int mode, const GemmParams& p, int grid, cudaStream_t stream) {
-    const size_t smem = gemm_smem_bytes(p.tile_n, p.stages);
-    if (mode == kFused)
-        dev::lora_gemm_kernel<kFused><<<grid, kThreads, smem, stream>>>(p);
-    else
-        dev::lora_gemm_kernel<kShrink><<<grid, kThreads, smem, stream>>>(p);
+cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t stream) {
+    const int b_rows = p.tile_n > p.shrink_n ? p.tile_n : p.shrink_n;
+    const size_t smem = gemm_smem_bytes(b_rows, p.stages);
+    dev::lora_gemm_kernel<<<grid, kThreads, smem, stream>>>(p);
     return cudaGetLastError();
 }
 

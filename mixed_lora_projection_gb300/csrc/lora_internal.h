@@ -19,35 +19,46 @@ constexpr int kSmemBudget = 232448 - 2048;             // opt-in dynamic smem mi
 constexpr int kThreads = 192;        // warp 0 TMA, warp 1 MMA + TMEM owner, warps 2..5 epilogue
 constexpr int kEpilogueThreads = 128;
 
-enum Mode { kFused = 0, kShrink = 1 };
-
 struct Tile {                        // one planner tile, as uploaded to the device
-    int32_t row0, nrows, adapter, pad;
+    int32_t row0, nrows, adapter;    // adapter: compact slot (1-based), 0 = none
+    int32_t fused_index;             // shrink tiles: index of the same rows among the fused tiles
 };
 
 // Parameters of one launch of the tile GEMM. Passed by value as a __grid_constant__.
+// Work units: [0, n_shrink) are shrink units (U rows of one adapter tile, N = shrink_n),
+// then n_fused x n_ntiles fused units (a 128 x tile_n block of Y: base K-loop over d_in,
+// then, for adapter tiles, the expand K-loop over the rank into the same accumulator).
+// When `flags` is set, a fused unit's expand waits until flags[tile] == epoch, which the
+// shrink unit of that tile publishes after its U rows are stored (single-launch mode).
 struct GemmParams {
     CUtensorMap tm_x;                // X [T, d_in], box 64 x 128
-    CUtensorMap tm_w;                // W [d_out, d_in], box 64 x tile_n (fused only)
-    CUtensorMap tm_u;                // U [u_rows, rank], box 64 x 128 (fused only)
-    const CUtensorMap* tm_adapter;   // device array, per compact adapter: fused -> B_a, shrink -> A_a
-    const Tile* tiles;               // device array [n_tiles]
+    CUtensorMap tm_w;                // W [d_out, d_in], box 64 x tile_n
+    CUtensorMap tm_u;                // U [u_rows, rank], box 64 x 128
+    const CUtensorMap* tm_b;         // device array per compact adapter: B_a [d_out, rank], box 64 x tile_n
+    const CUtensorMap* tm_a;         // device array per compact adapter: A_a [rank, d_in], box 64 x shrink_n
+    const Tile* shrink_tiles;        // device [n_shrink]
+    const Tile* fused_tiles;         // device [n_fused]
     const int32_t* seg_off;          // merged segments (device), compact ids
     const int32_t* seg_id;
     const float* scales;             // per compact adapter (device)
-    void* out;                       // Y [T, d_out] (fused) or U [u_rows, rank] (shrink), bf16
+    void* y;                         // Y [T, d_out] bf16
+    void* u;                         // U [u_rows, rank] bf16
+    int* flags;                      // per fused tile; nullptr = no in-kernel dependency
     int* status;                     // device status word: bit 0 = a bounded wait ran out
     unsigned long long wait_limit_ns;
+    int epoch;
     int n_seg;
-    int n_tiles;                     // planner tiles in this launch
-    int n_ntiles;                    // output-column tiles
-    int tile_n;                      // output-tile width (multiple of 16, <= 256)
+    int n_shrink;
+    int n_fused;
+    int n_ntiles;                    // output-column tiles of the fused units
+    int tile_n;                      // fused output-tile width (multiple of 16, <= 256)
+    int shrink_n;                    // shrink output-tile width = rank rounded up to 16
     int stages;
-    int m_fastest;                   // 1: consecutive work units walk row tiles first
+    int m_fastest;                   // 1: consecutive fused units walk row tiles first
     int k_main_blocks;               // ceil(d_in / 64)
-    int k_lora_blocks;               // ceil(rank / 64) (fused) or 0
-    int ld_out;                      // row stride of out, elements
-    int n_out;                       // valid output columns (d_out or rank)
+    int k_lora_blocks;               // ceil(rank / 64)
+    int d_out;
+    int rank;
     int debug_stall;
 };
 
@@ -63,8 +74,8 @@ int plan_segments(const int32_t* seg_offsets, const int32_t* seg_ids, int n_seg,
                   int n_adapters, Plan* plan);
 
 // kernels.cu
-size_t gemm_smem_bytes(int tile_n, int stages);
+size_t gemm_smem_bytes(int b_tile_rows, int stages);
 cudaError_t gemm_prepare_device();           // sets the opt-in smem limit on the current device
-cudaError_t launch_gemm(int mode, const GemmParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t stream);
 
 }  // namespace lora

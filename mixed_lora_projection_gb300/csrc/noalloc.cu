@@ -149,6 +149,7 @@ void plan_fixed(const int32_t* off, const int32_t* ids, int n_seg, FixedPlan* p)
                 --j;
             }
             p->shrink[j] = p->fused[i];
+            p->shrink[j].fused_index = i;
         }
     for (int i = 0; i < p->n_shrink; ++i)
         if (!p->n_used || p->used[p->n_used - 1] != p->shrink[i].adapter - 1) p->used[p->n_used++] = p->shrink[i].adapter - 1;
@@ -217,45 +218,41 @@ extern "C" int lora_linear_forward_noalloc(const void* x, int T, const int32_t* 
     GemmParams p;
     memset(&p, 0, sizeof(p));
     if (encode(&p.tm_x, x, d_in, T, lora::kTileK, lora::kTileM) != CUDA_SUCCESS) return LORA_ECUDA;
+    if (encode(&p.tm_w, W, d_in, d_out, lora::kTileK, tile_n) != CUDA_SUCCESS) return LORA_ECUDA;
+    if (encode(&p.tm_u, scratch, rank, kURows, lora::kTileK, lora::kTileM) != CUDA_SUCCESS) return LORA_ECUDA;
+    p.tm_b = reinterpret_cast<const CUtensorMap*>(wdev + kOffBMaps);
+    p.tm_a = reinterpret_cast<const CUtensorMap*>(wdev + kOffAMaps);
+    p.shrink_tiles = reinterpret_cast<const Tile*>(wdev + kOffShrink);
+    p.fused_tiles = reinterpret_cast<const Tile*>(wdev + kOffFused);
     p.seg_off = reinterpret_cast<const int32_t*>(wdev + kOffSegOff);
     p.seg_id = reinterpret_cast<const int32_t*>(wdev + kOffSegId);
     p.scales = reinterpret_cast<const float*>(wdev + kOffScale);
-    p.n_seg = plan.n_m;
+    p.y = y;
+    p.u = scratch;
     p.status = status;
     p.wait_limit_ns = 4000000000ull;
+    p.n_seg = plan.n_m;
+    p.n_fused = plan.n_fused;
+    p.n_ntiles = cdiv(d_out, tile_n);
+    p.tile_n = tile_n;
+    p.shrink_n = shrink_n;
+    p.stages = stages_for(tile_n > shrink_n ? tile_n : shrink_n);
+    // keep the smaller operand L2-resident: walk row tiles first when X is smaller than W
+    p.m_fastest = ((long long)plan.n_fused * lora::kTileM < (long long)d_out) ? 1 : 0;
     p.k_main_blocks = cdiv(d_in, lora::kTileK);
+    p.k_lora_blocks = cdiv(rank, lora::kTileK);
+    p.d_out = d_out;
+    p.rank = rank;
+    // two launches ordered by the stream: the shrink units, then the fused units
     if (plan.n_shrink > 0) {
         GemmParams s = p;
-        s.tm_adapter = reinterpret_cast<const CUtensorMap*>(wdev + kOffAMaps);
-        s.tiles = reinterpret_cast<const Tile*>(wdev + kOffShrink);
-        s.n_tiles = plan.n_shrink;
-        s.n_ntiles = 1;
-        s.tile_n = shrink_n;
-        s.stages = stages_for(shrink_n);
-        s.m_fastest = 1;
-        s.out = scratch;  // U
-        s.ld_out = rank;
-        s.n_out = rank;
+        s.n_shrink = plan.n_shrink;
+        s.n_fused = 0;
         int grid = plan.n_shrink < ds->num_sms ? plan.n_shrink : ds->num_sms;
-        if (lora::launch_gemm(lora::kShrink, s, grid, stream) != cudaSuccess) return LORA_ECUDA;
+        if (lora::launch_gemm(s, grid, stream) != cudaSuccess) return LORA_ECUDA;
     }
-    GemmParams f = p;
-    if (encode(&f.tm_w, W, d_in, d_out, lora::kTileK, tile_n) != CUDA_SUCCESS) return LORA_ECUDA;
-    if (encode(&f.tm_u, scratch, rank, kURows, lora::kTileK, lora::kTileM) != CUDA_SUCCESS) return LORA_ECUDA;
-    f.tm_adapter = reinterpret_cast<const CUtensorMap*>(wdev + kOffBMaps);
-    f.tiles = reinterpret_cast<const Tile*>(wdev + kOffFused);
-    f.n_tiles = plan.n_fused;
-    f.n_ntiles = cdiv(d_out, tile_n);
-    f.tile_n = tile_n;
-    f.stages = stages_for(tile_n);
-    // keep the smaller operand L2-resident: walk row tiles first when X is smaller than W
-    f.m_fastest = ((long long)plan.n_fused * lora::kTileM < (long long)d_out) ? 1 : 0;
-    f.k_lora_blocks = cdiv(rank, lora::kTileK);
-    f.out = y;
-    f.ld_out = d_out;
-    f.n_out = d_out;
-    long long units = (long long)plan.n_fused * f.n_ntiles;
+    long long units = (long long)plan.n_fused * p.n_ntiles;
     int grid = units < ds->num_sms ? (int)units : ds->num_sms;
-    if (lora::launch_gemm(lora::kFused, f, grid, stream) != cudaSuccess) return LORA_ECUDA;
+    if (lora::launch_gemm(p, grid, stream) != cudaSuccess) return LORA_ECUDA;
     return LORA_OK;
 }

@@ -60,8 +60,12 @@ int plan_segments(const int32_t* seg_offsets, const int32_t* seg_ids, int n_seg,
     }
     if (cur.nrows) plan->fused.push_back(cur);
     // shrink tiles: adapter tiles, stably ordered by adapter id
-    for (const Tile& t : plan->fused)
-        if (t.adapter) plan->shrink.push_back(t);
+    for (size_t i = 0; i < plan->fused.size(); ++i)
+        if (plan->fused[i].adapter) {
+            Tile t = plan->fused[i];
+            t.fused_index = (int32_t)i;
+            plan->shrink.push_back(t);
+        }
     std::stable_sort(plan->shrink.begin(), plan->shrink.end(),
                      [](const Tile& a, const Tile& b) { return a.adapter < b.adapter; });
     // compact adapter slots in order of id (used by the device work list)

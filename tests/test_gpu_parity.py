@@ -147,6 +147,33 @@ def test_zero_b_adapter_rows_bit_identical_to_base(dev):
     assert torch.equal(y, y0)
 
 
+@pytest.mark.parametrize("name", ["sweep_qkv_multi", "mixed_near_ridge", "tiny"])
+def test_one_launch_equals_two_launches(dev, name):
+    # the in-kernel shrink->expand dependency gives exactly the two-launch result
+    from mixed_lora_projection_gb300 import _lib as L
+    w = WORKLOADS[name]
+    inp = make_inputs(w, dev)
+    with _ll(w) as ll:
+        y1 = run(ll, inp, w.seg_offsets, w.seg_ids).clone()
+        ll.set_option(L.OPT_TWO_LAUNCH, 1)
+        y2 = run(ll, inp, w.seg_offsets, w.seg_ids)
+        torch.cuda.synchronize()
+        assert ll.status() == 0
+    assert torch.equal(y1, y2)
+
+
+def test_repeated_calls_reuse_flags(dev):
+    # many calls in a row on one handle: the epoch-tagged ready flags never go stale
+    w = WORKLOADS["sweep_o_multi"]
+    inp = make_inputs(w, dev)
+    with _ll(w) as ll:
+        ys = [run(ll, inp, w.seg_offsets, w.seg_ids).clone() for _ in range(20)]
+        torch.cuda.synchronize()
+        assert ll.status() == 0
+    for y in ys[1:]:
+        assert torch.equal(y, ys[0])
+
+
 def test_deterministic(dev):
     w = WORKLOADS["sweep_down"]
     inp = make_inputs(w, dev)
