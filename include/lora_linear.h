@@ -158,7 +158,8 @@ enum {
     LORA_OPT_DEBUG_STALL = 3,   /* 1 = the load warp never issues: every wait runs out (tests only) */
     LORA_OPT_TIMING = 4,        /* 1 = record CUDA events around each kernel launch */
     LORA_OPT_RASTER = 5,        /* 0 = auto, 1 = row tiles fastest, 2 = column tiles fastest */
-    LORA_OPT_TWO_LAUNCH = 6     /* 1 = shrink and fused pass as two launches (default 0: one launch) */
+    LORA_OPT_TWO_LAUNCH = 6,    /* 1 = shrink and fused pass as two launches (default 0: one launch) */
+    LORA_OPT_CLUSTER = 7        /* 0 = auto, 1 = no clusters, 2 = CTA pairs share B tiles by TMA multicast */
 };
 
 /* lora_linear_set_option -- set one option above. Returns LORA_OK or LORA_EINVAL. */

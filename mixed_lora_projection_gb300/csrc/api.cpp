@@ -73,7 +73,8 @@ struct lora_linear {
     int max_fused = 0;
     EncodeTiledFn encode = nullptr;
     // options
-    int force_tile_n = 0, raster = 0, debug_stall = 0, timing = 0, two_launch = 0;
+    int force_tile_n = 0, raster = 0, debug_stall = 0, timing = 0, two_launch = 0, cluster = 0;
+    int max_clusters_cache[2][kMaxTileN / 16 + 1] = {};  // co-resident clusters by (size, B rows)
     unsigned long long wait_limit_ns = 4000000000ull;
     std::vector<TimingRec> trec;
     std::vector<cudaEvent_t> ev_pool;
@@ -147,15 +148,15 @@ int stages_for(int tile_n) {
 
 // Output-tile width: the per-SM critical path is (waves x (tile_n + fixed cost)); narrow
 // tiles only where the row count is small enough that the pass streams W from memory.
-int choose_tile_n(const lora_linear* h, int n_fused) {
+int choose_tile_n(const lora_linear* h, int n_fused, int n_groups, int slots) {
     if (h->force_tile_n) return h->force_tile_n;
     const bool small_batch = (long long)n_fused * kTileM <= 384;
     long long best_cost = -1;
     int best = kMaxTileN;
     for (int tn = kMaxTileN; tn >= 16; tn -= 16) {
         if (!small_batch && tn < 128) break;
-        long long units = (long long)n_fused * ceil_div(h->d_out, tn);
-        long long waves = (units + h->num_sms - 1) / h->num_sms;
+        long long units = (long long)n_groups * ceil_div(h->d_out, tn);
+        long long waves = (units + slots - 1) / slots;
         long long cost = waves * (tn + 16);
         if (best_cost < 0 || cost < best_cost) {
             best_cost = cost;
@@ -169,19 +170,71 @@ int choose_tile_n(const lora_linear* h, int n_fused) {
 // "wave"). Walking output-column tiles fastest re-reads all of W every wave; walking row
 // tiles fastest re-reads all of X. Pick the order whose per-wave DRAM bytes are smaller,
 // counting an operand as L2-resident across waves when it fits in ~96 MB of the 129 MB L2.
-int choose_m_fastest(const lora_linear* h, int n_tiles, int n_ntiles, int tile_n) {
+int choose_m_fastest(const lora_linear* h, int n_tiles, int n_ntiles, int tile_n, int rows_per_unit,
+                     int slots) {
     if (h->raster == 1) return 1;
     if (h->raster == 2) return 0;
     const double l2_budget = 96e6;
     const long long units = (long long)n_tiles * n_ntiles;
-    const long long g = std::min<long long>(units, h->num_sms);
-    const double xb = (double)kTileM * h->d_in * 2, wb = (double)tile_n * h->d_in * 2;
+    const long long g = std::min<long long>(units, slots);
+    const double xb = (double)rows_per_unit * h->d_in * 2, wb = (double)tile_n * h->d_in * 2;
     const double total_x = (double)n_tiles * xb, total_w = (double)n_ntiles * wb;
     const double rows_n = ceil_div(g, n_ntiles), cols_n = (double)std::min<long long>(g, n_ntiles);
     const double rows_m = (double)std::min<long long>(g, n_tiles), cols_m = ceil_div(g, n_tiles);
     const double cost_n = rows_n * xb + (total_w > l2_budget ? cols_n * wb : 0.0);
     const double cost_m = cols_m * wb + (total_x > l2_budget ? rows_m * xb : 0.0);
     return cost_m < cost_n ? 1 : 0;
+}
+
+// Launch shape of one call: cluster size, tile widths, pipeline depth, rasterisation.
+struct Shape {
+    int cs = 1, tile_n = 0, shrink_n = 0, n_ntiles = 0, stages = 0, m_fastest = 0;
+    std::vector<Tile> fused_groups, shrink_groups;  // cs tiles per group
+};
+
+// Groups of `cs` consecutive tiles that name the same adapter (they share the B tile);
+// a tile without a partner is padded with a copy of itself that has no rows. A padding
+// shrink tile gets flag slot -1 (it publishes nothing); a padding fused tile keeps its
+// partner's slot (it waits for the same U rows, then stores nothing).
+void make_groups(const std::vector<Tile>& tiles, int cs, bool shrink, std::vector<Tile>* out) {
+    out->clear();
+    for (size_t i = 0; i < tiles.size();) {
+        out->push_back(tiles[i]);
+        if (cs == 1) { ++i; continue; }
+        if (i + 1 < tiles.size() && tiles[i + 1].adapter == tiles[i].adapter) {
+            out->push_back(tiles[i + 1]);
+            i += 2;
+        } else {
+            Tile pad = tiles[i];
+            pad.nrows = 0;
+            if (shrink) pad.fused_index = -1;
+            out->push_back(pad);
+            i += 1;
+        }
+    }
+}
+
+int max_clusters(lora_linear* h, const GemmParams& p) {
+    const int b_rows = std::max(p.tile_n, p.shrink_n);
+    int& c = h->max_clusters_cache[p.cluster_size - 1][b_rows / 16];
+    if (c == 0) c = gemm_max_clusters(p);
+    return c;
+}
+
+Shape choose_shape(const lora_linear* h, const Plan& plan) {
+    Shape sh;
+    const int nf = (int)plan.fused.size();
+    sh.cs = h->cluster ? h->cluster : (nf >= 2 ? 2 : 1);
+    make_groups(plan.fused, sh.cs, false, &sh.fused_groups);
+    make_groups(plan.shrink, sh.cs, true, &sh.shrink_groups);
+    const int nfg = (int)sh.fused_groups.size() / sh.cs;
+    const int slots = h->num_sms / sh.cs;
+    sh.tile_n = choose_tile_n(h, nf, nfg, slots);
+    sh.shrink_n = ceil_div(h->rank, 16) * 16;
+    sh.n_ntiles = ceil_div(h->d_out, sh.tile_n);
+    sh.stages = stages_for(std::max(sh.tile_n, sh.shrink_n));
+    sh.m_fastest = choose_m_fastest(h, nfg, sh.n_ntiles, sh.tile_n, kTileM * sh.cs, slots);
+    return sh;
 }
 
 Slot* acquire_slot(lora_linear* h) {
@@ -292,7 +345,7 @@ int lora_linear_create(lora_linear** out, int d_in, int d_out, int rank, int max
     h->u_rows = ceil_div(max_tokens, kTileM) * kTileM + kTileM;
     h->max_fused = ceil_div(max_tokens, kTileM) + max_segments + 1;
     h->slot_bytes = align_up(2 * (size_t)max_segments * sizeof(CUtensorMap), 128) +
-                    2 * (size_t)h->max_fused * sizeof(Tile) +
+                    4 * (size_t)h->max_fused * sizeof(Tile) +
                     align_up(4 * (2 * (size_t)max_segments + 1), 16) +
                     align_up(4 * (size_t)max_segments, 16) + 256;
     if (cudaMalloc(&h->u_ws, (size_t)h->u_rows * rank * 2) != cudaSuccess ||
@@ -366,6 +419,10 @@ int lora_linear_set_option(lora_linear* h, int option, long long value) {
         case LORA_OPT_TWO_LAUNCH:
             h->two_launch = value ? 1 : 0;
             return LORA_OK;
+        case LORA_OPT_CLUSTER:
+            if (value < 0 || value > 2) return LORA_EINVAL;
+            h->cluster = (int)value;
+            return LORA_OK;
         default:
             return LORA_EINVAL;
     }
@@ -411,14 +468,20 @@ int lora_linear_describe(lora_linear* h, int T, const int32_t* seg_offsets,
     Plan plan;
     int rc = plan_segments(seg_offsets, seg_adapter_ids, n_seg, T, -1, &plan);
     if (rc != LORA_OK) return rc;
-    int nf = (int)plan.fused.size();
-    int tn = nf ? choose_tile_n(h, nf) : 0;
-    int units = nf ? nf * ceil_div(h->d_out, tn) : 0;
+    const int nf = (int)plan.fused.size();
+    int units = 0, tn = 0, st = 0, g = 0;
+    if (nf) {
+        Shape sh = choose_shape(h, plan);
+        units = (int)(sh.fused_groups.size() / sh.cs) * sh.n_ntiles + (int)(sh.shrink_groups.size() / sh.cs);
+        tn = sh.tile_n;
+        st = sh.stages;
+        g = std::min(units, h->num_sms / sh.cs) * sh.cs;
+    }
     if (tile_n) *tile_n = tn;
     if (n_tiles) *n_tiles = nf;
     if (n_units) *n_units = units;
-    if (grid) *grid = std::min(units + (int)plan.shrink.size(), h->num_sms);
-    if (stages) *stages = tn ? stages_for(std::max(tn, ceil_div(h->rank, 16) * 16)) : 0;
+    if (grid) *grid = g;
+    if (stages) *stages = st;
     if (has_shrink) *has_shrink = plan.shrink.empty() ? 0 : 1;
     return LORA_OK;
 }
@@ -445,22 +508,24 @@ int lora_linear_forward(lora_linear* h, const void* x, int T, const int32_t* seg
     for (Tile& t : plan.shrink) t.adapter = compact[t.adapter];
     for (int32_t& a : plan.seg_id) a = compact[a];
 
+    for (size_t i = 0; i < plan.fused.size(); ++i) plan.fused[i].fused_index = (int32_t)i;
+
     DeviceGuard guard(h->device);
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
-    const int nf = (int)plan.fused.size(), ns = (int)plan.shrink.size();
+    const Shape sh = choose_shape(h, plan);
+    const int cs = sh.cs, tile_n = sh.tile_n, shrink_n = sh.shrink_n;
+    const int nfg = (int)sh.fused_groups.size() / cs, nsg = (int)sh.shrink_groups.size() / cs;
+    const int nft = (int)sh.fused_groups.size(), nst = (int)sh.shrink_groups.size();
     const int n_m = (int)plan.seg_id.size();
-    const int tile_n = choose_tile_n(h, nf);
-    const int n_ntiles = ceil_div(h->d_out, tile_n);
-    const int shrink_n = ceil_div(h->rank, 16) * 16;
 
     Slot* slot = acquire_slot(h);
     if (!slot) return LORA_ECUDA;
-    // work list: [B_a maps][A_a maps][fused tiles][shrink tiles][seg_off][seg_id][scales]
+    // work list: [B_a maps][A_a maps][fused groups][shrink groups][seg_off][seg_id][scales]
     size_t off_bmaps = 0;
     size_t off_amaps = off_bmaps + (size_t)n_used * sizeof(CUtensorMap);
     size_t off_fused = align_up(off_amaps + (size_t)n_used * sizeof(CUtensorMap), 128);
-    size_t off_shrink = off_fused + (size_t)nf * sizeof(Tile);
-    size_t off_segoff = align_up(off_shrink + (size_t)ns * sizeof(Tile), 16);
+    size_t off_shrink = off_fused + (size_t)nft * sizeof(Tile);
+    size_t off_segoff = align_up(off_shrink + (size_t)nst * sizeof(Tile), 16);
     size_t off_segid = off_segoff + 4 * (size_t)(n_m + 1);
     size_t off_scale = align_up(off_segid + 4 * (size_t)n_m, 16);
     size_t used_bytes = off_scale + 4 * (size_t)n_used;
@@ -471,11 +536,11 @@ int lora_linear_forward(lora_linear* h, const void* x, int T, const int32_t* seg
     CUtensorMap* amaps = reinterpret_cast<CUtensorMap*>(hb + off_amaps);
     for (int k = 0; k < n_used; ++k) {
         int a = plan.used_adapters[k];
-        if (encode_2d(h, &bmaps[k], B[a], h->rank, h->d_out, kTileK, tile_n) != CUDA_SUCCESS) return LORA_ECUDA;
-        if (encode_2d(h, &amaps[k], A[a], h->d_in, h->rank, kTileK, shrink_n) != CUDA_SUCCESS) return LORA_ECUDA;
+        if (encode_2d(h, &bmaps[k], B[a], h->rank, h->d_out, kTileK, tile_n / cs) != CUDA_SUCCESS) return LORA_ECUDA;
+        if (encode_2d(h, &amaps[k], A[a], h->d_in, h->rank, kTileK, shrink_n / cs) != CUDA_SUCCESS) return LORA_ECUDA;
     }
-    memcpy(hb + off_fused, plan.fused.data(), (size_t)nf * sizeof(Tile));
-    memcpy(hb + off_shrink, plan.shrink.data(), (size_t)ns * sizeof(Tile));
+    memcpy(hb + off_fused, sh.fused_groups.data(), (size_t)nft * sizeof(Tile));
+    memcpy(hb + off_shrink, sh.shrink_groups.data(), (size_t)nst * sizeof(Tile));
     memcpy(hb + off_segoff, plan.seg_off.data(), 4 * (size_t)(n_m + 1));
     memcpy(hb + off_segid, plan.seg_id.data(), 4 * (size_t)n_m);
     float* sc = reinterpret_cast<float*>(hb + off_scale);
@@ -486,7 +551,7 @@ int lora_linear_forward(lora_linear* h, const void* x, int T, const int32_t* seg
     GemmParams p;
     memset(&p, 0, sizeof(p));
     if (encode_2d(h, &p.tm_x, x, h->d_in, T, kTileK, kTileM) != CUDA_SUCCESS) return LORA_ECUDA;
-    if (encode_2d(h, &p.tm_w, W, h->d_in, h->d_out, kTileK, tile_n) != CUDA_SUCCESS) return LORA_ECUDA;
+    if (encode_2d(h, &p.tm_w, W, h->d_in, h->d_out, kTileK, tile_n / cs) != CUDA_SUCCESS) return LORA_ECUDA;
     if (encode_2d(h, &p.tm_u, h->u_ws, h->rank, h->u_rows, kTileK, kTileM) != CUDA_SUCCESS) return LORA_ECUDA;
     p.tm_b = reinterpret_cast<const CUtensorMap*>(slot->dev + off_bmaps);
     p.tm_a = reinterpret_cast<const CUtensorMap*>(slot->dev + off_amaps);
@@ -500,18 +565,21 @@ int lora_linear_forward(lora_linear* h, const void* x, int T, const int32_t* seg
     p.status = h->status;
     p.wait_limit_ns = h->wait_limit_ns;
     p.n_seg = n_m;
-    p.n_shrink = ns;
-    p.n_fused = nf;
-    p.n_ntiles = n_ntiles;
+    p.n_shrink = nsg;
+    p.n_fused = nfg;
+    p.n_ntiles = sh.n_ntiles;
     p.tile_n = tile_n;
     p.shrink_n = shrink_n;
-    p.stages = stages_for(std::max(tile_n, shrink_n));
-    p.m_fastest = choose_m_fastest(h, nf, n_ntiles, tile_n);
+    p.stages = sh.stages;
+    p.m_fastest = sh.m_fastest;
     p.k_main_blocks = ceil_div(h->d_in, kTileK);
     p.k_lora_blocks = ceil_div(h->rank, kTileK);
     p.d_out = h->d_out;
     p.rank = h->rank;
+    p.cluster_size = cs;
     p.debug_stall = h->debug_stall;
+    const int slots = cs > 1 ? max_clusters(h, p) : h->num_sms;
+    if (slots < 1) return LORA_ECUDA;
 
     TimingRec rec{};
     if (h->timing) {
@@ -521,28 +589,28 @@ int lora_linear_forward(lora_linear* h, const void* x, int T, const int32_t* seg
         }
         cudaEventRecord(rec.ev[0], stream);
     }
-    const int fused_units = nf * n_ntiles;
-    if (h->two_launch && ns > 0) {
+    const int fused_units = nfg * sh.n_ntiles;
+    if (h->two_launch && nsg > 0) {
         // shrink, then fused base+expand ordered by the stream
         GemmParams s = p;
         s.n_fused = 0;
-        if (launch_gemm(s, std::min(ns, h->num_sms), stream) != cudaSuccess) return LORA_ECUDA;
+        if (launch_gemm(s, std::min(nsg, slots) * cs, stream) != cudaSuccess) return LORA_ECUDA;
         ++h->launches;
         rec.has_shrink = true;
         if (h->timing) cudaEventRecord(rec.ev[1], stream);
         GemmParams f = p;
         f.n_shrink = 0;
-        if (launch_gemm(f, std::min(fused_units, h->num_sms), stream) != cudaSuccess) return LORA_ECUDA;
+        if (launch_gemm(f, std::min(fused_units, slots) * cs, stream) != cudaSuccess) return LORA_ECUDA;
         ++h->launches;
     } else {
         // one launch: shrink units first, fused units wait on the per-tile ready flags
         if (h->timing) cudaEventRecord(rec.ev[1], stream);
-        if (ns > 0) {
+        if (nsg > 0) {
             h->epoch = h->epoch == 0x7fffffff ? 1 : h->epoch + 1;
             p.flags = h->flags;
             p.epoch = h->epoch;
         }
-        if (launch_gemm(p, std::min(ns + fused_units, h->num_sms), stream) != cudaSuccess) return LORA_ECUDA;
+        if (launch_gemm(p, std::min(nsg + fused_units, slots) * cs, stream) != cudaSuccess) return LORA_ECUDA;
         ++h->launches;
     }
     if (h->timing) {

@@ -34,6 +34,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <string.h>
 
 #include "lora_internal.h"
 
@@ -101,6 +102,25 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c_inner), "r"(c_outer)
         : "memory");
 }
+// Same, written to the same shared-memory offset of every CTA in `mask` (this cluster) and
+// completing bytes on the mbarrier at the same offset in each of them.
+__device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                                      int c_inner, int c_outer, uint16_t mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c_inner), "r"(c_outer), "h"(mask)
+        : "memory");
+}
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// All threads of every CTA in the cluster (also a CTA-wide barrier).
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -142,6 +162,13 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile(
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+}
+// Same, arriving on the mbarrier at the same offset in every CTA of `mask`.
+__device__ __forceinline__ void mma_commit_multicast(uint32_t bar, uint16_t mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(bar), "h"(mask)
         : "memory");
 }
 // 32 lanes x 32 bits x 16 columns: thread i of the warp gets 16 consecutive columns of lane
@@ -236,10 +263,11 @@ struct Unit {
     int nk;          // k-blocks of 64
 };
 
-__device__ __forceinline__ Unit decode_unit(const GemmParams& p, int u) {
+__device__ __forceinline__ Unit decode_unit(const GemmParams& p, int u, int rank) {
     Unit r;
+    const int cs = p.cluster_size;
     if (u < p.n_shrink) {
-        r.tile = p.shrink_tiles[u];
+        r.tile = p.shrink_tiles[u * cs + rank];
         r.shrink = 1;
         r.tile_index = r.tile.fused_index;
         r.n0 = 0;
@@ -249,9 +277,9 @@ __device__ __forceinline__ Unit decode_unit(const GemmParams& p, int u) {
         const int v = u - p.n_shrink;
         const int ti = p.m_fastest ? (v % p.n_fused) : (v / p.n_ntiles);
         const int nt = p.m_fastest ? (v / p.n_fused) : (v % p.n_ntiles);
-        r.tile = p.fused_tiles[ti];
+        r.tile = p.fused_tiles[ti * cs + rank];
         r.shrink = 0;
-        r.tile_index = ti;
+        r.tile_index = r.tile.fused_index;
         r.n0 = nt * p.tile_n;
         r.n = p.tile_n;
         r.nk = p.k_main_blocks + (r.tile.adapter ? p.k_lora_blocks : 0);
@@ -280,11 +308,16 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const int cs = p.cluster_size;
+    const int rank = cs > 1 ? (int)cluster_ctarank() : 0;
+    const int group = cs > 1 ? (int)(blockIdx.x / cs) : (int)blockIdx.x;  // cluster index
+    const int n_groups = (int)gridDim.x / cs;
+    const uint16_t mask = (uint16_t)((1u << cs) - 1u);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
             mbar_init(smem_addr(&full[s]), 1);
-            mbar_init(smem_addr(&empty[s]), 1);
+            mbar_init(smem_addr(&empty[s]), cs);  // both CTAs' MMAs must release a multicast stage
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(smem_addr(&tfull[a]), 1);
@@ -296,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
     }
     if (warp == 1) tmem_alloc(smem_addr(tmem_slot), 2 * kAccCols);
     tc_fence_before();
-    __syncthreads();
+    cluster_sync();  // barrier inits visible to the peer before any multicast or remote arrive
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
@@ -313,8 +346,8 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
             long long issued = 0;
             int acquired_a = -1, acquired_b = -1;  // adapters whose global tensor maps were acquired
             bool ok = true;
-            for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-                const Unit w = decode_unit(p, u);
+            for (int u = group; u < n_units && ok; u += n_groups) {
+                const Unit w = decode_unit(p, u, rank);
                 const int ad = w.tile.adapter;
                 const CUtensorMap* bmain = &p.tm_w;
                 if (w.shrink) {
@@ -325,6 +358,8 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
                     acquired_b = ad;
                 }
                 const uint32_t tx = kStageBytesA + (uint32_t)w.n * kTileK * 2;
+                const int half = w.n / cs;                      // B rows this CTA loads
+                const uint32_t b_off = (uint32_t)(rank * half) * (kTileK * 2);
                 for (int kb = 0; kb < w.nk; ++kb) {
                     if (kb == p.k_main_blocks && p.flags) {
                         // the expand reads U rows written by this tile's shrink unit
@@ -342,14 +377,14 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
                     mbar_arrive_expect_tx(fb, tx);
                     const uint32_t sa = smem_addr(a_ring + (size_t)stage * kStageBytesA);
                     const uint32_t sb = smem_addr(b_ring + (size_t)stage * b_stage_bytes);
-                    if (kb < p.k_main_blocks) {
-                        tma_load_2d(sa, &p.tm_x, fb, kb * kTileK, w.tile.row0);
-                        tma_load_2d(sb, bmain, fb, kb * kTileK, w.n0);
-                    } else {
-                        const int k = (kb - p.k_main_blocks) * kTileK;
-                        tma_load_2d(sa, &p.tm_u, fb, k, w.tile.row0);
-                        tma_load_2d(sb, &p.tm_b[ad - 1], fb, k, w.n0);
-                    }
+                    const bool main = kb < p.k_main_blocks;
+                    const int k = main ? kb * kTileK : (kb - p.k_main_blocks) * kTileK;
+                    tma_load_2d(sa, main ? &p.tm_x : &p.tm_u, fb, k, w.tile.row0);
+                    const CUtensorMap* bm = main ? bmain : &p.tm_b[ad - 1];
+                    if (cs > 1)
+                        tma_load_2d_multicast(sb + b_off, bm, fb, k, w.n0 + rank * half, mask);
+                    else
+                        tma_load_2d(sb, bm, fb, k, w.n0);
                     ++issued;
                     if (++stage == stages) { stage = 0; phase ^= 1; }
                 }
@@ -361,6 +396,14 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
                     wait_bounded(smem_addr(&full[j % stages]), (uint32_t)((j / stages) & 1), abort_flag,
                                  p.status, limit, false);
             }
+            if (cs > 1) {
+                // every MMA of the cluster has released this CTA's stages (so no remote
+                // arrive can still target this CTA's barriers when it exits)
+                long long first = issued > stages ? issued - stages : 0;
+                for (long long j = first; j < issued; ++j)
+                    wait_bounded(smem_addr(&empty[j % stages]), (uint32_t)((j / stages) & 1), abort_flag,
+                                 p.status, limit, false);
+            }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -369,8 +412,8 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
             uint32_t phase = 0;
             int it = 0;
             bool ok = true;
-            for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++it) {
-                const Unit w = decode_unit(p, u);
+            for (int u = group; u < n_units && ok; u += n_groups, ++it) {
+                const Unit w = decode_unit(p, u, rank);
                 const uint32_t idesc = instr_desc_bf16(kTileM, w.n);
                 const int acc = it & 1;
                 if (!wait_bounded(smem_addr(&tempty[acc]), ((it >> 1) & 1) ^ 1, abort_flag, p.status, limit, true)) {
@@ -393,7 +436,10 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
                         mma_bf16(d, ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), idesc,
                                  (kb > 0 || k > 0) ? 1u : 0u);
                     }
-                    mma_commit(smem_addr(&empty[stage]));
+                    if (cs > 1)
+                        mma_commit_multicast(smem_addr(&empty[stage]), mask);
+                    else
+                        mma_commit(smem_addr(&empty[stage]));
                     if (++stage == stages) { stage = 0; phase ^= 1; }
                 }
                 if (!ok) break;
@@ -409,8 +455,8 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
         const int r_local = q * 32 + lane;           // tile row held by this thread
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
         int it = 0;
-        for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++it) {
-            const Unit w = decode_unit(p, u);
+        for (int u = group; u < n_units; u += n_groups, ++it) {
+            const Unit w = decode_unit(p, u, rank);
             const int acc = it & 1;
             int ok = 1;
             if (lane == 0)
@@ -473,7 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
             }
             tc_fence_before();
             mbar_arrive(smem_addr(&tempty[acc]));
-            if (w.shrink && p.flags) {
+            if (w.shrink && p.flags && w.tile_index >= 0) {
                 // publish this tile's U rows to the fused units that wait for them
                 fence_proxy_async_global();
                 epilogue_bar_sync();
@@ -487,7 +533,7 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
 
     __syncwarp();
     tc_fence_before();
-    __syncthreads();
+    cluster_sync();  // the peer no longer writes into this CTA's shared memory
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem_base, 2 * kAccCols);
@@ -506,11 +552,39 @@ cudaError_t gemm_prepare_device() {
                                 kSmemBudget + 2048);
 }
 
-cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t stream) {
+static void launch_config(const GemmParams& p, int grid, cudaStream_t stream, cudaLaunchConfig_t* cfg,
+                          cudaLaunchAttribute* attr) {
     const int b_rows = p.tile_n > p.shrink_n ? p.tile_n : p.shrink_n;
-    const size_t smem = gemm_smem_bytes(b_rows, p.stages);
-    dev::lora_gemm_kernel<<<grid, kThreads, smem, stream>>>(p);
-    return cudaGetLastError();
+    memset(cfg, 0, sizeof(*cfg));
+    cfg->gridDim = dim3(grid, 1, 1);
+    cfg->blockDim = dim3(kThreads, 1, 1);
+    cfg->dynamicSmemBytes = gemm_smem_bytes(b_rows, p.stages);
+    cfg->stream = stream;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = p.cluster_size;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg->attrs = attr;
+    cfg->numAttrs = 1;
+}
+
+cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[1];
+    launch_config(p, grid, stream, &cfg, attr);
+    return cudaLaunchKernelEx(&cfg, dev::lora_gemm_kernel, p);
+}
+
+int gemm_max_clusters(const GemmParams& p) {
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[1];
+    launch_config(p, p.cluster_size, nullptr, &cfg, attr);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, dev::lora_gemm_kernel, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n;
 }
 
 }  // namespace lora

@@ -21,13 +21,17 @@ constexpr int kEpilogueThreads = 128;
 
 struct Tile {                        // one planner tile, as uploaded to the device
     int32_t row0, nrows, adapter;    // adapter: compact slot (1-based), 0 = none
-    int32_t fused_index;             // shrink tiles: index of the same rows among the fused tiles
+    int32_t fused_index;             // ready-flag slot: index of these rows among the fused tiles
+                                     // (-1 on a shrink tile that only pads a cluster group)
 };
 
 // Parameters of one launch of the tile GEMM. Passed by value as a __grid_constant__.
-// Work units: [0, n_shrink) are shrink units (U rows of one adapter tile, N = shrink_n),
-// then n_fused x n_ntiles fused units (a 128 x tile_n block of Y: base K-loop over d_in,
-// then, for adapter tiles, the expand K-loop over the rank into the same accumulator).
+// Work units: [0, n_shrink) are shrink units (U rows of adapter tiles, N = shrink_n), then
+// n_fused x n_ntiles fused units (128 x tile_n blocks of Y: base K-loop over d_in, then,
+// for adapter tiles, the expand K-loop over the rank into the same accumulator). With
+// cluster_size 2 a unit is a group of two row tiles (tiles 2g and 2g+1 of the arrays, one
+// per CTA of the cluster) that share the same B operand tile; each CTA loads half of that
+// tile and multicasts it to both. Groups are padded with tiles of nrows 0.
 // When `flags` is set, a fused unit's expand waits until flags[tile] == epoch, which the
 // shrink unit of that tile publishes after its U rows are stored (single-launch mode).
 struct GemmParams {
@@ -48,8 +52,8 @@ struct GemmParams {
     unsigned long long wait_limit_ns;
     int epoch;
     int n_seg;
-    int n_shrink;
-    int n_fused;
+    int n_shrink;                    // shrink groups (tiles = cluster_size x groups)
+    int n_fused;                     // fused row groups
     int n_ntiles;                    // output-column tiles of the fused units
     int tile_n;                      // fused output-tile width (multiple of 16, <= 256)
     int shrink_n;                    // shrink output-tile width = rank rounded up to 16
@@ -59,6 +63,7 @@ struct GemmParams {
     int k_lora_blocks;               // ceil(rank / 64)
     int d_out;
     int rank;
+    int cluster_size;                // 1, or 2 (TMA multicast of the B operand across the pair)
     int debug_stall;
 };
 
@@ -77,5 +82,6 @@ int plan_segments(const int32_t* seg_offsets, const int32_t* seg_ids, int n_seg,
 size_t gemm_smem_bytes(int b_tile_rows, int stages);
 cudaError_t gemm_prepare_device();           // sets the opt-in smem limit on the current device
 cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t stream);
+int gemm_max_clusters(const GemmParams& p);  // co-resident clusters of this launch shape
 
 }  // namespace lora

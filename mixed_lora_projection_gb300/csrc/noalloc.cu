@@ -243,6 +243,7 @@ extern "C" int lora_linear_forward_noalloc(const void* x, int T, const int32_t* 
     p.k_lora_blocks = cdiv(rank, lora::kTileK);
     p.d_out = d_out;
     p.rank = rank;
+    p.cluster_size = 1;
     // two launches ordered by the stream: the shrink units, then the fused units
     if (plan.n_shrink > 0) {
         GemmParams s = p;

@@ -162,6 +162,22 @@ def test_one_launch_equals_two_launches(dev, name):
     assert torch.equal(y1, y2)
 
 
+@pytest.mark.parametrize("name", ["tiny", "sweep_qkv_multi", "mixed_near_ridge", "prefill_16k"])
+def test_cta_pairs_equal_single_ctas(dev, name):
+    # CTA pairs that share the B tile by TMA multicast compute exactly what single CTAs do
+    from mixed_lora_projection_gb300 import _lib as L
+    w = WORKLOADS[name]
+    inp = make_inputs(w, dev)
+    with _ll(w) as ll:
+        ll.set_option(L.OPT_CLUSTER, 2)
+        y2 = run(ll, inp, w.seg_offsets, w.seg_ids).clone()
+        ll.set_option(L.OPT_CLUSTER, 1)
+        y1 = run(ll, inp, w.seg_offsets, w.seg_ids)
+        torch.cuda.synchronize()
+        assert ll.status() == 0
+    assert torch.equal(y1, y2)
+
+
 def test_repeated_calls_reuse_flags(dev):
     # many calls in a row on one handle: the epoch-tagged ready flags never go stale
     w = WORKLOADS["sweep_o_multi"]
