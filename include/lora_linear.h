@@ -157,9 +157,14 @@ enum {
     LORA_OPT_WAIT_LIMIT_US = 2, /* bound of every in-kernel wait, microseconds (default 4,000,000) */
     LORA_OPT_DEBUG_STALL = 3,   /* 1 = the load warp never issues: every wait runs out (tests only) */
     LORA_OPT_TIMING = 4,        /* 1 = record CUDA events around each kernel launch */
-    LORA_OPT_RASTER = 5,        /* 0 = auto, 1 = row tiles fastest, 2 = column tiles fastest */
+    LORA_OPT_RASTER = 5,        /* 0 = auto, 1 = row tiles fastest, 2 = column tiles fastest,
+                                   3 = groups of LORA_OPT_RASTER_GROUP column tiles, row tiles fastest */
     LORA_OPT_TWO_LAUNCH = 6,    /* 1 = shrink and fused pass as two launches (default 0: one launch) */
-    LORA_OPT_CLUSTER = 7        /* 0 = auto, 1 = no clusters, 2 = CTA pairs share B tiles by TMA multicast */
+    LORA_OPT_CLUSTER = 7,       /* 0 = auto, 1 = one CTA per tile, 2 = SM pairs run M = 256 MMAs (tcgen05 cta_group::2) */
+    LORA_OPT_RASTER_GROUP = 8,  /* column tiles per group for LORA_OPT_RASTER = 3 (default 4) */
+    LORA_OPT_L2_HINTS = 9,      /* L2 eviction priorities, bit mask: 1 = weights evict_last, 2 = activations
+                                   evict_first (with 8: evict_normal), 4 = output stores evict_first */
+    LORA_OPT_TILE_K = 10        /* K per pipeline stage: 0 = auto, 32 or 64 */
 };
 
 /* lora_linear_set_option -- set one option above. Returns LORA_OK or LORA_EINVAL. */

@@ -74,6 +74,7 @@ struct lora_linear {
     EncodeTiledFn encode = nullptr;
     // options
     int force_tile_n = 0, raster = 0, debug_stall = 0, timing = 0, two_launch = 0, cluster = 0;
+    int raster_group = 4, l2_hints = 0, tile_k = 0;
     int max_clusters_cache[2][kMaxTileN / 16 + 1] = {};  // co-resident clusters by (size, B rows)
     unsigned long long wait_limit_ns = 4000000000ull;
     std::vector<TimingRec> trec;
@@ -131,19 +132,22 @@ cudaEvent_t take_event(lora_linear* h) {
 
 CUresult encode_2d(lora_linear* h, CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer,
                    uint32_t box_inner, uint32_t box_outer) {
+    // the swizzle is as wide as the box rows: 64 bf16 -> 128 bytes, 32 bf16 -> 64 bytes
     cuuint64_t dims[2] = {inner, outer};
     cuuint64_t strides[1] = {inner * 2};
     cuuint32_t box[2] = {box_inner, box_outer};
     cuuint32_t estr[2] = {1, 1};
     return h->encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
-                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     box_inner == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
-int stages_for(int tile_n) {
-    int per = kStageBytesA + tile_n * kTileK * 2;
-    int s = (kSmemBudget - 1024 - 256) / per;
-    return std::max(2, std::min(kMaxStages, s));
+// Deepest ring that fits the opt-in shared memory, for `b_rows` B rows per CTA.
+int stages_for(int b_rows, int bk) {
+    int s = kMaxStages;
+    while (s > 2 && gemm_smem_bytes(b_rows, s, bk) > (size_t)kSmemLimit) --s;
+    return s;
 }
 
 // Output-tile width: the per-SM critical path is (waves x (tile_n + fixed cost)); narrow
@@ -174,6 +178,7 @@ int choose_m_fastest(const lora_linear* h, int n_tiles, int n_ntiles, int tile_n
                      int slots) {
     if (h->raster == 1) return 1;
     if (h->raster == 2) return 0;
+    if (h->raster == 3) return 2;
     const double l2_budget = 96e6;
     const long long units = (long long)n_tiles * n_ntiles;
     const long long g = std::min<long long>(units, slots);
@@ -188,7 +193,7 @@ int choose_m_fastest(const lora_linear* h, int n_tiles, int n_ntiles, int tile_n
 
 // Launch shape of one call: cluster size, tile widths, pipeline depth, rasterisation.
 struct Shape {
-    int cs = 1, tile_n = 0, shrink_n = 0, n_ntiles = 0, stages = 0, m_fastest = 0;
+    int cs = 1, tile_n = 0, shrink_n = 0, n_ntiles = 0, stages = 0, m_fastest = 0, bk = 64;
     std::vector<Tile> fused_groups, shrink_groups;  // cs tiles per group
 };
 
@@ -232,7 +237,8 @@ Shape choose_shape(const lora_linear* h, const Plan& plan) {
     sh.tile_n = choose_tile_n(h, nf, nfg, slots);
     sh.shrink_n = ceil_div(h->rank, 16) * 16;
     sh.n_ntiles = ceil_div(h->d_out, sh.tile_n);
-    sh.stages = stages_for(std::max(sh.tile_n, sh.shrink_n));
+    sh.bk = h->tile_k ? h->tile_k : 64;
+    sh.stages = stages_for(std::max(sh.tile_n, sh.shrink_n) / sh.cs, sh.bk);
     sh.m_fastest = choose_m_fastest(h, nfg, sh.n_ntiles, sh.tile_n, kTileM * sh.cs, slots);
     return sh;
 }
@@ -413,8 +419,20 @@ int lora_linear_set_option(lora_linear* h, int option, long long value) {
             return LORA_OK;
         }
         case LORA_OPT_RASTER:
-            if (value < 0 || value > 2) return LORA_EINVAL;
+            if (value < 0 || value > 3) return LORA_EINVAL;
             h->raster = (int)value;
+            return LORA_OK;
+        case LORA_OPT_RASTER_GROUP:
+            if (value < 1 || value > 4096) return LORA_EINVAL;
+            h->raster_group = (int)value;
+            return LORA_OK;
+        case LORA_OPT_TILE_K:
+            if (value != 0 && value != 32 && value != 64) return LORA_EINVAL;
+            h->tile_k = (int)value;
+            return LORA_OK;
+        case LORA_OPT_L2_HINTS:
+            if (value < 0 || value > 15) return LORA_EINVAL;
+            h->l2_hints = (int)value;
             return LORA_OK;
         case LORA_OPT_TWO_LAUNCH:
             h->two_launch = value ? 1 : 0;
@@ -475,7 +493,19 @@ int lora_linear_describe(lora_linear* h, int T, const int32_t* seg_offsets,
         units = (int)(sh.fused_groups.size() / sh.cs) * sh.n_ntiles + (int)(sh.shrink_groups.size() / sh.cs);
         tn = sh.tile_n;
         st = sh.stages;
-        g = std::min(units, h->num_sms / sh.cs) * sh.cs;
+        int slots = h->num_sms;
+        if (sh.cs > 1) {
+            GemmParams q;
+            memset(&q, 0, sizeof(q));
+            q.tile_n = sh.tile_n;
+            q.shrink_n = sh.shrink_n;
+            q.stages = sh.stages;
+            q.cluster_size = sh.cs;
+            q.bk = sh.bk;
+            DeviceGuard guard(h->device);
+            slots = max_clusters(h, q);
+        }
+        g = std::min(units, slots) * sh.cs;
     }
     if (tile_n) *tile_n = tn;
     if (n_tiles) *n_tiles = nf;
@@ -513,7 +543,7 @@ int lora_linear_forward(lora_linear* h, const void* x, int T, const int32_t* seg
     DeviceGuard guard(h->device);
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
     const Shape sh = choose_shape(h, plan);
-    const int cs = sh.cs, tile_n = sh.tile_n, shrink_n = sh.shrink_n;
+    const int cs = sh.cs, tile_n = sh.tile_n, shrink_n = sh.shrink_n, bk = sh.bk;
     const int nfg = (int)sh.fused_groups.size() / cs, nsg = (int)sh.shrink_groups.size() / cs;
     const int nft = (int)sh.fused_groups.size(), nst = (int)sh.shrink_groups.size();
     const int n_m = (int)plan.seg_id.size();
@@ -536,8 +566,8 @@ int lora_linear_forward(lora_linear* h, const void* x, int T, const int32_t* seg
     CUtensorMap* amaps = reinterpret_cast<CUtensorMap*>(hb + off_amaps);
     for (int k = 0; k < n_used; ++k) {
         int a = plan.used_adapters[k];
-        if (encode_2d(h, &bmaps[k], B[a], h->rank, h->d_out, kTileK, tile_n / cs) != CUDA_SUCCESS) return LORA_ECUDA;
-        if (encode_2d(h, &amaps[k], A[a], h->d_in, h->rank, kTileK, shrink_n / cs) != CUDA_SUCCESS) return LORA_ECUDA;
+        if (encode_2d(h, &bmaps[k], B[a], h->rank, h->d_out, bk, tile_n / cs) != CUDA_SUCCESS) return LORA_ECUDA;
+        if (encode_2d(h, &amaps[k], A[a], h->d_in, h->rank, bk, shrink_n / cs) != CUDA_SUCCESS) return LORA_ECUDA;
     }
     memcpy(hb + off_fused, sh.fused_groups.data(), (size_t)nft * sizeof(Tile));
     memcpy(hb + off_shrink, sh.shrink_groups.data(), (size_t)nst * sizeof(Tile));
@@ -550,9 +580,9 @@ int lora_linear_forward(lora_linear* h, const void* x, int T, const int32_t* seg
 
     GemmParams p;
     memset(&p, 0, sizeof(p));
-    if (encode_2d(h, &p.tm_x, x, h->d_in, T, kTileK, kTileM) != CUDA_SUCCESS) return LORA_ECUDA;
-    if (encode_2d(h, &p.tm_w, W, h->d_in, h->d_out, kTileK, tile_n / cs) != CUDA_SUCCESS) return LORA_ECUDA;
-    if (encode_2d(h, &p.tm_u, h->u_ws, h->rank, h->u_rows, kTileK, kTileM) != CUDA_SUCCESS) return LORA_ECUDA;
+    if (encode_2d(h, &p.tm_x, x, h->d_in, T, bk, kTileM) != CUDA_SUCCESS) return LORA_ECUDA;
+    if (encode_2d(h, &p.tm_w, W, h->d_in, h->d_out, bk, tile_n / cs) != CUDA_SUCCESS) return LORA_ECUDA;
+    if (encode_2d(h, &p.tm_u, h->u_ws, h->rank, h->u_rows, bk, kTileM) != CUDA_SUCCESS) return LORA_ECUDA;
     p.tm_b = reinterpret_cast<const CUtensorMap*>(slot->dev + off_bmaps);
     p.tm_a = reinterpret_cast<const CUtensorMap*>(slot->dev + off_amaps);
     p.shrink_tiles = reinterpret_cast<const Tile*>(slot->dev + off_shrink);
@@ -572,8 +602,11 @@ int lora_linear_forward(lora_linear* h, const void* x, int T, const int32_t* seg
     p.shrink_n = shrink_n;
     p.stages = sh.stages;
     p.m_fastest = sh.m_fastest;
-    p.k_main_blocks = ceil_div(h->d_in, kTileK);
-    p.k_lora_blocks = ceil_div(h->rank, kTileK);
+    p.raster_group = h->raster_group;
+    p.l2_hints = h->l2_hints;
+    p.k_main_blocks = ceil_div(h->d_in, bk);
+    p.k_lora_blocks = ceil_div(h->rank, bk);
+    p.bk = bk;
     p.d_out = h->d_out;
     p.rank = h->rank;
     p.cluster_size = cs;

@@ -18,14 +18,24 @@
 // CTA reaches without waiting, so the dependency cannot cycle.
 //
 // Per CTA (one per SM, persistent over the work units):
-//   warp 0      one thread issues TMA loads (cp.async.bulk.tensor, 128-byte swizzle) of a
-//               128x64 A tile and a tile_n x 64 B tile per stage into a shared-memory ring;
+//   warp 0      one thread issues TMA loads (cp.async.bulk.tensor, swizzle as wide as the
+//               K-step) of the A tile (128 rows) and the B tile per stage into a ring;
 //   warp 1      owns 512 TMEM columns (two 128x256 fp32 accumulators); one thread issues
-//               tcgen05.mma kind::f16 (M=128, N=tile_n, K=16) and commits each stage back
-//               to the producer and each finished accumulator to the epilogue;
+//               tcgen05.mma kind::f16 and commits each stage back to the producer and each
+//               finished accumulator to the epilogue;
 //   warps 2..5  epilogue: tcgen05.ld the accumulator (warp w reads TMEM lanes 32*(w%4)..),
 //               round to bf16 and store the tile's rows with 16-byte stores.
 // Two accumulators let the epilogue of one tile overlap the mainloop of the next.
+//
+// CTA group 2 (CG = 2): a cluster of two CTAs on an SM pair computes a 256-row unit (two
+// row tiles that share the B tile) with tcgen05.mma.cta_group::2 (M = 256). Each CTA loads
+// its own 128 A rows and one half of the B tile's rows; the even CTA issues the MMAs, which
+// read the peer's half of B from the peer's shared memory, and each CTA's TMEM receives its
+// own 128 rows. Each SM thus lands 32 KB per 64-wide K-step instead of 48 KB, which is what
+// bounds the single-CTA form (the rate at which an SM's shared memory can be filled).
+// Barriers: the even CTA's full barrier counts both CTAs' bytes; its MMA commits release
+// both CTAs' stages and accumulators (multicast); both epilogues release the even CTA's
+// accumulator barrier.
 //
 // Every mbarrier wait is bounded by a wall-clock limit; a wait that runs out sets bit 0
 // of the status word and a CTA-wide abort flag, and all roles leave their loops, wait
@@ -51,6 +61,23 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
     return t;
 }
 
+// ---------------------------------------------------------------- cluster
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// All threads of every CTA in the cluster (also a CTA-wide barrier).
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Shared::cluster address of the same shared variable in CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t local, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+    return r;
+}
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
@@ -61,6 +88,10 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
 }
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+// Arrive on a barrier given by its shared::cluster address (this CTA's or the peer's).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
 }
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
@@ -94,32 +125,24 @@ __device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatil
 }
 
 // ---------------------------------------------------------------- TMA
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                            int c_inner, int c_outer) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c_inner), "r"(c_outer)
-        : "memory");
-}
-// Same, written to the same shared-memory offset of every CTA in `mask` (this cluster) and
-// completing bytes on the mbarrier at the same offset in each of them.
-__device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                                      int c_inner, int c_outer, uint16_t mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c_inner), "r"(c_outer), "h"(mask)
-        : "memory");
-}
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-// All threads of every CTA in the cluster (also a CTA-wide barrier).
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+// 2-D tiled load into this CTA's shared memory, completing bytes on `bar` (a barrier of
+// this CTA; with CG = 2 it may be the even CTA's barrier, as a shared::cluster address).
+template <int CG>
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c_inner,
+                                            int c_outer) {
+    if (CG == 1) {
+        asm volatile(
+            "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+            " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+            "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c_inner), "r"(c_outer)
+            : "memory");
+    } else {
+        asm volatile(
+            "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.cta_group::2"
+            " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+            "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c_inner), "r"(c_outer)
+            : "memory");
+    }
 }
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
@@ -138,42 +161,73 @@ __device__ __forceinline__ void tc_fence_before() {
 __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
+// With CG = 2 one warp of each CTA of the pair executes these together.
+template <int CG>
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
-                 "r"(ncols)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    if (CG == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+                     "r"(ncols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    } else {
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+                     "r"(ncols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    }
 }
+template <int CG>
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-                 : "memory");
+    if (CG == 1)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+    else
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
 // D[tmem] (+)= A[smem] * B[smem]^T, bf16 inputs, fp32 accumulate; one thread issues.
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                         uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
+template <int CG>
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate) {
+    if (CG == 1)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+            "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+            "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+            : "memory");
 }
-// Arrive once on `bar` when every tcgen05 op this thread issued so far has completed.
+// Arrive once on `bar` (CG = 1: this CTA's; CG = 2: the barrier at that offset in both CTAs
+// of the pair) when every tcgen05 op this thread issued so far has completed.
+template <int CG>
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-        : "memory");
+    if (CG == 1)
+        asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                     : "memory");
+    else
+        asm volatile(
+            "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+            " [%0], %1;" ::"r"(bar), "h"((uint16_t)3)
+            : "memory");
 }
-// Same, arriving on the mbarrier at the same offset in every CTA of `mask`.
-__device__ __forceinline__ void mma_commit_multicast(uint32_t bar, uint16_t mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-        " [%0], %1;" ::"r"(bar), "h"(mask)
-        : "memory");
+// Same, arriving only on this CTA's barrier.
+template <int CG>
+__device__ __forceinline__ void mma_commit_local(uint32_t bar) {
+    if (CG == 1)
+        asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                     : "memory");
+    else
+        asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                     : "memory");
 }
 // 32 lanes x 32 bits x 16 columns: thread i of the warp gets 16 consecutive columns of lane
 // (taddr.lane + i).
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* v) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32"
         " {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
@@ -186,17 +240,20 @@ __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-// Shared-memory matrix descriptor: K-major tile written by TMA with 128-byte swizzle.
-// Rows are 128 bytes (64 bf16), groups of 8 rows are 1024 bytes apart (stride byte
-// offset); the leading byte offset is unused for this layout; version 1; layout 2 =
-// 128-byte swizzle. The tile base must be 1024-byte aligned.
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
+// Shared-memory matrix descriptor of a K-major tile written by TMA with a swizzle as wide
+// as its rows: BK = 64 -> 128-byte rows and 128-byte swizzle (layout 2), BK = 32 ->
+// 64-byte rows and 64-byte swizzle (layout 4). Groups of 8 rows are 8 x row bytes apart
+// (stride byte offset); the leading byte offset is unused for these layouts; version 1.
+// The tile base must be aligned to the swizzle pattern (1024 bytes here).
+template <int BK>
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr) {
+    static_assert(BK == 64 || BK == 32, "K per stage must be 32 or 64");
     uint64_t d = 0;
     d |= (uint64_t)((addr & 0x3FFFFu) >> 4);
     d |= (uint64_t)1 << 16;
-    d |= (uint64_t)(1024 >> 4) << 32;
+    d |= (uint64_t)((8 * BK * 2) >> 4) << 32;
     d |= (uint64_t)1 << 46;
-    d |= (uint64_t)2 << 61;
+    d |= (uint64_t)(BK == 64 ? 2 : 4) << 61;
     return d;
 }
 // Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major, shape M x N.
@@ -257,10 +314,10 @@ __device__ __noinline__ bool wait_flag(const int* flag, int epoch, volatile int*
 struct Unit {
     Tile tile;
     int shrink;      // 1: shrink unit (U rows), 0: fused unit (Y block)
-    int tile_index;  // fused tile index (flag slot)
+    int tile_index;  // ready-flag slot
     int n0;          // first output column
     int n;           // MMA N of this unit
-    int nk;          // k-blocks of 64
+    int nk;          // k-blocks
 };
 
 __device__ __forceinline__ Unit decode_unit(const GemmParams& p, int u, int rank) {
@@ -275,8 +332,18 @@ __device__ __forceinline__ Unit decode_unit(const GemmParams& p, int u, int rank
         r.nk = p.k_main_blocks;
     } else {
         const int v = u - p.n_shrink;
-        const int ti = p.m_fastest ? (v % p.n_fused) : (v / p.n_ntiles);
-        const int nt = p.m_fastest ? (v / p.n_fused) : (v % p.n_ntiles);
+        int ti, nt;
+        if (p.m_fastest == 2) {
+            // column-tile groups of raster_group: all row tiles of a group, then the next group
+            const int per = p.n_fused * p.raster_group;
+            const int g = v / per, rr = v % per;
+            const int gw = min(p.raster_group, p.n_ntiles - g * p.raster_group);
+            ti = rr / gw;
+            nt = g * p.raster_group + rr % gw;
+        } else {
+            ti = p.m_fastest ? (v % p.n_fused) : (v / p.n_ntiles);
+            nt = p.m_fastest ? (v / p.n_fused) : (v % p.n_ntiles);
+        }
         r.tile = p.fused_tiles[ti * cs + rank];
         r.shrink = 0;
         r.tile_index = r.tile.fused_index;
@@ -287,16 +354,18 @@ __device__ __forceinline__ Unit decode_unit(const GemmParams& p, int u, int rank
     return r;
 }
 
+template <int BK, int CG>
 __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_constant__ GemmParams p) {
+    constexpr uint32_t kStageA = kTileM * BK * 2;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // carve: rings (1024-aligned), then barriers, then the TMEM slot and the abort flag
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
     const int stages = p.stages;
-    const int b_rows = p.tile_n > p.shrink_n ? p.tile_n : p.shrink_n;  // B stage sized for either kind
-    const uint32_t b_stage_bytes = (uint32_t)b_rows * kTileK * 2;
+    const int b_rows = (p.tile_n > p.shrink_n ? p.tile_n : p.shrink_n) / CG;  // this CTA's B rows
+    const uint32_t b_stage_bytes = (uint32_t)b_rows * BK * 2;
     uint8_t* a_ring = base;
-    uint8_t* b_ring = a_ring + (size_t)stages * kStageBytesA;
+    uint8_t* b_ring = a_ring + (size_t)stages * kStageA;
     uint64_t* bars = reinterpret_cast<uint64_t*>(b_ring + (size_t)stages * b_stage_bytes);
     uint64_t* full = bars;
     uint64_t* empty = full + stages;
@@ -308,28 +377,28 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int cs = p.cluster_size;
-    const int rank = cs > 1 ? (int)cluster_ctarank() : 0;
-    const int group = cs > 1 ? (int)(blockIdx.x / cs) : (int)blockIdx.x;  // cluster index
-    const int n_groups = (int)gridDim.x / cs;
-    const uint16_t mask = (uint16_t)((1u << cs) - 1u);
+    const int rank = CG > 1 ? (int)cluster_ctarank() : 0;
+    const bool leader = rank == 0;                 // issues the MMAs of the pair
+    const int group = (int)blockIdx.x / CG;        // cluster index
+    const int n_groups = (int)gridDim.x / CG;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
             mbar_init(smem_addr(&full[s]), 1);
-            mbar_init(smem_addr(&empty[s]), cs);  // both CTAs' MMAs must release a multicast stage
+            mbar_init(smem_addr(&empty[s]), 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(smem_addr(&tfull[a]), 1);
-            mbar_init(smem_addr(&tempty[a]), kEpilogueThreads);
+            mbar_init(smem_addr(&tempty[a]), CG * kEpilogueThreads);  // both CTAs' epilogues
         }
         mbar_init(smem_addr(drain), 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == 1) tmem_alloc(smem_addr(tmem_slot), 2 * kAccCols);
+    if (warp == 1) tmem_alloc<CG>(smem_addr(tmem_slot), 2 * kAccCols);
     tc_fence_before();
-    cluster_sync();  // barrier inits visible to the peer before any multicast or remote arrive
+    if (CG > 1) cluster_sync();  // barrier inits visible to the peer before any remote arrive
+    else __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
@@ -357,9 +426,9 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
                     tensormap_acquire(&p.tm_b[ad - 1]);
                     acquired_b = ad;
                 }
-                const uint32_t tx = kStageBytesA + (uint32_t)w.n * kTileK * 2;
-                const int half = w.n / cs;                      // B rows this CTA loads
-                const uint32_t b_off = (uint32_t)(rank * half) * (kTileK * 2);
+                const int half = w.n / CG;                       // B rows this CTA loads
+                // bytes the (even CTA's) full barrier receives per stage, from the whole group
+                const uint32_t tx = CG * (kStageA + (uint32_t)half * BK * 2);
                 for (int kb = 0; kb < w.nk; ++kb) {
                     if (kb == p.k_main_blocks && p.flags) {
                         // the expand reads U rows written by this tile's shrink unit
@@ -373,32 +442,29 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
                         ok = false;
                         break;
                     }
-                    const uint32_t fb = smem_addr(&full[stage]);
-                    mbar_arrive_expect_tx(fb, tx);
-                    const uint32_t sa = smem_addr(a_ring + (size_t)stage * kStageBytesA);
+                    const uint32_t fb_local = smem_addr(&full[stage]);
+                    if (leader) mbar_arrive_expect_tx(fb_local, tx);
+                    const uint32_t fb = CG > 1 ? map_to_rank(fb_local, 0) : fb_local;
+                    const uint32_t sa = smem_addr(a_ring + (size_t)stage * kStageA);
                     const uint32_t sb = smem_addr(b_ring + (size_t)stage * b_stage_bytes);
                     const bool main = kb < p.k_main_blocks;
-                    const int k = main ? kb * kTileK : (kb - p.k_main_blocks) * kTileK;
-                    tma_load_2d(sa, main ? &p.tm_x : &p.tm_u, fb, k, w.tile.row0);
-                    const CUtensorMap* bm = main ? bmain : &p.tm_b[ad - 1];
-                    if (cs > 1)
-                        tma_load_2d_multicast(sb + b_off, bm, fb, k, w.n0 + rank * half, mask);
-                    else
-                        tma_load_2d(sb, bm, fb, k, w.n0);
+                    const int k = main ? kb * BK : (kb - p.k_main_blocks) * BK;
+                    tma_load_2d<CG>(sa, main ? &p.tm_x : &p.tm_u, fb, k, w.tile.row0);
+                    tma_load_2d<CG>(sb, main ? bmain : &p.tm_b[ad - 1], fb, k, w.n0 + rank * half);
                     ++issued;
                     if (++stage == stages) { stage = 0; phase ^= 1; }
                 }
             }
-            if (!ok) {
+            if (!ok && leader) {
                 // wait (bounded, ignoring the abort flag) for the copies still in flight
                 long long first = issued > stages ? issued - stages : 0;
                 for (long long j = first; j < issued; ++j)
                     wait_bounded(smem_addr(&full[j % stages]), (uint32_t)((j / stages) & 1), abort_flag,
                                  p.status, limit, false);
             }
-            if (cs > 1) {
-                // every MMA of the cluster has released this CTA's stages (so no remote
-                // arrive can still target this CTA's barriers when it exits)
+            if (CG > 1) {
+                // the pair's MMAs have released every stage of this CTA: no copy into it and
+                // no remote arrive on its barriers is still pending when it exits
                 long long first = issued > stages ? issued - stages : 0;
                 for (long long j = first; j < issued; ++j)
                     wait_bounded(smem_addr(&empty[j % stages]), (uint32_t)((j / stages) & 1), abort_flag,
@@ -406,15 +472,15 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
             }
         }
     } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        // ------------------------------------------------------------ MMA issuer (even CTA)
+        if (lane == 0 && leader) {
             int stage = 0;
             uint32_t phase = 0;
             int it = 0;
             bool ok = true;
             for (int u = group; u < n_units && ok; u += n_groups, ++it) {
                 const Unit w = decode_unit(p, u, rank);
-                const uint32_t idesc = instr_desc_bf16(kTileM, w.n);
+                const uint32_t idesc = instr_desc_bf16(kTileM * CG, w.n);
                 const int acc = it & 1;
                 if (!wait_bounded(smem_addr(&tempty[acc]), ((it >> 1) & 1) ^ 1, abort_flag, p.status, limit, true)) {
                     ok = false;
@@ -428,25 +494,22 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t ad = smem_desc_sw128(smem_addr(a_ring + (size_t)stage * kStageBytesA));
-                    const uint64_t bd = smem_desc_sw128(smem_addr(b_ring + (size_t)stage * b_stage_bytes));
+                    const uint64_t ad = smem_desc<BK>(smem_addr(a_ring + (size_t)stage * kStageA));
+                    const uint64_t bd = smem_desc<BK>(smem_addr(b_ring + (size_t)stage * b_stage_bytes));
 #pragma unroll
-                    for (int k = 0; k < kTileK / 16; ++k) {
+                    for (int k = 0; k < BK / 16; ++k) {
                         // advance 16 bf16 = 32 bytes along K inside the swizzled rows
-                        mma_bf16(d, ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), idesc,
-                                 (kb > 0 || k > 0) ? 1u : 0u);
+                        mma_bf16<CG>(d, ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), idesc,
+                                     (kb > 0 || k > 0) ? 1u : 0u);
                     }
-                    if (cs > 1)
-                        mma_commit_multicast(smem_addr(&empty[stage]), mask);
-                    else
-                        mma_commit(smem_addr(&empty[stage]));
+                    mma_commit<CG>(smem_addr(&empty[stage]));
                     if (++stage == stages) { stage = 0; phase ^= 1; }
                 }
                 if (!ok) break;
-                mma_commit(smem_addr(&tfull[acc]));
+                mma_commit<CG>(smem_addr(&tfull[acc]));
             }
             // every MMA this thread issued has completed before TMEM is released
-            mma_commit(smem_addr(drain));
+            mma_commit_local<CG>(smem_addr(drain));
             wait_bounded(smem_addr(drain), 0, abort_flag, p.status, limit, false);
         }
     } else {
@@ -479,34 +542,16 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
                 n_out = p.d_out - w.n0;
             }
             const uint32_t taddr = tmem_base + (uint32_t)(acc * kAccCols) + lane_off;
-            int c = 0;
-            for (; c + 32 <= w.n; c += 32) {
+            for (int c = 0; c < w.n; c += 32) {
                 uint32_t v[32];
-                tmem_ld16(taddr + (uint32_t)c, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
-                tmem_ld16(taddr + (uint32_t)c + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
+                const bool two = c + 16 < w.n;  // w.n is a multiple of 16
+                tmem_ld16(taddr + (uint32_t)c, v);
+                if (two) tmem_ld16(taddr + (uint32_t)c + 16, v + 16);
                 tmem_ld_wait();
                 if (row_ok) {
 #pragma unroll
                     for (int h = 0; h < 4; ++h) {
-                        if (c + 8 * h < n_out) {
-                            uint4 o;
-                            o.x = pack_bf16x2(__uint_as_float(v[8 * h + 0]) * scale, __uint_as_float(v[8 * h + 1]) * scale);
-                            o.y = pack_bf16x2(__uint_as_float(v[8 * h + 2]) * scale, __uint_as_float(v[8 * h + 3]) * scale);
-                            o.z = pack_bf16x2(__uint_as_float(v[8 * h + 4]) * scale, __uint_as_float(v[8 * h + 5]) * scale);
-                            o.w = pack_bf16x2(__uint_as_float(v[8 * h + 6]) * scale, __uint_as_float(v[8 * h + 7]) * scale);
-                            *reinterpret_cast<uint4*>(out + c + 8 * h) = o;
-                        }
-                    }
-                }
-            }
-            if (c < w.n) {  // a last 16 columns
-                uint32_t v[16];
-                tmem_ld16(taddr + (uint32_t)c, v);
-                tmem_ld_wait();
-                if (row_ok) {
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        if (c + 8 * h < n_out) {
+                        if ((h < 2 || two) && c + 8 * h < n_out) {
                             uint4 o;
                             o.x = pack_bf16x2(__uint_as_float(v[8 * h + 0]) * scale, __uint_as_float(v[8 * h + 1]) * scale);
                             o.y = pack_bf16x2(__uint_as_float(v[8 * h + 2]) * scale, __uint_as_float(v[8 * h + 3]) * scale);
@@ -518,7 +563,10 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
                 }
             }
             tc_fence_before();
-            mbar_arrive(smem_addr(&tempty[acc]));
+            if (CG > 1)
+                mbar_arrive_cluster(map_to_rank(smem_addr(&tempty[acc]), 0));  // the even CTA's barrier
+            else
+                mbar_arrive(smem_addr(&tempty[acc]));
             if (w.shrink && p.flags && w.tile_index >= 0) {
                 // publish this tile's U rows to the fused units that wait for them
                 fence_proxy_async_global();
@@ -533,32 +581,42 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
 
     __syncwarp();
     tc_fence_before();
-    cluster_sync();  // the peer no longer writes into this CTA's shared memory
+    if (CG > 1) cluster_sync();  // neither CTA of the pair touches the other's memory after this
+    else __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, 2 * kAccCols);
+        tmem_dealloc<CG>(tmem_base, 2 * kAccCols);
     }
 }
 
 }  // namespace dev
 
-size_t gemm_smem_bytes(int b_tile_rows, int stages) {
-    return 1024 + (size_t)stages * (kStageBytesA + (size_t)b_tile_rows * kTileK * 2) +
+size_t gemm_smem_bytes(int b_tile_rows, int stages, int bk) {
+    return 1024 + (size_t)stages * ((size_t)kTileM * bk * 2 + (size_t)b_tile_rows * bk * 2) +
            8 * (2 * (size_t)stages + 5) + 16;
 }
 
+template <int BK, int CG>
+static cudaError_t set_smem_attr() {
+    return cudaFuncSetAttribute(dev::lora_gemm_kernel<BK, CG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kSmemLimit);
+}
+
 cudaError_t gemm_prepare_device() {
-    return cudaFuncSetAttribute(dev::lora_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                kSmemBudget + 2048);
+    cudaError_t e;
+    if ((e = set_smem_attr<64, 1>()) != cudaSuccess) return e;
+    if ((e = set_smem_attr<64, 2>()) != cudaSuccess) return e;
+    if ((e = set_smem_attr<32, 1>()) != cudaSuccess) return e;
+    return set_smem_attr<32, 2>();
 }
 
 static void launch_config(const GemmParams& p, int grid, cudaStream_t stream, cudaLaunchConfig_t* cfg,
                           cudaLaunchAttribute* attr) {
-    const int b_rows = p.tile_n > p.shrink_n ? p.tile_n : p.shrink_n;
+    const int b_rows = (p.tile_n > p.shrink_n ? p.tile_n : p.shrink_n) / p.cluster_size;
     memset(cfg, 0, sizeof(*cfg));
     cfg->gridDim = dim3(grid, 1, 1);
     cfg->blockDim = dim3(kThreads, 1, 1);
-    cfg->dynamicSmemBytes = gemm_smem_bytes(b_rows, p.stages);
+    cfg->dynamicSmemBytes = gemm_smem_bytes(b_rows, p.stages, p.bk);
     cfg->stream = stream;
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = p.cluster_size;
@@ -568,11 +626,20 @@ static void launch_config(const GemmParams& p, int grid, cudaStream_t stream, cu
     cfg->numAttrs = 1;
 }
 
+template <typename F>
+static cudaError_t dispatch(const GemmParams& p, F&& f) {
+    if (p.bk == 64 && p.cluster_size == 1) return f(dev::lora_gemm_kernel<64, 1>);
+    if (p.bk == 64 && p.cluster_size == 2) return f(dev::lora_gemm_kernel<64, 2>);
+    if (p.bk == 32 && p.cluster_size == 1) return f(dev::lora_gemm_kernel<32, 1>);
+    if (p.bk == 32 && p.cluster_size == 2) return f(dev::lora_gemm_kernel<32, 2>);
+    return cudaErrorInvalidValue;
+}
+
 cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t stream) {
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[1];
     launch_config(p, grid, stream, &cfg, attr);
-    return cudaLaunchKernelEx(&cfg, dev::lora_gemm_kernel, p);
+    return dispatch(p, [&](auto kernel) { return cudaLaunchKernelEx(&cfg, kernel, p); });
 }
 
 int gemm_max_clusters(const GemmParams& p) {
@@ -580,7 +647,8 @@ int gemm_max_clusters(const GemmParams& p) {
     cudaLaunchAttribute attr[1];
     launch_config(p, p.cluster_size, nullptr, &cfg, attr);
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, dev::lora_gemm_kernel, &cfg) != cudaSuccess) {
+    cudaError_t e = dispatch(p, [&](auto kernel) { return cudaOccupancyMaxActiveClusters(&n, kernel, &cfg); });
+    if (e != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }

@@ -10,12 +10,12 @@
 namespace lora {
 
 constexpr int kTileM = 128;          // rows per tile = tcgen05 M (cta_group::1)
-constexpr int kTileK = 64;           // K per pipeline stage: one 128-byte swizzle row of bf16
+constexpr int kTileK = 64;           // default K per pipeline stage: one 128-byte swizzle row of bf16
 constexpr int kMaxTileN = 256;       // widest output tile = one TMEM accumulator (256 fp32 columns)
 constexpr int kAccCols = 256;        // TMEM columns per accumulator; two accumulators per CTA
-constexpr int kStageBytesA = kTileM * kTileK * 2;      // 16 KB
-constexpr int kMaxStages = 12;
-constexpr int kSmemBudget = 232448 - 2048;             // opt-in dynamic smem minus slack
+constexpr int kStageBytesA = kTileM * kTileK * 2;      // 16 KB at K = 64
+constexpr int kMaxStages = 16;
+constexpr int kSmemLimit = 232448;                     // opt-in dynamic shared memory per CTA (227 KB)
 constexpr int kThreads = 192;        // warp 0 TMA, warp 1 MMA + TMEM owner, warps 2..5 epilogue
 constexpr int kEpilogueThreads = 128;
 
@@ -31,7 +31,7 @@ struct Tile {                        // one planner tile, as uploaded to the dev
 // for adapter tiles, the expand K-loop over the rank into the same accumulator). With
 // cluster_size 2 a unit is a group of two row tiles (tiles 2g and 2g+1 of the arrays, one
 // per CTA of the cluster) that share the same B operand tile; each CTA loads half of that
-// tile and multicasts it to both. Groups are padded with tiles of nrows 0.
+// tile's rows and the pair runs M = 256 MMAs. Groups are padded with tiles of nrows 0.
 // When `flags` is set, a fused unit's expand waits until flags[tile] == epoch, which the
 // shrink unit of that tile publishes after its U rows are stored (single-launch mode).
 struct GemmParams {
@@ -58,12 +58,16 @@ struct GemmParams {
     int tile_n;                      // fused output-tile width (multiple of 16, <= 256)
     int shrink_n;                    // shrink output-tile width = rank rounded up to 16
     int stages;
-    int m_fastest;                   // 1: consecutive fused units walk row tiles first
+    int m_fastest;                   // 1: row tiles first, 0: column tiles first, 2: column-tile groups
+    int raster_group;                // column tiles per group when m_fastest == 2
+    int l2_hints;                    // bit 0: B loads evict_last, 1: A loads evict_first (8: normal),
+                                     // 2: Y stores evict_first
     int k_main_blocks;               // ceil(d_in / 64)
     int k_lora_blocks;               // ceil(rank / 64)
     int d_out;
     int rank;
-    int cluster_size;                // 1, or 2 (TMA multicast of the B operand across the pair)
+    int cluster_size;                // CTA group of the MMA: 1, or 2 (an SM pair, M = 256)
+    int bk;                          // K per pipeline stage: 64 (128-byte swizzle) or 32 (64-byte swizzle)
     int debug_stall;
 };
 
@@ -79,7 +83,7 @@ int plan_segments(const int32_t* seg_offsets, const int32_t* seg_ids, int n_seg,
                   int n_adapters, Plan* plan);
 
 // kernels.cu
-size_t gemm_smem_bytes(int b_tile_rows, int stages);
+size_t gemm_smem_bytes(int b_tile_rows, int stages, int bk);
 cudaError_t gemm_prepare_device();           // sets the opt-in smem limit on the current device
 cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t stream);
 int gemm_max_clusters(const GemmParams& p);  // co-resident clusters of this launch shape

@@ -188,7 +188,8 @@ extern "C" int lora_linear_forward_noalloc(const void* x, int T, const int32_t* 
     const int tile_n = lora::kMaxTileN;
     const int shrink_n = cdiv(rank, 16) * 16;
     auto stages_for = [](int tn) {
-        int s = (lora::kSmemBudget - 1280) / (lora::kStageBytesA + tn * lora::kTileK * 2);
+        int s = lora::kMaxStages;
+        while (s > 2 && lora::gemm_smem_bytes(tn, s, lora::kTileK) > (size_t)lora::kSmemLimit) --s;
         return s < 2 ? 2 : (s > lora::kMaxStages ? lora::kMaxStages : s);
     };
 
@@ -244,6 +245,8 @@ extern "C" int lora_linear_forward_noalloc(const void* x, int T, const int32_t* 
     p.d_out = d_out;
     p.rank = rank;
     p.cluster_size = 1;
+    p.raster_group = 1;
+    p.bk = lora::kTileK;
     // two launches ordered by the stream: the shrink units, then the fused units
     if (plan.n_shrink > 0) {
         GemmParams s = p;

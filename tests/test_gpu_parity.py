@@ -178,6 +178,22 @@ def test_cta_pairs_equal_single_ctas(dev, name):
     assert torch.equal(y1, y2)
 
 
+@pytest.mark.parametrize("name", ["tiny", "sweep_down_multi", "mixed_near_ridge", "mixed_decode"])
+def test_k_step_32_equals_64(dev, name):
+    # 64-byte-swizzled 32-wide K stages issue the same K=16 MMA sequence as 64-wide ones
+    from mixed_lora_projection_gb300 import _lib as L
+    w = WORKLOADS[name]
+    inp = make_inputs(w, dev)
+    with _ll(w) as ll:
+        ll.set_option(L.OPT_TILE_K, 64)
+        y64 = run(ll, inp, w.seg_offsets, w.seg_ids).clone()
+        ll.set_option(L.OPT_TILE_K, 32)
+        y32 = run(ll, inp, w.seg_offsets, w.seg_ids)
+        torch.cuda.synchronize()
+        assert ll.status() == 0
+    assert torch.equal(y64, y32)
+
+
 def test_repeated_calls_reuse_flags(dev):
     # many calls in a row on one handle: the epoch-tagged ready flags never go stale
     w = WORKLOADS["sweep_o_multi"]
