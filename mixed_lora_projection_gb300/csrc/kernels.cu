@@ -18,11 +18,13 @@
 // CTA reaches without waiting, so the dependency cannot cycle.
 //
 // Per CTA (one per SM, persistent over the work units):
-//   warp 0      one thread issues TMA loads (cp.async.bulk.tensor, swizzle as wide as the
-//               K-step) of the A tile (128 rows) and the B tile per stage into a ring;
-//   warp 1      owns 512 TMEM columns (two 128x256 fp32 accumulators); one thread issues
-//               tcgen05.mma kind::f16 and commits each stage back to the producer and each
-//               finished accumulator to the epilogue;
+//   warp 0      TMA loads (cp.async.bulk.tensor, swizzle as wide as the K-step) of the A
+//               tile (128 rows) and the B tile per stage into a ring;
+//   warp 1      owns 512 TMEM columns (two 128x256 fp32 accumulators); issues tcgen05.mma
+//               kind::f16 and commits each stage back to the producer and each finished
+//               accumulator to the epilogue;
+//               both warps run their loops converged and let lane 0 issue (predicated): a
+//               lone diverged lane cannot feed the tensor pipe back to back;
 //   warps 2..5  epilogue: tcgen05.ld the accumulator (warp w reads TMEM lanes 32*(w%4)..),
 //               round to bf16 and store the tile's rows with 16-byte stores.
 // Two accumulators let the epilogue of one tile overlap the mainloop of the next.
@@ -82,9 +84,11 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t local, uint32_t rank) {
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-                 : "memory");
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes, uint32_t pred) {
+    asm volatile(
+        "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %2, 0;\n\t"
+        "@q mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n\t}" ::"r"(bar), "r"(bytes), "r"(pred)
+        : "memory");
 }
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
@@ -105,6 +109,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Warp-wide form of wait_bounded for the converged producer and MMA warps: every lane
+// tests the phase (one instruction for the warp); only if it is not complete yet does lane 0
+// fall back to the bounded loop. Returns the same value in every lane.
+__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* status,
+                                          uint64_t limit_ns);
+
 // Waits for the phase with the given parity to complete. Gives up (returns false) when
 // another role has aborted or when `limit_ns` of wall time pass; in the latter case it
 // records the timeout in the status word and raises the CTA's abort flag.
@@ -124,23 +134,34 @@ __device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatil
     }
 }
 
+__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* status,
+                                          uint64_t limit_ns) {
+    if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0) ok = wait_bounded(bar, parity, abort_flag, status, limit_ns, true);
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
 // ---------------------------------------------------------------- TMA
 // 2-D tiled load into this CTA's shared memory, completing bytes on `bar` (a barrier of
 // this CTA; with CG = 2 it may be the even CTA's barrier, as a shared::cluster address).
+// Issued by the lanes with pred != 0 (one lane of a converged warp).
 template <int CG>
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c_inner,
-                                            int c_outer) {
+                                            int c_outer, uint32_t pred) {
     if (CG == 1) {
         asm volatile(
-            "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-            " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
-            "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c_inner), "r"(c_outer)
+            "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %5, 0;\n\t"
+            "@q cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+            " [%0], [%1, {%3, %4}], [%2];\n\t}" ::"r"(dst),
+            "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c_inner), "r"(c_outer), "r"(pred)
             : "memory");
     } else {
         asm volatile(
-            "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.cta_group::2"
-            " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
-            "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c_inner), "r"(c_outer)
+            "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %5, 0;\n\t"
+            "@q cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.cta_group::2"
+            " [%0], [%1, {%3, %4}], [%2];\n\t}" ::"r"(dst),
+            "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c_inner), "r"(c_outer), "r"(pred)
             : "memory");
     }
 }
@@ -183,47 +204,61 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
     else
         asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
-// D[tmem] (+)= A[smem] * B[smem]^T, bf16 inputs, fp32 accumulate; one thread issues.
+// D[tmem] (+)= A[smem] * B[smem]^T, bf16 inputs, fp32 accumulate. Issued by the lane with
+// pred != 0 of a converged warp: the MMA stream keeps the tensor pipe busy only when the
+// issuing warp is converged (a lone diverged lane issues MMAs far more slowly).
 template <int CG>
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                         uint32_t accumulate) {
+                                         uint32_t accumulate, uint32_t pred) {
     if (CG == 1)
         asm volatile(
-            "{\n\t.reg .pred p;\n\t"
+            "{\n\t.reg .pred p, q;\n\t"
             "setp.ne.b32 p, %4, 0;\n\t"
-            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-            "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+            "setp.ne.b32 q, %5, 0;\n\t"
+            "@q tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+            "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(pred)
             : "memory");
     else
         asm volatile(
-            "{\n\t.reg .pred p;\n\t"
+            "{\n\t.reg .pred p, q;\n\t"
             "setp.ne.b32 p, %4, 0;\n\t"
-            "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-            "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+            "setp.ne.b32 q, %5, 0;\n\t"
+            "@q tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+            "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(pred)
             : "memory");
 }
 // Arrive once on `bar` (CG = 1: this CTA's; CG = 2: the barrier at that offset in both CTAs
-// of the pair) when every tcgen05 op this thread issued so far has completed.
+// of the pair) when every tcgen05 op the issuing lane issued so far has completed.
 template <int CG>
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
+__device__ __forceinline__ void mma_commit(uint32_t bar, uint32_t pred) {
     if (CG == 1)
-        asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-                     : "memory");
+        asm volatile(
+            "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %1, 0;\n\t"
+            "@q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar),
+            "r"(pred)
+            : "memory");
     else
         asm volatile(
-            "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-            " [%0], %1;" ::"r"(bar), "h"((uint16_t)3)
+            "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %2, 0;\n\t"
+            "@q tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+            " [%0], %1;\n\t}" ::"r"(bar), "h"((uint16_t)3), "r"(pred)
             : "memory");
 }
 // Same, arriving only on this CTA's barrier.
 template <int CG>
-__device__ __forceinline__ void mma_commit_local(uint32_t bar) {
+__device__ __forceinline__ void mma_commit_local(uint32_t bar, uint32_t pred) {
     if (CG == 1)
-        asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-                     : "memory");
+        asm volatile(
+            "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %1, 0;\n\t"
+            "@q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar),
+            "r"(pred)
+            : "memory");
     else
-        asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-                     : "memory");
+        asm volatile(
+            "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %1, 0;\n\t"
+            "@q tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar),
+            "r"(pred)
+            : "memory");
 }
 // 32 lanes x 32 bits x 16 columns: thread i of the warp gets 16 consecutive columns of lane
 // (taddr.lane + i).
@@ -407,9 +442,14 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
-        if (lane == 0 && !p.debug_stall) {
-            tma_prefetch_desc(&p.tm_x);
-            if (p.n_fused) { tma_prefetch_desc(&p.tm_w); tma_prefetch_desc(&p.tm_u); }
+        // The whole warp runs the loop (converged); lane 0 issues.
+        const uint32_t issuer = lane == 0 ? 1u : 0u;
+        if (!p.debug_stall) {
+            if (lane == 0) {
+                tma_prefetch_desc(&p.tm_x);
+                if (p.n_fused) { tma_prefetch_desc(&p.tm_w); tma_prefetch_desc(&p.tm_u); }
+            }
+            __syncwarp();
             int stage = 0;
             uint32_t phase = 0;
             long long issued = 0;
@@ -432,48 +472,54 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
                 for (int kb = 0; kb < w.nk; ++kb) {
                     if (kb == p.k_main_blocks && p.flags) {
                         // the expand reads U rows written by this tile's shrink unit
-                        if (!wait_flag(&p.flags[w.tile_index], p.epoch, abort_flag, p.status, limit)) {
+                        int fok = 1;
+                        if (lane == 0) fok = wait_flag(&p.flags[w.tile_index], p.epoch, abort_flag, p.status, limit);
+                        if (!__shfl_sync(0xffffffffu, fok, 0)) {
                             ok = false;
                             break;
                         }
                         fence_proxy_async_global();
                     }
-                    if (!wait_bounded(smem_addr(&empty[stage]), phase ^ 1, abort_flag, p.status, limit, true)) {
+                    if (!wait_warp(smem_addr(&empty[stage]), phase ^ 1, abort_flag, p.status, limit)) {
                         ok = false;
                         break;
                     }
                     const uint32_t fb_local = smem_addr(&full[stage]);
-                    if (leader) mbar_arrive_expect_tx(fb_local, tx);
+                    mbar_arrive_expect_tx(fb_local, tx, leader ? issuer : 0u);
                     const uint32_t fb = CG > 1 ? map_to_rank(fb_local, 0) : fb_local;
                     const uint32_t sa = smem_addr(a_ring + (size_t)stage * kStageA);
                     const uint32_t sb = smem_addr(b_ring + (size_t)stage * b_stage_bytes);
                     const bool main = kb < p.k_main_blocks;
                     const int k = main ? kb * BK : (kb - p.k_main_blocks) * BK;
-                    tma_load_2d<CG>(sa, main ? &p.tm_x : &p.tm_u, fb, k, w.tile.row0);
-                    tma_load_2d<CG>(sb, main ? bmain : &p.tm_b[ad - 1], fb, k, w.n0 + rank * half);
+                    tma_load_2d<CG>(sa, main ? &p.tm_x : &p.tm_u, fb, k, w.tile.row0, issuer);
+                    tma_load_2d<CG>(sb, main ? bmain : &p.tm_b[ad - 1], fb, k, w.n0 + rank * half, issuer);
                     ++issued;
                     if (++stage == stages) { stage = 0; phase ^= 1; }
                 }
             }
-            if (!ok && leader) {
-                // wait (bounded, ignoring the abort flag) for the copies still in flight
-                long long first = issued > stages ? issued - stages : 0;
-                for (long long j = first; j < issued; ++j)
-                    wait_bounded(smem_addr(&full[j % stages]), (uint32_t)((j / stages) & 1), abort_flag,
-                                 p.status, limit, false);
-            }
-            if (CG > 1) {
-                // the pair's MMAs have released every stage of this CTA: no copy into it and
-                // no remote arrive on its barriers is still pending when it exits
-                long long first = issued > stages ? issued - stages : 0;
-                for (long long j = first; j < issued; ++j)
-                    wait_bounded(smem_addr(&empty[j % stages]), (uint32_t)((j / stages) & 1), abort_flag,
-                                 p.status, limit, false);
+            if (lane == 0) {
+                if (!ok && leader) {
+                    // wait (bounded, ignoring the abort flag) for the copies still in flight
+                    long long first = issued > stages ? issued - stages : 0;
+                    for (long long j = first; j < issued; ++j)
+                        wait_bounded(smem_addr(&full[j % stages]), (uint32_t)((j / stages) & 1), abort_flag,
+                                     p.status, limit, false);
+                }
+                if (CG > 1) {
+                    // the pair's MMAs have released every stage of this CTA: no copy into it and
+                    // no remote arrive on its barriers is still pending when it exits
+                    long long first = issued > stages ? issued - stages : 0;
+                    for (long long j = first; j < issued; ++j)
+                        wait_bounded(smem_addr(&empty[j % stages]), (uint32_t)((j / stages) & 1), abort_flag,
+                                     p.status, limit, false);
+                }
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer (even CTA)
-        if (lane == 0 && leader) {
+        // The whole warp runs the loop (converged); lane 0 issues the MMAs and commits.
+        const uint32_t issuer = lane == 0 ? 1u : 0u;
+        if (leader) {
             int stage = 0;
             uint32_t phase = 0;
             int it = 0;
@@ -482,14 +528,14 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
                 const Unit w = decode_unit(p, u, rank);
                 const uint32_t idesc = instr_desc_bf16(kTileM * CG, w.n);
                 const int acc = it & 1;
-                if (!wait_bounded(smem_addr(&tempty[acc]), ((it >> 1) & 1) ^ 1, abort_flag, p.status, limit, true)) {
+                if (!wait_warp(smem_addr(&tempty[acc]), ((it >> 1) & 1) ^ 1, abort_flag, p.status, limit)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 const uint32_t d = tmem_base + (uint32_t)(acc * kAccCols);
                 for (int kb = 0; kb < w.nk; ++kb) {
-                    if (!wait_bounded(smem_addr(&full[stage]), phase, abort_flag, p.status, limit, true)) {
+                    if (!wait_warp(smem_addr(&full[stage]), phase, abort_flag, p.status, limit)) {
                         ok = false;
                         break;
                     }
@@ -500,17 +546,17 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
                     for (int k = 0; k < BK / 16; ++k) {
                         // advance 16 bf16 = 32 bytes along K inside the swizzled rows
                         mma_bf16<CG>(d, ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), idesc,
-                                     (kb > 0 || k > 0) ? 1u : 0u);
+                                     (kb > 0 || k > 0) ? 1u : 0u, issuer);
                     }
-                    mma_commit<CG>(smem_addr(&empty[stage]));
+                    mma_commit<CG>(smem_addr(&empty[stage]), issuer);
                     if (++stage == stages) { stage = 0; phase ^= 1; }
                 }
                 if (!ok) break;
-                mma_commit<CG>(smem_addr(&tfull[acc]));
+                mma_commit<CG>(smem_addr(&tfull[acc]), issuer);
             }
-            // every MMA this thread issued has completed before TMEM is released
-            mma_commit_local<CG>(smem_addr(drain));
-            wait_bounded(smem_addr(drain), 0, abort_flag, p.status, limit, false);
+            // every MMA this warp issued has completed before TMEM is released
+            mma_commit_local<CG>(smem_addr(drain), issuer);
+            if (lane == 0) wait_bounded(smem_addr(drain), 0, abort_flag, p.status, limit, false);
         }
     } else {
         // ------------------------------------------------------------ epilogue (warps 2..5)
