@@ -283,6 +283,7 @@ def run_ours(args, rank, world, dist):
                 "d2h_bytes_per_step": sum(2 * w.T * w.d_out for w, _, _ in items),
                 "ms_per_step": round(e2e_ms, 4), "steps": e2e_steps},
         "gpu_launches": launches,
+        "launch_shape": setups[0][1].describe(w0.T, w0.seg_offsets, w0.seg_ids),
         "clocks": sampler.summary(t0, t1),
     }
     if w0.T <= 512 and len(items) == 1:

@@ -11,6 +11,7 @@
 
 #include <algorithm>
 #include <cmath>
+#include <unordered_map>
 #include <vector>
 
 #include "../../include/lora_linear.h"
@@ -76,6 +77,7 @@ struct lora_linear {
     int force_tile_n = 0, raster = 0, debug_stall = 0, timing = 0, two_launch = 0, cluster = 0;
     int raster_group = 4, l2_hints = 0, tile_k = 0;
     int max_clusters_cache[2][kMaxTileN / 16 + 1] = {};  // co-resident clusters by (size, B rows)
+    std::unordered_map<uint64_t, uint32_t> shape_cache;   // plan signature -> (cs << 16) | tile_n
     unsigned long long wait_limit_ns = 4000000000ull;
     std::vector<TimingRec> trec;
     std::vector<cudaEvent_t> ev_pool;
@@ -226,18 +228,87 @@ int max_clusters(lora_linear* h, const GemmParams& p) {
     return c;
 }
 
-Shape choose_shape(const lora_linear* h, const Plan& plan) {
+// Per-SM cycles of one 64-wide K-step of an N-column unit, measured on GB300: a single CTA
+// is bound by how fast its shared memory fills (A + B tile, ~61 bytes per clock); an SM pair
+// lands only half of B per SM and is bound by the MMA stream (N/2 cycles per K=16 MMA, plus
+// the per-step barrier round trip) and the pair's coupling.
+double kstep_cycles(int cs, int n) {
+    const double mma = 4.0 * std::max(n / 2.0, 48.0) + 130.0;
+    const double fill = (kTileM + (double)n / cs) * kTileK * 2.0 / 61.0;
+    return cs == 1 ? std::max(fill, mma) : 1.2 * std::max(fill, mma);
+}
+
+// Makespan (per-SM cycles) of the persistent round-robin schedule of one launch shape.
+double makespan(const lora_linear* h, const std::vector<Tile>& fused_groups, const std::vector<Tile>& shrink_groups,
+                int cs, int tile_n, int shrink_n, int slots) {
+    const int k_main = ceil_div(h->d_in, kTileK), k_lora = ceil_div(h->rank, kTileK);
+    const int n_ntiles = ceil_div(h->d_out, tile_n);
+    const int nsg = (int)shrink_groups.size() / cs, nfg = (int)fused_groups.size() / cs;
+    const double c_shrink = k_main * kstep_cycles(cs, shrink_n);
+    const double c_base = k_main * kstep_cycles(cs, tile_n), c_lora = k_lora * kstep_cycles(cs, tile_n);
+    std::vector<double> load(slots, 0.0);
+    long long u = 0;
+    for (int g = 0; g < nsg; ++g, ++u) load[u % slots] += c_shrink;
+    // fused units in the kernel's order do not change the per-slot sums by much; use row-major
+    for (int g = 0; g < nfg; ++g) {
+        const double c = c_base + (fused_groups[(size_t)g * cs].adapter ? c_lora : 0.0);
+        for (int t = 0; t < n_ntiles; ++t, ++u) load[u % slots] += c;
+    }
+    return *std::max_element(load.begin(), load.end());
+}
+
+Shape choose_shape(lora_linear* h, const Plan& plan) {
     Shape sh;
     const int nf = (int)plan.fused.size();
-    sh.cs = h->cluster ? h->cluster : (nf >= 2 ? 2 : 1);
+    sh.shrink_n = ceil_div(h->rank, 16) * 16;
+    sh.bk = h->tile_k ? h->tile_k : 64;
+    const bool small_batch = (long long)nf * kTileM <= 384;
+    int cs = h->cluster, tn = h->force_tile_n;
+    if (!cs || !tn) {
+        if (small_batch && !cs) cs = 1;
+        // plan signature: tile count and each tile's adapter / row count
+        uint64_t key = 1469598103934665603ull ^ (uint64_t)nf;
+        for (const Tile& t : plan.fused) key = (key ^ (uint64_t)(t.adapter * 131 + t.nrows)) * 1099511628211ull;
+        key ^= ((uint64_t)cs << 56) ^ ((uint64_t)tn << 40);
+        auto it = h->shape_cache.find(key);
+        if (it != h->shape_cache.end()) {
+            cs = (int)(it->second >> 16);
+            tn = (int)(it->second & 0xFFFF);
+        } else {
+            double best = -1;
+            int best_cs = 1, best_tn = kMaxTileN;
+            for (int c = 1; c <= 2; ++c) {
+                if (cs && c != cs) continue;
+                if (c == 2 && nf < 2) continue;
+                std::vector<Tile> fg, sg;
+                make_groups(plan.fused, c, false, &fg);
+                make_groups(plan.shrink, c, true, &sg);
+                const int slots = h->num_sms / c;
+                if (small_batch) {
+                    const int t = tn ? tn : choose_tile_n(h, nf, (int)fg.size() / c, slots);
+                    const double m = makespan(h, fg, sg, c, t, sh.shrink_n, slots);
+                    if (best < 0 || m < best) { best = m; best_cs = c; best_tn = t; }
+                    continue;
+                }
+                for (int t = kMaxTileN; t >= 128; t -= 16) {
+                    if (tn && t != tn) continue;
+                    const double m = makespan(h, fg, sg, c, t, sh.shrink_n, slots);
+                    if (best < 0 || m < best * 0.999) { best = m; best_cs = c; best_tn = t; }
+                }
+            }
+            cs = best_cs;
+            tn = best_tn;
+            if (h->shape_cache.size() > 256) h->shape_cache.clear();
+            h->shape_cache[key] = ((uint32_t)cs << 16) | (uint32_t)tn;
+        }
+    }
+    sh.cs = cs;
     make_groups(plan.fused, sh.cs, false, &sh.fused_groups);
     make_groups(plan.shrink, sh.cs, true, &sh.shrink_groups);
     const int nfg = (int)sh.fused_groups.size() / sh.cs;
     const int slots = h->num_sms / sh.cs;
-    sh.tile_n = choose_tile_n(h, nf, nfg, slots);
-    sh.shrink_n = ceil_div(h->rank, 16) * 16;
+    sh.tile_n = tn;
     sh.n_ntiles = ceil_div(h->d_out, sh.tile_n);
-    sh.bk = h->tile_k ? h->tile_k : 64;
     sh.stages = stages_for(std::max(sh.tile_n, sh.shrink_n) / sh.cs, sh.bk);
     sh.m_fastest = choose_m_fastest(h, nfg, sh.n_ntiles, sh.tile_n, kTileM * sh.cs, slots);
     return sh;
