@@ -21,7 +21,7 @@ using namespace lora;
 
 namespace {
 
-constexpr int kRing = 4;  // work-list slots in flight per handle
+constexpr int kRing = 8;  // work-list slots in flight per handle
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -82,9 +82,11 @@ struct lora_linear {
     std::vector<TimingRec> trec;
     std::vector<cudaEvent_t> ev_pool;
     long long launches = 0;
-    // staging for forward_host
+    // staging for forward_host: device copies of X and Y, copy streams, chunk events
     void* x_stage = nullptr;
     void* y_stage = nullptr;
+    cudaStream_t s_in = nullptr, s_out = nullptr;
+    cudaEvent_t ev_in[16] = {}, ev_done[16] = {};
 };
 
 namespace {
@@ -118,6 +120,12 @@ void free_handle(lora_linear* h) {
     if (h->status_host) cudaFreeHost(h->status_host);
     if (h->x_stage) cudaFree(h->x_stage);
     if (h->y_stage) cudaFree(h->y_stage);
+    if (h->s_in) cudaStreamDestroy(h->s_in);
+    if (h->s_out) cudaStreamDestroy(h->s_out);
+    for (int i = 0; i < 16; ++i) {
+        if (h->ev_in[i]) cudaEventDestroy(h->ev_in[i]);
+        if (h->ev_done[i]) cudaEventDestroy(h->ev_done[i]);
+    }
     delete h;
 }
 
@@ -587,10 +595,18 @@ int lora_linear_describe(lora_linear* h, int T, const int32_t* seg_offsets,
     return LORA_OK;
 }
 
-int lora_linear_forward(lora_linear* h, const void* x, int T, const int32_t* seg_offsets,
-                        const int32_t* seg_adapter_ids, int n_seg, const void* W,
-                        const void* const* A, const void* const* B, const float* scale,
-                        int n_adapters, void* y, void* stream_) {
+}  // extern "C"
+
+namespace {
+// The projection on `stream`. The call's work list is uploaded on `upload`: the same stream,
+// or (host-buffer path) a copy stream that then also copies the call's X rows from `x_src`
+// and records `ready`, on which `stream` waits before the launch. Keeping the small work-list
+// copy on the copy stream, ahead of the X rows, stops it from queueing behind the next
+// chunk's X copy.
+int forward_impl(lora_linear* h, const void* x, int T, const int32_t* seg_offsets,
+                 const int32_t* seg_adapter_ids, int n_seg, const void* W, const void* const* A,
+                 const void* const* B, const float* scale, int n_adapters, void* y, cudaStream_t stream,
+                 cudaStream_t upload, const void* x_src, cudaEvent_t ready) {
     if (!h) return LORA_EINVAL;
     int rc = lora_linear_validate(h->d_in, h->d_out, h->rank, h->max_tokens, h->max_segments, x, T,
                                   seg_offsets, seg_adapter_ids, n_seg, W, A, B, scale, n_adapters, y);
@@ -612,7 +628,6 @@ int lora_linear_forward(lora_linear* h, const void* x, int T, const int32_t* seg
     for (size_t i = 0; i < plan.fused.size(); ++i) plan.fused[i].fused_index = (int32_t)i;
 
     DeviceGuard guard(h->device);
-    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
     const Shape sh = choose_shape(h, plan);
     const int cs = sh.cs, tile_n = sh.tile_n, shrink_n = sh.shrink_n, bk = sh.bk;
     const int nfg = (int)sh.fused_groups.size() / cs, nsg = (int)sh.shrink_groups.size() / cs;
@@ -646,7 +661,14 @@ int lora_linear_forward(lora_linear* h, const void* x, int T, const int32_t* seg
     memcpy(hb + off_segid, plan.seg_id.data(), 4 * (size_t)n_m);
     float* sc = reinterpret_cast<float*>(hb + off_scale);
     for (int k = 0; k < n_used; ++k) sc[k] = scale[plan.used_adapters[k]];
-    if (cudaMemcpyAsync(slot->dev, hb, used_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess)
+    if (cudaMemcpyAsync(slot->dev, hb, used_bytes, cudaMemcpyHostToDevice, upload) != cudaSuccess)
+        return LORA_ECUDA;
+    if (x_src &&
+        cudaMemcpyAsync(const_cast<void*>(x), x_src, (size_t)T * h->d_in * 2, cudaMemcpyHostToDevice, upload) !=
+            cudaSuccess)
+        return LORA_ECUDA;
+    if (upload != stream &&
+        (cudaEventRecord(ready, upload) != cudaSuccess || cudaStreamWaitEvent(stream, ready, 0) != cudaSuccess))
         return LORA_ECUDA;
 
     GemmParams p;
@@ -725,6 +747,18 @@ int lora_linear_forward(lora_linear* h, const void* x, int T, const int32_t* seg
     slot->pending = true;
     return LORA_OK;
 }
+}  // namespace
+
+extern "C" {
+
+int lora_linear_forward(lora_linear* h, const void* x, int T, const int32_t* seg_offsets,
+                        const int32_t* seg_adapter_ids, int n_seg, const void* W,
+                        const void* const* A, const void* const* B, const float* scale,
+                        int n_adapters, void* y, void* stream_) {
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    return forward_impl(h, x, T, seg_offsets, seg_adapter_ids, n_seg, W, A, B, scale, n_adapters, y, stream,
+                        stream, nullptr, nullptr);
+}
 
 int lora_linear_forward_host(lora_linear* h, const void* x_host, int T, const int32_t* seg_offsets,
                              const int32_t* seg_adapter_ids, int n_seg, const void* W,
@@ -733,6 +767,15 @@ int lora_linear_forward_host(lora_linear* h, const void* x_host, int T, const in
     if (!h) return LORA_EINVAL;
     if (T < 0 || T > h->max_tokens) return LORA_EINVAL;
     if (T > 0 && (!x_host || !y_host)) return LORA_EINVAL;
+    // the call's segments are checked once, up front (the chunks only re-slice them); each
+    // chunk's device-side arguments are checked by lora_linear_forward
+    if (n_seg > h->max_segments) return LORA_EINVAL;
+    {
+        Plan whole;
+        int prc = plan_segments(seg_offsets, seg_adapter_ids, n_seg, T, n_adapters, &whole);
+        if (prc != LORA_OK) return prc;
+    }
+    int rc = LORA_OK;
     DeviceGuard guard(h->device);
     if (!h->x_stage) {
         if (cudaMalloc(&h->x_stage, (size_t)h->max_tokens * h->d_in * 2) != cudaSuccess ||
@@ -744,18 +787,60 @@ int lora_linear_forward_host(lora_linear* h, const void* x_host, int T, const in
             return LORA_ENOMEM;
         }
     }
+    if (!h->s_in) {
+        if (cudaStreamCreateWithFlags(&h->s_in, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaStreamCreateWithFlags(&h->s_out, cudaStreamNonBlocking) != cudaSuccess)
+            return LORA_ECUDA;
+        for (int i = 0; i < 16; ++i)
+            if (cudaEventCreateWithFlags(&h->ev_in[i], cudaEventDisableTiming) != cudaSuccess ||
+                cudaEventCreateWithFlags(&h->ev_done[i], cudaEventDisableTiming) != cudaSuccess)
+                return LORA_ECUDA;
+    }
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
-    const size_t xb = (size_t)T * h->d_in * 2, yb = (size_t)T * h->d_out * 2;
-    if (T > 0 && cudaMemcpyAsync(h->x_stage, x_host, xb, cudaMemcpyHostToDevice, stream) != cudaSuccess)
+    // Row chunks: copy-in of chunk c+1 and copy-out of chunk c-1 overlap the kernel of chunk c
+    // (rows are independent, so each chunk is a call of its own on its rows).
+    const int n_chunks = std::max(1, std::min(8, T / 1024));
+    const int chunk_rows = n_chunks == 1 ? T : ceil_div(ceil_div(T, n_chunks), kTileM) * kTileM;
+    const uint8_t* xh = static_cast<const uint8_t*>(x_host);
+    uint8_t* yh = static_cast<uint8_t*>(y_host);
+    uint8_t* xd = static_cast<uint8_t*>(h->x_stage);
+    uint8_t* yd = static_cast<uint8_t*>(h->y_stage);
+    const size_t xrow = (size_t)h->d_in * 2, yrow = (size_t)h->d_out * 2;
+    std::vector<int32_t> off, ids;
+    int c = 0;
+    for (int a = 0; a < T || (T == 0 && c == 0); a += chunk_rows, ++c) {
+        const int b = std::min(T, a + chunk_rows);
+        const int n = b - a;
+        // the segments restricted to rows [a, b), offsets made relative to a
+        off.assign(1, 0);
+        ids.clear();
+        for (int i = 0; i < n_seg; ++i) {
+            int lo = std::max(seg_offsets[i], a), hi = std::min(seg_offsets[i + 1], b);
+            if (hi <= lo) continue;
+            off.push_back(hi - a);
+            ids.push_back(seg_adapter_ids[i]);
+        }
+        if (ids.empty() && n > 0) return LORA_EINVAL;
+        const int e = c % 16;
+        // work list (on s_in, planned and uploaded by forward_impl), then X rows, both
+        // ordered before the event the kernel waits on
+        rc = forward_impl(h, xd + (size_t)a * xrow, n, off.data(), ids.data(), (int)ids.size(), W, A, B, scale,
+                          n_adapters, yd + (size_t)a * yrow, stream, h->s_in, xh + (size_t)a * xrow, h->ev_in[e]);
+        if (rc != LORA_OK) return rc;
+        if (n > 0) {
+            if (cudaEventRecord(h->ev_done[e], stream) != cudaSuccess ||
+                cudaStreamWaitEvent(h->s_out, h->ev_done[e], 0) != cudaSuccess)
+                return LORA_ECUDA;
+            if (cudaMemcpyAsync(yh + (size_t)a * yrow, yd + (size_t)a * yrow, (size_t)n * yrow, cudaMemcpyDeviceToHost,
+                                h->s_out) != cudaSuccess)
+                return LORA_ECUDA;
+        }
+        if (T == 0) break;
+    }
+    if (cudaStreamSynchronize(stream) != cudaSuccess || cudaStreamSynchronize(h->s_out) != cudaSuccess)
         return LORA_ECUDA;
-    int rc = lora_linear_forward(h, h->x_stage, T, seg_offsets, seg_adapter_ids, n_seg, W, A, B, scale,
-                                 n_adapters, h->y_stage, stream_);
-    if (rc != LORA_OK) return rc;
-    if (T > 0 && cudaMemcpyAsync(y_host, h->y_stage, yb, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+    if (cudaMemcpy(h->status_host, h->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
         return LORA_ECUDA;
-    if (cudaMemcpyAsync(h->status_host, h->status, sizeof(int), cudaMemcpyDeviceToHost, stream) != cudaSuccess)
-        return LORA_ECUDA;
-    if (cudaStreamSynchronize(stream) != cudaSuccess) return LORA_ECUDA;
     return *h->status_host ? LORA_ETIMEOUT : LORA_OK;
 }
 

@@ -254,8 +254,10 @@ def test_invalid_call_leaves_output_untouched(dev):
         assert ll.timing(1)[2] == 0
 
 
-def test_host_buffers_path_matches_device_path(dev):
-    w = WORKLOADS["tiny"]
+@pytest.mark.parametrize("name", ["tiny", "mixed_batch", "sweep_qkv_multi"])
+def test_host_buffers_path_matches_device_path(dev, name):
+    # the host-buffer entry point pipelines row chunks over copy and compute streams
+    w = WORKLOADS[name]
     inp = make_inputs(w, dev)
     x_host = inp.x.cpu().pin_memory()
     y_host = torch.empty((w.T, w.d_out), dtype=torch.bfloat16).pin_memory()
@@ -263,7 +265,11 @@ def test_host_buffers_path_matches_device_path(dev):
         y = run(ll, inp, w.seg_offsets, w.seg_ids)
         ll.forward_host(x_host, w.seg_offsets, w.seg_ids, inp.w, inp.a, inp.b, inp.scales, y_host)
     torch.cuda.synchronize()
-    assert torch.equal(y.cpu(), y_host)
+    if w.T < 2048:
+        assert torch.equal(y.cpu(), y_host)          # one chunk: the same launch
+    else:
+        # chunks are planned on their own rows: same values up to the tolerance
+        assert rel_err(y_host, f64(y).astype("float64")) <= TOL
 
 
 # --------------------------------------------------------------------------- full-size workloads
