@@ -153,6 +153,21 @@ def _fused_flops(w):
     return 2.0 * w.T * w.d_in * w.d_out + 2.0 * w.adapter_rows * w.rank * w.d_out
 
 
+# --------------------------------------------------------------------------- ranks
+
+def aggregate_ranks(elapsed_ms, e2e_ms, flops_per_step, steps, world, dist):
+    """Slowest rank's device and end-to-end times; whole-job TFLOP/s (every rank runs the
+    workload: replicas, so the job's work is world x one rank's)."""
+    if dist is not None:
+        import torch
+        t = torch.tensor([elapsed_ms, e2e_ms], dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms, e2e_ms = float(t[0]), float(t[1])
+    value = world * flops_per_step * steps / (elapsed_ms * 1e-3) / 1e12
+    e2e_value = world * flops_per_step / (e2e_ms * 1e-3) / 1e12
+    return elapsed_ms, e2e_ms, value, e2e_value
+
+
 # --------------------------------------------------------------------------- our arm
 
 def run_ours(args, rank, world, dist):
@@ -241,16 +256,9 @@ def run_ours(args, rank, world, dist):
     if dist:
         dist.barrier()
 
-    if dist:
-        import torch.distributed as D
-        t = torch.tensor([elapsed_ms, e2e_ms], dtype=torch.float64)
-        D.all_reduce(t, op=D.ReduceOp.MAX)
-        elapsed_ms, e2e_ms = float(t[0]), float(t[1])
-
-    ms_per_step = elapsed_ms / args.steps
     flops = _flops_of(items)
-    value = world * flops * args.steps / (elapsed_ms * 1e-3) / 1e12
-    e2e_value = world * flops / (e2e_ms * 1e-3) / 1e12
+    elapsed_ms, e2e_ms, value, e2e_value = aggregate_ranks(elapsed_ms, e2e_ms, flops, args.steps, world, dist)
+    ms_per_step = elapsed_ms / args.steps
     peak_burst, peak_sust, hbm, src = _peaks()
     # the timed kernel: the one launch per call (shrink + base + expand), or, in two-launch
     # mode, the fused base+expand launch alone

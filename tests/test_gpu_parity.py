@@ -229,6 +229,31 @@ def test_guard_rows_untouched(dev):
     assert rel_err(full[G:G + T], oracle_full(inp, off, ids)) <= TOL
 
 
+@pytest.mark.parametrize("cluster", [1, 2])
+def test_bounded_waits_report_timeout_and_the_handle_recovers(dev, cluster):
+    # the load warp never issues: every wait runs out after 20 ms, the kernel returns with
+    # the status word set (no hang, no trap), and the next normal call is correct again
+    from mixed_lora_projection_gb300 import _lib as L
+    w = WORKLOADS["sweep_o"]
+    inp = make_inputs(w, dev)
+    with _ll(w) as ll:
+        ll.set_option(L.OPT_CLUSTER, cluster)
+        ll.set_option(L.OPT_WAIT_LIMIT_US, 20000)
+        ll.set_option(L.OPT_DEBUG_STALL, 1)
+        run(ll, inp, w.seg_offsets, w.seg_ids)
+        torch.cuda.synchronize()
+        assert ll.status(reset=True) == L.LORA_ETIMEOUT
+        assert ll.status() == L.LORA_OK
+        ll.set_option(L.OPT_DEBUG_STALL, 0)
+        ll.set_option(L.OPT_WAIT_LIMIT_US, 4000000)
+        y = run(ll, inp, w.seg_offsets, w.seg_ids)
+        torch.cuda.synchronize()
+        assert ll.status() == L.LORA_OK
+    rows = sample_rows(w.T, list(w.seg_offsets), list(w.seg_ids), n_random=64, seed=1)
+    ref = oracle_rows(inp, list(w.seg_offsets), list(w.seg_ids), rows)
+    assert rel_err(y[torch.as_tensor(rows, device=dev)], ref) <= TOL
+
+
 def test_empty_batch_launches_nothing(dev):
     w = WORKLOADS["tiny"]
     inp = make_inputs(w, dev)
