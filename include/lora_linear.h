@@ -164,7 +164,9 @@ enum {
     LORA_OPT_RASTER_GROUP = 8,  /* column tiles per group for LORA_OPT_RASTER = 3 (default 4) */
     LORA_OPT_L2_HINTS = 9,      /* L2 eviction priorities, bit mask: 1 = weights evict_last, 2 = activations
                                    evict_first (with 8: evict_normal), 4 = output stores evict_first */
-    LORA_OPT_TILE_K = 10        /* K per pipeline stage: 0 = auto, 32 or 64 */
+    LORA_OPT_TILE_K = 10,       /* K per pipeline stage: 0 = auto, 32 or 64 */
+    LORA_OPT_INLINE_WORK_LIST = 11 /* 1 (default) = small work lists travel in the kernel parameters,
+                                      0 = always upload them to device memory */
 };
 
 /* lora_linear_set_option -- set one option above. Returns LORA_OK or LORA_EINVAL. */

@@ -75,7 +75,7 @@ struct lora_linear {
     EncodeTiledFn encode = nullptr;
     // options
     int force_tile_n = 0, raster = 0, debug_stall = 0, timing = 0, two_launch = 0, cluster = 0;
-    int raster_group = 4, l2_hints = 0, tile_k = 0;
+    int raster_group = 4, l2_hints = 0, tile_k = 0, allow_inline = 1;
     int max_clusters_cache[2][kMaxTileN / 16 + 1] = {};  // co-resident clusters by (size, B rows)
     std::unordered_map<uint64_t, uint32_t> shape_cache;   // plan signature -> (cs << 16) | tile_n
     unsigned long long wait_limit_ns = 4000000000ull;
@@ -505,6 +505,9 @@ int lora_linear_set_option(lora_linear* h, int option, long long value) {
             if (value < 1 || value > 4096) return LORA_EINVAL;
             h->raster_group = (int)value;
             return LORA_OK;
+        case LORA_OPT_INLINE_WORK_LIST:
+            h->allow_inline = value ? 1 : 0;
+            return LORA_OK;
         case LORA_OPT_TILE_K:
             if (value != 0 && value != 32 && value != 64) return LORA_EINVAL;
             h->tile_k = (int)value;
@@ -633,56 +636,86 @@ int forward_impl(lora_linear* h, const void* x, int T, const int32_t* seg_offset
     const int nfg = (int)sh.fused_groups.size() / cs, nsg = (int)sh.shrink_groups.size() / cs;
     const int nft = (int)sh.fused_groups.size(), nst = (int)sh.shrink_groups.size();
     const int n_m = (int)plan.seg_id.size();
-
-    Slot* slot = acquire_slot(h);
-    if (!slot) return LORA_ECUDA;
-    // work list: [B_a maps][A_a maps][fused groups][shrink groups][seg_off][seg_id][scales]
-    size_t off_bmaps = 0;
-    size_t off_amaps = off_bmaps + (size_t)n_used * sizeof(CUtensorMap);
-    size_t off_fused = align_up(off_amaps + (size_t)n_used * sizeof(CUtensorMap), 128);
-    size_t off_shrink = off_fused + (size_t)nft * sizeof(Tile);
-    size_t off_segoff = align_up(off_shrink + (size_t)nst * sizeof(Tile), 16);
-    size_t off_segid = off_segoff + 4 * (size_t)(n_m + 1);
-    size_t off_scale = align_up(off_segid + 4 * (size_t)n_m, 16);
-    size_t used_bytes = off_scale + 4 * (size_t)n_used;
-    if (used_bytes > h->slot_bytes) return LORA_EINVAL;
-
-    uint8_t* hb = slot->host;
-    CUtensorMap* bmaps = reinterpret_cast<CUtensorMap*>(hb + off_bmaps);
-    CUtensorMap* amaps = reinterpret_cast<CUtensorMap*>(hb + off_amaps);
-    for (int k = 0; k < n_used; ++k) {
-        int a = plan.used_adapters[k];
-        if (encode_2d(h, &bmaps[k], B[a], h->rank, h->d_out, bk, tile_n / cs) != CUDA_SUCCESS) return LORA_ECUDA;
-        if (encode_2d(h, &amaps[k], A[a], h->d_in, h->rank, bk, shrink_n / cs) != CUDA_SUCCESS) return LORA_ECUDA;
-    }
-    memcpy(hb + off_fused, sh.fused_groups.data(), (size_t)nft * sizeof(Tile));
-    memcpy(hb + off_shrink, sh.shrink_groups.data(), (size_t)nst * sizeof(Tile));
-    memcpy(hb + off_segoff, plan.seg_off.data(), 4 * (size_t)(n_m + 1));
-    memcpy(hb + off_segid, plan.seg_id.data(), 4 * (size_t)n_m);
-    float* sc = reinterpret_cast<float*>(hb + off_scale);
-    for (int k = 0; k < n_used; ++k) sc[k] = scale[plan.used_adapters[k]];
-    if (cudaMemcpyAsync(slot->dev, hb, used_bytes, cudaMemcpyHostToDevice, upload) != cudaSuccess)
-        return LORA_ECUDA;
-    if (x_src &&
-        cudaMemcpyAsync(const_cast<void*>(x), x_src, (size_t)T * h->d_in * 2, cudaMemcpyHostToDevice, upload) !=
-            cudaSuccess)
-        return LORA_ECUDA;
-    if (upload != stream &&
-        (cudaEventRecord(ready, upload) != cudaSuccess || cudaStreamWaitEvent(stream, ready, 0) != cudaSuccess))
-        return LORA_ECUDA;
+    const int nf = (int)plan.fused.size();
 
     GemmParams p;
     memset(&p, 0, sizeof(p));
+    const bool inline_wl = h->allow_inline && nft + nst <= kInlineTiles && n_m <= kInlineSegs &&
+                           n_used <= kInlineAdapters;
+    Slot* slot = nullptr;
+    if (inline_wl) {
+        // small work list: it travels in the kernel parameters, no upload
+        for (int k = 0; k < n_used; ++k) {
+            int a = plan.used_adapters[k];
+            if (encode_2d(h, &p.inline_maps[k], B[a], h->rank, h->d_out, bk, tile_n / cs) != CUDA_SUCCESS)
+                return LORA_ECUDA;
+            if (encode_2d(h, &p.inline_maps[kInlineAdapters + k], A[a], h->d_in, h->rank, bk, shrink_n / cs) !=
+                CUDA_SUCCESS)
+                return LORA_ECUDA;
+            p.inline_scales[k] = scale[a];
+        }
+        memcpy(p.inline_tiles, sh.fused_groups.data(), (size_t)nft * sizeof(Tile));
+        memcpy(p.inline_tiles + nft, sh.shrink_groups.data(), (size_t)nst * sizeof(Tile));
+        memcpy(p.inline_seg, plan.seg_off.data(), 4 * (size_t)(n_m + 1));
+        memcpy(p.inline_seg + n_m + 1, plan.seg_id.data(), 4 * (size_t)n_m);
+        p.inline_wl = 1;
+        p.inline_shrink_off = nft;
+        if (x_src &&
+            cudaMemcpyAsync(const_cast<void*>(x), x_src, (size_t)T * h->d_in * 2, cudaMemcpyHostToDevice, upload) !=
+                cudaSuccess)
+            return LORA_ECUDA;
+        if (upload != stream &&
+            (cudaEventRecord(ready, upload) != cudaSuccess || cudaStreamWaitEvent(stream, ready, 0) != cudaSuccess))
+            return LORA_ECUDA;
+    } else {
+        slot = acquire_slot(h);
+        if (!slot) return LORA_ECUDA;
+        // work list: [B_a maps][A_a maps][fused groups][shrink groups][seg_off][seg_id][scales]
+        size_t off_bmaps = 0;
+        size_t off_amaps = off_bmaps + (size_t)n_used * sizeof(CUtensorMap);
+        size_t off_fused = align_up(off_amaps + (size_t)n_used * sizeof(CUtensorMap), 128);
+        size_t off_shrink = off_fused + (size_t)nft * sizeof(Tile);
+        size_t off_segoff = align_up(off_shrink + (size_t)nst * sizeof(Tile), 16);
+        size_t off_segid = off_segoff + 4 * (size_t)(n_m + 1);
+        size_t off_scale = align_up(off_segid + 4 * (size_t)n_m, 16);
+        size_t used_bytes = off_scale + 4 * (size_t)n_used;
+        if (used_bytes > h->slot_bytes) return LORA_EINVAL;
+
+        uint8_t* hb = slot->host;
+        CUtensorMap* bmaps = reinterpret_cast<CUtensorMap*>(hb + off_bmaps);
+        CUtensorMap* amaps = reinterpret_cast<CUtensorMap*>(hb + off_amaps);
+        for (int k = 0; k < n_used; ++k) {
+            int a = plan.used_adapters[k];
+            if (encode_2d(h, &bmaps[k], B[a], h->rank, h->d_out, bk, tile_n / cs) != CUDA_SUCCESS) return LORA_ECUDA;
+            if (encode_2d(h, &amaps[k], A[a], h->d_in, h->rank, bk, shrink_n / cs) != CUDA_SUCCESS) return LORA_ECUDA;
+        }
+        memcpy(hb + off_fused, sh.fused_groups.data(), (size_t)nft * sizeof(Tile));
+        memcpy(hb + off_shrink, sh.shrink_groups.data(), (size_t)nst * sizeof(Tile));
+        memcpy(hb + off_segoff, plan.seg_off.data(), 4 * (size_t)(n_m + 1));
+        memcpy(hb + off_segid, plan.seg_id.data(), 4 * (size_t)n_m);
+        float* sc = reinterpret_cast<float*>(hb + off_scale);
+        for (int k = 0; k < n_used; ++k) sc[k] = scale[plan.used_adapters[k]];
+        if (cudaMemcpyAsync(slot->dev, hb, used_bytes, cudaMemcpyHostToDevice, upload) != cudaSuccess)
+            return LORA_ECUDA;
+        if (x_src &&
+            cudaMemcpyAsync(const_cast<void*>(x), x_src, (size_t)T * h->d_in * 2, cudaMemcpyHostToDevice, upload) !=
+                cudaSuccess)
+            return LORA_ECUDA;
+        if (upload != stream &&
+            (cudaEventRecord(ready, upload) != cudaSuccess || cudaStreamWaitEvent(stream, ready, 0) != cudaSuccess))
+            return LORA_ECUDA;
+
+        p.tm_b = reinterpret_cast<const CUtensorMap*>(slot->dev + off_bmaps);
+        p.tm_a = reinterpret_cast<const CUtensorMap*>(slot->dev + off_amaps);
+        p.shrink_tiles = reinterpret_cast<const Tile*>(slot->dev + off_shrink);
+        p.fused_tiles = reinterpret_cast<const Tile*>(slot->dev + off_fused);
+        p.seg_off = reinterpret_cast<const int32_t*>(slot->dev + off_segoff);
+        p.seg_id = reinterpret_cast<const int32_t*>(slot->dev + off_segid);
+        p.scales = reinterpret_cast<const float*>(slot->dev + off_scale);
+    }
     if (encode_2d(h, &p.tm_x, x, h->d_in, T, bk, kTileM) != CUDA_SUCCESS) return LORA_ECUDA;
     if (encode_2d(h, &p.tm_w, W, h->d_in, h->d_out, bk, tile_n / cs) != CUDA_SUCCESS) return LORA_ECUDA;
     if (encode_2d(h, &p.tm_u, h->u_ws, h->rank, h->u_rows, bk, kTileM) != CUDA_SUCCESS) return LORA_ECUDA;
-    p.tm_b = reinterpret_cast<const CUtensorMap*>(slot->dev + off_bmaps);
-    p.tm_a = reinterpret_cast<const CUtensorMap*>(slot->dev + off_amaps);
-    p.shrink_tiles = reinterpret_cast<const Tile*>(slot->dev + off_shrink);
-    p.fused_tiles = reinterpret_cast<const Tile*>(slot->dev + off_fused);
-    p.seg_off = reinterpret_cast<const int32_t*>(slot->dev + off_segoff);
-    p.seg_id = reinterpret_cast<const int32_t*>(slot->dev + off_segid);
-    p.scales = reinterpret_cast<const float*>(slot->dev + off_scale);
     p.y = y;
     p.u = h->u_ws;
     p.status = h->status;
@@ -706,6 +739,16 @@ int forward_impl(lora_linear* h, const void* x, int T, const int32_t* seg_offset
     p.debug_stall = h->debug_stall;
     const int slots = cs > 1 ? max_clusters(h, p) : h->num_sms;
     if (slots < 1) return LORA_ECUDA;
+    // every tile the kernel will decode names a valid adapter slot and flag slot: the kernel
+    // indexes tensor maps and flags with them, so a malformed list must never reach it
+    for (const Tile& t : sh.fused_groups)
+        if (t.adapter < 0 || t.adapter > n_used || t.fused_index < 0 || t.fused_index >= nf ||
+            t.row0 < 0 || t.nrows < 0 || t.row0 + t.nrows > T)
+            return LORA_EINVAL;
+    for (const Tile& t : sh.shrink_groups)
+        if (t.adapter < 1 || t.adapter > n_used || t.fused_index < -1 || t.fused_index >= nf || t.row0 < 0 ||
+            t.nrows < 0 || t.row0 + t.nrows > T)
+            return LORA_EINVAL;
 
     TimingRec rec{};
     if (h->timing) {
@@ -743,8 +786,10 @@ int forward_impl(lora_linear* h, const void* x, int T, const int32_t* seg_offset
         cudaEventRecord(rec.ev[2], stream);
         h->trec.push_back(rec);
     }
-    if (cudaEventRecord(slot->done, stream) != cudaSuccess) return LORA_ECUDA;
-    slot->pending = true;
+    if (slot) {
+        if (cudaEventRecord(slot->done, stream) != cudaSuccess) return LORA_ECUDA;
+        slot->pending = true;
+    }
     return LORA_OK;
 }
 }  // namespace

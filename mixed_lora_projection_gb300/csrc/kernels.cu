@@ -355,11 +355,46 @@ struct Unit {
     int nk;          // k-blocks
 };
 
-__device__ __forceinline__ Unit decode_unit(const GemmParams& p, int u, int rank) {
+// The work list of a launch, in global memory or in the kernel parameters.
+struct WorkList {
+    const Tile* fused;
+    const Tile* shrink;
+    const int32_t* seg_off;
+    const int32_t* seg_id;
+    const float* scales;
+    const CUtensorMap* tm_a;
+    const CUtensorMap* tm_b;
+};
+
+__device__ __forceinline__ WorkList resolve_work_list(const GemmParams& p) {
+    WorkList wl;
+    if (p.inline_wl) {
+        // the offset is stored, not derived from n_fused: a launch of the shrink units alone
+        // runs with n_fused = 0 over the same list
+        wl.fused = p.inline_tiles;
+        wl.shrink = p.inline_tiles + p.inline_shrink_off;
+        wl.seg_off = p.inline_seg;
+        wl.seg_id = p.inline_seg + p.n_seg + 1;
+        wl.scales = p.inline_scales;
+        wl.tm_b = p.inline_maps;
+        wl.tm_a = p.inline_maps + kInlineAdapters;
+    } else {
+        wl.fused = p.fused_tiles;
+        wl.shrink = p.shrink_tiles;
+        wl.seg_off = p.seg_off;
+        wl.seg_id = p.seg_id;
+        wl.scales = p.scales;
+        wl.tm_b = p.tm_b;
+        wl.tm_a = p.tm_a;
+    }
+    return wl;
+}
+
+__device__ __forceinline__ Unit decode_unit(const GemmParams& p, const WorkList& wl, int u, int rank) {
     Unit r;
     const int cs = p.cluster_size;
     if (u < p.n_shrink) {
-        r.tile = p.shrink_tiles[u * cs + rank];
+        r.tile = wl.shrink[u * cs + rank];
         r.shrink = 1;
         r.tile_index = r.tile.fused_index;
         r.n0 = 0;
@@ -379,7 +414,7 @@ __device__ __forceinline__ Unit decode_unit(const GemmParams& p, int u, int rank
             ti = p.m_fastest ? (v % p.n_fused) : (v / p.n_ntiles);
             nt = p.m_fastest ? (v / p.n_fused) : (v % p.n_ntiles);
         }
-        r.tile = p.fused_tiles[ti * cs + rank];
+        r.tile = wl.fused[ti * cs + rank];
         r.shrink = 0;
         r.tile_index = r.tile.fused_index;
         r.n0 = nt * p.tile_n;
@@ -439,6 +474,7 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
 
     const int n_units = p.n_shrink + p.n_fused * p.n_ntiles;
     const uint64_t limit = p.wait_limit_ns;
+    const WorkList wl = resolve_work_list(p);
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
@@ -456,14 +492,17 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
             int acquired_a = -1, acquired_b = -1;  // adapters whose global tensor maps were acquired
             bool ok = true;
             for (int u = group; u < n_units && ok; u += n_groups) {
-                const Unit w = decode_unit(p, u, rank);
+                const Unit w = decode_unit(p, wl, u, rank);
                 const int ad = w.tile.adapter;
                 const CUtensorMap* bmain = &p.tm_w;
                 if (w.shrink) {
-                    bmain = &p.tm_a[ad - 1];
-                    if (acquired_a != ad) { tensormap_acquire(bmain); acquired_a = ad; }
+                    bmain = &wl.tm_a[ad - 1];
+                    if (acquired_a != ad) {
+                        if (!p.inline_wl) tensormap_acquire(bmain);
+                        acquired_a = ad;
+                    }
                 } else if (ad && acquired_b != ad) {
-                    tensormap_acquire(&p.tm_b[ad - 1]);
+                    if (!p.inline_wl) tensormap_acquire(&wl.tm_b[ad - 1]);
                     acquired_b = ad;
                 }
                 const int half = w.n / CG;                       // B rows this CTA loads
@@ -492,7 +531,7 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
                     const bool main = kb < p.k_main_blocks;
                     const int k = main ? kb * BK : (kb - p.k_main_blocks) * BK;
                     tma_load_2d<CG>(sa, main ? &p.tm_x : &p.tm_u, fb, k, w.tile.row0, issuer);
-                    tma_load_2d<CG>(sb, main ? bmain : &p.tm_b[ad - 1], fb, k, w.n0 + rank * half, issuer);
+                    tma_load_2d<CG>(sb, main ? bmain : &wl.tm_b[ad - 1], fb, k, w.n0 + rank * half, issuer);
                     ++issued;
                     if (++stage == stages) { stage = 0; phase ^= 1; }
                 }
@@ -525,7 +564,7 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
             int it = 0;
             bool ok = true;
             for (int u = group; u < n_units && ok; u += n_groups, ++it) {
-                const Unit w = decode_unit(p, u, rank);
+                const Unit w = decode_unit(p, wl, u, rank);
                 const uint32_t idesc = instr_desc_bf16(kTileM * CG, w.n);
                 const int acc = it & 1;
                 if (!wait_warp(smem_addr(&tempty[acc]), ((it >> 1) & 1) ^ 1, abort_flag, p.status, limit)) {
@@ -565,7 +604,7 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
         int it = 0;
         for (int u = group; u < n_units; u += n_groups, ++it) {
-            const Unit w = decode_unit(p, u, rank);
+            const Unit w = decode_unit(p, wl, u, rank);
             const int acc = it & 1;
             int ok = 1;
             if (lane == 0)
@@ -579,8 +618,8 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
             __nv_bfloat16* out;
             int n_out;
             if (w.shrink) {
-                const int a = row_ok ? row_adapter(p.seg_off, p.seg_id, p.n_seg, row) : 0;
-                scale = (a == w.tile.adapter) ? p.scales[w.tile.adapter - 1] : 0.0f;
+                const int a = row_ok ? row_adapter(wl.seg_off, wl.seg_id, p.n_seg, row) : 0;
+                scale = (a == w.tile.adapter) ? wl.scales[w.tile.adapter - 1] : 0.0f;
                 out = reinterpret_cast<__nv_bfloat16*>(p.u) + (size_t)row * p.rank;
                 n_out = p.rank;
             } else {

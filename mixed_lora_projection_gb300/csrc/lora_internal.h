@@ -18,6 +18,10 @@ constexpr int kMaxStages = 16;
 constexpr int kSmemLimit = 232448;                     // opt-in dynamic shared memory per CTA (227 KB)
 constexpr int kThreads = 192;        // warp 0 TMA, warp 1 MMA + TMEM owner, warps 2..5 epilogue
 constexpr int kEpilogueThreads = 128;
+// Work lists this small travel inside the kernel parameters (no upload copy per call).
+constexpr int kInlineTiles = 64;     // fused + shrink tiles (cluster groups included)
+constexpr int kInlineSegs = 48;      // merged segments
+constexpr int kInlineAdapters = 4;   // adapters named in the call
 
 struct Tile {                        // one planner tile, as uploaded to the device
     int32_t row0, nrows, adapter;    // adapter: compact slot (1-based), 0 = none
@@ -35,6 +39,14 @@ struct Tile {                        // one planner tile, as uploaded to the dev
 // When `flags` is set, a fused unit's expand waits until flags[tile] == epoch, which the
 // shrink unit of that tile publishes after its U rows are stored (single-launch mode).
 struct GemmParams {
+    // inline work list (used when inline_wl != 0): adapter tensor maps (B_a at [0, 4), A_a
+    // at [4, 8)), tiles (fused then shrink), merged segments (offsets then ids), scales
+    CUtensorMap inline_maps[2 * kInlineAdapters];
+    Tile inline_tiles[kInlineTiles];
+    int32_t inline_seg[2 * kInlineSegs + 1];
+    float inline_scales[kInlineAdapters];
+    int inline_wl;
+    int inline_shrink_off;           // index of the first shrink tile in inline_tiles
     CUtensorMap tm_x;                // X [T, d_in], box 64 x 128
     CUtensorMap tm_w;                // W [d_out, d_in], box 64 x tile_n
     CUtensorMap tm_u;                // U [u_rows, rank], box 64 x 128

@@ -194,6 +194,21 @@ def test_k_step_32_equals_64(dev, name):
     assert torch.equal(y64, y32)
 
 
+@pytest.mark.parametrize("name", ["tiny", "sweep_qkv_multi", "mixed_decode", "mixed_near_ridge"])
+def test_inline_work_list_equals_uploaded(dev, name):
+    # small work lists travel in the kernel parameters; the result equals the uploaded path
+    from mixed_lora_projection_gb300 import _lib as L
+    w = WORKLOADS[name]
+    inp = make_inputs(w, dev)
+    with _ll(w) as ll:
+        y1 = run(ll, inp, w.seg_offsets, w.seg_ids).clone()
+        ll.set_option(L.OPT_INLINE_WORK_LIST, 0)
+        y2 = run(ll, inp, w.seg_offsets, w.seg_ids)
+        torch.cuda.synchronize()
+        assert ll.status() == 0
+    assert torch.equal(y1, y2)
+
+
 def test_repeated_calls_reuse_flags(dev):
     # many calls in a row on one handle: the epoch-tagged ready flags never go stale
     w = WORKLOADS["sweep_o_multi"]
