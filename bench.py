@@ -173,7 +173,7 @@ def aggregate_ranks(elapsed_ms, e2e_ms, flops_per_step, steps, world, dist):
 def run_ours(args, rank, world, dist):
     import torch
     from mixed_lora_projection_gb300 import LoraLinear, _lib as L
-    from mixed_lora_projection_gb300.synth import make_inputs
+    from mixed_lora_projection_gb300.synth import make_inputs, make_w4_base
 
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
@@ -188,6 +188,9 @@ def run_ours(args, rank, world, dist):
             if args.two_launch:
                 handles[key].set_option(L.OPT_TWO_LAUNCH, 1)
         copies = [make_inputs(w, dev, layer=layer, proj_index=pi + 4 * c, with_x=(c == 0)) for c in range(n_copies)]
+        if args.w4:
+            for c, inp in enumerate(copies):
+                inp.w = make_w4_base(w, dev, layer=layer, proj_index=pi + 4 * c)
         y = torch.empty((w.T, w.d_out), dtype=torch.bfloat16, device=dev)
         setups.append((w, handles[key], copies, y))
     stream = torch.cuda.current_stream(dev)
@@ -195,7 +198,11 @@ def run_ours(args, rank, world, dist):
     def step(i):
         for (w, ll, copies, y) in setups:
             c = copies[i % len(copies)]
-            ll.forward(copies[0].x, w.seg_offsets, w.seg_ids, c.w, c.a, c.b, c.scales, y=y, stream=stream)
+            if args.w4:
+                ll.forward_w4(copies[0].x, w.seg_offsets, w.seg_ids, c.w[0], c.w[1], c.a, c.b, c.scales, y=y,
+                              stream=stream)
+            else:
+                ll.forward(copies[0].x, w.seg_offsets, w.seg_ids, c.w, c.a, c.b, c.scales, y=y, stream=stream)
 
     for i in range(args.warmup):
         step(i)
@@ -240,7 +247,11 @@ def run_ours(args, rank, world, dist):
     def e2e_step(i):
         for j, (w, ll, copies, y) in enumerate(setups):
             c = copies[i % len(copies)]
-            ll.forward_host(x_host[j], w.seg_offsets, w.seg_ids, c.w, c.a, c.b, c.scales, y_host[j], stream=stream)
+            if args.w4:
+                ll.forward_host_w4(x_host[j], w.seg_offsets, w.seg_ids, c.w[0], c.w[1], c.a, c.b, c.scales, y_host[j],
+                                   stream=stream)
+            else:
+                ll.forward_host(x_host[j], w.seg_offsets, w.seg_ids, c.w, c.a, c.b, c.scales, y_host[j], stream=stream)
 
     for i in range(min(args.warmup, 3)):
         e2e_step(i)
@@ -265,14 +276,15 @@ def run_ours(args, rank, world, dist):
     fused_flops = sum((_fused_flops(w) if shrink_n else w.useful_flops()) for w, _, _ in items)
     avg_fused_ms = fused_ms / args.steps if fused_n else None  # device time of the fused launches per step
     achieved = fused_flops / (avg_fused_ms * 1e-3) / 1e12 if avg_fused_ms else None
-    traffic = _profiled_traffic(args.workload)
+    traffic = _profiled_traffic(args.workload + ("+w4" if args.w4 else ""))
     w0 = items[0][0]
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded Gaussian bf16; no checkpoint)",
-        "config": {"workload": args.workload, "T": w0.T, "d_in": w0.d_in if len(items) == 1 else "per projection",
+        "config": {"workload": args.workload + ("+w4" if args.w4 else ""),
+                   "base": "int4 (symmetric, group 128, bf16 scales)" if args.w4 else "bf16", "T": w0.T, "d_in": w0.d_in if len(items) == 1 else "per projection",
                    "d_out": w0.d_out if len(items) == 1 else "per projection", "rank": w0.rank,
                    "segments": len(w0.seg_ids), "adapter_rows": w0.adapter_rows, "calls_per_step": len(items),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
@@ -295,10 +307,13 @@ def run_ours(args, rank, world, dist):
         "clocks": sampler.summary(t0, t1),
     }
     if w0.T <= 512 and len(items) == 1:
-        gbs = w0.algorithmic_bytes() / (avg_fused_ms * 1e-3) / 1e9 if avg_fused_ms else None
+        alg = w0.algorithmic_bytes()
+        if args.w4:   # packed weights (half a byte) and bf16 scales instead of bf16 W
+            alg += -2.0 * w0.d_out * w0.d_in + 0.5 * w0.d_out * w0.d_in + 2.0 * w0.d_out * w0.d_in / 128
+        gbs = alg / (avg_fused_ms * 1e-3) / 1e9 if avg_fused_ms else None
         out["roofline_hbm"] = {"bound": "hbm", "achieved": round(gbs, 1) if gbs else None, "peak": hbm,
                                "unit": "GB/s", "frac": round(gbs / hbm, 4) if gbs else None,
-                               "algorithmic_bytes": w0.algorithmic_bytes()}
+                               "algorithmic_bytes": alg}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(items, args.cpu_seconds)
     for ll in handles.values():
@@ -400,6 +415,7 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--two-launch", action="store_true", help="shrink as its own launch (for comparison)")
+    ap.add_argument("--w4", action="store_true", help="4-bit base weights (int4, group 128, bf16 scales)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

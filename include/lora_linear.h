@@ -114,6 +114,34 @@ int lora_linear_forward_host(lora_linear* h, const void* x_host, int T,
                              const void* W, const void* const* A, const void* const* B,
                              const float* scale, int n_adapters, void* y_host, void* stream);
 
+/*
+ * lora_linear_forward_w4 -- lora_linear_forward with a 4-bit base weight.
+ *   Wq  device uint8 [d_out, d_in / 2]: signed 4-bit weights (two's complement nibbles);
+ *       byte j of row n holds input feature 2j in its low nibble and 2j + 1 in its high one.
+ *   Ws  device bf16 [d_in / 128, d_out]: one scale per output row and group of 128 inputs.
+ *   The base weight is W[n, k] = q[n, k] * Ws[k / 128, n]; on the GPU each weight is
+ *   rounded to bf16 (round to nearest even) before the bf16 tensor-core product. The
+ *   adapters (A, B) stay bf16. Requires d_in to be a multiple of 128 (else LORA_EINVAL);
+ *   all other arguments, layouts and errors as lora_linear_forward.
+ * Source: "Two 27B models on a single RTX 5090", section 4 (the memory budget: a 4-bit base
+ * of 18.1 GiB with a bf16 adapter of 1.3 GiB) and "Qwen3.8-27B on one RTX 3090 with patched
+ * vLLM + DFlash2" (the W4A16 base); the group size and symmetric form are this library's.
+ */
+int lora_linear_forward_w4(lora_linear* h, const void* x, int T,
+                           const int32_t* seg_offsets, const int32_t* seg_adapter_ids, int n_seg,
+                           const void* Wq, const void* Ws, const void* const* A, const void* const* B,
+                           const float* scale, int n_adapters, void* y, void* stream);
+
+/*
+ * lora_linear_forward_host_w4 -- lora_linear_forward_host with the 4-bit base of
+ * lora_linear_forward_w4 (Wq, Ws device pointers; X and Y host buffers).
+ * Source: as lora_linear_forward_w4.
+ */
+int lora_linear_forward_host_w4(lora_linear* h, const void* x_host, int T,
+                                const int32_t* seg_offsets, const int32_t* seg_adapter_ids, int n_seg,
+                                const void* Wq, const void* Ws, const void* const* A, const void* const* B,
+                                const float* scale, int n_adapters, void* y_host, void* stream);
+
 /* lora_linear_destroy -- wait for the handle's work, free everything it owns. NULL-safe. */
 int lora_linear_destroy(lora_linear* h);
 

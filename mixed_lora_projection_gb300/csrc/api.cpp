@@ -154,10 +154,21 @@ CUresult encode_2d(lora_linear* h, CUtensorMap* m, const void* ptr, uint64_t inn
 }
 
 // Deepest ring that fits the opt-in shared memory, for `b_rows` B rows per CTA.
-int stages_for(int b_rows, int bk) {
+int stages_for(int b_rows, int bk, int w4_rows = 0) {
     int s = kMaxStages;
-    while (s > 2 && gemm_smem_bytes(b_rows, s, bk) > (size_t)kSmemLimit) --s;
+    while (s > 2 && gemm_smem_bytes(b_rows, s, bk, w4_rows) > (size_t)kSmemLimit) --s;
     return s;
+}
+
+// 2-D map without swizzle (the 4-bit base's packed rows and scales).
+CUresult encode_plain_2d(lora_linear* h, CUtensorMap* m, CUtensorMapDataType dtype, int elem_bytes,
+                         const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_inner, uint32_t box_outer) {
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {inner * (uint64_t)elem_bytes};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    return h->encode(m, dtype, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
 // Output-tile width: the per-SM critical path is (waves x (tile_n + fixed cost)); narrow
@@ -349,10 +360,11 @@ const char* lora_linear_error_string(int code) {
     }
 }
 
-int lora_linear_validate(int d_in, int d_out, int rank, int max_tokens, int max_segments,
-                         const void* x, int T, const int32_t* seg_offsets,
-                         const int32_t* seg_adapter_ids, int n_seg, const void* W,
-                         const void* const* A, const void* const* B, const float* scale,
+}  // extern "C"
+
+static int validate_impl(int d_in, int d_out, int rank, int max_tokens, int max_segments, const void* x, int T,
+                         const int32_t* seg_offsets, const int32_t* seg_adapter_ids, int n_seg, const void* W,
+                         size_t w_bytes, const void* const* A, const void* const* B, const float* scale,
                          int n_adapters, const void* y) {
     int rc = check_shape(d_in, d_out, rank, max_tokens, max_segments);
     if (rc != LORA_OK) return rc;
@@ -370,7 +382,7 @@ int lora_linear_validate(int d_in, int d_out, int rank, int max_tokens, int max_
     if (n_seg < 1 || !seg_offsets || !seg_adapter_ids) return LORA_EINVAL;
     if (!x || !y || !W || !aligned16(x) || !aligned16(y) || !aligned16(W)) return LORA_EINVAL;
     if (seg_offsets[0] != 0 || seg_offsets[n_seg] != T) return LORA_EINVAL;
-    const size_t xb = (size_t)T * d_in * 2, yb = (size_t)T * d_out * 2, wb = (size_t)d_out * d_in * 2;
+    const size_t xb = (size_t)T * d_in * 2, yb = (size_t)T * d_out * 2, wb = w_bytes;
     const size_t ab = (size_t)rank * d_in * 2, bb = (size_t)d_out * rank * 2;
     if (overlaps(y, yb, x, xb) || overlaps(y, yb, W, wb)) return LORA_EINVAL;
     for (int i = 0; i < n_seg; ++i) {
@@ -386,6 +398,17 @@ int lora_linear_validate(int d_in, int d_out, int rank, int max_tokens, int max_
         if (overlaps(y, yb, pa, ab) || overlaps(y, yb, pb, bb)) return LORA_EINVAL;
     }
     return LORA_OK;
+}
+
+extern "C" {
+
+int lora_linear_validate(int d_in, int d_out, int rank, int max_tokens, int max_segments,
+                         const void* x, int T, const int32_t* seg_offsets,
+                         const int32_t* seg_adapter_ids, int n_seg, const void* W,
+                         const void* const* A, const void* const* B, const float* scale,
+                         int n_adapters, const void* y) {
+    return validate_impl(d_in, d_out, rank, max_tokens, max_segments, x, T, seg_offsets, seg_adapter_ids, n_seg, W,
+                         (size_t)d_out * d_in * 2, A, B, scale, n_adapters, y);
 }
 
 int lora_linear_create(lora_linear** out, int d_in, int d_out, int rank, int max_tokens,
@@ -609,10 +632,13 @@ namespace {
 int forward_impl(lora_linear* h, const void* x, int T, const int32_t* seg_offsets,
                  const int32_t* seg_adapter_ids, int n_seg, const void* W, const void* const* A,
                  const void* const* B, const float* scale, int n_adapters, void* y, cudaStream_t stream,
-                 cudaStream_t upload, const void* x_src, cudaEvent_t ready) {
+                 cudaStream_t upload, const void* x_src, cudaEvent_t ready, const void* Wq = nullptr,
+                 const void* Ws = nullptr) {
     if (!h) return LORA_EINVAL;
-    int rc = lora_linear_validate(h->d_in, h->d_out, h->rank, h->max_tokens, h->max_segments, x, T,
-                                  seg_offsets, seg_adapter_ids, n_seg, W, A, B, scale, n_adapters, y);
+    int rc = validate_impl(h->d_in, h->d_out, h->rank, h->max_tokens, h->max_segments, x, T, seg_offsets,
+                           seg_adapter_ids, n_seg, Wq ? Wq : W,
+                           Wq ? (size_t)h->d_out * h->d_in / 2 : (size_t)h->d_out * h->d_in * 2, A, B, scale,
+                           n_adapters, y);
     if (rc != LORA_OK) return rc;
     if (T == 0) return LORA_OK;
     Plan plan;
@@ -631,7 +657,13 @@ int forward_impl(lora_linear* h, const void* x, int T, const int32_t* seg_offset
     for (size_t i = 0; i < plan.fused.size(); ++i) plan.fused[i].fused_index = (int32_t)i;
 
     DeviceGuard guard(h->device);
-    const Shape sh = choose_shape(h, plan);
+    const bool w4 = Wq != nullptr;
+    Shape sh = choose_shape(h, plan);
+    if (w4) {
+        // 64-wide K-steps (32 packed bytes per row) and room for the packed staging ring
+        sh.bk = 64;
+        sh.stages = stages_for(std::max(sh.tile_n, sh.shrink_n) / sh.cs, 64, sh.tile_n / sh.cs);
+    }
     const int cs = sh.cs, tile_n = sh.tile_n, shrink_n = sh.shrink_n, bk = sh.bk;
     const int nfg = (int)sh.fused_groups.size() / cs, nsg = (int)sh.shrink_groups.size() / cs;
     const int nft = (int)sh.fused_groups.size(), nst = (int)sh.shrink_groups.size();
@@ -714,7 +746,16 @@ int forward_impl(lora_linear* h, const void* x, int T, const int32_t* seg_offset
         p.scales = reinterpret_cast<const float*>(slot->dev + off_scale);
     }
     if (encode_2d(h, &p.tm_x, x, h->d_in, T, bk, kTileM) != CUDA_SUCCESS) return LORA_ECUDA;
-    if (encode_2d(h, &p.tm_w, W, h->d_in, h->d_out, bk, tile_n / cs) != CUDA_SUCCESS) return LORA_ECUDA;
+    if (w4) {
+        if (encode_plain_2d(h, &p.tm_wq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, Wq, (uint64_t)h->d_in / 2, h->d_out,
+                            bk / 2, tile_n / cs) != CUDA_SUCCESS ||
+            encode_plain_2d(h, &p.tm_ws, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Ws, h->d_out,
+                            (uint64_t)h->d_in / kW4Group, tile_n / cs, 1) != CUDA_SUCCESS)
+            return LORA_ECUDA;
+        p.w4 = 1;
+    } else if (encode_2d(h, &p.tm_w, W, h->d_in, h->d_out, bk, tile_n / cs) != CUDA_SUCCESS) {
+        return LORA_ECUDA;
+    }
     if (encode_2d(h, &p.tm_u, h->u_ws, h->rank, h->u_rows, bk, kTileM) != CUDA_SUCCESS) return LORA_ECUDA;
     p.y = y;
     p.u = h->u_ws;
@@ -805,9 +846,29 @@ int lora_linear_forward(lora_linear* h, const void* x, int T, const int32_t* seg
                         stream, nullptr, nullptr);
 }
 
-int lora_linear_forward_host(lora_linear* h, const void* x_host, int T, const int32_t* seg_offsets,
-                             const int32_t* seg_adapter_ids, int n_seg, const void* W,
-                             const void* const* A, const void* const* B, const float* scale,
+int lora_linear_forward_w4(lora_linear* h, const void* x, int T, const int32_t* seg_offsets,
+                           const int32_t* seg_adapter_ids, int n_seg, const void* Wq, const void* Ws,
+                           const void* const* A, const void* const* B, const float* scale, int n_adapters,
+                           void* y, void* stream_) {
+    if (!h) return LORA_EINVAL;
+    if (h->d_in % kW4Group) return LORA_EINVAL;
+    if (T > 0) {
+        if (!Wq || !Ws || !aligned16(Wq) || !aligned16(Ws)) return LORA_EINVAL;
+        const size_t yb = (size_t)T * h->d_out * 2;
+        if (overlaps(y, yb, Wq, (size_t)h->d_out * h->d_in / 2) ||
+            overlaps(y, yb, Ws, (size_t)(h->d_in / kW4Group) * h->d_out * 2))
+            return LORA_EINVAL;
+    }
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    return forward_impl(h, x, T, seg_offsets, seg_adapter_ids, n_seg, nullptr, A, B, scale, n_adapters, y, stream,
+                        stream, nullptr, nullptr, Wq, Ws);
+}
+
+}  // extern "C"
+
+static int forward_host_impl(lora_linear* h, const void* x_host, int T, const int32_t* seg_offsets,
+                             const int32_t* seg_adapter_ids, int n_seg, const void* W, const void* Wq,
+                             const void* Ws, const void* const* A, const void* const* B, const float* scale,
                              int n_adapters, void* y_host, void* stream_) {
     if (!h) return LORA_EINVAL;
     if (T < 0 || T > h->max_tokens) return LORA_EINVAL;
@@ -870,7 +931,8 @@ int lora_linear_forward_host(lora_linear* h, const void* x_host, int T, const in
         // work list (on s_in, planned and uploaded by forward_impl), then X rows, both
         // ordered before the event the kernel waits on
         rc = forward_impl(h, xd + (size_t)a * xrow, n, off.data(), ids.data(), (int)ids.size(), W, A, B, scale,
-                          n_adapters, yd + (size_t)a * yrow, stream, h->s_in, xh + (size_t)a * xrow, h->ev_in[e]);
+                          n_adapters, yd + (size_t)a * yrow, stream, h->s_in, xh + (size_t)a * xrow, h->ev_in[e],
+                          Wq, Ws);
         if (rc != LORA_OK) return rc;
         if (n > 0) {
             if (cudaEventRecord(h->ev_done[e], stream) != cudaSuccess ||
@@ -887,6 +949,28 @@ int lora_linear_forward_host(lora_linear* h, const void* x_host, int T, const in
     if (cudaMemcpy(h->status_host, h->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
         return LORA_ECUDA;
     return *h->status_host ? LORA_ETIMEOUT : LORA_OK;
+}
+
+
+extern "C" {
+
+int lora_linear_forward_host(lora_linear* h, const void* x_host, int T, const int32_t* seg_offsets,
+                             const int32_t* seg_adapter_ids, int n_seg, const void* W,
+                             const void* const* A, const void* const* B, const float* scale,
+                             int n_adapters, void* y_host, void* stream) {
+    return forward_host_impl(h, x_host, T, seg_offsets, seg_adapter_ids, n_seg, W, nullptr, nullptr, A, B, scale,
+                             n_adapters, y_host, stream);
+}
+
+int lora_linear_forward_host_w4(lora_linear* h, const void* x_host, int T, const int32_t* seg_offsets,
+                                const int32_t* seg_adapter_ids, int n_seg, const void* Wq, const void* Ws,
+                                const void* const* A, const void* const* B, const float* scale, int n_adapters,
+                                void* y_host, void* stream) {
+    if (!h) return LORA_EINVAL;
+    if (h->d_in % kW4Group) return LORA_EINVAL;
+    if (T > 0 && (!Wq || !Ws || !aligned16(Wq) || !aligned16(Ws))) return LORA_EINVAL;
+    return forward_host_impl(h, x_host, T, seg_offsets, seg_adapter_ids, n_seg, nullptr, Wq, Ws, A, B, scale,
+                             n_adapters, y_host, stream);
 }
 
 }  // extern "C"

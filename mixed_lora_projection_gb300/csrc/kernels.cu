@@ -424,8 +424,10 @@ __device__ __forceinline__ Unit decode_unit(const GemmParams& p, const WorkList&
     return r;
 }
 
-template <int BK, int CG>
-__global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_constant__ GemmParams p) {
+template <int BK, int CG, int QW>
+__global__ void __launch_bounds__(QW ? kThreadsW4 : kThreads, 1)
+    lora_gemm_kernel(const __grid_constant__ GemmParams p) {
+    static_assert(!QW || BK == 64, "the 4-bit base uses 64-wide K-steps (32 packed bytes per row)");
     constexpr uint32_t kStageA = kTileM * BK * 2;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // carve: rings (1024-aligned), then barriers, then the TMEM slot and the abort flag
@@ -436,10 +438,17 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
     const uint32_t b_stage_bytes = (uint32_t)b_rows * BK * 2;
     uint8_t* a_ring = base;
     uint8_t* b_ring = a_ring + (size_t)stages * kStageA;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(b_ring + (size_t)stages * b_stage_bytes);
+    // 4-bit base: staging rings of the packed tile (32 bytes per row) and its scales
+    const int q_rows = QW ? p.tile_n / CG : 0;
+    const uint32_t q_stage_bytes = (uint32_t)q_rows * (BK / 2);
+    const uint32_t s_stage_bytes = ((uint32_t)q_rows * 2 + 127u) & ~127u;
+    uint8_t* q_ring = b_ring + (size_t)stages * b_stage_bytes;
+    uint8_t* s_ring = q_ring + (size_t)stages * q_stage_bytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(s_ring + (size_t)stages * s_stage_bytes);
     uint64_t* full = bars;
     uint64_t* empty = full + stages;
-    uint64_t* tfull = empty + stages;
+    uint64_t* pfull = empty + stages;
+    uint64_t* tfull = pfull + stages;
     uint64_t* tempty = tfull + 2;
     uint64_t* drain = tempty + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -454,8 +463,10 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
-            mbar_init(smem_addr(&full[s]), 1);
+            // the producer's arrive, plus one arrive per converter warp of each CTA of the group
+            mbar_init(smem_addr(&full[s]), 1 + (QW ? CG * (kConvertThreads / 32) : 0));
             mbar_init(smem_addr(&empty[s]), 1);
+            mbar_init(smem_addr(&pfull[s]), 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(smem_addr(&tfull[a]), 1);
@@ -483,7 +494,11 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
         if (!p.debug_stall) {
             if (lane == 0) {
                 tma_prefetch_desc(&p.tm_x);
-                if (p.n_fused) { tma_prefetch_desc(&p.tm_w); tma_prefetch_desc(&p.tm_u); }
+                if (p.n_fused) {
+                    tma_prefetch_desc(QW ? &p.tm_wq : &p.tm_w);
+                    if (QW) tma_prefetch_desc(&p.tm_ws);
+                    tma_prefetch_desc(&p.tm_u);
+                }
             }
             __syncwarp();
             int stage = 0;
@@ -508,6 +523,11 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
                 const int half = w.n / CG;                       // B rows this CTA loads
                 // bytes the (even CTA's) full barrier receives per stage, from the whole group
                 const uint32_t tx = CG * (kStageA + (uint32_t)half * BK * 2);
+                // 4-bit base: TMA brings only A to the full barrier; the B tile of a base step
+                // comes from the converter warps, its packed form lands on pfull
+                const bool w4_unit = QW && !w.shrink;
+                const uint32_t tx_w4 = CG * kStageA;
+                const uint32_t ptx = (uint32_t)half * (BK / 2) + (uint32_t)half * 2;
                 for (int kb = 0; kb < w.nk; ++kb) {
                     if (kb == p.k_main_blocks && p.flags) {
                         // the expand reads U rows written by this tile's shrink unit
@@ -524,14 +544,25 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
                         break;
                     }
                     const uint32_t fb_local = smem_addr(&full[stage]);
-                    mbar_arrive_expect_tx(fb_local, tx, leader ? issuer : 0u);
+                    const bool main = kb < p.k_main_blocks;
+                    const bool w4_step = w4_unit && main;
+                    mbar_arrive_expect_tx(fb_local, w4_step ? tx_w4 : tx, leader ? issuer : 0u);
                     const uint32_t fb = CG > 1 ? map_to_rank(fb_local, 0) : fb_local;
                     const uint32_t sa = smem_addr(a_ring + (size_t)stage * kStageA);
                     const uint32_t sb = smem_addr(b_ring + (size_t)stage * b_stage_bytes);
-                    const bool main = kb < p.k_main_blocks;
                     const int k = main ? kb * BK : (kb - p.k_main_blocks) * BK;
                     tma_load_2d<CG>(sa, main ? &p.tm_x : &p.tm_u, fb, k, w.tile.row0, issuer);
-                    tma_load_2d<CG>(sb, main ? bmain : &wl.tm_b[ad - 1], fb, k, w.n0 + rank * half, issuer);
+                    if (w4_step) {
+                        // packed rows and this K-step's scales, into this CTA's staging ring
+                        const uint32_t pb = smem_addr(&pfull[stage]);
+                        mbar_arrive_expect_tx(pb, ptx, issuer);
+                        tma_load_2d<1>(smem_addr(q_ring + (size_t)stage * q_stage_bytes), &p.tm_wq, pb, kb * (BK / 2),
+                                       w.n0 + rank * half, issuer);
+                        tma_load_2d<1>(smem_addr(s_ring + (size_t)stage * s_stage_bytes), &p.tm_ws, pb,
+                                       w.n0 + rank * half, (kb * BK) / kW4Group, issuer);
+                    } else {
+                        tma_load_2d<CG>(sb, main ? bmain : &wl.tm_b[ad - 1], fb, k, w.n0 + rank * half, issuer);
+                    }
                     ++issued;
                     if (++stage == stages) { stage = 0; phase ^= 1; }
                 }
@@ -596,6 +627,71 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
             // every MMA this warp issued has completed before TMEM is released
             mma_commit_local<CG>(smem_addr(drain), issuer);
             if (lane == 0) wait_bounded(smem_addr(drain), 0, abort_flag, p.status, limit, false);
+        }
+    } else if (QW && warp >= 6) {
+        // ------------------------------------------------------------ 4-bit converter (warps 6..9)
+        // Base K-steps of fused units: packed int4 rows + scales (staging ring) -> bf16 B tile in
+        // the 128-byte-swizzled layout the MMA reads. W[n,k] = q * s, q = signed nibble (low
+        // nibble = even k); (128 + (q ^ 8) - 136) is q exactly, then one RNE multiply by s.
+        // Other K-steps (expand, shrink) load B by TMA; the converters only count themselves in.
+        const int ct = threadIdx.x - 6 * 32;
+        const uint32_t full_target_rank = 0;
+        const __nv_bfloat162 magic = __floats2bfloat162_rn(136.0f, 136.0f);
+        int stage = 0;
+        uint32_t phase = 0, pbits = 0;
+        bool ok = true;
+        for (int u = group; u < n_units && ok; u += n_groups) {
+            const Unit w = decode_unit(p, wl, u, rank);
+            const bool w4_unit = !w.shrink;
+            const int rows = w.n / CG;
+            for (int kb = 0; kb < w.nk; ++kb) {
+                if (!wait_warp(smem_addr(&empty[stage]), phase ^ 1, abort_flag, p.status, limit)) {
+                    ok = false;
+                    break;
+                }
+                if (w4_unit && kb < p.k_main_blocks) {
+                    if (!wait_warp(smem_addr(&pfull[stage]), (pbits >> stage) & 1u, abort_flag, p.status, limit)) {
+                        ok = false;
+                        break;
+                    }
+                    pbits ^= 1u << stage;
+                    const uint8_t* qs = q_ring + (size_t)stage * q_stage_bytes;
+                    const __nv_bfloat16* ss = reinterpret_cast<const __nv_bfloat16*>(s_ring + (size_t)stage * s_stage_bytes);
+                    uint8_t* bs = b_ring + (size_t)stage * b_stage_bytes;
+                    for (int r = ct; r < rows; r += kConvertThreads) {
+                        const uint4 q0 = *reinterpret_cast<const uint4*>(qs + (size_t)r * 32);
+                        const uint4 q1 = *reinterpret_cast<const uint4*>(qs + (size_t)r * 32 + 16);
+                        const __nv_bfloat162 s2 = __bfloat162bfloat162(ss[r]);
+                        const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) {
+                            const uint32_t wv = words[c] ^ 0x88888888u;  // nibbles to offset binary q + 8
+                            uint32_t o[4];
+#pragma unroll
+                            for (int pp = 0; pp < 4; ++pp) {
+                                const uint32_t v = ((wv >> (8 * pp)) & 0xFu) | (((wv >> (8 * pp + 4)) & 0xFu) << 16) |
+                                                   0x43004300u;  // bf16 pair 128 + (q + 8)
+                                __nv_bfloat162 t = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&v), magic);
+                                t = __hmul2(t, s2);
+                                o[pp] = *reinterpret_cast<const uint32_t*>(&t);
+                            }
+                            *reinterpret_cast<uint4*>(bs + (size_t)r * 128 + (((uint32_t)c ^ ((uint32_t)r & 7u)) << 4)) =
+                                make_uint4(o[0], o[1], o[2], o[3]);
+                        }
+                    }
+                    // generic stores -> visible to the tensor core (async proxy) before the arrive
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                }
+                __syncwarp();
+                if (lane == 0) {
+                    const uint32_t fb_local = smem_addr(&full[stage]);
+                    if (CG > 1)
+                        mbar_arrive_cluster(map_to_rank(fb_local, full_target_rank));
+                    else
+                        mbar_arrive(fb_local);
+                }
+                if (++stage == stages) { stage = 0; phase ^= 1; }
+            }
         }
     } else {
         // ------------------------------------------------------------ epilogue (warps 2..5)
@@ -676,23 +772,26 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
 
 }  // namespace dev
 
-size_t gemm_smem_bytes(int b_tile_rows, int stages, int bk) {
-    return 1024 + (size_t)stages * ((size_t)kTileM * bk * 2 + (size_t)b_tile_rows * bk * 2) +
-           8 * (2 * (size_t)stages + 5) + 16;
+size_t gemm_smem_bytes(int b_tile_rows, int stages, int bk, int w4_rows) {
+    const size_t w4 = w4_rows ? (size_t)w4_rows * (bk / 2) + (((size_t)w4_rows * 2 + 127) & ~(size_t)127) : 0;
+    return 1024 + (size_t)stages * ((size_t)kTileM * bk * 2 + (size_t)b_tile_rows * bk * 2 + w4) +
+           8 * (3 * (size_t)stages + 5) + 16;
 }
 
-template <int BK, int CG>
+template <int BK, int CG, int QW>
 static cudaError_t set_smem_attr() {
-    return cudaFuncSetAttribute(dev::lora_gemm_kernel<BK, CG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    return cudaFuncSetAttribute(dev::lora_gemm_kernel<BK, CG, QW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 kSmemLimit);
 }
 
 cudaError_t gemm_prepare_device() {
     cudaError_t e;
-    if ((e = set_smem_attr<64, 1>()) != cudaSuccess) return e;
-    if ((e = set_smem_attr<64, 2>()) != cudaSuccess) return e;
-    if ((e = set_smem_attr<32, 1>()) != cudaSuccess) return e;
-    return set_smem_attr<32, 2>();
+    if ((e = set_smem_attr<64, 1, 0>()) != cudaSuccess) return e;
+    if ((e = set_smem_attr<64, 2, 0>()) != cudaSuccess) return e;
+    if ((e = set_smem_attr<32, 1, 0>()) != cudaSuccess) return e;
+    if ((e = set_smem_attr<32, 2, 0>()) != cudaSuccess) return e;
+    if ((e = set_smem_attr<64, 1, 1>()) != cudaSuccess) return e;
+    return set_smem_attr<64, 2, 1>();
 }
 
 static void launch_config(const GemmParams& p, int grid, cudaStream_t stream, cudaLaunchConfig_t* cfg,
@@ -700,8 +799,8 @@ static void launch_config(const GemmParams& p, int grid, cudaStream_t stream, cu
     const int b_rows = (p.tile_n > p.shrink_n ? p.tile_n : p.shrink_n) / p.cluster_size;
     memset(cfg, 0, sizeof(*cfg));
     cfg->gridDim = dim3(grid, 1, 1);
-    cfg->blockDim = dim3(kThreads, 1, 1);
-    cfg->dynamicSmemBytes = gemm_smem_bytes(b_rows, p.stages, p.bk);
+    cfg->blockDim = dim3(p.w4 ? kThreadsW4 : kThreads, 1, 1);
+    cfg->dynamicSmemBytes = gemm_smem_bytes(b_rows, p.stages, p.bk, p.w4 ? p.tile_n / p.cluster_size : 0);
     cfg->stream = stream;
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = p.cluster_size;
@@ -713,10 +812,15 @@ static void launch_config(const GemmParams& p, int grid, cudaStream_t stream, cu
 
 template <typename F>
 static cudaError_t dispatch(const GemmParams& p, F&& f) {
-    if (p.bk == 64 && p.cluster_size == 1) return f(dev::lora_gemm_kernel<64, 1>);
-    if (p.bk == 64 && p.cluster_size == 2) return f(dev::lora_gemm_kernel<64, 2>);
-    if (p.bk == 32 && p.cluster_size == 1) return f(dev::lora_gemm_kernel<32, 1>);
-    if (p.bk == 32 && p.cluster_size == 2) return f(dev::lora_gemm_kernel<32, 2>);
+    if (p.w4) {
+        if (p.bk == 64 && p.cluster_size == 1) return f(dev::lora_gemm_kernel<64, 1, 1>);
+        if (p.bk == 64 && p.cluster_size == 2) return f(dev::lora_gemm_kernel<64, 2, 1>);
+        return cudaErrorInvalidValue;
+    }
+    if (p.bk == 64 && p.cluster_size == 1) return f(dev::lora_gemm_kernel<64, 1, 0>);
+    if (p.bk == 64 && p.cluster_size == 2) return f(dev::lora_gemm_kernel<64, 2, 0>);
+    if (p.bk == 32 && p.cluster_size == 1) return f(dev::lora_gemm_kernel<32, 1, 0>);
+    if (p.bk == 32 && p.cluster_size == 2) return f(dev::lora_gemm_kernel<32, 2, 0>);
     return cudaErrorInvalidValue;
 }
 

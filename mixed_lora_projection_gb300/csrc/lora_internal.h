@@ -17,7 +17,10 @@ constexpr int kStageBytesA = kTileM * kTileK * 2;      // 16 KB at K = 64
 constexpr int kMaxStages = 16;
 constexpr int kSmemLimit = 232448;                     // opt-in dynamic shared memory per CTA (227 KB)
 constexpr int kThreads = 192;        // warp 0 TMA, warp 1 MMA + TMEM owner, warps 2..5 epilogue
+constexpr int kThreadsW4 = 320;      // + warps 6..9: dequantise 4-bit base tiles into bf16
 constexpr int kEpilogueThreads = 128;
+constexpr int kConvertThreads = 128;
+constexpr int kW4Group = 128;        // input features per scale of a 4-bit base
 // Work lists this small travel inside the kernel parameters (no upload copy per call).
 constexpr int kInlineTiles = 64;     // fused + shrink tiles (cluster groups included)
 constexpr int kInlineSegs = 48;      // merged segments
@@ -50,6 +53,8 @@ struct GemmParams {
     CUtensorMap tm_x;                // X [T, d_in], box 64 x 128
     CUtensorMap tm_w;                // W [d_out, d_in], box 64 x tile_n
     CUtensorMap tm_u;                // U [u_rows, rank], box 64 x 128
+    CUtensorMap tm_wq;               // 4-bit base: packed W uint8 [d_out, d_in/2], box 32 x tile_n/cs
+    CUtensorMap tm_ws;               // 4-bit base: scales bf16 [d_in/128, d_out], box tile_n/cs x 1
     const CUtensorMap* tm_b;         // device array per compact adapter: B_a [d_out, rank], box 64 x tile_n
     const CUtensorMap* tm_a;         // device array per compact adapter: A_a [rank, d_in], box 64 x shrink_n
     const Tile* shrink_tiles;        // device [n_shrink]
@@ -80,6 +85,7 @@ struct GemmParams {
     int rank;
     int cluster_size;                // CTA group of the MMA: 1, or 2 (an SM pair, M = 256)
     int bk;                          // K per pipeline stage: 64 (128-byte swizzle) or 32 (64-byte swizzle)
+    int w4;                          // 1: the base weight is 4-bit (tm_wq, tm_ws) instead of tm_w
     int debug_stall;
 };
 
@@ -95,7 +101,7 @@ int plan_segments(const int32_t* seg_offsets, const int32_t* seg_ids, int n_seg,
                   int n_adapters, Plan* plan);
 
 // kernels.cu
-size_t gemm_smem_bytes(int b_tile_rows, int stages, int bk);
+size_t gemm_smem_bytes(int b_tile_rows, int stages, int bk, int w4_rows = 0);
 cudaError_t gemm_prepare_device();           // sets the opt-in smem limit on the current device
 cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t stream);
 int gemm_max_clusters(const GemmParams& p);  // co-resident clusters of this launch shape

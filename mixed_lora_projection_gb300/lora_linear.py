@@ -137,6 +137,43 @@ class LoraLinear:
         _check(rc, "lora_linear_forward")
         return y
 
+    def forward_w4(self, x: torch.Tensor, seg_offsets, seg_ids, Wq: torch.Tensor, Ws: torch.Tensor, A, B, scales,
+                   y: torch.Tensor | None = None, stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+        """Same with a 4-bit base: Wq uint8 [d_out, d_in/2] (low nibble = even input), Ws bf16
+        [d_in/128, d_out]; W[n,k] = q[n,k] * Ws[k//128, n]."""
+        if Wq.dtype != torch.uint8 or not Wq.is_contiguous() or Wq.device != self.device:
+            raise TypeError("Wq must be a contiguous uint8 tensor on the handle's device")
+        T = x.shape[0]
+        if y is None:
+            y = torch.empty((T, self.d_out), dtype=torch.bfloat16, device=self.device)
+        off, _ = _i32(seg_offsets)
+        ids, n = _i32(seg_ids)
+        a_arr, b_arr, s_arr, na = self._adapters(A, B, scales)
+        s = stream if stream is not None else torch.cuda.current_stream(self.device)
+        rc = self._lib.lora_linear_forward_w4(self._h, _bf16_ptr(x, "x", self.device), T, off, ids, n,
+                                              Wq.data_ptr(), _bf16_ptr(Ws, "Ws", self.device), a_arr, b_arr, s_arr,
+                                              na, _bf16_ptr(y, "y", self.device), C.c_void_p(s.cuda_stream))
+        _check(rc, "lora_linear_forward_w4")
+        return y
+
+    def forward_host_w4(self, x_host: torch.Tensor, seg_offsets, seg_ids, Wq: torch.Tensor, Ws: torch.Tensor, A, B,
+                        scales, y_host: torch.Tensor, stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+        """forward_w4 from and to host bf16 tensors; waits for completion."""
+        if x_host.device.type != "cpu" or y_host.device.type != "cpu":
+            raise ValueError("forward_host_w4 takes host tensors")
+        if Wq.dtype != torch.uint8 or not Wq.is_contiguous() or Wq.device != self.device:
+            raise TypeError("Wq must be a contiguous uint8 tensor on the handle's device")
+        T = x_host.shape[0]
+        off, _ = _i32(seg_offsets)
+        ids, n = _i32(seg_ids)
+        a_arr, b_arr, s_arr, na = self._adapters(A, B, scales)
+        s = stream if stream is not None else torch.cuda.current_stream(self.device)
+        rc = self._lib.lora_linear_forward_host_w4(self._h, _bf16_ptr(x_host, "x"), T, off, ids, n, Wq.data_ptr(),
+                                                   _bf16_ptr(Ws, "Ws", self.device), a_arr, b_arr, s_arr, na,
+                                                   _bf16_ptr(y_host, "y"), C.c_void_p(s.cuda_stream))
+        _check(rc, "lora_linear_forward_host_w4")
+        return y_host
+
     def forward_host(self, x_host: torch.Tensor, seg_offsets, seg_ids, W: torch.Tensor, A, B, scales,
                      y_host: torch.Tensor, stream: torch.cuda.Stream | None = None) -> torch.Tensor:
         """Same, from and to host bf16 tensors (pinned for speed); waits for completion."""

@@ -141,6 +141,19 @@ def make_inputs(w: Workload, device="cpu", layer: int = 0, proj_index: int = 0,
     return Inputs(x=x, w=W, a=A, b=B, scales=tuple(w.scales))
 
 
+def make_w4_base(w: Workload, device="cpu", layer: int = 0, proj_index: int = 0):
+    """A seeded 4-bit base for workload ``w``: (qweight uint8 [d_out, d_in/2], scales bf16
+    [d_in/128, d_out]). Nibbles are uniform over [-8, 7] (variance 21.25); scales are
+    uniform in [0.5, 1.5] x 1/sqrt(21.25 d_in), so W = q s has variance ~1/d_in like the bf16
+    base. Seed: the W seed of the workload + 500000."""
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed_for(w, 1, layer, proj_index)) + 500000)
+    q = torch.randint(0, 256, (w.d_out, w.d_in // 2), generator=g, device=device, dtype=torch.int32).to(torch.uint8)
+    s0 = 1.0 / math.sqrt(21.25 * w.d_in)
+    s = (torch.rand((w.d_in // 128, w.d_out), generator=g, device=device) + 0.5) * s0
+    return q, s.to(torch.bfloat16)
+
+
 def bf16_bits(t: torch.Tensor):
     """uint16 numpy view of a bf16 tensor's bit patterns (copied to the host)."""
     import numpy as np

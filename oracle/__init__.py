@@ -14,4 +14,7 @@ from .lora_linear_oracle import (  # noqa: F401
     merge_segments,
     plan_ref,
     max_rel_err,
+    W4_GROUP,
+    w4_dequantize_fp64,
+    lora_linear_w4_fp64,
 )

@@ -152,6 +152,43 @@ def lora_linear_rows_fp64(x_rows, row_ids, w, a_list, b_list, scales) -> np.ndar
     return lora_linear_fp64(x_rows, offs, list(row_ids), w, a_list, b_list, scales)
 
 
+# --------------------------------------------------------------------------- 4-bit base weights
+
+W4_GROUP = 128  # input features per scale group
+
+
+def w4_dequantize_fp64(qweight, scale_bits) -> np.ndarray:
+    """W [d_out, d_in] from 4-bit weights, exactly (float64).
+
+    "Two 27B models on a single RTX 5090", section 4 and "Qwen3.8-27B on one RTX 3090 with
+    patched vLLM + DFlash2" (the W4A16 base of the deployment): the base matrix is stored in 4
+    bits, the adapter in bf16. Format (a reading, the pages give none): symmetric int4 with
+    one bf16 scale per group of 128 consecutive input features of an output row,
+        W[n, k] = q[n, k] * s[k // 128, n],   q in [-8, 7] (two's complement nibbles),
+    qweight: uint8 [d_out, d_in / 2], byte j of row n holds k = 2j in its low nibble and
+    k = 2j + 1 in its high nibble; scale_bits: bf16 bit patterns [d_in / 128, d_out].
+    """
+    qweight = np.ascontiguousarray(qweight, dtype=np.uint8)
+    d_out, half = qweight.shape
+    d_in = 2 * half
+    lo = (qweight & 0x0F).astype(np.int64)
+    hi = (qweight >> 4).astype(np.int64)
+    q = np.empty((d_out, d_in), dtype=np.int64)
+    q[:, 0::2] = lo
+    q[:, 1::2] = hi
+    q = np.where(q >= 8, q - 16, q)                      # two's complement nibble
+    s = bf16_bits_to_f64(scale_bits)                     # [d_in // 128, d_out]
+    if s.shape != (d_in // W4_GROUP, d_out):
+        raise ValueError("scales must be [d_in / 128, d_out]")
+    return q.astype(np.float64) * np.repeat(s.T, W4_GROUP, axis=1)
+
+
+def lora_linear_w4_fp64(x, seg_offsets, seg_ids, qweight, scale_bits, a_list, b_list, scales) -> np.ndarray:
+    """The projection with a 4-bit base: the plain definition on the dequantised weights."""
+    return lora_linear_fp64(x, seg_offsets, seg_ids, w4_dequantize_fp64(qweight, scale_bits),
+                            a_list, b_list, scales)
+
+
 # --------------------------------------------------------------------------- the planner
 
 def merge_segments(seg_offsets, seg_ids):

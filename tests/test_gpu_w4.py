@@ -1,0 +1,122 @@
+"""GPU parity of the 4-bit-base path (lora_linear_forward_w4) against the fp64 oracle on the
+same seeded inputs: W[n,k] = q[n,k] * s[k//128, n], adapters in bf16."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import bf16_bits_to_f64, lora_linear_w4_fp64, row_adapter_ids, w4_dequantize_fp64
+from oracle import lora_linear_rows_fp64
+from mixed_lora_projection_gb300.synth import WORKLOADS, Workload, bf16_bits, make_inputs, make_w4_base
+
+from gpu_util import TOL, f64, rel_err, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from mixed_lora_projection_gb300 import build
+    build.ensure_built()
+    return torch.device("cuda", 0)
+
+
+def _ll(w, max_segments=64):
+    from mixed_lora_projection_gb300 import LoraLinear
+    return LoraLinear(w.d_in, w.d_out, w.rank, max(w.T, 1), max_segments, 0)
+
+
+def _oracle(inp, q, sc, off, ids, rows=None):
+    qn = q.cpu().numpy()
+    sb = bf16_bits(sc)
+    a64 = [f64(a) for a in inp.a]
+    b64 = [f64(b) for b in inp.b]
+    if rows is None:
+        return lora_linear_w4_fp64(f64(inp.x), off, ids, qn, sb, a64, b64, inp.scales)
+    w = w4_dequantize_fp64(qn, sb)
+    rid = row_adapter_ids(off, ids, inp.x.shape[0])[rows]
+    return lora_linear_rows_fp64(f64(inp.x[torch.as_tensor(rows, device=inp.x.device)]), rid, w, a64, b64, inp.scales)
+
+
+SMALL = [
+    # (T, d_in, d_out, r, lengths, ids, n_adapters)
+    (64, 256, 512, 16, [32, 32], [0, 1], 1),
+    (7, 128, 256, 16, [3, 4], [0, 1], 1),
+    (300, 512, 264, 24, [0, 100, 1, 0, 199], [1, 0, 2, 2, 1], 2),
+    (517, 384, 1000, 128, [10, 5, 10, 3, 200, 289], [1, 0, 2, 2, 0, 3], 3),
+]
+
+
+@pytest.mark.parametrize("case", SMALL, ids=[f"T{c[0]}_{c[1]}x{c[2]}" for c in SMALL])
+@pytest.mark.parametrize("cluster", [1, 2])
+def test_w4_small_shapes_match_oracle(dev, case, cluster):
+    from mixed_lora_projection_gb300 import _lib as L
+    T, d_in, d_out, r, lens, ids, na = case
+    off = [0] + np.cumsum(lens).tolist()
+    w = Workload("w4", 11, T, d_in, d_out, r, tuple(off), tuple(ids), n_adapters=na,
+                 scales=tuple(0.5 + 0.75 * k for k in range(na)))
+    inp = make_inputs(w, dev)
+    q, sc = make_w4_base(w, dev)
+    with _ll(w) as ll:
+        ll.set_option(L.OPT_CLUSTER, cluster if T > 128 else 1)
+        y = ll.forward_w4(inp.x, off, ids, q, sc, inp.a, inp.b, inp.scales)
+        torch.cuda.synchronize()
+        assert ll.status() == 0
+    assert rel_err(y, _oracle(inp, q, sc, off, ids)) <= TOL
+
+
+def test_w4_dequantisation_is_exact_per_weight(dev):
+    # X = I: row k of Y is bf16(column k of W) exactly (one product per output)
+    d_in, d_out = 128, 256
+    w = Workload("w4eye", 12, d_in, d_in, d_out, 16, (0, d_in), (0,))
+    inp = make_inputs(w, dev)
+    inp.x.zero_()
+    inp.x.fill_diagonal_(1.0)
+    q, sc = make_w4_base(w, dev)
+    with _ll(w) as ll:
+        y = ll.forward_w4(inp.x, [0, d_in], [0], q, sc, inp.a, inp.b, inp.scales)
+    torch.cuda.synchronize()
+    wd = w4_dequantize_fp64(q.cpu().numpy(), bf16_bits(sc))          # exact q * s
+    want = torch.from_numpy(wd.T.copy()).to(torch.bfloat16)           # rounded once, RNE
+    assert torch.equal(y.cpu(), want)
+
+
+@pytest.mark.parametrize("name", ["mixed_decode", "mixed_near_ridge", "sweep_qkv_multi", "prefill_16k"])
+def test_w4_full_size_sampled_rows(dev, name):
+    w = WORKLOADS[name]
+    inp = make_inputs(w, dev)
+    q, sc = make_w4_base(w, dev)
+    off, ids = list(w.seg_offsets), list(w.seg_ids)
+    with _ll(w) as ll:
+        y = ll.forward_w4(inp.x, off, ids, q, sc, inp.a, inp.b, inp.scales)
+        torch.cuda.synchronize()
+        assert ll.status() == 0
+    rows = sample_rows(w.T, off, ids, n_random=128, seed=5)
+    ref = _oracle(inp, q, sc, off, ids, rows)
+    assert rel_err(y[torch.as_tensor(rows, device=dev)], ref) <= TOL
+
+
+def test_w4_rejects_d_in_not_multiple_of_128(dev):
+    from mixed_lora_projection_gb300 import LoraError
+    w = Workload("w4bad", 13, 16, 192, 256, 16, (0, 16), (0,))
+    inp = make_inputs(w, dev)
+    q = torch.zeros((256, 96), dtype=torch.uint8, device=dev)
+    sc = torch.ones((1, 256), dtype=torch.bfloat16, device=dev)
+    with _ll(w) as ll:
+        with pytest.raises(LoraError):
+            ll.forward_w4(inp.x, [0, 16], [0], q, sc, inp.a, inp.b, inp.scales)
+
+
+@pytest.mark.parametrize("name", ["tiny", "mixed_batch"])
+def test_w4_host_buffers_match_device_path(dev, name):
+    w = WORKLOADS[name]
+    inp = make_inputs(w, dev)
+    q, sc = make_w4_base(w, dev) if w.d_in % 128 == 0 else (None, None)
+    x_host = inp.x.cpu().pin_memory()
+    y_host = torch.empty((w.T, w.d_out), dtype=torch.bfloat16).pin_memory()
+    with _ll(w) as ll:
+        y = ll.forward_w4(inp.x, w.seg_offsets, w.seg_ids, q, sc, inp.a, inp.b, inp.scales)
+        ll.forward_host_w4(x_host, w.seg_offsets, w.seg_ids, q, sc, inp.a, inp.b, inp.scales, y_host)
+    torch.cuda.synchronize()
+    assert rel_err(y_host, f64(y)) <= TOL
