@@ -172,7 +172,7 @@ def aggregate_ranks(elapsed_ms, e2e_ms, flops_per_step, steps, world, dist):
 
 def run_ours(args, rank, world, dist):
     import torch
-    from mixed_lora_projection_gb300 import LoraLinear, _lib as L
+    from mixed_lora_projection_gb300 import LoraLinear, w4_repack, _lib as L
     from mixed_lora_projection_gb300.synth import make_inputs, make_w4_base
 
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
@@ -190,7 +190,8 @@ def run_ours(args, rank, world, dist):
         copies = [make_inputs(w, dev, layer=layer, proj_index=pi + 4 * c, with_x=(c == 0)) for c in range(n_copies)]
         if args.w4:
             for c, inp in enumerate(copies):
-                inp.w = make_w4_base(w, dev, layer=layer, proj_index=pi + 4 * c)
+                q, sc = make_w4_base(w, dev, layer=layer, proj_index=pi + 4 * c)
+                inp.w = (w4_repack(q, q), sc)   # once, at load time: plain -> kernel layout
         y = torch.empty((w.T, w.d_out), dtype=torch.bfloat16, device=dev)
         setups.append((w, handles[key], copies, y))
     stream = torch.cuda.current_stream(dev)

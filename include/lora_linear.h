@@ -115,9 +115,26 @@ int lora_linear_forward_host(lora_linear* h, const void* x_host, int T,
                              const float* scale, int n_adapters, void* y_host, void* stream);
 
 /*
+ * lora_linear_w4_repack -- convert a 4-bit base weight from the plain layout to the kernel
+ * layout that lora_linear_forward_w4 reads. Run once when the weight is loaded.
+ *   src  device uint8 [d_out, d_in / 2], plain layout: signed 4-bit weights q in [-8, 7]
+ *        (two's complement nibbles); byte j of row n holds input feature 2j in its low
+ *        nibble and 2j + 1 in its high one.
+ *   dst  device, same size; may equal src (in place). Kernel layout, per 32-bit
+ *        little-endian word of a row (input features 8c .. 8c+7): offset-binary nibbles
+ *        q + 8, feature 8c+2j in nibble j and feature 8c+2j+1 in nibble j+4 (j = 0..3).
+ *   n_bytes  size of the weight in bytes: a multiple of 4, both pointers 4-byte aligned
+ *        (else LORA_EINVAL). Enqueued on `stream`; returns once launched.
+ * Source: no counterpart on the pages (the layout is this library's: the converter warps of
+ * lora_linear_forward_w4 turn one word into four bf16 pairs with a mask, an or and two
+ * bf16 operations per pair).
+ */
+int lora_linear_w4_repack(const void* src, void* dst, long long n_bytes, void* stream);
+
+/*
  * lora_linear_forward_w4 -- lora_linear_forward with a 4-bit base weight.
- *   Wq  device uint8 [d_out, d_in / 2]: signed 4-bit weights (two's complement nibbles);
- *       byte j of row n holds input feature 2j in its low nibble and 2j + 1 in its high one.
+ *   Wq  device uint8 [d_out, d_in / 2], in the kernel layout written by
+ *       lora_linear_w4_repack from the plain layout (signed 4-bit q[n, k], see there).
  *   Ws  device bf16 [d_in / 128, d_out]: one scale per output row and group of 128 inputs.
  *   The base weight is W[n, k] = q[n, k] * Ws[k / 128, n]; on the GPU each weight is
  *   rounded to bf16 (round to nearest even) before the bf16 tensor-core product. The

@@ -22,6 +22,7 @@ SIGNATURES = {
                                       C.POINTER(C.c_float), C.c_int, P, P]),
     "lora_linear_forward_host": (C.c_int, [P, P, C.c_int, I32P, I32P, C.c_int, P, C.POINTER(P), C.POINTER(P),
                                            C.POINTER(C.c_float), C.c_int, P, P]),
+    "lora_linear_w4_repack": (C.c_int, [P, P, C.c_longlong, P]),
     "lora_linear_forward_w4": (C.c_int, [P, P, C.c_int, I32P, I32P, C.c_int, P, P, C.POINTER(P), C.POINTER(P),
                                          C.POINTER(C.c_float), C.c_int, P, P]),
     "lora_linear_forward_host_w4": (C.c_int, [P, P, C.c_int, I32P, I32P, C.c_int, P, P, C.POINTER(P),

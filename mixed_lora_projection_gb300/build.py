@@ -19,7 +19,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "liblora_linear.so")
-SOURCES = ["kernels.cu", "api.cpp", "planner.cpp", "noalloc.cu"]
+SOURCES = ["kernels.cu", "kernels_w4.cu", "api.cpp", "planner.cpp", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

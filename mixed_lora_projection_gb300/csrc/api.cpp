@@ -154,10 +154,39 @@ CUresult encode_2d(lora_linear* h, CUtensorMap* m, const void* ptr, uint64_t inn
 }
 
 // Deepest ring that fits the opt-in shared memory, for `b_rows` B rows per CTA.
-int stages_for(int b_rows, int bk, int w4_rows = 0) {
+int stages_for(int b_rows, int bk) {
     int s = kMaxStages;
-    while (s > 2 && gemm_smem_bytes(b_rows, s, bk, w4_rows) > (size_t)kSmemLimit) --s;
+    while (s > 2 && gemm_smem_bytes(b_rows, s, bk) > (size_t)kSmemLimit) --s;
     return s;
+}
+
+// 2-D map of bytes whose 128-byte box rows are 128-byte swizzled (the 4-bit base's packed
+// rows, read 16 bytes per thread without bank conflicts).
+CUresult encode_u8_sw128(lora_linear* h, CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer,
+                         uint32_t box_outer) {
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {inner};
+    cuuint32_t box[2] = {128, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    return h->encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+// Token groups of the 4-bit base kernel: consecutive planner tiles in pairs.
+std::vector<W4Group> make_w4_groups(const std::vector<Tile>& fused) {
+    std::vector<W4Group> g;
+    for (size_t i = 0; i < fused.size(); i += 2) {
+        W4Group w;
+        memset(&w, 0, sizeof(w));
+        for (int k = 0; k < 2 && i + k < fused.size(); ++k) {
+            w.row0[k] = fused[i + k].row0;
+            w.nrows[k] = fused[i + k].nrows;
+            w.adapter[k] = fused[i + k].adapter;
+        }
+        g.push_back(w);
+    }
+    return g;
 }
 
 // 2-D map without swizzle (the 4-bit base's packed rows and scales).
@@ -445,7 +474,7 @@ int lora_linear_create(lora_linear** out, int d_in, int d_out, int rank, int max
         return LORA_ECUDA;
     }
     h->encode = reinterpret_cast<EncodeTiledFn>(fn);
-    if (gemm_prepare_device() != cudaSuccess) {
+    if (gemm_prepare_device() != cudaSuccess || w4_prepare_device() != cudaSuccess) {
         free_handle(h);
         return LORA_ECUDA;
     }
@@ -455,7 +484,10 @@ int lora_linear_create(lora_linear** out, int d_in, int d_out, int rank, int max
     h->slot_bytes = align_up(2 * (size_t)max_segments * sizeof(CUtensorMap), 128) +
                     4 * (size_t)h->max_fused * sizeof(Tile) +
                     align_up(4 * (2 * (size_t)max_segments + 1), 16) +
-                    align_up(4 * (size_t)max_segments, 16) + 256;
+                    align_up(4 * (size_t)max_segments, 16) + 256 +
+                    // 4-bit base kernel: B_a maps of its own box and the token groups
+                    align_up((size_t)max_segments * sizeof(CUtensorMap), 128) +
+                    (size_t)(h->max_fused / 2 + 1) * sizeof(W4Group) + 256;
     if (cudaMalloc(&h->u_ws, (size_t)h->u_rows * rank * 2) != cudaSuccess ||
         cudaMalloc((void**)&h->status, sizeof(int)) != cudaSuccess ||
         cudaMalloc((void**)&h->flags, sizeof(int) * (size_t)h->max_fused) != cudaSuccess ||
@@ -659,11 +691,12 @@ int forward_impl(lora_linear* h, const void* x, int T, const int32_t* seg_offset
     DeviceGuard guard(h->device);
     const bool w4 = Wq != nullptr;
     Shape sh = choose_shape(h, plan);
-    if (w4) {
-        // 64-wide K-steps (32 packed bytes per row) and room for the packed staging ring
-        sh.bk = 64;
-        sh.stages = stages_for(std::max(sh.tile_n, sh.shrink_n) / sh.cs, 64, sh.tile_n / sh.cs);
-    }
+    // 4-bit base: the shrink pass runs on the bf16 kernel (64-wide K-steps), then the 4-bit
+    // kernel runs the base and expand passes over token groups
+    if (w4) sh.bk = 64;
+    const std::vector<W4Group> w4_groups = w4 ? make_w4_groups(plan.fused) : std::vector<W4Group>();
+    const int n_w4g = (int)w4_groups.size();
+    const bool w4_inline = n_used <= kInlineAdapters && n_w4g <= kW4InlineGroups;
     const int cs = sh.cs, tile_n = sh.tile_n, shrink_n = sh.shrink_n, bk = sh.bk;
     const int nfg = (int)sh.fused_groups.size() / cs, nsg = (int)sh.shrink_groups.size() / cs;
     const int nft = (int)sh.fused_groups.size(), nst = (int)sh.shrink_groups.size();
@@ -672,8 +705,10 @@ int forward_impl(lora_linear* h, const void* x, int T, const int32_t* seg_offset
 
     GemmParams p;
     memset(&p, 0, sizeof(p));
+    W4Params q;
+    memset(&q, 0, sizeof(q));
     const bool inline_wl = h->allow_inline && nft + nst <= kInlineTiles && n_m <= kInlineSegs &&
-                           n_used <= kInlineAdapters;
+                           n_used <= kInlineAdapters && (!w4 || w4_inline);
     Slot* slot = nullptr;
     if (inline_wl) {
         // small work list: it travels in the kernel parameters, no upload
@@ -692,6 +727,14 @@ int forward_impl(lora_linear* h, const void* x, int T, const int32_t* seg_offset
         memcpy(p.inline_seg + n_m + 1, plan.seg_id.data(), 4 * (size_t)n_m);
         p.inline_wl = 1;
         p.inline_shrink_off = nft;
+        if (w4) {
+            for (int k = 0; k < n_used; ++k)
+                if (encode_2d(h, &q.inline_bmaps[k], B[plan.used_adapters[k]], h->rank, h->d_out, 64, kW4TileM) !=
+                    CUDA_SUCCESS)
+                    return LORA_ECUDA;
+            memcpy(q.inline_groups, w4_groups.data(), (size_t)n_w4g * sizeof(W4Group));
+            q.inline_wl = 1;
+        }
         if (x_src &&
             cudaMemcpyAsync(const_cast<void*>(x), x_src, (size_t)T * h->d_in * 2, cudaMemcpyHostToDevice, upload) !=
                 cudaSuccess)
@@ -711,6 +754,10 @@ int forward_impl(lora_linear* h, const void* x, int T, const int32_t* seg_offset
         size_t off_segid = off_segoff + 4 * (size_t)(n_m + 1);
         size_t off_scale = align_up(off_segid + 4 * (size_t)n_m, 16);
         size_t used_bytes = off_scale + 4 * (size_t)n_used;
+        // 4-bit base kernel: its B_a maps and token groups follow
+        const size_t off_w4maps = align_up(used_bytes, 128);
+        const size_t off_w4groups = off_w4maps + (size_t)n_used * sizeof(CUtensorMap);
+        if (w4) used_bytes = off_w4groups + (size_t)n_w4g * sizeof(W4Group);
         if (used_bytes > h->slot_bytes) return LORA_EINVAL;
 
         uint8_t* hb = slot->host;
@@ -727,6 +774,16 @@ int forward_impl(lora_linear* h, const void* x, int T, const int32_t* seg_offset
         memcpy(hb + off_segid, plan.seg_id.data(), 4 * (size_t)n_m);
         float* sc = reinterpret_cast<float*>(hb + off_scale);
         for (int k = 0; k < n_used; ++k) sc[k] = scale[plan.used_adapters[k]];
+        if (w4) {
+            CUtensorMap* w4maps = reinterpret_cast<CUtensorMap*>(hb + off_w4maps);
+            for (int k = 0; k < n_used; ++k)
+                if (encode_2d(h, &w4maps[k], B[plan.used_adapters[k]], h->rank, h->d_out, 64, kW4TileM) !=
+                    CUDA_SUCCESS)
+                    return LORA_ECUDA;
+            memcpy(hb + off_w4groups, w4_groups.data(), (size_t)n_w4g * sizeof(W4Group));
+            q.tm_b = reinterpret_cast<const CUtensorMap*>(slot->dev + off_w4maps);
+            q.groups = reinterpret_cast<const W4Group*>(slot->dev + off_w4groups);
+        }
         if (cudaMemcpyAsync(slot->dev, hb, used_bytes, cudaMemcpyHostToDevice, upload) != cudaSuccess)
             return LORA_ECUDA;
         if (x_src &&
@@ -747,12 +804,11 @@ int forward_impl(lora_linear* h, const void* x, int T, const int32_t* seg_offset
     }
     if (encode_2d(h, &p.tm_x, x, h->d_in, T, bk, kTileM) != CUDA_SUCCESS) return LORA_ECUDA;
     if (w4) {
-        if (encode_plain_2d(h, &p.tm_wq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, Wq, (uint64_t)h->d_in / 2, h->d_out,
-                            bk / 2, tile_n / cs) != CUDA_SUCCESS ||
-            encode_plain_2d(h, &p.tm_ws, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Ws, h->d_out,
-                            (uint64_t)h->d_in / kW4Group, tile_n / cs, 1) != CUDA_SUCCESS)
+        q.tm_x = p.tm_x;
+        if (encode_u8_sw128(h, &q.tm_wq, Wq, (uint64_t)h->d_in / 2, h->d_out, kW4TileM) != CUDA_SUCCESS ||
+            encode_plain_2d(h, &q.tm_ws, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Ws, h->d_out,
+                            (uint64_t)h->d_in / kW4Group, kW4TileM, 2) != CUDA_SUCCESS)
             return LORA_ECUDA;
-        p.w4 = 1;
     } else if (encode_2d(h, &p.tm_w, W, h->d_in, h->d_out, bk, tile_n / cs) != CUDA_SUCCESS) {
         return LORA_ECUDA;
     }
@@ -800,7 +856,38 @@ int forward_impl(lora_linear* h, const void* x, int T, const int32_t* seg_offset
         cudaEventRecord(rec.ev[0], stream);
     }
     const int fused_units = nfg * sh.n_ntiles;
-    if (h->two_launch && nsg > 0) {
+    if (w4) {
+        // shrink (bf16 kernel), then base + expand on the 4-bit kernel, ordered by the stream
+        if (nsg > 0) {
+            GemmParams sp = p;
+            sp.n_fused = 0;
+            if (launch_gemm(sp, std::min(nsg, slots) * cs, stream) != cudaSuccess) return LORA_ECUDA;
+            ++h->launches;
+            rec.has_shrink = true;
+        }
+        if (h->timing) cudaEventRecord(rec.ev[1], stream);
+        for (const W4Group& g : w4_groups)
+            for (int k = 0; k < 2; ++k)
+                if (g.adapter[k] < 0 || g.adapter[k] > n_used || g.nrows[k] < 0 || g.row0[k] < 0 ||
+                    g.row0[k] + g.nrows[k] > T || g.nrows[k] > kTileM || (k == 0 && g.nrows[0] == 0))
+                    return LORA_EINVAL;
+        q.tm_u = p.tm_u;
+        q.y = y;
+        q.status = h->status;
+        q.wait_limit_ns = h->wait_limit_ns;
+        q.n_groups = n_w4g;
+        q.n_ntiles = ceil_div(h->d_out, kW4TileM);
+        q.k_main_blocks = ceil_div(h->d_in, 64);
+        q.k_lora_blocks = ceil_div(h->rank, 64);
+        q.k_pack_blocks = ceil_div(q.k_main_blocks, 4);
+        q.d_out = h->d_out;
+        q.stages = 4;
+        q.pstages = 5;
+        q.debug_stall = h->debug_stall;
+        const int units = q.n_groups * q.n_ntiles;
+        if (launch_w4(q, std::min(units, h->num_sms), stream) != cudaSuccess) return LORA_ECUDA;
+        ++h->launches;
+    } else if (h->two_launch && nsg > 0) {
         // shrink, then fused base+expand ordered by the stream
         GemmParams s = p;
         s.n_fused = 0;
@@ -844,6 +931,23 @@ int lora_linear_forward(lora_linear* h, const void* x, int T, const int32_t* seg
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
     return forward_impl(h, x, T, seg_offsets, seg_adapter_ids, n_seg, W, A, B, scale, n_adapters, y, stream,
                         stream, nullptr, nullptr);
+}
+
+int lora_linear_w4_repack(const void* src, void* dst, long long n_bytes, void* stream) {
+    if (n_bytes < 0 || (n_bytes % 4) != 0) return LORA_EINVAL;
+    if (n_bytes == 0) return LORA_OK;
+    if (!src || !dst || (reinterpret_cast<uintptr_t>(src) & 3) || (reinterpret_cast<uintptr_t>(dst) & 3))
+        return LORA_EINVAL;
+    // partial overlap would let one thread read a word another has already rewritten
+    if (src != dst && overlaps(dst, (size_t)n_bytes, src, (size_t)n_bytes)) return LORA_EINVAL;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return LORA_ECUDA;
+    const long long n_words = n_bytes / 4;
+    const long long want = (n_words + 255) / 256;
+    const int grid = (int)std::min<long long>(want, (long long)sms * 8);
+    return w4_repack(src, dst, n_words, grid, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? LORA_OK
+                                                                                                   : LORA_ECUDA;
 }
 
 int lora_linear_forward_w4(lora_linear* h, const void* x, int T, const int32_t* seg_offsets,

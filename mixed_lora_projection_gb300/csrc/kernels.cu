@@ -48,303 +48,11 @@
 #include <stdint.h>
 #include <string.h>
 
+#include "dev_common.cuh"
 #include "lora_internal.h"
 
 namespace lora {
 namespace dev {
-
-__device__ __forceinline__ uint32_t smem_addr(const void* p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ uint64_t global_timer_ns() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-// ---------------------------------------------------------------- cluster
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-// All threads of every CTA in the cluster (also a CTA-wide barrier).
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// Shared::cluster address of the same shared variable in CTA `rank` of this cluster.
-__device__ __forceinline__ uint32_t map_to_rank(uint32_t local, uint32_t rank) {
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
-    return r;
-}
-
-// ---------------------------------------------------------------- mbarrier
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes, uint32_t pred) {
-    asm volatile(
-        "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %2, 0;\n\t"
-        "@q mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n\t}" ::"r"(bar), "r"(bytes), "r"(pred)
-        : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-// Arrive on a barrier given by its shared::cluster address (this CTA's or the peer's).
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Warp-wide form of wait_bounded for the converged producer and MMA warps: every lane
-// tests the phase (one instruction for the warp); only if it is not complete yet does lane 0
-// fall back to the bounded loop. Returns the same value in every lane.
-__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* status,
-                                          uint64_t limit_ns);
-
-// Waits for the phase with the given parity to complete. Gives up (returns false) when
-// another role has aborted or when `limit_ns` of wall time pass; in the latter case it
-// records the timeout in the status word and raises the CTA's abort flag.
-__device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          int* status, uint64_t limit_ns, bool honour_abort) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = global_timer_ns();
-    while (true) {
-        for (int i = 0; i < 32; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
-        if (honour_abort && *abort_flag) return false;
-        if (global_timer_ns() - t0 > limit_ns) {
-            atomicOr(status, 1);
-            *abort_flag = 1;
-            return false;
-        }
-    }
-}
-
-__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* status,
-                                          uint64_t limit_ns) {
-    if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
-    int ok = 1;
-    if ((threadIdx.x & 31) == 0) ok = wait_bounded(bar, parity, abort_flag, status, limit_ns, true);
-    return __shfl_sync(0xffffffffu, ok, 0) != 0;
-}
-
-// ---------------------------------------------------------------- TMA
-// 2-D tiled load into this CTA's shared memory, completing bytes on `bar` (a barrier of
-// this CTA; with CG = 2 it may be the even CTA's barrier, as a shared::cluster address).
-// Issued by the lanes with pred != 0 (one lane of a converged warp).
-template <int CG>
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c_inner,
-                                            int c_outer, uint32_t pred) {
-    if (CG == 1) {
-        asm volatile(
-            "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %5, 0;\n\t"
-            "@q cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-            " [%0], [%1, {%3, %4}], [%2];\n\t}" ::"r"(dst),
-            "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c_inner), "r"(c_outer), "r"(pred)
-            : "memory");
-    } else {
-        asm volatile(
-            "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %5, 0;\n\t"
-            "@q cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.cta_group::2"
-            " [%0], [%1, {%3, %4}], [%2];\n\t}" ::"r"(dst),
-            "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c_inner), "r"(c_outer), "r"(pred)
-            : "memory");
-    }
-}
-__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
-}
-// Tensor maps written to global memory by the host: make the tensormap proxy see them.
-__device__ __forceinline__ void tensormap_acquire(const CUtensorMap* map) {
-    asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(
-                     reinterpret_cast<uint64_t>(map))
-                 : "memory");
-}
-
-// ---------------------------------------------------------------- tcgen05
-__device__ __forceinline__ void tc_fence_before() {
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-// With CG = 2 one warp of each CTA of the pair executes these together.
-template <int CG>
-__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
-    if (CG == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
-                     "r"(ncols)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-    } else {
-        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
-                     "r"(ncols)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
-    }
-}
-template <int CG>
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-    if (CG == 1)
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
-    else
-        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
-}
-// D[tmem] (+)= A[smem] * B[smem]^T, bf16 inputs, fp32 accumulate. Issued by the lane with
-// pred != 0 of a converged warp: the MMA stream keeps the tensor pipe busy only when the
-// issuing warp is converged (a lone diverged lane issues MMAs far more slowly).
-template <int CG>
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                         uint32_t accumulate, uint32_t pred) {
-    if (CG == 1)
-        asm volatile(
-            "{\n\t.reg .pred p, q;\n\t"
-            "setp.ne.b32 p, %4, 0;\n\t"
-            "setp.ne.b32 q, %5, 0;\n\t"
-            "@q tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-            "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(pred)
-            : "memory");
-    else
-        asm volatile(
-            "{\n\t.reg .pred p, q;\n\t"
-            "setp.ne.b32 p, %4, 0;\n\t"
-            "setp.ne.b32 q, %5, 0;\n\t"
-            "@q tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-            "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(pred)
-            : "memory");
-}
-// Arrive once on `bar` (CG = 1: this CTA's; CG = 2: the barrier at that offset in both CTAs
-// of the pair) when every tcgen05 op the issuing lane issued so far has completed.
-template <int CG>
-__device__ __forceinline__ void mma_commit(uint32_t bar, uint32_t pred) {
-    if (CG == 1)
-        asm volatile(
-            "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %1, 0;\n\t"
-            "@q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar),
-            "r"(pred)
-            : "memory");
-    else
-        asm volatile(
-            "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %2, 0;\n\t"
-            "@q tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-            " [%0], %1;\n\t}" ::"r"(bar), "h"((uint16_t)3), "r"(pred)
-            : "memory");
-}
-// Same, arriving only on this CTA's barrier.
-template <int CG>
-__device__ __forceinline__ void mma_commit_local(uint32_t bar, uint32_t pred) {
-    if (CG == 1)
-        asm volatile(
-            "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %1, 0;\n\t"
-            "@q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar),
-            "r"(pred)
-            : "memory");
-    else
-        asm volatile(
-            "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %1, 0;\n\t"
-            "@q tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar),
-            "r"(pred)
-            : "memory");
-}
-// 32 lanes x 32 bits x 16 columns: thread i of the warp gets 16 consecutive columns of lane
-// (taddr.lane + i).
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* v) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32"
-        " {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
-          "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]),
-          "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
-        : "r"(taddr));
-}
-__device__ __forceinline__ void tmem_ld_wait() {
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
-// Shared-memory matrix descriptor of a K-major tile written by TMA with a swizzle as wide
-// as its rows: BK = 64 -> 128-byte rows and 128-byte swizzle (layout 2), BK = 32 ->
-// 64-byte rows and 64-byte swizzle (layout 4). Groups of 8 rows are 8 x row bytes apart
-// (stride byte offset); the leading byte offset is unused for these layouts; version 1.
-// The tile base must be aligned to the swizzle pattern (1024 bytes here).
-template <int BK>
-__device__ __forceinline__ uint64_t smem_desc(uint32_t addr) {
-    static_assert(BK == 64 || BK == 32, "K per stage must be 32 or 64");
-    uint64_t d = 0;
-    d |= (uint64_t)((addr & 0x3FFFFu) >> 4);
-    d |= (uint64_t)1 << 16;
-    d |= (uint64_t)((8 * BK * 2) >> 4) << 32;
-    d |= (uint64_t)1 << 46;
-    d |= (uint64_t)(BK == 64 ? 2 : 4) << 61;
-    return d;
-}
-// Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major, shape M x N.
-__device__ __forceinline__ uint32_t instr_desc_bf16(int m, int n) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) |
-           ((uint32_t)(m >> 4) << 24);
-}
-
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&v);
-}
-
-// Adapter id of row t among the merged segments (binary search over offsets).
-__device__ __forceinline__ int row_adapter(const int32_t* off, const int32_t* ids, int n, int t) {
-    int lo = 0, hi = n - 1;
-    while (lo < hi) {
-        int mid = (lo + hi + 1) >> 1;
-        if (off[mid] <= t) lo = mid; else hi = mid - 1;
-    }
-    return ids[lo];
-}
-
-// ---------------------------------------------------------------- cross-CTA flags
-__device__ __forceinline__ int ld_acquire(const int* p) {
-    int v;
-    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-__device__ __forceinline__ void st_release(int* p, int v) {
-    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-// Generic-proxy global writes / reads ordered against the async proxy (TMA).
-__device__ __forceinline__ void fence_proxy_async_global() {
-    asm volatile("fence.proxy.async.global;" ::: "memory");
-}
-__device__ __forceinline__ void epilogue_bar_sync() {
-    asm volatile("bar.sync 1, %0;" ::"n"(kEpilogueThreads) : "memory");
-}
-// Waits until *flag == epoch (bounded like wait_bounded).
-__device__ __noinline__ bool wait_flag(const int* flag, int epoch, volatile int* abort_flag, int* status,
-                                       uint64_t limit_ns) {
-    if (ld_acquire(flag) == epoch) return true;
-    const uint64_t t0 = global_timer_ns();
-    while (true) {
-        __nanosleep(64);
-        if (ld_acquire(flag) == epoch) return true;
-        if (*abort_flag) return false;
-        if (global_timer_ns() - t0 > limit_ns) {
-            atomicOr(status, 1);
-            *abort_flag = 1;
-            return false;
-        }
-    }
-}
-
 // One work unit, as every role decodes it.
 struct Unit {
     Tile tile;
@@ -424,10 +132,8 @@ __device__ __forceinline__ Unit decode_unit(const GemmParams& p, const WorkList&
     return r;
 }
 
-template <int BK, int CG, int QW>
-__global__ void __launch_bounds__(QW ? kThreadsW4 : kThreads, 1)
-    lora_gemm_kernel(const __grid_constant__ GemmParams p) {
-    static_assert(!QW || BK == 64, "the 4-bit base uses 64-wide K-steps (32 packed bytes per row)");
+template <int BK, int CG>
+__global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_constant__ GemmParams p) {
     constexpr uint32_t kStageA = kTileM * BK * 2;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // carve: rings (1024-aligned), then barriers, then the TMEM slot and the abort flag
@@ -438,17 +144,10 @@ __global__ void __launch_bounds__(QW ? kThreadsW4 : kThreads, 1)
     const uint32_t b_stage_bytes = (uint32_t)b_rows * BK * 2;
     uint8_t* a_ring = base;
     uint8_t* b_ring = a_ring + (size_t)stages * kStageA;
-    // 4-bit base: staging rings of the packed tile (32 bytes per row) and its scales
-    const int q_rows = QW ? p.tile_n / CG : 0;
-    const uint32_t q_stage_bytes = (uint32_t)q_rows * (BK / 2);
-    const uint32_t s_stage_bytes = ((uint32_t)q_rows * 2 + 127u) & ~127u;
-    uint8_t* q_ring = b_ring + (size_t)stages * b_stage_bytes;
-    uint8_t* s_ring = q_ring + (size_t)stages * q_stage_bytes;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(s_ring + (size_t)stages * s_stage_bytes);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(b_ring + (size_t)stages * b_stage_bytes);
     uint64_t* full = bars;
     uint64_t* empty = full + stages;
-    uint64_t* pfull = empty + stages;
-    uint64_t* tfull = pfull + stages;
+    uint64_t* tfull = empty + stages;
     uint64_t* tempty = tfull + 2;
     uint64_t* drain = tempty + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -463,10 +162,8 @@ __global__ void __launch_bounds__(QW ? kThreadsW4 : kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
-            // the producer's arrive, plus one arrive per converter warp of each CTA of the group
-            mbar_init(smem_addr(&full[s]), 1 + (QW ? CG * (kConvertThreads / 32) : 0));
+            mbar_init(smem_addr(&full[s]), 1);
             mbar_init(smem_addr(&empty[s]), 1);
-            mbar_init(smem_addr(&pfull[s]), 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(smem_addr(&tfull[a]), 1);
@@ -495,8 +192,7 @@ __global__ void __launch_bounds__(QW ? kThreadsW4 : kThreads, 1)
             if (lane == 0) {
                 tma_prefetch_desc(&p.tm_x);
                 if (p.n_fused) {
-                    tma_prefetch_desc(QW ? &p.tm_wq : &p.tm_w);
-                    if (QW) tma_prefetch_desc(&p.tm_ws);
+                    tma_prefetch_desc(&p.tm_w);
                     tma_prefetch_desc(&p.tm_u);
                 }
             }
@@ -523,11 +219,6 @@ __global__ void __launch_bounds__(QW ? kThreadsW4 : kThreads, 1)
                 const int half = w.n / CG;                       // B rows this CTA loads
                 // bytes the (even CTA's) full barrier receives per stage, from the whole group
                 const uint32_t tx = CG * (kStageA + (uint32_t)half * BK * 2);
-                // 4-bit base: TMA brings only A to the full barrier; the B tile of a base step
-                // comes from the converter warps, its packed form lands on pfull
-                const bool w4_unit = QW && !w.shrink;
-                const uint32_t tx_w4 = CG * kStageA;
-                const uint32_t ptx = (uint32_t)half * (BK / 2) + (uint32_t)half * 2;
                 for (int kb = 0; kb < w.nk; ++kb) {
                     if (kb == p.k_main_blocks && p.flags) {
                         // the expand reads U rows written by this tile's shrink unit
@@ -545,24 +236,13 @@ __global__ void __launch_bounds__(QW ? kThreadsW4 : kThreads, 1)
                     }
                     const uint32_t fb_local = smem_addr(&full[stage]);
                     const bool main = kb < p.k_main_blocks;
-                    const bool w4_step = w4_unit && main;
-                    mbar_arrive_expect_tx(fb_local, w4_step ? tx_w4 : tx, leader ? issuer : 0u);
+                    mbar_arrive_expect_tx(fb_local, tx, leader ? issuer : 0u);
                     const uint32_t fb = CG > 1 ? map_to_rank(fb_local, 0) : fb_local;
                     const uint32_t sa = smem_addr(a_ring + (size_t)stage * kStageA);
                     const uint32_t sb = smem_addr(b_ring + (size_t)stage * b_stage_bytes);
                     const int k = main ? kb * BK : (kb - p.k_main_blocks) * BK;
                     tma_load_2d<CG>(sa, main ? &p.tm_x : &p.tm_u, fb, k, w.tile.row0, issuer);
-                    if (w4_step) {
-                        // packed rows and this K-step's scales, into this CTA's staging ring
-                        const uint32_t pb = smem_addr(&pfull[stage]);
-                        mbar_arrive_expect_tx(pb, ptx, issuer);
-                        tma_load_2d<1>(smem_addr(q_ring + (size_t)stage * q_stage_bytes), &p.tm_wq, pb, kb * (BK / 2),
-                                       w.n0 + rank * half, issuer);
-                        tma_load_2d<1>(smem_addr(s_ring + (size_t)stage * s_stage_bytes), &p.tm_ws, pb,
-                                       w.n0 + rank * half, (kb * BK) / kW4Group, issuer);
-                    } else {
-                        tma_load_2d<CG>(sb, main ? bmain : &wl.tm_b[ad - 1], fb, k, w.n0 + rank * half, issuer);
-                    }
+                    tma_load_2d<CG>(sb, main ? bmain : &wl.tm_b[ad - 1], fb, k, w.n0 + rank * half, issuer);
                     ++issued;
                     if (++stage == stages) { stage = 0; phase ^= 1; }
                 }
@@ -627,71 +307,6 @@ __global__ void __launch_bounds__(QW ? kThreadsW4 : kThreads, 1)
             // every MMA this warp issued has completed before TMEM is released
             mma_commit_local<CG>(smem_addr(drain), issuer);
             if (lane == 0) wait_bounded(smem_addr(drain), 0, abort_flag, p.status, limit, false);
-        }
-    } else if (QW && warp >= 6) {
-        // ------------------------------------------------------------ 4-bit converter (warps 6..9)
-        // Base K-steps of fused units: packed int4 rows + scales (staging ring) -> bf16 B tile in
-        // the 128-byte-swizzled layout the MMA reads. W[n,k] = q * s, q = signed nibble (low
-        // nibble = even k); (128 + (q ^ 8) - 136) is q exactly, then one RNE multiply by s.
-        // Other K-steps (expand, shrink) load B by TMA; the converters only count themselves in.
-        const int ct = threadIdx.x - 6 * 32;
-        const uint32_t full_target_rank = 0;
-        const __nv_bfloat162 magic = __floats2bfloat162_rn(136.0f, 136.0f);
-        int stage = 0;
-        uint32_t phase = 0, pbits = 0;
-        bool ok = true;
-        for (int u = group; u < n_units && ok; u += n_groups) {
-            const Unit w = decode_unit(p, wl, u, rank);
-            const bool w4_unit = !w.shrink;
-            const int rows = w.n / CG;
-            for (int kb = 0; kb < w.nk; ++kb) {
-                if (!wait_warp(smem_addr(&empty[stage]), phase ^ 1, abort_flag, p.status, limit)) {
-                    ok = false;
-                    break;
-                }
-                if (w4_unit && kb < p.k_main_blocks) {
-                    if (!wait_warp(smem_addr(&pfull[stage]), (pbits >> stage) & 1u, abort_flag, p.status, limit)) {
-                        ok = false;
-                        break;
-                    }
-                    pbits ^= 1u << stage;
-                    const uint8_t* qs = q_ring + (size_t)stage * q_stage_bytes;
-                    const __nv_bfloat16* ss = reinterpret_cast<const __nv_bfloat16*>(s_ring + (size_t)stage * s_stage_bytes);
-                    uint8_t* bs = b_ring + (size_t)stage * b_stage_bytes;
-                    for (int r = ct; r < rows; r += kConvertThreads) {
-                        const uint4 q0 = *reinterpret_cast<const uint4*>(qs + (size_t)r * 32);
-                        const uint4 q1 = *reinterpret_cast<const uint4*>(qs + (size_t)r * 32 + 16);
-                        const __nv_bfloat162 s2 = __bfloat162bfloat162(ss[r]);
-                        const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-#pragma unroll
-                        for (int c = 0; c < 8; ++c) {
-                            const uint32_t wv = words[c] ^ 0x88888888u;  // nibbles to offset binary q + 8
-                            uint32_t o[4];
-#pragma unroll
-                            for (int pp = 0; pp < 4; ++pp) {
-                                const uint32_t v = ((wv >> (8 * pp)) & 0xFu) | (((wv >> (8 * pp + 4)) & 0xFu) << 16) |
-                                                   0x43004300u;  // bf16 pair 128 + (q + 8)
-                                __nv_bfloat162 t = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&v), magic);
-                                t = __hmul2(t, s2);
-                                o[pp] = *reinterpret_cast<const uint32_t*>(&t);
-                            }
-                            *reinterpret_cast<uint4*>(bs + (size_t)r * 128 + (((uint32_t)c ^ ((uint32_t)r & 7u)) << 4)) =
-                                make_uint4(o[0], o[1], o[2], o[3]);
-                        }
-                    }
-                    // generic stores -> visible to the tensor core (async proxy) before the arrive
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                }
-                __syncwarp();
-                if (lane == 0) {
-                    const uint32_t fb_local = smem_addr(&full[stage]);
-                    if (CG > 1)
-                        mbar_arrive_cluster(map_to_rank(fb_local, full_target_rank));
-                    else
-                        mbar_arrive(fb_local);
-                }
-                if (++stage == stages) { stage = 0; phase ^= 1; }
-            }
         }
     } else {
         // ------------------------------------------------------------ epilogue (warps 2..5)
@@ -770,28 +385,50 @@ __global__ void __launch_bounds__(QW ? kThreadsW4 : kThreads, 1)
     }
 }
 
-}  // namespace dev
-
-size_t gemm_smem_bytes(int b_tile_rows, int stages, int bk, int w4_rows) {
-    const size_t w4 = w4_rows ? (size_t)w4_rows * (bk / 2) + (((size_t)w4_rows * 2 + 127) & ~(size_t)127) : 0;
-    return 1024 + (size_t)stages * ((size_t)kTileM * bk * 2 + (size_t)b_tile_rows * bk * 2 + w4) +
-           8 * (3 * (size_t)stages + 5) + 16;
+// Plain 4-bit layout -> kernel layout, one 32-bit word (8 input features) per step:
+// feature 8c+i sits in plain nibble i (two's complement); the kernel layout puts feature
+// 8c+2j in nibble j and 8c+2j+1 in nibble j+4, offset binary (q + 8 = nibble ^ 8).
+__global__ void w4_repack_kernel(const uint32_t* src, uint32_t* dst, long long n_words) {
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n_words;
+         i += (long long)gridDim.x * blockDim.x) {
+        const uint32_t w = src[i];
+        uint32_t o = 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            o |= ((w >> (8 * j)) & 0xFu) << (4 * j);
+            o |= ((w >> (8 * j + 4)) & 0xFu) << (4 * j + 16);
+        }
+        dst[i] = o ^ 0x88888888u;
+    }
 }
 
-template <int BK, int CG, int QW>
+}  // namespace dev
+
+cudaError_t w4_repack(const void* src, void* dst, long long n_words, int grid, cudaStream_t stream) {
+    if (n_words <= 0) return cudaSuccess;
+    // src may equal dst: each thread reads its word before writing it, no other thread touches it
+    dev::w4_repack_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint32_t*>(src), static_cast<uint32_t*>(dst),
+                                                    n_words);
+    return cudaGetLastError();
+}
+
+size_t gemm_smem_bytes(int b_tile_rows, int stages, int bk) {
+    return 1024 + (size_t)stages * ((size_t)kTileM * bk * 2 + (size_t)b_tile_rows * bk * 2) +
+           8 * (2 * (size_t)stages + 5) + 16;
+}
+
+template <int BK, int CG>
 static cudaError_t set_smem_attr() {
-    return cudaFuncSetAttribute(dev::lora_gemm_kernel<BK, CG, QW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    return cudaFuncSetAttribute(dev::lora_gemm_kernel<BK, CG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 kSmemLimit);
 }
 
 cudaError_t gemm_prepare_device() {
     cudaError_t e;
-    if ((e = set_smem_attr<64, 1, 0>()) != cudaSuccess) return e;
-    if ((e = set_smem_attr<64, 2, 0>()) != cudaSuccess) return e;
-    if ((e = set_smem_attr<32, 1, 0>()) != cudaSuccess) return e;
-    if ((e = set_smem_attr<32, 2, 0>()) != cudaSuccess) return e;
-    if ((e = set_smem_attr<64, 1, 1>()) != cudaSuccess) return e;
-    return set_smem_attr<64, 2, 1>();
+    if ((e = set_smem_attr<64, 1>()) != cudaSuccess) return e;
+    if ((e = set_smem_attr<64, 2>()) != cudaSuccess) return e;
+    if ((e = set_smem_attr<32, 1>()) != cudaSuccess) return e;
+    return set_smem_attr<32, 2>();
 }
 
 static void launch_config(const GemmParams& p, int grid, cudaStream_t stream, cudaLaunchConfig_t* cfg,
@@ -799,8 +436,8 @@ static void launch_config(const GemmParams& p, int grid, cudaStream_t stream, cu
     const int b_rows = (p.tile_n > p.shrink_n ? p.tile_n : p.shrink_n) / p.cluster_size;
     memset(cfg, 0, sizeof(*cfg));
     cfg->gridDim = dim3(grid, 1, 1);
-    cfg->blockDim = dim3(p.w4 ? kThreadsW4 : kThreads, 1, 1);
-    cfg->dynamicSmemBytes = gemm_smem_bytes(b_rows, p.stages, p.bk, p.w4 ? p.tile_n / p.cluster_size : 0);
+    cfg->blockDim = dim3(kThreads, 1, 1);
+    cfg->dynamicSmemBytes = gemm_smem_bytes(b_rows, p.stages, p.bk);
     cfg->stream = stream;
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = p.cluster_size;
@@ -812,15 +449,10 @@ static void launch_config(const GemmParams& p, int grid, cudaStream_t stream, cu
 
 template <typename F>
 static cudaError_t dispatch(const GemmParams& p, F&& f) {
-    if (p.w4) {
-        if (p.bk == 64 && p.cluster_size == 1) return f(dev::lora_gemm_kernel<64, 1, 1>);
-        if (p.bk == 64 && p.cluster_size == 2) return f(dev::lora_gemm_kernel<64, 2, 1>);
-        return cudaErrorInvalidValue;
-    }
-    if (p.bk == 64 && p.cluster_size == 1) return f(dev::lora_gemm_kernel<64, 1, 0>);
-    if (p.bk == 64 && p.cluster_size == 2) return f(dev::lora_gemm_kernel<64, 2, 0>);
-    if (p.bk == 32 && p.cluster_size == 1) return f(dev::lora_gemm_kernel<32, 1, 0>);
-    if (p.bk == 32 && p.cluster_size == 2) return f(dev::lora_gemm_kernel<32, 2, 0>);
+    if (p.bk == 64 && p.cluster_size == 1) return f(dev::lora_gemm_kernel<64, 1>);
+    if (p.bk == 64 && p.cluster_size == 2) return f(dev::lora_gemm_kernel<64, 2>);
+    if (p.bk == 32 && p.cluster_size == 1) return f(dev::lora_gemm_kernel<32, 1>);
+    if (p.bk == 32 && p.cluster_size == 2) return f(dev::lora_gemm_kernel<32, 2>);
     return cudaErrorInvalidValue;
 }
 

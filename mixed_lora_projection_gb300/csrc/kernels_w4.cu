@@ -1,0 +1,476 @@
+// sm_103a kernel of the projection with a 4-bit base weight (W4A16 base, bf16 adapter).
+//
+// The 4-bit base has to be expanded to bf16 before the tensor core can use it. Doing that
+// into shared memory puts a second full-width tile through the shared-memory port on every
+// K-step, beside the TMA fills and the MMA's operand reads, and that port then sets the
+// pace. Here the dequantised weights go to tensor memory instead: the tile is transposed,
+//
+//   D[n, t] = sum_k W[n, k] X[t, k]  (+ sum_j B_a[n, j] U[t, j] for adapter tokens)
+//
+// with the unit's 128 output features n on the MMA's M side (TMEM lanes) and its tokens t
+// on N (up to 256: two planner tiles). tcgen05.mma kind::f16 reads A (the weights) from
+// tensor memory, written with tcgen05.st by the converter warps, and B (the X rows) from
+// shared memory, filled by TMA. The adapter's expand (B_a tile as A, U rows as B) runs
+// from shared memory into the same accumulator; U comes from the shrink pass, launched
+// before this kernel on the same stream.
+//
+// Per CTA (one per SM, persistent over the units, feature tile fastest):
+//   warp 0      TMA: X tiles (base K-steps), U and B_a tiles (expand K-steps);
+//   warp 1      TMEM owner (512 columns: one 128 x 256 fp32 accumulator and one 32-column
+//               stage of dequantised A per ring stage), issues the MMAs: one wait, four MMAs
+//               and one commit per K-step, as in the bf16 kernel;
+//   warps 2..5  epilogue: warp w reads lanes 32 (w % 4) .. (one output feature per thread)
+//               and writes Y[t, n] for the unit's tokens (32 lanes = 64 contiguous bytes);
+//   warps 6..13 converters: warp w dequantises whole K-steps (6..9 the even ring stages,
+//               10..13 the odd ones) for the 32 features of lane quadrant w % 4, packed
+//               ring -> TMEM, and counts itself in on the stage's full barrier;
+//   warp 14     TMA of the packed base and its scales (4 K-steps per box) into their ring.
+// Every wait is bounded as in the bf16 kernel (status word, abort flag, orderly exit).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "dev_common.cuh"
+#include "lora_internal.h"
+
+namespace lora {
+namespace dev {
+
+namespace {
+
+constexpr uint32_t kXStageBytes = 256 * 128;      // B operand: up to 256 token rows x 64 bf16
+constexpr uint32_t kQStageBytes = 128 * kW4PackBytes;   // packed rows of 4 K-steps
+constexpr uint32_t kSStageBytes = 2 * 128 * 2;          // two scale groups of 128 features
+constexpr uint32_t kAccCols4 = 256;               // accumulator columns (tokens)
+
+// D[tmem] (+)= A[tmem] * B[smem]^T, kind::f16 (bf16 in, fp32 accumulate), issued by the lane
+// with pred != 0 of a converged warp.
+__device__ __forceinline__ void mma_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate, uint32_t pred) {
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "setp.ne.b32 q, %5, 0;\n\t"
+        "@q tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(pred)
+        : "memory");
+}
+
+// 32 lanes x 32 bits x 16 columns from registers: thread i writes lane (taddr.lane + i).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* v) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0],"
+        " {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+        "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+struct W4Unit {
+    W4Group g;
+    int n0;          // first output feature
+    int n;           // MMA N of the base K-steps (tokens, multiple of 16)
+};
+
+__device__ __forceinline__ W4Unit w4_unit(const W4Params& p, const W4Group* groups, int u) {
+    W4Unit r;
+    const int gi = u / p.n_ntiles;
+    r.g = groups[gi];
+    r.n0 = (u % p.n_ntiles) * kW4TileM;
+    r.n = r.g.nrows[1] > 0 ? 128 + ((r.g.nrows[1] + 15) & ~15) : ((r.g.nrows[0] + 15) & ~15);
+    return r;
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(kW4Threads, 1) lora_w4_kernel(const __grid_constant__ W4Params p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~static_cast<uintptr_t>(1023));
+    const int stages = p.stages, pstages = p.pstages;
+    // ring stage s: base K-step -> X rows (B operand, up to 256 rows) in smem and the
+    // dequantised weights (A operand) in TMEM columns 256 + 32 s; expand K-step -> U rows
+    // (B operand) in the first 16 KB and the B_a tile (A operand) in the second 16 KB
+    uint8_t* x_ring = base;
+    uint8_t* q_ring = x_ring + (size_t)stages * kXStageBytes;
+    uint8_t* s_ring = q_ring + (size_t)pstages * kQStageBytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(s_ring + (size_t)pstages * kSStageBytes);
+    uint64_t* full = bars;                          // TMA bytes + one arrive per converter quadrant
+    uint64_t* empty = full + stages;                // MMA done with the stage (smem and TMEM)
+    uint64_t* pfull = empty + stages;               // packed rows + scales landed
+    uint64_t* pempty = pfull + pstages;             // converters done with them
+    uint64_t* tfull = pempty + pstages;             // accumulator complete
+    uint64_t* tempty = tfull + 1;                   // accumulator drained by the epilogue
+    uint64_t* drain = tempty + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < stages; ++s) {
+            mbar_init(smem_addr(&full[s]), 1 + kW4ConvertWarps / 2);
+            mbar_init(smem_addr(&empty[s]), 1);
+        }
+        for (int s = 0; s < pstages; ++s) {
+            mbar_init(smem_addr(&pfull[s]), 1);
+            mbar_init(smem_addr(&pempty[s]), kW4ConvertWarps);
+        }
+        mbar_init(smem_addr(tfull), 1);
+        mbar_init(smem_addr(tempty), kEpilogueThreads);
+        mbar_init(smem_addr(drain), 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) tmem_alloc<1>(smem_addr(tmem_slot), 2 * kAccCols4);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const uint32_t tmem_a = tmem_base + kAccCols4;  // A stages: columns 256 + 32 s
+
+    const int n_units = p.n_groups * p.n_ntiles;
+    const uint64_t limit = p.wait_limit_ns;
+    const W4Group* groups = p.inline_wl ? p.inline_groups : p.groups;
+    const CUtensorMap* bmaps = p.inline_wl ? p.inline_bmaps : p.tm_b;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA: X, U, B_a
+        const uint32_t issuer = lane == 0 ? 1u : 0u;
+        if (!p.debug_stall) {
+            if (lane == 0) {
+                tma_prefetch_desc(&p.tm_x);
+                tma_prefetch_desc(&p.tm_u);
+            }
+            __syncwarp();
+            int stage = 0;
+            uint32_t phase = 0;
+            long long issued = 0;
+            int acquired = -1;
+            bool ok = true;
+            for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+                const W4Unit w = w4_unit(p, groups, u);
+                const int ntile = w.g.nrows[1] > 0 ? 2 : 1;
+                for (int kb = 0; kb < p.k_main_blocks; ++kb) {
+                    if (!wait_warp(smem_addr(&empty[stage]), phase ^ 1, abort_flag, p.status, limit)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = smem_addr(&full[stage]);
+                    mbar_arrive_expect_tx(fb, (uint32_t)ntile * 16384u, issuer);
+                    const uint32_t xs = smem_addr(x_ring + (size_t)stage * kXStageBytes);
+                    for (int h = 0; h < ntile; ++h)
+                        tma_load_2d<1>(xs + (uint32_t)h * 16384u, &p.tm_x, fb, kb * 64, w.g.row0[h], issuer);
+                    ++issued;
+                    if (++stage == stages) { stage = 0; phase ^= 1; }
+                }
+                for (int h = 0; h < 2 && ok; ++h) {
+                    const int a = w.g.adapter[h];
+                    if (w.g.nrows[h] == 0 || a == 0) continue;
+                    const CUtensorMap* bm = &bmaps[a - 1];
+                    if (!p.inline_wl && acquired != a) {
+                        tensormap_acquire(bm);
+                        acquired = a;
+                    }
+                    for (int kr = 0; kr < p.k_lora_blocks; ++kr) {
+                        if (!wait_warp(smem_addr(&empty[stage]), phase ^ 1, abort_flag, p.status, limit)) {
+                            ok = false;
+                            break;
+                        }
+                        const uint32_t fb = smem_addr(&full[stage]);
+                        mbar_arrive_expect_tx(fb, 32768u, issuer);
+                        const uint32_t xs = smem_addr(x_ring + (size_t)stage * kXStageBytes);
+                        tma_load_2d<1>(xs, &p.tm_u, fb, kr * 64, w.g.row0[h], issuer);
+                        tma_load_2d<1>(xs + 16384u, bm, fb, kr * 64, w.n0, issuer);
+                        ++issued;
+                        if (++stage == stages) { stage = 0; phase ^= 1; }
+                    }
+                }
+            }
+            if (lane == 0 && !ok) {
+                // wait (bounded, ignoring the abort flag) for the copies still in flight
+                long long first = issued > stages ? issued - stages : 0;
+                for (long long j = first; j < issued; ++j)
+                    wait_bounded(smem_addr(&full[j % stages]), (uint32_t)((j / stages) & 1), abort_flag, p.status,
+                                 limit, false);
+            }
+        }
+    } else if (warp == 14) {
+        // ------------------------------------------------------------ TMA: packed base + scales
+        const uint32_t issuer = lane == 0 ? 1u : 0u;
+        if (!p.debug_stall) {
+            if (lane == 0) {
+                tma_prefetch_desc(&p.tm_wq);
+                tma_prefetch_desc(&p.tm_ws);
+            }
+            __syncwarp();
+            int ps = 0;
+            uint32_t pph = 0;
+            long long issued = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+                const int n0 = (u % p.n_ntiles) * kW4TileM;
+                for (int pb = 0; pb < p.k_pack_blocks; ++pb) {
+                    if (!wait_warp(smem_addr(&pempty[ps]), pph ^ 1, abort_flag, p.status, limit)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t pbar = smem_addr(&pfull[ps]);
+                    mbar_arrive_expect_tx(pbar, kQStageBytes + kSStageBytes, issuer);
+                    tma_load_2d<1>(smem_addr(q_ring + (size_t)ps * kQStageBytes), &p.tm_wq, pbar, pb * kW4PackBytes,
+                                   n0, issuer);
+                    tma_load_2d<1>(smem_addr(s_ring + (size_t)ps * kSStageBytes), &p.tm_ws, pbar, n0, 2 * pb, issuer);
+                    ++issued;
+                    if (++ps == pstages) { ps = 0; pph ^= 1; }
+                }
+            }
+            if (lane == 0 && !ok) {
+                long long first = issued > pstages ? issued - pstages : 0;
+                for (long long j = first; j < issued; ++j)
+                    wait_bounded(smem_addr(&pfull[j % pstages]), (uint32_t)((j / pstages) & 1), abort_flag, p.status,
+                                 limit, false);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        const uint32_t issuer = lane == 0 ? 1u : 0u;
+        int stage = 0;
+        uint32_t phase = 0;
+        int it = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++it) {
+            const W4Unit w = w4_unit(p, groups, u);
+            if (!wait_warp(smem_addr(tempty), (it & 1) ^ 1, abort_flag, p.status, limit)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            // Stages are taken two at a time: a shared-memory read by this warp (the barrier
+            // wait) does not complete before the MMAs it issued earlier have, so each wait
+            // costs a drain of the tensor pipe; eight MMAs per wait hide it where four do not.
+            const uint32_t idesc = instr_desc_bf16(kW4TileM, w.n);
+            for (int kb = 0; kb < p.k_main_blocks; kb += 2) {   // k_main_blocks is even (d_in % 128 == 0)
+                int st1 = stage + 1;
+                uint32_t ph1 = phase;
+                if (st1 == stages) { st1 = 0; ph1 ^= 1; }
+                if (!wait_warp(smem_addr(&full[stage]), phase, abort_flag, p.status, limit) ||
+                    !wait_warp(smem_addr(&full[st1]), ph1, abort_flag, p.status, limit)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const int st = j ? st1 : stage;
+                    const uint64_t bd = smem_desc<64>(smem_addr(x_ring + (size_t)st * kXStageBytes));
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        mma_tmem_a(tmem_base, tmem_a + (uint32_t)(32 * st + 8 * k), bd + (uint64_t)(2 * k), idesc,
+                                   (kb > 0 || j > 0 || k > 0) ? 1u : 0u, issuer);
+                    mma_commit<1>(smem_addr(&empty[st]), issuer);
+                }
+                stage = st1 + 1;
+                phase = ph1;
+                if (stage == stages) { stage = 0; phase ^= 1; }
+            }
+            const uint32_t idesc_e = instr_desc_bf16(kW4TileM, 128);
+            for (int h = 0; h < 2 && ok; ++h) {
+                if (w.g.nrows[h] == 0 || w.g.adapter[h] == 0) continue;
+                for (int kr = 0; kr < p.k_lora_blocks; kr += 2) {
+                    const int ns = kr + 1 < p.k_lora_blocks ? 2 : 1;
+                    int st1 = stage + 1;
+                    uint32_t ph1 = phase;
+                    if (st1 == stages) { st1 = 0; ph1 ^= 1; }
+                    if (!wait_warp(smem_addr(&full[stage]), phase, abort_flag, p.status, limit) ||
+                        (ns == 2 && !wait_warp(smem_addr(&full[st1]), ph1, abort_flag, p.status, limit))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    for (int j = 0; j < ns; ++j) {
+                        const int st = j ? st1 : stage;
+                        const uint32_t xs = smem_addr(x_ring + (size_t)st * kXStageBytes);
+                        const uint64_t ad = smem_desc<64>(xs + 16384u);
+                        const uint64_t bd = smem_desc<64>(xs);
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            mma_bf16<1>(tmem_base + (uint32_t)(128 * h), ad + (uint64_t)(2 * k),
+                                        bd + (uint64_t)(2 * k), idesc_e, 1u, issuer);
+                        mma_commit<1>(smem_addr(&empty[st]), issuer);
+                    }
+                    if (ns == 2) {
+                        stage = st1 + 1;
+                        phase = ph1;
+                    } else {
+                        stage = st1;
+                        phase = ph1;
+                        continue;
+                    }
+                    if (stage == stages) { stage = 0; phase ^= 1; }
+                }
+            }
+            if (!ok) break;
+            mma_commit<1>(smem_addr(tfull), issuer);
+        }
+        // every MMA this warp issued has completed before TMEM is released
+        mma_commit_local<1>(smem_addr(drain), issuer);
+        if (lane == 0) wait_bounded(smem_addr(drain), 0, abort_flag, p.status, limit, false);
+    } else if (warp >= 6) {
+        // ------------------------------------------------------------ converters (warps 6..13)
+        // Kernel layout of the packed base (lora_linear_w4_repack): 32-bit word c of a row's
+        // K-step holds inputs 8c..8c+7 as offset-binary nibbles (q + 8), input 8c+2j in nibble
+        // j and 8c+2j+1 in nibble j+4. ((word >> 4j) & 0x000F000F) | 0x43004300 is then the
+        // bf16 pair (128 + q + 8) of inputs (8c+2j, 8c+2j+1), exact; minus 136 is q exactly,
+        // and one round-to-nearest-even multiply gives q * s. The pair is one TMEM column.
+        // Warp w serves the ring stages of parity (w - 6) / 4 for the 32 features of lane
+        // quadrant w % 4: a whole base K-step (64 inputs, 32 columns) per stage, and on
+        // expand K-steps only its arrive on the stage's full barrier.
+        const int q = warp & 3;                       // lane quadrant: features 32q .. 32q+31
+        const int par = (warp - 6) >> 2;              // ring-stage parity this warp serves
+        const int nl = 32 * q + lane;                 // feature within the unit
+        const uint32_t lane_off = (uint32_t)(32 * q) << 16;
+        const __nv_bfloat162 magic = __floats2bfloat162_rn(136.0f, 136.0f);
+        int ps = 0, stage = 0;
+        uint32_t pph = 0, phase = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+            const W4Unit w = w4_unit(p, groups, u);
+            for (int kb = 0; kb < p.k_main_blocks; ++kb) {
+                if ((kb & 3) == 0 &&
+                    !wait_warp(smem_addr(&pfull[ps]), pph, abort_flag, p.status, limit)) {
+                    ok = false;
+                    break;
+                }
+                if ((stage & 1) == par) {
+                    // the packed box rows are 128 bytes, 128-byte swizzled: 16-byte chunk c of
+                    // row r sits at chunk c ^ (r % 8)
+                    const uint8_t* row = q_ring + (size_t)ps * kQStageBytes + (size_t)nl * kW4PackBytes;
+                    const uint32_t c0 = (uint32_t)(2 * (kb & 3)) ^ (uint32_t)(nl & 7);
+                    const uint32_t c1 = (uint32_t)(2 * (kb & 3) + 1) ^ (uint32_t)(nl & 7);
+                    const uint4 q0 = *reinterpret_cast<const uint4*>(row + (c0 << 4));
+                    const uint4 q1 = *reinterpret_cast<const uint4*>(row + (c1 << 4));
+                    const __nv_bfloat16* ss =
+                        reinterpret_cast<const __nv_bfloat16*>(s_ring + (size_t)ps * kSStageBytes);
+                    const __nv_bfloat162 s2 = __bfloat162bfloat162(ss[((kb & 3) >> 1) * 128 + nl]);
+                    const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+                    uint32_t o[32];
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const uint32_t v = ((words[c] >> (4 * j)) & 0x000F000Fu) | 0x43004300u;
+                            __nv_bfloat162 t = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&v), magic);
+                            t = __hmul2(t, s2);
+                            o[4 * c + j] = *reinterpret_cast<const uint32_t*>(&t);
+                        }
+                    }
+                    if (!wait_warp(smem_addr(&empty[stage]), phase ^ 1, abort_flag, p.status, limit)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t ta = tmem_a + lane_off + (uint32_t)(32 * stage);
+                    tmem_st16(ta, o);
+                    tmem_st16(ta + 16u, o + 16);
+                    tmem_st_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_addr(&full[stage]));
+                }
+                if ((kb & 3) == 3 || kb == p.k_main_blocks - 1) {
+                    // this packed slot is read (by this warp's K-steps in it): hand it back
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_addr(&pempty[ps]));
+                    if (++ps == pstages) { ps = 0; pph ^= 1; }
+                }
+                if (++stage == stages) { stage = 0; phase ^= 1; }
+            }
+            // expand K-steps: no weights to convert, only this quadrant's arrive
+            for (int h = 0; h < 2 && ok; ++h) {
+                if (w.g.nrows[h] == 0 || w.g.adapter[h] == 0) continue;
+                for (int kr = 0; kr < p.k_lora_blocks; ++kr) {
+                    if ((stage & 1) == par) {
+                        if (!wait_warp(smem_addr(&empty[stage]), phase ^ 1, abort_flag, p.status, limit)) {
+                            ok = false;
+                            break;
+                        }
+                        if (lane == 0) mbar_arrive(smem_addr(&full[stage]));
+                        __syncwarp();
+                    }
+                    if (++stage == stages) { stage = 0; phase ^= 1; }
+                }
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue (warps 2..5)
+        const int q = warp & 3;
+        const uint32_t lane_off = (uint32_t)(32 * q) << 16;
+        __nv_bfloat16* y = reinterpret_cast<__nv_bfloat16*>(p.y);
+        int it = 0;
+        for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++it) {
+            const W4Unit w = w4_unit(p, groups, u);
+            int ok = 1;
+            if (lane == 0) ok = wait_bounded(smem_addr(tfull), it & 1, abort_flag, p.status, limit, true);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            tc_fence_after();
+            const int n = w.n0 + 32 * q + lane;
+            const bool n_ok = n < p.d_out;
+            for (int h = 0; h < 2; ++h) {
+                const int rows = w.g.nrows[h];
+                for (int c = 0; c < rows; c += 32) {
+                    uint32_t v[32];
+                    const uint32_t taddr = tmem_base + lane_off + (uint32_t)(128 * h + c);
+                    tmem_ld16(taddr, v);
+                    tmem_ld16(taddr + 16u, v + 16);
+                    tmem_ld_wait();
+                    if (n_ok) {
+                        __nv_bfloat16* col = y + (size_t)(w.g.row0[h] + c) * p.d_out + n;
+                        const int m = rows - c < 32 ? rows - c : 32;
+#pragma unroll
+                        for (int t = 0; t < 32; ++t)
+                            if (t < m) col[(size_t)t * p.d_out] = __float2bfloat16_rn(__uint_as_float(v[t]));
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(smem_addr(tempty));
+        }
+    }
+
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc<1>(tmem_base, 2 * kAccCols4);
+    }
+}
+
+}  // namespace dev
+
+size_t w4_smem_bytes(int stages, int pstages) {
+    return 1024 + (size_t)stages * dev::kXStageBytes + (size_t)pstages * (dev::kQStageBytes + dev::kSStageBytes) +
+           8 * (2 * (size_t)stages + 2 * (size_t)pstages + 3) + 16;
+}
+
+cudaError_t w4_prepare_device() {
+    return cudaFuncSetAttribute(dev::lora_w4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+}
+
+cudaError_t launch_w4(const W4Params& p, int grid, cudaStream_t stream) {
+    // the TMEM A stages sit in columns 256 + 32 s; the converters' warp sets take alternate stages
+    if (w4_smem_bytes(p.stages, p.pstages) > (size_t)kSmemLimit || p.stages < 2 || p.stages > kW4AStages ||
+        (p.stages & 1) || p.pstages < 2)
+        return cudaErrorInvalidValue;
+    dev::lora_w4_kernel<<<grid, kW4Threads, w4_smem_bytes(p.stages, p.pstages), stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace lora

@@ -17,9 +17,7 @@ constexpr int kStageBytesA = kTileM * kTileK * 2;      // 16 KB at K = 64
 constexpr int kMaxStages = 16;
 constexpr int kSmemLimit = 232448;                     // opt-in dynamic shared memory per CTA (227 KB)
 constexpr int kThreads = 192;        // warp 0 TMA, warp 1 MMA + TMEM owner, warps 2..5 epilogue
-constexpr int kThreadsW4 = 320;      // + warps 6..9: dequantise 4-bit base tiles into bf16
 constexpr int kEpilogueThreads = 128;
-constexpr int kConvertThreads = 128;
 constexpr int kW4Group = 128;        // input features per scale of a 4-bit base
 // Work lists this small travel inside the kernel parameters (no upload copy per call).
 constexpr int kInlineTiles = 64;     // fused + shrink tiles (cluster groups included)
@@ -53,8 +51,6 @@ struct GemmParams {
     CUtensorMap tm_x;                // X [T, d_in], box 64 x 128
     CUtensorMap tm_w;                // W [d_out, d_in], box 64 x tile_n
     CUtensorMap tm_u;                // U [u_rows, rank], box 64 x 128
-    CUtensorMap tm_wq;               // 4-bit base: packed W uint8 [d_out, d_in/2], box 32 x tile_n/cs
-    CUtensorMap tm_ws;               // 4-bit base: scales bf16 [d_in/128, d_out], box tile_n/cs x 1
     const CUtensorMap* tm_b;         // device array per compact adapter: B_a [d_out, rank], box 64 x tile_n
     const CUtensorMap* tm_a;         // device array per compact adapter: A_a [rank, d_in], box 64 x shrink_n
     const Tile* shrink_tiles;        // device [n_shrink]
@@ -85,7 +81,46 @@ struct GemmParams {
     int rank;
     int cluster_size;                // CTA group of the MMA: 1, or 2 (an SM pair, M = 256)
     int bk;                          // K per pipeline stage: 64 (128-byte swizzle) or 32 (64-byte swizzle)
-    int w4;                          // 1: the base weight is 4-bit (tm_wq, tm_ws) instead of tm_w
+    int debug_stall;
+};
+
+// 4-bit base kernel (transposed tile: output features on the MMA's M side, tokens on N).
+// A token group is one or two consecutive planner tiles (each <= 128 rows and one adapter);
+// its X rows form the B operand of up to 256 columns. Units = groups x output tiles of 128
+// features, feature tile fastest.
+constexpr int kW4TileM = 128;         // output features per unit (TMEM lanes)
+constexpr int kW4Threads = 480;       // warp 0 TMA (X, U, B_a), 1 MMA, 2..5 epilogue,
+                                      // 6..13 dequantise into TMEM, 14 TMA of the packed base
+constexpr int kW4ConvertWarps = 8;
+constexpr int kW4AStages = 8;         // most ring stages (TMEM A stages of 32 columns each)
+constexpr int kW4InlineGroups = 48;
+constexpr int kW4PackBytes = 128;     // packed bytes per row per TMA box (4 K-steps of 64)
+
+struct W4Group {
+    int32_t row0[2], nrows[2], adapter[2];  // second tile absent when nrows[1] == 0
+};
+
+struct W4Params {
+    CUtensorMap inline_bmaps[kInlineAdapters];  // B_a [d_out, rank], box 64 x 128 (inline work list)
+    W4Group inline_groups[kW4InlineGroups];
+    int inline_wl;
+    CUtensorMap tm_x;                // X [T, d_in] bf16, box 64 x 128, 128-byte swizzle
+    CUtensorMap tm_u;                // U [u_rows, rank] bf16, box 64 x 128, 128-byte swizzle
+    CUtensorMap tm_wq;               // packed base [d_out, d_in/2] u8 (kernel layout), box 128 x 128, swizzled
+    CUtensorMap tm_ws;               // scales [d_in/128, d_out] bf16, box 128 x 2
+    const CUtensorMap* tm_b;         // device array per compact adapter (when not inline)
+    const W4Group* groups;           // device array (when not inline)
+    void* y;                         // Y [T, d_out] bf16
+    int* status;
+    unsigned long long wait_limit_ns;
+    int n_groups;
+    int n_ntiles;                    // ceil(d_out / 128)
+    int k_main_blocks;               // ceil(d_in / 64)
+    int k_lora_blocks;               // ceil(rank / 64)
+    int k_pack_blocks;               // ceil(k_main_blocks / 4)
+    int d_out;
+    int stages;                      // X / U ring
+    int pstages;                     // packed ring
     int debug_stall;
 };
 
@@ -101,9 +136,15 @@ int plan_segments(const int32_t* seg_offsets, const int32_t* seg_ids, int n_seg,
                   int n_adapters, Plan* plan);
 
 // kernels.cu
-size_t gemm_smem_bytes(int b_tile_rows, int stages, int bk, int w4_rows = 0);
+size_t gemm_smem_bytes(int b_tile_rows, int stages, int bk);
 cudaError_t gemm_prepare_device();           // sets the opt-in smem limit on the current device
 cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t stream);
 int gemm_max_clusters(const GemmParams& p);  // co-resident clusters of this launch shape
+cudaError_t w4_repack(const void* src, void* dst, long long n_words, int grid, cudaStream_t stream);
+
+// kernels_w4.cu
+size_t w4_smem_bytes(int stages, int pstages);
+cudaError_t w4_prepare_device();
+cudaError_t launch_w4(const W4Params& p, int grid, cudaStream_t stream);
 
 }  // namespace lora

@@ -75,6 +75,24 @@ def validate(d_in, d_out, rank, max_tokens, max_segments, x_ptr, T, seg_offsets,
                                     S if scales is not None else None, na, y_ptr)
 
 
+def w4_repack(src: torch.Tensor, dst: torch.Tensor | None = None,
+              stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+    """4-bit base weight, plain layout (uint8 [d_out, d_in/2], low nibble = even input,
+    two's complement) -> the kernel layout that ``forward_w4`` reads. ``dst`` may be ``src``."""
+    lib = L.load()
+    if src.dtype != torch.uint8 or not src.is_contiguous() or src.device.type != "cuda":
+        raise TypeError("src must be a contiguous uint8 CUDA tensor")
+    if dst is None:
+        dst = torch.empty_like(src)
+    if dst.dtype != torch.uint8 or not dst.is_contiguous() or dst.device != src.device or dst.numel() != src.numel():
+        raise TypeError("dst must be a contiguous uint8 tensor of src's size on src's device")
+    s = stream if stream is not None else torch.cuda.current_stream(src.device)
+    with torch.cuda.device(src.device):
+        _check(lib.lora_linear_w4_repack(src.data_ptr(), dst.data_ptr(), src.numel(), C.c_void_p(s.cuda_stream)),
+               "lora_linear_w4_repack")
+    return dst
+
+
 class LoraLinear:
     """One handle: a projection shape (d_in -> d_out, rank r) on one CUDA device."""
 
@@ -139,8 +157,8 @@ class LoraLinear:
 
     def forward_w4(self, x: torch.Tensor, seg_offsets, seg_ids, Wq: torch.Tensor, Ws: torch.Tensor, A, B, scales,
                    y: torch.Tensor | None = None, stream: torch.cuda.Stream | None = None) -> torch.Tensor:
-        """Same with a 4-bit base: Wq uint8 [d_out, d_in/2] (low nibble = even input), Ws bf16
-        [d_in/128, d_out]; W[n,k] = q[n,k] * Ws[k//128, n]."""
+        """Same with a 4-bit base: Wq uint8 [d_out, d_in/2] in the kernel layout (``w4_repack`` of
+        the plain layout), Ws bf16 [d_in/128, d_out]; W[n,k] = q[n,k] * Ws[k//128, n]."""
         if Wq.dtype != torch.uint8 or not Wq.is_contiguous() or Wq.device != self.device:
             raise TypeError("Wq must be a contiguous uint8 tensor on the handle's device")
         T = x.shape[0]

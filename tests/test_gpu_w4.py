@@ -1,5 +1,6 @@
-"""GPU parity of the 4-bit-base path (lora_linear_forward_w4) against the fp64 oracle on the
-same seeded inputs: W[n,k] = q[n,k] * s[k//128, n], adapters in bf16."""
+"""GPU parity of the 4-bit-base path (lora_linear_w4_repack + lora_linear_forward_w4) against
+the fp64 oracle on the same seeded inputs: W[n,k] = q[n,k] * s[k//128, n], adapters in bf16.
+The oracle reads the plain layout; the library reads the kernel layout written by its repack."""
 import numpy as np
 import pytest
 import torch
@@ -25,6 +26,22 @@ def dev():
 def _ll(w, max_segments=64):
     from mixed_lora_projection_gb300 import LoraLinear
     return LoraLinear(w.d_in, w.d_out, w.rank, max(w.T, 1), max_segments, 0)
+
+
+def _kq(q):
+    from mixed_lora_projection_gb300 import w4_repack
+    return w4_repack(q)
+
+
+def _kernel_layout_np(q):
+    """The kernel layout, restated from the header's description, one word at a time."""
+    w = np.ascontiguousarray(q.cpu().numpy()).view(np.uint32).astype(np.uint64)
+    out = np.zeros_like(w)
+    for j in range(4):
+        out |= ((w >> (8 * j)) & 0xF) << (4 * j)           # feature 8c+2j -> nibble j
+        out |= ((w >> (8 * j + 4)) & 0xF) << (4 * j + 16)  # feature 8c+2j+1 -> nibble j+4
+    out ^= 0x88888888                                      # offset binary q + 8
+    return out.astype(np.uint32).view(np.uint8).reshape(q.shape)
 
 
 def _oracle(inp, q, sc, off, ids, rows=None):
@@ -60,7 +77,7 @@ def test_w4_small_shapes_match_oracle(dev, case, cluster):
     q, sc = make_w4_base(w, dev)
     with _ll(w) as ll:
         ll.set_option(L.OPT_CLUSTER, cluster if T > 128 else 1)
-        y = ll.forward_w4(inp.x, off, ids, q, sc, inp.a, inp.b, inp.scales)
+        y = ll.forward_w4(inp.x, off, ids, _kq(q), sc, inp.a, inp.b, inp.scales)
         torch.cuda.synchronize()
         assert ll.status() == 0
     assert rel_err(y, _oracle(inp, q, sc, off, ids)) <= TOL
@@ -75,7 +92,7 @@ def test_w4_dequantisation_is_exact_per_weight(dev):
     inp.x.fill_diagonal_(1.0)
     q, sc = make_w4_base(w, dev)
     with _ll(w) as ll:
-        y = ll.forward_w4(inp.x, [0, d_in], [0], q, sc, inp.a, inp.b, inp.scales)
+        y = ll.forward_w4(inp.x, [0, d_in], [0], _kq(q), sc, inp.a, inp.b, inp.scales)
     torch.cuda.synchronize()
     wd = w4_dequantize_fp64(q.cpu().numpy(), bf16_bits(sc))          # exact q * s
     want = torch.from_numpy(wd.T.copy()).to(torch.bfloat16)           # rounded once, RNE
@@ -89,7 +106,7 @@ def test_w4_full_size_sampled_rows(dev, name):
     q, sc = make_w4_base(w, dev)
     off, ids = list(w.seg_offsets), list(w.seg_ids)
     with _ll(w) as ll:
-        y = ll.forward_w4(inp.x, off, ids, q, sc, inp.a, inp.b, inp.scales)
+        y = ll.forward_w4(inp.x, off, ids, _kq(q), sc, inp.a, inp.b, inp.scales)
         torch.cuda.synchronize()
         assert ll.status() == 0
     rows = sample_rows(w.T, off, ids, n_random=128, seed=5)
@@ -115,8 +132,34 @@ def test_w4_host_buffers_match_device_path(dev, name):
     q, sc = make_w4_base(w, dev) if w.d_in % 128 == 0 else (None, None)
     x_host = inp.x.cpu().pin_memory()
     y_host = torch.empty((w.T, w.d_out), dtype=torch.bfloat16).pin_memory()
+    kq = _kq(q)
     with _ll(w) as ll:
-        y = ll.forward_w4(inp.x, w.seg_offsets, w.seg_ids, q, sc, inp.a, inp.b, inp.scales)
-        ll.forward_host_w4(x_host, w.seg_offsets, w.seg_ids, q, sc, inp.a, inp.b, inp.scales, y_host)
+        y = ll.forward_w4(inp.x, w.seg_offsets, w.seg_ids, kq, sc, inp.a, inp.b, inp.scales)
+        ll.forward_host_w4(x_host, w.seg_offsets, w.seg_ids, kq, sc, inp.a, inp.b, inp.scales, y_host)
     torch.cuda.synchronize()
     assert rel_err(y_host, f64(y)) <= TOL
+
+
+def test_w4_repack_layout_bit_exact(dev):
+    w = WORKLOADS["sweep_o"]
+    q, _ = make_w4_base(w, dev)
+    got = _kq(q)
+    torch.cuda.synchronize()
+    assert np.array_equal(got.cpu().numpy(), _kernel_layout_np(q))
+    # in place gives the same bytes
+    q2 = q.clone()
+    from mixed_lora_projection_gb300 import w4_repack
+    w4_repack(q2, q2)
+    torch.cuda.synchronize()
+    assert torch.equal(q2, got)
+
+
+def test_w4_repack_rejects_bad_arguments(dev):
+    from mixed_lora_projection_gb300 import _lib as L
+    lib = L.load()
+    buf = torch.zeros(64, dtype=torch.uint8, device=dev)
+    p = buf.data_ptr()
+    assert lib.lora_linear_w4_repack(p, p, 6, None) == L.LORA_EINVAL        # not whole words
+    assert lib.lora_linear_w4_repack(p + 1, p + 1, 8, None) == L.LORA_EINVAL  # misaligned
+    assert lib.lora_linear_w4_repack(p, p + 4, 32, None) == L.LORA_EINVAL    # partial overlap
+    assert lib.lora_linear_w4_repack(p, p, 0, None) == L.LORA_OK             # nothing to do
