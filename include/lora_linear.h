@@ -207,11 +207,12 @@ enum {
     LORA_OPT_TWO_LAUNCH = 6,    /* 1 = shrink and fused pass as two launches (default 0: one launch) */
     LORA_OPT_CLUSTER = 7,       /* 0 = auto, 1 = one CTA per tile, 2 = SM pairs run M = 256 MMAs (tcgen05 cta_group::2) */
     LORA_OPT_RASTER_GROUP = 8,  /* column tiles per group for LORA_OPT_RASTER = 3 (default 4) */
-    LORA_OPT_L2_HINTS = 9,      /* L2 eviction priorities, bit mask: 1 = weights evict_last, 2 = activations
-                                   evict_first (with 8: evict_normal), 4 = output stores evict_first */
+    /* 9: retired (L2 eviction hints measured no gain and were removed; rejected with LORA_EINVAL) */
     LORA_OPT_TILE_K = 10,       /* K per pipeline stage: 0 = auto, 32 or 64 */
-    LORA_OPT_INLINE_WORK_LIST = 11 /* 1 (default) = small work lists travel in the kernel parameters,
+    LORA_OPT_INLINE_WORK_LIST = 11, /* 1 (default) = small work lists travel in the kernel parameters,
                                       0 = always upload them to device memory */
+    LORA_OPT_MMA_GROUP = 12     /* pipeline stages the MMA warp waits for at once: 0 = auto (2 for SM
+                                   pairs, 1 for single CTAs), 1 or 2 */
 };
 
 /* lora_linear_set_option -- set one option above. Returns LORA_OK or LORA_EINVAL. */

@@ -75,7 +75,7 @@ struct lora_linear {
     EncodeTiledFn encode = nullptr;
     // options
     int force_tile_n = 0, raster = 0, debug_stall = 0, timing = 0, two_launch = 0, cluster = 0;
-    int raster_group = 4, l2_hints = 0, tile_k = 0, allow_inline = 1;
+    int raster_group = 4, tile_k = 0, allow_inline = 1, mma_group = 0;  // 0: 2 for SM pairs, else 1
     int max_clusters_cache[2][kMaxTileN / 16 + 1] = {};  // co-resident clusters by (size, B rows)
     std::unordered_map<uint64_t, uint32_t> shape_cache;   // plan signature -> (cs << 16) | tile_n
     unsigned long long wait_limit_ns = 4000000000ull;
@@ -279,11 +279,11 @@ int max_clusters(lora_linear* h, const GemmParams& p) {
 // Per-SM cycles of one 64-wide K-step of an N-column unit, measured on GB300: a single CTA
 // is bound by how fast its shared memory fills (A + B tile, ~61 bytes per clock); an SM pair
 // lands only half of B per SM and is bound by the MMA stream (N/2 cycles per K=16 MMA, plus
-// the per-step barrier round trip) and the pair's coupling.
+// the per-step barrier round trip, paid once per two K-steps) and the pair's coupling.
 double kstep_cycles(int cs, int n) {
     const double mma = 4.0 * std::max(n / 2.0, 48.0) + 130.0;
     const double fill = (kTileM + (double)n / cs) * kTileK * 2.0 / 61.0;
-    return cs == 1 ? std::max(fill, mma) : 1.2 * std::max(fill, mma);
+    return cs == 1 ? std::max(fill, mma) : 1.1 * std::max(fill, mma);
 }
 
 // Makespan (per-SM cycles) of the persistent round-robin schedule of one launch shape.
@@ -560,16 +560,16 @@ int lora_linear_set_option(lora_linear* h, int option, long long value) {
             if (value < 1 || value > 4096) return LORA_EINVAL;
             h->raster_group = (int)value;
             return LORA_OK;
+        case LORA_OPT_MMA_GROUP:
+            if (value < 0 || value > 2) return LORA_EINVAL;
+            h->mma_group = (int)value;
+            return LORA_OK;
         case LORA_OPT_INLINE_WORK_LIST:
             h->allow_inline = value ? 1 : 0;
             return LORA_OK;
         case LORA_OPT_TILE_K:
             if (value != 0 && value != 32 && value != 64) return LORA_EINVAL;
             h->tile_k = (int)value;
-            return LORA_OK;
-        case LORA_OPT_L2_HINTS:
-            if (value < 0 || value > 15) return LORA_EINVAL;
-            h->l2_hints = (int)value;
             return LORA_OK;
         case LORA_OPT_TWO_LAUNCH:
             h->two_launch = value ? 1 : 0;
@@ -826,10 +826,10 @@ int forward_impl(lora_linear* h, const void* x, int T, const int32_t* seg_offset
     p.stages = sh.stages;
     p.m_fastest = sh.m_fastest;
     p.raster_group = h->raster_group;
-    p.l2_hints = h->l2_hints;
     p.k_main_blocks = ceil_div(h->d_in, bk);
     p.k_lora_blocks = ceil_div(h->rank, bk);
     p.bk = bk;
+    p.mma_group = h->mma_group ? h->mma_group : (cs > 1 ? 2 : 1);
     p.d_out = h->d_out;
     p.rank = h->rank;
     p.cluster_size = cs;

@@ -284,22 +284,42 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
                 }
                 tc_fence_after();
                 const uint32_t d = tmem_base + (uint32_t)(acc * kAccCols);
-                for (int kb = 0; kb < w.nk; ++kb) {
-                    if (!wait_warp(smem_addr(&full[stage]), phase, abort_flag, p.status, limit)) {
+                // With mma_group 2 the stages are taken two at a time: a shared-memory read by
+                // this warp (the barrier wait) does not complete before the MMAs it issued
+                // earlier have, so each wait drains the tensor pipe; one wait per two K-steps
+                // halves those drains.
+                for (int kb = 0; kb < w.nk;) {
+                    const int ns = (p.mma_group > 1 && kb + 1 < w.nk) ? 2 : 1;
+                    int st1 = stage + 1;
+                    uint32_t ph1 = phase;
+                    if (st1 == stages) { st1 = 0; ph1 ^= 1; }
+                    if (!wait_warp(smem_addr(&full[stage]), phase, abort_flag, p.status, limit) ||
+                        (ns == 2 && !wait_warp(smem_addr(&full[st1]), ph1, abort_flag, p.status, limit))) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t ad = smem_desc<BK>(smem_addr(a_ring + (size_t)stage * kStageA));
-                    const uint64_t bd = smem_desc<BK>(smem_addr(b_ring + (size_t)stage * b_stage_bytes));
+                    for (int j = 0; j < ns; ++j) {
+                        const int st = j ? st1 : stage;
+                        const uint64_t ad = smem_desc<BK>(smem_addr(a_ring + (size_t)st * kStageA));
+                        const uint64_t bd = smem_desc<BK>(smem_addr(b_ring + (size_t)st * b_stage_bytes));
 #pragma unroll
-                    for (int k = 0; k < BK / 16; ++k) {
-                        // advance 16 bf16 = 32 bytes along K inside the swizzled rows
-                        mma_bf16<CG>(d, ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), idesc,
-                                     (kb > 0 || k > 0) ? 1u : 0u, issuer);
+                        for (int k = 0; k < BK / 16; ++k) {
+                            // advance 16 bf16 = 32 bytes along K inside the swizzled rows
+                            mma_bf16<CG>(d, ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), idesc,
+                                         (kb + j > 0 || k > 0) ? 1u : 0u, issuer);
+                        }
+                        mma_commit<CG>(smem_addr(&empty[st]), issuer);
                     }
-                    mma_commit<CG>(smem_addr(&empty[stage]), issuer);
-                    if (++stage == stages) { stage = 0; phase ^= 1; }
+                    if (ns == 2) {
+                        stage = st1 + 1;
+                        phase = ph1;
+                        if (stage == stages) { stage = 0; phase ^= 1; }
+                    } else {
+                        stage = st1;
+                        phase = ph1;
+                    }
+                    kb += ns;
                 }
                 if (!ok) break;
                 mma_commit<CG>(smem_addr(&tfull[acc]), issuer);

@@ -73,14 +73,13 @@ struct GemmParams {
     int stages;
     int m_fastest;                   // 1: row tiles first, 0: column tiles first, 2: column-tile groups
     int raster_group;                // column tiles per group when m_fastest == 2
-    int l2_hints;                    // bit 0: B loads evict_last, 1: A loads evict_first (8: normal),
-                                     // 2: Y stores evict_first
     int k_main_blocks;               // ceil(d_in / 64)
     int k_lora_blocks;               // ceil(rank / 64)
     int d_out;
     int rank;
     int cluster_size;                // CTA group of the MMA: 1, or 2 (an SM pair, M = 256)
     int bk;                          // K per pipeline stage: 64 (128-byte swizzle) or 32 (64-byte swizzle)
+    int mma_group;                   // stages the MMA warp waits for at once (1 or 2)
     int debug_stall;
 };
 

@@ -247,6 +247,7 @@ extern "C" int lora_linear_forward_noalloc(const void* x, int T, const int32_t* 
     p.cluster_size = 1;
     p.raster_group = 1;
     p.bk = lora::kTileK;
+    p.mma_group = 1;  // single CTAs: one stage per wait
     // two launches ordered by the stream: the shrink units, then the fused units
     if (plan.n_shrink > 0) {
         GemmParams s = p;

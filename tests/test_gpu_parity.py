@@ -194,6 +194,32 @@ def test_k_step_32_equals_64(dev, name):
     assert torch.equal(y64, y32)
 
 
+@pytest.mark.parametrize("cluster", [1, 2])
+@pytest.mark.parametrize("case", [(300, 320, 272, 64), (517, 384, 1000, 128)], ids=["odd_k_steps", "even_k_steps"])
+def test_mma_grouping_is_exact(dev, case, cluster):
+    # the MMA warp waiting for one or two stages at once issues the same MMA sequence; an odd
+    # number of K-steps per unit (5 base + 1 expand) exercises the single-stage tail
+    from mixed_lora_projection_gb300 import _lib as L
+    T, d_in, d_out, r = case
+    lens, ids = [100, 1, 0, 199], [1, 0, 2, 2]
+    if T == 517:
+        lens, ids = [10, 5, 10, 3, 200, 289], [1, 0, 2, 2, 0, 3]
+    off = [0] + np.cumsum(lens).tolist()
+    na = max(ids)
+    w = Workload("grp", 14, T, d_in, d_out, r, tuple(off), tuple(ids), n_adapters=na, scales=(0.5,) * na)
+    inp = make_inputs(w, dev)
+    with _ll(w) as ll:
+        ll.set_option(L.OPT_CLUSTER, cluster)
+        ll.set_option(L.OPT_MMA_GROUP, 1)
+        y1 = run(ll, inp, off, ids).clone()
+        ll.set_option(L.OPT_MMA_GROUP, 2)
+        y2 = run(ll, inp, off, ids)
+        torch.cuda.synchronize()
+        assert ll.status() == 0
+    assert torch.equal(y1, y2)
+    assert rel_err(y2, oracle_full(inp, off, ids)) <= TOL
+
+
 @pytest.mark.parametrize("name", ["tiny", "sweep_qkv_multi", "mixed_decode", "mixed_near_ridge"])
 def test_inline_work_list_equals_uploaded(dev, name):
     # small work lists travel in the kernel parameters; the result equals the uploaded path
