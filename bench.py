@@ -46,9 +46,9 @@ def _peaks():
     return 1900.0, 1700.0, 6800.0, "fallback"
 
 
-def _kernel_hash():
+def _kernel_hash(w4: bool = False):
     h = hashlib.sha256()
-    for f in ("kernels.cu", "lora_internal.h"):
+    for f in ("kernels.cu", "lora_internal.h") + (("kernels_w4.cu",) if w4 else ()):
         with open(os.path.join(ROOT, "mixed_lora_projection_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -60,7 +60,7 @@ def _profiled_traffic(workload: str):
     p = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(p):
         return None
-    kh = _kernel_hash()
+    kh = _kernel_hash(workload.endswith("+w4"))
     with open(p) as f:
         for line in f:
             parts = line.split()
@@ -295,8 +295,9 @@ def run_ours(args, rank, world, dist):
                      "peak": peak_burst, "unit": "TFLOP/s",
                      "frac": round(achieved / peak_burst, 4) if achieved else None,
                      "traffic": traffic, "peak_source": f"{src} bf16 burst",
-                     "kernel": "lora_gemm_kernel (shrink + base + expand, one launch per call)" if not shrink_n
-                     else "lora_gemm_kernel (fused base + expand launch)", "algorithmic_flops_per_step": fused_flops},
+                     "kernel": ("lora_w4_kernel (4-bit base + expand; shrink on lora_gemm_kernel before it)" if args.w4
+                                else "lora_gemm_kernel (shrink + base + expand, one launch per call)" if not shrink_n
+                                else "lora_gemm_kernel (fused base + expand launch)"), "algorithmic_flops_per_step": fused_flops},
         "kernel_ms": {"main": round(fused_ms / max(1, args.steps), 5), "separate_shrink": round(shrink_ms / max(1, args.steps), 5),
                       "main_launches": fused_n, "separate_shrink_launches": shrink_n},
         "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s",
