@@ -247,22 +247,40 @@ struct Shape {
     std::vector<Tile> fused_groups, shrink_groups;  // cs tiles per group
 };
 
-// Groups of `cs` consecutive tiles that name the same adapter (they share the B tile);
-// a tile without a partner is padded with a copy of itself that has no rows. A padding
-// shrink tile gets flag slot -1 (it publishes nothing); a padding fused tile keeps its
-// partner's slot (it waits for the same U rows, then stores nothing).
-void make_groups(const std::vector<Tile>& tiles, int cs, bool shrink, std::vector<Tile>* out) {
+// Groups of `cs` consecutive tiles that share the B tile of their MMAs. Shrink tiles pair
+// when they name the same adapter (their B operand is A_a). Fused tiles pair when they name
+// the same adapter or when one of them names none: the pair then runs the adapter's expand,
+// and the base tile's half reads its U operand from `zero_row`, a block of U that is always
+// zero, so its rows gain exact zeros. A tile without a partner is padded with a copy of
+// itself that has no rows. A padding shrink tile gets flag slot -1 (it publishes nothing); a
+// padding or base fused tile takes its partner's slot (it waits for the same U rows).
+void make_groups(const std::vector<Tile>& tiles, int cs, bool shrink, int zero_row, std::vector<Tile>* out) {
     out->clear();
     for (size_t i = 0; i < tiles.size();) {
-        out->push_back(tiles[i]);
-        if (cs == 1) { ++i; continue; }
-        if (i + 1 < tiles.size() && tiles[i + 1].adapter == tiles[i].adapter) {
-            out->push_back(tiles[i + 1]);
+        if (cs == 1) {
+            out->push_back(tiles[i]);
+            ++i;
+            continue;
+        }
+        const bool has_next = i + 1 < tiles.size();
+        const int a0 = tiles[i].adapter, a1 = has_next ? tiles[i + 1].adapter : -1;
+        if (has_next && (a0 == a1 || (!shrink && (a0 == 0 || a1 == 0)))) {
+            Tile t0 = tiles[i], t1 = tiles[i + 1];
+            if (a0 != a1) {
+                Tile& base = a0 == 0 ? t0 : t1;
+                const Tile& other = a0 == 0 ? t1 : t0;
+                base.adapter = other.adapter;
+                base.fused_index = other.fused_index;
+                base.u_row = zero_row;
+            }
+            out->push_back(t0);
+            out->push_back(t1);
             i += 2;
         } else {
             Tile pad = tiles[i];
             pad.nrows = 0;
             if (shrink) pad.fused_index = -1;
+            out->push_back(tiles[i]);
             out->push_back(pad);
             i += 1;
         }
@@ -329,8 +347,8 @@ Shape choose_shape(lora_linear* h, const Plan& plan) {
                 if (cs && c != cs) continue;
                 if (c == 2 && nf < 2) continue;
                 std::vector<Tile> fg, sg;
-                make_groups(plan.fused, c, false, &fg);
-                make_groups(plan.shrink, c, true, &sg);
+                make_groups(plan.fused, c, false, h->u_rows - kTileM, &fg);
+                make_groups(plan.shrink, c, true, h->u_rows - kTileM, &sg);
                 const int slots = h->num_sms / c;
                 if (small_batch) {
                     const int t = tn ? tn : choose_tile_n(h, nf, (int)fg.size() / c, slots);
@@ -351,8 +369,8 @@ Shape choose_shape(lora_linear* h, const Plan& plan) {
         }
     }
     sh.cs = cs;
-    make_groups(plan.fused, sh.cs, false, &sh.fused_groups);
-    make_groups(plan.shrink, sh.cs, true, &sh.shrink_groups);
+    make_groups(plan.fused, sh.cs, false, h->u_rows - kTileM, &sh.fused_groups);
+    make_groups(plan.shrink, sh.cs, true, h->u_rows - kTileM, &sh.shrink_groups);
     const int nfg = (int)sh.fused_groups.size() / sh.cs;
     const int slots = h->num_sms / sh.cs;
     sh.tile_n = tn;
@@ -840,7 +858,8 @@ int forward_impl(lora_linear* h, const void* x, int T, const int32_t* seg_offset
     // indexes tensor maps and flags with them, so a malformed list must never reach it
     for (const Tile& t : sh.fused_groups)
         if (t.adapter < 0 || t.adapter > n_used || t.fused_index < 0 || t.fused_index >= nf ||
-            t.row0 < 0 || t.nrows < 0 || t.row0 + t.nrows > T)
+            t.row0 < 0 || t.nrows < 0 || t.row0 + t.nrows > T ||
+            (t.adapter && t.u_row != t.row0 && t.u_row != h->u_rows - kTileM))
             return LORA_EINVAL;
     for (const Tile& t : sh.shrink_groups)
         if (t.adapter < 1 || t.adapter > n_used || t.fused_index < -1 || t.fused_index >= nf || t.row0 < 0 ||

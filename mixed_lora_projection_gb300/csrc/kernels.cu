@@ -241,7 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
                     const uint32_t sa = smem_addr(a_ring + (size_t)stage * kStageA);
                     const uint32_t sb = smem_addr(b_ring + (size_t)stage * b_stage_bytes);
                     const int k = main ? kb * BK : (kb - p.k_main_blocks) * BK;
-                    tma_load_2d<CG>(sa, main ? &p.tm_x : &p.tm_u, fb, k, w.tile.row0, issuer);
+                    tma_load_2d<CG>(sa, main ? &p.tm_x : &p.tm_u, fb, k, main ? w.tile.row0 : w.tile.u_row, issuer);
                     tma_load_2d<CG>(sb, main ? bmain : &wl.tm_b[ad - 1], fb, k, w.n0 + rank * half, issuer);
                     ++issued;
                     if (++stage == stages) { stage = 0; phase ^= 1; }

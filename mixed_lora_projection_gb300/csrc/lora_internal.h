@@ -28,6 +28,9 @@ struct Tile {                        // one planner tile, as uploaded to the dev
     int32_t row0, nrows, adapter;    // adapter: compact slot (1-based), 0 = none
     int32_t fused_index;             // ready-flag slot: index of these rows among the fused tiles
                                      // (-1 on a shrink tile that only pads a cluster group)
+    int32_t u_row;                   // first U row the expand reads (fused tiles): row0, or a
+                                     // block of U that is always zero for a base tile that shares
+                                     // an SM pair (and so the pair's expand) with an adapter tile
 };
 
 // Parameters of one launch of the tile GEMM. Passed by value as a __grid_constant__.

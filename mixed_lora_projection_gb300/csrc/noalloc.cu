@@ -126,13 +126,13 @@ void plan_fixed(const int32_t* off, const int32_t* ids, int n_seg, FixedPlan* p)
             p->seg_off[++p->n_m] = hi;
         }
     }
-    Tile cur{0, 0, 0, 0};
+    Tile cur{0, 0, 0, 0, 0};
     for (int r = 0; r < p->n_m; ++r) {
         int pos = p->seg_off[r], hi = p->seg_off[r + 1], a = p->seg_id[r];
         while (pos < hi) {
             if (cur.nrows == lora::kTileM || (a != 0 && cur.adapter != 0 && a != cur.adapter)) {
                 p->fused[p->n_fused++] = cur;
-                cur = Tile{pos, 0, 0, 0};
+                cur = Tile{pos, 0, 0, 0, pos};
             }
             int take = hi - pos < lora::kTileM - cur.nrows ? hi - pos : lora::kTileM - cur.nrows;
             cur.nrows += take;

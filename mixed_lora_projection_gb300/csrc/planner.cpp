@@ -44,13 +44,13 @@ int plan_segments(const int32_t* seg_offsets, const int32_t* seg_ids, int n_seg,
         return LORA_OK;
     }
     // fused tiles: greedy walk; cut at kTileM rows or where a second nonzero id would enter
-    Tile cur{0, 0, 0, 0};
+    Tile cur{0, 0, 0, 0, 0};
     for (size_t r = 0; r < plan->seg_id.size(); ++r) {
         int pos = plan->seg_off[r], hi = plan->seg_off[r + 1], a = plan->seg_id[r];
         while (pos < hi) {
             if (cur.nrows == kTileM || (a != 0 && cur.adapter != 0 && a != cur.adapter)) {
                 plan->fused.push_back(cur);
-                cur = Tile{pos, 0, 0, 0};
+                cur = Tile{pos, 0, 0, 0, pos};
             }
             int take = std::min(hi - pos, kTileM - cur.nrows);
             cur.nrows += take;

@@ -194,6 +194,31 @@ def test_k_step_32_equals_64(dev, name):
     assert torch.equal(y64, y32)
 
 
+def test_mixed_base_and_adapter_pairs(dev):
+    # SM pairs may combine a base tile with an adapter tile (the base half's expand reads a
+    # block of U that is always zero): row tiles base | a1 | a2 | base | a1 (+ base rows) | a3 |
+    # base | base give pairs base-first, adapter-first, an a1/a3 pair that cannot form (padded)
+    # and a trailing pad
+    from mixed_lora_projection_gb300 import _lib as L
+    lens, ids = [128, 128, 128, 128, 64, 64, 128, 256], [0, 1, 2, 0, 1, 0, 3, 0]
+    off = [0] + np.cumsum(lens).tolist()
+    w = Workload("mixpair", 15, off[-1], 512, 768, 64, tuple(off), tuple(ids), n_adapters=3,
+                 scales=(0.5, 1.25, 2.0))
+    inp = make_inputs(w, dev)
+    with _ll(w) as ll:
+        ll.set_option(L.OPT_CLUSTER, 2)
+        y2 = run(ll, inp, off, ids).clone()
+        y0 = run(ll, inp, off, [0] * len(ids)).clone()
+        ll.set_option(L.OPT_CLUSTER, 1)
+        y1 = run(ll, inp, off, ids)
+        torch.cuda.synchronize()
+        assert ll.status() == 0
+    assert rel_err(y2, oracle_full(inp, off, ids)) <= TOL
+    base = torch.as_tensor(row_adapter_ids(off, ids, w.T) == 0, device=dev)
+    assert torch.equal(y2[base], y0[base])
+    assert torch.equal(y1, y2)
+
+
 @pytest.mark.parametrize("cluster", [1, 2])
 @pytest.mark.parametrize("case", [(300, 320, 272, 64), (517, 384, 1000, 128)], ids=["odd_k_steps", "even_k_steps"])
 def test_mma_grouping_is_exact(dev, case, cluster):

@@ -62,6 +62,12 @@ SMALL = [
     (7, 128, 256, 16, [3, 4], [0, 1], 1),
     (300, 512, 264, 24, [0, 100, 1, 0, 199], [1, 0, 2, 2, 1], 2),
     (517, 384, 1000, 128, [10, 5, 10, 3, 200, 289], [1, 0, 2, 2, 0, 3], 3),
+    # decode-sized batches: X boxes as tall as the one token tile (16 .. 128 rows), deeper rings
+    (1, 256, 384, 16, [1], [0], 1),
+    (33, 384, 640, 16, [33], [1], 1),
+    (48, 512, 1000, 32, [8] * 6, [0] * 6, 1),
+    (100, 256, 256, 16, [30, 40, 30], [1, 0, 2], 2),
+    (128, 256, 512, 16, [128], [0], 1),
 ]
 
 
