@@ -196,14 +196,15 @@ def run_ours(args, rank, world, dist):
         setups.append((w, handles[key], copies, y))
     stream = torch.cuda.current_stream(dev)
 
-    def step(i):
+    def step(i, s=None):
+        s = s or stream
         for (w, ll, copies, y) in setups:
             c = copies[i % len(copies)]
             if args.w4:
                 ll.forward_w4(copies[0].x, w.seg_offsets, w.seg_ids, c.w[0], c.w[1], c.a, c.b, c.scales, y=y,
-                              stream=stream)
+                              stream=s)
             else:
-                ll.forward(copies[0].x, w.seg_offsets, w.seg_ids, c.w, c.a, c.b, c.scales, y=y, stream=stream)
+                ll.forward(copies[0].x, w.seg_offsets, w.seg_ids, c.w, c.a, c.b, c.scales, y=y, stream=s)
 
     for i in range(args.warmup):
         step(i)
@@ -229,8 +230,6 @@ def run_ours(args, rank, world, dist):
     t1 = time.time()
     if dist:
         dist.barrier()
-    time.sleep(0.1)
-    sampler.stop()
     elapsed_ms = ev0.elapsed_time(ev1)
     launches = sum(ll.timing(1)[2] for ll in handles.values()) - launches0
     fused_ms = sum(ll.timing(1)[0] for ll in handles.values())
@@ -240,6 +239,44 @@ def run_ours(args, rank, world, dist):
     for ll in handles.values():
         ll.set_option(L.OPT_TIMING, 0)
         assert ll.status() == 0, "a kernel's bounded wait ran out"
+    graph = None
+    if args.graph:
+        # the same steps replayed from CUDA graphs (one captured step per rotating weight copy)
+        n_graphs = len(setups[0][2])
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            for i in range(n_graphs):
+                step(i, side)                         # the shapes once before capture
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        c0 = sum(ll.timing(1)[2] for ll in handles.values())
+        graphs = []
+        for i in range(n_graphs):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                step(i, torch.cuda.current_stream(dev))   # the capture stream
+            graphs.append(g)
+        per_step = (sum(ll.timing(1)[2] for ll in handles.values()) - c0) // n_graphs
+        for i in range(args.warmup):
+            graphs[i % n_graphs].replay()
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        replay_stream = torch.cuda.current_stream(dev)
+        t0 = time.time()
+        g0.record(replay_stream)
+        for i in range(args.steps):
+            graphs[i % n_graphs].replay()
+        g1.record(replay_stream)
+        torch.cuda.synchronize()
+        t1 = time.time()
+        graph = {"ms_per_step": g0.elapsed_time(g1) / args.steps, "launches_per_step": per_step}
+        for ll in handles.values():
+            assert ll.status() == 0, "a kernel's bounded wait ran out"
+    time.sleep(0.1)
+    sampler.stop()
 
     # e2e: the host-buffer entry point, X in and Y out every step
     x_host = [s[2][0].x.cpu().pin_memory() for s in setups]
@@ -269,6 +306,13 @@ def run_ours(args, rank, world, dist):
         dist.barrier()
 
     flops = _flops_of(items)
+    eager = None
+    if graph is not None:
+        # the headline numbers come from the graph replays; the eager pass stays for reference
+        eager = {"ms_per_step": round(elapsed_ms / args.steps, 5),
+                 "value": round(world * flops / (elapsed_ms / args.steps * 1e-3) / 1e12, 2)}
+        elapsed_ms = graph["ms_per_step"] * args.steps
+        launches = graph["launches_per_step"] * args.steps
     elapsed_ms, e2e_ms, value, e2e_value = aggregate_ranks(elapsed_ms, e2e_ms, flops, args.steps, world, dist)
     ms_per_step = elapsed_ms / args.steps
     peak_burst, peak_sust, hbm, src = _peaks()
@@ -305,6 +349,8 @@ def run_ours(args, rank, world, dist):
                 "d2h_bytes_per_step": sum(2 * w.T * w.d_out for w, _, _ in items),
                 "ms_per_step": round(e2e_ms, 4), "steps": e2e_steps},
         "gpu_launches": launches,
+        "cuda_graph": ({"replayed": True, "launches_per_step": graph["launches_per_step"], "eager": eager}
+                       if graph is not None else None),
         "launch_shape": setups[0][1].describe(w0.T, w0.seg_offsets, w0.seg_ids),
         "clocks": sampler.summary(t0, t1),
     }
@@ -418,6 +464,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--two-launch", action="store_true", help="shrink as its own launch (for comparison)")
     ap.add_argument("--w4", action="store_true", help="4-bit base weights (int4, group 128, bf16 scales)")
+    ap.add_argument("--graph", action="store_true", help="time the steps as CUDA-graph replays (each call's "
+                    "work list must travel in the kernel parameters, e.g. the 24-layer sweep)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -90,6 +90,13 @@ int lora_linear_create(lora_linear** out, int d_in, int d_out, int rank,
  * stream (they share the handle's workspace); the handle is not thread-safe.
  * Returns LORA_OK, LORA_EINVAL (nothing launched) or LORA_ECUDA. A bounded wait that
  * ran out inside a kernel is reported later by lora_linear_status.
+ * CUDA graphs: a call may be recorded by stream capture when its work list travels in the
+ * kernel parameters (at most 64 row tiles over both passes, SM-pair padding included, 48
+ * merged segments and 4 named adapters; a 2,048-row batch of a few requests fits); a larger
+ * call returns LORA_EUNSUPPORTED while the stream is capturing and records nothing. Each launch
+ * leaves the handle's workspace as it found it, so a graph can be replayed any number of
+ * times (the host arrays are read at capture; device buffers are read at every replay).
+ * Make one call of the same shape before capturing: it caches the launch shape.
  * Source: "Two 27B models on a single RTX 5090", section 4 (per-request adapter in a
  * shared batch) and section 3 (W + B.A).
  */
@@ -211,8 +218,11 @@ enum {
     LORA_OPT_TILE_K = 10,       /* K per pipeline stage: 0 = auto, 32 or 64 */
     LORA_OPT_INLINE_WORK_LIST = 11, /* 1 (default) = small work lists travel in the kernel parameters,
                                       0 = always upload them to device memory */
-    LORA_OPT_MMA_GROUP = 12     /* pipeline stages the MMA warp waits for at once: 0 = auto (2 for SM
-                                   pairs, 1 for single CTAs), 1 or 2 */
+    LORA_OPT_MMA_GROUP = 12,    /* pipeline stages the MMA warp waits for at once: 0 = auto (2 for SM
+                                   pairs, 1 for single CTAs), 1, 2 or 4 (reduced so that at least two
+                                   stages stay with the producer) */
+    LORA_OPT_DEBUG_PUBLISH_DELAY_US = 13 /* tests only: each shrink unit of a one-launch call publishes
+                                   its U rows this many microseconds late (0..1,000,000; default 0) */
 };
 
 /* lora_linear_set_option -- set one option above. Returns LORA_OK or LORA_EINVAL. */

@@ -65,8 +65,8 @@ struct lora_linear {
     void* u_ws = nullptr;       // bf16 [u_rows, rank]: shrink output, read by the fused pass
     int u_rows = 0;
     int* status = nullptr;      // device status word
-    int* flags = nullptr;       // per fused tile: epoch of the call whose U rows are ready
-    int epoch = 0;
+    int* flags = nullptr;       // per fused tile: U rows ready (1) in the running launch; then the
+                                // launch's exit counter. All zero between launches.
     int* status_host = nullptr; // pinned copy for forward_host
     Slot slots[kRing];
     size_t slot_bytes = 0;
@@ -75,6 +75,7 @@ struct lora_linear {
     EncodeTiledFn encode = nullptr;
     // options
     int force_tile_n = 0, raster = 0, debug_stall = 0, timing = 0, two_launch = 0, cluster = 0;
+    unsigned long long debug_publish_delay_ns = 0;
     int raster_group = 4, tile_k = 0, allow_inline = 1, mma_group = 0;  // 0: 2 for SM pairs, else 1
     int max_clusters_cache[2][kMaxTileN / 16 + 1] = {};  // co-resident clusters by (size, B rows)
     std::unordered_map<uint64_t, uint32_t> shape_cache;   // plan signature -> (cs << 16) | tile_n
@@ -508,7 +509,7 @@ int lora_linear_create(lora_linear** out, int d_in, int d_out, int rank, int max
                     (size_t)(h->max_fused / 2 + 1) * sizeof(W4Group) + 256;
     if (cudaMalloc(&h->u_ws, (size_t)h->u_rows * rank * 2) != cudaSuccess ||
         cudaMalloc((void**)&h->status, sizeof(int)) != cudaSuccess ||
-        cudaMalloc((void**)&h->flags, sizeof(int) * (size_t)h->max_fused) != cudaSuccess ||
+        cudaMalloc((void**)&h->flags, sizeof(int) * ((size_t)h->max_fused + 1)) != cudaSuccess ||
         cudaHostAlloc((void**)&h->status_host, sizeof(int), cudaHostAllocDefault) != cudaSuccess) {
         cudaGetLastError();
         free_handle(h);
@@ -527,7 +528,7 @@ int lora_linear_create(lora_linear** out, int d_in, int d_out, int rank, int max
         }
     }
     if (cudaMemset(h->status, 0, sizeof(int)) != cudaSuccess ||
-        cudaMemset(h->flags, 0, sizeof(int) * (size_t)h->max_fused) != cudaSuccess ||
+        cudaMemset(h->flags, 0, sizeof(int) * ((size_t)h->max_fused + 1)) != cudaSuccess ||
         cudaMemset(h->u_ws, 0, (size_t)h->u_rows * rank * 2) != cudaSuccess) {
         free_handle(h);
         return LORA_ECUDA;
@@ -562,6 +563,10 @@ int lora_linear_set_option(lora_linear* h, int option, long long value) {
         case LORA_OPT_DEBUG_STALL:
             h->debug_stall = value ? 1 : 0;
             return LORA_OK;
+        case LORA_OPT_DEBUG_PUBLISH_DELAY_US:
+            if (value < 0 || value > 1000000) return LORA_EINVAL;
+            h->debug_publish_delay_ns = (unsigned long long)value * 1000ull;
+            return LORA_OK;
         case LORA_OPT_TIMING: {
             DeviceGuard guard(h->device);
             for (TimingRec& r : h->trec)
@@ -579,7 +584,7 @@ int lora_linear_set_option(lora_linear* h, int option, long long value) {
             h->raster_group = (int)value;
             return LORA_OK;
         case LORA_OPT_MMA_GROUP:
-            if (value < 0 || value > 2) return LORA_EINVAL;
+            if (value != 0 && value != 1 && value != 2 && value != 4) return LORA_EINVAL;
             h->mma_group = (int)value;
             return LORA_OK;
         case LORA_OPT_INLINE_WORK_LIST:
@@ -727,6 +732,13 @@ int forward_impl(lora_linear* h, const void* x, int T, const int32_t* seg_offset
     memset(&q, 0, sizeof(q));
     const bool inline_wl = h->allow_inline && nft + nst <= kInlineTiles && n_m <= kInlineSegs &&
                            n_used <= kInlineAdapters && (!w4 || w4_inline);
+    // Under stream capture only calls whose whole work list travels in the kernel parameters
+    // are recorded: an uploaded list would be read from a ring slot that later calls reuse.
+    cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &capture) != cudaSuccess) return LORA_ECUDA;
+    const bool capturing = capture != cudaStreamCaptureStatusNone;
+    if (capturing && (!inline_wl || x_src)) return LORA_EUNSUPPORTED;
+    const bool timing = h->timing && !capturing;   // timing events are read back eagerly
     Slot* slot = nullptr;
     if (inline_wl) {
         // small work list: it travels in the kernel parameters, no upload
@@ -848,10 +860,13 @@ int forward_impl(lora_linear* h, const void* x, int T, const int32_t* seg_offset
     p.k_lora_blocks = ceil_div(h->rank, bk);
     p.bk = bk;
     p.mma_group = h->mma_group ? h->mma_group : (cs > 1 ? 2 : 1);
+    // the stages the MMA warp holds at once leave at least two to the producer
+    while (p.mma_group > 1 && p.mma_group > sh.stages - 2) p.mma_group /= 2;
     p.d_out = h->d_out;
     p.rank = h->rank;
     p.cluster_size = cs;
     p.debug_stall = h->debug_stall;
+    p.debug_publish_delay_ns = h->debug_publish_delay_ns;
     const int slots = cs > 1 ? max_clusters(h, p) : h->num_sms;
     if (slots < 1) return LORA_ECUDA;
     // every tile the kernel will decode names a valid adapter slot and flag slot: the kernel
@@ -867,7 +882,7 @@ int forward_impl(lora_linear* h, const void* x, int T, const int32_t* seg_offset
             return LORA_EINVAL;
 
     TimingRec rec{};
-    if (h->timing) {
+    if (timing) {
         for (int i = 0; i < 3; ++i) {
             rec.ev[i] = take_event(h);
             if (!rec.ev[i]) return LORA_ECUDA;
@@ -884,7 +899,7 @@ int forward_impl(lora_linear* h, const void* x, int T, const int32_t* seg_offset
             ++h->launches;
             rec.has_shrink = true;
         }
-        if (h->timing) cudaEventRecord(rec.ev[1], stream);
+        if (timing) cudaEventRecord(rec.ev[1], stream);
         for (const W4Group& g : w4_groups)
             for (int k = 0; k < 2; ++k)
                 if (g.adapter[k] < 0 || g.adapter[k] > n_used || g.nrows[k] < 0 || g.row0[k] < 0 ||
@@ -913,23 +928,23 @@ int forward_impl(lora_linear* h, const void* x, int T, const int32_t* seg_offset
         if (launch_gemm(s, std::min(nsg, slots) * cs, stream) != cudaSuccess) return LORA_ECUDA;
         ++h->launches;
         rec.has_shrink = true;
-        if (h->timing) cudaEventRecord(rec.ev[1], stream);
+        if (timing) cudaEventRecord(rec.ev[1], stream);
         GemmParams f = p;
         f.n_shrink = 0;
         if (launch_gemm(f, std::min(fused_units, slots) * cs, stream) != cudaSuccess) return LORA_ECUDA;
         ++h->launches;
     } else {
         // one launch: shrink units first, fused units wait on the per-tile ready flags
-        if (h->timing) cudaEventRecord(rec.ev[1], stream);
+        if (timing) cudaEventRecord(rec.ev[1], stream);
         if (nsg > 0) {
-            h->epoch = h->epoch == 0x7fffffff ? 1 : h->epoch + 1;
             p.flags = h->flags;
-            p.epoch = h->epoch;
+            p.done_count = h->flags + h->max_fused;
+            p.n_flags = nf;
         }
         if (launch_gemm(p, std::min(nsg + fused_units, slots) * cs, stream) != cudaSuccess) return LORA_ECUDA;
         ++h->launches;
     }
-    if (h->timing) {
+    if (timing) {
         cudaEventRecord(rec.ev[2], stream);
         h->trec.push_back(rec);
     }

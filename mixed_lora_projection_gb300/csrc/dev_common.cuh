@@ -286,14 +286,14 @@ __device__ __forceinline__ void fence_proxy_async_global() {
 __device__ __forceinline__ void epilogue_bar_sync() {
     asm volatile("bar.sync 1, %0;" ::"n"(kEpilogueThreads) : "memory");
 }
-// Waits until *flag == epoch (bounded like wait_bounded).
-static __device__ __noinline__ bool wait_flag(const int* flag, int epoch, volatile int* abort_flag, int* status,
+// Waits until *flag == value (bounded like wait_bounded).
+static __device__ __noinline__ bool wait_flag(const int* flag, int value, volatile int* abort_flag, int* status,
                                        uint64_t limit_ns) {
-    if (ld_acquire(flag) == epoch) return true;
+    if (ld_acquire(flag) == value) return true;
     const uint64_t t0 = global_timer_ns();
     while (true) {
         __nanosleep(64);
-        if (ld_acquire(flag) == epoch) return true;
+        if (ld_acquire(flag) == value) return true;
         if (*abort_flag) return false;
         if (global_timer_ns() - t0 > limit_ns) {
             atomicOr(status, 1);

@@ -40,8 +40,8 @@ struct Tile {                        // one planner tile, as uploaded to the dev
 // cluster_size 2 a unit is a group of two row tiles (tiles 2g and 2g+1 of the arrays, one
 // per CTA of the cluster) that share the same B operand tile; each CTA loads half of that
 // tile's rows and the pair runs M = 256 MMAs. Groups are padded with tiles of nrows 0.
-// When `flags` is set, a fused unit's expand waits until flags[tile] == epoch, which the
-// shrink unit of that tile publishes after its U rows are stored (single-launch mode).
+// When `flags` is set, a fused unit's expand waits until flags[tile] == 1, which the shrink
+// unit of that tile publishes after its U rows are stored (single-launch mode).
 struct GemmParams {
     // inline work list (used when inline_wl != 0): adapter tensor maps (B_a at [0, 4), A_a
     // at [4, 8)), tiles (fused then shrink), merged segments (offsets then ids), scales
@@ -63,10 +63,12 @@ struct GemmParams {
     const float* scales;             // per compact adapter (device)
     void* y;                         // Y [T, d_out] bf16
     void* u;                         // U [u_rows, rank] bf16
-    int* flags;                      // per fused tile; nullptr = no in-kernel dependency
+    int* flags;                      // per fused tile: 1 once its U rows are stored; nullptr = no
+                                     // in-kernel dependency. Zero at launch, cleared at exit.
+    int* done_count;                 // CTAs that finished the launch (the last one clears flags)
+    int n_flags;                     // flags [0, n_flags) in use
     int* status;                     // device status word: bit 0 = a bounded wait ran out
     unsigned long long wait_limit_ns;
-    int epoch;
     int n_seg;
     int n_shrink;                    // shrink groups (tiles = cluster_size x groups)
     int n_fused;                     // fused row groups
@@ -82,8 +84,9 @@ struct GemmParams {
     int rank;
     int cluster_size;                // CTA group of the MMA: 1, or 2 (an SM pair, M = 256)
     int bk;                          // K per pipeline stage: 64 (128-byte swizzle) or 32 (64-byte swizzle)
-    int mma_group;                   // stages the MMA warp waits for at once (1 or 2)
+    int mma_group;                   // stages the MMA warp waits for at once (1, 2 or 4)
     int debug_stall;
+    unsigned long long debug_publish_delay_ns;   // tests: shrink units publish their flag this late
 };
 
 // 4-bit base kernel (transposed tile: output features on the MMA's M side, tokens on N).

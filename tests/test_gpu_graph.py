@@ -1,0 +1,112 @@
+"""CUDA-graph capture and the in-kernel shrink -> expand dependency across launches.
+
+One launch runs the shrink units and the fused units; a fused unit's expand waits for its
+tile's ready flag. The flags are cleared by the last CTA of each launch, so a launch never
+sees a flag left by an earlier one: consecutive calls and replays of a captured graph each
+wait for their own shrink. A test-only option holds every flag back for a while, so an
+expand that did not wait would read the previous call's U rows and give wrong output."""
+import pytest
+import torch
+
+from mixed_lora_projection_gb300.synth import WORKLOADS, make_inputs
+
+from gpu_util import TOL, oracle_rows, rel_err, run, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+DELAY_US = 300
+
+
+@pytest.fixture(scope="module")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from mixed_lora_projection_gb300 import build
+    build.ensure_built()
+    return torch.device("cuda", 0)
+
+
+def _ll(w):
+    from mixed_lora_projection_gb300 import LoraLinear
+    return LoraLinear(w.d_in, w.d_out, w.rank, w.T, 16, 0)
+
+
+def _fresh_x(inp, seed):
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    inp.x.copy_(torch.randn(inp.x.shape, generator=g).to(torch.bfloat16))
+
+
+@pytest.mark.parametrize("cluster", [1, 2])
+def test_delayed_flags_are_awaited_across_calls(dev, cluster):
+    from mixed_lora_projection_gb300 import _lib as L
+    w = WORKLOADS["sweep_qkv_multi"]
+    inp = make_inputs(w, dev)
+    off, ids = list(w.seg_offsets), list(w.seg_ids)
+    with _ll(w) as ll:
+        ll.set_option(L.OPT_CLUSTER, cluster)
+        want = []
+        for seed in (1, 2):
+            _fresh_x(inp, seed)
+            want.append(run(ll, inp, off, ids).clone())
+        ll.set_option(L.OPT_DEBUG_PUBLISH_DELAY_US, DELAY_US)
+        for seed, ref in zip((1, 2), want):
+            _fresh_x(inp, seed)
+            y = run(ll, inp, off, ids)
+            torch.cuda.synchronize()
+            assert ll.status() == 0
+            assert torch.equal(y, ref)
+
+
+def test_graph_replays_match_eager_calls(dev):
+    from mixed_lora_projection_gb300 import _lib as L
+    w = WORKLOADS["sweep_qkv_multi"]
+    inp = make_inputs(w, dev)
+    off, ids = list(w.seg_offsets), list(w.seg_ids)
+    seeds = (11, 12, 13)
+    with _ll(w) as ll:
+        want = []
+        for seed in seeds:
+            _fresh_x(inp, seed)
+            want.append(run(ll, inp, off, ids).clone())
+        y = torch.empty_like(want[0])
+        ll.set_option(L.OPT_DEBUG_PUBLISH_DELAY_US, DELAY_US)
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            run(ll, inp, off, ids, y=y)          # same shape once before capture
+        torch.cuda.current_stream(dev).wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            run(ll, inp, off, ids, y=y)
+        for rep in range(2):
+            for seed, ref in zip(seeds, want):
+                _fresh_x(inp, seed)              # device buffers are read at every replay
+                y.zero_()
+                g.replay()
+                torch.cuda.synchronize()
+                assert torch.equal(y, ref), (rep, seed)
+        assert ll.status() == 0
+    rows = sample_rows(w.T, off, ids, n_random=64, seed=3)
+    assert rel_err(y[torch.as_tensor(rows, device=dev)], oracle_rows(inp, off, ids, rows)) <= TOL
+
+
+def test_capture_of_a_call_with_an_uploaded_work_list_is_refused(dev):
+    from mixed_lora_projection_gb300 import LoraError, _lib as L
+    w = WORKLOADS["prefill_16k"]          # 128 row tiles: the work list is uploaded per call
+    inp = make_inputs(w, dev)
+    off, ids = list(w.seg_offsets), list(w.seg_ids)
+    with _ll(w) as ll:
+        y = run(ll, inp, off, ids).clone()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            marker = torch.zeros(1, device=dev)
+            marker += 1
+            with pytest.raises(LoraError) as e:
+                run(ll, inp, off, ids, y=y)
+        assert e.value.code == L.LORA_EUNSUPPORTED
+        torch.cuda.synchronize()
+        y2 = run(ll, inp, off, ids)            # the handle still works eagerly
+        torch.cuda.synchronize()
+        assert ll.status() == 0
+    assert torch.equal(y, y2)
