@@ -1004,6 +1004,33 @@ int lora_linear_forward_w4(lora_linear* h, const void* x, int T, const int32_t* 
 
 }  // extern "C"
 
+// Row boundaries of the host-buffer path's chunks: {0, T} below 2,048 rows; else chunks of up to
+// max(1024, T / 8) rows (multiples of 128) between ramps that halve down to max(256, T / 32) rows
+// at both ends.
+static std::vector<int> host_chunk_bounds(int T) {
+    std::vector<int> b(1, 0);
+    if (T < 2048) {
+        b.push_back(T);
+        return b;
+    }
+    const auto r128 = [](int v) { return std::max(kTileM, v / kTileM * kTileM); };
+    const int big = r128(std::max(1024, T / 8)), small = r128(std::max(256, T / 32));
+    std::vector<int> ramp;                       // small, 2 small, ... below big
+    for (int v = small; v < big && 2 * (int)ramp.size() < 8; v *= 2) ramp.push_back(r128(v));
+    int ramp_rows = 0;
+    for (int v : ramp) ramp_rows += 2 * v;
+    if (ramp_rows >= T) ramp.clear(), ramp_rows = 0;
+    for (int v : ramp) b.push_back(b.back() + v);
+    const int mid = T - ramp_rows, n_mid = std::max(1, ceil_div(mid, big));
+    for (int i = 1; i <= n_mid; ++i) {
+        const int end = b[0] + (ramp_rows / 2) + (int)((long long)mid * i / n_mid);
+        b.push_back(i == n_mid ? end : std::max(b.back() + 1, end / kTileM * kTileM));
+    }
+    for (int i = (int)ramp.size() - 1; i >= 0; --i) b.push_back(b.back() + ramp[i]);
+    b.back() = T;
+    return b;
+}
+
 static int forward_host_impl(lora_linear* h, const void* x_host, int T, const int32_t* seg_offsets,
                              const int32_t* seg_adapter_ids, int n_seg, const void* W, const void* Wq,
                              const void* Ws, const void* const* A, const void* const* B, const float* scale,
@@ -1042,18 +1069,18 @@ static int forward_host_impl(lora_linear* h, const void* x_host, int T, const in
     }
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
     // Row chunks: copy-in of chunk c+1 and copy-out of chunk c-1 overlap the kernel of chunk c
-    // (rows are independent, so each chunk is a call of its own on its rows).
-    const int n_chunks = std::max(1, std::min(8, T / 1024));
-    const int chunk_rows = n_chunks == 1 ? T : ceil_div(ceil_div(T, n_chunks), kTileM) * kTileM;
+    // (rows are independent, so each chunk is a call of its own on its rows). The host link is
+    // the bound, and only the first chunk's copy-in and the last chunk's kernel and copy-out
+    // overlap nothing, so the chunks ramp up from and back down to small ones.
+    std::vector<int> bounds = host_chunk_bounds(T);
     const uint8_t* xh = static_cast<const uint8_t*>(x_host);
     uint8_t* yh = static_cast<uint8_t*>(y_host);
     uint8_t* xd = static_cast<uint8_t*>(h->x_stage);
     uint8_t* yd = static_cast<uint8_t*>(h->y_stage);
     const size_t xrow = (size_t)h->d_in * 2, yrow = (size_t)h->d_out * 2;
     std::vector<int32_t> off, ids;
-    int c = 0;
-    for (int a = 0; a < T || (T == 0 && c == 0); a += chunk_rows, ++c) {
-        const int b = std::min(T, a + chunk_rows);
+    for (int c = 0; c + 1 < (int)bounds.size(); ++c) {
+        const int a = bounds[c], b = bounds[c + 1];
         const int n = b - a;
         // the segments restricted to rows [a, b), offsets made relative to a
         off.assign(1, 0);
@@ -1080,7 +1107,6 @@ static int forward_host_impl(lora_linear* h, const void* x_host, int T, const in
                                 h->s_out) != cudaSuccess)
                 return LORA_ECUDA;
         }
-        if (T == 0) break;
     }
     if (cudaStreamSynchronize(stream) != cudaSuccess || cudaStreamSynchronize(h->s_out) != cudaSuccess)
         return LORA_ECUDA;
