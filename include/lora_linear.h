@@ -219,8 +219,7 @@ enum {
     LORA_OPT_INLINE_WORK_LIST = 11, /* 1 (default) = small work lists travel in the kernel parameters,
                                       0 = always upload them to device memory */
     LORA_OPT_MMA_GROUP = 12,    /* pipeline stages the MMA warp waits for at once: 0 = auto (2 for SM
-                                   pairs, 1 for single CTAs), 1, 2 or 4 (reduced so that at least two
-                                   stages stay with the producer) */
+                                   pairs, 1 for single CTAs), 1 or 2 */
     LORA_OPT_DEBUG_PUBLISH_DELAY_US = 13 /* tests only: each shrink unit of a one-launch call publishes
                                    its U rows this many microseconds late (0..1,000,000; default 0) */
 };

@@ -584,7 +584,7 @@ int lora_linear_set_option(lora_linear* h, int option, long long value) {
             h->raster_group = (int)value;
             return LORA_OK;
         case LORA_OPT_MMA_GROUP:
-            if (value != 0 && value != 1 && value != 2 && value != 4) return LORA_EINVAL;
+            if (value < 0 || value > 2) return LORA_EINVAL;
             h->mma_group = (int)value;
             return LORA_OK;
         case LORA_OPT_INLINE_WORK_LIST:
@@ -860,8 +860,6 @@ int forward_impl(lora_linear* h, const void* x, int T, const int32_t* seg_offset
     p.k_lora_blocks = ceil_div(h->rank, bk);
     p.bk = bk;
     p.mma_group = h->mma_group ? h->mma_group : (cs > 1 ? 2 : 1);
-    // the stages the MMA warp holds at once leave at least two to the producer
-    while (p.mma_group > 1 && p.mma_group > sh.stages - 2) p.mma_group /= 2;
     p.d_out = h->d_out;
     p.rank = h->rank;
     p.cluster_size = cs;

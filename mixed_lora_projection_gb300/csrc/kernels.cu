@@ -134,47 +134,6 @@ __device__ __forceinline__ Unit decode_unit(const GemmParams& p, const WorkList&
     return r;
 }
 
-// One step of the MMA warp: wait until the next NS ring stages are full, then issue their
-// MMAs (BK / 16 per stage) and release each stage to the producer. Fully unrolled: any
-// run-time loop control between MMAs lowers the issue rate. Returns false if a wait ran out.
-template <int NS, int BK, int CG>
-__device__ __forceinline__ bool mma_step(uint64_t* full, uint64_t* empty, const uint8_t* a_ring, const uint8_t* b_ring,
-                                         uint32_t b_stage_bytes, int stages, int& stage, uint32_t& phase,
-                                         uint32_t d, uint32_t idesc, bool first, uint32_t issuer,
-                                         volatile int* abort_flag, int* status, uint64_t limit) {
-    constexpr uint32_t kStageA = kTileM * BK * 2;
-    int st[NS];
-    uint32_t ph[NS];
-    st[0] = stage;
-    ph[0] = phase;
-#pragma unroll
-    for (int j = 1; j < NS; ++j) {
-        st[j] = st[j - 1] + 1;
-        ph[j] = ph[j - 1];
-        if (st[j] == stages) { st[j] = 0; ph[j] ^= 1; }
-    }
-#pragma unroll
-    for (int j = 0; j < NS; ++j)
-        if (!wait_warp(smem_addr(&full[st[j]]), ph[j], abort_flag, status, limit)) return false;
-    tc_fence_after();
-#pragma unroll
-    for (int j = 0; j < NS; ++j) {
-        const uint64_t ad = smem_desc<BK>(smem_addr(a_ring + (size_t)st[j] * kStageA));
-        const uint64_t bd = smem_desc<BK>(smem_addr(b_ring + (size_t)st[j] * b_stage_bytes));
-#pragma unroll
-        for (int k = 0; k < BK / 16; ++k) {
-            // advance 16 bf16 = 32 bytes along K inside the swizzled rows
-            mma_bf16<CG>(d, ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), idesc, (!first || j > 0 || k > 0) ? 1u : 0u,
-                         issuer);
-        }
-        mma_commit<CG>(smem_addr(&empty[st[j]]), issuer);
-    }
-    stage = st[NS - 1] + 1;
-    phase = ph[NS - 1];
-    if (stage == stages) { stage = 0; phase ^= 1; }
-    return true;
-}
-
 template <int BK, int CG>
 __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_constant__ GemmParams p) {
     constexpr uint32_t kStageA = kTileM * BK * 2;
@@ -327,25 +286,42 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
                 }
                 tc_fence_after();
                 const uint32_t d = tmem_base + (uint32_t)(acc * kAccCols);
-                // The stages are taken up to mma_group (1, 2 or 4) at a time: a shared-memory read by
-                // this warp (the barrier wait) does not complete before the MMAs it issued earlier
-                // have, so each wait drains the tensor pipe; fewer waits per K-step, fewer drains.
-                for (int kb = 0; kb < w.nk && ok;) {
-                    const int left = w.nk - kb;
-                    const bool first = kb == 0;
-                    if (p.mma_group >= 4 && left >= 4) {
-                        ok = mma_step<4, BK, CG>(full, empty, a_ring, b_ring, b_stage_bytes, stages, stage, phase, d,
-                                                 idesc, first, issuer, abort_flag, p.status, limit);
-                        kb += 4;
-                    } else if (p.mma_group >= 2 && left >= 2) {
-                        ok = mma_step<2, BK, CG>(full, empty, a_ring, b_ring, b_stage_bytes, stages, stage, phase, d,
-                                                 idesc, first, issuer, abort_flag, p.status, limit);
-                        kb += 2;
-                    } else {
-                        ok = mma_step<1, BK, CG>(full, empty, a_ring, b_ring, b_stage_bytes, stages, stage, phase, d,
-                                                 idesc, first, issuer, abort_flag, p.status, limit);
-                        kb += 1;
+                // With mma_group 2 the stages are taken two at a time: a shared-memory read by
+                // this warp (the barrier wait) does not complete before the MMAs it issued
+                // earlier have, so each wait drains the tensor pipe; one wait per two K-steps
+                // halves those drains.
+                for (int kb = 0; kb < w.nk;) {
+                    const int ns = (p.mma_group > 1 && kb + 1 < w.nk) ? 2 : 1;
+                    int st1 = stage + 1;
+                    uint32_t ph1 = phase;
+                    if (st1 == stages) { st1 = 0; ph1 ^= 1; }
+                    if (!wait_warp(smem_addr(&full[stage]), phase, abort_flag, p.status, limit) ||
+                        (ns == 2 && !wait_warp(smem_addr(&full[st1]), ph1, abort_flag, p.status, limit))) {
+                        ok = false;
+                        break;
                     }
+                    tc_fence_after();
+                    for (int j = 0; j < ns; ++j) {
+                        const int st = j ? st1 : stage;
+                        const uint64_t ad = smem_desc<BK>(smem_addr(a_ring + (size_t)st * kStageA));
+                        const uint64_t bd = smem_desc<BK>(smem_addr(b_ring + (size_t)st * b_stage_bytes));
+#pragma unroll
+                        for (int k = 0; k < BK / 16; ++k) {
+                            // advance 16 bf16 = 32 bytes along K inside the swizzled rows
+                            mma_bf16<CG>(d, ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), idesc,
+                                         (kb + j > 0 || k > 0) ? 1u : 0u, issuer);
+                        }
+                        mma_commit<CG>(smem_addr(&empty[st]), issuer);
+                    }
+                    if (ns == 2) {
+                        stage = st1 + 1;
+                        phase = ph1;
+                        if (stage == stages) { stage = 0; phase ^= 1; }
+                    } else {
+                        stage = st1;
+                        phase = ph1;
+                    }
+                    kb += ns;
                 }
                 if (!ok) break;
                 mma_commit<CG>(smem_addr(&tfull[acc]), issuer);

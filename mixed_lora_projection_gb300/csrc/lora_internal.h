@@ -84,7 +84,7 @@ struct GemmParams {
     int rank;
     int cluster_size;                // CTA group of the MMA: 1, or 2 (an SM pair, M = 256)
     int bk;                          // K per pipeline stage: 64 (128-byte swizzle) or 32 (64-byte swizzle)
-    int mma_group;                   // stages the MMA warp waits for at once (1, 2 or 4)
+    int mma_group;                   // stages the MMA warp waits for at once (1 or 2)
     int debug_stall;
     unsigned long long debug_publish_delay_ns;   // tests: shrink units publish their flag this late
 };

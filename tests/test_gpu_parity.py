@@ -222,8 +222,8 @@ def test_mixed_base_and_adapter_pairs(dev):
 @pytest.mark.parametrize("cluster", [1, 2])
 @pytest.mark.parametrize("case", [(300, 320, 272, 64), (517, 384, 1000, 128)], ids=["odd_k_steps", "even_k_steps"])
 def test_mma_grouping_is_exact(dev, case, cluster):
-    # the MMA warp waiting for one, two or four stages at once issues the same MMA sequence; an
-    # odd number of K-steps per unit (5 base + 1 expand) exercises the shorter tails
+    # the MMA warp waiting for one or two stages at once issues the same MMA sequence; an odd
+    # number of K-steps per unit (5 base + 1 expand) exercises the single-stage tail
     from mixed_lora_projection_gb300 import _lib as L
     T, d_in, d_out, r = case
     lens, ids = [100, 1, 0, 199], [1, 0, 2, 2]
@@ -238,13 +238,10 @@ def test_mma_grouping_is_exact(dev, case, cluster):
         ll.set_option(L.OPT_MMA_GROUP, 1)
         y1 = run(ll, inp, off, ids).clone()
         ll.set_option(L.OPT_MMA_GROUP, 2)
-        y2 = run(ll, inp, off, ids).clone()
-        ll.set_option(L.OPT_MMA_GROUP, 4)
-        y4 = run(ll, inp, off, ids)
+        y2 = run(ll, inp, off, ids)
         torch.cuda.synchronize()
         assert ll.status() == 0
     assert torch.equal(y1, y2)
-    assert torch.equal(y1, y4)
     assert rel_err(y2, oracle_full(inp, off, ids)) <= TOL
 
 
