@@ -220,6 +220,31 @@ def test_mixed_base_and_adapter_pairs(dev):
 
 
 @pytest.mark.parametrize("cluster", [1, 2])
+def test_raster_orders_are_exact(dev, cluster):
+    # the order in which units visit row and column tiles (row tiles first, column tiles first,
+    # groups of column tiles, groups that do not divide the column-tile count) changes which
+    # SM computes a block, never its MMA sequence: all results are identical
+    from mixed_lora_projection_gb300 import _lib as L
+    lens, ids = [200, 300, 1, 267, 256], [1, 0, 2, 2, 1]
+    off = [0] + np.cumsum(lens).tolist()
+    w = Workload("raster", 20, off[-1], 384, 1000, 64, tuple(off), tuple(ids), n_adapters=2, scales=(0.5, 1.5))
+    inp = make_inputs(w, dev)
+    outs = []
+    with _ll(w) as ll:
+        ll.set_option(L.OPT_CLUSTER, cluster)
+        ll.set_option(L.OPT_TILE_N, 128)                      # 8 column tiles
+        for mode, group in [(0, 4), (1, 4), (2, 4), (3, 1), (3, 3), (3, 4), (3, 8), (3, 100)]:
+            ll.set_option(L.OPT_RASTER, mode)
+            ll.set_option(L.OPT_RASTER_GROUP, group)
+            outs.append(run(ll, inp, off, ids).clone())
+        torch.cuda.synchronize()
+        assert ll.status() == 0
+    for y in outs[1:]:
+        assert torch.equal(y, outs[0])
+    assert rel_err(outs[0], oracle_full(inp, off, ids)) <= TOL
+
+
+@pytest.mark.parametrize("cluster", [1, 2])
 @pytest.mark.parametrize("case", [(300, 320, 272, 64), (517, 384, 1000, 128)], ids=["odd_k_steps", "even_k_steps"])
 def test_mma_grouping_is_exact(dev, case, cluster):
     # the MMA warp waiting for one or two stages at once issues the same MMA sequence; an odd
