@@ -187,6 +187,11 @@ def run_ours(args, rank, world, dist):
             handles[key] = LoraLinear(w.d_in, w.d_out, w.rank, w.T, max(8, len(w.seg_ids)), dev)
             if args.two_launch:
                 handles[key].set_option(L.OPT_TWO_LAUNCH, 1)
+            if args.raster:
+                mode, _, group = args.raster.partition(":")
+                handles[key].set_option(L.OPT_RASTER, int(mode))
+                if group:
+                    handles[key].set_option(L.OPT_RASTER_GROUP, int(group))
         copies = [make_inputs(w, dev, layer=layer, proj_index=pi + 4 * c, with_x=(c == 0)) for c in range(n_copies)]
         if args.w4:
             for c, inp in enumerate(copies):
@@ -329,6 +334,7 @@ def run_ours(args, rank, world, dist):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded Gaussian bf16; no checkpoint)",
         "config": {"workload": args.workload + ("+w4" if args.w4 else ""),
+                   **({"raster": args.raster} if args.raster else {}),
                    "base": "int4 (symmetric, group 128, bf16 scales)" if args.w4 else "bf16", "T": w0.T, "d_in": w0.d_in if len(items) == 1 else "per projection",
                    "d_out": w0.d_out if len(items) == 1 else "per projection", "rank": w0.rank,
                    "segments": len(w0.seg_ids), "adapter_rows": w0.adapter_rows, "calls_per_step": len(items),
@@ -464,6 +470,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--two-launch", action="store_true", help="shrink as its own launch (for comparison)")
     ap.add_argument("--w4", action="store_true", help="4-bit base weights (int4, group 128, bf16 scales)")
+    ap.add_argument("--raster", default="", help="unit order MODE[:GROUP] (the library's raster option: 0 auto, "
+                    "1 row tiles first, 2 column tiles first, 3 groups of GROUP column tiles)")
     ap.add_argument("--graph", action="store_true", help="time the steps as CUDA-graph replays (each call's "
                     "work list must travel in the kernel parameters, e.g. the 24-layer sweep)")
     args = ap.parse_args()
