@@ -41,11 +41,11 @@ enum {
     LORA_ENOMEM = -2,       /* a device or pinned-host allocation failed in lora_linear_create */
     LORA_ECUDA = -3,        /* a CUDA runtime/driver call failed */
     LORA_ETIMEOUT = -4,     /* a kernel's bounded wait ran out (read by lora_linear_status) */
-    LORA_EUNSUPPORTED = -5, /* valid request this build does not run (no sm_103a device, rank > 256) */
+    LORA_EUNSUPPORTED = -5, /* valid request this library does not run (e.g. a capture of a call whose work list is uploaded) */
     LORA_ENODEV = -6        /* the device is not an sm_103 GPU or cannot be used */
 };
 
-/* Limits of this build. */
+/* Limits of this library. */
 #define LORA_MAX_RANK 256   /* adapter rank: the shrink writes at most one 256-column tile */
 #define LORA_TILE_ROWS 128  /* rows per tile of the planner (the tensor-core tile height) */
 

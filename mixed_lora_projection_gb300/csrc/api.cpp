@@ -409,7 +409,7 @@ const char* lora_linear_error_string(int code) {
         case LORA_ENOMEM: return "out of memory";
         case LORA_ECUDA: return "CUDA call failed";
         case LORA_ETIMEOUT: return "a kernel's bounded wait ran out";
-        case LORA_EUNSUPPORTED: return "unsupported by this build";
+        case LORA_EUNSUPPORTED: return "unsupported by this library";
         case LORA_ENODEV: return "no usable sm_103 device";
         default: return "unknown error";
     }
