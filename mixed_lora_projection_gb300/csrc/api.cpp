@@ -842,9 +842,14 @@ int forward_impl(lora_linear* h, const void* x, int T, const int32_t* seg_offset
     if (encode_2d(h, &p.tm_x, x, h->d_in, T, bk, kTileM) != CUDA_SUCCESS) return LORA_ECUDA;
     if (w4) {
         q.tm_x = p.tm_x;
-        if (encode_u8_sw128(h, &q.tm_wq, Wq, (uint64_t)h->d_in / 2, h->d_out, kW4TileM) != CUDA_SUCCESS ||
+        // a batch of one token tile of at most 128 rows and no adapter rows (a decode step) runs
+        // two feature tiles per unit
+        q.feature_tiles = (n_w4g == 1 && w4_groups[0].nrows[1] == 0 && w4_groups[0].nrows[0] <= kTileM &&
+                           w4_groups[0].adapter[0] == 0) ? 2 : 1;
+        const uint32_t q_box = (uint32_t)(kW4TileM * q.feature_tiles);
+        if (encode_u8_sw128(h, &q.tm_wq, Wq, (uint64_t)h->d_in / 2, h->d_out, q_box) != CUDA_SUCCESS ||
             encode_plain_2d(h, &q.tm_ws, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Ws, h->d_out,
-                            (uint64_t)h->d_in / kW4Group, kW4TileM, 2) != CUDA_SUCCESS)
+                            (uint64_t)h->d_in / kW4Group, q_box, 2) != CUDA_SUCCESS)
             return LORA_ECUDA;
     } else if (encode_2d(h, &p.tm_w, W, h->d_in, h->d_out, bk, tile_n / cs) != CUDA_SUCCESS) {
         return LORA_ECUDA;
@@ -915,13 +920,19 @@ int forward_impl(lora_linear* h, const void* x, int T, const int32_t* seg_offset
         q.status = h->status;
         q.wait_limit_ns = h->wait_limit_ns;
         q.n_groups = n_w4g;
-        q.n_ntiles = ceil_div(h->d_out, kW4TileM);
+        q.n_ntiles = ceil_div(h->d_out, kW4TileM * q.feature_tiles);
         q.k_main_blocks = ceil_div(h->d_in, 64);
         q.k_lora_blocks = ceil_div(h->rank, 64);
         q.k_pack_blocks = ceil_div(q.k_main_blocks, 4);
         q.d_out = h->d_out;
+        // X stages: two token tiles (and the expand's U + B_a boxes), or one tile when FT = 2;
+        // the packed ring takes the rest of shared memory
+        q.x_stage_bytes = q.feature_tiles == 2 ? kTileM * 128 : 2 * kTileM * 128;
         q.stages = 4;
-        q.pstages = 5;
+        q.pstages = 2;
+        while (q.pstages < 8 && w4_smem_bytes(q.stages, q.pstages + 1, q.x_stage_bytes, q.feature_tiles) <=
+                                    (size_t)kSmemLimit)
+            ++q.pstages;
         q.debug_stall = h->debug_stall;
         const int units = q.n_groups * q.n_ntiles;
         if (launch_w4(q, std::min(units, h->num_sms), stream) != cudaSuccess) return LORA_ECUDA;

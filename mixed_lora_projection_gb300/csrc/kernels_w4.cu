@@ -40,7 +40,7 @@ namespace dev {
 
 namespace {
 
-constexpr uint32_t kXStageBytes = 256 * 128;      // B operand: up to 256 token rows x 64 bf16
+constexpr uint32_t kXStageMaxBytes = 256 * 128;   // B operand: up to 256 token rows x 64 bf16
 constexpr uint32_t kQStageBytes = 128 * kW4PackBytes;   // packed rows of 4 K-steps
 constexpr uint32_t kSStageBytes = 2 * 128 * 2;          // two scale groups of 128 features
 constexpr uint32_t kAccCols4 = 256;               // accumulator columns (tokens)
@@ -77,18 +77,28 @@ struct W4Unit {
     int n;           // MMA N of the base K-steps (tokens, multiple of 16)
 };
 
+template <int FT>
 __device__ __forceinline__ W4Unit w4_unit(const W4Params& p, const W4Group* groups, int u) {
     W4Unit r;
     const int gi = u / p.n_ntiles;
     r.g = groups[gi];
-    r.n0 = (u % p.n_ntiles) * kW4TileM;
+    r.n0 = (u % p.n_ntiles) * kW4TileM * FT;
     r.n = r.g.nrows[1] > 0 ? 128 + ((r.g.nrows[1] + 15) & ~15) : ((r.g.nrows[0] + 15) & ~15);
     return r;
 }
 
 }  // namespace
 
+// FT feature tiles of 128 per unit. FT = 2 serves batches of one token tile of at most 128 rows
+// with no adapter rows (decode steps): the unit's two tiles share each K-step's X stage, barrier
+// round trips and ring slots, which halves the K-steps an SM runs in sequence. Tensor memory
+// then holds two 128-column accumulators (tile f at column 128 f) and A stages of 64 columns.
+template <int FT>
 __global__ void __launch_bounds__(kW4Threads, 1) lora_w4_kernel(const __grid_constant__ W4Params p) {
+    static_assert(FT == 1 || FT == 2, "one or two feature tiles per unit");
+    constexpr uint32_t kQStage = FT * kQStageBytes;    // packed rows of the unit's feature tiles
+    constexpr uint32_t kSStage = FT * kSStageBytes;    // their scales (two groups of 128 inputs)
+    constexpr uint32_t kAStageCols = 32 * FT;          // TMEM columns of one A stage
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
@@ -96,10 +106,11 @@ __global__ void __launch_bounds__(kW4Threads, 1) lora_w4_kernel(const __grid_con
     // ring stage s: base K-step -> X rows (B operand, up to 256 rows) in smem and the
     // dequantised weights (A operand) in TMEM columns 256 + 32 s; expand K-step -> U rows
     // (B operand) in the first 16 KB and the B_a tile (A operand) in the second 16 KB
+    const uint32_t x_stage = (uint32_t)p.x_stage_bytes;
     uint8_t* x_ring = base;
-    uint8_t* q_ring = x_ring + (size_t)stages * kXStageBytes;
-    uint8_t* s_ring = q_ring + (size_t)pstages * kQStageBytes;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(s_ring + (size_t)pstages * kSStageBytes);
+    uint8_t* q_ring = x_ring + (size_t)stages * x_stage;
+    uint8_t* s_ring = q_ring + (size_t)pstages * kQStage;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(s_ring + (size_t)pstages * kSStage);
     uint64_t* full = bars;                          // TMA bytes + one arrive per converter quadrant
     uint64_t* empty = full + stages;                // MMA done with the stage (smem and TMEM)
     uint64_t* pfull = empty + stages;               // packed rows + scales landed
@@ -133,7 +144,7 @@ __global__ void __launch_bounds__(kW4Threads, 1) lora_w4_kernel(const __grid_con
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    const uint32_t tmem_a = tmem_base + kAccCols4;  // A stages: columns 256 + 32 s
+    const uint32_t tmem_a = tmem_base + kAccCols4;  // A stages: columns 256 + 32 FT s
 
     const int n_units = p.n_groups * p.n_ntiles;
     const uint64_t limit = p.wait_limit_ns;
@@ -155,7 +166,7 @@ __global__ void __launch_bounds__(kW4Threads, 1) lora_w4_kernel(const __grid_con
             int acquired = -1;
             bool ok = true;
             for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-                const W4Unit w = w4_unit(p, groups, u);
+                const W4Unit w = w4_unit<FT>(p, groups, u);
                 const int ntile = w.g.nrows[1] > 0 ? 2 : 1;
                 for (int kb = 0; kb < p.k_main_blocks; ++kb) {
                     if (!wait_warp(smem_addr(&empty[stage]), phase ^ 1, abort_flag, p.status, limit)) {
@@ -164,7 +175,7 @@ __global__ void __launch_bounds__(kW4Threads, 1) lora_w4_kernel(const __grid_con
                     }
                     const uint32_t fb = smem_addr(&full[stage]);
                     mbar_arrive_expect_tx(fb, (uint32_t)ntile * 16384u, issuer);
-                    const uint32_t xs = smem_addr(x_ring + (size_t)stage * kXStageBytes);
+                    const uint32_t xs = smem_addr(x_ring + (size_t)stage * x_stage);
                     for (int h = 0; h < ntile; ++h)
                         tma_load_2d<1>(xs + (uint32_t)h * 16384u, &p.tm_x, fb, kb * 64, w.g.row0[h], issuer);
                     ++issued;
@@ -185,7 +196,7 @@ __global__ void __launch_bounds__(kW4Threads, 1) lora_w4_kernel(const __grid_con
                         }
                         const uint32_t fb = smem_addr(&full[stage]);
                         mbar_arrive_expect_tx(fb, 32768u, issuer);
-                        const uint32_t xs = smem_addr(x_ring + (size_t)stage * kXStageBytes);
+                        const uint32_t xs = smem_addr(x_ring + (size_t)stage * x_stage);
                         tma_load_2d<1>(xs, &p.tm_u, fb, kr * 64, w.g.row0[h], issuer);
                         tma_load_2d<1>(xs + 16384u, bm, fb, kr * 64, w.n0, issuer);
                         ++issued;
@@ -215,17 +226,17 @@ __global__ void __launch_bounds__(kW4Threads, 1) lora_w4_kernel(const __grid_con
             long long issued = 0;
             bool ok = true;
             for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-                const int n0 = (u % p.n_ntiles) * kW4TileM;
+                const int n0 = (u % p.n_ntiles) * kW4TileM * FT;
                 for (int pb = 0; pb < p.k_pack_blocks; ++pb) {
                     if (!wait_warp(smem_addr(&pempty[ps]), pph ^ 1, abort_flag, p.status, limit)) {
                         ok = false;
                         break;
                     }
                     const uint32_t pbar = smem_addr(&pfull[ps]);
-                    mbar_arrive_expect_tx(pbar, kQStageBytes + kSStageBytes, issuer);
-                    tma_load_2d<1>(smem_addr(q_ring + (size_t)ps * kQStageBytes), &p.tm_wq, pbar, pb * kW4PackBytes,
+                    mbar_arrive_expect_tx(pbar, kQStage + kSStage, issuer);
+                    tma_load_2d<1>(smem_addr(q_ring + (size_t)ps * kQStage), &p.tm_wq, pbar, pb * kW4PackBytes,
                                    n0, issuer);
-                    tma_load_2d<1>(smem_addr(s_ring + (size_t)ps * kSStageBytes), &p.tm_ws, pbar, n0, 2 * pb, issuer);
+                    tma_load_2d<1>(smem_addr(s_ring + (size_t)ps * kSStage), &p.tm_ws, pbar, n0, 2 * pb, issuer);
                     ++issued;
                     if (++ps == pstages) { ps = 0; pph ^= 1; }
                 }
@@ -245,7 +256,7 @@ __global__ void __launch_bounds__(kW4Threads, 1) lora_w4_kernel(const __grid_con
         int it = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++it) {
-            const W4Unit w = w4_unit(p, groups, u);
+            const W4Unit w = w4_unit<FT>(p, groups, u);
             if (!wait_warp(smem_addr(tempty), (it & 1) ^ 1, abort_flag, p.status, limit)) {
                 ok = false;
                 break;
@@ -268,11 +279,13 @@ __global__ void __launch_bounds__(kW4Threads, 1) lora_w4_kernel(const __grid_con
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
                     const int st = j ? st1 : stage;
-                    const uint64_t bd = smem_desc<64>(smem_addr(x_ring + (size_t)st * kXStageBytes));
+                    const uint64_t bd = smem_desc<64>(smem_addr(x_ring + (size_t)st * x_stage));
 #pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        mma_tmem_a(tmem_base, tmem_a + (uint32_t)(32 * st + 8 * k), bd + (uint64_t)(2 * k), idesc,
-                                   (kb > 0 || j > 0 || k > 0) ? 1u : 0u, issuer);
+                    for (int f = 0; f < FT; ++f)
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            mma_tmem_a(tmem_base + (uint32_t)(128 * f), tmem_a + kAStageCols * st + (uint32_t)(32 * f + 8 * k),
+                                       bd + (uint64_t)(2 * k), idesc, (kb > 0 || j > 0 || k > 0) ? 1u : 0u, issuer);
                     mma_commit<1>(smem_addr(&empty[st]), issuer);
                 }
                 stage = st1 + 1;
@@ -295,7 +308,7 @@ __global__ void __launch_bounds__(kW4Threads, 1) lora_w4_kernel(const __grid_con
                     tc_fence_after();
                     for (int j = 0; j < ns; ++j) {
                         const int st = j ? st1 : stage;
-                        const uint32_t xs = smem_addr(x_ring + (size_t)st * kXStageBytes);
+                        const uint32_t xs = smem_addr(x_ring + (size_t)st * x_stage);
                         const uint64_t ad = smem_desc<64>(xs + 16384u);
                         const uint64_t bd = smem_desc<64>(xs);
 #pragma unroll
@@ -340,7 +353,7 @@ __global__ void __launch_bounds__(kW4Threads, 1) lora_w4_kernel(const __grid_con
         uint32_t pph = 0, phase = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-            const W4Unit w = w4_unit(p, groups, u);
+            const W4Unit w = w4_unit<FT>(p, groups, u);
             for (int kb = 0; kb < p.k_main_blocks; ++kb) {
                 if ((kb & 3) == 0 &&
                     !wait_warp(smem_addr(&pfull[ps]), pph, abort_flag, p.status, limit)) {
@@ -348,36 +361,48 @@ __global__ void __launch_bounds__(kW4Threads, 1) lora_w4_kernel(const __grid_con
                     break;
                 }
                 if ((stage & 1) == par) {
-                    // the packed box rows are 128 bytes, 128-byte swizzled: 16-byte chunk c of
-                    // row r sits at chunk c ^ (r % 8)
-                    const uint8_t* row = q_ring + (size_t)ps * kQStageBytes + (size_t)nl * kW4PackBytes;
-                    const uint32_t c0 = (uint32_t)(2 * (kb & 3)) ^ (uint32_t)(nl & 7);
-                    const uint32_t c1 = (uint32_t)(2 * (kb & 3) + 1) ^ (uint32_t)(nl & 7);
-                    const uint4 q0 = *reinterpret_cast<const uint4*>(row + (c0 << 4));
-                    const uint4 q1 = *reinterpret_cast<const uint4*>(row + (c1 << 4));
-                    const __nv_bfloat16* ss =
-                        reinterpret_cast<const __nv_bfloat16*>(s_ring + (size_t)ps * kSStageBytes);
-                    const __nv_bfloat162 s2 = __bfloat162bfloat162(ss[((kb & 3) >> 1) * 128 + nl]);
-                    const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-                    uint32_t o[32];
+                    bool got = true;
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
+                    for (int f = 0; f < FT && got; ++f) {
+                        // the packed box rows are 128 bytes, 128-byte swizzled: 16-byte chunk c of
+                        // row r sits at chunk c ^ (r % 8); feature tile f's rows start at 128 f
+                        const int r = 128 * f + nl;
+                        const uint8_t* row = q_ring + (size_t)ps * kQStage + (size_t)r * kW4PackBytes;
+                        const uint32_t c0 = (uint32_t)(2 * (kb & 3)) ^ (uint32_t)(r & 7);
+                        const uint32_t c1 = (uint32_t)(2 * (kb & 3) + 1) ^ (uint32_t)(r & 7);
+                        const uint4 q0 = *reinterpret_cast<const uint4*>(row + (c0 << 4));
+                        const uint4 q1 = *reinterpret_cast<const uint4*>(row + (c1 << 4));
+                        const __nv_bfloat16* ss =
+                            reinterpret_cast<const __nv_bfloat16*>(s_ring + (size_t)ps * kSStage);
+                        const __nv_bfloat162 s2 =
+                            __bfloat162bfloat162(ss[((kb & 3) >> 1) * (kW4TileM * FT) + r]);
+                        const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+                        uint32_t o[32];
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const uint32_t v = ((words[c] >> (4 * j)) & 0x000F000Fu) | 0x43004300u;
-                            __nv_bfloat162 t = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&v), magic);
-                            t = __hmul2(t, s2);
-                            o[4 * c + j] = *reinterpret_cast<const uint32_t*>(&t);
+                        for (int c = 0; c < 8; ++c) {
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                const uint32_t v = ((words[c] >> (4 * j)) & 0x000F000Fu) | 0x43004300u;
+                                __nv_bfloat162 t = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&v), magic);
+                                t = __hmul2(t, s2);
+                                o[4 * c + j] = *reinterpret_cast<const uint32_t*>(&t);
+                            }
                         }
+                        if (f == 0) {
+                            if (!wait_warp(smem_addr(&empty[stage]), phase ^ 1, abort_flag, p.status, limit)) {
+                                got = false;
+                                break;
+                            }
+                            tc_fence_after();
+                        }
+                        const uint32_t ta = tmem_a + lane_off + kAStageCols * (uint32_t)stage + (uint32_t)(32 * f);
+                        tmem_st16(ta, o);
+                        tmem_st16(ta + 16u, o + 16);
                     }
-                    if (!wait_warp(smem_addr(&empty[stage]), phase ^ 1, abort_flag, p.status, limit)) {
+                    if (!got) {
                         ok = false;
                         break;
                     }
-                    tc_fence_after();
-                    const uint32_t ta = tmem_a + lane_off + (uint32_t)(32 * stage);
-                    tmem_st16(ta, o);
-                    tmem_st16(ta + 16u, o + 16);
                     tmem_st_wait();
                     tc_fence_before();
                     __syncwarp();
@@ -414,19 +439,22 @@ __global__ void __launch_bounds__(kW4Threads, 1) lora_w4_kernel(const __grid_con
         __nv_bfloat16* y = reinterpret_cast<__nv_bfloat16*>(p.y);
         int it = 0;
         for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++it) {
-            const W4Unit w = w4_unit(p, groups, u);
+            const W4Unit w = w4_unit<FT>(p, groups, u);
             int ok = 1;
             if (lane == 0) ok = wait_bounded(smem_addr(tfull), it & 1, abort_flag, p.status, limit, true);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             tc_fence_after();
-            const int n = w.n0 + 32 * q + lane;
-            const bool n_ok = n < p.d_out;
-            for (int h = 0; h < 2; ++h) {
-                const int rows = w.g.nrows[h];
+            // FT = 1: token tile h at accumulator columns 128 h; FT = 2 (one token tile): feature
+            // tile f at accumulator columns 128 f
+            for (int hf = 0; hf < 2; ++hf) {
+                const int h = FT == 1 ? hf : 0;
+                const int n = w.n0 + (FT == 1 ? 0 : kW4TileM * hf) + 32 * q + lane;
+                const bool n_ok = n < p.d_out;
+                const int rows = (FT == 1 || hf < FT) ? w.g.nrows[h] : 0;
                 for (int c = 0; c < rows; c += 32) {
                     uint32_t v[32];
-                    const uint32_t taddr = tmem_base + lane_off + (uint32_t)(128 * h + c);
+                    const uint32_t taddr = tmem_base + lane_off + (uint32_t)(128 * hf + c);
                     tmem_ld16(taddr, v);
                     tmem_ld16(taddr + 16u, v + 16);
                     tmem_ld_wait();
@@ -455,21 +483,33 @@ __global__ void __launch_bounds__(kW4Threads, 1) lora_w4_kernel(const __grid_con
 
 }  // namespace dev
 
-size_t w4_smem_bytes(int stages, int pstages) {
-    return 1024 + (size_t)stages * dev::kXStageBytes + (size_t)pstages * (dev::kQStageBytes + dev::kSStageBytes) +
+size_t w4_smem_bytes(int stages, int pstages, int x_stage_bytes, int ft) {
+    return 1024 + (size_t)stages * (size_t)x_stage_bytes +
+           (size_t)pstages * (size_t)ft * (dev::kQStageBytes + dev::kSStageBytes) +
            8 * (2 * (size_t)stages + 2 * (size_t)pstages + 3) + 16;
 }
 
 cudaError_t w4_prepare_device() {
-    return cudaFuncSetAttribute(dev::lora_w4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+    cudaError_t e = cudaFuncSetAttribute(dev::lora_w4_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kSmemLimit);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(dev::lora_w4_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
 }
 
 cudaError_t launch_w4(const W4Params& p, int grid, cudaStream_t stream) {
-    // the TMEM A stages sit in columns 256 + 32 s; the converters' warp sets take alternate stages
-    if (w4_smem_bytes(p.stages, p.pstages) > (size_t)kSmemLimit || p.stages < 2 || p.stages > kW4AStages ||
-        (p.stages & 1) || p.pstages < 2)
+    // the TMEM A stages (32 FT columns each) sit after the 256 accumulator columns; the
+    // converters' warp sets take alternate stages; an X stage holds the unit's token tiles (and,
+    // with FT = 1, the expand's U and B_a boxes of 16 KB each)
+    const int ft = p.feature_tiles;
+    if ((ft != 1 && ft != 2) || w4_smem_bytes(p.stages, p.pstages, p.x_stage_bytes, ft) > (size_t)kSmemLimit ||
+        p.stages < 2 || p.stages * 32 * ft > 256 || (p.stages & 1) || p.pstages < 2 || (p.x_stage_bytes & 1023) ||
+        p.x_stage_bytes < 16384 || p.x_stage_bytes > (int)dev::kXStageMaxBytes || (ft == 2 && p.n_ntiles * 256 < p.d_out))
         return cudaErrorInvalidValue;
-    dev::lora_w4_kernel<<<grid, kW4Threads, w4_smem_bytes(p.stages, p.pstages), stream>>>(p);
+    const size_t smem = w4_smem_bytes(p.stages, p.pstages, p.x_stage_bytes, ft);
+    if (ft == 2)
+        dev::lora_w4_kernel<2><<<grid, kW4Threads, smem, stream>>>(p);
+    else
+        dev::lora_w4_kernel<1><<<grid, kW4Threads, smem, stream>>>(p);
     return cudaGetLastError();
 }
 

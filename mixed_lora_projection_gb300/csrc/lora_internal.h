@@ -126,6 +126,9 @@ struct W4Params {
     int d_out;
     int stages;                      // X / U ring
     int pstages;                     // packed ring
+    int x_stage_bytes;               // bytes per X / U ring stage (a multiple of 1024)
+    int feature_tiles;               // 128-feature tiles per unit: 1, or 2 for one token tile of at
+                                     // most 128 rows with no adapter rows (tm_wq / tm_ws boxes 128 x FT)
     int debug_stall;
 };
 
@@ -148,7 +151,7 @@ int gemm_max_clusters(const GemmParams& p);  // co-resident clusters of this lau
 cudaError_t w4_repack(const void* src, void* dst, long long n_words, int grid, cudaStream_t stream);
 
 // kernels_w4.cu
-size_t w4_smem_bytes(int stages, int pstages);
+size_t w4_smem_bytes(int stages, int pstages, int x_stage_bytes, int ft);
 cudaError_t w4_prepare_device();
 cudaError_t launch_w4(const W4Params& p, int grid, cudaStream_t stream);
 
