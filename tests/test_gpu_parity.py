@@ -286,7 +286,7 @@ def test_inline_work_list_equals_uploaded(dev, name):
 
 
 def test_repeated_calls_reuse_flags(dev):
-    # many calls in a row on one handle: the epoch-tagged ready flags never go stale
+    # many calls in a row on one handle: each launch clears its ready flags, none goes stale
     w = WORKLOADS["sweep_o_multi"]
     inp = make_inputs(w, dev)
     with _ll(w) as ll:
