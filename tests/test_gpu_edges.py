@@ -1,7 +1,7 @@
 """GPU edge cases through the C-ABI: many requests and many adapters (work lists too large for
 the kernel parameters, dozens of tensor maps), adapters named out of order and more than once,
-unnamed adapters passed as NULL, scale 0 and negative scales, and one handle reused for
-batches of very different sizes."""
+unnamed adapters passed as NULL, scale 0 and negative scales, one handle reused for batches of
+very different sizes, and rows that give the same bits in any batch."""
 import numpy as np
 import pytest
 import torch
@@ -91,3 +91,23 @@ def test_one_handle_serves_batches_of_any_size(dev):
             rows = sample_rows(T, off, ids, n_random=64, seed=i) if T > 512 else list(range(T))
             ref = oracle_rows(inp, off, ids, rows)
             assert rel_err(y[torch.as_tensor(rows, device=dev)], ref) <= TOL, T
+
+
+def test_rows_do_not_depend_on_the_batch_they_are_in(dev):
+    # the 48 decode rows of the mixed batch, computed inside the 4,144-row batch (SM pairs,
+    # 256-column tiles, next to 4,096 adapter rows) and alone (single CTAs, 240-column tiles):
+    # the same bits
+    from mixed_lora_projection_gb300 import LoraLinear
+    from mixed_lora_projection_gb300.synth import WORKLOADS
+    w = WORKLOADS["mixed_batch"]
+    inp = make_inputs(w, dev)
+    off, ids = list(w.seg_offsets), list(w.seg_ids)
+    with LoraLinear(w.d_in, w.d_out, w.rank, w.T, 16, 0) as ll:
+        full = run(ll, inp, off, ids).clone()
+        shape_full = ll.describe(w.T, off, ids)
+        alone = ll.forward(inp.x[:48], off[:7], ids[:6], inp.w, inp.a, inp.b, inp.scales)
+        shape_alone = ll.describe(48, off[:7], ids[:6])
+        torch.cuda.synchronize()
+        assert ll.status() == 0
+    assert shape_full["tile_n"] != shape_alone["tile_n"] or shape_full["grid"] != shape_alone["grid"]
+    assert torch.equal(full[:48], alone)
