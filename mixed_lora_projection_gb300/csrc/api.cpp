@@ -155,9 +155,9 @@ CUresult encode_2d(lora_linear* h, CUtensorMap* m, const void* ptr, uint64_t inn
 }
 
 // Deepest ring that fits the opt-in shared memory, for `b_rows` B rows per CTA.
-int stages_for(int b_rows, int bk) {
+int stages_for(int b_rows, int bk, int a_rows = kTileM) {
     int s = kMaxStages;
-    while (s > 2 && gemm_smem_bytes(b_rows, s, bk) > (size_t)kSmemLimit) --s;
+    while (s > 2 && gemm_smem_bytes(b_rows, s, bk, a_rows) > (size_t)kSmemLimit) --s;
     return s;
 }
 
@@ -251,6 +251,7 @@ int choose_m_fastest(const lora_linear* h, int n_tiles, int n_ntiles, int tile_n
 // Launch shape of one call: cluster size, tile widths, pipeline depth, rasterisation.
 struct Shape {
     int cs = 1, tile_n = 0, shrink_n = 0, n_ntiles = 0, stages = 0, m_fastest = 0, bk = 64, raster_group = 1;
+    int a_rows = kTileM;   // rows of one A box: the tile's rows when the batch is one short tile
     std::vector<Tile> fused_groups, shrink_groups;  // cs tiles per group
 };
 
@@ -382,7 +383,11 @@ Shape choose_shape(lora_linear* h, const Plan& plan) {
     const int slots = h->num_sms / sh.cs;
     sh.tile_n = tn;
     sh.n_ntiles = ceil_div(h->d_out, sh.tile_n);
-    sh.stages = stages_for(std::max(sh.tile_n, sh.shrink_n) / sh.cs, sh.bk);
+    // a batch of one tile of fewer than 128 rows (a decode step) on single CTAs loads only its
+    // rows of X (and U): smaller A stages, a deeper ring for the W stream
+    if (sh.cs == 1 && plan.fused.size() == 1) sh.a_rows = std::max(16, ceil_div(plan.fused[0].nrows, 16) * 16);
+    if (plan.shrink.empty()) sh.shrink_n = 0;   // no shrink units: the B ring holds output tiles only
+    sh.stages = stages_for(std::max(sh.tile_n, sh.shrink_n) / sh.cs, sh.bk, sh.a_rows);
     sh.m_fastest = choose_m_fastest(h, nfg, sh.n_ntiles, sh.tile_n, kTileM * sh.cs, slots);
     sh.raster_group = h->raster == 3 ? h->raster_group : ceil_div(sh.n_ntiles, 2);
     return sh;
@@ -723,7 +728,12 @@ int forward_impl(lora_linear* h, const void* x, int T, const int32_t* seg_offset
     Shape sh = choose_shape(h, plan);
     // 4-bit base: the shrink pass runs on the bf16 kernel (64-wide K-steps), then the 4-bit
     // kernel runs the base and expand passes over token groups
-    if (w4) sh.bk = 64;
+    if (w4) {
+        // the 4-bit kernel reads X and U through the same maps with 128-row boxes
+        sh.bk = 64;
+        sh.a_rows = kTileM;
+        sh.stages = stages_for(std::max(sh.tile_n, sh.shrink_n) / sh.cs, sh.bk);
+    }
     const std::vector<W4Group> w4_groups = w4 ? make_w4_groups(plan.fused) : std::vector<W4Group>();
     const int n_w4g = (int)w4_groups.size();
     const bool w4_inline = n_used <= kInlineAdapters && n_w4g <= kW4InlineGroups;
@@ -839,7 +849,7 @@ int forward_impl(lora_linear* h, const void* x, int T, const int32_t* seg_offset
         p.seg_id = reinterpret_cast<const int32_t*>(slot->dev + off_segid);
         p.scales = reinterpret_cast<const float*>(slot->dev + off_scale);
     }
-    if (encode_2d(h, &p.tm_x, x, h->d_in, T, bk, kTileM) != CUDA_SUCCESS) return LORA_ECUDA;
+    if (encode_2d(h, &p.tm_x, x, h->d_in, T, bk, (uint32_t)sh.a_rows) != CUDA_SUCCESS) return LORA_ECUDA;
     if (w4) {
         q.tm_x = p.tm_x;
         // a batch of one token tile of at most 128 rows and no adapter rows (a decode step) runs
@@ -854,7 +864,8 @@ int forward_impl(lora_linear* h, const void* x, int T, const int32_t* seg_offset
     } else if (encode_2d(h, &p.tm_w, W, h->d_in, h->d_out, bk, tile_n / cs) != CUDA_SUCCESS) {
         return LORA_ECUDA;
     }
-    if (encode_2d(h, &p.tm_u, h->u_ws, h->rank, h->u_rows, bk, kTileM) != CUDA_SUCCESS) return LORA_ECUDA;
+    if (encode_2d(h, &p.tm_u, h->u_ws, h->rank, h->u_rows, bk, (uint32_t)sh.a_rows) != CUDA_SUCCESS)
+        return LORA_ECUDA;
     p.y = y;
     p.u = h->u_ws;
     p.status = h->status;
@@ -872,6 +883,7 @@ int forward_impl(lora_linear* h, const void* x, int T, const int32_t* seg_offset
     p.k_lora_blocks = ceil_div(h->rank, bk);
     p.bk = bk;
     p.mma_group = h->mma_group ? h->mma_group : (cs > 1 ? 2 : 1);
+    p.a_rows = sh.a_rows;
     p.d_out = h->d_out;
     p.rank = h->rank;
     p.cluster_size = cs;

@@ -136,7 +136,10 @@ __device__ __forceinline__ Unit decode_unit(const GemmParams& p, const WorkList&
 
 template <int BK, int CG>
 __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_constant__ GemmParams p) {
-    constexpr uint32_t kStageA = kTileM * BK * 2;
+    // A stage: the tile's rows of X (or U) for this K-step; a batch of one short tile loads
+    // only its rows (a_rows < 128), and the MMA's remaining A rows read unrelated shared memory
+    // whose output rows are never stored
+    const uint32_t kStageA = (uint32_t)(p.a_rows ? p.a_rows : kTileM) * BK * 2;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // carve: rings (1024-aligned), then barriers, then the TMEM slot and the abort flag
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -456,8 +459,8 @@ cudaError_t w4_repack(const void* src, void* dst, long long n_words, int grid, c
     return cudaGetLastError();
 }
 
-size_t gemm_smem_bytes(int b_tile_rows, int stages, int bk) {
-    return 1024 + (size_t)stages * ((size_t)kTileM * bk * 2 + (size_t)b_tile_rows * bk * 2) +
+size_t gemm_smem_bytes(int b_tile_rows, int stages, int bk, int a_rows) {
+    return 1024 + (size_t)stages * ((size_t)a_rows * bk * 2 + (size_t)b_tile_rows * bk * 2) +
            8 * (2 * (size_t)stages + 5) + 16;
 }
 
@@ -481,7 +484,7 @@ static void launch_config(const GemmParams& p, int grid, cudaStream_t stream, cu
     memset(cfg, 0, sizeof(*cfg));
     cfg->gridDim = dim3(grid, 1, 1);
     cfg->blockDim = dim3(kThreads, 1, 1);
-    cfg->dynamicSmemBytes = gemm_smem_bytes(b_rows, p.stages, p.bk);
+    cfg->dynamicSmemBytes = gemm_smem_bytes(b_rows, p.stages, p.bk, p.a_rows ? p.a_rows : kTileM);
     cfg->stream = stream;
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = p.cluster_size;

@@ -85,6 +85,8 @@ struct GemmParams {
     int cluster_size;                // CTA group of the MMA: 1, or 2 (an SM pair, M = 256)
     int bk;                          // K per pipeline stage: 64 (128-byte swizzle) or 32 (64-byte swizzle)
     int mma_group;                   // stages the MMA warp waits for at once (1 or 2)
+    int a_rows;                      // rows of one A box (tm_x, tm_u): 0 or 128, or fewer (a multiple
+                                     // of 16) for a batch of one tile on single CTAs
     int debug_stall;
     unsigned long long debug_publish_delay_ns;   // tests: shrink units publish their flag this late
 };
@@ -144,7 +146,7 @@ int plan_segments(const int32_t* seg_offsets, const int32_t* seg_ids, int n_seg,
                   int n_adapters, Plan* plan);
 
 // kernels.cu
-size_t gemm_smem_bytes(int b_tile_rows, int stages, int bk);
+size_t gemm_smem_bytes(int b_tile_rows, int stages, int bk, int a_rows = kTileM);
 cudaError_t gemm_prepare_device();           // sets the opt-in smem limit on the current device
 cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t stream);
 int gemm_max_clusters(const GemmParams& p);  // co-resident clusters of this launch shape
