@@ -1107,6 +1107,10 @@ static int forward_host_impl(lora_linear* h, const void* x_host, int T, const in
     uint8_t* yd = static_cast<uint8_t*>(h->y_stage);
     const size_t xrow = (size_t)h->d_in * 2, yrow = (size_t)h->d_out * 2;
     std::vector<int32_t> off, ids;
+    // one chunk: nothing to overlap, so copy-in, kernel and copy-out stay on the caller's stream
+    // (no cross-stream events on the path of a short call)
+    const bool single = bounds.size() == 2;
+    cudaStream_t s_in = single ? stream : h->s_in, s_out = single ? stream : h->s_out;
     for (int c = 0; c + 1 < (int)bounds.size(); ++c) {
         const int a = bounds[c], b = bounds[c + 1];
         const int n = b - a;
@@ -1124,21 +1128,26 @@ static int forward_host_impl(lora_linear* h, const void* x_host, int T, const in
         // work list (on s_in, planned and uploaded by forward_impl), then X rows, both
         // ordered before the event the kernel waits on
         rc = forward_impl(h, xd + (size_t)a * xrow, n, off.data(), ids.data(), (int)ids.size(), W, A, B, scale,
-                          n_adapters, yd + (size_t)a * yrow, stream, h->s_in, xh + (size_t)a * xrow, h->ev_in[e],
+                          n_adapters, yd + (size_t)a * yrow, stream, s_in, xh + (size_t)a * xrow, h->ev_in[e],
                           Wq, Ws);
         if (rc != LORA_OK) return rc;
         if (n > 0) {
-            if (cudaEventRecord(h->ev_done[e], stream) != cudaSuccess ||
-                cudaStreamWaitEvent(h->s_out, h->ev_done[e], 0) != cudaSuccess)
+            if (!single && (cudaEventRecord(h->ev_done[e], stream) != cudaSuccess ||
+                            cudaStreamWaitEvent(s_out, h->ev_done[e], 0) != cudaSuccess))
                 return LORA_ECUDA;
             if (cudaMemcpyAsync(yh + (size_t)a * yrow, yd + (size_t)a * yrow, (size_t)n * yrow, cudaMemcpyDeviceToHost,
-                                h->s_out) != cudaSuccess)
+                                s_out) != cudaSuccess)
                 return LORA_ECUDA;
         }
     }
-    if (cudaStreamSynchronize(stream) != cudaSuccess || cudaStreamSynchronize(h->s_out) != cudaSuccess)
+    // the status word travels back with the last rows of Y (on the copy-out stream, after the
+    // last kernel), so the call ends with waits only and no further round trip
+    if (!single && (cudaEventRecord(h->ev_done[15], stream) != cudaSuccess ||
+                    cudaStreamWaitEvent(s_out, h->ev_done[15], 0) != cudaSuccess))
         return LORA_ECUDA;
-    if (cudaMemcpy(h->status_host, h->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    if (cudaMemcpyAsync(h->status_host, h->status, sizeof(int), cudaMemcpyDeviceToHost, s_out) != cudaSuccess)
+        return LORA_ECUDA;
+    if (cudaStreamSynchronize(stream) != cudaSuccess || (!single && cudaStreamSynchronize(s_out) != cudaSuccess))
         return LORA_ECUDA;
     return *h->status_host ? LORA_ETIMEOUT : LORA_OK;
 }
