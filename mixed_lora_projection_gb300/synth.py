@@ -84,6 +84,13 @@ _ridge_off, _ridge_ids = _segs([8] * 6 + [300], [0] * 6 + [1])
 _NEAR_RIDGE = Workload("mixed_near_ridge", 5, 348, 5120, 34816, 256, _ridge_off, _ridge_ids,
                        note="48 decode rows + one 300-token decision on adapter 1, gate_up 5120->34816")
 
+_c8_off, _c8_ids = _segs([8] * 6 + [300] * 8, [0] * 6 + [1] * 8)
+_CONCURRENT_8 = Workload("mixed_8x300", 6, 2448, 5120, 34816, 256, _c8_off, _c8_ids,
+                         note="48 decode rows + eight concurrent 300-token decisions on adapter 1, gate_up 5120->34816")
+_tail_off, _tail_ids = _segs([8] * 6 + [1552], [0] * 6 + [1])
+_PREFIX_TAIL = Workload("prefix_tail_1552", 7, 1600, 5120, 34816, 256, _tail_off, _tail_ids,
+                        note="48 decode rows + a 1,552-row decision tail after a reused prefix on adapter 1, gate_up")
+
 # 2048-row batch of the 24-layer sweep: base 300, A 400, base 362, A 333, base 362, A 291.
 SWEEP_LENGTHS = (300, 400, 362, 333, 362, 291)
 SWEEP_IDS = (0, 1, 0, 1, 0, 1)
@@ -102,7 +109,8 @@ def sweep_workload(proj: str, multi_adapter: bool = False) -> Workload:
                     note="2048-token batch, half adapter rows in 3 segments, half base rows")
 
 
-WORKLOADS = {w.name: w for w in (_TINY, _PREFILL_16K, _MIXED, _MIXED_DECODE, _PREFILL_32K, _NEAR_RIDGE)}
+WORKLOADS = {w.name: w for w in (_TINY, _PREFILL_16K, _MIXED, _MIXED_DECODE, _PREFILL_32K, _NEAR_RIDGE,
+                                  _CONCURRENT_8, _PREFIX_TAIL)}
 for _p, _, _ in SWEEP_PROJECTIONS:
     WORKLOADS[f"sweep_{_p}"] = sweep_workload(_p)
     WORKLOADS[f"sweep_{_p}_multi"] = sweep_workload(_p, True)

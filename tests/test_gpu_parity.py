@@ -390,7 +390,8 @@ def test_host_buffers_path_matches_device_path(dev, name):
 
 # --------------------------------------------------------------------------- full-size workloads
 
-FULL = ["prefill_16k", "mixed_batch", "mixed_decode", "mixed_near_ridge", "prefill_32k"]
+FULL = ["prefill_16k", "mixed_batch", "mixed_decode", "mixed_near_ridge", "prefill_32k", "mixed_8x300",
+        "prefix_tail_1552"]
 
 
 @pytest.mark.parametrize("name", FULL)
