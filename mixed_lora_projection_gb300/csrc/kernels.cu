@@ -481,7 +481,7 @@ cudaError_t gemm_prepare_device() {
 static void launch_config(const GemmParams& p, int grid, cudaStream_t stream, cudaLaunchConfig_t* cfg,
                           cudaLaunchAttribute* attr) {
     const int b_rows = (p.tile_n > p.shrink_n ? p.tile_n : p.shrink_n) / p.cluster_size;
-    memset(cfg, 0, sizeof(*cfg));
+    *cfg = cudaLaunchConfig_t{};
     cfg->gridDim = dim3(grid, 1, 1);
     cfg->blockDim = dim3(kThreads, 1, 1);
     cfg->dynamicSmemBytes = gemm_smem_bytes(b_rows, p.stages, p.bk, p.a_rows ? p.a_rows : kTileM);
