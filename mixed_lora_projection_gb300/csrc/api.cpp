@@ -304,12 +304,14 @@ int max_clusters(lora_linear* h, const GemmParams& p) {
 
 // Per-SM cycles of one 64-wide K-step of an N-column unit, measured on GB300: a single CTA
 // is bound by how fast its shared memory fills (A + B tile, ~61 bytes per clock); an SM pair
-// lands only half of B per SM and is bound by the MMA stream (N/2 cycles per K=16 MMA, plus
-// the per-step barrier round trip, paid once per two K-steps) and the pair's coupling.
+// lands only half of B per SM and its cost falls less than proportionally with N (the A tile
+// and the per-step barrier round trips stay): fitted to 16k-prefill units of 256, 224 and 192
+// columns, which cost 1 : 0.954 : 0.862 per unit.
 double kstep_cycles(int cs, int n) {
+    if (cs > 1) return 300.0 + 1.58 * n;
     const double mma = 4.0 * std::max(n / 2.0, 48.0) + 130.0;
-    const double fill = (kTileM + (double)n / cs) * kTileK * 2.0 / 61.0;
-    return cs == 1 ? std::max(fill, mma) : 1.1 * std::max(fill, mma);
+    const double fill = (kTileM + (double)n) * kTileK * 2.0 / 61.0;
+    return std::max(fill, mma);
 }
 
 // Makespan (per-SM cycles) of the persistent round-robin schedule of one launch shape.
