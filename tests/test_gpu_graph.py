@@ -110,3 +110,38 @@ def test_capture_of_a_call_with_an_uploaded_work_list_is_refused(dev):
         torch.cuda.synchronize()
         assert ll.status() == 0
     assert torch.equal(y, y2)
+
+
+def test_four_bit_base_graph_replays(dev):
+    # the 4-bit-base path (shrink launch + 4-bit kernel) recorded once and replayed with fresh X
+    from mixed_lora_projection_gb300 import w4_repack
+    from mixed_lora_projection_gb300.synth import Workload, make_w4_base
+    import numpy as np
+    lens, ids = [48, 200, 8], [0, 1, 0]
+    off = [0] + np.cumsum(lens).tolist()
+    w = Workload("w4g", 31, off[-1], 512, 1024, 64, tuple(off), tuple(ids), scales=(0.75,))
+    inp = make_inputs(w, dev)
+    q, sc = make_w4_base(w, dev)
+    kq = w4_repack(q)
+    with _ll(w) as ll:
+        want = []
+        for seed in (41, 42):
+            _fresh_x(inp, seed)
+            want.append(ll.forward_w4(inp.x, off, ids, kq, sc, inp.a, inp.b, inp.scales).clone())
+        y = torch.empty_like(want[0])
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            ll.forward_w4(inp.x, off, ids, kq, sc, inp.a, inp.b, inp.scales, y=y)
+        torch.cuda.current_stream(dev).wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            ll.forward_w4(inp.x, off, ids, kq, sc, inp.a, inp.b, inp.scales, y=y)
+        for seed, ref in zip((41, 42, 41), (want[0], want[1], want[0])):
+            _fresh_x(inp, seed)
+            y.zero_()
+            g.replay()
+            torch.cuda.synchronize()
+            assert torch.equal(y, ref)
+        assert ll.status() == 0
