@@ -947,6 +947,11 @@ int forward_impl(lora_linear* h, const void* x, int T, const int32_t* seg_offset
         while (q.pstages < 8 && w4_smem_bytes(q.stages, q.pstages + 1, q.x_stage_bytes, q.feature_tiles) <=
                                     (size_t)kSmemLimit)
             ++q.pstages;
+        // whole 32-row chunks of Y leave through TMA stores (Y 16-byte aligned, d_out % 8 == 0:
+        // both checked before any launch)
+        if (encode_plain_2d(h, &q.tm_y, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, y, h->d_out, T, kW4TileM, 32) !=
+            CUDA_SUCCESS)
+            return LORA_ECUDA;
         q.debug_stall = h->debug_stall;
         const int units = q.n_groups * q.n_ntiles;
         if (launch_w4(q, std::min(units, h->num_sms), stream) != cudaSuccess) return LORA_ECUDA;

@@ -44,6 +44,35 @@ constexpr uint32_t kXStageMaxBytes = 256 * 128;   // B operand: up to 256 token 
 constexpr uint32_t kQStageBytes = 128 * kW4PackBytes;   // packed rows of 4 K-steps
 constexpr uint32_t kSStageBytes = 2 * 128 * 2;          // two scale groups of 128 features
 constexpr uint32_t kAccCols4 = 256;               // accumulator columns (tokens)
+constexpr uint32_t kYChunkRows = 32;              // tokens per Y chunk (one tcgen05.ld of 32 columns)
+constexpr uint32_t kYStageBytes = kYChunkRows * 128 * 2;   // [32 tokens][128 features] bf16
+
+// Y chunk from shared memory to global memory through a tensor map, in this thread's bulk
+// async-group; rows and features past the tensor's extent are not written.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int c_inner, int c_outer) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(src), "r"(c_inner), "r"(c_outer)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// all of this thread's bulk stores have finished reading shared memory
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// all of this thread's bulk stores are complete
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// generic-proxy shared-memory writes made visible to the async proxy (the TMA store that follows)
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+// named barrier of the four epilogue warps that also ANDs a predicate over them
+__device__ __forceinline__ int epilogue_bar_and(int v) {
+    int r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 q, %1, 0;\n\t"
+        "bar.red.and.pred p, 1, %2, q;\n\tselp.b32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"(v), "n"(kEpilogueThreads)
+        : "memory");
+    return r;
+}
 
 // D[tmem] (+)= A[tmem] * B[smem]^T, kind::f16 (bf16 in, fp32 accumulate), issued by the lane
 // with pred != 0 of a converged warp.
@@ -108,7 +137,8 @@ __global__ void __launch_bounds__(kW4Threads, 1) lora_w4_kernel(const __grid_con
     // (B operand) in the first 16 KB and the B_a tile (A operand) in the second 16 KB
     const uint32_t x_stage = (uint32_t)p.x_stage_bytes;
     uint8_t* x_ring = base;
-    uint8_t* q_ring = x_ring + (size_t)stages * x_stage;
+    uint8_t* y_stage = x_ring + (size_t)stages * x_stage;   // 2 x 8 KB: Y chunks on their way out
+    uint8_t* q_ring = y_stage + kYStageBytes * 2;
     uint8_t* s_ring = q_ring + (size_t)pstages * kQStage;
     uint64_t* bars = reinterpret_cast<uint64_t*>(s_ring + (size_t)pstages * kSStage);
     uint64_t* full = bars;                          // TMA bytes + one arrive per converter quadrant
@@ -436,20 +466,30 @@ __global__ void __launch_bounds__(kW4Threads, 1) lora_w4_kernel(const __grid_con
         // ------------------------------------------------------------ epilogue (warps 2..5)
         const int q = warp & 3;
         const uint32_t lane_off = (uint32_t)(32 * q) << 16;
+        // Whole 32-token chunks go out through shared memory and TMA stores (two 8 KB buffers;
+        // thread = feature, so each warp writes 64 contiguous bytes per token row), so the
+        // accumulator is released once it has been read rather than after ~256 strided global
+        // stores per thread; the ragged last chunk of a tile is stored from registers.
         __nv_bfloat16* y = reinterpret_cast<__nv_bfloat16*>(p.y);
+        const bool issuer = warp == 2 && lane == 0;
+        int chunk = 0;
         int it = 0;
         for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++it) {
             const W4Unit w = w4_unit<FT>(p, groups, u);
             int ok = 1;
             if (lane == 0) ok = wait_bounded(smem_addr(tfull), it & 1, abort_flag, p.status, limit, true);
             ok = __shfl_sync(0xffffffffu, ok, 0);
+            ok = epilogue_bar_and(ok);   // the four warps leave together (they share barriers)
             if (!ok) break;
             tc_fence_after();
             // FT = 1: token tile h at accumulator columns 128 h; FT = 2 (one token tile): feature
-            // tile f at accumulator columns 128 f
+            // tile f at accumulator columns 128 f. The accumulator is released right after the
+            // unit's last tensor-memory load, before that chunk's stores.
+            const int last_hf = FT == 1 ? (w.g.nrows[1] > 0 ? 1 : 0) : 1;
             for (int hf = 0; hf < 2; ++hf) {
                 const int h = FT == 1 ? hf : 0;
-                const int n = w.n0 + (FT == 1 ? 0 : kW4TileM * hf) + 32 * q + lane;
+                const int n_tile = w.n0 + (FT == 1 ? 0 : kW4TileM * hf);
+                const int n = n_tile + 32 * q + lane;
                 const bool n_ok = n < p.d_out;
                 const int rows = (FT == 1 || hf < FT) ? w.g.nrows[h] : 0;
                 for (int c = 0; c < rows; c += 32) {
@@ -458,18 +498,36 @@ __global__ void __launch_bounds__(kW4Threads, 1) lora_w4_kernel(const __grid_con
                     tmem_ld16(taddr, v);
                     tmem_ld16(taddr + 16u, v + 16);
                     tmem_ld_wait();
-                    if (n_ok) {
+                    if (hf == last_hf && c + 32 >= rows) {
+                        tc_fence_before();
+                        mbar_arrive(smem_addr(tempty));
+                    }
+                    const int m = rows - c < 32 ? rows - c : 32;
+                    if (m == 32) {
+                        uint8_t* buf = y_stage + (size_t)(chunk & 1) * kYStageBytes;
+                        __nv_bfloat16* sb = reinterpret_cast<__nv_bfloat16*>(buf) + 32 * q + lane;
+#pragma unroll
+                        for (int t = 0; t < 32; ++t) sb[t * 128] = __float2bfloat16_rn(__uint_as_float(v[t]));
+                        fence_proxy_async_smem();
+                        // the store issued from this buffer two chunks ago has read it before the
+                        // barrier of the previous chunk; the one from the other buffer before this one
+                        if (issuer) bulk_wait_read_all();
+                        epilogue_bar_sync();
+                        if (issuer) {
+                            tma_store_2d(&p.tm_y, smem_addr(buf), n_tile, w.g.row0[h] + c);
+                            bulk_commit_group();
+                        }
+                        ++chunk;
+                    } else if (n_ok) {
                         __nv_bfloat16* col = y + (size_t)(w.g.row0[h] + c) * p.d_out + n;
-                        const int m = rows - c < 32 ? rows - c : 32;
 #pragma unroll
                         for (int t = 0; t < 32; ++t)
                             if (t < m) col[(size_t)t * p.d_out] = __float2bfloat16_rn(__uint_as_float(v[t]));
                     }
                 }
             }
-            tc_fence_before();
-            mbar_arrive(smem_addr(tempty));
         }
+        if (issuer) bulk_wait_all();
     }
 
     __syncwarp();
@@ -484,7 +542,7 @@ __global__ void __launch_bounds__(kW4Threads, 1) lora_w4_kernel(const __grid_con
 }  // namespace dev
 
 size_t w4_smem_bytes(int stages, int pstages, int x_stage_bytes, int ft) {
-    return 1024 + (size_t)stages * (size_t)x_stage_bytes +
+    return 1024 + (size_t)stages * (size_t)x_stage_bytes + 2 * (size_t)dev::kYStageBytes +
            (size_t)pstages * (size_t)ft * (dev::kQStageBytes + dev::kSStageBytes) +
            8 * (2 * (size_t)stages + 2 * (size_t)pstages + 3) + 16;
 }

@@ -115,6 +115,7 @@ struct W4Params {
     CUtensorMap tm_u;                // U [u_rows, rank] bf16, box 64 x 128, 128-byte swizzle
     CUtensorMap tm_wq;               // packed base [d_out, d_in/2] u8 (kernel layout), box 128 x 128, swizzled
     CUtensorMap tm_ws;               // scales [d_in/128, d_out] bf16, box 128 x 2
+    CUtensorMap tm_y;                // Y [T, d_out] bf16, box 128 x 32, no swizzle (whole 32-row chunks)
     const CUtensorMap* tm_b;         // device array per compact adapter (when not inline)
     const W4Group* groups;           // device array (when not inline)
     void* y;                         // Y [T, d_out] bf16
