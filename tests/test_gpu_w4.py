@@ -120,6 +120,43 @@ def test_w4_full_size_sampled_rows(dev, name):
     assert rel_err(y[torch.as_tensor(rows, device=dev)], ref) <= TOL
 
 
+ROWS = [1, 16, 17, 48, 64, 80, 128]
+
+
+@pytest.mark.parametrize("T", ROWS)
+def test_w4_decode_batches_match_oracle(dev, T):
+    # one token tile without adapter rows (two 128-feature tiles per unit, X boxes of the
+    # batch's rows); d_out not a multiple of 256
+    lens = [T // 2, T - T // 2] if T > 1 else [1]
+    off = [0] + np.cumsum(lens).tolist()
+    w = Workload("w4dec", 15, T, 640, 1000, 32, tuple(off), tuple([0] * len(lens)))
+    inp = make_inputs(w, dev)
+    q, sc = make_w4_base(w, dev)
+    with _ll(w) as ll:
+        y = ll.forward_w4(inp.x, off, [0] * len(lens), _kq(q), sc, inp.a, inp.b, inp.scales)
+        torch.cuda.synchronize()
+        assert ll.status() == 0
+    assert rel_err(y, _oracle(inp, q, sc, off, [0] * len(lens))) <= TOL
+
+
+def test_w4_decode_rows_equal_the_same_rows_in_a_larger_batch(dev):
+    # 48 base rows alone (two feature tiles per unit, 48-row X boxes) and as the first rows of
+    # a 300-row batch with adapter rows (one feature tile, two token tiles per unit): every
+    # output summed in the same K order, the same bits
+    lens, ids = [8] * 6 + [252], [0] * 6 + [1]
+    off = [0] + np.cumsum(lens).tolist()
+    w = Workload("w4inv", 16, off[-1], 1024, 1536, 64, tuple(off), tuple(ids), scales=(0.5,))
+    inp = make_inputs(w, dev)
+    q, sc = make_w4_base(w, dev)
+    kq = _kq(q)
+    with _ll(w) as ll:
+        full = ll.forward_w4(inp.x, off, ids, kq, sc, inp.a, inp.b, inp.scales).clone()
+        alone = ll.forward_w4(inp.x[:48], off[:7], ids[:6], kq, sc, inp.a, inp.b, inp.scales)
+        torch.cuda.synchronize()
+        assert ll.status() == 0
+    assert torch.equal(full[:48], alone)
+
+
 def test_w4_rejects_d_in_not_multiple_of_128(dev):
     from mixed_lora_projection_gb300 import LoraError
     w = Workload("w4bad", 13, 16, 192, 256, 16, (0, 16), (0,))
