@@ -16,5 +16,7 @@ from .lora_linear_oracle import (  # noqa: F401
     max_rel_err,
     W4_GROUP,
     w4_dequantize_fp64,
+    w4_weights_bf16_fp64,
+    round_to_bf16_fp64,
     lora_linear_w4_fp64,
 )

@@ -23,7 +23,9 @@ What it computes (plain definitions, written out; no blocking, fusion or reorder
 
 Arithmetic: every input arrives as the exact bf16 values (``bf16_bits_to_f64``), and all
 products and sums are fp64 (numpy float64 matmul) with no intermediate rounding. The
-GPU path rounds the shrink output U and the output Y to bf16; the oracle does not.
+GPU path rounds the shrink output U and the output Y to bf16; the oracle does not. The one
+rounding the oracle does take is part of the method: a 4-bit base (W4A16) is widened to the
+16-bit activation type, so ``w4_weights_bf16_fp64`` rounds each q * s to bf16 once.
 
 Pins (tests/test_oracle.py, run with ``-m "not gpu"``): brute-force triple loops on tiny
 shapes, the merged-weight identity, routing (id-0 rows equal the base product), B = 0 is a
@@ -183,9 +185,36 @@ def w4_dequantize_fp64(qweight, scale_bits) -> np.ndarray:
     return q.astype(np.float64) * np.repeat(s.T, W4_GROUP, axis=1)
 
 
+def round_to_bf16_fp64(values) -> np.ndarray:
+    """Each value rounded to the nearest bf16 (ties to the even significand), as float64.
+
+    Defined for values that binary32 holds exactly (checked): bf16 keeps the upper 16 bits of
+    a binary32, so the rounding adds 0x7FFF plus the lowest kept bit to the pattern and drops
+    the lower 16 bits (round half to even on the 16 dropped bits).
+    """
+    v = np.asarray(values, dtype=np.float64)
+    f = v.astype(np.float32)
+    if not np.array_equal(f.astype(np.float64), v) or not np.all(np.isfinite(f)):
+        raise ValueError("values must be finite and exact in binary32")
+    bits = f.view(np.uint32).astype(np.uint64)
+    bits = (bits + 0x7FFF + ((bits >> 16) & 1)) & 0xFFFF0000
+    return bits.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def w4_weights_bf16_fp64(qweight, scale_bits) -> np.ndarray:
+    """The 4-bit base widened to the activation type: bf16(q[n, k] * s[k // 128, n]).
+
+    "Qwen3.8-27B on one RTX 3090 with patched vLLM + DFlash2" runs the base as W4A16: 4-bit
+    weights, 16-bit activations, so each weight times its group scale is widened to the
+    16-bit activation type (bf16 here) before it meets X. q * s has up to 11 significant bits
+    (a 4-bit integer times an 8-bit significand), so the widening rounds it once (RNE).
+    """
+    return round_to_bf16_fp64(w4_dequantize_fp64(qweight, scale_bits))
+
+
 def lora_linear_w4_fp64(x, seg_offsets, seg_ids, qweight, scale_bits, a_list, b_list, scales) -> np.ndarray:
-    """The projection with a 4-bit base: the plain definition on the dequantised weights."""
-    return lora_linear_fp64(x, seg_offsets, seg_ids, w4_dequantize_fp64(qweight, scale_bits),
+    """The projection with a 4-bit base: the plain definition on the widened weights."""
+    return lora_linear_fp64(x, seg_offsets, seg_ids, w4_weights_bf16_fp64(qweight, scale_bits),
                             a_list, b_list, scales)
 
 

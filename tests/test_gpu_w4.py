@@ -5,7 +5,7 @@ import numpy as np
 import pytest
 import torch
 
-from oracle import bf16_bits_to_f64, lora_linear_w4_fp64, row_adapter_ids, w4_dequantize_fp64
+from oracle import bf16_bits_to_f64, lora_linear_w4_fp64, row_adapter_ids, w4_dequantize_fp64, w4_weights_bf16_fp64
 from oracle import lora_linear_rows_fp64
 from mixed_lora_projection_gb300.synth import WORKLOADS, Workload, bf16_bits, make_inputs, make_w4_base
 
@@ -51,7 +51,7 @@ def _oracle(inp, q, sc, off, ids, rows=None):
     b64 = [f64(b) for b in inp.b]
     if rows is None:
         return lora_linear_w4_fp64(f64(inp.x), off, ids, qn, sb, a64, b64, inp.scales)
-    w = w4_dequantize_fp64(qn, sb)
+    w = w4_weights_bf16_fp64(qn, sb)
     rid = row_adapter_ids(off, ids, inp.x.shape[0])[rows]
     return lora_linear_rows_fp64(f64(inp.x[torch.as_tensor(rows, device=inp.x.device)]), rid, w, a64, b64, inp.scales)
 
@@ -68,6 +68,9 @@ SMALL = [
     (48, 512, 1000, 32, [8] * 6, [0] * 6, 1),
     (100, 256, 256, 16, [30, 40, 30], [1, 0, 2], 2),
     (128, 256, 512, 16, [128], [0], 1),
+    # the smallest legal shapes (d_in one 128-input group, d_out and rank 8)
+    (3, 128, 8, 8, [3], [1], 1),
+    (2, 128, 16, 8, [2], [0], 1),
 ]
 
 
@@ -103,6 +106,8 @@ def test_w4_dequantisation_is_exact_per_weight(dev):
     wd = w4_dequantize_fp64(q.cpu().numpy(), bf16_bits(sc))          # exact q * s
     want = torch.from_numpy(wd.T.copy()).to(torch.bfloat16)           # rounded once, RNE
     assert torch.equal(y.cpu(), want)
+    widened = w4_weights_bf16_fp64(q.cpu().numpy(), bf16_bits(sc))    # the oracle's widening
+    assert torch.equal(y.cpu().double(), torch.from_numpy(widened.T.copy()))
 
 
 @pytest.mark.parametrize("name", ["mixed_decode", "mixed_near_ridge", "sweep_qkv_multi", "prefill_16k"])
@@ -170,6 +175,7 @@ def test_w4_rejects_d_in_not_multiple_of_128(dev):
 
 @pytest.mark.parametrize("name", ["tiny", "mixed_batch"])
 def test_w4_host_buffers_match_device_path(dev, name):
+    # row chunks from 2,048 rows; every row summed as in the device path: the same bits
     w = WORKLOADS[name]
     inp = make_inputs(w, dev)
     q, sc = make_w4_base(w, dev) if w.d_in % 128 == 0 else (None, None)
@@ -180,7 +186,7 @@ def test_w4_host_buffers_match_device_path(dev, name):
         y = ll.forward_w4(inp.x, w.seg_offsets, w.seg_ids, kq, sc, inp.a, inp.b, inp.scales)
         ll.forward_host_w4(x_host, w.seg_offsets, w.seg_ids, kq, sc, inp.a, inp.b, inp.scales, y_host)
     torch.cuda.synchronize()
-    assert rel_err(y_host, f64(y)) <= TOL
+    assert torch.equal(y.cpu(), y_host)
 
 
 def test_w4_repack_layout_bit_exact(dev):

@@ -1,8 +1,12 @@
-"""Pins for the oracle's 4-bit base-weight decoding (W[n,k] = q[n,k] * s[k//128, n])."""
+"""Pins for the oracle's 4-bit base-weight decoding (W[n,k] = q[n,k] * s[k//128, n]) and its
+widening to bf16 (one round-to-nearest-even of q * s)."""
 import numpy as np
 import pytest
 
-from oracle import W4_GROUP, lora_linear_fp64, lora_linear_w4_fp64, max_rel_err, w4_dequantize_fp64
+import torch
+
+from oracle import (W4_GROUP, lora_linear_fp64, lora_linear_w4_fp64, max_rel_err, round_to_bf16_fp64,
+                    w4_dequantize_fp64, w4_weights_bf16_fp64)
 
 
 def _bf16_bits_of(values):
@@ -57,7 +61,7 @@ def test_w4_projection_is_the_projection_of_the_decoded_weights():
     B = [rng.standard_normal((d_out, r))]
     off, ids = [0, 7, 20], [1, 0]
     y = lora_linear_w4_fp64(x, off, ids, packed, sc, A, B, [1.5])
-    w = w4_dequantize_fp64(packed, sc)
+    w = w4_weights_bf16_fp64(packed, sc)
     # brute force for one row of each kind
     for t in (3, 15):
         base = np.array([sum(x[t, k] * w[n, k] for k in range(d_in)) for n in range(d_out)])
@@ -66,6 +70,44 @@ def test_w4_projection_is_the_projection_of_the_decoded_weights():
             base = base + 1.5 * (B[0] @ u)
         assert max_rel_err(y[t], base) < 1e-12
     assert max_rel_err(y, lora_linear_fp64(x, off, ids, w, A, B, [1.5])) == 0.0
+
+
+def test_bf16_rounding_closed_forms():
+    # 7 (1 + 2^-7) = 7.0546875 lies between the bf16 values 7.03125 and 7.0625: nearest 7.0625
+    assert round_to_bf16_fp64([7 * (1 + 2.0 ** -7)]).tolist() == [7.0625]
+    # ties go to the even significand: 3.0234375 is halfway between 3.015625 (odd) and 3.03125
+    assert round_to_bf16_fp64([3 * (1 + 2.0 ** -7), -3 * (1 + 2.0 ** -7)]).tolist() == [3.03125, -3.03125]
+    # 1 + 2^-8 is halfway between 1 (even) and 1 + 2^-7 (odd); 1 + 3 2^-8 between odd and even
+    assert round_to_bf16_fp64([1 + 2.0 ** -8, 1 + 3 * 2.0 ** -8]).tolist() == [1.0, 1 + 2.0 ** -6]
+    # bf16 values and zero are fixed points
+    assert round_to_bf16_fp64([0.0, -0.0, 0.5, -4.0, 1 + 2.0 ** -7]).tolist() == [0.0, 0.0, 0.5, -4.0, 1 + 2.0 ** -7]
+    with pytest.raises(ValueError):
+        round_to_bf16_fp64([0.1])                    # not exact in binary32
+
+
+def test_bf16_rounding_equals_the_library_conversion():
+    # random binary32 values of every magnitude: the same as PyTorch's float32 -> bfloat16 cast
+    rng = np.random.default_rng(2)
+    f = (rng.standard_normal(20000) * np.exp2(rng.integers(-30, 30, 20000))).astype(np.float32)
+    f[:64] = np.arange(64, dtype=np.float32) * np.float32(1 + 2.0 ** -9)     # many exact ties
+    want = torch.from_numpy(f).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(round_to_bf16_fp64(f.astype(np.float64)), want)
+
+
+def test_widened_weights_round_each_decoded_weight_once():
+    rng = np.random.default_rng(3)
+    d_out, d_in = 4, 256
+    packed = rng.integers(0, 256, (d_out, d_in // 2)).astype(np.uint8)
+    sc = _bf16_bits_of(np.array([[1 + 2.0 ** -7, 0.5, 0.1015625, 3.0], [0.25, 1.0078125, 2.0, 0.0625]]))
+    exact = w4_dequantize_fp64(packed, sc)
+    wide = w4_weights_bf16_fp64(packed, sc)
+    assert np.array_equal(wide, round_to_bf16_fp64(exact))
+    # power-of-two scales: q s is already a bf16 value
+    assert np.array_equal(wide[1, :128], exact[1, :128]) and np.array_equal(wide[0, 128:], exact[0, 128:])
+    # q = 7 or -3 with s = 1 + 2^-7 (row 0, first group): 7.0625 and -3.03125
+    q = exact[0, :128] / (1 + 2.0 ** -7)
+    assert np.all(wide[0, :128][q == 7] == 7.0625) and np.all(wide[0, :128][q == -3] == -3.03125)
+    assert np.count_nonzero(wide != exact) > 0
 
 
 def test_bad_scale_shape_is_rejected():
