@@ -233,17 +233,20 @@ def run_ours(args, rank, world, dist):
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # one event per step boundary: the total over the K steps is the reported time; the
+    # per-step durations give the median / min / max beside it
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
     t0 = time.time()
-    ev0.record(stream)
+    evs[0].record(stream)
     for i in range(args.steps):
         step(i)
-    ev1.record(stream)
+        evs[i + 1].record(stream)
     torch.cuda.synchronize()
     t1 = time.time()
     if dist:
         dist.barrier()
-    elapsed_ms = ev0.elapsed_time(ev1)
+    elapsed_ms = evs[0].elapsed_time(evs[-1])
+    step_ms = sorted(evs[i].elapsed_time(evs[i + 1]) for i in range(args.steps))
     launches = sum(ll.timing(1)[2] for ll in handles.values()) - launches0
     fused_ms = sum(ll.timing(1)[0] for ll in handles.values())
     fused_n = sum(ll.timing(1)[1] for ll in handles.values())
@@ -340,6 +343,8 @@ def run_ours(args, rank, world, dist):
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "step_ms": {"median": round(step_ms[len(step_ms) // 2], 5), "min": round(step_ms[0], 5),
+                    "max": round(step_ms[-1], 5), "of": "eager steps, rank 0"},
         "data": "synthetic (seeded Gaussian bf16; no checkpoint)",
         "config": {"workload": args.workload + ("+w4" if args.w4 else ""),
                    **({"raster": args.raster} if args.raster else {}),
