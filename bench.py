@@ -413,12 +413,44 @@ def _block_flops(w, off, ids):
     return 2.0 * rows * w.d_in * w.d_out + 2.0 * ta * w.rank * (w.d_in + w.d_out)
 
 
+def _blas_threads():
+    """Threads of the BLAS behind numpy's matmul (what the oracle runs on), or None."""
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i["num_threads"] for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return max(n)
+    except Exception:
+        pass
+    import ctypes
+    import glob
+    import numpy
+    for path in glob.glob(os.path.join(os.path.dirname(numpy.__file__), os.pardir, "numpy.libs", "*openblas*")):
+        try:
+            lib = ctypes.CDLL(path)
+        except OSError:
+            continue
+        for name in ("scipy_openblas_get_num_threads64_", "scipy_openblas_get_num_threads",
+                     "openblas_get_num_threads64_", "openblas_get_num_threads"):
+            f = getattr(lib, name, None)
+            if f is not None:
+                return int(f())
+    return None
+
+
+def _host_threads():
+    """(threads the oracle uses, cores in this process's affinity mask)."""
+    affinity = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    blas = _blas_threads()
+    return (min(blas, affinity) if blas else affinity), affinity
+
+
 def cpu_baseline(items, seconds):
     """The fp64 oracle, as it stands, on a contiguous block of the workload's rows, sized
     to about `seconds` of host time."""
     from oracle import lora_linear_fp64
     w, layer, pi = items[0]
-    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    cores, affinity = _host_threads()
     rows = min(w.T, 64)
     data = _oracle_block(w, layer, pi, rows)
     t = time.perf_counter()
@@ -432,8 +464,9 @@ def cpu_baseline(items, seconds):
     dt = time.perf_counter() - t
     fl = _block_flops(w, data[1], data[2])
     return {"value": round(fl / dt / 1e12, 5), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "host_cores": affinity,
             "sample": f"rows [0,{rows}) of {w.name} ({w.T} rows), layer 0, all {w.d_out} outputs: "
-                      f"{fl / 1e9:.1f} GFLOP fp64 in {dt:.1f} s (numpy/OpenBLAS, {cores} threads)"}
+                      f"{fl / 1e9:.1f} GFLOP fp64 in {dt:.1f} s (numpy/OpenBLAS, {cores} BLAS threads)"}
 
 
 def run_reference(args, rank, world):
@@ -441,7 +474,7 @@ def run_reference(args, rank, world):
     from oracle import lora_linear_fp64
     items = _workloads(args.workload)
     w, layer, pi = items[0]
-    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    cores, affinity = _host_threads()
     budget = max(0.05, args.cpu_seconds * 4 / max(1, args.steps + args.warmup))  # ~a few minutes in all
     rows = min(w.T, 32)
     data = _oracle_block(w, layer, pi, rows)
@@ -467,7 +500,7 @@ def run_reference(args, rank, world):
             "config": {"workload": args.workload, "T": w.T, "d_in": w.d_in, "d_out": w.d_out, "rank": w.rank,
                        "sample_rows": rows},
             "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                             "sample": sample},
+                             "host_cores": affinity, "sample": sample},
             "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
