@@ -210,7 +210,9 @@ enum {
     LORA_OPT_DEBUG_STALL = 3,   /* 1 = the load warp never issues: every wait runs out (tests only) */
     LORA_OPT_TIMING = 4,        /* 1 = record CUDA events around each kernel launch */
     LORA_OPT_RASTER = 5,        /* 0 = auto, 1 = row tiles fastest, 2 = column tiles fastest,
-                                   3 = groups of LORA_OPT_RASTER_GROUP column tiles, row tiles fastest */
+                                   3 = groups of LORA_OPT_RASTER_GROUP column tiles, row tiles fastest;
+                                   4-bit base: 1 = token groups fastest, 2 = feature tiles fastest,
+                                   0 or 3 = auto */
     LORA_OPT_TWO_LAUNCH = 6,    /* 1 = shrink and fused pass as two launches (default 0: one launch) */
     LORA_OPT_CLUSTER = 7,       /* 0 = auto, 1 = one CTA per tile, 2 = SM pairs run M = 256 MMAs (tcgen05 cta_group::2) */
     LORA_OPT_RASTER_GROUP = 8,  /* column tiles per group for LORA_OPT_RASTER = 3 (default 4) */

@@ -935,6 +935,13 @@ int forward_impl(lora_linear* h, const void* x, int T, const int32_t* seg_offset
         q.wait_limit_ns = h->wait_limit_ns;
         q.n_groups = n_w4g;
         q.n_ntiles = ceil_div(h->d_out, kW4TileM * q.feature_tiles);
+        // unit order: token groups fastest when the packed base is too large to stay in L2
+        // beside the output stream while the batch's X fits there (the mixed batch on gate_up:
+        // 89 MB packed, 42 MB of X), else feature tiles fastest; LORA_OPT_RASTER 1 / 2 force it
+        const double packed_bytes = (double)h->d_out * h->d_in / 2, x_bytes = (double)T * h->d_in * 2;
+        q.tokens_fastest = h->raster == 1 ? 1
+                           : h->raster == 2 ? 0
+                           : (n_w4g > 1 && packed_bytes > 32e6 && x_bytes <= 64e6) ? 1 : 0;
         q.k_main_blocks = ceil_div(h->d_in, 64);
         q.k_lora_blocks = ceil_div(h->rank, 64);
         q.k_pack_blocks = ceil_div(q.k_main_blocks, 4);

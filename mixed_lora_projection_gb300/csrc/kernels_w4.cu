@@ -100,6 +100,16 @@ __device__ __forceinline__ void tmem_st_wait() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// Unit order: feature tiles fastest (each token group's X stays in L2 while the packed base
+// streams past it), or token groups fastest (each packed feature tile is read once per wave
+// while every group's X stays in L2: for a base too large to stay in L2 beside the output).
+__device__ __forceinline__ int w4_group_of(const W4Params& p, int u) {
+    return p.tokens_fastest ? u % p.n_groups : u / p.n_ntiles;
+}
+__device__ __forceinline__ int w4_ntile_of(const W4Params& p, int u) {
+    return p.tokens_fastest ? u / p.n_groups : u % p.n_ntiles;
+}
+
 struct W4Unit {
     W4Group g;
     int n0;          // first output feature
@@ -109,9 +119,9 @@ struct W4Unit {
 template <int FT>
 __device__ __forceinline__ W4Unit w4_unit(const W4Params& p, const W4Group* groups, int u) {
     W4Unit r;
-    const int gi = u / p.n_ntiles;
+    const int gi = w4_group_of(p, u);
     r.g = groups[gi];
-    r.n0 = (u % p.n_ntiles) * kW4TileM * FT;
+    r.n0 = w4_ntile_of(p, u) * kW4TileM * FT;
     r.n = r.g.nrows[1] > 0 ? 128 + ((r.g.nrows[1] + 15) & ~15) : ((r.g.nrows[0] + 15) & ~15);
     return r;
 }
@@ -256,7 +266,7 @@ __global__ void __launch_bounds__(kW4Threads, 1) lora_w4_kernel(const __grid_con
             long long issued = 0;
             bool ok = true;
             for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-                const int n0 = (u % p.n_ntiles) * kW4TileM * FT;
+                const int n0 = w4_ntile_of(p, u) * kW4TileM * FT;
                 for (int pb = 0; pb < p.k_pack_blocks; ++pb) {
                     if (!wait_warp(smem_addr(&pempty[ps]), pph ^ 1, abort_flag, p.status, limit)) {
                         ok = false;

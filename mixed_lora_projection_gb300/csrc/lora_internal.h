@@ -130,6 +130,7 @@ struct W4Params {
     int stages;                      // X / U ring
     int pstages;                     // packed ring
     int x_stage_bytes;               // bytes per X / U ring stage (a multiple of 1024)
+    int tokens_fastest;              // unit order: 1 = token groups fastest, 0 = feature tiles fastest
     int feature_tiles;               // 128-feature tiles per unit: 1, or 2 for one token tile of at
                                      // most 128 rows with no adapter rows (tm_wq / tm_ws boxes 128 x FT)
     int debug_stall;

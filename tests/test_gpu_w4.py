@@ -162,6 +162,28 @@ def test_w4_decode_rows_equal_the_same_rows_in_a_larger_batch(dev):
     assert torch.equal(full[:48], alone)
 
 
+@pytest.mark.parametrize("name", ["mixed_batch", "mixed_8x300"])
+def test_w4_unit_orders_are_exact(dev, name):
+    # token groups fastest (the default for these: packed gate_up 89 MB, X under 64 MB) and
+    # feature tiles fastest run the same sums: the same bits
+    from mixed_lora_projection_gb300 import _lib as L
+    w = WORKLOADS[name]
+    inp = make_inputs(w, dev)
+    q, sc = make_w4_base(w, dev)
+    kq = _kq(q)
+    off, ids = list(w.seg_offsets), list(w.seg_ids)
+    with _ll(w) as ll:
+        ys = []
+        for raster in (1, 2, 0):
+            ll.set_option(L.OPT_RASTER, raster)
+            ys.append(ll.forward_w4(inp.x, off, ids, kq, sc, inp.a, inp.b, inp.scales).clone())
+        torch.cuda.synchronize()
+        assert ll.status() == 0
+    assert torch.equal(ys[0], ys[1]) and torch.equal(ys[0], ys[2])
+    rows = sample_rows(w.T, off, ids, n_random=64, seed=6)
+    assert rel_err(ys[0][torch.as_tensor(rows, device=dev)], _oracle(inp, q, sc, off, ids, rows)) <= TOL
+
+
 def test_w4_rejects_d_in_not_multiple_of_128(dev):
     from mixed_lora_projection_gb300 import LoraError
     w = Workload("w4bad", 13, 16, 192, 256, 16, (0, 16), (0,))
