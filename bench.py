@@ -47,16 +47,16 @@ def _peaks():
 
 
 def _kernel_hash(w4: bool = False):
-    """Hash of the code the GPU runs for the projection: the device part of the kernel files
-    (up to the end of their device namespace; the host launch code after it does not count),
-    the device helpers and the shared parameter header."""
+    """Hash of the code the GPU runs for the measured kernel: the device part of its source file
+    (up to the end of its device namespace; the host launch code after it does not count), the
+    device helpers and the parameter headers it compiles from (lora_internal.h, and lora_w4.h
+    for the 4-bit kernel)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "mixed_lora_projection_gb300", "csrc")
-    for f in ("kernels.cu",) + (("kernels_w4.cu",) if w4 else ()):
-        with open(os.path.join(csrc, f)) as fh:
-            text = fh.read()
-        h.update(text[:text.index("}  // namespace dev")].encode())
-    for f in ("dev_common.cuh", "lora_internal.h"):
+    with open(os.path.join(csrc, "kernels_w4.cu" if w4 else "kernels.cu")) as fh:
+        text = fh.read()
+    h.update(text[:text.index("}  // namespace dev")].encode())
+    for f in ("dev_common.cuh", "lora_internal.h") + (("lora_w4.h",) if w4 else ()):
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]

@@ -16,6 +16,7 @@
 
 #include "../../include/lora_linear.h"
 #include "lora_internal.h"
+#include "lora_w4.h"
 
 using namespace lora;
 

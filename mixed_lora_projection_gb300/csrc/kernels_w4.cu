@@ -34,6 +34,7 @@
 
 #include "dev_common.cuh"
 #include "lora_internal.h"
+#include "lora_w4.h"
 
 namespace lora {
 namespace dev {

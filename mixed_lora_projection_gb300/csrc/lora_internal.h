@@ -91,51 +91,6 @@ struct GemmParams {
     unsigned long long debug_publish_delay_ns;   // tests: shrink units publish their flag this late
 };
 
-// 4-bit base kernel (transposed tile: output features on the MMA's M side, tokens on N).
-// A token group is one or two consecutive planner tiles (each <= 128 rows and one adapter);
-// its X rows form the B operand of up to 256 columns. Units = groups x output tiles of 128
-// features, feature tile fastest.
-constexpr int kW4TileM = 128;         // output features per unit (TMEM lanes)
-constexpr int kW4Threads = 480;       // warp 0 TMA (X, U, B_a), 1 MMA, 2..5 epilogue,
-                                      // 6..13 dequantise into TMEM, 14 TMA of the packed base
-constexpr int kW4ConvertWarps = 8;
-constexpr int kW4AStages = 8;         // most ring stages (TMEM A stages of 32 columns each)
-constexpr int kW4InlineGroups = 48;
-constexpr int kW4PackBytes = 128;     // packed bytes per row per TMA box (4 K-steps of 64)
-
-struct W4Group {
-    int32_t row0[2], nrows[2], adapter[2];  // second tile absent when nrows[1] == 0
-};
-
-struct W4Params {
-    CUtensorMap inline_bmaps[kInlineAdapters];  // B_a [d_out, rank], box 64 x 128 (inline work list)
-    W4Group inline_groups[kW4InlineGroups];
-    int inline_wl;
-    CUtensorMap tm_x;                // X [T, d_in] bf16, box 64 x 128, 128-byte swizzle
-    CUtensorMap tm_u;                // U [u_rows, rank] bf16, box 64 x 128, 128-byte swizzle
-    CUtensorMap tm_wq;               // packed base [d_out, d_in/2] u8 (kernel layout), box 128 x 128, swizzled
-    CUtensorMap tm_ws;               // scales [d_in/128, d_out] bf16, box 128 x 2
-    CUtensorMap tm_y;                // Y [T, d_out] bf16, box 128 x 32, no swizzle (whole 32-row chunks)
-    const CUtensorMap* tm_b;         // device array per compact adapter (when not inline)
-    const W4Group* groups;           // device array (when not inline)
-    void* y;                         // Y [T, d_out] bf16
-    int* status;
-    unsigned long long wait_limit_ns;
-    int n_groups;
-    int n_ntiles;                    // ceil(d_out / 128)
-    int k_main_blocks;               // ceil(d_in / 64)
-    int k_lora_blocks;               // ceil(rank / 64)
-    int k_pack_blocks;               // ceil(k_main_blocks / 4)
-    int d_out;
-    int stages;                      // X / U ring
-    int pstages;                     // packed ring
-    int x_stage_bytes;               // bytes per X / U ring stage (a multiple of 1024)
-    int tokens_fastest;              // unit order: 1 = token groups fastest, 0 = feature tiles fastest
-    int feature_tiles;               // 128-feature tiles per unit: 1, or 2 for one token tile of at
-                                     // most 128 rows with no adapter rows (tm_wq / tm_ws boxes 128 x FT)
-    int debug_stall;
-};
-
 // The plan of one call: merged segments and tiles, ids remapped to compact adapter slots.
 struct Plan {
     std::vector<int32_t> seg_off, seg_id;    // merged runs (compact ids)
@@ -153,10 +108,5 @@ cudaError_t gemm_prepare_device();           // sets the opt-in smem limit on th
 cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t stream);
 int gemm_max_clusters(const GemmParams& p);  // co-resident clusters of this launch shape
 cudaError_t w4_repack(const void* src, void* dst, long long n_words, int grid, cudaStream_t stream);
-
-// kernels_w4.cu
-size_t w4_smem_bytes(int stages, int pstages, int x_stage_bytes, int ft);
-cudaError_t w4_prepare_device();
-cudaError_t launch_w4(const W4Params& p, int grid, cudaStream_t stream);
 
 }  // namespace lora
