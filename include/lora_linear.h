@@ -48,14 +48,18 @@ enum {
 /* Limits of this library. */
 #define LORA_MAX_RANK 256   /* adapter rank: the shrink writes at most one 256-column tile */
 #define LORA_TILE_ROWS 128  /* rows per tile of the planner (the tensor-core tile height) */
+#define LORA_MAX_FEATURES (1 << 20)  /* d_in, d_out */
+#define LORA_MAX_TOKENS (1 << 24)    /* max_tokens: keeps every row and tile count in int range */
+#define LORA_MAX_SEGMENTS (1 << 20)  /* max_segments */
 
 /*
  * lora_linear_create -- make a handle for one projection shape on one device.
  *   out          receives the handle (set to NULL on failure).
- *   d_in, d_out  input / output features; each a positive multiple of 8 (16-byte rows).
+ *   d_in, d_out  input / output features; each a multiple of 8 (16-byte rows) in
+ *                [8, LORA_MAX_FEATURES].
  *   rank         adapter rank r, a multiple of 8 in [8, LORA_MAX_RANK].
- *   max_tokens   largest T a forward call will pass (>= 1).
- *   max_segments largest n_seg a forward call will pass (>= 1).
+ *   max_tokens   largest T a forward call will pass, in [1, LORA_MAX_TOKENS].
+ *   max_segments largest n_seg a forward call will pass, in [1, LORA_MAX_SEGMENTS].
  *   device       CUDA device ordinal; it must be an sm_103 GPU.
  * The handle owns its workspace: the shrink output U (bf16 [max_tokens + 128, rank]),
  * a ring of work-list buffers (device and pinned host), a device status word and CUDA

@@ -53,8 +53,10 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 
 int check_shape(int d_in, int d_out, int rank, int max_tokens, int max_segments) {
     if (d_in <= 0 || d_out <= 0 || (d_in % 8) || (d_out % 8)) return LORA_EINVAL;
+    if (d_in > LORA_MAX_FEATURES || d_out > LORA_MAX_FEATURES) return LORA_EINVAL;
     if (rank < 8 || rank > LORA_MAX_RANK || (rank % 8)) return LORA_EINVAL;
-    if (max_tokens < 1 || max_segments < 1) return LORA_EINVAL;
+    if (max_tokens < 1 || max_segments < 1 || max_tokens > LORA_MAX_TOKENS || max_segments > LORA_MAX_SEGMENTS)
+        return LORA_EINVAL;
     return LORA_OK;
 }
 

@@ -112,6 +112,8 @@ def test_validate_accepts_good_arguments(lib):
 @pytest.mark.parametrize("kw", [
     dict(d_in=250), dict(d_out=0), dict(rank=4), dict(rank=264), dict(rank=12),
     dict(max_tokens=0), dict(T=65), dict(T=-1),
+    dict(max_tokens=(1 << 24) + 1), dict(max_segments=(1 << 20) + 1), dict(max_tokens=2**31 - 1),
+    dict(d_in=(1 << 20) + 8), dict(d_out=(1 << 20) + 8),
     dict(seg_offsets=[0, 32, 63]), dict(seg_offsets=[1, 32, 64]), dict(seg_offsets=[0, 40, 32, 64], seg_ids=[0, 1, 0]),
     dict(seg_ids=[0, 2]), dict(seg_ids=[-1, 1]),
     dict(seg_offsets=[0, 8, 16, 32, 48, 64], seg_ids=[0, 1, 0, 1, 0]),   # n_seg > max_segments
