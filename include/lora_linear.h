@@ -117,7 +117,9 @@ int lora_linear_forward(lora_linear* h, const void* x, int T,
  *   back and waits for the stream before returning. The staging buffers are allocated on
  *   the first call and grow to max_tokens rows. Returns as lora_linear_forward, plus
  *   LORA_ENOMEM if staging cannot be allocated and LORA_ETIMEOUT if a kernel's bounded
- *   wait ran out.
+ *   wait ran out. Large T runs as row chunks whose copies overlap the kernels; on any error
+ *   the call still waits for the copies it has queued, so x_host and y_host are not touched
+ *   after it returns.
  * Source: as lora_linear_forward.
  */
 int lora_linear_forward_host(lora_linear* h, const void* x_host, int T,

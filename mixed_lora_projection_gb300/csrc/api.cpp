@@ -1128,6 +1128,17 @@ static int forward_host_impl(lora_linear* h, const void* x_host, int T, const in
     // (no cross-stream events on the path of a short call)
     const bool single = bounds.size() == 2;
     cudaStream_t s_in = single ? stream : h->s_in, s_out = single ? stream : h->s_out;
+    // an error after the first chunk was issued waits for the copies already queued, so that
+    // none of them touches the caller's host buffers after this call has returned
+    const auto fail = [&](int code) {
+        cudaStreamSynchronize(stream);
+        if (!single) {
+            cudaStreamSynchronize(s_in);
+            cudaStreamSynchronize(s_out);
+        }
+        cudaGetLastError();
+        return code;
+    };
     for (int c = 0; c + 1 < (int)bounds.size(); ++c) {
         const int a = bounds[c], b = bounds[c + 1];
         const int n = b - a;
@@ -1140,30 +1151,30 @@ static int forward_host_impl(lora_linear* h, const void* x_host, int T, const in
             off.push_back(hi - a);
             ids.push_back(seg_adapter_ids[i]);
         }
-        if (ids.empty() && n > 0) return LORA_EINVAL;
+        if (ids.empty() && n > 0) return fail(LORA_EINVAL);
         const int e = c % 16;
         // work list (on s_in, planned and uploaded by forward_impl), then X rows, both
         // ordered before the event the kernel waits on
         rc = forward_impl(h, xd + (size_t)a * xrow, n, off.data(), ids.data(), (int)ids.size(), W, A, B, scale,
                           n_adapters, yd + (size_t)a * yrow, stream, s_in, xh + (size_t)a * xrow, h->ev_in[e],
                           Wq, Ws);
-        if (rc != LORA_OK) return rc;
+        if (rc != LORA_OK) return fail(rc);
         if (n > 0) {
             if (!single && (cudaEventRecord(h->ev_done[e], stream) != cudaSuccess ||
                             cudaStreamWaitEvent(s_out, h->ev_done[e], 0) != cudaSuccess))
-                return LORA_ECUDA;
+                return fail(LORA_ECUDA);
             if (cudaMemcpyAsync(yh + (size_t)a * yrow, yd + (size_t)a * yrow, (size_t)n * yrow, cudaMemcpyDeviceToHost,
                                 s_out) != cudaSuccess)
-                return LORA_ECUDA;
+                return fail(LORA_ECUDA);
         }
     }
     // the status word travels back with the last rows of Y (on the copy-out stream, after the
     // last kernel), so the call ends with waits only and no further round trip
     if (!single && (cudaEventRecord(h->ev_done[15], stream) != cudaSuccess ||
                     cudaStreamWaitEvent(s_out, h->ev_done[15], 0) != cudaSuccess))
-        return LORA_ECUDA;
+        return fail(LORA_ECUDA);
     if (cudaMemcpyAsync(h->status_host, h->status, sizeof(int), cudaMemcpyDeviceToHost, s_out) != cudaSuccess)
-        return LORA_ECUDA;
+        return fail(LORA_ECUDA);
     if (cudaStreamSynchronize(stream) != cudaSuccess || (!single && cudaStreamSynchronize(s_out) != cudaSuccess))
         return LORA_ECUDA;
     return *h->status_host ? LORA_ETIMEOUT : LORA_OK;
