@@ -184,6 +184,33 @@ def test_w4_unit_orders_are_exact(dev, name):
     assert rel_err(ys[0][torch.as_tensor(rows, device=dev)], _oracle(inp, q, sc, off, ids, rows)) <= TOL
 
 
+@pytest.mark.parametrize("case", [("tiny2", [48, 200, 8], [0, 1, 0]), ("decode", [24, 24], [0, 0])])
+def test_w4_bounded_waits_report_timeout_and_the_handle_recovers(dev, case):
+    # the load warps never issue: every wait of the shrink launch and of the 4-bit kernel
+    # (transposed tile with two token tiles, or two feature tiles for a decode batch) runs out
+    # after 20 ms; the kernels return with the status word set, and the next call is correct
+    from mixed_lora_projection_gb300 import _lib as L
+    _, lens, ids = case
+    off = [0] + np.cumsum(lens).tolist()
+    w = Workload("w4stall", 17, off[-1], 512, 768, 32, tuple(off), tuple(ids), scales=(0.5,))
+    inp = make_inputs(w, dev)
+    q, sc = make_w4_base(w, dev)
+    kq = _kq(q)
+    with _ll(w) as ll:
+        ll.set_option(L.OPT_WAIT_LIMIT_US, 20000)
+        ll.set_option(L.OPT_DEBUG_STALL, 1)
+        ll.forward_w4(inp.x, off, ids, kq, sc, inp.a, inp.b, inp.scales)
+        torch.cuda.synchronize()
+        assert ll.status(reset=True) == L.LORA_ETIMEOUT
+        assert ll.status() == L.LORA_OK
+        ll.set_option(L.OPT_DEBUG_STALL, 0)
+        ll.set_option(L.OPT_WAIT_LIMIT_US, 4000000)
+        y = ll.forward_w4(inp.x, off, ids, kq, sc, inp.a, inp.b, inp.scales)
+        torch.cuda.synchronize()
+        assert ll.status() == L.LORA_OK
+    assert rel_err(y, _oracle(inp, q, sc, off, ids)) <= TOL
+
+
 def test_w4_rejects_d_in_not_multiple_of_128(dev):
     from mixed_lora_projection_gb300 import LoraError
     w = Workload("w4bad", 13, 16, 192, 256, 16, (0, 16), (0,))
