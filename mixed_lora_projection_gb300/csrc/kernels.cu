@@ -479,7 +479,7 @@ cudaError_t gemm_prepare_device() {
 }
 
 static void launch_config(const GemmParams& p, int grid, cudaStream_t stream, cudaLaunchConfig_t* cfg,
-                          cudaLaunchAttribute* attr) {
+                          cudaLaunchAttribute* attr /* [2] */) {
     const int b_rows = (p.tile_n > p.shrink_n ? p.tile_n : p.shrink_n) / p.cluster_size;
     *cfg = cudaLaunchConfig_t{};
     cfg->gridDim = dim3(grid, 1, 1);
@@ -492,6 +492,14 @@ static void launch_config(const GemmParams& p, int grid, cudaStream_t stream, cu
     attr[0].val.clusterDim.z = 1;
     cfg->attrs = attr;
     cfg->numAttrs = 1;
+    if (p.flags) {
+        // fused units wait for ready flags set by shrink units on other CTAs of the grid: a
+        // cooperative launch starts only when every CTA can be resident at once, so a CTA never
+        // waits on one that another kernel keeps from starting
+        attr[1].id = cudaLaunchAttributeCooperative;
+        attr[1].val.cooperative = 1;
+        cfg->numAttrs = 2;
+    }
 }
 
 template <typename F>
@@ -505,14 +513,14 @@ static cudaError_t dispatch(const GemmParams& p, F&& f) {
 
 cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t stream) {
     cudaLaunchConfig_t cfg;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     launch_config(p, grid, stream, &cfg, attr);
     return dispatch(p, [&](auto kernel) { return cudaLaunchKernelEx(&cfg, kernel, p); });
 }
 
 int gemm_max_clusters(const GemmParams& p) {
     cudaLaunchConfig_t cfg;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     launch_config(p, p.cluster_size, nullptr, &cfg, attr);
     int n = 0;
     cudaError_t e = dispatch(p, [&](auto kernel) { return cudaOccupancyMaxActiveClusters(&n, kernel, &cfg); });

@@ -145,3 +145,54 @@ def test_four_bit_base_graph_replays(dev):
             torch.cuda.synchronize()
             assert torch.equal(y, ref)
         assert ll.status() == 0
+
+
+def test_one_launch_calls_beside_a_busy_stream(dev):
+    # one-launch calls (fused units wait for other CTAs' shrink units) issued while another
+    # stream keeps the GPU busy with long matmuls: the launch starts only when its whole grid
+    # can be resident, so with a 20 ms wait limit every call still completes and matches
+    from mixed_lora_projection_gb300 import _lib as L
+    w = WORKLOADS["sweep_qkv_multi"]
+    inp = make_inputs(w, dev)
+    off, ids = list(w.seg_offsets), list(w.seg_ids)
+    a = torch.randn(8192, 8192, device=dev).to(torch.bfloat16)
+    with _ll(w) as ll:
+        ref = run(ll, inp, off, ids).clone()
+        torch.cuda.synchronize()
+        ll.set_option(L.OPT_WAIT_LIMIT_US, 20000)
+        busy = torch.cuda.Stream(dev)
+        busy.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(busy):
+            c = a
+            for _ in range(60):
+                c = (c @ a) * 1e-2                     # tens of ms of full-GPU work
+        ys = [run(ll, inp, off, ids).clone() for _ in range(6)]
+        torch.cuda.synchronize()
+        assert ll.status() == 0
+    for y in ys:
+        assert torch.equal(y, ref)
+
+
+def test_two_handles_on_two_streams(dev):
+    # two handles' one-launch calls interleaved on two streams (each grid waits only on itself)
+    from mixed_lora_projection_gb300 import _lib as L
+    w1, w2 = WORKLOADS["sweep_qkv_multi"], WORKLOADS["sweep_o_multi"]
+    in1, in2 = make_inputs(w1, dev), make_inputs(w2, dev)
+    o1, i1, o2, i2 = list(w1.seg_offsets), list(w1.seg_ids), list(w2.seg_offsets), list(w2.seg_ids)
+    with _ll(w1) as l1, _ll(w2) as l2:
+        r1, r2 = run(l1, in1, o1, i1).clone(), run(l2, in2, o2, i2).clone()
+        torch.cuda.synchronize()
+        for ll in (l1, l2):
+            ll.set_option(L.OPT_WAIT_LIMIT_US, 20000)
+        s1, s2 = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        s1.wait_stream(torch.cuda.current_stream(dev))
+        s2.wait_stream(torch.cuda.current_stream(dev))
+        y1, y2 = [], []
+        for _ in range(8):
+            with torch.cuda.stream(s1):
+                y1.append(run(l1, in1, o1, i1).clone())
+            with torch.cuda.stream(s2):
+                y2.append(run(l2, in2, o2, i2).clone())
+        torch.cuda.synchronize()
+        assert l1.status() == 0 and l2.status() == 0
+    assert all(torch.equal(y, r1) for y in y1) and all(torch.equal(y, r2) for y in y2)
