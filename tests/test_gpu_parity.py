@@ -417,6 +417,23 @@ def test_sweep_layer_sampled_rows(dev, proj):
     with _ll(w) as ll:
         y = run(ll, inp, off, ids)
     torch.cuda.synchronize()
-    rows = sample_rows(w.T, off, ids, n_random=128, seed=3)
+    rows = sample_rows(w.T, off, ids, n_random=1024, seed=3)
     ref = oracle_rows(inp, off, ids, rows)
     assert rel_err(y[torch.as_tensor(rows, device=dev)], ref) <= TOL
+
+
+@pytest.mark.parametrize("proj", ["qkv", "o", "gate_up", "down"])
+def test_sweep_every_layer_sampled_rows(dev, proj):
+    # each of the 24 layers on its own seeded X, W, A and B (layers are not chained): rows
+    # [0, 64), every segment boundary +-2, every tile boundary +-1 and 256 seeded random rows
+    w = WORKLOADS[f"sweep_{proj}"]
+    off, ids = list(w.seg_offsets), list(w.seg_ids)
+    with _ll(w) as ll:
+        for layer in range(24):
+            inp = make_inputs(w, dev, layer=layer)
+            y = run(ll, inp, off, ids)
+            torch.cuda.synchronize()
+            assert ll.status() == 0
+            rows = sample_rows(w.T, off, ids, n_random=256, seed=100 + layer)
+            ref = oracle_rows(inp, off, ids, rows)
+            assert rel_err(y[torch.as_tensor(rows, device=dev)], ref) <= TOL, layer
