@@ -35,6 +35,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "LoRA-linear TFLOP/s & tokens/s at 1 GB300; % of bf16 tensor peak / HBM BW"
 SWEEP = "sweep_24_layers"
+SWEEP_MULTI = "sweep_24_layers_multi"   # the same stack with three adapters (ids 1, 2, 3)
 
 
 def _peaks():
@@ -142,8 +143,8 @@ class ClockSampler:
 
 def _workloads(name):
     from mixed_lora_projection_gb300.synth import SWEEP_LAYERS, SWEEP_PROJECTIONS, WORKLOADS, sweep_workload
-    if name == SWEEP:
-        return [(sweep_workload(p), layer, i) for layer in range(SWEEP_LAYERS)
+    if name in (SWEEP, SWEEP_MULTI):
+        return [(sweep_workload(p, name == SWEEP_MULTI), layer, i) for layer in range(SWEEP_LAYERS)
                 for i, (p, _, _) in enumerate(SWEEP_PROJECTIONS)]
     return [(WORKLOADS[name], 0, 0)]
 
@@ -186,7 +187,7 @@ def run_ours(args, rank, world, dist):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     items = _workloads(args.workload)
-    n_copies = 1 if args.workload == SWEEP else 3
+    n_copies = 1 if args.workload in (SWEEP, SWEEP_MULTI) else 3
     setups = []
     handles = {}
     for (w, layer, pi) in items:

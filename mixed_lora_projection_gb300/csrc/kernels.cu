@@ -478,6 +478,18 @@ cudaError_t gemm_prepare_device() {
     return set_smem_attr<32, 2>();
 }
 
+// Cooperative launches can be switched off for a profiler (LORA_LINEAR_NONCOOPERATIVE=1 in the
+// environment): Nsight Compute rejects the cooperative grid that fits without its
+// instrumentation ("LaunchFailed"), and it runs one kernel at a time, so the grid is
+// co-resident anyway.
+static bool cooperative_launches() {
+    static const bool on = [] {
+        const char* v = getenv("LORA_LINEAR_NONCOOPERATIVE");
+        return !(v && v[0] == '1');
+    }();
+    return on;
+}
+
 static void launch_config(const GemmParams& p, int grid, cudaStream_t stream, cudaLaunchConfig_t* cfg,
                           cudaLaunchAttribute* attr /* [2] */) {
     const int b_rows = (p.tile_n > p.shrink_n ? p.tile_n : p.shrink_n) / p.cluster_size;
@@ -492,7 +504,7 @@ static void launch_config(const GemmParams& p, int grid, cudaStream_t stream, cu
     attr[0].val.clusterDim.z = 1;
     cfg->attrs = attr;
     cfg->numAttrs = 1;
-    if (p.flags) {
+    if (p.flags && cooperative_launches()) {
         // fused units wait for ready flags set by shrink units on other CTAs of the grid: a
         // cooperative launch starts only when every CTA can be resident at once, so a CTA never
         // waits on one that another kernel keeps from starting
