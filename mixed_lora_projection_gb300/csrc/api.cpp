@@ -1058,20 +1058,24 @@ static std::vector<int> host_chunk_bounds(int T) {
         b.push_back(T);
         return b;
     }
-    const auto r128 = [](int v) { return std::max(kTileM, v / kTileM * kTileM); };
-    const int big = r128(std::max(1024, T / 8)), small = r128(std::max(256, T / 32));
-    std::vector<int> ramp;                       // small, 2 small, ... below big
-    for (int v = small; v < big && 2 * (int)ramp.size() < 8; v *= 2) ramp.push_back(r128(v));
-    int ramp_rows = 0;
-    for (int v : ramp) ramp_rows += 2 * v;
-    if (ramp_rows >= T) ramp.clear(), ramp_rows = 0;
-    for (int v : ramp) b.push_back(b.back() + v);
-    const int mid = T - ramp_rows, n_mid = std::max(1, ceil_div(mid, big));
-    for (int i = 1; i <= n_mid; ++i) {
-        const int end = b[0] + (ramp_rows / 2) + (int)((long long)mid * i / n_mid);
-        b.push_back(i == n_mid ? end : std::max(b.back() + 1, end / kTileM * kTileM));
+    // chunk sizes in whole 128-row tiles: a ramp of small chunks (small, 2 small, ... up to half
+    // the middle chunks' size, at most four), the middle split evenly, the ramp mirrored; only
+    // the last chunk takes the rows past the last whole tile
+    const int tiles = T / kTileM;
+    const int big = std::max(8, tiles / 8), small = std::max(2, tiles / 32);
+    std::vector<int> ramp;
+    for (int v = small; v <= big / 2 && (int)ramp.size() < 4; v *= 2) ramp.push_back(v);
+    int ramp_tiles = 0;
+    for (int v : ramp) ramp_tiles += 2 * v;
+    if (ramp_tiles >= tiles) {
+        ramp.clear();
+        ramp_tiles = 0;
     }
-    for (int i = (int)ramp.size() - 1; i >= 0; --i) b.push_back(b.back() + ramp[i]);
+    const int mid = tiles - ramp_tiles, n_mid = std::max(1, ceil_div(mid, big));
+    std::vector<int> sizes(ramp);
+    for (int i = 0; i < n_mid; ++i) sizes.push_back(mid / n_mid + (i < mid % n_mid ? 1 : 0));
+    for (int i = (int)ramp.size() - 1; i >= 0; --i) sizes.push_back(ramp[i]);
+    for (int v : sizes) b.push_back(b.back() + v * kTileM);
     b.back() = T;
     return b;
 }
@@ -1200,6 +1204,51 @@ int lora_linear_forward_host_w4(lora_linear* h, const void* x_host, int T, const
     if (T > 0 && (!Wq || !Ws || !aligned16(Wq) || !aligned16(Ws))) return LORA_EINVAL;
     return forward_host_impl(h, x_host, T, seg_offsets, seg_adapter_ids, n_seg, nullptr, Wq, Ws, A, B, scale,
                              n_adapters, y_host, stream);
+}
+
+}  // extern "C"
+
+extern "C" {
+
+int lora_linear_shape(int d_in, int d_out, int rank, int num_sms, int T, const int32_t* seg_offsets,
+                      const int32_t* seg_adapter_ids, int n_seg, int* cluster, int* tile_n, int* bk,
+                      int* stages, int* unit_order, int* fused_units, int* shrink_units) {
+    int* outs[] = {cluster, tile_n, bk, stages, unit_order, fused_units, shrink_units};
+    for (int* o : outs)
+        if (o) *o = 0;
+    if (num_sms < 2 || T < 0) return LORA_EINVAL;
+    int rc = check_shape(d_in, d_out, rank, std::max(T, 1), std::max(n_seg, 1));
+    if (rc != LORA_OK) return rc;
+    Plan plan;
+    rc = plan_segments(seg_offsets, seg_adapter_ids, n_seg, T, -1, &plan);
+    if (rc != LORA_OK || plan.fused.empty()) return rc;
+    // a handle on the host alone: the shape model reads only its sizes and options
+    lora_linear h;
+    h.d_in = d_in;
+    h.d_out = d_out;
+    h.rank = rank;
+    h.max_tokens = std::max(T, 1);
+    h.num_sms = num_sms;
+    h.u_rows = ceil_div(h.max_tokens, kTileM) * kTileM + kTileM;
+    for (size_t i = 0; i < plan.fused.size(); ++i) plan.fused[i].fused_index = (int32_t)i;
+    const Shape sh = choose_shape(&h, plan);
+    if (cluster) *cluster = sh.cs;
+    if (tile_n) *tile_n = sh.tile_n;
+    if (bk) *bk = sh.bk;
+    if (stages) *stages = sh.stages;
+    if (unit_order) *unit_order = sh.m_fastest;   // 0, 1, 2 as documented
+    if (fused_units) *fused_units = (int)(sh.fused_groups.size() / sh.cs) * sh.n_ntiles;
+    if (shrink_units) *shrink_units = (int)(sh.shrink_groups.size() / sh.cs);
+    return LORA_OK;
+}
+
+int lora_linear_host_chunks(int T, int32_t* bounds, int* n) {
+    if (T < 0 || !bounds || !n) return LORA_EINVAL;
+    const std::vector<int> b = host_chunk_bounds(T);
+    if ((int)b.size() - 1 > LORA_MAX_HOST_CHUNKS) return LORA_EINVAL;   // never: the schedule's bound
+    for (size_t i = 0; i < b.size(); ++i) bounds[i] = b[i];
+    *n = (int)b.size() - 1;
+    return LORA_OK;
 }
 
 }  // extern "C"

@@ -75,6 +75,28 @@ def validate(d_in, d_out, rank, max_tokens, max_segments, x_ptr, T, seg_offsets,
                                     S if scales is not None else None, na, y_ptr)
 
 
+def launch_shape(d_in, d_out, rank, num_sms, T, seg_offsets, seg_ids) -> dict:
+    """The launch shape ``forward`` would choose for these rows on a GPU with ``num_sms`` SMs,
+    computed by the library on the host alone (no device needed)."""
+    lib = L.load()
+    off, _ = _i32(seg_offsets)
+    ids, n = _i32(seg_ids)
+    v = [C.c_int() for _ in range(7)]
+    _check(lib.lora_linear_shape(d_in, d_out, rank, num_sms, T, off, ids, n, *[C.byref(x) for x in v]),
+           "lora_linear_shape")
+    return dict(zip(("cluster", "tile_n", "bk", "stages", "unit_order", "fused_units", "shrink_units"),
+                    [x.value for x in v]))
+
+
+def host_chunks(T) -> list:
+    """Row bounds of the chunks ``forward_host`` runs T rows in (0 first, T last)."""
+    lib = L.load()
+    bounds = (C.c_int32 * 17)()
+    n = C.c_int()
+    _check(lib.lora_linear_host_chunks(T, bounds, C.byref(n)), "lora_linear_host_chunks")
+    return [bounds[i] for i in range(n.value + 1)]
+
+
 def w4_repack(src: torch.Tensor, dst: torch.Tensor | None = None,
               stream: torch.cuda.Stream | None = None) -> torch.Tensor:
     """4-bit base weight, plain layout (uint8 [d_out, d_in/2], low nibble = even input,

@@ -137,3 +137,68 @@ def test_create_without_a_gpu_reports_no_device(lib):
     assert lib.lora_linear_create(ctypes.byref(h), 256, 512, 16, 64, 4, 0) == -6
     assert not h.value
     assert lib.lora_linear_destroy(None) == 0
+
+
+# --------------------------------------------------------------------------- host logic
+
+# the launch-shape model's choices for the configured workloads on a 152-SM GB300 (SM pairs
+# with 256 columns for the prefills and mixed batches, grouped column tiles for the prefills,
+# single CTAs with 240 columns for the decode and near-ridge batches, the sweep's widths)
+SHAPES = {
+    "prefill_16k": (2, 256, 2), "prefill_32k": (2, 256, 2), "mixed_batch": (2, 256, 1),
+    "mixed_8x300": (2, 256, 1), "prefix_tail_1552": (2, 256, 1), "mixed_decode": (1, 240, None),
+    "mixed_near_ridge": (1, 240, None), "sweep_qkv": (2, 224, None), "sweep_o": (2, 192, None),
+    "sweep_gate_up": (2, 256, None), "sweep_down": (2, 192, None),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SHAPES))
+def test_launch_shape_model_choices(lib, name):
+    from mixed_lora_projection_gb300 import launch_shape
+    from mixed_lora_projection_gb300.synth import WORKLOADS
+    w = WORKLOADS[name]
+    s = launch_shape(w.d_in, w.d_out, w.rank, 152, w.T, w.seg_offsets, w.seg_ids)
+    cluster, tile_n, order = SHAPES[name]
+    assert (s["cluster"], s["tile_n"]) == (cluster, tile_n), s
+    if order is not None:
+        assert s["unit_order"] == order, s
+    # work units: every fused group crosses every column tile once; one shrink unit per group of
+    # adapter tiles
+    n_tiles = -(-w.T // 128)
+    groups = -(-n_tiles // cluster)
+    assert s["fused_units"] >= groups * -(-w.d_out // tile_n) - 1
+    assert (s["shrink_units"] == 0) == (w.adapter_rows == 0)
+    assert s["bk"] == 64 and 2 <= s["stages"] <= 16
+
+
+def test_launch_shape_of_an_empty_batch_and_bad_arguments(lib):
+    from mixed_lora_projection_gb300 import LoraError, launch_shape
+    assert launch_shape(256, 512, 16, 152, 0, [0], [])["fused_units"] == 0
+    with pytest.raises(LoraError):
+        launch_shape(256, 512, 16, 1, 64, [0, 64], [0])           # fewer than 2 SMs
+    with pytest.raises(LoraError):
+        launch_shape(250, 512, 16, 152, 64, [0, 64], [0])         # d_in not a multiple of 8
+    with pytest.raises(LoraError):
+        launch_shape(256, 512, 16, 152, 64, [0, 60], [0])         # segments do not span T
+
+
+@pytest.mark.parametrize("T", [0, 1, 127, 2047, 2048, 2049, 4144, 9999, 16384, 32768, 100000, 1 << 24])
+def test_host_chunk_schedule(lib, T):
+    # the host-buffer path's row chunks: cover [0, T] in order, at most 16 (its event ring),
+    # interior bounds on 128-row tiles, one chunk below 2,048 rows, and no chunk at either end
+    # larger than the chunks in the middle (the copy-in before the first kernel and the
+    # copy-out after the last one overlap nothing)
+    from mixed_lora_projection_gb300 import host_chunks
+    b = host_chunks(T)
+    assert b[0] == 0 and b[-1] == T
+    n = len(b) - 1
+    assert 1 <= n <= 16
+    if T < 2048:
+        assert n == 1
+        return
+    sizes = [b[i + 1] - b[i] for i in range(n)]
+    assert all(x > 0 for x in sizes)
+    assert all(v % 128 == 0 for v in b[1:-1])
+    mid = max(sizes)
+    assert sizes[0] <= mid and sizes[-1] <= mid
+    assert sizes[0] < mid and sizes[-1] <= mid   # a ramp at the start

@@ -111,3 +111,19 @@ def test_rows_do_not_depend_on_the_batch_they_are_in(dev):
         assert ll.status() == 0
     assert shape_full["tile_n"] != shape_alone["tile_n"] or shape_full["grid"] != shape_alone["grid"]
     assert torch.equal(full[:48], alone)
+
+
+@pytest.mark.parametrize("name", ["prefill_16k", "mixed_batch", "mixed_decode", "mixed_near_ridge",
+                                  "sweep_o", "sweep_down"])
+def test_host_shape_model_equals_the_device_handle(dev, name):
+    # the host-only launch_shape (given the device's SM count) and a device handle's describe
+    # name the same shape
+    from mixed_lora_projection_gb300 import LoraLinear, launch_shape
+    from mixed_lora_projection_gb300.synth import WORKLOADS
+    w = WORKLOADS[name]
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    host = launch_shape(w.d_in, w.d_out, w.rank, sms, w.T, w.seg_offsets, w.seg_ids)
+    with LoraLinear(w.d_in, w.d_out, w.rank, w.T, 16, 0) as ll:
+        d = ll.describe(w.T, w.seg_offsets, w.seg_ids)
+    assert d["tile_n"] == host["tile_n"] and d["stages"] == host["stages"]
+    assert d["n_units"] == host["fused_units"] + host["shrink_units"]
