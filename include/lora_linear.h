@@ -256,17 +256,18 @@ int lora_linear_describe(lora_linear* h, int T, const int32_t* seg_offsets,
                          int* n_units, int* grid, int* stages, int* has_shrink);
 
 /*
- * lora_linear_shape -- the launch shape lora_linear_forward would choose, computed on the host
- * alone (no device, no handle): for d_in, d_out, rank as in lora_linear_create, a GPU with
- * num_sms SMs (>= 2), the default options, and T rows in these segments (checked as by
- * lora_linear_plan). Outputs (any may be NULL): cluster (2 = SM pairs, 1 = single CTAs),
- * tile_n (output columns per fused unit), bk (K per pipeline stage), stages, unit_order
- * (0 = column tiles first, 1 = row tiles first, 2 = groups of column tiles), fused_units and
- * shrink_units (work units of the launch). T = 0 gives zeros. Returns LORA_OK or LORA_EINVAL.
- * Diagnostics and tests.
+ * lora_linear_shape -- the launch shape lora_linear_forward (w4 = 0) or
+ * lora_linear_forward_w4 (w4 = 1) would choose, computed on the host alone (no device, no
+ * handle): for d_in, d_out, rank as in lora_linear_create, a GPU with num_sms SMs (>= 2), the
+ * default options, and T rows in these segments (checked as by lora_linear_plan). Outputs
+ * (any may be NULL): cluster (2 = SM pairs, 1 = single CTAs), tile_n (output columns per
+ * fused unit), bk (K per pipeline stage), stages, unit_order (0 = column (feature) tiles
+ * first, 1 = row tiles (token groups) first, 2 = groups of column tiles), fused_units (work
+ * units of the fused launch, or of the 4-bit kernel) and shrink_units (shrink work units).
+ * T = 0 gives zeros. Returns LORA_OK or LORA_EINVAL. Diagnostics and tests.
  */
 int lora_linear_shape(int d_in, int d_out, int rank, int num_sms, int T, const int32_t* seg_offsets,
-                      const int32_t* seg_adapter_ids, int n_seg, int* cluster, int* tile_n, int* bk,
+                      const int32_t* seg_adapter_ids, int n_seg, int w4, int* cluster, int* tile_n, int* bk,
                       int* stages, int* unit_order, int* fused_units, int* shrink_units);
 
 /*

@@ -37,7 +37,7 @@ SIGNATURES = {
                                      C.POINTER(C.c_longlong)]),
     "lora_linear_describe": (C.c_int, [P, C.c_int, I32P, I32P, C.c_int, IP, IP, IP, IP, IP, IP]),
     "lora_linear_error_string": (C.c_char_p, [C.c_int]),
-    "lora_linear_shape": (C.c_int, [C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, I32P, I32P, C.c_int,
+    "lora_linear_shape": (C.c_int, [C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, I32P, I32P, C.c_int, C.c_int,
                                     IP, IP, IP, IP, IP, IP, IP]),
     "lora_linear_host_chunks": (C.c_int, [C.c_int, I32P, IP]),
     "lora_linear_forward_noalloc": (C.c_int, [P, C.c_int, I32P, I32P, C.c_int, C.c_int, C.c_int, C.c_int, P,

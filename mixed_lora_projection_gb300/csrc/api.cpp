@@ -398,6 +398,35 @@ Shape choose_shape(lora_linear* h, const Plan& plan) {
     return sh;
 }
 
+// Launch shape of the 4-bit kernel for a call's token groups (host logic only).
+struct W4Shape {
+    int feature_tiles = 1, n_ntiles = 0, tokens_fastest = 0, x_stage_bytes = 0, stages = 4, pstages = 2;
+};
+
+W4Shape w4_shape(const lora_linear* h, const std::vector<W4Group>& groups, int T) {
+    W4Shape w;
+    const int n = (int)groups.size();
+    // a batch of one token tile of at most 128 rows and no adapter rows (a decode step) runs
+    // two feature tiles per unit
+    w.feature_tiles =
+        (n == 1 && groups[0].nrows[1] == 0 && groups[0].nrows[0] <= kTileM && groups[0].adapter[0] == 0) ? 2 : 1;
+    w.n_ntiles = ceil_div(h->d_out, kW4TileM * w.feature_tiles);
+    // unit order: token groups fastest when the packed base is too large to stay in L2 beside
+    // the output stream while the batch's X fits there (the mixed batch on gate_up: 89 MB
+    // packed, 42 MB of X), else feature tiles fastest; LORA_OPT_RASTER 1 / 2 force it
+    const double packed_bytes = (double)h->d_out * h->d_in / 2, x_bytes = (double)T * h->d_in * 2;
+    w.tokens_fastest = h->raster == 1   ? 1
+                       : h->raster == 2 ? 0
+                                        : (n > 1 && packed_bytes > 32e6 && x_bytes <= 64e6) ? 1 : 0;
+    // X stages: two token tiles (and the expand's U + B_a boxes), or one tile when FT = 2; the
+    // packed ring takes the rest of shared memory
+    w.x_stage_bytes = w.feature_tiles == 2 ? kTileM * 128 : 2 * kTileM * 128;
+    while (w.pstages < 8 &&
+           w4_smem_bytes(w.stages, w.pstages + 1, w.x_stage_bytes, w.feature_tiles) <= (size_t)kSmemLimit)
+        ++w.pstages;
+    return w;
+}
+
 Slot* acquire_slot(lora_linear* h) {
     Slot* s = &h->slots[h->next_slot];
     h->next_slot = (h->next_slot + 1) % kRing;
@@ -741,6 +770,7 @@ int forward_impl(lora_linear* h, const void* x, int T, const int32_t* seg_offset
     }
     const std::vector<W4Group> w4_groups = w4 ? make_w4_groups(plan.fused) : std::vector<W4Group>();
     const int n_w4g = (int)w4_groups.size();
+    const W4Shape w4s = w4 ? w4_shape(h, w4_groups, T) : W4Shape();
     const bool w4_inline = n_used <= kInlineAdapters && n_w4g <= kW4InlineGroups;
     const int cs = sh.cs, tile_n = sh.tile_n, shrink_n = sh.shrink_n, bk = sh.bk;
     const int nfg = (int)sh.fused_groups.size() / cs, nsg = (int)sh.shrink_groups.size() / cs;
@@ -857,10 +887,7 @@ int forward_impl(lora_linear* h, const void* x, int T, const int32_t* seg_offset
     if (encode_2d(h, &p.tm_x, x, h->d_in, T, bk, (uint32_t)sh.a_rows) != CUDA_SUCCESS) return LORA_ECUDA;
     if (w4) {
         q.tm_x = p.tm_x;
-        // a batch of one token tile of at most 128 rows and no adapter rows (a decode step) runs
-        // two feature tiles per unit
-        q.feature_tiles = (n_w4g == 1 && w4_groups[0].nrows[1] == 0 && w4_groups[0].nrows[0] <= kTileM &&
-                           w4_groups[0].adapter[0] == 0) ? 2 : 1;
+        q.feature_tiles = w4s.feature_tiles;
         const uint32_t q_box = (uint32_t)(kW4TileM * q.feature_tiles);
         if (encode_u8_sw128(h, &q.tm_wq, Wq, (uint64_t)h->d_in / 2, h->d_out, q_box) != CUDA_SUCCESS ||
             encode_plain_2d(h, &q.tm_ws, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Ws, h->d_out,
@@ -937,26 +964,15 @@ int forward_impl(lora_linear* h, const void* x, int T, const int32_t* seg_offset
         q.status = h->status;
         q.wait_limit_ns = h->wait_limit_ns;
         q.n_groups = n_w4g;
-        q.n_ntiles = ceil_div(h->d_out, kW4TileM * q.feature_tiles);
-        // unit order: token groups fastest when the packed base is too large to stay in L2
-        // beside the output stream while the batch's X fits there (the mixed batch on gate_up:
-        // 89 MB packed, 42 MB of X), else feature tiles fastest; LORA_OPT_RASTER 1 / 2 force it
-        const double packed_bytes = (double)h->d_out * h->d_in / 2, x_bytes = (double)T * h->d_in * 2;
-        q.tokens_fastest = h->raster == 1 ? 1
-                           : h->raster == 2 ? 0
-                           : (n_w4g > 1 && packed_bytes > 32e6 && x_bytes <= 64e6) ? 1 : 0;
+        q.n_ntiles = w4s.n_ntiles;
+        q.tokens_fastest = w4s.tokens_fastest;
         q.k_main_blocks = ceil_div(h->d_in, 64);
         q.k_lora_blocks = ceil_div(h->rank, 64);
         q.k_pack_blocks = ceil_div(q.k_main_blocks, 4);
         q.d_out = h->d_out;
-        // X stages: two token tiles (and the expand's U + B_a boxes), or one tile when FT = 2;
-        // the packed ring takes the rest of shared memory
-        q.x_stage_bytes = q.feature_tiles == 2 ? kTileM * 128 : 2 * kTileM * 128;
-        q.stages = 4;
-        q.pstages = 2;
-        while (q.pstages < 8 && w4_smem_bytes(q.stages, q.pstages + 1, q.x_stage_bytes, q.feature_tiles) <=
-                                    (size_t)kSmemLimit)
-            ++q.pstages;
+        q.x_stage_bytes = w4s.x_stage_bytes;
+        q.stages = w4s.stages;
+        q.pstages = w4s.pstages;
         // whole 32-row chunks of Y leave through TMA stores (Y 16-byte aligned, d_out % 8 == 0:
         // both checked before any launch)
         if (encode_plain_2d(h, &q.tm_y, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, y, h->d_out, T, kW4TileM, 32) !=
@@ -1211,12 +1227,12 @@ int lora_linear_forward_host_w4(lora_linear* h, const void* x_host, int T, const
 extern "C" {
 
 int lora_linear_shape(int d_in, int d_out, int rank, int num_sms, int T, const int32_t* seg_offsets,
-                      const int32_t* seg_adapter_ids, int n_seg, int* cluster, int* tile_n, int* bk,
+                      const int32_t* seg_adapter_ids, int n_seg, int w4, int* cluster, int* tile_n, int* bk,
                       int* stages, int* unit_order, int* fused_units, int* shrink_units) {
     int* outs[] = {cluster, tile_n, bk, stages, unit_order, fused_units, shrink_units};
     for (int* o : outs)
         if (o) *o = 0;
-    if (num_sms < 2 || T < 0) return LORA_EINVAL;
+    if (num_sms < 2 || T < 0 || (w4 && d_in % kW4Group)) return LORA_EINVAL;
     int rc = check_shape(d_in, d_out, rank, std::max(T, 1), std::max(n_seg, 1));
     if (rc != LORA_OK) return rc;
     Plan plan;
@@ -1232,6 +1248,19 @@ int lora_linear_shape(int d_in, int d_out, int rank, int num_sms, int T, const i
     h.u_rows = ceil_div(h.max_tokens, kTileM) * kTileM + kTileM;
     for (size_t i = 0; i < plan.fused.size(); ++i) plan.fused[i].fused_index = (int32_t)i;
     const Shape sh = choose_shape(&h, plan);
+    if (w4) {
+        // the 4-bit kernel over token groups; the shrink runs as the bf16 kernel's shrink units
+        const std::vector<W4Group> groups = make_w4_groups(plan.fused);
+        const W4Shape ws = w4_shape(&h, groups, T);
+        if (cluster) *cluster = 1;
+        if (tile_n) *tile_n = kW4TileM * ws.feature_tiles;
+        if (bk) *bk = 64;
+        if (stages) *stages = ws.stages;
+        if (unit_order) *unit_order = ws.tokens_fastest;
+        if (fused_units) *fused_units = (int)groups.size() * ws.n_ntiles;
+        if (shrink_units) *shrink_units = (int)(sh.shrink_groups.size() / sh.cs);
+        return LORA_OK;
+    }
     if (cluster) *cluster = sh.cs;
     if (tile_n) *tile_n = sh.tile_n;
     if (bk) *bk = sh.bk;

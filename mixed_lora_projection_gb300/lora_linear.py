@@ -75,14 +75,15 @@ def validate(d_in, d_out, rank, max_tokens, max_segments, x_ptr, T, seg_offsets,
                                     S if scales is not None else None, na, y_ptr)
 
 
-def launch_shape(d_in, d_out, rank, num_sms, T, seg_offsets, seg_ids) -> dict:
-    """The launch shape ``forward`` would choose for these rows on a GPU with ``num_sms`` SMs,
-    computed by the library on the host alone (no device needed)."""
+def launch_shape(d_in, d_out, rank, num_sms, T, seg_offsets, seg_ids, w4=False) -> dict:
+    """The launch shape ``forward`` (or ``forward_w4``) would choose for these rows on a GPU with
+    ``num_sms`` SMs, computed by the library on the host alone (no device needed)."""
     lib = L.load()
     off, _ = _i32(seg_offsets)
     ids, n = _i32(seg_ids)
     v = [C.c_int() for _ in range(7)]
-    _check(lib.lora_linear_shape(d_in, d_out, rank, num_sms, T, off, ids, n, *[C.byref(x) for x in v]),
+    _check(lib.lora_linear_shape(d_in, d_out, rank, num_sms, T, off, ids, n, int(bool(w4)),
+                                 *[C.byref(x) for x in v]),
            "lora_linear_shape")
     return dict(zip(("cluster", "tile_n", "bk", "stages", "unit_order", "fused_units", "shrink_units"),
                     [x.value for x in v]))

@@ -202,3 +202,31 @@ def test_host_chunk_schedule(lib, T):
     mid = max(sizes)
     assert sizes[0] <= mid and sizes[-1] <= mid
     assert sizes[0] < mid and sizes[-1] <= mid   # a ramp at the start
+
+
+# the 4-bit kernel's shape: two feature tiles per unit for a decode batch (one token tile, no
+# adapter rows); token groups fastest where the packed base exceeds 32 MB and X fits in 64 MB
+W4_SHAPES = {
+    # name: (output columns per unit, unit order, token groups)
+    "prefill_16k": (128, 0, 64), "mixed_batch": (128, 1, 17), "mixed_8x300": (128, 1, 10),
+    "prefix_tail_1552": (128, 1, 7), "mixed_near_ridge": (128, 1, 2), "mixed_decode": (256, 0, 1),
+    "prefill_32k": (128, 0, 128),
+}
+
+
+@pytest.mark.parametrize("name", sorted(W4_SHAPES))
+def test_w4_launch_shape_choices(lib, name):
+    from mixed_lora_projection_gb300 import launch_shape
+    from mixed_lora_projection_gb300.synth import WORKLOADS
+    w = WORKLOADS[name]
+    s = launch_shape(w.d_in, w.d_out, w.rank, 152, w.T, w.seg_offsets, w.seg_ids, w4=True)
+    cols, order, groups = W4_SHAPES[name]
+    assert (s["cluster"], s["tile_n"], s["unit_order"]) == (1, cols, order), s
+    assert s["fused_units"] == groups * -(-w.d_out // cols)
+    assert (s["shrink_units"] == 0) == (w.adapter_rows == 0)
+
+
+def test_w4_launch_shape_rejects_d_in_not_multiple_of_128(lib):
+    from mixed_lora_projection_gb300 import LoraError, launch_shape
+    with pytest.raises(LoraError):
+        launch_shape(192, 256, 16, 152, 16, [0, 16], [0], w4=True)
