@@ -15,7 +15,8 @@
 // its expand k-blocks, for a ready flag that the tile's shrink unit publishes (release /
 // acquire at GPU scope, plus async-proxy fences because U is written with plain stores and
 // read by TMA). A CTA only ever waits for units earlier in the order, which every other
-// CTA reaches without waiting, so the dependency cannot cycle. The last CTA to finish
+// CTA reaches without waiting, so the dependency cannot cycle, given that the grid's CTAs
+// are resident together (such launches are cooperative launches). The last CTA to finish
 // clears the flags, so a launch depends on no value left by an earlier one (CUDA graphs
 // replay it unchanged).
 //

@@ -14,13 +14,15 @@
 // from shared memory into the same accumulator; U comes from the shrink pass, launched
 // before this kernel on the same stream.
 //
-// Per CTA (one per SM, persistent over the units, feature tile fastest):
+// Per CTA (one per SM, persistent over the units, in the order W4Params::tokens_fastest
+// selects: feature tiles or token groups fastest):
 //   warp 0      TMA: X tiles (base K-steps), U and B_a tiles (expand K-steps);
 //   warp 1      TMEM owner (512 columns: one 128 x 256 fp32 accumulator and one 32-column
-//               stage of dequantised A per ring stage), issues the MMAs: one wait, four MMAs
-//               and one commit per K-step, as in the bf16 kernel;
-//   warps 2..5  epilogue: warp w reads lanes 32 (w % 4) .. (one output feature per thread)
-//               and writes Y[t, n] for the unit's tokens (32 lanes = 64 contiguous bytes);
+//               stage of dequantised A per ring stage), issues the MMAs: one wait per two
+//               ring stages, four MMAs per feature tile and one commit per K-step;
+//   warps 2..5  epilogue: warp w reads lanes 32 (w % 4) .. (one output feature per thread),
+//               stages each whole 32-token chunk of Y in shared memory ([token][feature])
+//               and writes it with one TMA store (a tile's ragged last chunk from registers);
 //   warps 6..13 converters: warp w dequantises whole K-steps (6..9 the even ring stages,
 //               10..13 the odd ones) for the 32 features of lane quadrant w % 4, packed
 //               ring -> TMEM, and counts itself in on the stage's full barrier;
