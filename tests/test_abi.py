@@ -65,6 +65,27 @@ def test_planner_equals_plan_ref_exhaustive(lib, nseg):
             assert _lib_plan(off, ids, T) == plan_ref(off, list(ids), T)
 
 
+def test_planner_equals_plan_ref_four_segments(lib):
+    # four segments over the tile-boundary lengths, every id pattern over 0..2
+    lens4 = (0, 1, 127, 128, 129, 300)
+    for lens in itertools.product(lens4, repeat=4):
+        off = [0] + np.cumsum(lens).tolist()
+        for ids in itertools.product((0, 1, 2), repeat=4):
+            assert _lib_plan(off, ids, off[-1]) == plan_ref(off, list(ids), off[-1])
+
+
+def test_planner_equals_plan_ref_every_length(lib):
+    # one segment of every length 0..300 and two segments on a 7-row grid of lengths, ids 0..2
+    for n in range(301):
+        for a in (0, 1, 2):
+            assert _lib_plan([0, n], [a], n) == plan_ref([0, n], [a], n)
+    for l0 in range(0, 301, 7):
+        for l1 in range(0, 301, 7):
+            off = [0, l0, l0 + l1]
+            for ids in itertools.product((0, 1, 2), repeat=2):
+                assert _lib_plan(off, ids, off[-1]) == plan_ref(off, list(ids), off[-1])
+
+
 @pytest.mark.parametrize("seed", range(30))
 def test_planner_equals_plan_ref_random(lib, seed):
     rng = np.random.default_rng(1000 + seed)
