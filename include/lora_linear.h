@@ -17,7 +17,9 @@
  * Arithmetic: bf16 operands, fp32 accumulation on the tensor cores. The shrink output
  * U = s_a X A_a^T is rounded to bf16 (round to nearest even) before the expand; Y is
  * rounded from fp32 to bf16 (round to nearest even). The summation order is not
- * specified, so results are not bitwise equal to any other implementation.
+ * specified, so results are not bitwise equal to any other implementation; within this
+ * library a row's output does not depend on the other rows of its batch (the same bits in
+ * any batch, launch shape or host-buffer chunking).
  *
  * Errors: every function returns LORA_OK (0) or a negative code below. Argument checks
  * run on the host before any launch; a failed check launches nothing and leaves every
@@ -101,6 +103,10 @@ int lora_linear_create(lora_linear** out, int d_in, int d_out, int rank,
  * leaves the handle's workspace as it found it, so a graph can be replayed any number of
  * times (the host arrays are read at capture; device buffers are read at every replay).
  * Make one call of the same shape before capturing: it caches the launch shape.
+ * A call with adapter rows runs its shrink and fused passes in one cooperative launch, which
+ * starts only when its whole grid can be resident, so calls on different handles and streams
+ * may run side by side; profilers that reject cooperative launches can set
+ * LORA_LINEAR_NONCOOPERATIVE=1 in the environment (they run one kernel at a time).
  * Source: "Two 27B models on a single RTX 5090", section 4 (per-request adapter in a
  * shared batch) and section 3 (W + B.A).
  */
