@@ -383,7 +383,7 @@ def run_ours(args, rank, world, dist):
                                "unit": "GB/s", "frac": round(gbs / hbm, 4) if gbs else None,
                                "algorithmic_bytes": alg}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(items, args.cpu_seconds)
+        out["cpu_baseline"] = cpu_baseline(items, args.cpu_seconds, args.w4)
     for ll in handles.values():
         ll.close()
     return out
@@ -391,21 +391,28 @@ def run_ours(args, rank, world, dist):
 
 # --------------------------------------------------------------------------- oracle timing
 
-def _oracle_block(w, layer, pi, rows, seed_rows=0):
+def _oracle_block(w, layer, pi, rows, seed_rows=0, w4=False):
     """Inputs for a contiguous block of `rows` rows of workload w (starting at row 0), as
-    exact fp64 values, and the segments restricted to the block."""
+    exact fp64 values, and the segments restricted to the block. With w4 the base weight is
+    the workload's seeded 4-bit base, widened to bf16 as the oracle defines it (built here,
+    outside the timed call, like a weight being loaded)."""
     import numpy as np
-    from mixed_lora_projection_gb300.synth import bf16_bits, make_inputs
-    from oracle import bf16_bits_to_f64
+    from mixed_lora_projection_gb300.synth import bf16_bits, make_inputs, make_w4_base
+    from oracle import bf16_bits_to_f64, w4_weights_bf16_fp64
     inp = make_inputs(w, "cpu", layer=layer, proj_index=pi, x_rows=rows)
     f = lambda t: bf16_bits_to_f64(bf16_bits(t))  # noqa: E731
+    if w4:
+        q, sc = make_w4_base(w, "cpu", layer=layer, proj_index=pi)
+        wmat = w4_weights_bf16_fp64(q.numpy(), bf16_bits(sc))
+    else:
+        wmat = f(inp.w)
     off, ids = [0], []
     for i, a in enumerate(w.seg_ids):
         lo, hi = min(w.seg_offsets[i], rows), min(w.seg_offsets[i + 1], rows)
         if hi > lo:
             off.append(hi)
             ids.append(a)
-    return f(inp.x), off, ids, f(inp.w), [f(a) for a in inp.a], [f(b) for b in inp.b], inp.scales
+    return f(inp.x), off, ids, wmat, [f(a) for a in inp.a], [f(b) for b in inp.b], inp.scales
 
 
 def _block_flops(w, off, ids):
@@ -446,20 +453,20 @@ def _host_threads():
     return (min(blas, affinity) if blas else affinity), affinity
 
 
-def cpu_baseline(items, seconds):
+def cpu_baseline(items, seconds, w4=False):
     """The fp64 oracle, as it stands, on a contiguous block of the workload's rows, sized
     to about `seconds` of host time."""
     from oracle import lora_linear_fp64
     w, layer, pi = items[0]
     cores, affinity = _host_threads()
     rows = min(w.T, 64)
-    data = _oracle_block(w, layer, pi, rows)
+    data = _oracle_block(w, layer, pi, rows, w4=w4)
     t = time.perf_counter()
     lora_linear_fp64(*data)
     dt = time.perf_counter() - t
     rate = _block_flops(w, data[1], data[2]) / max(dt, 1e-6)
     rows = int(min(w.T, max(64, rows * seconds / max(dt, 1e-6) * 0.8)))
-    data = _oracle_block(w, layer, pi, rows)
+    data = _oracle_block(w, layer, pi, rows, w4=w4)
     t = time.perf_counter()
     lora_linear_fp64(*data)
     dt = time.perf_counter() - t
@@ -467,7 +474,8 @@ def cpu_baseline(items, seconds):
     return {"value": round(fl / dt / 1e12, 5), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
             "host_cores": affinity,
             "sample": f"rows [0,{rows}) of {w.name} ({w.T} rows), layer 0, all {w.d_out} outputs: "
-                      f"{fl / 1e9:.1f} GFLOP fp64 in {dt:.1f} s (numpy/OpenBLAS, {cores} BLAS threads)"}
+                      f"{fl / 1e9:.1f} GFLOP fp64 in {dt:.1f} s (numpy/OpenBLAS, {cores} BLAS threads)"
+                      + ("; base: the 4-bit weights widened to bf16" if w4 else "")}
 
 
 def run_reference(args, rank, world):
@@ -475,15 +483,16 @@ def run_reference(args, rank, world):
     from oracle import lora_linear_fp64
     items = _workloads(args.workload)
     w, layer, pi = items[0]
+    w4 = args.w4
     cores, affinity = _host_threads()
     budget = max(0.05, args.cpu_seconds * 4 / max(1, args.steps + args.warmup))  # ~a few minutes in all
     rows = min(w.T, 32)
-    data = _oracle_block(w, layer, pi, rows)
+    data = _oracle_block(w, layer, pi, rows, w4=w4)
     t = time.perf_counter()
     lora_linear_fp64(*data)
     dt = time.perf_counter() - t
     rows = int(min(w.T, max(8, rows * budget / max(dt, 1e-6))))
-    data = _oracle_block(w, layer, pi, rows)
+    data = _oracle_block(w, layer, pi, rows, w4=w4)
     fl = _block_flops(w, data[1], data[2])
     for _ in range(args.warmup):
         lora_linear_fp64(*data)
@@ -492,14 +501,16 @@ def run_reference(args, rank, world):
         lora_linear_fp64(*data)
     dt = (time.perf_counter() - t) / args.steps
     value = fl / dt / 1e12
-    sample = f"rows [0,{rows}) of {w.name} per step ({w.T} rows in the full batch), all {w.d_out} outputs, fp64"
+    sample = (f"rows [0,{rows}) of {w.name} per step ({w.T} rows in the full batch), all {w.d_out} outputs, fp64"
+              + ("; base: the 4-bit weights widened to bf16" if w4 else ""))
     return {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world,
             "host": "rank 0 only, host cores",
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded Gaussian bf16 values, exact in fp64)",
-            "config": {"workload": args.workload, "T": w.T, "d_in": w.d_in, "d_out": w.d_out, "rank": w.rank,
-                       "sample_rows": rows},
+            "config": {"workload": args.workload + ("+w4" if w4 else ""),
+                       "base": "int4 (symmetric, group 128, bf16 scales)" if w4 else "bf16",
+                       "T": w.T, "d_in": w.d_in, "d_out": w.d_out, "rank": w.rank, "sample_rows": rows},
             "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                              "host_cores": affinity, "sample": sample},
             "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
