@@ -10,9 +10,12 @@ X alone is larger than the 129 MB L2 for the prefill workloads.
 
 Prints one JSON line (rank 0). `value` is useful TFLOP/s of the whole job (all ranks);
 `e2e` is the same metric through the host-buffer entry point (X copied in, Y copied
-out every step); `roofline` is the fused kernel's achieved TFLOP/s (CUDA events around
-each launch, on the launch stream) against the measured bf16 peak; `cpu_baseline` is the
-fp64 oracle timed on a bounded sample on the host cores.
+out every step); `roofline` is the projection kernel against the roof that binds it (CUDA
+events around each launch, on the launch stream): useful TFLOP/s against the measured bf16
+peak, or algorithmic GB/s against the measured copy bandwidth for batches that stream W
+(`roofline_other` holds the other roof); `cpu_baseline` is the fp64 oracle timed on a
+bounded sample on the host cores. The default run (the 16k prefill) also times the
+decode-sized batch (48 chat rows, gate_up) in the same process, under `decode`.
 
 Multi-GPU: launched under torchrun, every rank runs an independent replica (the
 projection's rows need no exchange); the timed region is bracketed by barriers and the
@@ -160,6 +163,113 @@ def _tokens_of(items):
 def _fused_flops(w):
     """Algorithmic FLOPs of the fused base+expand kernel: 2 T d_in d_out + 2 T_a r d_out."""
     return 2.0 * w.T * w.d_in * w.d_out + 2.0 * w.adapter_rows * w.rank * w.d_out
+
+
+L2_BYTES = 129e6   # GB300 L2
+
+
+def _alg_bytes(w, w4=False):
+    """Algorithmic bytes of one call: bf16 X, W, Y and the named adapters; with a 4-bit base, W
+    counts as its packed nibbles (half a byte per weight) plus its bf16 group scales."""
+    b = w.algorithmic_bytes()
+    if w4:
+        b += -2.0 * w.d_out * w.d_in + 0.5 * w.d_out * w.d_in + 2.0 * w.d_out * w.d_in / 128
+    return b
+
+
+def _l2_note(items, n_copies, w4=False):
+    """What keeps the timed steps from running out of L2 (129 MB), for this workload."""
+    if len(items) > 1:
+        wb = sum(2.0 * w.d_in * w.d_out for w, _, _ in items)
+        return f"{len(items)} distinct weight sets per step ({wb / 1e9:.1f} GB), each read once per step"
+    w = items[0][0]
+    xb = 2.0 * w.T * w.d_in
+    wb = (0.5 + 2.0 / 128) * w.d_in * w.d_out if w4 else 2.0 * w.d_in * w.d_out
+    wdesc = f"{n_copies} rotating weight copies of {wb / 1e6:.0f} MB ({n_copies * wb / 1e6:.0f} MB in all)"
+    if xb > L2_BYTES:
+        return f"X ({xb / 1e6:.0f} MB) larger than L2; {wdesc}"
+    if wb > L2_BYTES:
+        return f"X ({xb / 1e6:.1f} MB) fits in L2; each step reads a weight copy ({wb / 1e6:.0f} MB) larger than L2"
+    return f"X ({xb / 1e6:.1f} MB) fits in L2; {wdesc}, larger than L2 together"
+
+
+def _rooflines(items, w4, fused_flops, avg_fused_ms, traffic, peak_burst, hbm, src, shrink_n):
+    """(binding roof, other roof) of the timed kernel: the tensor roof (algorithmic FLOPs against
+    the measured bf16 burst) and the HBM roof (algorithmic bytes against the measured copy
+    bandwidth); the one that takes longer at its peak binds."""
+    alg = sum(_alg_bytes(w, w4) for w, _, _ in items)
+    kernel = ("lora_w4_kernel (4-bit base + expand; shrink on lora_gemm_kernel before it)" if w4
+              else "lora_gemm_kernel (shrink + base + expand, one launch per call)" if not shrink_n
+              else "lora_gemm_kernel (fused base + expand launch)")
+    achieved_tf = fused_flops / (avg_fused_ms * 1e-3) / 1e12 if avg_fused_ms else None
+    achieved_gbs = alg / (avg_fused_ms * 1e-3) / 1e9 if avg_fused_ms else None
+    tensor = {"bound": "tensor", "achieved": round(achieved_tf, 2) if achieved_tf else None, "peak": peak_burst,
+              "unit": "TFLOP/s", "frac": round(achieved_tf / peak_burst, 4) if achieved_tf else None,
+              "traffic": traffic, "peak_source": f"{src} bf16 burst", "kernel": kernel,
+              "algorithmic_flops_per_step": fused_flops}
+    mem = {"bound": "hbm", "achieved": round(achieved_gbs, 1) if achieved_gbs else None, "peak": hbm,
+           "unit": "GB/s", "frac": round(achieved_gbs / hbm, 4) if achieved_gbs else None, "traffic": traffic,
+           "peak_source": f"{src} copy bandwidth", "kernel": kernel, "algorithmic_bytes_per_step": alg}
+    if alg / (hbm * 1e9) > fused_flops / (peak_burst * 1e12):
+        return mem, tensor
+    return tensor, mem
+
+
+def decode_line(dev, steps, warmup):
+    """The decode-sized batch (the 48 chat rows of the mixed batch, gate_up 5120 -> 34816, no
+    adapter rows) timed in the same process as the headline: its kernel streams W, so the HBM
+    roof binds. Three weight copies of 356 MB rotate, so W never stays in L2."""
+    import torch
+    from mixed_lora_projection_gb300 import LoraLinear, _lib as L
+    from mixed_lora_projection_gb300.synth import WORKLOADS, make_inputs
+    w = WORKLOADS["mixed_decode"]
+    copies = [make_inputs(w, dev, proj_index=4 * c, with_x=(c == 0)) for c in range(3)]
+    y = torch.empty((w.T, w.d_out), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    with LoraLinear(w.d_in, w.d_out, w.rank, w.T, len(w.seg_ids), dev) as ll:
+        def f(i):
+            c = copies[i % 3]
+            ll.forward(copies[0].x, w.seg_offsets, w.seg_ids, c.w, c.a, c.b, c.scales, y=y, stream=stream)
+        for i in range(warmup):
+            f(i)
+        torch.cuda.synchronize()
+        assert ll.status() == 0
+        ll.set_option(L.OPT_TIMING, 1)
+        n0 = ll.timing(1)[2]
+        sampler = ClockSampler(dev.index)
+        sampler.start()
+        time.sleep(0.2)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        t0 = time.time()
+        e0.record(stream)
+        for i in range(steps):
+            f(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        t1 = time.time()
+        time.sleep(0.1)
+        sampler.stop()
+        kernel_ms, n_timed, n_all = ll.timing(1)
+        ll.set_option(L.OPT_TIMING, 0)
+        assert ll.status() == 0, "a kernel's bounded wait ran out"
+        shape = ll.describe(w.T, w.seg_offsets, w.seg_ids)
+    ms = e0.elapsed_time(e1) / steps
+    k_ms = kernel_ms / max(1, n_timed)
+    alg = _alg_bytes(w)
+    peak_burst, _, hbm, src = _peaks()
+    gbs = alg / (k_ms * 1e-3) / 1e9
+    return {"workload": w.name, "T": w.T, "d_in": w.d_in, "d_out": w.d_out, "segments": len(w.seg_ids),
+            "adapter_rows": w.adapter_rows, "steps": steps, "warmup": warmup, "ms_per_step": round(ms, 5),
+            "value": round(w.useful_flops() / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+            "tokens_per_s": round(w.T / (ms * 1e-3), 1), "kernel_ms": round(k_ms, 5),
+            "gpu_launches": n_all - n0,
+            "l2": _l2_note([(w, 0, 0)], 3),
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
+                         "frac": round(gbs / hbm, 4), "traffic": _profiled_traffic(w.name),
+                         "peak_source": f"{src} copy bandwidth", "kernel": "lora_gemm_kernel",
+                         "algorithmic_bytes_per_step": alg},
+            "launch_shape": shape, "clocks": sampler.summary(t0, t1)}
 
 
 # --------------------------------------------------------------------------- ranks
@@ -340,6 +450,7 @@ def run_ours(args, rank, world, dist):
     achieved = fused_flops / (avg_fused_ms * 1e-3) / 1e12 if avg_fused_ms else None
     traffic = _profiled_traffic(args.workload + ("+w4" if args.w4 else ""))
     w0 = items[0][0]
+    roof, roof_other = _rooflines(items, args.w4, fused_flops, avg_fused_ms, traffic, peak_burst, hbm, src, shrink_n)
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
@@ -353,15 +464,10 @@ def run_ours(args, rank, world, dist):
                    "d_out": w0.d_out if len(items) == 1 else "per projection", "rank": w0.rank,
                    "segments": len(w0.seg_ids), "adapter_rows": w0.adapter_rows, "calls_per_step": len(items),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "l2": "X larger than L2; 3 rotating weight copies" if n_copies > 1 else "96 distinct weight sets per step (17 GB)"},
+                   "l2": _l2_note(items, n_copies, args.w4)},
         "tokens_per_s": round(world * _tokens_of(items) * args.steps / (elapsed_ms * 1e-3), 1),
-        "roofline": {"bound": "tensor", "achieved": round(achieved, 2) if achieved else None,
-                     "peak": peak_burst, "unit": "TFLOP/s",
-                     "frac": round(achieved / peak_burst, 4) if achieved else None,
-                     "traffic": traffic, "peak_source": f"{src} bf16 burst",
-                     "kernel": ("lora_w4_kernel (4-bit base + expand; shrink on lora_gemm_kernel before it)" if args.w4
-                                else "lora_gemm_kernel (shrink + base + expand, one launch per call)" if not shrink_n
-                                else "lora_gemm_kernel (fused base + expand launch)"), "algorithmic_flops_per_step": fused_flops},
+        "roofline": roof,
+        **({"roofline_other": roof_other} if roof_other else {}),
         "kernel_ms": {"main": round(fused_ms / max(1, args.steps), 5), "separate_shrink": round(shrink_ms / max(1, args.steps), 5),
                       "main_launches": fused_n, "separate_shrink_launches": shrink_n},
         "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s",
@@ -374,14 +480,9 @@ def run_ours(args, rank, world, dist):
         "launch_shape": setups[0][1].describe(w0.T, w0.seg_offsets, w0.seg_ids),
         "clocks": sampler.summary(t0, t1),
     }
-    if w0.T <= 512 and len(items) == 1:
-        alg = w0.algorithmic_bytes()
-        if args.w4:   # packed weights (half a byte) and bf16 scales instead of bf16 W
-            alg += -2.0 * w0.d_out * w0.d_in + 0.5 * w0.d_out * w0.d_in + 2.0 * w0.d_out * w0.d_in / 128
-        gbs = alg / (avg_fused_ms * 1e-3) / 1e9 if avg_fused_ms else None
-        out["roofline_hbm"] = {"bound": "hbm", "achieved": round(gbs, 1) if gbs else None, "peak": hbm,
-                               "unit": "GB/s", "frac": round(gbs / hbm, 4) if gbs else None,
-                               "algorithmic_bytes": alg}
+    if args.workload == "prefill_16k" and not args.w4 and not args.no_decode:
+        # the decode-sized batch beside the headline: the HBM roof, in the same process
+        out["decode"] = decode_line(dev, args.decode_steps, max(args.warmup, 20))
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(items, args.cpu_seconds, args.w4)
     for ll in handles.values():
@@ -526,6 +627,9 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-decode", action="store_true", help="skip the decode-sized batch timed beside the default "
+                    "16k prefill")
+    ap.add_argument("--decode-steps", type=int, default=4000)
     ap.add_argument("--two-launch", action="store_true", help="shrink as its own launch (for comparison)")
     ap.add_argument("--w4", action="store_true", help="4-bit base weights (int4, group 128, bf16 scales)")
     ap.add_argument("--raster", default="", help="unit order MODE[:GROUP] (the library's raster option: 0 auto, "
