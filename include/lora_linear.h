@@ -305,10 +305,14 @@ int lora_linear_host_chunks(int T, int32_t* bounds, int* n);
  * (cudaGetSymbolAddress) and sets the kernels' shared-memory limit; make that first call
  * before any stream capture. Every call shares the one scratch array and leaves its
  * contents behind: calls that overlap on the GPU (on different streams, or from several
- * threads) race and give wrong results; order them on one stream. The work list is copied
- * from host memory with cudaMemcpyAsync before the launches. A kernel wait that runs out
- * stops that kernel early; this entry point cannot report it afterwards.
- * Returns LORA_OK, LORA_EINVAL, LORA_ENODEV or LORA_ECUDA.
+ * threads) race and give wrong results; order them on one stream. A work list of at most
+ * 64 row tiles (shrink and fused), 48 merged segments and 4 named adapters travels in the
+ * kernel parameters; a larger one is copied from a buffer on the call's stack into the
+ * scratch array with cudaMemcpyAsync. While `stream` is capturing, the call returns
+ * LORA_EUNSUPPORTED and enqueues nothing. Every tensor map is encoded before anything is
+ * enqueued, so a call that fails enqueues nothing. A kernel wait that runs out stops that
+ * kernel early (Y incomplete); this entry point has no way to report it afterwards.
+ * Returns LORA_OK, LORA_EINVAL, LORA_ENODEV, LORA_EUNSUPPORTED or LORA_ECUDA.
  */
 #define LORA_NOALLOC_MAX_TOKENS 4096
 #define LORA_NOALLOC_MAX_SEGMENTS 64

@@ -7,7 +7,8 @@
 // (the shrink output U, the device work list and a status word) is one file-scope
 // __device__ array of fixed size, resident on every GPU that loads the library. It runs
 // the same kernels as lora_linear_forward and allocates nothing, on the device or the
-// host: the plan and the work list are built in fixed-size arrays on the stack.
+// host: the plan and the work list are built in fixed-size arrays on the stack, and a
+// small work list travels in the kernel parameters instead of being copied.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -193,41 +194,64 @@ extern "C" int lora_linear_forward_noalloc(const void* x, int T, const int32_t* 
         return s < 2 ? 2 : (s > lora::kMaxStages ? lora::kMaxStages : s);
     };
 
-    // host copy of the work list, on the stack
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    // The work list below lives on this call's stack (or in the kernel parameters); a stream
+    // capture would record work that reads it after the call has returned, so no work is
+    // enqueued while the stream is capturing.
+    cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &capture) != cudaSuccess) return LORA_ECUDA;
+    if (capture != cudaStreamCaptureStatusNone) return LORA_EUNSUPPORTED;
+
+    unsigned char* scratch = ds->scratch;
+    unsigned char* wdev = scratch + kUBytes;
+    int* status = reinterpret_cast<int*>(scratch + kOffStatus);
+    GemmParams p;
+    memset(&p, 0, sizeof(p));
+    // Every tensor map is encoded before anything is enqueued, so a failed call leaves the
+    // stream untouched. A work list within the kernel-parameter limits travels in the
+    // parameters (no copy at all); a larger one is copied into the scratch array.
+    const bool inline_wl = plan.n_fused + plan.n_shrink <= lora::kInlineTiles && plan.n_m <= lora::kInlineSegs &&
+                           plan.n_used <= lora::kInlineAdapters;
     alignas(128) unsigned char work[kWorkBytes];
-    CUtensorMap* bmaps = reinterpret_cast<CUtensorMap*>(work + kOffBMaps);
-    CUtensorMap* amaps = reinterpret_cast<CUtensorMap*>(work + kOffAMaps);
+    CUtensorMap* bmaps = inline_wl ? p.inline_maps : reinterpret_cast<CUtensorMap*>(work + kOffBMaps);
+    CUtensorMap* amaps =
+        inline_wl ? p.inline_maps + lora::kInlineAdapters : reinterpret_cast<CUtensorMap*>(work + kOffAMaps);
     for (int k = 0; k < plan.n_used; ++k) {
         int a = plan.used[k];
         if (encode(&bmaps[k], B[a], rank, d_out, lora::kTileK, tile_n) != CUDA_SUCCESS) return LORA_ECUDA;
         if (encode(&amaps[k], A[a], d_in, rank, lora::kTileK, shrink_n) != CUDA_SUCCESS) return LORA_ECUDA;
     }
-    memcpy(work + kOffFused, plan.fused, sizeof(Tile) * plan.n_fused);
-    memcpy(work + kOffShrink, plan.shrink, sizeof(Tile) * plan.n_shrink);
-    memcpy(work + kOffSegOff, plan.seg_off, 4 * (size_t)(plan.n_m + 1));
-    memcpy(work + kOffSegId, plan.seg_id, 4 * (size_t)plan.n_m);
-    float* sc = reinterpret_cast<float*>(work + kOffScale);
-    for (int k = 0; k < plan.n_used; ++k) sc[k] = scale[plan.used[k]];
-
-    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
-    unsigned char* scratch = ds->scratch;
-    unsigned char* wdev = scratch + kUBytes;
-    int* status = reinterpret_cast<int*>(scratch + kOffStatus);
-    if (cudaMemcpyAsync(wdev, work, kWorkBytes, cudaMemcpyHostToDevice, stream) != cudaSuccess) return LORA_ECUDA;
-    if (cudaMemsetAsync(status, 0, sizeof(int), stream) != cudaSuccess) return LORA_ECUDA;
-
-    GemmParams p;
-    memset(&p, 0, sizeof(p));
     if (encode(&p.tm_x, x, d_in, T, lora::kTileK, lora::kTileM) != CUDA_SUCCESS) return LORA_ECUDA;
     if (encode(&p.tm_w, W, d_in, d_out, lora::kTileK, tile_n) != CUDA_SUCCESS) return LORA_ECUDA;
     if (encode(&p.tm_u, scratch, rank, kURows, lora::kTileK, lora::kTileM) != CUDA_SUCCESS) return LORA_ECUDA;
-    p.tm_b = reinterpret_cast<const CUtensorMap*>(wdev + kOffBMaps);
-    p.tm_a = reinterpret_cast<const CUtensorMap*>(wdev + kOffAMaps);
-    p.shrink_tiles = reinterpret_cast<const Tile*>(wdev + kOffShrink);
-    p.fused_tiles = reinterpret_cast<const Tile*>(wdev + kOffFused);
-    p.seg_off = reinterpret_cast<const int32_t*>(wdev + kOffSegOff);
-    p.seg_id = reinterpret_cast<const int32_t*>(wdev + kOffSegId);
-    p.scales = reinterpret_cast<const float*>(wdev + kOffScale);
+    if (inline_wl) {
+        memcpy(p.inline_tiles, plan.fused, sizeof(Tile) * plan.n_fused);
+        memcpy(p.inline_tiles + plan.n_fused, plan.shrink, sizeof(Tile) * plan.n_shrink);
+        memcpy(p.inline_seg, plan.seg_off, 4 * (size_t)(plan.n_m + 1));
+        memcpy(p.inline_seg + plan.n_m + 1, plan.seg_id, 4 * (size_t)plan.n_m);
+        for (int k = 0; k < plan.n_used; ++k) p.inline_scales[k] = scale[plan.used[k]];
+        p.inline_wl = 1;
+        p.inline_shrink_off = plan.n_fused;
+    } else {
+        memcpy(work + kOffFused, plan.fused, sizeof(Tile) * plan.n_fused);
+        memcpy(work + kOffShrink, plan.shrink, sizeof(Tile) * plan.n_shrink);
+        memcpy(work + kOffSegOff, plan.seg_off, 4 * (size_t)(plan.n_m + 1));
+        memcpy(work + kOffSegId, plan.seg_id, 4 * (size_t)plan.n_m);
+        float* sc = reinterpret_cast<float*>(work + kOffScale);
+        for (int k = 0; k < plan.n_used; ++k) sc[k] = scale[plan.used[k]];
+        p.tm_b = reinterpret_cast<const CUtensorMap*>(wdev + kOffBMaps);
+        p.tm_a = reinterpret_cast<const CUtensorMap*>(wdev + kOffAMaps);
+        p.shrink_tiles = reinterpret_cast<const Tile*>(wdev + kOffShrink);
+        p.fused_tiles = reinterpret_cast<const Tile*>(wdev + kOffFused);
+        p.seg_off = reinterpret_cast<const int32_t*>(wdev + kOffSegOff);
+        p.seg_id = reinterpret_cast<const int32_t*>(wdev + kOffSegId);
+        p.scales = reinterpret_cast<const float*>(wdev + kOffScale);
+        // cudaMemcpyAsync from pageable memory returns once the source has been read, so the
+        // stack buffer may go away with this call
+        if (cudaMemcpyAsync(wdev, work, kWorkBytes, cudaMemcpyHostToDevice, stream) != cudaSuccess) return LORA_ECUDA;
+    }
+    if (cudaMemsetAsync(status, 0, sizeof(int), stream) != cudaSuccess) return LORA_ECUDA;
+
     p.y = y;
     p.u = scratch;
     p.status = status;
