@@ -125,6 +125,47 @@ def test_w4_full_size_sampled_rows(dev, name):
     assert rel_err(y[torch.as_tensor(rows, device=dev)], ref) <= TOL
 
 
+@pytest.mark.parametrize("name", ["mixed_decode", "mixed_near_ridge", "sweep_qkv_multi", "prefill_16k"])
+def test_w4_gap_to_exact_dequantisation_within_the_widening_bound(dev, name, record_property):
+    """The 4-bit base is widened to bf16 before it meets X (the W4A16 reading). Measured here:
+    how far the GPU result sits from the result on the exact weights q * s (no widening), on the
+    full-size workloads. Round to nearest even to bf16 (8 significant bits) moves each weight by
+    at most half an ulp, 2^-8 of its magnitude, so the widened and exact products differ by at
+    most 2^-8 (|X| |W|^T) per element; with the triangle inequality that bounds the GPU's gap to
+    the exact result by its gap to the widened result plus that bound."""
+    w = WORKLOADS[name]
+    inp = make_inputs(w, dev)
+    q, sc = make_w4_base(w, dev)
+    off, ids = list(w.seg_offsets), list(w.seg_ids)
+    with _ll(w) as ll:
+        y = ll.forward_w4(inp.x, off, ids, _kq(q), sc, inp.a, inp.b, inp.scales)
+        torch.cuda.synchronize()
+        assert ll.status() == 0
+    rows = sample_rows(w.T, off, ids, n_random=64, seed=8)
+    w_exact = w4_dequantize_fp64(q.cpu().numpy(), bf16_bits(sc))
+    w_wide = w4_weights_bf16_fp64(q.cpu().numpy(), bf16_bits(sc))
+    x = f64(inp.x[torch.as_tensor(rows, device=dev)])
+    rid = row_adapter_ids(off, ids, w.T)[rows]
+    a64, b64 = [f64(a) for a in inp.a], [f64(b) for b in inp.b]
+    y_exact = lora_linear_rows_fp64(x, rid, w_exact, a64, b64, inp.scales)
+    y_wide = lora_linear_rows_fp64(x, rid, w_wide, a64, b64, inp.scales)
+    bound = 2.0 ** -8 * (np.abs(x) @ np.abs(w_exact).T)
+    # the widening's own effect, in the oracle alone, stays inside its bound element by element
+    assert np.all(np.abs(y_wide - y_exact) <= bound * (1 + 1e-9))
+    yg = f64(y[torch.as_tensor(rows, device=dev)])
+    ref_max = np.max(np.abs(y_exact))
+    gap_wide = np.max(np.abs(yg - y_wide)) / np.max(np.abs(y_wide))
+    gap_exact = np.max(np.abs(yg - y_exact)) / ref_max
+    widening = np.max(np.abs(y_wide - y_exact)) / ref_max
+    record_property("gap_to_widened", float(gap_wide))
+    record_property("gap_to_exact", float(gap_exact))
+    record_property("widening_alone", float(widening))
+    print(f"\nw4 {name}: max|dY|/max|Y| to the widened-weight oracle {gap_wide:.3e}, to the exact-weight "
+          f"oracle {gap_exact:.3e}; widening alone {widening:.3e}, its bound {np.max(bound) / ref_max:.3e}")
+    assert gap_wide <= TOL
+    assert gap_exact <= gap_wide * np.max(np.abs(y_wide)) / ref_max + np.max(bound) / ref_max
+
+
 ROWS = [1, 16, 17, 48, 64, 80, 128]
 
 
