@@ -167,7 +167,8 @@ def test_one_launch_equals_two_launches(dev, name):
 
 @pytest.mark.parametrize("name", ["tiny", "sweep_qkv_multi", "mixed_near_ridge", "prefill_16k"])
 def test_cta_pairs_equal_single_ctas(dev, name):
-    # CTA pairs that share the B tile by TMA multicast compute exactly what single CTAs do
+    # SM pairs (tcgen05 cta_group::2, M = 256: each CTA loads its own 128 A rows and half of the
+    # B tile, the even CTA issues the MMAs) compute exactly what single CTAs do
     from mixed_lora_projection_gb300 import _lib as L
     w = WORKLOADS[name]
     inp = make_inputs(w, dev)
