@@ -39,6 +39,7 @@ sys.path.insert(0, ROOT)
 METRIC = "LoRA-linear TFLOP/s & tokens/s at 1 GB300; % of bf16 tensor peak / HBM BW"
 SWEEP = "sweep_24_layers"
 SWEEP_MULTI = "sweep_24_layers_multi"   # the same stack with three adapters (ids 1, 2, 3)
+DECODE_SWEEP = "decode_24_layers"        # one decode step of six chats (48 rows) through the same stack
 
 
 def _peaks():
@@ -145,9 +146,13 @@ class ClockSampler:
 # --------------------------------------------------------------------------- workloads
 
 def _workloads(name):
-    from mixed_lora_projection_gb300.synth import SWEEP_LAYERS, SWEEP_PROJECTIONS, WORKLOADS, sweep_workload
+    from mixed_lora_projection_gb300.synth import (SWEEP_LAYERS, SWEEP_PROJECTIONS, WORKLOADS, decode_workload,
+                                                   sweep_workload)
     if name in (SWEEP, SWEEP_MULTI):
         return [(sweep_workload(p, name == SWEEP_MULTI), layer, i) for layer in range(SWEEP_LAYERS)
+                for i, (p, _, _) in enumerate(SWEEP_PROJECTIONS)]
+    if name == DECODE_SWEEP:
+        return [(decode_workload(p), layer, i) for layer in range(SWEEP_LAYERS)
                 for i, (p, _, _) in enumerate(SWEEP_PROJECTIONS)]
     return [(WORKLOADS[name], 0, 0)]
 
@@ -297,7 +302,7 @@ def run_ours(args, rank, world, dist):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     items = _workloads(args.workload)
-    n_copies = 1 if args.workload in (SWEEP, SWEEP_MULTI) else 3
+    n_copies = 1 if args.workload in (SWEEP, SWEEP_MULTI, DECODE_SWEEP) else 3
     setups = []
     handles = {}
     for (w, layer, pi) in items:
@@ -306,6 +311,8 @@ def run_ours(args, rank, world, dist):
             handles[key] = LoraLinear(w.d_in, w.d_out, w.rank, w.T, max(8, len(w.seg_ids)), dev)
             if args.two_launch:
                 handles[key].set_option(L.OPT_TWO_LAUNCH, 1)
+            if args.k_split:
+                handles[key].set_option(L.OPT_K_SPLIT, args.k_split)
             if args.raster:
                 mode, _, group = args.raster.partition(":")
                 handles[key].set_option(L.OPT_RASTER, int(mode))
@@ -460,6 +467,7 @@ def run_ours(args, rank, world, dist):
         "data": "synthetic (seeded Gaussian bf16; no checkpoint)",
         "config": {"workload": args.workload + ("+w4" if args.w4 else ""),
                    **({"raster": args.raster} if args.raster else {}),
+                   **({"k_split": args.k_split} if args.k_split else {}),
                    "base": "int4 (symmetric, group 128, bf16 scales)" if args.w4 else "bf16", "T": w0.T, "d_in": w0.d_in if len(items) == 1 else "per projection",
                    "d_out": w0.d_out if len(items) == 1 else "per projection", "rank": w0.rank,
                    "segments": len(w0.seg_ids), "adapter_rows": w0.adapter_rows, "calls_per_step": len(items),
@@ -634,6 +642,8 @@ def main():
     ap.add_argument("--w4", action="store_true", help="4-bit base weights (int4, group 128, bf16 scales)")
     ap.add_argument("--raster", default="", help="unit order MODE[:GROUP] (the library's raster option: 0 auto, "
                     "1 row tiles first, 2 column tiles first, 3 groups of GROUP column tiles)")
+    ap.add_argument("--k-split", type=int, default=0, choices=[0, 1, 2], help="K halves per output block (the "
+                    "library's K-split option: 0 = each handle's own choice, 1 = whole K, 2 = two halves)")
     ap.add_argument("--graph", action="store_true", help="time the steps as CUDA-graph replays (each call's "
                     "work list must travel in the kernel parameters, e.g. the 24-layer sweep)")
     args = ap.parse_args()

@@ -17,9 +17,11 @@
  * Arithmetic: bf16 operands, fp32 accumulation on the tensor cores. The shrink output
  * U = s_a X A_a^T is rounded to bf16 (round to nearest even) before the expand; Y is
  * rounded from fp32 to bf16 (round to nearest even). The summation order is not
- * specified, so results are not bitwise equal to any other implementation; within this
- * library a row's output does not depend on the other rows of its batch (the same bits in
- * any batch, launch shape or host-buffer chunking).
+ * specified, so results are not bitwise equal to any other implementation; on one handle a
+ * row's output does not depend on the other rows of its batch (the same bits in any batch,
+ * launch shape or host-buffer chunking). A handle may sum the base product in two K halves
+ * (LORA_OPT_K_SPLIT); it decides that once, at create, from its shape and max_tokens, so two
+ * handles of one shape but different max_tokens may differ in the last bit.
  *
  * Errors: every function returns LORA_OK (0) or a negative code below. Argument checks
  * run on the host before any launch; a failed check launches nothing and leaves every
@@ -234,8 +236,14 @@ enum {
                                       0 = always upload them to device memory */
     LORA_OPT_MMA_GROUP = 12,    /* pipeline stages the MMA warp waits for at once: 0 = auto (2 for SM
                                    pairs, 1 for single CTAs), 1 or 2 */
-    LORA_OPT_DEBUG_PUBLISH_DELAY_US = 13 /* tests only: each shrink unit of a one-launch call publishes
+    LORA_OPT_DEBUG_PUBLISH_DELAY_US = 13, /* tests only: each shrink unit of a one-launch call publishes
                                    its U rows this many microseconds late (0..1,000,000; default 0) */
+    LORA_OPT_K_SPLIT = 14       /* bf16 base: 0 = the handle's own choice (made at create), 1 = whole K
+                                   per output block, 2 = two K halves: each output block runs as two
+                                   work units whose fp32 sums are added (one stores its partial sums, the
+                                   other adds them) before the bf16 rounding; fills the GPU when long-K,
+                                   narrow projections leave too few or too ragged waves of blocks.
+                                   Changes the summation for later calls; may allocate (LORA_ENOMEM) */
 };
 
 /* lora_linear_set_option -- set one option above. Returns LORA_OK or LORA_EINVAL. */
@@ -275,6 +283,13 @@ int lora_linear_describe(lora_linear* h, int T, const int32_t* seg_offsets,
 int lora_linear_shape(int d_in, int d_out, int rank, int num_sms, int T, const int32_t* seg_offsets,
                       const int32_t* seg_adapter_ids, int n_seg, int w4, int* cluster, int* tile_n, int* bk,
                       int* stages, int* unit_order, int* fused_units, int* shrink_units);
+
+/*
+ * lora_linear_k_split -- the K split (1 or 2, see LORA_OPT_K_SPLIT) a handle of this shape
+ * and max_tokens would choose at create on a GPU with num_sms SMs, computed on the host alone.
+ * Returns LORA_OK or LORA_EINVAL. Diagnostics and tests.
+ */
+int lora_linear_k_split(int d_in, int d_out, int rank, int max_tokens, int num_sms, int* k_split);
 
 /*
  * lora_linear_host_chunks -- the row chunks lora_linear_forward_host runs T rows in (its

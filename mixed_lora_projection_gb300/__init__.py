@@ -11,7 +11,7 @@ from .synth import WORKLOADS, Workload, make_inputs  # noqa: F401
 
 
 def __getattr__(name):
-    if name in ("LoraLinear", "plan", "LoraError", "validate", "w4_repack", "launch_shape", "host_chunks"):
+    if name in ("LoraLinear", "plan", "LoraError", "validate", "w4_repack", "launch_shape", "host_chunks", "k_split"):
         from . import lora_linear as _ll
         return getattr(_ll, name)
     raise AttributeError(name)

@@ -40,6 +40,7 @@ SIGNATURES = {
     "lora_linear_shape": (C.c_int, [C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, I32P, I32P, C.c_int, C.c_int,
                                     IP, IP, IP, IP, IP, IP, IP]),
     "lora_linear_host_chunks": (C.c_int, [C.c_int, I32P, IP]),
+    "lora_linear_k_split": (C.c_int, [C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, IP]),
     "lora_linear_forward_noalloc": (C.c_int, [P, C.c_int, I32P, I32P, C.c_int, C.c_int, C.c_int, C.c_int, P,
                                               C.POINTER(P), C.POINTER(P), C.POINTER(C.c_float), C.c_int, P, P]),
 }
@@ -48,7 +49,7 @@ SIGNATURES = {
 LORA_OK, LORA_EINVAL, LORA_ENOMEM, LORA_ECUDA, LORA_ETIMEOUT, LORA_EUNSUPPORTED, LORA_ENODEV = 0, -1, -2, -3, -4, -5, -6
 (OPT_TILE_N, OPT_WAIT_LIMIT_US, OPT_DEBUG_STALL, OPT_TIMING, OPT_RASTER, OPT_TWO_LAUNCH, OPT_CLUSTER,
  OPT_RASTER_GROUP, _OPT_RETIRED_9, OPT_TILE_K, OPT_INLINE_WORK_LIST, OPT_MMA_GROUP,
- OPT_DEBUG_PUBLISH_DELAY_US) = 1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 11, 12, 13
+ OPT_DEBUG_PUBLISH_DELAY_US, OPT_K_SPLIT) = 1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 11, 12, 13, 14
 
 
 def load():

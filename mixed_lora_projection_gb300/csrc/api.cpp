@@ -81,6 +81,12 @@ struct lora_linear {
     unsigned long long debug_publish_delay_ns = 0;
     int raster_group = 4, tile_k = 0, allow_inline = 1, mma_group = 0;  // 0: 2 for SM pairs, else 1
     int max_clusters_cache[2][kMaxTileN / 16 + 1] = {};  // co-resident clusters by (size, B rows)
+    // K halves: chosen once per handle (every call on it sums each output the same way)
+    int k_split = 1;            // 1, or 2: every fused unit runs as two units over the K halves
+    int k_split_opt = 0;        // LORA_OPT_K_SPLIT: 0 = the handle's own choice, 1 or 2 = forced
+    float4* partials = nullptr; // fp32 partial sums, ceil(d_out / 4) float4 chunks x max_tokens rows
+    int* split_ctr = nullptr;   // per (fused tile, column tile): halves arrived, partials stored
+    size_t split_slots = 0;     // counter pairs allocated
     std::unordered_map<uint64_t, uint32_t> shape_cache;   // plan signature -> (cs << 16) | tile_n
     unsigned long long wait_limit_ns = 4000000000ull;
     std::vector<TimingRec> trec;
@@ -119,6 +125,8 @@ void free_handle(lora_linear* h) {
         for (cudaEvent_t e : r.ev) h->ev_pool.push_back(e);
     for (cudaEvent_t e : h->ev_pool) cudaEventDestroy(e);
     if (h->u_ws) cudaFree(h->u_ws);
+    if (h->partials) cudaFree(h->partials);
+    if (h->split_ctr) cudaFree(h->split_ctr);
     if (h->status) cudaFree(h->status);
     if (h->flags) cudaFree(h->flags);
     if (h->status_host) cudaFreeHost(h->status_host);
@@ -206,14 +214,15 @@ CUresult encode_plain_2d(lora_linear* h, CUtensorMap* m, CUtensorMapDataType dty
 
 // Output-tile width: the per-SM critical path is (waves x (tile_n + fixed cost)); narrow
 // tiles only where the row count is small enough that the pass streams W from memory.
-int choose_tile_n(const lora_linear* h, int n_fused, int n_groups, int slots) {
+int choose_tile_n(const lora_linear* h, int n_fused, int n_groups, int slots, int k_split = 1) {
     if (h->force_tile_n) return h->force_tile_n;
     const bool small_batch = (long long)n_fused * kTileM <= 384;
     long long best_cost = -1;
     int best = kMaxTileN;
     for (int tn = kMaxTileN; tn >= 16; tn -= 16) {
         if (!small_batch && tn < 128) break;
-        long long units = (long long)n_groups * ceil_div(h->d_out, tn);
+        // with K halves every output block is two units of half the K-steps
+        long long units = (long long)n_groups * ceil_div(h->d_out, tn) * k_split;
         long long waves = (units + slots - 1) / slots;
         long long cost = waves * (tn + 16);
         if (best_cost < 0 || cost < best_cost) {
@@ -319,21 +328,71 @@ double kstep_cycles(int cs, int n) {
 
 // Makespan (per-SM cycles) of the persistent round-robin schedule of one launch shape.
 double makespan(const lora_linear* h, const std::vector<Tile>& fused_groups, const std::vector<Tile>& shrink_groups,
-                int cs, int tile_n, int shrink_n, int slots) {
+                int cs, int tile_n, int shrink_n, int slots, int k_split = 1) {
     const int k_main = ceil_div(h->d_in, kTileK), k_lora = ceil_div(h->rank, kTileK);
     const int n_ntiles = ceil_div(h->d_out, tile_n);
     const int nsg = (int)shrink_groups.size() / cs, nfg = (int)fused_groups.size() / cs;
+    const double ks = kstep_cycles(cs, tile_n);
     const double c_shrink = k_main * kstep_cycles(cs, shrink_n);
-    const double c_base = k_main * kstep_cycles(cs, tile_n), c_lora = k_lora * kstep_cycles(cs, tile_n);
+    const double c_lora = k_lora * ks;
+    // K halves: two units per output block; each pays about two K-steps more for the fp32
+    // partial sums one half stores and the other reads back
+    const int k0 = k_split > 1 ? ceil_div(k_main, 2) : k_main;
+    const double c_half0 = k0 * ks + (k_split > 1 ? 2 * ks : 0.0), c_half1 = (k_main - k0 + 2) * ks;
     std::vector<double> load(slots, 0.0);
     long long u = 0;
-    for (int g = 0; g < nsg; ++g, ++u) load[u % slots] += c_shrink;
+    for (int g = 0; g < nsg; ++g) {
+        if (k_split > 1) {
+            const double sk = c_shrink / k_main;
+            load[u++ % slots] += (k0 + 2) * sk;
+            load[u++ % slots] += (k_main - k0 + 2) * sk;
+        } else {
+            load[u++ % slots] += c_shrink;
+        }
+    }
     // fused units in the kernel's order do not change the per-slot sums by much; use row-major
     for (int g = 0; g < nfg; ++g) {
-        const double c = c_base + (fused_groups[(size_t)g * cs].adapter ? c_lora : 0.0);
-        for (int t = 0; t < n_ntiles; ++t, ++u) load[u % slots] += c;
+        const double lora = fused_groups[(size_t)g * cs].adapter ? c_lora : 0.0;
+        for (int t = 0; t < n_ntiles; ++t) {
+            load[u++ % slots] += c_half0 + (k_split > 1 ? 0.0 : lora);
+            if (k_split > 1) load[u++ % slots] += c_half1 + lora;
+        }
     }
     return *std::max_element(load.begin(), load.end());
+}
+
+// The launch shape (SM pair or single CTA, output-tile width) the makespan model expects to
+// finish a plan soonest with K in `k_split` parts; cs / tn nonzero fix that choice. Returns the
+// expected makespan.
+double search_shape(const lora_linear* h, const Plan& plan, int cs, int tn, int k_split, int* out_cs, int* out_tn) {
+    const int nf = (int)plan.fused.size();
+    const int shrink_n = ceil_div(h->rank, 16) * 16;
+    const bool small_batch = (long long)nf * kTileM <= 384;
+    if (small_batch && !cs) cs = 1;
+    double best = -1;
+    int best_cs = cs ? cs : 1, best_tn = tn ? tn : kMaxTileN;
+    for (int c = 1; c <= 2; ++c) {
+        if (cs && c != cs) continue;
+        if (c == 2 && nf < 2) continue;
+        std::vector<Tile> fg, sg;
+        make_groups(plan.fused, c, false, h->u_rows - kTileM, &fg);
+        make_groups(plan.shrink, c, true, h->u_rows - kTileM, &sg);
+        const int slots = h->num_sms / c;
+        if (small_batch) {
+            const int t = tn ? tn : choose_tile_n(h, nf, (int)fg.size() / c, slots, k_split);
+            const double m = makespan(h, fg, sg, c, t, shrink_n, slots, k_split);
+            if (best < 0 || m < best) { best = m; best_cs = c; best_tn = t; }
+            continue;
+        }
+        for (int t = kMaxTileN; t >= 128; t -= 16) {
+            if (tn && t != tn) continue;
+            const double m = makespan(h, fg, sg, c, t, shrink_n, slots, k_split);
+            if (best < 0 || m < best * 0.999) { best = m; best_cs = c; best_tn = t; }
+        }
+    }
+    *out_cs = best_cs;
+    *out_tn = best_tn;
+    return best;
 }
 
 Shape choose_shape(lora_linear* h, const Plan& plan) {
@@ -343,40 +402,20 @@ Shape choose_shape(lora_linear* h, const Plan& plan) {
     sh.bk = h->tile_k ? h->tile_k : 64;
     const bool small_batch = (long long)nf * kTileM <= 384;
     int cs = h->cluster, tn = h->force_tile_n;
+    // K halves: whole 256-column blocks (narrower ones gained nothing where halves were measured)
+    if (h->k_split > 1 && !small_batch && !tn) tn = kMaxTileN;
     if (!cs || !tn) {
         if (small_batch && !cs) cs = 1;
         // plan signature: tile count and each tile's adapter / row count
         uint64_t key = 1469598103934665603ull ^ (uint64_t)nf;
         for (const Tile& t : plan.fused) key = (key ^ (uint64_t)(t.adapter * 131 + t.nrows)) * 1099511628211ull;
-        key ^= ((uint64_t)cs << 56) ^ ((uint64_t)tn << 40);
+        key ^= ((uint64_t)cs << 56) ^ ((uint64_t)tn << 40) ^ ((uint64_t)h->k_split << 32);
         auto it = h->shape_cache.find(key);
         if (it != h->shape_cache.end()) {
             cs = (int)(it->second >> 16);
             tn = (int)(it->second & 0xFFFF);
         } else {
-            double best = -1;
-            int best_cs = 1, best_tn = kMaxTileN;
-            for (int c = 1; c <= 2; ++c) {
-                if (cs && c != cs) continue;
-                if (c == 2 && nf < 2) continue;
-                std::vector<Tile> fg, sg;
-                make_groups(plan.fused, c, false, h->u_rows - kTileM, &fg);
-                make_groups(plan.shrink, c, true, h->u_rows - kTileM, &sg);
-                const int slots = h->num_sms / c;
-                if (small_batch) {
-                    const int t = tn ? tn : choose_tile_n(h, nf, (int)fg.size() / c, slots);
-                    const double m = makespan(h, fg, sg, c, t, sh.shrink_n, slots);
-                    if (best < 0 || m < best) { best = m; best_cs = c; best_tn = t; }
-                    continue;
-                }
-                for (int t = kMaxTileN; t >= 128; t -= 16) {
-                    if (tn && t != tn) continue;
-                    const double m = makespan(h, fg, sg, c, t, sh.shrink_n, slots);
-                    if (best < 0 || m < best * 0.999) { best = m; best_cs = c; best_tn = t; }
-                }
-            }
-            cs = best_cs;
-            tn = best_tn;
+            search_shape(h, plan, cs, tn, h->k_split, &cs, &tn);
             if (h->shape_cache.size() > 256) h->shape_cache.clear();
             h->shape_cache[key] = ((uint32_t)cs << 16) | (uint32_t)tn;
         }
@@ -396,6 +435,50 @@ Shape choose_shape(lora_linear* h, const Plan& plan) {
     sh.m_fastest = choose_m_fastest(h, nfg, sh.n_ntiles, sh.tile_n, kTileM * sh.cs, slots);
     sh.raster_group = h->raster == 3 ? h->raster_group : ceil_div(sh.n_ntiles, 2);
     return sh;
+}
+
+// K halves for a handle, decided once from its shape and max_tokens, so that every call on the
+// handle sums each output the same way (a row's bits never depend on the batch it is in). Two
+// halves when the handle serves small batches (the single-CTA path: at most three 128-row tiles)
+// of a projection with long K (at least 96 K-steps of 64, d_in >= 6,144) and the launch-shape
+// model expects them to finish at least 7% sooner: each SM then streams half of K over twice as
+// many column blocks. Measured on 48-row batches: the o projection (6,144 -> 5,120) 1.3x and the
+// down projection (17,408 -> 5,120) 2x faster, qkv (5,120 -> 12,288) no faster. Past the
+// small-batch path the round trip of the fp32 partial sums through L2 cancels what the halves
+// gain in the last wave (2,048 rows: o +4%, down -4%, qkv -12%), so whole K stays.
+int choose_k_split(lora_linear* h) {
+    if (h->k_split_opt) return h->k_split_opt;
+    if (ceil_div(h->d_in, kTileK) < 96) return 1;
+    const int32_t off[2] = {0, h->max_tokens}, ids[1] = {0};
+    Plan plan;
+    if (plan_segments(off, ids, 1, h->max_tokens, -1, &plan) != LORA_OK) return 1;
+    if ((long long)plan.fused.size() * kTileM > 384) return 1;
+    int cs = 0, tn = 0;
+    const double whole = search_shape(h, plan, 0, 0, 1, &cs, &tn);
+    const double halves = search_shape(h, plan, 0, 0, 2, &cs, &tn);
+    return halves < 0.93 * whole ? 2 : 1;
+}
+
+// Device buffers of the K halves (fp32 partial sums and the per-block counters), allocated when
+// the handle first splits K.
+int ensure_split_buffers(lora_linear* h) {
+    if (h->k_split < 2 || h->partials) return LORA_OK;
+    // float4 chunks of Y's columns, then of U's; counter pairs: (fused tile, column tile), then
+    // shrink tiles (SM-pair padding included)
+    const size_t chunks = (size_t)ceil_div(h->d_out, 4) + (size_t)ceil_div(h->rank, 4);
+    const size_t slots = (size_t)std::min(h->max_fused, h->max_tokens) * ceil_div(h->d_out, 16) + 2 * (size_t)h->max_fused;
+    if (cudaMalloc((void**)&h->partials, chunks * (size_t)h->max_tokens * sizeof(float4)) != cudaSuccess ||
+        cudaMalloc((void**)&h->split_ctr, 2 * slots * sizeof(int)) != cudaSuccess) {
+        cudaGetLastError();
+        if (h->partials) cudaFree(h->partials);
+        h->partials = nullptr;
+        h->split_ctr = nullptr;
+        return LORA_ENOMEM;
+    }
+    if (cudaMemset(h->split_ctr, 0, 2 * slots * sizeof(int)) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess)
+        return LORA_ECUDA;
+    h->split_slots = slots;
+    return LORA_OK;
 }
 
 // Launch shape of the 4-bit kernel for a call's token groups (host logic only).
@@ -546,6 +629,7 @@ int lora_linear_create(lora_linear** out, int d_in, int d_out, int rank, int max
 
     h->u_rows = ceil_div(max_tokens, kTileM) * kTileM + kTileM;
     h->max_fused = ceil_div(max_tokens, kTileM) + max_segments + 1;
+    h->k_split = choose_k_split(h);
     h->slot_bytes = align_up(2 * (size_t)max_segments * sizeof(CUtensorMap), 128) +
                     4 * (size_t)h->max_fused * sizeof(Tile) +
                     align_up(4 * (2 * (size_t)max_segments + 1), 16) +
@@ -572,6 +656,11 @@ int lora_linear_create(lora_linear** out, int d_in, int d_out, int rank, int max
             free_handle(h);
             return LORA_ECUDA;
         }
+    }
+    rc = ensure_split_buffers(h);
+    if (rc != LORA_OK) {
+        free_handle(h);
+        return rc;
     }
     if (cudaMemset(h->status, 0, sizeof(int)) != cudaSuccess ||
         cudaMemset(h->flags, 0, sizeof(int) * ((size_t)h->max_fused + 1)) != cudaSuccess ||
@@ -647,6 +736,19 @@ int lora_linear_set_option(lora_linear* h, int option, long long value) {
             if (value < 0 || value > 2) return LORA_EINVAL;
             h->cluster = (int)value;
             return LORA_OK;
+        case LORA_OPT_K_SPLIT: {
+            if (value < 0 || value > 2) return LORA_EINVAL;
+            DeviceGuard guard(h->device);
+            const int prev_opt = h->k_split_opt, prev = h->k_split;
+            h->k_split_opt = (int)value;
+            h->k_split = choose_k_split(h);
+            const int rc = ensure_split_buffers(h);
+            if (rc != LORA_OK) {
+                h->k_split_opt = prev_opt;
+                h->k_split = prev;
+            }
+            return rc;
+        }
         default:
             return LORA_EINVAL;
     }
@@ -696,7 +798,8 @@ int lora_linear_describe(lora_linear* h, int T, const int32_t* seg_offsets,
     int units = 0, tn = 0, st = 0, g = 0;
     if (nf) {
         Shape sh = choose_shape(h, plan);
-        units = (int)(sh.fused_groups.size() / sh.cs) * sh.n_ntiles + (int)(sh.shrink_groups.size() / sh.cs);
+        units = ((int)(sh.fused_groups.size() / sh.cs) * sh.n_ntiles + (int)(sh.shrink_groups.size() / sh.cs)) *
+                h->k_split;
         tn = sh.tile_n;
         st = sh.stages;
         int slots = h->num_sms;
@@ -755,7 +858,7 @@ int forward_impl(lora_linear* h, const void* x, int T, const int32_t* seg_offset
     for (Tile& t : plan.shrink) t.adapter = compact[t.adapter];
     for (int32_t& a : plan.seg_id) a = compact[a];
 
-    for (size_t i = 0; i < plan.fused.size(); ++i) plan.fused[i].fused_index = (int32_t)i;
+    for (size_t i = 0; i < plan.fused.size(); ++i) plan.fused[i].fused_index = plan.fused[i].split_index = (int32_t)i;
 
     DeviceGuard guard(h->device);
     const bool w4 = Wq != nullptr;
@@ -921,12 +1024,29 @@ int forward_impl(lora_linear* h, const void* x, int T, const int32_t* seg_offset
     p.cluster_size = cs;
     p.debug_stall = h->debug_stall;
     p.debug_publish_delay_ns = h->debug_publish_delay_ns;
+    // K halves (bf16 base): every fused output block runs as two units; the split point is set
+    // in 64-wide K-steps, so that it does not move with the K-step width of the stages
+    const int k_split = (!w4 && h->k_split > 1) ? 2 : 1;
+    if (k_split > 1) {
+        if (!h->partials || (size_t)nf * sh.n_ntiles + nst > h->split_slots || T > h->max_tokens) return LORA_ENOMEM;
+        p.k_split = 2;
+        p.k_chunk = ceil_div(ceil_div(h->d_in, 64), 2) * 64 / bk;
+        if (p.k_chunk < 1 || p.k_chunk >= p.k_main_blocks) return LORA_EINVAL;
+        p.partials = h->partials;
+        p.part_rows = h->max_tokens;
+        p.split_ctr = h->split_ctr;
+        p.shrink_slot0 = nf * sh.n_ntiles;
+        p.n_split_slots = nf * sh.n_ntiles + nst;
+        p.u_chunk0 = ceil_div(h->d_out, 4);
+        p.done_count = h->flags + h->max_fused;
+    }
     const int slots = cs > 1 ? max_clusters(h, p) : h->num_sms;
     if (slots < 1) return LORA_ECUDA;
     // every tile the kernel will decode names a valid adapter slot and flag slot: the kernel
     // indexes tensor maps and flags with them, so a malformed list must never reach it
     for (const Tile& t : sh.fused_groups)
         if (t.adapter < 0 || t.adapter > n_used || t.fused_index < 0 || t.fused_index >= nf ||
+            t.split_index < 0 || t.split_index >= nf ||
             t.row0 < 0 || t.nrows < 0 || t.row0 + t.nrows > T ||
             (t.adapter && t.u_row != t.row0 && t.u_row != h->u_rows - kTileM))
             return LORA_EINVAL;
@@ -943,7 +1063,8 @@ int forward_impl(lora_linear* h, const void* x, int T, const int32_t* seg_offset
         }
         cudaEventRecord(rec.ev[0], stream);
     }
-    const int fused_units = nfg * sh.n_ntiles;
+    const int fused_units = nfg * sh.n_ntiles * k_split;
+    const int shrink_units = nsg * k_split;
     if (w4) {
         // shrink (bf16 kernel), then base + expand on the 4-bit kernel, ordered by the stream
         if (nsg > 0) {
@@ -986,7 +1107,7 @@ int forward_impl(lora_linear* h, const void* x, int T, const int32_t* seg_offset
         // shrink, then fused base+expand ordered by the stream
         GemmParams s = p;
         s.n_fused = 0;
-        if (launch_gemm(s, std::min(nsg, slots) * cs, stream) != cudaSuccess) return LORA_ECUDA;
+        if (launch_gemm(s, std::min(shrink_units, slots) * cs, stream) != cudaSuccess) return LORA_ECUDA;
         ++h->launches;
         rec.has_shrink = true;
         if (timing) cudaEventRecord(rec.ev[1], stream);
@@ -1002,7 +1123,7 @@ int forward_impl(lora_linear* h, const void* x, int T, const int32_t* seg_offset
             p.done_count = h->flags + h->max_fused;
             p.n_flags = nf;
         }
-        if (launch_gemm(p, std::min(nsg + fused_units, slots) * cs, stream) != cudaSuccess) return LORA_ECUDA;
+        if (launch_gemm(p, std::min(shrink_units + fused_units, slots) * cs, stream) != cudaSuccess) return LORA_ECUDA;
         ++h->launches;
     }
     if (timing) {
@@ -1246,7 +1367,8 @@ int lora_linear_shape(int d_in, int d_out, int rank, int num_sms, int T, const i
     h.max_tokens = std::max(T, 1);
     h.num_sms = num_sms;
     h.u_rows = ceil_div(h.max_tokens, kTileM) * kTileM + kTileM;
-    for (size_t i = 0; i < plan.fused.size(); ++i) plan.fused[i].fused_index = (int32_t)i;
+    if (!w4) h.k_split = choose_k_split(&h);   // a handle of max_tokens = T
+    for (size_t i = 0; i < plan.fused.size(); ++i) plan.fused[i].fused_index = plan.fused[i].split_index = (int32_t)i;
     const Shape sh = choose_shape(&h, plan);
     if (w4) {
         // the 4-bit kernel over token groups; the shrink runs as the bf16 kernel's shrink units
@@ -1266,8 +1388,25 @@ int lora_linear_shape(int d_in, int d_out, int rank, int num_sms, int T, const i
     if (bk) *bk = sh.bk;
     if (stages) *stages = sh.stages;
     if (unit_order) *unit_order = sh.m_fastest;   // 0, 1, 2 as documented
-    if (fused_units) *fused_units = (int)(sh.fused_groups.size() / sh.cs) * sh.n_ntiles;
-    if (shrink_units) *shrink_units = (int)(sh.shrink_groups.size() / sh.cs);
+    if (fused_units) *fused_units = (int)(sh.fused_groups.size() / sh.cs) * sh.n_ntiles * h.k_split;
+    if (shrink_units) *shrink_units = (int)(sh.shrink_groups.size() / sh.cs) * h.k_split;
+    return LORA_OK;
+}
+
+int lora_linear_k_split(int d_in, int d_out, int rank, int max_tokens, int num_sms, int* k_split) {
+    if (!k_split) return LORA_EINVAL;
+    *k_split = 0;
+    if (num_sms < 2) return LORA_EINVAL;
+    int rc = check_shape(d_in, d_out, rank, max_tokens, 1);
+    if (rc != LORA_OK) return rc;
+    lora_linear h;
+    h.d_in = d_in;
+    h.d_out = d_out;
+    h.rank = rank;
+    h.max_tokens = max_tokens;
+    h.num_sms = num_sms;
+    h.u_rows = ceil_div(max_tokens, kTileM) * kTileM + kTileM;
+    *k_split = choose_k_split(&h);
     return LORA_OK;
 }
 

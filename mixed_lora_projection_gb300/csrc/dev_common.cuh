@@ -286,6 +286,17 @@ __device__ __forceinline__ void fence_proxy_async_global() {
 __device__ __forceinline__ void epilogue_bar_sync() {
     asm volatile("bar.sync 1, %0;" ::"n"(kEpilogueThreads) : "memory");
 }
+// The same named barrier of the four epilogue warps, also ANDing a predicate over them.
+__device__ __forceinline__ int epilogue_bar_and(int v) {
+    int r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 q, %1, 0;\n\t"
+        "bar.red.and.pred p, 1, %2, q;\n\tselp.b32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"(v), "n"(kEpilogueThreads)
+        : "memory");
+    return r;
+}
 // Waits until *flag == value (bounded like wait_bounded).
 static __device__ __noinline__ bool wait_flag(const int* flag, int value, volatile int* abort_flag, int* status,
                                        uint64_t limit_ns) {

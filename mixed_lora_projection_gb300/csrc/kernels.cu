@@ -63,7 +63,12 @@ struct Unit {
     int tile_index;  // ready-flag slot
     int n0;          // first output column
     int n;           // MMA N of this unit
-    int nk;          // k-blocks
+    int nk;          // k-blocks (base K-steps of this unit, then the expand's)
+    int kb0;         // first base K-step
+    int kmain;       // base K-steps of this unit
+    int half;        // K half when the launch splits K (0 or 1), else 0
+    int slot;        // K halves: this block's counter pair
+    int pchunk;      // K halves: float4 column chunk of the block's first column in `partials`
 };
 
 // The work list of a launch, in global memory or in the kernel parameters.
@@ -104,15 +109,24 @@ __device__ __forceinline__ WorkList resolve_work_list(const GemmParams& p) {
 __device__ __forceinline__ Unit decode_unit(const GemmParams& p, const WorkList& wl, int u, int rank) {
     Unit r;
     const int cs = p.cluster_size;
-    if (u < p.n_shrink) {
-        r.tile = wl.shrink[u * cs + rank];
+    // with K halves every block (shrink or fused) is two consecutive units, one per half of the
+    // base K-steps; the expand's K-steps go with the second half
+    const bool split = p.k_split > 1;
+    const int v0 = split ? u >> 1 : u;
+    r.half = split ? u & 1 : 0;
+    r.kb0 = r.half ? p.k_chunk : 0;
+    r.kmain = split ? (r.half ? p.k_main_blocks - p.k_chunk : p.k_chunk) : p.k_main_blocks;
+    if (v0 < p.n_shrink) {
+        r.tile = wl.shrink[v0 * cs + rank];
         r.shrink = 1;
         r.tile_index = r.tile.fused_index;
         r.n0 = 0;
         r.n = p.shrink_n;
-        r.nk = p.k_main_blocks;
+        r.nk = r.kmain;
+        r.slot = p.shrink_slot0 + v0 * cs + rank;
+        r.pchunk = p.u_chunk0;
     } else {
-        const int v = u - p.n_shrink;
+        const int v = v0 - p.n_shrink;
         int ti, nt;
         if (p.m_fastest == 2) {
             // column-tile groups of raster_group: all row tiles of a group, then the next group
@@ -130,7 +144,9 @@ __device__ __forceinline__ Unit decode_unit(const GemmParams& p, const WorkList&
         r.tile_index = r.tile.fused_index;
         r.n0 = nt * p.tile_n;
         r.n = p.tile_n;
-        r.nk = p.k_main_blocks + (r.tile.adapter ? p.k_lora_blocks : 0);
+        r.nk = r.kmain + ((r.tile.adapter && (!split || r.half)) ? p.k_lora_blocks : 0);
+        r.slot = r.tile.split_index * p.n_ntiles + nt;
+        r.pchunk = r.n0 >> 2;
     }
     return r;
 }
@@ -186,7 +202,7 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    const int n_units = p.n_shrink + p.n_fused * p.n_ntiles;
+    const int n_units = (p.n_shrink + p.n_fused * p.n_ntiles) * (p.k_split > 1 ? 2 : 1);
     const uint64_t limit = p.wait_limit_ns;
     const WorkList wl = resolve_work_list(p);
 
@@ -226,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
                 // bytes the (even CTA's) full barrier receives per stage, from the whole group
                 const uint32_t tx = CG * (kStageA + (uint32_t)half * BK * 2);
                 for (int kb = 0; kb < w.nk; ++kb) {
-                    if (kb == p.k_main_blocks && p.flags) {
+                    if (kb == w.kmain && p.flags) {
                         // the expand reads U rows written by this tile's shrink unit
                         int fok = 1;
                         if (lane == 0) fok = wait_flag(&p.flags[w.tile_index], 1, abort_flag, p.status, limit);
@@ -241,12 +257,12 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
                         break;
                     }
                     const uint32_t fb_local = smem_addr(&full[stage]);
-                    const bool main = kb < p.k_main_blocks;
+                    const bool main = kb < w.kmain;
                     mbar_arrive_expect_tx(fb_local, tx, leader ? issuer : 0u);
                     const uint32_t fb = CG > 1 ? map_to_rank(fb_local, 0) : fb_local;
                     const uint32_t sa = smem_addr(a_ring + (size_t)stage * kStageA);
                     const uint32_t sb = smem_addr(b_ring + (size_t)stage * b_stage_bytes);
-                    const int k = main ? kb * BK : (kb - p.k_main_blocks) * BK;
+                    const int k = main ? (w.kb0 + kb) * BK : (kb - w.kmain) * BK;
                     tma_load_2d<CG>(sa, main ? &p.tm_x : &p.tm_u, fb, k, main ? w.tile.row0 : w.tile.u_row, issuer);
                     tma_load_2d<CG>(sb, main ? bmain : &wl.tm_b[ad - 1], fb, k, w.n0 + rank * half, issuer);
                     ++issued;
@@ -339,6 +355,10 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
         const int q = warp & 3;                      // TMEM lane quadrant this warp may read
         const int r_local = q * 32 + lane;           // tile row held by this thread
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+        // with K halves the four epilogue warps meet at named barriers in every unit: they first
+        // agree on going on, so that none waits at a barrier for a warp that has left
+        const bool split_launch = p.k_split > 1;
+        volatile int* ticket = abort_flag + 1;       // this unit's K-half role, shared by the warps
         int it = 0;
         for (int u = group; u < n_units; u += n_groups, ++it) {
             const Unit w = decode_unit(p, wl, u, rank);
@@ -347,8 +367,27 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
             if (lane == 0)
                 ok = wait_bounded(smem_addr(&tfull[acc]), (it >> 1) & 1, abort_flag, p.status, limit, true);
             ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (split_launch) ok = epilogue_bar_and(ok);
             if (!ok) break;
             tc_fence_after();
+            // K halves: the half that arrives first stores its fp32 sums; the other waits until
+            // they are stored and adds them to its own (the same sum in either order)
+            const bool split = split_launch && w.tile.nrows > 0;
+            bool first = false;
+            int* ctr = nullptr;
+            if (split) {
+                ctr = p.split_ctr + 2 * (size_t)w.slot;
+                if (warp == 2 && lane == 0) {
+                    const int old = atomicAdd(ctr, 1);
+                    int wok = 1;
+                    if (old != 0) wok = wait_flag(ctr + 1, 1, abort_flag, p.status, limit);
+                    *ticket = (old == 0 ? 1 : 0) | (wok ? 0 : 2);
+                }
+                epilogue_bar_sync();
+                const int tk = *ticket;
+                if (tk & 2) break;                   // the wait ran out: the CTA is aborting
+                first = (tk & 1) != 0;
+            }
             const int row = w.tile.row0 + r_local;
             const bool row_ok = r_local < w.tile.nrows;
             float scale = 1.0f;
@@ -364,13 +403,40 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
                 n_out = p.d_out - w.n0;
             }
             const uint32_t taddr = tmem_base + (uint32_t)(acc * kAccCols) + lane_off;
+            // partial sums of this row: float4 chunk j (columns n0 + 4j ..) at part[j * part_rows]
+            float4* part = split ? p.partials + (size_t)w.pchunk * p.part_rows + row : nullptr;
             for (int c = 0; c < w.n; c += 32) {
                 uint32_t v[32];
                 const bool two = c + 16 < w.n;  // w.n is a multiple of 16
                 tmem_ld16(taddr + (uint32_t)c, v);
                 if (two) tmem_ld16(taddr + (uint32_t)c + 16, v + 16);
                 tmem_ld_wait();
-                if (row_ok) {
+                if (row_ok && split) {
+                    if (first) {
+                        float4* pc = part + (size_t)(c >> 2) * p.part_rows;
+#pragma unroll
+                        for (int h = 0; h < 8; ++h)
+                            if ((h < 4 || two) && c + 4 * h < n_out)
+                                __stcg(pc + (size_t)h * p.part_rows,
+                                       make_float4(__uint_as_float(v[4 * h]), __uint_as_float(v[4 * h + 1]),
+                                                   __uint_as_float(v[4 * h + 2]), __uint_as_float(v[4 * h + 3])));
+                    } else {
+                        // all eight loads of the chunk in flight at once (addresses past the
+                        // block's last column are clamped to it; those sums are never stored)
+                        const int last = (n_out - 1) >> 2;
+                        float4 o[8];
+#pragma unroll
+                        for (int h = 0; h < 8; ++h) o[h] = __ldcg(part + (size_t)min((c >> 2) + h, last) * p.part_rows);
+#pragma unroll
+                        for (int h = 0; h < 8; ++h) {
+                            v[4 * h] = __float_as_uint(__uint_as_float(v[4 * h]) + o[h].x);
+                            v[4 * h + 1] = __float_as_uint(__uint_as_float(v[4 * h + 1]) + o[h].y);
+                            v[4 * h + 2] = __float_as_uint(__uint_as_float(v[4 * h + 2]) + o[h].z);
+                            v[4 * h + 3] = __float_as_uint(__uint_as_float(v[4 * h + 3]) + o[h].w);
+                        }
+                    }
+                }
+                if (row_ok && !first) {
 #pragma unroll
                     for (int h = 0; h < 4; ++h) {
                         if ((h < 2 || two) && c + 8 * h < n_out) {
@@ -389,8 +455,15 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
                 mbar_arrive_cluster(map_to_rank(smem_addr(&tempty[acc]), 0));  // the even CTA's barrier
             else
                 mbar_arrive(smem_addr(&tempty[acc]));
-            if (w.shrink && p.flags && w.tile_index >= 0) {
-                // publish this tile's U rows to the fused units that wait for them
+            if (first) {
+                // every thread's partial sums are stored before the other half may read them
+                __threadfence();
+                epilogue_bar_sync();
+                if (warp == 2 && lane == 0) st_release(ctr + 1, 1);
+            }
+            if (w.shrink && p.flags && w.tile_index >= 0 && !first) {
+                // publish this tile's U rows to the fused units that wait for them (with K
+                // halves, the half that stored them)
                 fence_proxy_async_global();
                 epilogue_bar_sync();
                 if (warp == 2 && lane == 0) {
@@ -414,11 +487,11 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
         tc_fence_after();
         tmem_dealloc<CG>(tmem_base, 2 * kAccCols);
     }
-    if (p.flags) {
-        // The last CTA of the launch to get here clears the ready flags and the exit counter:
-        // every CTA counts itself in only after all of its flag reads, so none is still
-        // waiting, and the next launch on the stream (a replay of a captured graph included)
-        // starts from zero.
+    if (p.flags || p.split_ctr) {
+        // The last CTA of the launch to get here clears the ready flags, the K-half counters and
+        // the exit counter: every CTA counts itself in only after all of its flag and counter
+        // reads, so none is still waiting, and the next launch on the stream (a replay of a
+        // captured graph included) starts from zero.
         int last = 0;
         if (threadIdx.x == 0) {
             __threadfence();
@@ -427,7 +500,10 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
         last = __syncthreads_or(last);
         if (last) {
             __threadfence();
-            for (int i = threadIdx.x; i < p.n_flags; i += blockDim.x) p.flags[i] = 0;
+            if (p.flags)
+                for (int i = threadIdx.x; i < p.n_flags; i += blockDim.x) p.flags[i] = 0;
+            if (p.split_ctr)
+                for (int i = threadIdx.x; i < 2 * p.n_split_slots; i += blockDim.x) p.split_ctr[i] = 0;
             if (threadIdx.x == 0) *p.done_count = 0;
         }
     }

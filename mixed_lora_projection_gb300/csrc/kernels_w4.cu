@@ -65,17 +65,6 @@ __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bu
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 // generic-proxy shared-memory writes made visible to the async proxy (the TMA store that follows)
 __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-// named barrier of the four epilogue warps that also ANDs a predicate over them
-__device__ __forceinline__ int epilogue_bar_and(int v) {
-    int r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 q, %1, 0;\n\t"
-        "bar.red.and.pred p, 1, %2, q;\n\tselp.b32 %0, 1, 0, p;\n\t}"
-        : "=r"(r)
-        : "r"(v), "n"(kEpilogueThreads)
-        : "memory");
-    return r;
-}
 
 // D[tmem] (+)= A[tmem] * B[smem]^T, kind::f16 (bf16 in, fp32 accumulate), issued by the lane
 // with pred != 0 of a converged warp.

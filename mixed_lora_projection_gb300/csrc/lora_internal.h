@@ -31,6 +31,8 @@ struct Tile {                        // one planner tile, as uploaded to the dev
     int32_t u_row;                   // first U row the expand reads (fused tiles): row0, or a
                                      // block of U that is always zero for a base tile that shares
                                      // an SM pair (and so the pair's expand) with an adapter tile
+    int32_t split_index;             // fused tiles: this tile's own index among the fused tiles
+                                     // (its K-half counters; unlike fused_index, never a partner's)
 };
 
 // Parameters of one launch of the tile GEMM. Passed by value as a __grid_constant__.
@@ -42,6 +44,10 @@ struct Tile {                        // one planner tile, as uploaded to the dev
 // tile's rows and the pair runs M = 256 MMAs. Groups are padded with tiles of nrows 0.
 // When `flags` is set, a fused unit's expand waits until flags[tile] == 1, which the shrink
 // unit of that tile publishes after its U rows are stored (single-launch mode).
+// With k_split == 2 every unit (shrink or fused) is split into two units over the two halves of
+// the base K-steps (the expand goes with the second half): the unit that finishes first stores
+// its fp32 partial sums, the other adds them to its own (fp32 addition is commutative, so the sum
+// does not depend on which half finishes first) and stores Y (or U, and publishes its flag).
 struct GemmParams {
     // inline work list (used when inline_wl != 0): adapter tensor maps (B_a at [0, 4), A_a
     // at [4, 8)), tiles (fused then shrink), merged segments (offsets then ids), scales
@@ -89,6 +95,18 @@ struct GemmParams {
                                      // of 16) for a batch of one tile on single CTAs
     int debug_stall;
     unsigned long long debug_publish_delay_ns;   // tests: shrink units publish their flag this late
+    // K halves (k_split == 2; 0 or 1 = whole K per unit)
+    int k_split;
+    int k_chunk;                     // base K-steps of the first half: ceil(k_main_blocks / 2)
+    float4* partials;                // fp32 partial sums of the first-finished half: float4 chunk c
+                                     // (output columns 4c .. 4c+3) of row t at [c * part_rows + t]
+    int part_rows;                   // row stride of `partials` (>= T)
+    int* split_ctr;                  // per (fused tile, column tile): {halves arrived, partials stored};
+                                     // zero at launch, cleared at exit by the last CTA
+    int n_split_slots;               // counter pairs in use: fused tiles x column tiles, then the
+                                     // shrink tiles (padding included) from shrink_slot0
+    int shrink_slot0;
+    int u_chunk0;                    // float4 chunk of U's column 0 in `partials` (after Y's chunks)
 };
 
 // The plan of one call: merged segments and tiles, ids remapped to compact adapter slots.

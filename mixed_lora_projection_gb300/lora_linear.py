@@ -89,6 +89,15 @@ def launch_shape(d_in, d_out, rank, num_sms, T, seg_offsets, seg_ids, w4=False) 
                     [x.value for x in v]))
 
 
+def k_split(d_in, d_out, rank, max_tokens, num_sms) -> int:
+    """The K split (1 or 2) a handle of this shape and max_tokens chooses at create on a GPU
+    with ``num_sms`` SMs, computed by the library on the host alone."""
+    lib = L.load()
+    v = C.c_int()
+    _check(lib.lora_linear_k_split(d_in, d_out, rank, max_tokens, num_sms, C.byref(v)), "lora_linear_k_split")
+    return v.value
+
+
 def host_chunks(T) -> list:
     """Row bounds of the chunks ``forward_host`` runs T rows in (0 first, T last)."""
     lib = L.load()

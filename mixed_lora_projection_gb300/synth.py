@@ -109,11 +109,21 @@ def sweep_workload(proj: str, multi_adapter: bool = False) -> Workload:
                     note="2048-token batch, half adapter rows in 3 segments, half base rows")
 
 
+def decode_workload(proj: str) -> Workload:
+    """One decode step of six chats (8 rows each: a seven-token draft block and one token, no
+    adapter) through one projection of the adapted stack."""
+    d_in, d_out = {p: (i, o) for p, i, o in SWEEP_PROJECTIONS}[proj]
+    off, ids = _segs([8] * 6, [0] * 6)
+    return Workload(f"decode_{proj}", 8, 48, d_in, d_out, 256, off, ids,
+                    note="6 chats x 8 decode/draft rows (no adapter) through one projection")
+
+
 WORKLOADS = {w.name: w for w in (_TINY, _PREFILL_16K, _MIXED, _MIXED_DECODE, _PREFILL_32K, _NEAR_RIDGE,
                                   _CONCURRENT_8, _PREFIX_TAIL)}
 for _p, _, _ in SWEEP_PROJECTIONS:
     WORKLOADS[f"sweep_{_p}"] = sweep_workload(_p)
     WORKLOADS[f"sweep_{_p}_multi"] = sweep_workload(_p, True)
+    WORKLOADS[f"decode_{_p}"] = decode_workload(_p)
 
 
 def seed_for(w: Workload, tensor_index: int, layer: int = 0, proj_index: int = 0) -> int:

@@ -171,6 +171,11 @@ SHAPES = {
     "mixed_near_ridge": (1, 240, None), "sweep_qkv": (2, 224, None), "sweep_o": (2, 192, None),
     "sweep_gate_up": (2, 256, None), "sweep_down": (2, 192, None),
 }
+# K halves chosen by a handle of max_tokens = the workload's rows: none of the configured
+# workloads (their batches are past the small-batch path, or their K is 5,120)
+K_SPLITS = {"sweep_o": 1, "sweep_down": 1, "sweep_qkv": 1, "sweep_gate_up": 1, "prefill_16k": 1, "prefill_32k": 1,
+            "mixed_batch": 1, "mixed_decode": 1, "mixed_near_ridge": 1, "mixed_8x300": 1, "prefix_tail_1552": 1,
+            "tiny": 1}
 
 
 @pytest.mark.parametrize("name", sorted(SHAPES))
@@ -190,6 +195,40 @@ def test_launch_shape_model_choices(lib, name):
     assert s["fused_units"] >= groups * -(-w.d_out // tile_n) - 1
     assert (s["shrink_units"] == 0) == (w.adapter_rows == 0)
     assert s["bk"] == 64 and 2 <= s["stages"] <= 16
+
+
+@pytest.mark.parametrize("name", sorted(K_SPLITS))
+def test_k_split_choices(lib, name):
+    from mixed_lora_projection_gb300 import k_split, launch_shape
+    from mixed_lora_projection_gb300.synth import WORKLOADS
+    w = WORKLOADS[name]
+    ks = k_split(w.d_in, w.d_out, w.rank, w.T, 152)
+    assert ks == K_SPLITS[name]
+    # with halves every block is two units: the shape model's unit counts are even
+    s = launch_shape(w.d_in, w.d_out, w.rank, 152, w.T, w.seg_offsets, w.seg_ids)
+    if ks == 2:
+        assert s["fused_units"] % 2 == 0 and s["shrink_units"] % 2 == 0 and s["tile_n"] == 256
+
+
+def test_k_split_rule(lib):
+    from mixed_lora_projection_gb300 import LoraError, k_split, launch_shape
+    # decode-sized handles on narrow projections with long K split (o 6,144 and down 17,408 ->
+    # 5,120); K of 5,120 never does, nor do handles whose batches pass the small-batch path
+    for d_in in (6144, 17408):
+        for T in (1, 8, 48, 200, 384):
+            assert k_split(d_in, 5120, 256, T, 152) == 2, (d_in, T)
+        for T in (385, 2048, 32768):
+            assert k_split(d_in, 5120, 256, T, 152) == 1, (d_in, T)
+    for d_out in (5120, 12288, 34816):
+        assert k_split(5120, d_out, 256, 48, 152) == 1
+    assert k_split(6080, 5120, 256, 48, 152) == 1        # 95 K-steps of 64
+    # a split handle's units come in pairs
+    s = launch_shape(6144, 5120, 256, 152, 48, [0, 48], [0])
+    assert s["fused_units"] % 2 == 0 and s["fused_units"] >= 2 * 5120 // s["tile_n"]
+    with pytest.raises(LoraError):
+        k_split(6144, 5120, 256, 48, 1)          # fewer than 2 SMs
+    with pytest.raises(LoraError):
+        k_split(6144, 5120, 300, 48, 152)        # rank above 256
 
 
 def test_launch_shape_of_an_empty_batch_and_bad_arguments(lib):

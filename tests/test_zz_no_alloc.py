@@ -66,8 +66,9 @@ def _limit_workload():
 
 
 def _handle_forward(w, inp):
-    from mixed_lora_projection_gb300 import LoraLinear
+    from mixed_lora_projection_gb300 import LoraLinear, _lib as L
     with LoraLinear(w.d_in, w.d_out, w.rank, w.T, len(w.seg_ids), 0) as ll:
+        ll.set_option(L.OPT_K_SPLIT, 1)   # whole K per block, as the allocation-free entry point sums
         y = ll.forward(inp.x, w.seg_offsets, w.seg_ids, inp.w, inp.a, inp.b, inp.scales)
         torch.cuda.synchronize()
         assert ll.status() == 0
