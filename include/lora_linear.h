@@ -238,12 +238,15 @@ enum {
                                    pairs, 1 for single CTAs), 1 or 2 */
     LORA_OPT_DEBUG_PUBLISH_DELAY_US = 13, /* tests only: each shrink unit of a one-launch call publishes
                                    its U rows this many microseconds late (0..1,000,000; default 0) */
-    LORA_OPT_K_SPLIT = 14       /* bf16 base: 0 = the handle's own choice (made at create), 1 = whole K
+    LORA_OPT_K_SPLIT = 14,      /* bf16 base: 0 = the handle's own choice (made at create), 1 = whole K
                                    per output block, 2 = two K halves: each output block runs as two
                                    work units whose fp32 sums are added (one stores its partial sums, the
                                    other adds them) before the bf16 rounding; fills the GPU when long-K,
                                    narrow projections leave too few or too ragged waves of blocks.
                                    Changes the summation for later calls; may allocate (LORA_ENOMEM) */
+    LORA_OPT_MAX_CTAS = 15      /* at most this many CTAs (one per SM) per launch, >= 2; 0 = every SM (default).
+                                   Leaves the other SMs to calls on other streams; the launch shape is chosen
+                                   for the SMs it may use. Does not change any result */
 };
 
 /* lora_linear_set_option -- set one option above. Returns LORA_OK or LORA_EINVAL. */

@@ -80,6 +80,7 @@ struct lora_linear {
     int force_tile_n = 0, raster = 0, debug_stall = 0, timing = 0, two_launch = 0, cluster = 0;
     unsigned long long debug_publish_delay_ns = 0;
     int raster_group = 4, tile_k = 0, allow_inline = 1, mma_group = 0;  // 0: 2 for SM pairs, else 1
+    int max_ctas = 0;           // LORA_OPT_MAX_CTAS: at most this many CTAs per launch (0 = one per SM)
     int max_clusters_cache[2][kMaxTileN / 16 + 1] = {};  // co-resident clusters by (size, B rows)
     // K halves: chosen once per handle (every call on it sums each output the same way)
     int k_split = 1;            // 1, or 2: every fused unit runs as two units over the K halves
@@ -210,6 +211,12 @@ CUresult encode_plain_2d(lora_linear* h, CUtensorMap* m, CUtensorMapDataType dty
     cuuint32_t estr[2] = {1, 1};
     return h->encode(m, dtype, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                      CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+// SMs a launch of this handle may use: all of them, or LORA_OPT_MAX_CTAS of them (so that
+// calls on other streams can run beside it on the rest).
+int usable_sms(const lora_linear* h) {
+    return h->max_ctas > 0 ? std::min(h->num_sms, h->max_ctas) : h->num_sms;
 }
 
 // Output-tile width: the per-SM critical path is (waves x (tile_n + fixed cost)); narrow
@@ -377,7 +384,7 @@ double search_shape(const lora_linear* h, const Plan& plan, int cs, int tn, int 
         std::vector<Tile> fg, sg;
         make_groups(plan.fused, c, false, h->u_rows - kTileM, &fg);
         make_groups(plan.shrink, c, true, h->u_rows - kTileM, &sg);
-        const int slots = h->num_sms / c;
+        const int slots = usable_sms(h) / c;
         if (small_batch) {
             const int t = tn ? tn : choose_tile_n(h, nf, (int)fg.size() / c, slots, k_split);
             const double m = makespan(h, fg, sg, c, t, shrink_n, slots, k_split);
@@ -424,7 +431,7 @@ Shape choose_shape(lora_linear* h, const Plan& plan) {
     make_groups(plan.fused, sh.cs, false, h->u_rows - kTileM, &sh.fused_groups);
     make_groups(plan.shrink, sh.cs, true, h->u_rows - kTileM, &sh.shrink_groups);
     const int nfg = (int)sh.fused_groups.size() / sh.cs;
-    const int slots = h->num_sms / sh.cs;
+    const int slots = usable_sms(h) / sh.cs;
     sh.tile_n = tn;
     sh.n_ntiles = ceil_div(h->d_out, sh.tile_n);
     // a batch of one tile of fewer than 128 rows (a decode step) on single CTAs loads only its
@@ -736,6 +743,11 @@ int lora_linear_set_option(lora_linear* h, int option, long long value) {
             if (value < 0 || value > 2) return LORA_EINVAL;
             h->cluster = (int)value;
             return LORA_OK;
+        case LORA_OPT_MAX_CTAS:
+            if (value < 0 || value > (1 << 20) || (value > 0 && value < 2)) return LORA_EINVAL;
+            h->max_ctas = (int)value;
+            h->shape_cache.clear();
+            return LORA_OK;
         case LORA_OPT_K_SPLIT: {
             if (value < 0 || value > 2) return LORA_EINVAL;
             DeviceGuard guard(h->device);
@@ -802,7 +814,7 @@ int lora_linear_describe(lora_linear* h, int T, const int32_t* seg_offsets,
                 h->k_split;
         tn = sh.tile_n;
         st = sh.stages;
-        int slots = h->num_sms;
+        int slots = usable_sms(h);
         if (sh.cs > 1) {
             GemmParams q;
             memset(&q, 0, sizeof(q));
@@ -812,7 +824,7 @@ int lora_linear_describe(lora_linear* h, int T, const int32_t* seg_offsets,
             q.cluster_size = sh.cs;
             q.bk = sh.bk;
             DeviceGuard guard(h->device);
-            slots = max_clusters(h, q);
+            slots = std::min(max_clusters(h, q), usable_sms(h) / sh.cs);
         }
         g = std::min(units, slots) * sh.cs;
     }
@@ -1040,7 +1052,7 @@ int forward_impl(lora_linear* h, const void* x, int T, const int32_t* seg_offset
         p.u_chunk0 = ceil_div(h->d_out, 4);
         p.done_count = h->flags + h->max_fused;
     }
-    const int slots = cs > 1 ? max_clusters(h, p) : h->num_sms;
+    const int slots = cs > 1 ? std::min(max_clusters(h, p), usable_sms(h) / cs) : usable_sms(h);
     if (slots < 1) return LORA_ECUDA;
     // every tile the kernel will decode names a valid adapter slot and flag slot: the kernel
     // indexes tensor maps and flags with them, so a malformed list must never reach it
@@ -1101,7 +1113,7 @@ int forward_impl(lora_linear* h, const void* x, int T, const int32_t* seg_offset
             return LORA_ECUDA;
         q.debug_stall = h->debug_stall;
         const int units = q.n_groups * q.n_ntiles;
-        if (launch_w4(q, std::min(units, h->num_sms), stream) != cudaSuccess) return LORA_ECUDA;
+        if (launch_w4(q, std::min(units, usable_sms(h)), stream) != cudaSuccess) return LORA_ECUDA;
         ++h->launches;
     } else if (h->two_launch && nsg > 0) {
         // shrink, then fused base+expand ordered by the stream

@@ -127,3 +127,54 @@ def test_host_shape_model_equals_the_device_handle(dev, name):
         d = ll.describe(w.T, w.seg_offsets, w.seg_ids)
     assert d["tile_n"] == host["tile_n"] and d["stages"] == host["stages"]
     assert d["n_units"] == host["fused_units"] + host["shrink_units"]
+
+
+def test_max_ctas_caps_the_grid_and_changes_no_bit(dev):
+    # a launch capped to fewer SMs (SM pairs round down to whole pairs) computes the same bits
+    from mixed_lora_projection_gb300 import LoraError, _lib as L
+    from mixed_lora_projection_gb300.synth import WORKLOADS
+    w = WORKLOADS["sweep_o_multi"]
+    inp = make_inputs(w, dev)
+    off, ids = list(w.seg_offsets), list(w.seg_ids)
+    with _ll(w.d_in, w.d_out, w.rank, w.T, 16) as ll:
+        y0 = run(ll, inp, off, ids).clone()
+        ys = []
+        for cap in (40, 7):
+            ll.set_option(L.OPT_MAX_CTAS, cap)
+            assert ll.describe(w.T, off, ids)["grid"] <= cap
+            ys.append(run(ll, inp, off, ids).clone())
+        for bad in (1, -1):
+            with pytest.raises(LoraError):
+                ll.set_option(L.OPT_MAX_CTAS, bad)
+        torch.cuda.synchronize()
+        assert ll.status() == 0
+    assert all(torch.equal(y, y0) for y in ys)
+
+
+def test_two_calls_side_by_side_on_disjoint_sm_counts(dev):
+    # the near-ridge batch as one call, and as two calls on two streams capped to 100 and 52 SMs
+    # (rows 0-255 on SM pairs, the 92-row tail on single CTAs): the same bits
+    from mixed_lora_projection_gb300 import LoraLinear, _lib as L
+    from mixed_lora_projection_gb300.synth import WORKLOADS
+    w = WORKLOADS["mixed_near_ridge"]
+    inp = make_inputs(w, dev)
+    off, ids = list(w.seg_offsets), list(w.seg_ids)
+    y = torch.empty((w.T, w.d_out), dtype=torch.bfloat16, device=dev)
+    main = torch.cuda.current_stream(dev)
+    sa, sb = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    with LoraLinear(w.d_in, w.d_out, w.rank, w.T, 16, 0) as one, \
+            LoraLinear(w.d_in, w.d_out, w.rank, 256, 16, 0) as ha, LoraLinear(w.d_in, w.d_out, w.rank, 128, 16, 0) as hb:
+        ref = run(one, inp, off, ids).clone()
+        ha.set_option(L.OPT_CLUSTER, 2)
+        ha.set_option(L.OPT_MAX_CTAS, 100)
+        hb.set_option(L.OPT_MAX_CTAS, 52)
+        for _ in range(3):
+            sa.wait_stream(main)
+            sb.wait_stream(main)
+            ha.forward(inp.x[:256], off[:7] + [256], ids, inp.w, inp.a, inp.b, inp.scales, y=y[:256], stream=sa)
+            hb.forward(inp.x[256:], [0, w.T - 256], [1], inp.w, inp.a, inp.b, inp.scales, y=y[256:], stream=sb)
+            main.wait_stream(sa)
+            main.wait_stream(sb)
+        torch.cuda.synchronize()
+        assert ha.status() == 0 and hb.status() == 0
+    assert torch.equal(y, ref)
