@@ -318,7 +318,9 @@ int lora_linear_host_chunks(int T, int32_t* bounds, int* n);
  * n_seg <= LORA_NOALLOC_MAX_SEGMENTS, rank <= LORA_MAX_RANK; larger requests return
  * LORA_EINVAL and launch nothing.
  * Arguments are those of lora_linear_forward plus the shape (d_in, d_out, rank), with the
- * same layouts, alignment rules and checks; the caller still owns x, W, A, B and y.
+ * same layouts, alignment rules and checks; the caller still owns x, W, A, B and y. It sums
+ * each output over the whole of K in one unit, as a handle does with LORA_OPT_K_SPLIT = 1,
+ * and gives the same bits as such a handle.
  * The first call on a device looks up the scratch array's device address there
  * (cudaGetSymbolAddress) and sets the kernels' shared-memory limit; make that first call
  * before any stream capture. Every call shares the one scratch array and leaves its
