@@ -313,6 +313,8 @@ def run_ours(args, rank, world, dist):
                 handles[key].set_option(L.OPT_TWO_LAUNCH, 1)
             if args.k_split:
                 handles[key].set_option(L.OPT_K_SPLIT, args.k_split)
+            if args.pdl:
+                handles[key].set_option(L.OPT_PDL, 1)
             if args.raster:
                 mode, _, group = args.raster.partition(":")
                 handles[key].set_option(L.OPT_RASTER, int(mode))
@@ -468,6 +470,7 @@ def run_ours(args, rank, world, dist):
         "config": {"workload": args.workload + ("+w4" if args.w4 else ""),
                    **({"raster": args.raster} if args.raster else {}),
                    **({"k_split": args.k_split} if args.k_split else {}),
+                   **({"pdl": True} if args.pdl else {}),
                    "base": "int4 (symmetric, group 128, bf16 scales)" if args.w4 else "bf16", "T": w0.T, "d_in": w0.d_in if len(items) == 1 else "per projection",
                    "d_out": w0.d_out if len(items) == 1 else "per projection", "rank": w0.rank,
                    "segments": len(w0.seg_ids), "adapter_rows": w0.adapter_rows, "calls_per_step": len(items),
@@ -644,6 +647,8 @@ def main():
                     "1 row tiles first, 2 column tiles first, 3 groups of GROUP column tiles)")
     ap.add_argument("--k-split", type=int, default=0, choices=[0, 1, 2], help="K halves per output block (the "
                     "library's K-split option: 0 = each handle's own choice, 1 = whole K, 2 = two halves)")
+    ap.add_argument("--pdl", action="store_true", help="programmatic dependent launch for calls without adapter "
+                    "rows (the library's PDL option): each kernel may start while the previous one ends")
     ap.add_argument("--graph", action="store_true", help="time the steps as CUDA-graph replays (each call's "
                     "work list must travel in the kernel parameters, e.g. the 24-layer sweep)")
     args = ap.parse_args()

@@ -235,7 +235,7 @@ enum {
     LORA_OPT_INLINE_WORK_LIST = 11, /* 1 (default) = small work lists travel in the kernel parameters,
                                       0 = always upload them to device memory */
     LORA_OPT_MMA_GROUP = 12,    /* pipeline stages the MMA warp waits for at once: 0 = auto (2 for SM
-                                   pairs, 1 for single CTAs), 1 or 2 */
+                                   pairs and for batches of one tile, 1 otherwise), 1 or 2 */
     LORA_OPT_DEBUG_PUBLISH_DELAY_US = 13, /* tests only: each shrink unit of a one-launch call publishes
                                    its U rows this many microseconds late (0..1,000,000; default 0) */
     LORA_OPT_K_SPLIT = 14,      /* bf16 base: 0 = the handle's own choice (made at create), 1 = whole K
@@ -244,9 +244,15 @@ enum {
                                    other adds them) before the bf16 rounding; fills the GPU when long-K,
                                    narrow projections leave too few or too ragged waves of blocks.
                                    Changes the summation for later calls; may allocate (LORA_ENOMEM) */
-    LORA_OPT_MAX_CTAS = 15      /* at most this many CTAs (one per SM) per launch, >= 2; 0 = every SM (default).
+    LORA_OPT_MAX_CTAS = 15,     /* at most this many CTAs (one per SM) per launch, >= 2; 0 = every SM (default).
                                    Leaves the other SMs to calls on other streams; the launch shape is chosen
                                    for the SMs it may use. Does not change any result */
+    LORA_OPT_PDL = 16           /* 1 = programmatic dependent launch for calls without adapter rows (bf16 base,
+                                   one launch): the launch may start on SMs the previous kernel of the stream
+                                   leaves, requests its first W tiles, and waits for that kernel before it
+                                   reads or writes anything else; it lets the next kernel start early in turn.
+                                   The previous kernel must not write this call's W. 0 (default) = off.
+                                   Does not change any result */
 };
 
 /* lora_linear_set_option -- set one option above. Returns LORA_OK or LORA_EINVAL. */

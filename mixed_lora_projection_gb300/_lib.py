@@ -49,7 +49,7 @@ SIGNATURES = {
 LORA_OK, LORA_EINVAL, LORA_ENOMEM, LORA_ECUDA, LORA_ETIMEOUT, LORA_EUNSUPPORTED, LORA_ENODEV = 0, -1, -2, -3, -4, -5, -6
 (OPT_TILE_N, OPT_WAIT_LIMIT_US, OPT_DEBUG_STALL, OPT_TIMING, OPT_RASTER, OPT_TWO_LAUNCH, OPT_CLUSTER,
  OPT_RASTER_GROUP, _OPT_RETIRED_9, OPT_TILE_K, OPT_INLINE_WORK_LIST, OPT_MMA_GROUP,
- OPT_DEBUG_PUBLISH_DELAY_US, OPT_K_SPLIT, OPT_MAX_CTAS) = 1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 11, 12, 13, 14, 15
+ OPT_DEBUG_PUBLISH_DELAY_US, OPT_K_SPLIT, OPT_MAX_CTAS, OPT_PDL) = 1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 11, 12, 13, 14, 15, 16
 
 
 def load():

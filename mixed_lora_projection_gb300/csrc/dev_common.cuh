@@ -270,6 +270,18 @@ __device__ __forceinline__ int row_adapter(const int32_t* off, const int32_t* id
     return ids[lo];
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+// Lets the next kernel of the stream (launched with programmatic stream serialization) start
+// while this one finishes; a no-op when none is.
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Waits until the kernels this one depends on have completed and their writes are visible; returns
+// at once when this kernel was launched without a programmatic dependency.
+__device__ __forceinline__ void griddep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- cross-CTA flags
 __device__ __forceinline__ int ld_acquire(const int* p) {
     int v;

@@ -205,6 +205,8 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
     const int n_units = (p.n_shrink + p.n_fused * p.n_ntiles) * (p.k_split > 1 ? 2 : 1);
     const uint64_t limit = p.wait_limit_ns;
     const WorkList wl = resolve_work_list(p);
+    // the next call's kernel may start on the SMs this one leaves, and stream its first W tiles
+    if (p.pdl && threadIdx.x == 0) griddep_launch_dependents();
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
@@ -224,6 +226,28 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
             long long issued = 0;
             int acquired_a = -1, acquired_b = -1;  // adapters whose global tensor maps were acquired
             bool ok = true;
+            // Launched ahead of the previous kernel's end: the W tiles of the first unit's first
+            // ring stages (W is not written by that kernel) are requested before the wait, into
+            // stages that are free at the start; their X rows follow the wait.
+            int pre = 0;
+            if (p.pdl) {
+                if (group < n_units) {
+                    const Unit w0 = decode_unit(p, wl, group, rank);
+                    if (!w0.shrink) {
+                        const int half0 = w0.n / CG;
+                        const uint32_t tx0 = CG * (kStageA + (uint32_t)half0 * BK * 2);
+                        pre = w0.kmain < stages ? w0.kmain : stages;
+                        for (int kb = 0; kb < pre; ++kb) {
+                            const uint32_t fb_local = smem_addr(&full[kb]);
+                            mbar_arrive_expect_tx(fb_local, tx0, leader ? issuer : 0u);
+                            const uint32_t fb = CG > 1 ? map_to_rank(fb_local, 0) : fb_local;
+                            tma_load_2d<CG>(smem_addr(b_ring + (size_t)kb * b_stage_bytes), &p.tm_w, fb,
+                                            (w0.kb0 + kb) * BK, w0.n0 + rank * half0, issuer);
+                        }
+                    }
+                }
+                griddep_wait();
+            }
             for (int u = group; u < n_units && ok; u += n_groups) {
                 const Unit w = decode_unit(p, wl, u, rank);
                 const int ad = w.tile.adapter;
@@ -252,19 +276,22 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
                         }
                         fence_proxy_async_global();
                     }
-                    if (!wait_warp(smem_addr(&empty[stage]), phase ^ 1, abort_flag, p.status, limit)) {
+                    // a stage whose W tile went out before the dependency wait: armed and free
+                    const bool prefetched = issued < pre;
+                    if (!prefetched && !wait_warp(smem_addr(&empty[stage]), phase ^ 1, abort_flag, p.status, limit)) {
                         ok = false;
                         break;
                     }
                     const uint32_t fb_local = smem_addr(&full[stage]);
                     const bool main = kb < w.kmain;
-                    mbar_arrive_expect_tx(fb_local, tx, leader ? issuer : 0u);
+                    if (!prefetched) mbar_arrive_expect_tx(fb_local, tx, leader ? issuer : 0u);
                     const uint32_t fb = CG > 1 ? map_to_rank(fb_local, 0) : fb_local;
                     const uint32_t sa = smem_addr(a_ring + (size_t)stage * kStageA);
                     const uint32_t sb = smem_addr(b_ring + (size_t)stage * b_stage_bytes);
                     const int k = main ? (w.kb0 + kb) * BK : (kb - w.kmain) * BK;
                     tma_load_2d<CG>(sa, main ? &p.tm_x : &p.tm_u, fb, k, main ? w.tile.row0 : w.tile.u_row, issuer);
-                    tma_load_2d<CG>(sb, main ? bmain : &wl.tm_b[ad - 1], fb, k, w.n0 + rank * half, issuer);
+                    if (!prefetched)
+                        tma_load_2d<CG>(sb, main ? bmain : &wl.tm_b[ad - 1], fb, k, w.n0 + rank * half, issuer);
                     ++issued;
                     if (++stage == stages) { stage = 0; phase ^= 1; }
                 }
@@ -291,6 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
         // ------------------------------------------------------------ MMA issuer (even CTA)
         // The whole warp runs the loop (converged); lane 0 issues the MMAs and commits.
         const uint32_t issuer = lane == 0 ? 1u : 0u;
+        if (p.pdl) griddep_wait();
         if (leader) {
             int stage = 0;
             uint32_t phase = 0;
@@ -359,6 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
         // agree on going on, so that none waits at a barrier for a warp that has left
         const bool split_launch = p.k_split > 1;
         volatile int* ticket = abort_flag + 1;       // this unit's K-half role, shared by the warps
+        if (p.pdl) griddep_wait();                   // global reads and writes follow the previous kernel
         int it = 0;
         for (int u = group; u < n_units; u += n_groups, ++it) {
             const Unit w = decode_unit(p, wl, u, rank);
@@ -568,7 +597,7 @@ static bool cooperative_launches() {
 }
 
 static void launch_config(const GemmParams& p, int grid, cudaStream_t stream, cudaLaunchConfig_t* cfg,
-                          cudaLaunchAttribute* attr /* [2] */) {
+                          cudaLaunchAttribute* attr /* [3] */) {
     const int b_rows = (p.tile_n > p.shrink_n ? p.tile_n : p.shrink_n) / p.cluster_size;
     *cfg = cudaLaunchConfig_t{};
     cfg->gridDim = dim3(grid, 1, 1);
@@ -588,6 +617,12 @@ static void launch_config(const GemmParams& p, int grid, cudaStream_t stream, cu
         attr[1].id = cudaLaunchAttributeCooperative;
         attr[1].val.cooperative = 1;
         cfg->numAttrs = 2;
+    } else if (p.pdl) {
+        // may start while the previous kernel of the stream finishes (it waits for it before
+        // touching anything but W)
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
+        cfg->numAttrs = 2;
     }
 }
 
@@ -602,14 +637,14 @@ static cudaError_t dispatch(const GemmParams& p, F&& f) {
 
 cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t stream) {
     cudaLaunchConfig_t cfg;
-    cudaLaunchAttribute attr[2];
+    cudaLaunchAttribute attr[3];
     launch_config(p, grid, stream, &cfg, attr);
     return dispatch(p, [&](auto kernel) { return cudaLaunchKernelEx(&cfg, kernel, p); });
 }
 
 int gemm_max_clusters(const GemmParams& p) {
     cudaLaunchConfig_t cfg;
-    cudaLaunchAttribute attr[2];
+    cudaLaunchAttribute attr[3];
     launch_config(p, p.cluster_size, nullptr, &cfg, attr);
     int n = 0;
     cudaError_t e = dispatch(p, [&](auto kernel) { return cudaOccupancyMaxActiveClusters(&n, kernel, &cfg); });

@@ -107,6 +107,10 @@ struct GemmParams {
                                      // shrink tiles (padding included) from shrink_slot0
     int shrink_slot0;
     int u_chunk0;                    // float4 chunk of U's column 0 in `partials` (after Y's chunks)
+    // Programmatic dependent launch: the launch may start before the previous kernel of the stream
+    // ends; only the W tiles of its first unit's first ring stages are loaded before it waits for
+    // that kernel, and it lets the next kernel start early in turn
+    int pdl;
 };
 
 // The plan of one call: merged segments and tiles, ids remapped to compact adapter slots.

@@ -8,7 +8,7 @@ expand that did not wait would read the previous call's U rows and give wrong ou
 import pytest
 import torch
 
-from mixed_lora_projection_gb300.synth import WORKLOADS, make_inputs
+from mixed_lora_projection_gb300.synth import WORKLOADS, Workload, make_inputs
 
 from gpu_util import TOL, oracle_rows, rel_err, run, sample_rows
 
@@ -196,3 +196,49 @@ def test_two_handles_on_two_streams(dev):
         torch.cuda.synchronize()
         assert l1.status() == 0 and l2.status() == 0
     assert all(torch.equal(y, r1) for y in y1) and all(torch.equal(y, r2) for y in y2)
+
+
+def test_programmatic_dependent_launch_keeps_every_dependency(dev):
+    # a chain in which every call reads the previous call's Y as its X, through two handles
+    # (5,120 -> 6,144 and back; the second splits K in halves for these 48-row batches): with
+    # LORA_OPT_PDL each kernel starts on the SMs the previous one leaves, requests its first W
+    # tiles and waits for it before anything else, so every output equals the chain run without
+    # it, eagerly and replayed from a CUDA graph
+    from mixed_lora_projection_gb300 import LoraLinear, _lib as L
+    T = 48
+    wa = Workload("pdl_a", 21, T, 5120, 6144, 16, (0, T), (0,))
+    wb = Workload("pdl_b", 22, T, 6144, 5120, 16, (0, T), (0,))
+    ia, ib = make_inputs(wa, dev), make_inputs(wb, dev)
+    x0 = ia.x.clone()
+    with LoraLinear(5120, 6144, 16, T, 8, 0) as ha, LoraLinear(6144, 5120, 16, T, 8, 0) as hb:
+        def chain(pdl, outs):
+            for h in (ha, hb):
+                h.set_option(L.OPT_PDL, pdl)
+            x = x0
+            for i in range(6):
+                h, inp = (ha, ia) if i % 2 == 0 else (hb, ib)
+                x = h.forward(x, [0, T], [0], inp.w, inp.a, inp.b, inp.scales, y=outs[i])
+            return outs
+        shapes = [(T, 6144) if i % 2 == 0 else (T, 5120) for i in range(6)]
+        ref = chain(0, [torch.empty(s, dtype=torch.bfloat16, device=dev) for s in shapes])
+        ref = [y.clone() for y in ref]
+        eager = chain(1, [torch.empty(s, dtype=torch.bfloat16, device=dev) for s in shapes])
+        torch.cuda.synchronize()
+        assert all(torch.equal(a, b) for a, b in zip(ref, eager))
+        bufs = [torch.zeros(s, dtype=torch.bfloat16, device=dev) for s in shapes]
+        s = torch.cuda.Stream(dev)
+        s.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(s):
+            chain(1, bufs)
+        torch.cuda.current_stream(dev).wait_stream(s)
+        torch.cuda.synchronize()
+        for b in bufs:
+            b.zero_()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            chain(1, bufs)
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        assert all(torch.equal(a, b) for a, b in zip(ref, bufs))
+        assert ha.status() == 0 and hb.status() == 0
