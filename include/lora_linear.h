@@ -19,7 +19,7 @@
  * rounded from fp32 to bf16 (round to nearest even). The summation order is not
  * specified, so results are not bitwise equal to any other implementation; on one handle a
  * row's output does not depend on the other rows of its batch (the same bits in any batch,
- * launch shape or host-buffer chunking). A handle may sum the base product in two K halves
+ * launch shape or host-buffer chunking). A handle may sum the base product in parts of K
  * (LORA_OPT_K_SPLIT); it decides that once, at create, from its shape and max_tokens, so two
  * handles of one shape but different max_tokens may differ in the last bit.
  *
@@ -238,12 +238,14 @@ enum {
                                    pairs and for batches of one tile, 1 otherwise), 1 or 2 */
     LORA_OPT_DEBUG_PUBLISH_DELAY_US = 13, /* tests only: each shrink unit of a one-launch call publishes
                                    its U rows this many microseconds late (0..1,000,000; default 0) */
-    LORA_OPT_K_SPLIT = 14,      /* bf16 base: 0 = the handle's own choice (made at create), 1 = whole K
-                                   per output block, 2 = two K halves: each output block runs as two
-                                   work units whose fp32 sums are added (one stores its partial sums, the
-                                   other adds them) before the bf16 rounding; fills the GPU when long-K,
-                                   narrow projections leave too few or too ragged waves of blocks.
-                                   Changes the summation for later calls; may allocate (LORA_ENOMEM) */
+    LORA_OPT_K_SPLIT = 14,      /* bf16 base: 0 = the handle's own choice (made at create), 1 = whole K per
+                                   output block, 2 or 4 = K in that many parts: each block runs as that many
+                                   work units; every part but the last to finish stores its fp32 sums, the
+                                   last adds all of them in part order before the bf16 rounding (the same sum
+                                   whichever part ends last). Fills the GPU when long-K, narrow projections
+                                   leave too few or too ragged waves of blocks; fewer parts are used where K
+                                   is too short for every part to get a 64-wide K-step. Changes the
+                                   summation for later calls; may allocate (LORA_ENOMEM) */
     LORA_OPT_MAX_CTAS = 15,     /* at most this many CTAs (one per SM) per launch, >= 2; 0 = every SM (default).
                                    Leaves the other SMs to calls on other streams; the launch shape is chosen
                                    for the SMs it may use. Does not change any result */
@@ -294,7 +296,7 @@ int lora_linear_shape(int d_in, int d_out, int rank, int num_sms, int T, const i
                       int* stages, int* unit_order, int* fused_units, int* shrink_units);
 
 /*
- * lora_linear_k_split -- the K split (1 or 2, see LORA_OPT_K_SPLIT) a handle of this shape
+ * lora_linear_k_split -- the K parts (1 or 2, see LORA_OPT_K_SPLIT) a handle of this shape
  * and max_tokens would choose at create on a GPU with num_sms SMs, computed on the host alone.
  * Returns LORA_OK or LORA_EINVAL. Diagnostics and tests.
  */

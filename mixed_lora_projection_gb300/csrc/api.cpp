@@ -84,9 +84,11 @@ struct lora_linear {
     int pdl = 0;                // LORA_OPT_PDL: launches without ready flags may start early
     int max_clusters_cache[2][kMaxTileN / 16 + 1] = {};  // co-resident clusters by (size, B rows)
     // K halves: chosen once per handle (every call on it sums each output the same way)
-    int k_split = 1;            // 1, or 2: every fused unit runs as two units over the K halves
-    int k_split_opt = 0;        // LORA_OPT_K_SPLIT: 0 = the handle's own choice, 1 or 2 = forced
-    float4* partials = nullptr; // fp32 partial sums, ceil(d_out / 4) float4 chunks x max_tokens rows
+    int k_split = 1;            // 1, 2 or 4: every block runs as that many units over parts of K
+    int k_split_opt = 0;        // LORA_OPT_K_SPLIT: 0 = the handle's own choice, 1, 2 or 4 = forced
+    float4* partials = nullptr; // fp32 partial sums: per K part, the float4 chunks of Y's and U's
+                                // columns x max_tokens rows
+    int partial_parts = 0;      // K parts `partials` has room for
     int* split_ctr = nullptr;   // per (fused tile, column tile): halves arrived, partials stored
     size_t split_slots = 0;     // counter pairs allocated
     std::unordered_map<uint64_t, uint32_t> shape_cache;   // plan signature -> (cs << 16) | tile_n
@@ -343,28 +345,26 @@ double makespan(const lora_linear* h, const std::vector<Tile>& fused_groups, con
     const double ks = kstep_cycles(cs, tile_n);
     const double c_shrink = k_main * kstep_cycles(cs, shrink_n);
     const double c_lora = k_lora * ks;
-    // K halves: two units per output block; each pays about two K-steps more for the fp32
-    // partial sums one half stores and the other reads back
-    const int k0 = k_split > 1 ? ceil_div(k_main, 2) : k_main;
-    const double c_half0 = k0 * ks + (k_split > 1 ? 2 * ks : 0.0), c_half1 = (k_main - k0 + 2) * ks;
+    // K parts: S units per block over k_chunk K-steps each (the last one the rest); with parts,
+    // each unit pays about two K-steps more for the fp32 partial sums stored and read back
+    const int S = k_split > 1 ? k_split : 1;
+    const int k_chunk = ceil_div(k_main, S), extra = S > 1 ? 2 : 0;
     std::vector<double> load(slots, 0.0);
     long long u = 0;
-    for (int g = 0; g < nsg; ++g) {
-        if (k_split > 1) {
-            const double sk = c_shrink / k_main;
-            load[u++ % slots] += (k0 + 2) * sk;
-            load[u++ % slots] += (k_main - k0 + 2) * sk;
-        } else {
-            load[u++ % slots] += c_shrink;
+    const double sk = c_shrink / k_main;
+    for (int g = 0; g < nsg; ++g)
+        for (int q = 0; q < S; ++q) {
+            const int k = q == S - 1 ? k_main - (S - 1) * k_chunk : k_chunk;
+            load[u++ % slots] += (k + extra) * sk;
         }
-    }
     // fused units in the kernel's order do not change the per-slot sums by much; use row-major
     for (int g = 0; g < nfg; ++g) {
         const double lora = fused_groups[(size_t)g * cs].adapter ? c_lora : 0.0;
-        for (int t = 0; t < n_ntiles; ++t) {
-            load[u++ % slots] += c_half0 + (k_split > 1 ? 0.0 : lora);
-            if (k_split > 1) load[u++ % slots] += c_half1 + lora;
-        }
+        for (int t = 0; t < n_ntiles; ++t)
+            for (int q = 0; q < S; ++q) {
+                const int k = q == S - 1 ? k_main - (S - 1) * k_chunk : k_chunk;
+                load[u++ % slots] += (k + extra) * ks + (q == S - 1 ? lora : 0.0);
+            }
     }
     return *std::max_element(load.begin(), load.end());
 }
@@ -445,17 +445,26 @@ Shape choose_shape(lora_linear* h, const Plan& plan) {
     return sh;
 }
 
-// K halves for a handle, decided once from its shape and max_tokens, so that every call on the
-// handle sums each output the same way (a row's bits never depend on the batch it is in). Two
-// halves when the handle serves small batches (the single-CTA path: at most three 128-row tiles)
-// of a projection with long K (at least 96 K-steps of 64, d_in >= 6,144) and the launch-shape
-// model expects them to finish at least 7% sooner: each SM then streams half of K over twice as
-// many column blocks. Measured on 48-row batches: the o projection (6,144 -> 5,120) 1.3x and the
-// down projection (17,408 -> 5,120) 2x faster, qkv (5,120 -> 12,288) no faster. Past the
-// small-batch path the round trip of the fp32 partial sums through L2 cancels what the halves
-// gain in the last wave (2,048 rows: o +4%, down -4%, qkv -12%), so whole K stays.
+// K parts for a handle, decided once from its shape and max_tokens, so that every call on the
+// handle sums each output the same way (a row's bits never depend on the batch it is in). The
+// handle splits K in halves when it serves small batches (the single-CTA path: at most three
+// 128-row tiles) of a projection with long K (at least 96 K-steps of 64, d_in >= 6,144) and the
+// launch-shape model expects them to finish at least 7% sooner. Each SM then streams half of K
+// over twice as many column blocks. Measured on 48-row batches: the o projection (6,144 ->
+// 5,120) 1.3x and the down projection (17,408 -> 5,120) 2x faster with halves, qkv (5,120 ->
+// 12,288) no faster; quarters were no faster than halves (o 30.0 against 25.2 us, down 47.4
+// against 47.7 us: the last part reads three sets of partial sums), so the handle chooses them
+// only when asked (LORA_OPT_K_SPLIT = 4). Past the small-batch path the round trip of the fp32
+// partial sums through L2 cancels what the parts gain in the last wave (2,048 rows, halves: o
+// +4%, down -4%, qkv -12%), so whole K stays.
 int choose_k_split(lora_linear* h) {
-    if (h->k_split_opt) return h->k_split_opt;
+    if (h->k_split_opt) {
+        // as many parts as asked for, as long as every part keeps at least one K-step
+        const int k64 = ceil_div(h->d_in, kTileK);
+        int s = h->k_split_opt;
+        while (s > 1 && (s - 1) * ceil_div(k64, s) >= k64) s /= 2;
+        return s;
+    }
     if (ceil_div(h->d_in, kTileK) < 96) return 1;
     const int32_t off[2] = {0, h->max_tokens}, ids[1] = {0};
     Plan plan;
@@ -467,25 +476,34 @@ int choose_k_split(lora_linear* h) {
     return halves < 0.93 * whole ? 2 : 1;
 }
 
-// Device buffers of the K halves (fp32 partial sums and the per-block counters), allocated when
-// the handle first splits K.
+// Device buffers of the K parts (fp32 partial sums per part and the per-block counters),
+// allocated when the handle first splits K, and grown when it splits into more parts.
 int ensure_split_buffers(lora_linear* h) {
-    if (h->k_split < 2 || h->partials) return LORA_OK;
-    // float4 chunks of Y's columns, then of U's; counter pairs: (fused tile, column tile), then
-    // shrink tiles (SM-pair padding included)
+    if (h->k_split < 2 || h->partial_parts >= h->k_split) return LORA_OK;
+    // float4 chunks of Y's columns, then of U's, per part; counter pairs: (fused tile, column
+    // tile), then shrink tiles (SM-pair padding included)
     const size_t chunks = (size_t)ceil_div(h->d_out, 4) + (size_t)ceil_div(h->rank, 4);
     const size_t slots = (size_t)std::min(h->max_fused, h->max_tokens) * ceil_div(h->d_out, 16) + 2 * (size_t)h->max_fused;
-    if (cudaMalloc((void**)&h->partials, chunks * (size_t)h->max_tokens * sizeof(float4)) != cudaSuccess ||
-        cudaMalloc((void**)&h->split_ctr, 2 * slots * sizeof(int)) != cudaSuccess) {
+    if (h->partials) cudaFree(h->partials);
+    h->partials = nullptr;
+    h->partial_parts = 0;
+    if (cudaMalloc((void**)&h->partials, (size_t)h->k_split * chunks * (size_t)h->max_tokens * sizeof(float4)) !=
+        cudaSuccess) {
         cudaGetLastError();
-        if (h->partials) cudaFree(h->partials);
         h->partials = nullptr;
-        h->split_ctr = nullptr;
         return LORA_ENOMEM;
     }
-    if (cudaMemset(h->split_ctr, 0, 2 * slots * sizeof(int)) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess)
-        return LORA_ECUDA;
-    h->split_slots = slots;
+    h->partial_parts = h->k_split;
+    if (!h->split_ctr) {
+        if (cudaMalloc((void**)&h->split_ctr, 2 * slots * sizeof(int)) != cudaSuccess) {
+            cudaGetLastError();
+            h->split_ctr = nullptr;
+            return LORA_ENOMEM;
+        }
+        if (cudaMemset(h->split_ctr, 0, 2 * slots * sizeof(int)) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess)
+            return LORA_ECUDA;
+        h->split_slots = slots;
+    }
     return LORA_OK;
 }
 
@@ -754,7 +772,7 @@ int lora_linear_set_option(lora_linear* h, int option, long long value) {
             h->shape_cache.clear();
             return LORA_OK;
         case LORA_OPT_K_SPLIT: {
-            if (value < 0 || value > 2) return LORA_EINVAL;
+            if (value != 0 && value != 1 && value != 2 && value != 4) return LORA_EINVAL;
             DeviceGuard guard(h->device);
             const int prev_opt = h->k_split_opt, prev = h->k_split;
             h->k_split_opt = (int)value;
@@ -1045,14 +1063,19 @@ int forward_impl(lora_linear* h, const void* x, int T, const int32_t* seg_offset
     p.debug_publish_delay_ns = h->debug_publish_delay_ns;
     // K halves (bf16 base): every fused output block runs as two units; the split point is set
     // in 64-wide K-steps, so that it does not move with the K-step width of the stages
-    const int k_split = (!w4 && h->k_split > 1) ? 2 : 1;
+    // K parts (bf16 base): every block runs as k_split units; the part boundaries are set in
+    // 64-wide K-steps, so that they do not move with the K-step width of the stages
+    const int k_split = (!w4 && h->k_split > 1) ? h->k_split : 1;
     if (k_split > 1) {
-        if (!h->partials || (size_t)nf * sh.n_ntiles + nst > h->split_slots || T > h->max_tokens) return LORA_ENOMEM;
-        p.k_split = 2;
-        p.k_chunk = ceil_div(ceil_div(h->d_in, 64), 2) * 64 / bk;
-        if (p.k_chunk < 1 || p.k_chunk >= p.k_main_blocks) return LORA_EINVAL;
+        if (!h->partials || h->partial_parts < k_split || (size_t)nf * sh.n_ntiles + nst > h->split_slots ||
+            T > h->max_tokens)
+            return LORA_ENOMEM;
+        p.k_split = k_split;
+        p.k_chunk = ceil_div(ceil_div(h->d_in, 64), k_split) * 64 / bk;
+        if (p.k_chunk < 1 || (k_split - 1) * p.k_chunk >= p.k_main_blocks) return LORA_EINVAL;
         p.partials = h->partials;
         p.part_rows = h->max_tokens;
+        p.part_chunks = ceil_div(h->d_out, 4) + ceil_div(h->rank, 4);
         p.split_ctr = h->split_ctr;
         p.shrink_slot0 = nf * sh.n_ntiles;
         p.n_split_slots = nf * sh.n_ntiles + nst;

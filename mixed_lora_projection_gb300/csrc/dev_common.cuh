@@ -309,6 +309,22 @@ __device__ __forceinline__ int epilogue_bar_and(int v) {
         : "memory");
     return r;
 }
+// Waits until *counter >= value (bounded like wait_bounded).
+static __device__ __noinline__ bool wait_count(const int* counter, int value, volatile int* abort_flag, int* status,
+                                        uint64_t limit_ns) {
+    if (ld_acquire(counter) >= value) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        __nanosleep(64);
+        if (ld_acquire(counter) >= value) return true;
+        if (*abort_flag) return false;
+        if (global_timer_ns() - t0 > limit_ns) {
+            atomicOr(status, 1);
+            *abort_flag = 1;
+            return false;
+        }
+    }
+}
 // Waits until *flag == value (bounded like wait_bounded).
 static __device__ __noinline__ bool wait_flag(const int* flag, int value, volatile int* abort_flag, int* status,
                                        uint64_t limit_ns) {

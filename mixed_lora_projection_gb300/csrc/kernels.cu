@@ -66,9 +66,9 @@ struct Unit {
     int nk;          // k-blocks (base K-steps of this unit, then the expand's)
     int kb0;         // first base K-step
     int kmain;       // base K-steps of this unit
-    int half;        // K half when the launch splits K (0 or 1), else 0
-    int slot;        // K halves: this block's counter pair
-    int pchunk;      // K halves: float4 column chunk of the block's first column in `partials`
+    int part;        // K part when the launch splits K (0 .. k_split - 1), else 0
+    int slot;        // K parts: this block's counter pair
+    int pchunk;      // K parts: float4 column chunk of the block's first column in `partials`
 };
 
 // The work list of a launch, in global memory or in the kernel parameters.
@@ -109,13 +109,15 @@ __device__ __forceinline__ WorkList resolve_work_list(const GemmParams& p) {
 __device__ __forceinline__ Unit decode_unit(const GemmParams& p, const WorkList& wl, int u, int rank) {
     Unit r;
     const int cs = p.cluster_size;
-    // with K halves every block (shrink or fused) is two consecutive units, one per half of the
-    // base K-steps; the expand's K-steps go with the second half
-    const bool split = p.k_split > 1;
-    const int v0 = split ? u >> 1 : u;
-    r.half = split ? u & 1 : 0;
-    r.kb0 = r.half ? p.k_chunk : 0;
-    r.kmain = split ? (r.half ? p.k_main_blocks - p.k_chunk : p.k_chunk) : p.k_main_blocks;
+    // with K split into S parts every block (shrink or fused) is S consecutive units, one per
+    // part of the base K-steps (k_chunk each, the last one the rest); the expand's K-steps go with
+    // the last part
+    const int S = p.k_split > 1 ? p.k_split : 1;
+    const bool split = S > 1;
+    const int v0 = u / S;
+    r.part = u - v0 * S;
+    r.kb0 = r.part * p.k_chunk;
+    r.kmain = r.part == S - 1 ? p.k_main_blocks - r.kb0 : p.k_chunk;
     if (v0 < p.n_shrink) {
         r.tile = wl.shrink[v0 * cs + rank];
         r.shrink = 1;
@@ -144,7 +146,7 @@ __device__ __forceinline__ Unit decode_unit(const GemmParams& p, const WorkList&
         r.tile_index = r.tile.fused_index;
         r.n0 = nt * p.tile_n;
         r.n = p.tile_n;
-        r.nk = r.kmain + ((r.tile.adapter && (!split || r.half)) ? p.k_lora_blocks : 0);
+        r.nk = r.kmain + ((r.tile.adapter && r.part == S - 1) ? p.k_lora_blocks : 0);
         r.slot = r.tile.split_index * p.n_ntiles + nt;
         r.pchunk = r.n0 >> 2;
     }
@@ -202,7 +204,7 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    const int n_units = (p.n_shrink + p.n_fused * p.n_ntiles) * (p.k_split > 1 ? 2 : 1);
+    const int n_units = (p.n_shrink + p.n_fused * p.n_ntiles) * (p.k_split > 1 ? p.k_split : 1);
     const uint64_t limit = p.wait_limit_ns;
     const WorkList wl = resolve_work_list(p);
     // the next call's kernel may start on the SMs this one leaves, and stream its first W tiles
@@ -386,7 +388,8 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
         // with K halves the four epilogue warps meet at named barriers in every unit: they first
         // agree on going on, so that none waits at a barrier for a warp that has left
         const bool split_launch = p.k_split > 1;
-        volatile int* ticket = abort_flag + 1;       // this unit's K-half role, shared by the warps
+        const int n_parts = split_launch ? p.k_split : 1;
+        volatile int* ticket = abort_flag + 1;       // this unit's K-part role, shared by the warps
         if (p.pdl) griddep_wait();                   // global reads and writes follow the previous kernel
         int it = 0;
         for (int u = group; u < n_units; u += n_groups, ++it) {
@@ -399,18 +402,19 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
             if (split_launch) ok = epilogue_bar_and(ok);
             if (!ok) break;
             tc_fence_after();
-            // K halves: the half that arrives first stores its fp32 sums; the other waits until
-            // they are stored and adds them to its own (the same sum in either order)
+            // K parts: every part but the last to arrive stores its fp32 sums in its own slot; the
+            // last waits until all of them are stored and adds the S sums in part order (P0 + P1,
+            // then + P2, + P3), its own from registers: the same sum whichever part arrives last
             const bool split = split_launch && w.tile.nrows > 0;
-            bool first = false;
+            bool first = false;                      // this part stores its sums (not the last)
             int* ctr = nullptr;
             if (split) {
                 ctr = p.split_ctr + 2 * (size_t)w.slot;
                 if (warp == 2 && lane == 0) {
                     const int old = atomicAdd(ctr, 1);
                     int wok = 1;
-                    if (old != 0) wok = wait_flag(ctr + 1, 1, abort_flag, p.status, limit);
-                    *ticket = (old == 0 ? 1 : 0) | (wok ? 0 : 2);
+                    if (old == n_parts - 1) wok = wait_count(ctr + 1, n_parts - 1, abort_flag, p.status, limit);
+                    *ticket = (old < n_parts - 1 ? 1 : 0) | (wok ? 0 : 2);
                 }
                 epilogue_bar_sync();
                 const int tk = *ticket;
@@ -432,7 +436,9 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
                 n_out = p.d_out - w.n0;
             }
             const uint32_t taddr = tmem_base + (uint32_t)(acc * kAccCols) + lane_off;
-            // partial sums of this row: float4 chunk j (columns n0 + 4j ..) at part[j * part_rows]
+            // partial sums of this row: part q's float4 chunk j (columns n0 + 4j ..) at
+            // part_base[(q * part_chunks + j) * part_rows]
+            const size_t part_stride = (size_t)p.part_chunks * p.part_rows;    // one part's slot
             float4* part = split ? p.partials + (size_t)w.pchunk * p.part_rows + row : nullptr;
             for (int c = 0; c < w.n; c += 32) {
                 uint32_t v[32];
@@ -442,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
                 tmem_ld_wait();
                 if (row_ok && split) {
                     if (first) {
-                        float4* pc = part + (size_t)(c >> 2) * p.part_rows;
+                        float4* pc = part + (size_t)w.part * part_stride + (size_t)(c >> 2) * p.part_rows;
 #pragma unroll
                         for (int h = 0; h < 8; ++h)
                             if ((h < 4 || two) && c + 4 * h < n_out)
@@ -450,19 +456,35 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
                                        make_float4(__uint_as_float(v[4 * h]), __uint_as_float(v[4 * h + 1]),
                                                    __uint_as_float(v[4 * h + 2]), __uint_as_float(v[4 * h + 3])));
                     } else {
-                        // all eight loads of the chunk in flight at once (addresses past the
-                        // block's last column are clamped to it; those sums are never stored)
+                        // the sum in part order; each other part's eight loads of the chunk are in
+                        // flight at once (addresses past the block's last column are clamped to it;
+                        // those sums are never stored)
                         const int last = (n_out - 1) >> 2;
-                        float4 o[8];
+                        float acc[32];
+                        for (int q = 0; q < n_parts; ++q) {
+                            float t[32];
+                            if (q == w.part) {
 #pragma unroll
-                        for (int h = 0; h < 8; ++h) o[h] = __ldcg(part + (size_t)min((c >> 2) + h, last) * p.part_rows);
+                                for (int i = 0; i < 32; ++i) t[i] = __uint_as_float(v[i]);
+                            } else {
+                                const float4* pq = part + (size_t)q * part_stride;
+                                float4 o[8];
 #pragma unroll
-                        for (int h = 0; h < 8; ++h) {
-                            v[4 * h] = __float_as_uint(__uint_as_float(v[4 * h]) + o[h].x);
-                            v[4 * h + 1] = __float_as_uint(__uint_as_float(v[4 * h + 1]) + o[h].y);
-                            v[4 * h + 2] = __float_as_uint(__uint_as_float(v[4 * h + 2]) + o[h].z);
-                            v[4 * h + 3] = __float_as_uint(__uint_as_float(v[4 * h + 3]) + o[h].w);
+                                for (int h = 0; h < 8; ++h)
+                                    o[h] = __ldcg(pq + (size_t)min((c >> 2) + h, last) * p.part_rows);
+#pragma unroll
+                                for (int h = 0; h < 8; ++h) {
+                                    t[4 * h] = o[h].x;
+                                    t[4 * h + 1] = o[h].y;
+                                    t[4 * h + 2] = o[h].z;
+                                    t[4 * h + 3] = o[h].w;
+                                }
+                            }
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) acc[i] = q == 0 ? t[i] : acc[i] + t[i];
                         }
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(acc[i]);
                     }
                 }
                 if (row_ok && !first) {
@@ -485,14 +507,17 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
             else
                 mbar_arrive(smem_addr(&tempty[acc]));
             if (first) {
-                // every thread's partial sums are stored before the other half may read them
+                // every thread's partial sums are stored before the last part may read them
                 __threadfence();
                 epilogue_bar_sync();
-                if (warp == 2 && lane == 0) st_release(ctr + 1, 1);
+                if (warp == 2 && lane == 0) {
+                    __threadfence();
+                    atomicAdd(ctr + 1, 1);
+                }
             }
             if (w.shrink && p.flags && w.tile_index >= 0 && !first) {
                 // publish this tile's U rows to the fused units that wait for them (with K
-                // halves, the half that stored them)
+                // parts, the last part, which stored them)
                 fence_proxy_async_global();
                 epilogue_bar_sync();
                 if (warp == 2 && lane == 0) {

@@ -23,6 +23,7 @@ constexpr int kW4Group = 128;        // input features per scale of a 4-bit base
 constexpr int kInlineTiles = 64;     // fused + shrink tiles (cluster groups included)
 constexpr int kInlineSegs = 48;      // merged segments
 constexpr int kInlineAdapters = 4;   // adapters named in the call
+constexpr int kMaxKSplit = 4;        // most parts a block's K is split into
 
 struct Tile {                        // one planner tile, as uploaded to the device
     int32_t row0, nrows, adapter;    // adapter: compact slot (1-based), 0 = none
@@ -44,10 +45,10 @@ struct Tile {                        // one planner tile, as uploaded to the dev
 // tile's rows and the pair runs M = 256 MMAs. Groups are padded with tiles of nrows 0.
 // When `flags` is set, a fused unit's expand waits until flags[tile] == 1, which the shrink
 // unit of that tile publishes after its U rows are stored (single-launch mode).
-// With k_split == 2 every unit (shrink or fused) is split into two units over the two halves of
-// the base K-steps (the expand goes with the second half): the unit that finishes first stores
-// its fp32 partial sums, the other adds them to its own (fp32 addition is commutative, so the sum
-// does not depend on which half finishes first) and stores Y (or U, and publishes its flag).
+// With k_split == S > 1 every unit (shrink or fused) is split into S units over S parts of the
+// base K-steps (the expand goes with the last part): every part but the last to finish stores its
+// fp32 partial sums; the last adds the S sums in part order (so the sum does not depend on which
+// part finishes last) and stores Y (or U, and publishes its flag).
 struct GemmParams {
     // inline work list (used when inline_wl != 0): adapter tensor maps (B_a at [0, 4), A_a
     // at [4, 8)), tiles (fused then shrink), merged segments (offsets then ids), scales
@@ -95,12 +96,13 @@ struct GemmParams {
                                      // of 16) for a batch of one tile on single CTAs
     int debug_stall;
     unsigned long long debug_publish_delay_ns;   // tests: shrink units publish their flag this late
-    // K halves (k_split == 2; 0 or 1 = whole K per unit)
+    // K parts (k_split == 2 or 4; 0 or 1 = whole K per unit)
     int k_split;
-    int k_chunk;                     // base K-steps of the first half: ceil(k_main_blocks / 2)
-    float4* partials;                // fp32 partial sums of the first-finished half: float4 chunk c
-                                     // (output columns 4c .. 4c+3) of row t at [c * part_rows + t]
+    int k_chunk;                     // base K-steps of every part but the last (which takes the rest)
+    float4* partials;                // fp32 partial sums: part q's float4 chunk c (output columns
+                                     // 4c .. 4c+3) of row t at [(q * part_chunks + c) * part_rows + t]
     int part_rows;                   // row stride of `partials` (>= T)
+    int part_chunks;                 // float4 chunks per part: Y's columns, then U's
     int* split_ctr;                  // per (fused tile, column tile): {halves arrived, partials stored};
                                      // zero at launch, cleared at exit by the last CTA
     int n_split_slots;               // counter pairs in use: fused tiles x column tiles, then the

@@ -212,10 +212,11 @@ def test_k_split_choices(lib, name):
 
 def test_k_split_rule(lib):
     from mixed_lora_projection_gb300 import LoraError, k_split, launch_shape
-    # decode-sized handles on narrow projections with long K split (o 6,144 and down 17,408 ->
-    # 5,120); K of 5,120 never does, nor do handles whose batches pass the small-batch path
+    # decode-sized handles on narrow projections with long K split in halves (o 6,144 and down
+    # 17,408 -> 5,120); K of 5,120 never does, nor do handles whose batches pass the small-batch
+    # path; quarters only when asked for
     for d_in in (6144, 17408):
-        for T in (1, 8, 48, 200, 384):
+        for T in (1, 8, 48, 128, 129, 200, 384):
             assert k_split(d_in, 5120, 256, T, 152) == 2, (d_in, T)
         for T in (385, 2048, 32768):
             assert k_split(d_in, 5120, 256, T, 152) == 1, (d_in, T)
@@ -224,7 +225,7 @@ def test_k_split_rule(lib):
     assert k_split(6080, 5120, 256, 48, 152) == 1        # 95 K-steps of 64
     # a split handle's units come in pairs
     s = launch_shape(6144, 5120, 256, 152, 48, [0, 48], [0])
-    assert s["fused_units"] % 2 == 0 and s["fused_units"] >= 2 * 5120 // s["tile_n"]
+    assert s["fused_units"] % 2 == 0 and s["fused_units"] >= 2 * (5120 // s["tile_n"])
     with pytest.raises(LoraError):
         k_split(6144, 5120, 256, 48, 1)          # fewer than 2 SMs
     with pytest.raises(LoraError):

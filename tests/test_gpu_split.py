@@ -1,6 +1,6 @@
-"""GPU tests of the K halves (LORA_OPT_K_SPLIT = 2): every shrink and fused block runs as two
-work units over the two halves of the base K-steps; the half that finishes first stores its
-fp32 sums, the other adds them and rounds. Against the fp64 oracle, and bit for bit across
+"""GPU tests of the K parts (LORA_OPT_K_SPLIT = 2 or 4): every shrink and fused block runs as
+that many work units over parts of the base K-steps; every part but the last to finish stores
+its fp32 sums, the last adds all of them in part order and rounds. Against the fp64 oracle, and bit for bit across
 everything that must not change a row's sum on one handle: launch shape, K-step width, unit
 order, one launch or two, the batch a row is in, host-buffer chunks, graph replays."""
 import numpy as np
@@ -51,14 +51,16 @@ SMALL = [
 
 @pytest.mark.parametrize("case", SMALL, ids=[f"T{c[0]}_{c[1]}x{c[2]}" for c in SMALL])
 @pytest.mark.parametrize("cluster", [1, 2])
-def test_halves_match_oracle_and_every_launch_form(dev, case, cluster):
+@pytest.mark.parametrize("parts", [2, 4])
+def test_parts_match_oracle_and_every_launch_form(dev, case, cluster, parts):
     from mixed_lora_projection_gb300 import _lib as L
     T, d_in, d_out, r, lens, ids = case
     w = _w("split", T, d_in, d_out, r, lens, ids)
     off = list(w.seg_offsets)
     inp = make_inputs(w, dev)
     outs = []
-    with _ll(w) as ll:
+    with _ll(w, split=parts) as ll:
+        assert ll.describe(T, off, ids)["n_units"] % parts == 0
         ll.set_option(L.OPT_CLUSTER, cluster if T > 128 else 1)
         outs.append(run(ll, inp, off, ids).clone())
         ll.set_option(L.OPT_TILE_K, 32)                 # 32-wide K stages: the same halves
@@ -96,7 +98,7 @@ def test_single_ctas_equal_sm_pairs_with_halves(dev):
 
 @pytest.mark.parametrize("proj", [("o", 6144), ("down", 17408)])
 def test_auto_halves_on_decode_batches_of_long_k_projections(dev, proj):
-    # a handle for 48-row batches of the o or down projection chooses halves by itself; the
+    # a handle for 48-row batches of the o or down projection chooses K halves by itself; the
     # result matches the oracle, and so does the same batch with whole K
     from mixed_lora_projection_gb300 import LoraLinear, k_split, _lib as L
     name, d_in = proj
@@ -147,6 +149,38 @@ def test_rows_do_not_depend_on_the_batch_with_halves(dev):
         assert ll.status() == 0
     assert torch.equal(full[s0:s1], alone)
     assert torch.equal(full[:48], dec)
+
+
+def test_quarters_in_part_order_whichever_part_ends_last(dev):
+    # four parts of K on a 48-row batch of the down projection: every output is ((P0 + P1) + P2) + P3
+    # whatever order the parts finish in; repeated calls (different arrival orders) give the same
+    # bits, single CTAs and SM pairs too, and the result matches the oracle
+    from mixed_lora_projection_gb300 import _lib as L
+    w = _w("q_down", 48, 17408, 5120, 64, [8] * 5 + [8], [0, 0, 0, 0, 0, 1])
+    inp = make_inputs(w, dev)
+    off, ids = list(w.seg_offsets), list(w.seg_ids)
+    with _ll(w, split=4) as ll:
+        ys = [run(ll, inp, off, ids).clone() for _ in range(5)]
+        ll.set_option(L.OPT_MAX_CTAS, 40)                 # fewer SMs: other arrival orders
+        ys.append(run(ll, inp, off, ids).clone())
+        torch.cuda.synchronize()
+        assert ll.status() == 0
+    assert all(torch.equal(y, ys[0]) for y in ys)
+    assert rel_err(ys[0], oracle_full(inp, off, ids)) <= TOL
+
+
+def test_forced_parts_are_clamped_to_short_k(dev):
+    # four parts asked for on d_in = 320 (five K-steps of 64): the handle keeps every part at least
+    # one K-step long (two parts), and the result matches the oracle
+    w = _w("short_k", 100, 320, 256, 16, [50, 50], [0, 1])
+    inp = make_inputs(w, dev)
+    off, ids = list(w.seg_offsets), list(w.seg_ids)
+    with _ll(w, split=4) as ll:
+        assert ll.describe(w.T, off, ids)["n_units"] % 2 == 0
+        y = run(ll, inp, off, ids)
+        torch.cuda.synchronize()
+        assert ll.status() == 0
+    assert rel_err(y, oracle_full(inp, off, ids)) <= TOL
 
 
 def test_decode_batch_on_a_narrow_long_k_projection(dev):
