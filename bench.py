@@ -645,8 +645,8 @@ def main():
     ap.add_argument("--w4", action="store_true", help="4-bit base weights (int4, group 128, bf16 scales)")
     ap.add_argument("--raster", default="", help="unit order MODE[:GROUP] (the library's raster option: 0 auto, "
                     "1 row tiles first, 2 column tiles first, 3 groups of GROUP column tiles)")
-    ap.add_argument("--k-split", type=int, default=0, choices=[0, 1, 2], help="K halves per output block (the "
-                    "library's K-split option: 0 = each handle's own choice, 1 = whole K, 2 = two halves)")
+    ap.add_argument("--k-split", type=int, default=0, choices=[0, 1, 2, 4], help="K parts per output block (the "
+                    "library's K-split option: 0 = each handle's own choice, 1 = whole K, 2 or 4 parts)")
     ap.add_argument("--pdl", action="store_true", help="programmatic dependent launch for calls without adapter "
                     "rows (the library's PDL option): each kernel may start while the previous one ends")
     ap.add_argument("--graph", action="store_true", help="time the steps as CUDA-graph replays (each call's "
