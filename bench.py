@@ -315,6 +315,8 @@ def run_ours(args, rank, world, dist):
                 handles[key].set_option(L.OPT_K_SPLIT, args.k_split)
             if args.pdl:
                 handles[key].set_option(L.OPT_PDL, 1)
+            if args.token_columns:
+                handles[key].set_option(L.OPT_TOKEN_COLUMNS, args.token_columns)
             if args.raster:
                 mode, _, group = args.raster.partition(":")
                 handles[key].set_option(L.OPT_RASTER, int(mode))
@@ -471,6 +473,7 @@ def run_ours(args, rank, world, dist):
                    **({"raster": args.raster} if args.raster else {}),
                    **({"k_split": args.k_split} if args.k_split else {}),
                    **({"pdl": True} if args.pdl else {}),
+                   **({"token_columns": args.token_columns} if args.token_columns else {}),
                    "base": "int4 (symmetric, group 128, bf16 scales)" if args.w4 else "bf16", "T": w0.T, "d_in": w0.d_in if len(items) == 1 else "per projection",
                    "d_out": w0.d_out if len(items) == 1 else "per projection", "rank": w0.rank,
                    "segments": len(w0.seg_ids), "adapter_rows": w0.adapter_rows, "calls_per_step": len(items),
@@ -649,6 +652,9 @@ def main():
                     "library's K-split option: 0 = each handle's own choice, 1 = whole K, 2 or 4 parts)")
     ap.add_argument("--pdl", action="store_true", help="programmatic dependent launch for calls without adapter "
                     "rows (the library's PDL option): each kernel may start while the previous one ends")
+    ap.add_argument("--token-columns", type=int, default=0, choices=[0, 1, 2], help="token-column units (the "
+                    "library's option: 0 = when the shape model expects them sooner, 1 = never, 2 = whenever the "
+                    "batch allows)")
     ap.add_argument("--graph", action="store_true", help="time the steps as CUDA-graph replays (each call's "
                     "work list must travel in the kernel parameters, e.g. the 24-layer sweep)")
     args = ap.parse_args()

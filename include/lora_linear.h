@@ -249,12 +249,19 @@ enum {
     LORA_OPT_MAX_CTAS = 15,     /* at most this many CTAs (one per SM) per launch, >= 2; 0 = every SM (default).
                                    Leaves the other SMs to calls on other streams; the launch shape is chosen
                                    for the SMs it may use. Does not change any result */
-    LORA_OPT_PDL = 16           /* 1 = programmatic dependent launch for calls without adapter rows (bf16 base,
+    LORA_OPT_PDL = 16,          /* 1 = programmatic dependent launch for calls without adapter rows (bf16 base,
                                    one launch): the launch may start on SMs the previous kernel of the stream
                                    leaves, requests its first W tiles, and waits for that kernel before it
                                    reads or writes anything else; it lets the next kernel start early in turn.
                                    The previous kernel must not write this call's W. 0 (default) = off.
                                    Does not change any result */
+    LORA_OPT_TOKEN_COLUMNS = 17 /* bf16 base: token-column units for batches of at most 512 rows whose rows
+                                   all name one adapter (or none), on handles that sum whole K: each unit of
+                                   an SM pair computes 256 output features for every token row of the batch
+                                   (features on the MMA's M, tokens on its N), so each W tile is read once
+                                   and no 128-row tile is padded. 0 (default) = when the launch-shape model
+                                   expects them to finish sooner, 1 = never, 2 = whenever the batch allows
+                                   them. Does not change any result */
 };
 
 /* lora_linear_set_option -- set one option above. Returns LORA_OK or LORA_EINVAL. */
@@ -273,12 +280,13 @@ int lora_linear_timing(lora_linear* h, int kind, double* total_ms, long long* la
 
 /*
  * lora_linear_describe -- the launch shape forward would use for T rows and these
- * segments, without launching: output-tile width, number of fused tiles, fused work
- * units, grid size, pipeline stages, and whether a shrink runs. Any pointer may be NULL.
+ * segments, without launching: output-tile width, number of fused tiles, work units (fused
+ * and shrink), grid size, pipeline stages, whether a shrink runs, and the unit order (as
+ * lora_linear_shape reports it; 3 = token-column units). Any pointer may be NULL.
  */
 int lora_linear_describe(lora_linear* h, int T, const int32_t* seg_offsets,
                          const int32_t* seg_adapter_ids, int n_seg, int* tile_n, int* n_tiles,
-                         int* n_units, int* grid, int* stages, int* has_shrink);
+                         int* n_units, int* grid, int* stages, int* has_shrink, int* unit_order);
 
 /*
  * lora_linear_shape -- the launch shape lora_linear_forward (w4 = 0) or
@@ -287,7 +295,8 @@ int lora_linear_describe(lora_linear* h, int T, const int32_t* seg_offsets,
  * default options, and T rows in these segments (checked as by lora_linear_plan). Outputs
  * (any may be NULL): cluster (2 = SM pairs, 1 = single CTAs), tile_n (output columns per
  * fused unit), bk (K per pipeline stage), stages, unit_order (0 = column (feature) tiles
- * first, 1 = row tiles (token groups) first, 2 = groups of column tiles), fused_units (work
+ * first, 1 = row tiles (token groups) first, 2 = groups of column tiles, 3 = token-column units:
+ * each covers every token row, see LORA_OPT_TOKEN_COLUMNS), fused_units (work
  * units of the fused launch, or of the 4-bit kernel) and shrink_units (shrink work units).
  * T = 0 gives zeros. Returns LORA_OK or LORA_EINVAL. Diagnostics and tests.
  */

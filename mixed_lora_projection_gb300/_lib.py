@@ -35,7 +35,7 @@ SIGNATURES = {
     "lora_linear_set_option": (C.c_int, [P, C.c_int, C.c_longlong]),
     "lora_linear_timing": (C.c_int, [P, C.c_int, C.POINTER(C.c_double), C.POINTER(C.c_longlong),
                                      C.POINTER(C.c_longlong)]),
-    "lora_linear_describe": (C.c_int, [P, C.c_int, I32P, I32P, C.c_int, IP, IP, IP, IP, IP, IP]),
+    "lora_linear_describe": (C.c_int, [P, C.c_int, I32P, I32P, C.c_int, IP, IP, IP, IP, IP, IP, IP]),
     "lora_linear_error_string": (C.c_char_p, [C.c_int]),
     "lora_linear_shape": (C.c_int, [C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, I32P, I32P, C.c_int, C.c_int,
                                     IP, IP, IP, IP, IP, IP, IP]),
@@ -49,7 +49,8 @@ SIGNATURES = {
 LORA_OK, LORA_EINVAL, LORA_ENOMEM, LORA_ECUDA, LORA_ETIMEOUT, LORA_EUNSUPPORTED, LORA_ENODEV = 0, -1, -2, -3, -4, -5, -6
 (OPT_TILE_N, OPT_WAIT_LIMIT_US, OPT_DEBUG_STALL, OPT_TIMING, OPT_RASTER, OPT_TWO_LAUNCH, OPT_CLUSTER,
  OPT_RASTER_GROUP, _OPT_RETIRED_9, OPT_TILE_K, OPT_INLINE_WORK_LIST, OPT_MMA_GROUP,
- OPT_DEBUG_PUBLISH_DELAY_US, OPT_K_SPLIT, OPT_MAX_CTAS, OPT_PDL) = 1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 11, 12, 13, 14, 15, 16
+ OPT_DEBUG_PUBLISH_DELAY_US, OPT_K_SPLIT, OPT_MAX_CTAS, OPT_PDL,
+ OPT_TOKEN_COLUMNS) = 1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 11, 12, 13, 14, 15, 16, 17
 
 
 def load():

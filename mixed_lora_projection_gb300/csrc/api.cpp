@@ -82,7 +82,8 @@ struct lora_linear {
     int raster_group = 4, tile_k = 0, allow_inline = 1, mma_group = 0;  // 0: 2 for SM pairs, else 1
     int max_ctas = 0;           // LORA_OPT_MAX_CTAS: at most this many CTAs per launch (0 = one per SM)
     int pdl = 0;                // LORA_OPT_PDL: launches without ready flags may start early
-    int max_clusters_cache[2][kMaxTileN / 16 + 1] = {};  // co-resident clusters by (size, B rows)
+    int yt_mode = 0;            // LORA_OPT_TOKEN_COLUMNS: 0 = auto, 1 = never, 2 = whenever a batch allows
+    int max_clusters_cache[2][kMaxYtRows / 8 + 1] = {};  // co-resident clusters by (size, B rows per CTA)
     // K halves: chosen once per handle (every call on it sums each output the same way)
     int k_split = 1;            // 1, 2 or 4: every block runs as that many units over parts of K
     int k_split_opt = 0;        // LORA_OPT_K_SPLIT: 0 = the handle's own choice, 1, 2 or 4 = forced
@@ -274,6 +275,7 @@ int choose_m_fastest(const lora_linear* h, int n_tiles, int n_ntiles, int tile_n
 struct Shape {
     int cs = 1, tile_n = 0, shrink_n = 0, n_ntiles = 0, stages = 0, m_fastest = 0, bk = 64, raster_group = 1;
     int a_rows = kTileM;   // rows of one A box: the tile's rows when the batch is one short tile
+    int yt = 0, yt_rows = 0, yt_h = 0;   // token-column units (SM pairs, 256 features x every token row)
     std::vector<Tile> fused_groups, shrink_groups;  // cs tiles per group
 };
 
@@ -318,8 +320,8 @@ void make_groups(const std::vector<Tile>& tiles, int cs, bool shrink, int zero_r
 }
 
 int max_clusters(lora_linear* h, const GemmParams& p) {
-    const int b_rows = std::max(p.tile_n, p.shrink_n);
-    int& c = h->max_clusters_cache[p.cluster_size - 1][b_rows / 16];
+    const int b_rows = gemm_b_rows(p);
+    int& c = h->max_clusters_cache[p.cluster_size - 1][b_rows / 8];
     if (c == 0) c = gemm_max_clusters(p);
     return c;
 }
@@ -369,6 +371,52 @@ double makespan(const lora_linear* h, const std::vector<Tile>& fused_groups, con
     return *std::max_element(load.begin(), load.end());
 }
 
+// Per-SM cycles of one 64-wide K-step of a token-column unit whose pair holds 2 * rows token
+// rows, its epilogue included, fitted to gate_up (5,120 -> 34,816) and qkv (5,120 -> 12,288)
+// batches of 200 to 512 rows timed on GB300: one MMA per 16-wide step up to 128 rows per CTA
+// (~1,020 cycles at 100 rows), a second one and a single accumulator (its epilogue no longer
+// overlaps the next unit) past it (~1,300 cycles at 152 rows, ~1,650 at 256). These units
+// stream W from memory, so they run well above their MMA time.
+double yt_kstep_cycles(int rows) {
+    return rows <= kTileM ? 940.0 + 0.8 * rows : 790.0 + 3.35 * rows;
+}
+
+// The row-tile model (kstep_cycles) is fitted to the tensor-bound shapes of large batches; on
+// the batches token-column units serve (at most 512 rows, W streamed from memory) row tiles
+// took 1.3-1.8x its makespan (gate_up and qkv, 200 to 512 rows). Token-column units are chosen
+// when their makespan is below the row-tile makespan times this factor.
+constexpr double kRowTileSmallBatchFactor = 1.45;
+
+// Token-column units serve a batch of at most 2 * kMaxYtRows rows whose tiles all name one
+// adapter (or none), on SM pairs with 64-wide K-steps and whole K per unit; options that fix
+// another shape rule them out.
+bool yt_allowed(const lora_linear* h, const Plan& plan) {
+    if (h->yt_mode == 1 || h->k_split > 1 || plan.fused.empty()) return false;
+    if ((h->tile_k && h->tile_k != kTileK) || h->cluster == 1 || usable_sms(h) < 2) return false;
+    if (h->force_tile_n && h->force_tile_n != kMaxTileN) return false;
+    if (plan.seg_off.back() > 2 * kMaxYtRows) return false;
+    for (const Tile& t : plan.fused)
+        if (t.adapter != plan.fused[0].adapter) return false;
+    return true;
+}
+
+// Makespan (per-SM cycles) of a token-column launch: the shrink groups (SM pairs), then one unit
+// per 256 output features over every token row, round-robin over the SM pairs.
+double yt_makespan(const lora_linear* h, const Plan& plan, int slots) {
+    int rows = 0, hh = 0;
+    yt_split(plan.seg_off.back(), &rows, &hh);
+    const int k_main = ceil_div(h->d_in, kTileK), k_lora = ceil_div(h->rank, kTileK);
+    const int shrink_n = ceil_div(h->rank, 16) * 16;
+    std::vector<Tile> sg;
+    make_groups(plan.shrink, 2, true, h->u_rows - kTileM, &sg);
+    std::vector<double> load(slots, 0.0);
+    long long u = 0;
+    for (size_t g = 0; g < sg.size() / 2; ++g) load[u++ % slots] += k_main * kstep_cycles(2, shrink_n);
+    const double unit = (k_main + (plan.fused[0].adapter ? k_lora : 0)) * yt_kstep_cycles(rows);
+    for (int t = 0; t < ceil_div(h->d_out, 2 * kTileM); ++t) load[u++ % slots] += unit;
+    return *std::max_element(load.begin(), load.end());
+}
+
 // The launch shape (SM pair or single CTA, output-tile width) the makespan model expects to
 // finish a plan soonest with K in `k_split` parts; cs / tn nonzero fix that choice. Returns the
 // expected makespan.
@@ -403,7 +451,7 @@ double search_shape(const lora_linear* h, const Plan& plan, int cs, int tn, int 
     return best;
 }
 
-Shape choose_shape(lora_linear* h, const Plan& plan) {
+Shape choose_shape(lora_linear* h, const Plan& plan, bool allow_yt = true) {
     Shape sh;
     const int nf = (int)plan.fused.size();
     sh.shrink_n = ceil_div(h->rank, 16) * 16;
@@ -412,20 +460,38 @@ Shape choose_shape(lora_linear* h, const Plan& plan) {
     int cs = h->cluster, tn = h->force_tile_n;
     // K halves: whole 256-column blocks (narrower ones gained nothing where halves were measured)
     if (h->k_split > 1 && !small_batch && !tn) tn = kMaxTileN;
-    if (!cs || !tn) {
+    const bool yt_ok = allow_yt && yt_allowed(h, plan);
+    int yt = 0;
+    if (!cs || !tn || yt_ok) {
+        const int cs0 = cs, tn0 = tn;
         if (small_batch && !cs) cs = 1;
         // plan signature: tile count and each tile's adapter / row count
         uint64_t key = 1469598103934665603ull ^ (uint64_t)nf;
         for (const Tile& t : plan.fused) key = (key ^ (uint64_t)(t.adapter * 131 + t.nrows)) * 1099511628211ull;
-        key ^= ((uint64_t)cs << 56) ^ ((uint64_t)tn << 40) ^ ((uint64_t)h->k_split << 32);
+        key ^= ((uint64_t)cs << 56) ^ ((uint64_t)tn << 40) ^ ((uint64_t)h->k_split << 32) ^
+               ((uint64_t)(yt_ok ? 1 + h->yt_mode : 0) << 48);
         auto it = h->shape_cache.find(key);
         if (it != h->shape_cache.end()) {
-            cs = (int)(it->second >> 16);
+            yt = (int)(it->second >> 31);
+            cs = (int)((it->second >> 16) & 0x7FFF);
             tn = (int)(it->second & 0xFFFF);
         } else {
-            search_shape(h, plan, cs, tn, h->k_split, &cs, &tn);
+            double m = 0.0;
+            if (!cs || !tn) m = search_shape(h, plan, cs, tn, h->k_split, &cs, &tn);
+            if (yt_ok) {
+                // token-column units when asked for, or, for batches of more than one row tile,
+                // when the model expects them to finish sooner
+                const int slots = usable_sms(h) / 2;
+                if (h->yt_mode == 2 ||
+                    (!cs0 && !tn0 && nf >= 2 && yt_makespan(h, plan, slots) < kRowTileSmallBatchFactor * m))
+                    yt = 1;
+            }
+            if (yt) {
+                cs = 2;
+                tn = kMaxTileN;
+            }
             if (h->shape_cache.size() > 256) h->shape_cache.clear();
-            h->shape_cache[key] = ((uint32_t)cs << 16) | (uint32_t)tn;
+            h->shape_cache[key] = ((uint32_t)yt << 31) | ((uint32_t)cs << 16) | (uint32_t)tn;
         }
     }
     sh.cs = cs;
@@ -442,7 +508,22 @@ Shape choose_shape(lora_linear* h, const Plan& plan) {
     sh.stages = stages_for(std::max(sh.tile_n, sh.shrink_n) / sh.cs, sh.bk, sh.a_rows);
     sh.m_fastest = choose_m_fastest(h, nfg, sh.n_ntiles, sh.tile_n, kTileM * sh.cs, slots);
     sh.raster_group = h->raster == 3 ? h->raster_group : ceil_div(sh.n_ntiles, 2);
+    if (yt) {
+        // one unit per 256 output features; a stage holds 128 W rows and this CTA's token rows
+        sh.yt = 1;
+        yt_split(plan.seg_off.back(), &sh.yt_rows, &sh.yt_h);
+        sh.bk = kTileK;
+        sh.a_rows = kTileM;
+        sh.n_ntiles = ceil_div(h->d_out, 2 * kTileM);
+        sh.stages = stages_for(std::max(sh.yt_rows, sh.shrink_n / 2), sh.bk, kTileM);
+        sh.m_fastest = 0;
+    }
     return sh;
+}
+
+// Fused row groups of a launch shape: token-column units span every token row in one group.
+int fused_row_groups(const Shape& sh) {
+    return sh.yt ? 1 : (int)(sh.fused_groups.size() / sh.cs);
 }
 
 // K parts for a handle, decided once from its shape and max_tokens, so that every call on the
@@ -766,6 +847,10 @@ int lora_linear_set_option(lora_linear* h, int option, long long value) {
             if (value < 0 || value > 1) return LORA_EINVAL;
             h->pdl = (int)value;
             return LORA_OK;
+        case LORA_OPT_TOKEN_COLUMNS:
+            if (value < 0 || value > 2) return LORA_EINVAL;
+            h->yt_mode = (int)value;
+            return LORA_OK;
         case LORA_OPT_MAX_CTAS:
             if (value < 0 || value > (1 << 20) || (value > 0 && value < 2)) return LORA_EINVAL;
             h->max_ctas = (int)value;
@@ -824,17 +909,17 @@ int lora_linear_status(lora_linear* h, int reset) {
 
 int lora_linear_describe(lora_linear* h, int T, const int32_t* seg_offsets,
                          const int32_t* seg_adapter_ids, int n_seg, int* tile_n, int* n_tiles,
-                         int* n_units, int* grid, int* stages, int* has_shrink) {
+                         int* n_units, int* grid, int* stages, int* has_shrink, int* unit_order) {
     if (!h) return LORA_EINVAL;
     Plan plan;
     int rc = plan_segments(seg_offsets, seg_adapter_ids, n_seg, T, -1, &plan);
     if (rc != LORA_OK) return rc;
     const int nf = (int)plan.fused.size();
-    int units = 0, tn = 0, st = 0, g = 0;
+    int units = 0, tn = 0, st = 0, g = 0, order = 0;
     if (nf) {
         Shape sh = choose_shape(h, plan);
-        units = ((int)(sh.fused_groups.size() / sh.cs) * sh.n_ntiles + (int)(sh.shrink_groups.size() / sh.cs)) *
-                h->k_split;
+        order = sh.yt ? 3 : sh.m_fastest;
+        units = (fused_row_groups(sh) * sh.n_ntiles + (int)(sh.shrink_groups.size() / sh.cs)) * h->k_split;
         tn = sh.tile_n;
         st = sh.stages;
         int slots = usable_sms(h);
@@ -846,6 +931,9 @@ int lora_linear_describe(lora_linear* h, int T, const int32_t* seg_offsets,
             q.stages = sh.stages;
             q.cluster_size = sh.cs;
             q.bk = sh.bk;
+            q.yt = sh.yt;
+            q.yt_rows = sh.yt_rows;
+            q.yt_h = sh.yt_h;
             DeviceGuard guard(h->device);
             slots = std::min(max_clusters(h, q), usable_sms(h) / sh.cs);
         }
@@ -857,6 +945,7 @@ int lora_linear_describe(lora_linear* h, int T, const int32_t* seg_offsets,
     if (grid) *grid = g;
     if (stages) *stages = st;
     if (has_shrink) *has_shrink = plan.shrink.empty() ? 0 : 1;
+    if (unit_order) *unit_order = order;
     return LORA_OK;
 }
 
@@ -897,7 +986,7 @@ int forward_impl(lora_linear* h, const void* x, int T, const int32_t* seg_offset
 
     DeviceGuard guard(h->device);
     const bool w4 = Wq != nullptr;
-    Shape sh = choose_shape(h, plan);
+    Shape sh = choose_shape(h, plan, !w4);
     // 4-bit base: the shrink pass runs on the bf16 kernel (64-wide K-steps), then the 4-bit
     // kernel runs the base and expand passes over token groups
     if (w4) {
@@ -911,7 +1000,8 @@ int forward_impl(lora_linear* h, const void* x, int T, const int32_t* seg_offset
     const W4Shape w4s = w4 ? w4_shape(h, w4_groups, T) : W4Shape();
     const bool w4_inline = n_used <= kInlineAdapters && n_w4g <= kW4InlineGroups;
     const int cs = sh.cs, tile_n = sh.tile_n, shrink_n = sh.shrink_n, bk = sh.bk;
-    const int nfg = (int)sh.fused_groups.size() / cs, nsg = (int)sh.shrink_groups.size() / cs;
+    // token-column units: one row group spanning every token row
+    const int nfg = sh.yt ? 1 : (int)sh.fused_groups.size() / cs, nsg = (int)sh.shrink_groups.size() / cs;
     const int nft = (int)sh.fused_groups.size(), nst = (int)sh.shrink_groups.size();
     const int n_m = (int)plan.seg_id.size();
     const int nf = (int)plan.fused.size();
@@ -1034,8 +1124,19 @@ int forward_impl(lora_linear* h, const void* x, int T, const int32_t* seg_offset
     } else if (encode_2d(h, &p.tm_w, W, h->d_in, h->d_out, bk, tile_n / cs) != CUDA_SUCCESS) {
         return LORA_ECUDA;
     }
-    if (encode_2d(h, &p.tm_u, h->u_ws, h->rank, h->u_rows, bk, (uint32_t)sh.a_rows) != CUDA_SUCCESS)
+    // the expand reads U as the A operand (a_rows-row boxes), or as the B operand of token-column
+    // units (yt_rows-row boxes)
+    if (encode_2d(h, &p.tm_u, h->u_ws, h->rank, h->u_rows, bk, (uint32_t)(sh.yt ? sh.yt_rows : sh.a_rows)) !=
+        CUDA_SUCCESS)
         return LORA_ECUDA;
+    if (sh.yt) {
+        if (encode_2d(h, &p.tm_xt, x, h->d_in, T, bk, (uint32_t)sh.yt_rows) != CUDA_SUCCESS) return LORA_ECUDA;
+        p.yt = 1;
+        p.yt_tokens = T;
+        p.yt_rows = sh.yt_rows;
+        p.yt_h = sh.yt_h;
+        p.yt_adapter = plan.fused[0].adapter;
+    }
     p.y = y;
     p.u = h->u_ws;
     p.status = h->status;
@@ -1413,7 +1514,7 @@ int lora_linear_shape(int d_in, int d_out, int rank, int num_sms, int T, const i
     h.u_rows = ceil_div(h.max_tokens, kTileM) * kTileM + kTileM;
     if (!w4) h.k_split = choose_k_split(&h);   // a handle of max_tokens = T
     for (size_t i = 0; i < plan.fused.size(); ++i) plan.fused[i].fused_index = plan.fused[i].split_index = (int32_t)i;
-    const Shape sh = choose_shape(&h, plan);
+    const Shape sh = choose_shape(&h, plan, !w4);
     if (w4) {
         // the 4-bit kernel over token groups; the shrink runs as the bf16 kernel's shrink units
         const std::vector<W4Group> groups = make_w4_groups(plan.fused);
@@ -1431,8 +1532,8 @@ int lora_linear_shape(int d_in, int d_out, int rank, int num_sms, int T, const i
     if (tile_n) *tile_n = sh.tile_n;
     if (bk) *bk = sh.bk;
     if (stages) *stages = sh.stages;
-    if (unit_order) *unit_order = sh.m_fastest;   // 0, 1, 2 as documented
-    if (fused_units) *fused_units = (int)(sh.fused_groups.size() / sh.cs) * sh.n_ntiles * h.k_split;
+    if (unit_order) *unit_order = sh.yt ? 3 : sh.m_fastest;   // 0, 1, 2, 3 as documented
+    if (fused_units) *fused_units = fused_row_groups(sh) * sh.n_ntiles * h.k_split;
     if (shrink_units) *shrink_units = (int)(sh.shrink_groups.size() / sh.cs) * h.k_split;
     return LORA_OK;
 }

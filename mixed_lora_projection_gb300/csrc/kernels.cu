@@ -106,6 +106,7 @@ __device__ __forceinline__ WorkList resolve_work_list(const GemmParams& p) {
     return wl;
 }
 
+template <bool YT>
 __device__ __forceinline__ Unit decode_unit(const GemmParams& p, const WorkList& wl, int u, int rank) {
     Unit r;
     const int cs = p.cluster_size;
@@ -127,6 +128,18 @@ __device__ __forceinline__ Unit decode_unit(const GemmParams& p, const WorkList&
         r.nk = r.kmain;
         r.slot = p.shrink_slot0 + v0 * cs + rank;
         r.pchunk = p.u_chunk0;
+    } else if (YT) {
+        // token-column unit: 256 output features (128 per CTA) for every token row
+        const int v = v0 - p.n_shrink;
+        r.tile = wl.fused[rank];
+        r.tile.adapter = p.yt_adapter;
+        r.shrink = 0;
+        r.tile_index = 0;
+        r.n0 = v * kTileM * cs;
+        r.n = 2 * p.yt_h;
+        r.nk = r.kmain + (p.yt_adapter ? p.k_lora_blocks : 0);
+        r.slot = 0;
+        r.pchunk = 0;
     } else {
         const int v = v0 - p.n_shrink;
         int ti, nt;
@@ -153,8 +166,41 @@ __device__ __forceinline__ Unit decode_unit(const GemmParams& p, const WorkList&
     return r;
 }
 
-template <int BK, int CG>
+// Token row of accumulator column c of a token-column unit: the first MMA's columns [0, 2 h)
+// hold stage rows [0, h) of the even CTA (tokens 0 ..) then of the odd CTA (tokens rows ..); the
+// second MMA's columns hold stage rows [h, rows) of the even CTA, then of the odd CTA.
+__device__ __forceinline__ int yt_token(int c, int h, int rows) {
+    if (c < 2 * h) return c < h ? c : rows + c - h;
+    const int cc = c - 2 * h, h1 = rows - h;
+    return cc < h1 ? h + cc : rows + h + cc - h1;
+}
+
+// Epilogue of a token-column unit: this thread's TMEM lane is output feature f and each
+// accumulator column a token row. Each store of a warp writes 32 neighbouring features of one
+// token row (64 bytes).
+__device__ __forceinline__ void yt_store(const GemmParams& p, uint32_t taddr, int f) {
+    const int h = p.yt_h, rows = p.yt_rows, n = 2 * p.yt_rows, T = p.yt_tokens;
+    const bool f_ok = f < p.d_out;
+    __nv_bfloat16* col = reinterpret_cast<__nv_bfloat16*>(p.y) + f;
+    for (int c = 0; c < n; c += 32) {
+        uint32_t v[32];
+        const bool two = c + 16 < n;  // n is a multiple of 16
+        tmem_ld16(taddr + (uint32_t)c, v);
+        if (two) tmem_ld16(taddr + (uint32_t)c + 16, v + 16);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            if (i < 16 || two) {
+                const int t = yt_token(c + i, h, rows);
+                if (f_ok && t < T) col[(size_t)t * p.d_out] = __float2bfloat16_rn(__uint_as_float(v[i]));
+            }
+        }
+    }
+}
+
+template <int BK, int CG, bool YT>
 __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_constant__ GemmParams p) {
+    static_assert(!YT || (CG == 2 && BK == 64), "token-column units run on SM pairs with 64-wide K-steps");
     // A stage: the tile's rows of X (or U) for this K-step; a batch of one short tile loads
     // only its rows (a_rows < 128), and the MMA's remaining A rows read unrelated shared memory
     // whose output rows are never stored
@@ -164,8 +210,11 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
     const int stages = p.stages;
-    const int b_rows = (p.tile_n > p.shrink_n ? p.tile_n : p.shrink_n) / CG;  // this CTA's B rows
+    // this CTA's B rows per stage: output-tile rows of W, rows of A_a, or token rows
+    const int b_rows = YT ? max(p.yt_rows, p.shrink_n / CG) : (p.tile_n > p.shrink_n ? p.tile_n : p.shrink_n) / CG;
     const uint32_t b_stage_bytes = (uint32_t)b_rows * BK * 2;
+    // token-column units wider than one accumulator take all of TMEM: one accumulator at a time
+    const int n_acc = (YT && 2 * p.yt_rows > kAccCols) ? 1 : 2;
     uint8_t* a_ring = base;
     uint8_t* b_ring = a_ring + (size_t)stages * kStageA;
     uint64_t* bars = reinterpret_cast<uint64_t*>(b_ring + (size_t)stages * b_stage_bytes);
@@ -220,6 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
                 if (p.n_fused) {
                     tma_prefetch_desc(&p.tm_w);
                     tma_prefetch_desc(&p.tm_u);
+                    if (YT) tma_prefetch_desc(&p.tm_xt);
                 }
             }
             __syncwarp();
@@ -234,24 +284,30 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
             int pre = 0;
             if (p.pdl) {
                 if (group < n_units) {
-                    const Unit w0 = decode_unit(p, wl, group, rank);
+                    const Unit w0 = decode_unit<YT>(p, wl, group, rank);
                     if (!w0.shrink) {
+                        // W is the B operand, or the A operand of a token-column unit
                         const int half0 = w0.n / CG;
-                        const uint32_t tx0 = CG * (kStageA + (uint32_t)half0 * BK * 2);
+                        const uint32_t tx0 = YT ? CG * (kStageA + (uint32_t)p.yt_rows * BK * 2)
+                                                  : CG * (kStageA + (uint32_t)half0 * BK * 2);
                         pre = w0.kmain < stages ? w0.kmain : stages;
                         for (int kb = 0; kb < pre; ++kb) {
                             const uint32_t fb_local = smem_addr(&full[kb]);
                             mbar_arrive_expect_tx(fb_local, tx0, leader ? issuer : 0u);
                             const uint32_t fb = CG > 1 ? map_to_rank(fb_local, 0) : fb_local;
-                            tma_load_2d<CG>(smem_addr(b_ring + (size_t)kb * b_stage_bytes), &p.tm_w, fb,
-                                            (w0.kb0 + kb) * BK, w0.n0 + rank * half0, issuer);
+                            if (YT)
+                                tma_load_2d<CG>(smem_addr(a_ring + (size_t)kb * kStageA), &p.tm_w, fb,
+                                                (w0.kb0 + kb) * BK, w0.n0 + rank * kTileM, issuer);
+                            else
+                                tma_load_2d<CG>(smem_addr(b_ring + (size_t)kb * b_stage_bytes), &p.tm_w, fb,
+                                                (w0.kb0 + kb) * BK, w0.n0 + rank * half0, issuer);
                         }
                     }
                 }
                 griddep_wait();
             }
             for (int u = group; u < n_units && ok; u += n_groups) {
-                const Unit w = decode_unit(p, wl, u, rank);
+                const Unit w = decode_unit<YT>(p, wl, u, rank);
                 const int ad = w.tile.adapter;
                 const CUtensorMap* bmain = &p.tm_w;
                 if (w.shrink) {
@@ -264,14 +320,24 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
                     if (!p.inline_wl) tensormap_acquire(&wl.tm_b[ad - 1]);
                     acquired_b = ad;
                 }
+                const bool yt_unit = YT && !w.shrink;
                 const int half = w.n / CG;                       // B rows this CTA loads
                 // bytes the (even CTA's) full barrier receives per stage, from the whole group
-                const uint32_t tx = CG * (kStageA + (uint32_t)half * BK * 2);
+                const uint32_t tx = yt_unit ? CG * (kStageA + (uint32_t)p.yt_rows * BK * 2)
+                                            : CG * (kStageA + (uint32_t)half * BK * 2);
                 for (int kb = 0; kb < w.nk; ++kb) {
                     if (kb == w.kmain && p.flags) {
-                        // the expand reads U rows written by this tile's shrink unit
+                        // the expand reads U rows written by this tile's shrink unit (a token-column
+                        // unit: by every tile's)
                         int fok = 1;
-                        if (lane == 0) fok = wait_flag(&p.flags[w.tile_index], 1, abort_flag, p.status, limit);
+                        if (lane == 0) {
+                            if (yt_unit) {
+                                for (int i = 0; i < p.n_flags && fok; ++i)
+                                    fok = wait_flag(&p.flags[i], 1, abort_flag, p.status, limit);
+                            } else {
+                                fok = wait_flag(&p.flags[w.tile_index], 1, abort_flag, p.status, limit);
+                            }
+                        }
                         if (!__shfl_sync(0xffffffffu, fok, 0)) {
                             ok = false;
                             break;
@@ -291,9 +357,18 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
                     const uint32_t sa = smem_addr(a_ring + (size_t)stage * kStageA);
                     const uint32_t sb = smem_addr(b_ring + (size_t)stage * b_stage_bytes);
                     const int k = main ? (w.kb0 + kb) * BK : (kb - w.kmain) * BK;
-                    tma_load_2d<CG>(sa, main ? &p.tm_x : &p.tm_u, fb, k, main ? w.tile.row0 : w.tile.u_row, issuer);
-                    if (!prefetched)
-                        tma_load_2d<CG>(sb, main ? bmain : &wl.tm_b[ad - 1], fb, k, w.n0 + rank * half, issuer);
+                    if (yt_unit) {
+                        // A: this CTA's 128 output features of W (B_a); B: its token rows of X (U)
+                        if (!prefetched)
+                            tma_load_2d<CG>(sa, main ? &p.tm_w : &wl.tm_b[ad - 1], fb, k, w.n0 + rank * kTileM,
+                                            issuer);
+                        tma_load_2d<CG>(sb, main ? &p.tm_xt : &p.tm_u, fb, k, rank * p.yt_rows, issuer);
+                    } else {
+                        tma_load_2d<CG>(sa, main ? &p.tm_x : &p.tm_u, fb, k, main ? w.tile.row0 : w.tile.u_row,
+                                        issuer);
+                        if (!prefetched)
+                            tma_load_2d<CG>(sb, main ? bmain : &wl.tm_b[ad - 1], fb, k, w.n0 + rank * half, issuer);
+                    }
                     ++issued;
                     if (++stage == stages) { stage = 0; phase ^= 1; }
                 }
@@ -327,10 +402,15 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
             int it = 0;
             bool ok = true;
             for (int u = group; u < n_units && ok; u += n_groups, ++it) {
-                const Unit w = decode_unit(p, wl, u, rank);
+                const Unit w = decode_unit<YT>(p, wl, u, rank);
                 const uint32_t idesc = instr_desc_bf16(kTileM * CG, w.n);
-                const int acc = it & 1;
-                if (!wait_warp(smem_addr(&tempty[acc]), ((it >> 1) & 1) ^ 1, abort_flag, p.status, limit)) {
+                // token-column units past 128 token rows per CTA: a second MMA per 16-wide K-step
+                // over the stage's remaining token rows, into the accumulator columns after the first's
+                const bool mma2 = YT && !w.shrink && p.yt_rows > p.yt_h;
+                const uint32_t idesc2 = instr_desc_bf16(kTileM * CG, 2 * (p.yt_rows - p.yt_h));
+                const uint64_t b_off2 = (uint64_t)((p.yt_h * BK * 2) >> 4);
+                const int acc = it % n_acc;
+                if (!wait_warp(smem_addr(&tempty[acc]), ((it / n_acc) & 1) ^ 1, abort_flag, p.status, limit)) {
                     ok = false;
                     break;
                 }
@@ -355,11 +435,23 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
                         const int st = j ? st1 : stage;
                         const uint64_t ad = smem_desc<BK>(smem_addr(a_ring + (size_t)st * kStageA));
                         const uint64_t bd = smem_desc<BK>(smem_addr(b_ring + (size_t)st * b_stage_bytes));
+                        if (!mma2) {
 #pragma unroll
-                        for (int k = 0; k < BK / 16; ++k) {
-                            // advance 16 bf16 = 32 bytes along K inside the swizzled rows
-                            mma_bf16<CG>(d, ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), idesc,
-                                         (kb + j > 0 || k > 0) ? 1u : 0u, issuer);
+                            for (int k = 0; k < BK / 16; ++k) {
+                                // advance 16 bf16 = 32 bytes along K inside the swizzled rows
+                                mma_bf16<CG>(d, ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), idesc,
+                                             (kb + j > 0 || k > 0) ? 1u : 0u, issuer);
+                            }
+                        } else {
+#pragma unroll
+                            for (int k = 0; k < BK / 16; ++k) {
+                                mma_bf16<CG>(d, ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), idesc,
+                                             (kb + j > 0 || k > 0) ? 1u : 0u, issuer);
+                                // the stage rows past the first yt_h (whole 1024-byte swizzle atoms)
+                                mma_bf16<CG>(d + (uint32_t)w.n, ad + (uint64_t)(2 * k),
+                                             bd + b_off2 + (uint64_t)(2 * k), idesc2,
+                                             (kb + j > 0 || k > 0) ? 1u : 0u, issuer);
+                            }
                         }
                         mma_commit<CG>(smem_addr(&empty[st]), issuer);
                     }
@@ -393,11 +485,11 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
         if (p.pdl) griddep_wait();                   // global reads and writes follow the previous kernel
         int it = 0;
         for (int u = group; u < n_units; u += n_groups, ++it) {
-            const Unit w = decode_unit(p, wl, u, rank);
-            const int acc = it & 1;
+            const Unit w = decode_unit<YT>(p, wl, u, rank);
+            const int acc = it % n_acc;
             int ok = 1;
             if (lane == 0)
-                ok = wait_bounded(smem_addr(&tfull[acc]), (it >> 1) & 1, abort_flag, p.status, limit, true);
+                ok = wait_bounded(smem_addr(&tfull[acc]), (it / n_acc) & 1, abort_flag, p.status, limit, true);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (split_launch) ok = epilogue_bar_and(ok);
             if (!ok) break;
@@ -421,82 +513,86 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
                 if (tk & 2) break;                   // the wait ran out: the CTA is aborting
                 first = (tk & 1) != 0;
             }
-            const int row = w.tile.row0 + r_local;
-            const bool row_ok = r_local < w.tile.nrows;
-            float scale = 1.0f;
-            __nv_bfloat16* out;
-            int n_out;
-            if (w.shrink) {
-                const int a = row_ok ? row_adapter(wl.seg_off, wl.seg_id, p.n_seg, row) : 0;
-                scale = (a == w.tile.adapter) ? wl.scales[w.tile.adapter - 1] : 0.0f;
-                out = reinterpret_cast<__nv_bfloat16*>(p.u) + (size_t)row * p.rank;
-                n_out = p.rank;
-            } else {
-                out = reinterpret_cast<__nv_bfloat16*>(p.y) + (size_t)row * p.d_out + w.n0;
-                n_out = p.d_out - w.n0;
-            }
             const uint32_t taddr = tmem_base + (uint32_t)(acc * kAccCols) + lane_off;
-            // partial sums of this row: part q's float4 chunk j (columns n0 + 4j ..) at
-            // part_base[(q * part_chunks + j) * part_rows]
-            const size_t part_stride = (size_t)p.part_chunks * p.part_rows;    // one part's slot
-            float4* part = split ? p.partials + (size_t)w.pchunk * p.part_rows + row : nullptr;
-            for (int c = 0; c < w.n; c += 32) {
-                uint32_t v[32];
-                const bool two = c + 16 < w.n;  // w.n is a multiple of 16
-                tmem_ld16(taddr + (uint32_t)c, v);
-                if (two) tmem_ld16(taddr + (uint32_t)c + 16, v + 16);
-                tmem_ld_wait();
-                if (row_ok && split) {
-                    if (first) {
-                        float4* pc = part + (size_t)w.part * part_stride + (size_t)(c >> 2) * p.part_rows;
+            if (YT && !w.shrink) {
+                yt_store(p, taddr, w.n0 + rank * kTileM + r_local);
+            } else {
+                const int row = w.tile.row0 + r_local;
+                const bool row_ok = r_local < w.tile.nrows;
+                float scale = 1.0f;
+                __nv_bfloat16* out;
+                int n_out;
+                if (w.shrink) {
+                    const int a = row_ok ? row_adapter(wl.seg_off, wl.seg_id, p.n_seg, row) : 0;
+                    scale = (a == w.tile.adapter) ? wl.scales[w.tile.adapter - 1] : 0.0f;
+                    out = reinterpret_cast<__nv_bfloat16*>(p.u) + (size_t)row * p.rank;
+                    n_out = p.rank;
+                } else {
+                    out = reinterpret_cast<__nv_bfloat16*>(p.y) + (size_t)row * p.d_out + w.n0;
+                    n_out = p.d_out - w.n0;
+                }
+                // partial sums of this row: part q's float4 chunk j (columns n0 + 4j ..) at
+                // part_base[(q * part_chunks + j) * part_rows]
+                const size_t part_stride = (size_t)p.part_chunks * p.part_rows;    // one part's slot
+                float4* part = split ? p.partials + (size_t)w.pchunk * p.part_rows + row : nullptr;
+                for (int c = 0; c < w.n; c += 32) {
+                    uint32_t v[32];
+                    const bool two = c + 16 < w.n;  // w.n is a multiple of 16
+                    tmem_ld16(taddr + (uint32_t)c, v);
+                    if (two) tmem_ld16(taddr + (uint32_t)c + 16, v + 16);
+                    tmem_ld_wait();
+                    if (row_ok && split) {
+                        if (first) {
+                            float4* pc = part + (size_t)w.part * part_stride + (size_t)(c >> 2) * p.part_rows;
 #pragma unroll
-                        for (int h = 0; h < 8; ++h)
-                            if ((h < 4 || two) && c + 4 * h < n_out)
-                                __stcg(pc + (size_t)h * p.part_rows,
-                                       make_float4(__uint_as_float(v[4 * h]), __uint_as_float(v[4 * h + 1]),
-                                                   __uint_as_float(v[4 * h + 2]), __uint_as_float(v[4 * h + 3])));
-                    } else {
-                        // the sum in part order; each other part's eight loads of the chunk are in
-                        // flight at once (addresses past the block's last column are clamped to it;
-                        // those sums are never stored)
-                        const int last = (n_out - 1) >> 2;
-                        float acc[32];
-                        for (int q = 0; q < n_parts; ++q) {
-                            float t[32];
-                            if (q == w.part) {
+                            for (int h = 0; h < 8; ++h)
+                                if ((h < 4 || two) && c + 4 * h < n_out)
+                                    __stcg(pc + (size_t)h * p.part_rows,
+                                           make_float4(__uint_as_float(v[4 * h]), __uint_as_float(v[4 * h + 1]),
+                                                       __uint_as_float(v[4 * h + 2]), __uint_as_float(v[4 * h + 3])));
+                        } else {
+                            // the sum in part order; each other part's eight loads of the chunk are in
+                            // flight at once (addresses past the block's last column are clamped to it;
+                            // those sums are never stored)
+                            const int last = (n_out - 1) >> 2;
+                            float acc[32];
+                            for (int q = 0; q < n_parts; ++q) {
+                                float t[32];
+                                if (q == w.part) {
 #pragma unroll
-                                for (int i = 0; i < 32; ++i) t[i] = __uint_as_float(v[i]);
-                            } else {
-                                const float4* pq = part + (size_t)q * part_stride;
-                                float4 o[8];
+                                    for (int i = 0; i < 32; ++i) t[i] = __uint_as_float(v[i]);
+                                } else {
+                                    const float4* pq = part + (size_t)q * part_stride;
+                                    float4 o[8];
 #pragma unroll
-                                for (int h = 0; h < 8; ++h)
-                                    o[h] = __ldcg(pq + (size_t)min((c >> 2) + h, last) * p.part_rows);
+                                    for (int h = 0; h < 8; ++h)
+                                        o[h] = __ldcg(pq + (size_t)min((c >> 2) + h, last) * p.part_rows);
 #pragma unroll
-                                for (int h = 0; h < 8; ++h) {
-                                    t[4 * h] = o[h].x;
-                                    t[4 * h + 1] = o[h].y;
-                                    t[4 * h + 2] = o[h].z;
-                                    t[4 * h + 3] = o[h].w;
+                                    for (int h = 0; h < 8; ++h) {
+                                        t[4 * h] = o[h].x;
+                                        t[4 * h + 1] = o[h].y;
+                                        t[4 * h + 2] = o[h].z;
+                                        t[4 * h + 3] = o[h].w;
+                                    }
                                 }
+#pragma unroll
+                                for (int i = 0; i < 32; ++i) acc[i] = q == 0 ? t[i] : acc[i] + t[i];
                             }
 #pragma unroll
-                            for (int i = 0; i < 32; ++i) acc[i] = q == 0 ? t[i] : acc[i] + t[i];
+                            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(acc[i]);
                         }
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(acc[i]);
                     }
-                }
-                if (row_ok && !first) {
+                    if (row_ok && !first) {
 #pragma unroll
-                    for (int h = 0; h < 4; ++h) {
-                        if ((h < 2 || two) && c + 8 * h < n_out) {
-                            uint4 o;
-                            o.x = pack_bf16x2(__uint_as_float(v[8 * h + 0]) * scale, __uint_as_float(v[8 * h + 1]) * scale);
-                            o.y = pack_bf16x2(__uint_as_float(v[8 * h + 2]) * scale, __uint_as_float(v[8 * h + 3]) * scale);
-                            o.z = pack_bf16x2(__uint_as_float(v[8 * h + 4]) * scale, __uint_as_float(v[8 * h + 5]) * scale);
-                            o.w = pack_bf16x2(__uint_as_float(v[8 * h + 6]) * scale, __uint_as_float(v[8 * h + 7]) * scale);
-                            *reinterpret_cast<uint4*>(out + c + 8 * h) = o;
+                        for (int h = 0; h < 4; ++h) {
+                            if ((h < 2 || two) && c + 8 * h < n_out) {
+                                uint4 o;
+                                o.x = pack_bf16x2(__uint_as_float(v[8 * h + 0]) * scale, __uint_as_float(v[8 * h + 1]) * scale);
+                                o.y = pack_bf16x2(__uint_as_float(v[8 * h + 2]) * scale, __uint_as_float(v[8 * h + 3]) * scale);
+                                o.z = pack_bf16x2(__uint_as_float(v[8 * h + 4]) * scale, __uint_as_float(v[8 * h + 5]) * scale);
+                                o.w = pack_bf16x2(__uint_as_float(v[8 * h + 6]) * scale, __uint_as_float(v[8 * h + 7]) * scale);
+                                *reinterpret_cast<uint4*>(out + c + 8 * h) = o;
+                            }
                         }
                     }
                 }
@@ -595,9 +691,9 @@ size_t gemm_smem_bytes(int b_tile_rows, int stages, int bk, int a_rows) {
            8 * (2 * (size_t)stages + 5) + 16;
 }
 
-template <int BK, int CG>
+template <int BK, int CG, bool YT = false>
 static cudaError_t set_smem_attr() {
-    return cudaFuncSetAttribute(dev::lora_gemm_kernel<BK, CG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    return cudaFuncSetAttribute(dev::lora_gemm_kernel<BK, CG, YT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 kSmemLimit);
 }
 
@@ -605,6 +701,7 @@ cudaError_t gemm_prepare_device() {
     cudaError_t e;
     if ((e = set_smem_attr<64, 1>()) != cudaSuccess) return e;
     if ((e = set_smem_attr<64, 2>()) != cudaSuccess) return e;
+    if ((e = set_smem_attr<64, 2, true>()) != cudaSuccess) return e;
     if ((e = set_smem_attr<32, 1>()) != cudaSuccess) return e;
     return set_smem_attr<32, 2>();
 }
@@ -621,9 +718,14 @@ static bool cooperative_launches() {
     return on;
 }
 
+int gemm_b_rows(const GemmParams& p) {
+    if (p.yt) return p.yt_rows > p.shrink_n / p.cluster_size ? p.yt_rows : p.shrink_n / p.cluster_size;
+    return (p.tile_n > p.shrink_n ? p.tile_n : p.shrink_n) / p.cluster_size;
+}
+
 static void launch_config(const GemmParams& p, int grid, cudaStream_t stream, cudaLaunchConfig_t* cfg,
                           cudaLaunchAttribute* attr /* [3] */) {
-    const int b_rows = (p.tile_n > p.shrink_n ? p.tile_n : p.shrink_n) / p.cluster_size;
+    const int b_rows = gemm_b_rows(p);
     *cfg = cudaLaunchConfig_t{};
     cfg->gridDim = dim3(grid, 1, 1);
     cfg->blockDim = dim3(kThreads, 1, 1);
@@ -653,10 +755,11 @@ static void launch_config(const GemmParams& p, int grid, cudaStream_t stream, cu
 
 template <typename F>
 static cudaError_t dispatch(const GemmParams& p, F&& f) {
-    if (p.bk == 64 && p.cluster_size == 1) return f(dev::lora_gemm_kernel<64, 1>);
-    if (p.bk == 64 && p.cluster_size == 2) return f(dev::lora_gemm_kernel<64, 2>);
-    if (p.bk == 32 && p.cluster_size == 1) return f(dev::lora_gemm_kernel<32, 1>);
-    if (p.bk == 32 && p.cluster_size == 2) return f(dev::lora_gemm_kernel<32, 2>);
+    if (p.yt) return p.bk == 64 && p.cluster_size == 2 ? f(dev::lora_gemm_kernel<64, 2, true>) : cudaErrorInvalidValue;
+    if (p.bk == 64 && p.cluster_size == 1) return f(dev::lora_gemm_kernel<64, 1, false>);
+    if (p.bk == 64 && p.cluster_size == 2) return f(dev::lora_gemm_kernel<64, 2, false>);
+    if (p.bk == 32 && p.cluster_size == 1) return f(dev::lora_gemm_kernel<32, 1, false>);
+    if (p.bk == 32 && p.cluster_size == 2) return f(dev::lora_gemm_kernel<32, 2, false>);
     return cudaErrorInvalidValue;
 }
 

@@ -113,7 +113,33 @@ struct GemmParams {
     // ends; only the W tiles of its first unit's first ring stages are loaded before it waits for
     // that kernel, and it lets the next kernel start early in turn
     int pdl;
+    // Token-column units (yt = 1, SM pairs, K-steps of 64): every fused unit computes a block of
+    // Y^T, 256 output features (the MMA's M: 128 per CTA of the pair) for every token row of the
+    // batch (the MMA's N), so a W tile is read once for all rows and no row tile is padded. CTA r
+    // of the pair holds token rows [r * yt_rows, (r + 1) * yt_rows) of each stage. The first MMA
+    // of a 16-wide K-step takes rows [0, yt_h) of both CTAs' stages (N = 2 yt_h) into accumulator
+    // columns [0, 2 yt_h); when yt_rows > yt_h a second takes rows [yt_h, yt_rows) (N = 2 (yt_rows
+    // - yt_h)) into the columns after them. The launch runs n_ntiles such units (n_fused = 1).
+    // Every token row names the same adapter, yt_adapter (0: none, no expand); the expand reads U
+    // through tm_u, whose box is then yt_rows rows.
+    int yt;
+    int yt_tokens;                   // T: token rows stored
+    int yt_rows;                     // token rows per CTA per stage (a multiple of 8, <= 256)
+    int yt_h;                        // token rows per CTA of the first MMA (a multiple of 8, <= 128)
+    int yt_adapter;
+    CUtensorMap tm_xt;               // X [T, d_in], box 64 x yt_rows (token-column units)
 };
+
+// Token rows per CTA and per CTA of the first MMA of a token-column launch for T rows
+// (T <= 2 * kMaxYtRows): an SM pair holds 2 * rows token rows; past 128 rows per CTA the first
+// MMA takes 128 of them (N = 256) and a second the rest.
+constexpr int kMaxYtRows = 256;
+inline void yt_split(int T, int* rows, int* h) {
+    int tb = (T + 1) / 2;
+    tb = (tb + 7) / 8 * 8;
+    *rows = tb;
+    *h = tb < 128 ? tb : 128;
+}
 
 // The plan of one call: merged segments and tiles, ids remapped to compact adapter slots.
 struct Plan {
@@ -131,6 +157,7 @@ size_t gemm_smem_bytes(int b_tile_rows, int stages, int bk, int a_rows = kTileM)
 cudaError_t gemm_prepare_device();           // sets the opt-in smem limit on the current device
 cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t stream);
 int gemm_max_clusters(const GemmParams& p);  // co-resident clusters of this launch shape
+int gemm_b_rows(const GemmParams& p);        // B rows of one CTA's pipeline stage
 cudaError_t w4_repack(const void* src, void* dst, long long n_words, int grid, cudaStream_t stream);
 
 }  // namespace lora

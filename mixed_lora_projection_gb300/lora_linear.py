@@ -256,7 +256,8 @@ class LoraLinear:
     def describe(self, T, seg_offsets, seg_ids) -> dict:
         off, _ = _i32(seg_offsets)
         ids, n = _i32(seg_ids)
-        v = [C.c_int() for _ in range(6)]
+        v = [C.c_int() for _ in range(7)]
         _check(self._lib.lora_linear_describe(self._h, T, off, ids, n, *[C.byref(x) for x in v]),
                "lora_linear_describe")
-        return dict(zip(("tile_n", "n_tiles", "n_units", "grid", "stages", "has_shrink"), [x.value for x in v]))
+        return dict(zip(("tile_n", "n_tiles", "n_units", "grid", "stages", "has_shrink", "unit_order"),
+                        [x.value for x in v]))

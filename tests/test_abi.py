@@ -164,11 +164,12 @@ def test_create_without_a_gpu_reports_no_device(lib):
 
 # the launch-shape model's choices for the configured workloads on a 152-SM GB300 (SM pairs
 # with 256 columns for the prefills and mixed batches, grouped column tiles for the prefills,
-# single CTAs with 240 columns for the decode and near-ridge batches, the sweep's widths)
+# single CTAs with 240 columns for the decode batch, token-column units of 256 features for the
+# near-ridge batch, the sweep's widths)
 SHAPES = {
     "prefill_16k": (2, 256, 2), "prefill_32k": (2, 256, 2), "mixed_batch": (2, 256, 1),
     "mixed_8x300": (2, 256, 1), "prefix_tail_1552": (2, 256, 1), "mixed_decode": (1, 240, None),
-    "mixed_near_ridge": (1, 240, None), "sweep_qkv": (2, 224, None), "sweep_o": (2, 192, None),
+    "mixed_near_ridge": (2, 256, 3), "sweep_qkv": (2, 224, None), "sweep_o": (2, 192, None),
     "sweep_gate_up": (2, 256, None), "sweep_down": (2, 192, None),
 }
 # K halves chosen by a handle of max_tokens = the workload's rows: none of the configured
@@ -188,10 +189,10 @@ def test_launch_shape_model_choices(lib, name):
     assert (s["cluster"], s["tile_n"]) == (cluster, tile_n), s
     if order is not None:
         assert s["unit_order"] == order, s
-    # work units: every fused group crosses every column tile once; one shrink unit per group of
-    # adapter tiles
+    # work units: every fused group crosses every column tile once (token-column units: one group
+    # of every row); one shrink unit per group of adapter tiles
     n_tiles = -(-w.T // 128)
-    groups = -(-n_tiles // cluster)
+    groups = 1 if s["unit_order"] == 3 else -(-n_tiles // cluster)
     assert s["fused_units"] >= groups * -(-w.d_out // tile_n) - 1
     assert (s["shrink_units"] == 0) == (w.adapter_rows == 0)
     assert s["bk"] == 64 and 2 <= s["stages"] <= 16
@@ -230,6 +231,32 @@ def test_k_split_rule(lib):
         k_split(6144, 5120, 256, 48, 1)          # fewer than 2 SMs
     with pytest.raises(LoraError):
         k_split(6144, 5120, 300, 48, 152)        # rank above 256
+
+
+def test_token_column_rule(lib):
+    from mixed_lora_projection_gb300 import launch_shape
+
+    def order(d_in, d_out, T, off, ids, sms=152):
+        return launch_shape(d_in, d_out, 256, sms, T, off, ids)["unit_order"]
+    # gate_up batches of 129 to 512 rows with one adapter (or none) take token-column units:
+    # 256 output features of an SM pair for every row, 136 units
+    for T in (129, 160, 200, 256, 300, 348, 400, 512):
+        for off, ids in (((0, 48, T), (0, 1)), ((0, T), (0,)), ((0, T), (1,))):
+            s = launch_shape(5120, 34816, 256, 152, T, off, ids)
+            assert s["unit_order"] == 3 and s["cluster"] == 2 and s["tile_n"] == 256, (T, ids)
+            assert s["fused_units"] == 136 and s["shrink_units"] == (0 if ids == (0,) else -(-(-(-T // 128)) // 2))
+    # not: one tile (a decode step), more than 512 rows, two adapters, a base-only tile next to an
+    # adapter tile, handles that split K (o and down up to 384 rows), 20 units on 76 SM pairs (o and
+    # down past 384 rows), qkv's 300- and 348-row base batches (row tiles measured faster)
+    assert order(5120, 34816, 48, (0, 48), (0,)) != 3
+    assert order(5120, 34816, 513, (0, 513), (0,)) != 3
+    assert order(5120, 34816, 300, (0, 100, 300), (1, 2)) != 3
+    assert order(5120, 34816, 300, (0, 128, 300), (0, 1)) != 3
+    for d_in in (6144, 17408):
+        for T in (200, 348, 400, 512):
+            assert order(d_in, 5120, T, (0, 48, T), (0, 1)) != 3, (d_in, T)
+    assert order(5120, 12288, 300, (0, 300), (0,)) != 3 and order(5120, 12288, 348, (0, 348), (0,)) != 3
+    assert order(5120, 12288, 400, (0, 400), (0,)) == 3 and order(5120, 12288, 512, (0, 48, 512), (0, 1)) == 3
 
 
 def test_launch_shape_of_an_empty_batch_and_bad_arguments(lib):
