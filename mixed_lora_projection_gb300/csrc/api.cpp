@@ -373,19 +373,26 @@ double makespan(const lora_linear* h, const std::vector<Tile>& fused_groups, con
 
 // Per-SM cycles of one 64-wide K-step of a token-column unit whose pair holds 2 * rows token
 // rows, its epilogue included, fitted to gate_up (5,120 -> 34,816) and qkv (5,120 -> 12,288)
-// batches of 200 to 512 rows timed on GB300: one MMA per 16-wide step up to 128 rows per CTA
-// (~1,020 cycles at 100 rows), a second one and a single accumulator (its epilogue no longer
-// overlaps the next unit) past it (~1,300 cycles at 152 rows, ~1,650 at 256). These units
-// stream W from memory, so they run well above their MMA time.
-double yt_kstep_cycles(int rows) {
-    return rows <= kTileM ? 940.0 + 0.8 * rows : 790.0 + 3.35 * rows;
+// batches of 200 to 512 rows without adapter rows timed on GB300: one MMA per 16-wide step up to
+// 128 rows per CTA (~940 cycles at 100 rows), a second one (from a second warp) and a single
+// accumulator, whose epilogue no longer overlaps the next unit, past it (~1,150 cycles at 152
+// rows, ~1,700 at 256). Units with an expand took ~8% more per K-step (the shrink units beside
+// them and the wait for their flags). These units stream W from memory, so they run well above
+// their MMA time.
+double yt_kstep_cycles(int rows, bool adapter) {
+    const double c = rows <= kTileM ? 850.0 + 0.9 * rows : 340.0 + 5.3 * rows;
+    return adapter ? 1.08 * c : c;
 }
 
 // The row-tile model (kstep_cycles) is fitted to the tensor-bound shapes of large batches; on
-// the batches token-column units serve (at most 512 rows, W streamed from memory) row tiles
-// took 1.3-1.8x its makespan (gate_up and qkv, 200 to 512 rows). Token-column units are chosen
-// when their makespan is below the row-tile makespan times this factor.
-constexpr double kRowTileSmallBatchFactor = 1.45;
+// the batches token-column units serve (W streamed from memory) row tiles took 1.05-1.67x its
+// makespan (gate_up and qkv, 200 to 512 rows). Token-column units are chosen when their makespan
+// is below the row-tile makespan times this factor (the factor that lost least time over those
+// 24 timed batches), and only up to kMaxYtAutoRows rows: past that the row tiles are four nearly
+// full 128-row tiles on SM pairs and token-column units hold all of TMEM (gate_up at 512 rows:
+// 134 against 115 us without adapter rows).
+constexpr double kRowTileSmallBatchFactor = 1.40;
+constexpr int kMaxYtAutoRows = 448;
 
 // Token-column units serve a batch of at most 2 * kMaxYtRows rows whose tiles all name one
 // adapter (or none), on SM pairs with 64-wide K-steps and whole K per unit; options that fix
@@ -412,7 +419,8 @@ double yt_makespan(const lora_linear* h, const Plan& plan, int slots) {
     std::vector<double> load(slots, 0.0);
     long long u = 0;
     for (size_t g = 0; g < sg.size() / 2; ++g) load[u++ % slots] += k_main * kstep_cycles(2, shrink_n);
-    const double unit = (k_main + (plan.fused[0].adapter ? k_lora : 0)) * yt_kstep_cycles(rows);
+    const bool ad = plan.fused[0].adapter != 0;
+    const double unit = (k_main + (ad ? k_lora : 0)) * yt_kstep_cycles(rows, ad);
     for (int t = 0; t < ceil_div(h->d_out, 2 * kTileM); ++t) load[u++ % slots] += unit;
     return *std::max_element(load.begin(), load.end());
 }
@@ -480,10 +488,10 @@ Shape choose_shape(lora_linear* h, const Plan& plan, bool allow_yt = true) {
             if (!cs || !tn) m = search_shape(h, plan, cs, tn, h->k_split, &cs, &tn);
             if (yt_ok) {
                 // token-column units when asked for, or, for batches of more than one row tile,
-                // when the model expects them to finish sooner
+                // when the calibrated models expect them to finish sooner
                 const int slots = usable_sms(h) / 2;
-                if (h->yt_mode == 2 ||
-                    (!cs0 && !tn0 && nf >= 2 && yt_makespan(h, plan, slots) < kRowTileSmallBatchFactor * m))
+                if (h->yt_mode == 2 || (!cs0 && !tn0 && nf >= 2 && plan.seg_off.back() <= kMaxYtAutoRows &&
+                                        yt_makespan(h, plan, slots) < kRowTileSmallBatchFactor * m))
                     yt = 1;
             }
             if (yt) {

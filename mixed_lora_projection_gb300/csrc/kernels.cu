@@ -199,7 +199,7 @@ __device__ __forceinline__ void yt_store(const GemmParams& p, uint32_t taddr, in
 }
 
 template <int BK, int CG, bool YT>
-__global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_constant__ GemmParams p) {
+__global__ void __launch_bounds__(YT ? kThreadsYt : kThreads, 1) lora_gemm_kernel(const __grid_constant__ GemmParams p) {
     static_assert(!YT || (CG == 2 && BK == 64), "token-column units run on SM pairs with 64-wide K-steps");
     // A stage: the tile's rows of X (or U) for this K-step; a batch of one short tile loads
     // only its rows (a_rows < 128), and the MMA's remaining A rows read unrelated shared memory
@@ -233,16 +233,18 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
     const int group = (int)blockIdx.x / CG;        // cluster index
     const int n_groups = (int)gridDim.x / CG;
 
+    // token-column units: two MMA warps (1 and 6) commit every stage, accumulator and drain
+    constexpr uint32_t kIssuers = YT ? 2 : 1;
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
             mbar_init(smem_addr(&full[s]), 1);
-            mbar_init(smem_addr(&empty[s]), 1);
+            mbar_init(smem_addr(&empty[s]), kIssuers);
         }
         for (int a = 0; a < 2; ++a) {
-            mbar_init(smem_addr(&tfull[a]), 1);
+            mbar_init(smem_addr(&tfull[a]), kIssuers);
             mbar_init(smem_addr(&tempty[a]), CG * kEpilogueThreads);  // both CTAs' epilogues
         }
-        mbar_init(smem_addr(drain), 1);
+        mbar_init(smem_addr(drain), kIssuers);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -391,10 +393,15 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
                 }
             }
         }
-    } else if (warp == 1) {
+    } else if (warp == 1 || (YT && warp == 6)) {
         // ------------------------------------------------------------ MMA issuer (even CTA)
-        // The whole warp runs the loop (converged); lane 0 issues the MMAs and commits.
+        // The whole warp runs the loop (converged); lane 0 issues the MMAs and commits. With
+        // token-column units warp 6 issues each K16 step's second MMA (the stage rows past the
+        // first yt_h) beside warp 1's first: one warp waits ~80 cycles between MMAs whatever their
+        // width, two warps keep the tensor pipe fed with both. Both commit every stage and
+        // accumulator (the barriers count two arrivals).
         const uint32_t issuer = lane == 0 ? 1u : 0u;
+        const bool second = YT && warp == 6;
         if (p.pdl) griddep_wait();
         if (leader) {
             int stage = 0;
@@ -435,18 +442,16 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
                         const int st = j ? st1 : stage;
                         const uint64_t ad = smem_desc<BK>(smem_addr(a_ring + (size_t)st * kStageA));
                         const uint64_t bd = smem_desc<BK>(smem_addr(b_ring + (size_t)st * b_stage_bytes));
-                        if (!mma2) {
+                        if (!second) {
 #pragma unroll
                             for (int k = 0; k < BK / 16; ++k) {
                                 // advance 16 bf16 = 32 bytes along K inside the swizzled rows
                                 mma_bf16<CG>(d, ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), idesc,
                                              (kb + j > 0 || k > 0) ? 1u : 0u, issuer);
                             }
-                        } else {
+                        } else if (mma2) {
 #pragma unroll
                             for (int k = 0; k < BK / 16; ++k) {
-                                mma_bf16<CG>(d, ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), idesc,
-                                             (kb + j > 0 || k > 0) ? 1u : 0u, issuer);
                                 // the stage rows past the first yt_h (whole 1024-byte swizzle atoms)
                                 mma_bf16<CG>(d + (uint32_t)w.n, ad + (uint64_t)(2 * k),
                                              bd + b_off2 + (uint64_t)(2 * k), idesc2,
@@ -472,7 +477,7 @@ __global__ void __launch_bounds__(kThreads, 1) lora_gemm_kernel(const __grid_con
             mma_commit_local<CG>(smem_addr(drain), issuer);
             if (lane == 0) wait_bounded(smem_addr(drain), 0, abort_flag, p.status, limit, false);
         }
-    } else {
+    } else if (warp <= 5) {
         // ------------------------------------------------------------ epilogue (warps 2..5)
         const int q = warp & 3;                      // TMEM lane quadrant this warp may read
         const int r_local = q * 32 + lane;           // tile row held by this thread
@@ -728,7 +733,7 @@ static void launch_config(const GemmParams& p, int grid, cudaStream_t stream, cu
     const int b_rows = gemm_b_rows(p);
     *cfg = cudaLaunchConfig_t{};
     cfg->gridDim = dim3(grid, 1, 1);
-    cfg->blockDim = dim3(kThreads, 1, 1);
+    cfg->blockDim = dim3(p.yt ? kThreadsYt : kThreads, 1, 1);
     cfg->dynamicSmemBytes = gemm_smem_bytes(b_rows, p.stages, p.bk, p.a_rows ? p.a_rows : kTileM);
     cfg->stream = stream;
     attr[0].id = cudaLaunchAttributeClusterDimension;

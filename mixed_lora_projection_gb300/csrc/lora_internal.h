@@ -17,6 +17,7 @@ constexpr int kStageBytesA = kTileM * kTileK * 2;      // 16 KB at K = 64
 constexpr int kMaxStages = 16;
 constexpr int kSmemLimit = 232448;                     // opt-in dynamic shared memory per CTA (227 KB)
 constexpr int kThreads = 192;        // warp 0 TMA, warp 1 MMA + TMEM owner, warps 2..5 epilogue
+constexpr int kThreadsYt = 224;      // token-column units: warp 6 issues the second MMA of each K16 step
 constexpr int kEpilogueThreads = 128;
 constexpr int kW4Group = 128;        // input features per scale of a 4-bit base
 // Work lists this small travel inside the kernel parameters (no upload copy per call).

@@ -238,25 +238,26 @@ def test_token_column_rule(lib):
 
     def order(d_in, d_out, T, off, ids, sms=152):
         return launch_shape(d_in, d_out, 256, sms, T, off, ids)["unit_order"]
-    # gate_up batches of 129 to 512 rows with one adapter (or none) take token-column units:
+    # gate_up batches of 129 to 448 rows with one adapter (or none) take token-column units:
     # 256 output features of an SM pair for every row, 136 units
-    for T in (129, 160, 200, 256, 300, 348, 400, 512):
+    for T in (129, 160, 200, 256, 300, 348, 400, 448):
         for off, ids in (((0, 48, T), (0, 1)), ((0, T), (0,)), ((0, T), (1,))):
             s = launch_shape(5120, 34816, 256, 152, T, off, ids)
             assert s["unit_order"] == 3 and s["cluster"] == 2 and s["tile_n"] == 256, (T, ids)
             assert s["fused_units"] == 136 and s["shrink_units"] == (0 if ids == (0,) else -(-(-(-T // 128)) // 2))
-    # not: one tile (a decode step), more than 512 rows, two adapters, a base-only tile next to an
-    # adapter tile, handles that split K (o and down up to 384 rows), 20 units on 76 SM pairs (o and
-    # down past 384 rows), qkv's 300- and 348-row base batches (row tiles measured faster)
+    # not: one tile (a decode step), more than 448 rows (four nearly full row tiles on SM pairs;
+    # only on request, up to 512), two adapters, a base-only tile next to an adapter tile, handles
+    # that split K (o and down up to 384 rows), 20 units on 76 SM pairs (o and down past 384 rows),
+    # qkv's 300- and 348-row base batches (row tiles measured faster)
     assert order(5120, 34816, 48, (0, 48), (0,)) != 3
-    assert order(5120, 34816, 513, (0, 513), (0,)) != 3
+    assert order(5120, 34816, 512, (0, 512), (0,)) != 3 and order(5120, 34816, 513, (0, 513), (0,)) != 3
     assert order(5120, 34816, 300, (0, 100, 300), (1, 2)) != 3
     assert order(5120, 34816, 300, (0, 128, 300), (0, 1)) != 3
     for d_in in (6144, 17408):
         for T in (200, 348, 400, 512):
             assert order(d_in, 5120, T, (0, 48, T), (0, 1)) != 3, (d_in, T)
     assert order(5120, 12288, 300, (0, 300), (0,)) != 3 and order(5120, 12288, 348, (0, 348), (0,)) != 3
-    assert order(5120, 12288, 400, (0, 400), (0,)) == 3 and order(5120, 12288, 512, (0, 48, 512), (0, 1)) == 3
+    assert order(5120, 12288, 400, (0, 400), (0,)) == 3 and order(5120, 12288, 448, (0, 48, 448), (0, 1)) == 3
 
 
 def test_launch_shape_of_an_empty_batch_and_bad_arguments(lib):
