@@ -19,14 +19,18 @@
 //   warp 0      TMA: X tiles (base K-steps), U and B_a tiles (expand K-steps);
 //   warp 1      TMEM owner (512 columns: one 128 x 256 fp32 accumulator and one 32-column
 //               stage of dequantised A per ring stage), issues the MMAs: one wait per two
-//               ring stages, four MMAs per feature tile and one commit per K-step;
+//               ring stages, four MMAs per feature tile and one commit per K-step; with two
+//               feature tiles per unit it issues the first tile's and warp 15 the second's
+//               (one warp waits ~80 cycles between MMAs whatever their width, and these MMAs
+//               are narrow: two warps keep the tensor pipe fed with both tiles);
 //   warps 2..5  epilogue: warp w reads lanes 32 (w % 4) .. (one output feature per thread),
 //               stages each whole 32-token chunk of Y in shared memory ([token][feature])
 //               and writes it with one TMA store (a tile's ragged last chunk from registers);
 //   warps 6..13 converters: warp w dequantises whole K-steps (6..9 the even ring stages,
 //               10..13 the odd ones) for the 32 features of lane quadrant w % 4, packed
 //               ring -> TMEM, and counts itself in on the stage's full barrier;
-//   warp 14     TMA of the packed base and its scales (4 K-steps per box) into their ring.
+//   warp 14     TMA of the packed base and its scales (4 K-steps per box) into their ring;
+//   warp 15     with two feature tiles per unit: the second tile's MMAs (see warp 1).
 // Every wait is bounded as in the bf16 kernel (status word, abort flag, orderly exit).
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -156,18 +160,20 @@ __global__ void __launch_bounds__(kW4Threads, 1) lora_w4_kernel(const __grid_con
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
+    // MMA warps: one per feature tile of a unit, each commits every stage, accumulator and drain
+    constexpr uint32_t kIssuers = FT;
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
             mbar_init(smem_addr(&full[s]), 1 + kW4ConvertWarps / 2);
-            mbar_init(smem_addr(&empty[s]), 1);
+            mbar_init(smem_addr(&empty[s]), kIssuers);
         }
         for (int s = 0; s < pstages; ++s) {
             mbar_init(smem_addr(&pfull[s]), 1);
             mbar_init(smem_addr(&pempty[s]), kW4ConvertWarps);
         }
-        mbar_init(smem_addr(tfull), 1);
+        mbar_init(smem_addr(tfull), kIssuers);
         mbar_init(smem_addr(tempty), kEpilogueThreads);
-        mbar_init(smem_addr(drain), 1);
+        mbar_init(smem_addr(drain), kIssuers);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -280,9 +286,12 @@ __global__ void __launch_bounds__(kW4Threads, 1) lora_w4_kernel(const __grid_con
                                  limit, false);
             }
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
+    } else if (warp == 1 || (FT == 2 && warp == 15)) {
+        // ------------------------------------------------------------ MMA issuers
+        // Warp 1 issues feature tile 0's MMAs (and the expand's), warp 15 tile 1's; both walk
+        // every stage and commit it.
         const uint32_t issuer = lane == 0 ? 1u : 0u;
+        const int my_tile = (FT == 2 && warp == 15) ? 1 : 0;
         int stage = 0;
         uint32_t phase = 0;
         int it = 0;
@@ -312,12 +321,11 @@ __global__ void __launch_bounds__(kW4Threads, 1) lora_w4_kernel(const __grid_con
                 for (int j = 0; j < 2; ++j) {
                     const int st = j ? st1 : stage;
                     const uint64_t bd = smem_desc<64>(smem_addr(x_ring + (size_t)st * x_stage));
+                    const int f = my_tile;
 #pragma unroll
-                    for (int f = 0; f < FT; ++f)
-#pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            mma_tmem_a(tmem_base + (uint32_t)(128 * f), tmem_a + kAStageCols * st + (uint32_t)(32 * f + 8 * k),
-                                       bd + (uint64_t)(2 * k), idesc, (kb > 0 || j > 0 || k > 0) ? 1u : 0u, issuer);
+                    for (int k = 0; k < 4; ++k)
+                        mma_tmem_a(tmem_base + (uint32_t)(128 * f), tmem_a + kAStageCols * st + (uint32_t)(32 * f + 8 * k),
+                                   bd + (uint64_t)(2 * k), idesc, (kb > 0 || j > 0 || k > 0) ? 1u : 0u, issuer);
                     mma_commit<1>(smem_addr(&empty[st]), issuer);
                 }
                 stage = st1 + 1;
@@ -343,10 +351,12 @@ __global__ void __launch_bounds__(kW4Threads, 1) lora_w4_kernel(const __grid_con
                         const uint32_t xs = smem_addr(x_ring + (size_t)st * x_stage);
                         const uint64_t ad = smem_desc<64>(xs + 16384u);
                         const uint64_t bd = smem_desc<64>(xs);
+                        if (my_tile == 0) {
 #pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            mma_bf16<1>(tmem_base + (uint32_t)(128 * h), ad + (uint64_t)(2 * k),
-                                        bd + (uint64_t)(2 * k), idesc_e, 1u, issuer);
+                            for (int k = 0; k < 4; ++k)
+                                mma_bf16<1>(tmem_base + (uint32_t)(128 * h), ad + (uint64_t)(2 * k),
+                                            bd + (uint64_t)(2 * k), idesc_e, 1u, issuer);
+                        }
                         mma_commit<1>(smem_addr(&empty[st]), issuer);
                     }
                     if (ns == 2) {
@@ -366,7 +376,7 @@ __global__ void __launch_bounds__(kW4Threads, 1) lora_w4_kernel(const __grid_con
         // every MMA this warp issued has completed before TMEM is released
         mma_commit_local<1>(smem_addr(drain), issuer);
         if (lane == 0) wait_bounded(smem_addr(drain), 0, abort_flag, p.status, limit, false);
-    } else if (warp >= 6) {
+    } else if (warp >= 6 && warp <= 13) {
         // ------------------------------------------------------------ converters (warps 6..13)
         // Kernel layout of the packed base (lora_linear_w4_repack): 32-bit word c of a row's
         // K-step holds inputs 8c..8c+7 as offset-binary nibbles (q + 8), input 8c+2j in nibble
@@ -464,7 +474,7 @@ __global__ void __launch_bounds__(kW4Threads, 1) lora_w4_kernel(const __grid_con
                 }
             }
         }
-    } else {
+    } else if (warp >= 2 && warp <= 5) {
         // ------------------------------------------------------------ epilogue (warps 2..5)
         const int q = warp & 3;
         const uint32_t lane_off = (uint32_t)(32 * q) << 16;

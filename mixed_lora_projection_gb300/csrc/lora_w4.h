@@ -12,8 +12,9 @@ namespace lora {
 // its X rows form the B operand of up to 256 columns. Units = groups x output tiles of 128
 // features, in the order W4Params::tokens_fastest selects.
 constexpr int kW4TileM = 128;         // output features per unit (TMEM lanes)
-constexpr int kW4Threads = 480;       // warp 0 TMA (X, U, B_a), 1 MMA, 2..5 epilogue,
-                                      // 6..13 dequantise into TMEM, 14 TMA of the packed base
+constexpr int kW4Threads = 512;       // warp 0 TMA (X, U, B_a), 1 MMA, 2..5 epilogue,
+                                      // 6..13 dequantise into TMEM, 14 TMA of the packed base,
+                                      // 15 the second feature tile's MMAs (two tiles per unit)
 constexpr int kW4ConvertWarps = 8;
 constexpr int kW4AStages = 8;         // most ring stages (TMEM A stages of 32 columns each)
 constexpr int kW4InlineGroups = 48;
