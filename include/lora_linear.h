@@ -255,13 +255,20 @@ enum {
                                    reads or writes anything else; it lets the next kernel start early in turn.
                                    The previous kernel must not write this call's W. 0 (default) = off.
                                    Does not change any result */
-    LORA_OPT_TOKEN_COLUMNS = 17 /* bf16 base: token-column units for batches of at most 512 rows whose rows
+    LORA_OPT_TOKEN_COLUMNS = 17, /* bf16 base: token-column units for batches of at most 512 rows whose rows
                                    all name one adapter (or none), on handles that sum whole K: each unit of
                                    an SM pair computes 256 output features for every token row of the batch
                                    (features on the MMA's M, tokens on its N), so each W tile is read once
                                    and no 128-row tile is padded. 0 (default) = when the launch-shape model
                                    expects them to finish sooner, 1 = never, 2 = whenever the batch allows
                                    them. Does not change any result */
+    LORA_OPT_W4_K_SPLIT = 18    /* 4-bit base: 0 = the handle's own choice (made at create: decode-sized
+                                   handles of at most 128 rows whose one-tile units would leave most SMs
+                                   idle split K in 2 to 4 parts), 1 = whole K, 2..4 = K in that many parts
+                                   (each a multiple of 4 K-steps, at least 8; fewer where K is too short).
+                                   Every part but the last to finish stores its fp32 sums, the last adds
+                                   them in part order before the bf16 rounding. Changes the summation for
+                                   later calls; may allocate (LORA_ENOMEM) */
 };
 
 /* lora_linear_set_option -- set one option above. Returns LORA_OK or LORA_EINVAL. */

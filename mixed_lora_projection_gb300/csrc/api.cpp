@@ -83,6 +83,13 @@ struct lora_linear {
     int max_ctas = 0;           // LORA_OPT_MAX_CTAS: at most this many CTAs per launch (0 = one per SM)
     int pdl = 0;                // LORA_OPT_PDL: launches without ready flags may start early
     int yt_mode = 0;            // LORA_OPT_TOKEN_COLUMNS: 0 = auto, 1 = never, 2 = whenever a batch allows
+    // 4-bit base K parts: chosen once per handle like k_split
+    int w4_k_split = 1;         // 1..4: every 4-bit block runs as that many units over parts of K
+    int w4_k_split_opt = 0;     // LORA_OPT_W4_K_SPLIT: 0 = the handle's own choice
+    float* w4_partials = nullptr;                 // [part][max_tokens][d_out] fp32
+    int w4_partial_parts = 0;
+    unsigned long long* w4_split_ctr = nullptr;   // per block {arrived, stored}, only ever growing
+    size_t w4_split_blocks = 0;
     int max_clusters_cache[2][kMaxYtRows / 8 + 1] = {};  // co-resident clusters by (size, B rows per CTA)
     // K halves: chosen once per handle (every call on it sums each output the same way)
     int k_split = 1;            // 1, 2 or 4: every block runs as that many units over parts of K
@@ -132,6 +139,8 @@ void free_handle(lora_linear* h) {
     if (h->u_ws) cudaFree(h->u_ws);
     if (h->partials) cudaFree(h->partials);
     if (h->split_ctr) cudaFree(h->split_ctr);
+    if (h->w4_partials) cudaFree(h->w4_partials);
+    if (h->w4_split_ctr) cudaFree(h->w4_split_ctr);
     if (h->status) cudaFree(h->status);
     if (h->flags) cudaFree(h->flags);
     if (h->status_host) cudaFreeHost(h->status_host);
@@ -596,6 +605,61 @@ int ensure_split_buffers(lora_linear* h) {
     return LORA_OK;
 }
 
+// K parts of the 4-bit base for a handle, decided once from its shape and max_tokens (a row's
+// bits never depend on the batch). Decode-sized handles (at most 128 rows: one token tile) of
+// narrow projections leave most SMs without a unit of one 128-feature tile (o and down on 5,120
+// outputs: 40 units for 152 SMs); they split the base K-steps into as many parts (at most 4,
+// each at least 8 K-steps, a multiple of 4) as still fit one wave of units.
+int choose_w4_k_split(const lora_linear* h) {
+    const int k64 = ceil_div(h->d_in, kTileK);
+    auto fits = [&](int s) {
+        const int chunk = ceil_div(ceil_div(k64, s), 4) * 4;
+        return s == 1 || (chunk >= 8 && (s - 1) * chunk < k64);
+    };
+    if (h->w4_k_split_opt) {
+        int s = h->w4_k_split_opt;
+        while (s > 1 && !fits(s)) --s;
+        return s;
+    }
+    if (h->max_tokens > kTileM) return 1;
+    const int units = ceil_div(h->d_out, kW4TileM);
+    int best = 1;
+    for (int s = 2; s <= 4; ++s)
+        if (units * s <= usable_sms(h) && fits(s)) best = s;
+    return best;
+}
+
+// The 4-bit K parts' device buffers: fp32 partial sums per part, and the block counters (zeroed
+// whenever they are (re)allocated or the parts change).
+int ensure_w4_split_buffers(lora_linear* h) {
+    if (h->w4_k_split < 2) return LORA_OK;
+    const size_t blocks = (size_t)h->max_fused * ceil_div(h->d_out, kW4TileM);
+    if (h->w4_partial_parts < h->w4_k_split) {
+        if (h->w4_partials) cudaFree(h->w4_partials);
+        h->w4_partials = nullptr;
+        h->w4_partial_parts = 0;
+        if (cudaMalloc((void**)&h->w4_partials,
+                       (size_t)h->w4_k_split * h->max_tokens * h->d_out * sizeof(float)) != cudaSuccess) {
+            cudaGetLastError();
+            h->w4_partials = nullptr;
+            return LORA_ENOMEM;
+        }
+        h->w4_partial_parts = h->w4_k_split;
+    }
+    if (!h->w4_split_ctr) {
+        if (cudaMalloc((void**)&h->w4_split_ctr, 2 * blocks * sizeof(unsigned long long)) != cudaSuccess) {
+            cudaGetLastError();
+            h->w4_split_ctr = nullptr;
+            return LORA_ENOMEM;
+        }
+        h->w4_split_blocks = blocks;
+    }
+    if (cudaMemset(h->w4_split_ctr, 0, 2 * h->w4_split_blocks * sizeof(unsigned long long)) != cudaSuccess ||
+        cudaDeviceSynchronize() != cudaSuccess)
+        return LORA_ECUDA;
+    return LORA_OK;
+}
+
 // Launch shape of the 4-bit kernel for a call's token groups (host logic only).
 struct W4Shape {
     int feature_tiles = 1, n_ntiles = 0, tokens_fastest = 0, x_stage_bytes = 0, stages = 4, pstages = 2;
@@ -774,6 +838,10 @@ int lora_linear_create(lora_linear** out, int d_in, int d_out, int rank, int max
         }
     }
     rc = ensure_split_buffers(h);
+    if (rc == LORA_OK) {
+        h->w4_k_split = choose_w4_k_split(h);
+        rc = ensure_w4_split_buffers(h);
+    }
     if (rc != LORA_OK) {
         free_handle(h);
         return rc;
@@ -860,6 +928,20 @@ int lora_linear_set_option(lora_linear* h, int option, long long value) {
             if (value < 0 || value > 2) return LORA_EINVAL;
             h->yt_mode = (int)value;
             return LORA_OK;
+        case LORA_OPT_W4_K_SPLIT: {
+            if (value < 0 || value > 4) return LORA_EINVAL;
+            DeviceGuard guard(h->device);
+            if (cudaDeviceSynchronize() != cudaSuccess) return LORA_ECUDA;
+            const int prev_opt = h->w4_k_split_opt, prev = h->w4_k_split;
+            h->w4_k_split_opt = (int)value;
+            h->w4_k_split = choose_w4_k_split(h);
+            const int rc = ensure_w4_split_buffers(h);
+            if (rc != LORA_OK) {
+                h->w4_k_split_opt = prev_opt;
+                h->w4_k_split = prev;
+            }
+            return rc;
+        }
         case LORA_OPT_MAX_CTAS:
             if (value < 0 || value > (1 << 20) || (value > 0 && value < 2)) return LORA_EINVAL;
             h->max_ctas = (int)value;
@@ -912,6 +994,10 @@ int lora_linear_status(lora_linear* h, int reset) {
     int v = 0;
     if (cudaMemcpy(&v, h->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return LORA_ECUDA;
     if (reset && cudaMemset(h->status, 0, sizeof(int)) != cudaSuccess) return LORA_ECUDA;
+    // a launch that gave up part-way may leave the 4-bit K-part counters between launches' counts
+    if (reset && v && h->w4_split_ctr &&
+        cudaMemset(h->w4_split_ctr, 0, 2 * h->w4_split_blocks * sizeof(unsigned long long)) != cudaSuccess)
+        return LORA_ECUDA;
     if (reset && cudaDeviceSynchronize() != cudaSuccess) return LORA_ECUDA;
     return v ? LORA_ETIMEOUT : LORA_OK;
 }
@@ -1244,6 +1330,16 @@ int forward_impl(lora_linear* h, const void* x, int T, const int32_t* seg_offset
         q.k_pack_blocks = ceil_div(q.k_main_blocks, 4);
         q.d_out = h->d_out;
         q.x_stage_bytes = w4s.x_stage_bytes;
+        if (h->w4_k_split > 1) {
+            if (!h->w4_partials || h->w4_partial_parts < h->w4_k_split || !h->w4_split_ctr ||
+                (size_t)n_w4g * w4s.n_ntiles > h->w4_split_blocks || T > h->max_tokens)
+                return LORA_ENOMEM;
+            q.k_split = h->w4_k_split;
+            q.k_chunk = ceil_div(ceil_div(ceil_div(h->d_in, 64), h->w4_k_split), 4) * 4;
+            q.partials = h->w4_partials;
+            q.part_rows = h->max_tokens;
+            q.split_ctr = h->w4_split_ctr;
+        }
         q.stages = w4s.stages;
         q.pstages = w4s.pstages;
         // whole 32-row chunks of Y leave through TMA stores (Y 16-byte aligned, d_out % 8 == 0:
@@ -1252,7 +1348,7 @@ int forward_impl(lora_linear* h, const void* x, int T, const int32_t* seg_offset
             CUDA_SUCCESS)
             return LORA_ECUDA;
         q.debug_stall = h->debug_stall;
-        const int units = q.n_groups * q.n_ntiles;
+        const int units = q.n_groups * q.n_ntiles * (q.k_split > 1 ? q.k_split : 1);
         if (launch_w4(q, std::min(units, usable_sms(h)), stream) != cudaSuccess) return LORA_ECUDA;
         ++h->launches;
     } else if (h->two_launch && nsg > 0) {
@@ -1522,6 +1618,7 @@ int lora_linear_shape(int d_in, int d_out, int rank, int num_sms, int T, const i
     h.num_sms = num_sms;
     h.u_rows = ceil_div(h.max_tokens, kTileM) * kTileM + kTileM;
     if (!w4) h.k_split = choose_k_split(&h);   // a handle of max_tokens = T
+    else h.w4_k_split = choose_w4_k_split(&h);
     for (size_t i = 0; i < plan.fused.size(); ++i) plan.fused[i].fused_index = plan.fused[i].split_index = (int32_t)i;
     const Shape sh = choose_shape(&h, plan, !w4);
     if (w4) {
@@ -1533,7 +1630,7 @@ int lora_linear_shape(int d_in, int d_out, int rank, int num_sms, int T, const i
         if (bk) *bk = 64;
         if (stages) *stages = ws.stages;
         if (unit_order) *unit_order = ws.tokens_fastest;
-        if (fused_units) *fused_units = (int)groups.size() * ws.n_ntiles;
+        if (fused_units) *fused_units = (int)groups.size() * ws.n_ntiles * h.w4_k_split;
         if (shrink_units) *shrink_units = (int)(sh.shrink_groups.size() / sh.cs);
         return LORA_OK;
     }

@@ -36,6 +36,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include "dev_common.cuh"
@@ -110,16 +111,45 @@ struct W4Unit {
     W4Group g;
     int n0;          // first output feature
     int n;           // MMA N of the base K-steps (tokens, multiple of 16)
+    int kb0, kend;   // base K-steps [kb0, kend) of this unit
+    int part;        // K part (0 .. k_split - 1), 0 without parts
+    int block;       // (token group, feature tile) block: its split counters
+    bool expand;     // runs the expand's K-steps (the last part)
 };
 
-template <int FT>
+template <int FT, bool SPLIT>
 __device__ __forceinline__ W4Unit w4_unit(const W4Params& p, const W4Group* groups, int u) {
     W4Unit r;
-    const int gi = w4_group_of(p, u);
+    const int S = SPLIT ? p.k_split : 1;
+    const int v = u / S;
+    r.part = u - v * S;
+    r.block = v;
+    r.kb0 = r.part * p.k_chunk;
+    r.kend = r.part == S - 1 ? p.k_main_blocks : r.kb0 + p.k_chunk;
+    r.expand = r.part == S - 1;
+    const int gi = w4_group_of(p, v);
     r.g = groups[gi];
-    r.n0 = w4_ntile_of(p, u) * kW4TileM * FT;
+    r.n0 = w4_ntile_of(p, v) * kW4TileM * FT;
     r.n = r.g.nrows[1] > 0 ? 128 + ((r.g.nrows[1] + 15) & ~15) : ((r.g.nrows[0] + 15) & ~15);
     return r;
+}
+
+// 64-bit counter reaches `value` (acquire), bounded like every other wait.
+static __device__ __noinline__ bool wait_count64(const unsigned long long* counter, unsigned long long value,
+                                                 volatile int* abort_flag, int* status, uint64_t limit_ns) {
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        unsigned long long v;
+        asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(counter) : "memory");
+        if (v >= value) return true;
+        if (*abort_flag) return false;
+        if (global_timer_ns() - t0 > limit_ns) {
+            atomicOr(status, 1);
+            *abort_flag = 1;
+            return false;
+        }
+        __nanosleep(256);
+    }
 }
 
 }  // namespace
@@ -128,7 +158,7 @@ __device__ __forceinline__ W4Unit w4_unit(const W4Params& p, const W4Group* grou
 // with no adapter rows (decode steps): the unit's two tiles share each K-step's X stage, barrier
 // round trips and ring slots, which halves the K-steps an SM runs in sequence. Tensor memory
 // then holds two 128-column accumulators (tile f at column 128 f) and A stages of 64 columns.
-template <int FT>
+template <int FT, bool SPLIT>
 __global__ void __launch_bounds__(kW4Threads, 1) lora_w4_kernel(const __grid_constant__ W4Params p) {
     static_assert(FT == 1 || FT == 2, "one or two feature tiles per unit");
     constexpr uint32_t kQStage = FT * kQStageBytes;    // packed rows of the unit's feature tiles
@@ -156,6 +186,7 @@ __global__ void __launch_bounds__(kW4Threads, 1) lora_w4_kernel(const __grid_con
     uint64_t* drain = tempty + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    volatile int* ticket = abort_flag + 1;          // K parts: the unit's role, shared by the epilogue warps
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -184,7 +215,7 @@ __global__ void __launch_bounds__(kW4Threads, 1) lora_w4_kernel(const __grid_con
     const uint32_t tmem_base = *tmem_slot;
     const uint32_t tmem_a = tmem_base + kAccCols4;  // A stages: columns 256 + 32 FT s
 
-    const int n_units = p.n_groups * p.n_ntiles;
+    const int n_units = p.n_groups * p.n_ntiles * (SPLIT ? p.k_split : 1);
     const uint64_t limit = p.wait_limit_ns;
     const W4Group* groups = p.inline_wl ? p.inline_groups : p.groups;
     const CUtensorMap* bmaps = p.inline_wl ? p.inline_bmaps : p.tm_b;
@@ -204,9 +235,9 @@ __global__ void __launch_bounds__(kW4Threads, 1) lora_w4_kernel(const __grid_con
             int acquired = -1;
             bool ok = true;
             for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-                const W4Unit w = w4_unit<FT>(p, groups, u);
+                const W4Unit w = w4_unit<FT, SPLIT>(p, groups, u);
                 const int ntile = w.g.nrows[1] > 0 ? 2 : 1;
-                for (int kb = 0; kb < p.k_main_blocks; ++kb) {
+                for (int kb = w.kb0; kb < w.kend; ++kb) {
                     if (!wait_warp(smem_addr(&empty[stage]), phase ^ 1, abort_flag, p.status, limit)) {
                         ok = false;
                         break;
@@ -219,7 +250,7 @@ __global__ void __launch_bounds__(kW4Threads, 1) lora_w4_kernel(const __grid_con
                     ++issued;
                     if (++stage == stages) { stage = 0; phase ^= 1; }
                 }
-                for (int h = 0; h < 2 && ok; ++h) {
+                for (int h = 0; h < 2 && ok && w.expand; ++h) {
                     const int a = w.g.adapter[h];
                     if (w.g.nrows[h] == 0 || a == 0) continue;
                     const CUtensorMap* bm = &bmaps[a - 1];
@@ -264,8 +295,10 @@ __global__ void __launch_bounds__(kW4Threads, 1) lora_w4_kernel(const __grid_con
             long long issued = 0;
             bool ok = true;
             for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-                const int n0 = w4_ntile_of(p, u) * kW4TileM * FT;
-                for (int pb = 0; pb < p.k_pack_blocks; ++pb) {
+                const W4Unit w = w4_unit<FT, SPLIT>(p, groups, u);
+                const int n0 = w.n0;
+                // packed boxes of 4 K-steps; part boundaries are multiples of 4 K-steps
+                for (int pb = w.kb0 >> 2; pb < ((w.kend + 3) >> 2); ++pb) {
                     if (!wait_warp(smem_addr(&pempty[ps]), pph ^ 1, abort_flag, p.status, limit)) {
                         ok = false;
                         break;
@@ -297,7 +330,7 @@ __global__ void __launch_bounds__(kW4Threads, 1) lora_w4_kernel(const __grid_con
         int it = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++it) {
-            const W4Unit w = w4_unit<FT>(p, groups, u);
+            const W4Unit w = w4_unit<FT, SPLIT>(p, groups, u);
             if (!wait_warp(smem_addr(tempty), (it & 1) ^ 1, abort_flag, p.status, limit)) {
                 ok = false;
                 break;
@@ -307,7 +340,8 @@ __global__ void __launch_bounds__(kW4Threads, 1) lora_w4_kernel(const __grid_con
             // wait) does not complete before the MMAs it issued earlier have, so each wait
             // costs a drain of the tensor pipe; eight MMAs per wait hide it where four do not.
             const uint32_t idesc = instr_desc_bf16(kW4TileM, w.n);
-            for (int kb = 0; kb < p.k_main_blocks; kb += 2) {   // k_main_blocks is even (d_in % 128 == 0)
+            // a part's K-steps are even in number (k_chunk % 4 == 0, k_main_blocks even: d_in % 128 == 0)
+            for (int kb = w.kb0; kb < w.kend; kb += 2) {
                 int st1 = stage + 1;
                 uint32_t ph1 = phase;
                 if (st1 == stages) { st1 = 0; ph1 ^= 1; }
@@ -325,7 +359,7 @@ __global__ void __launch_bounds__(kW4Threads, 1) lora_w4_kernel(const __grid_con
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
                         mma_tmem_a(tmem_base + (uint32_t)(128 * f), tmem_a + kAStageCols * st + (uint32_t)(32 * f + 8 * k),
-                                   bd + (uint64_t)(2 * k), idesc, (kb > 0 || j > 0 || k > 0) ? 1u : 0u, issuer);
+                                   bd + (uint64_t)(2 * k), idesc, (kb > w.kb0 || j > 0 || k > 0) ? 1u : 0u, issuer);
                     mma_commit<1>(smem_addr(&empty[st]), issuer);
                 }
                 stage = st1 + 1;
@@ -333,7 +367,7 @@ __global__ void __launch_bounds__(kW4Threads, 1) lora_w4_kernel(const __grid_con
                 if (stage == stages) { stage = 0; phase ^= 1; }
             }
             const uint32_t idesc_e = instr_desc_bf16(kW4TileM, 128);
-            for (int h = 0; h < 2 && ok; ++h) {
+            for (int h = 0; h < 2 && ok && w.expand; ++h) {
                 if (w.g.nrows[h] == 0 || w.g.adapter[h] == 0) continue;
                 for (int kr = 0; kr < p.k_lora_blocks; kr += 2) {
                     const int ns = kr + 1 < p.k_lora_blocks ? 2 : 1;
@@ -395,8 +429,8 @@ __global__ void __launch_bounds__(kW4Threads, 1) lora_w4_kernel(const __grid_con
         uint32_t pph = 0, phase = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-            const W4Unit w = w4_unit<FT>(p, groups, u);
-            for (int kb = 0; kb < p.k_main_blocks; ++kb) {
+            const W4Unit w = w4_unit<FT, SPLIT>(p, groups, u);
+            for (int kb = w.kb0; kb < w.kend; ++kb) {
                 if ((kb & 3) == 0 &&
                     !wait_warp(smem_addr(&pfull[ps]), pph, abort_flag, p.status, limit)) {
                     ok = false;
@@ -450,7 +484,7 @@ __global__ void __launch_bounds__(kW4Threads, 1) lora_w4_kernel(const __grid_con
                     __syncwarp();
                     if (lane == 0) mbar_arrive(smem_addr(&full[stage]));
                 }
-                if ((kb & 3) == 3 || kb == p.k_main_blocks - 1) {
+                if ((kb & 3) == 3 || kb == w.kend - 1) {
                     // this packed slot is read (by this warp's K-steps in it): hand it back
                     __syncwarp();
                     if (lane == 0) mbar_arrive(smem_addr(&pempty[ps]));
@@ -459,7 +493,7 @@ __global__ void __launch_bounds__(kW4Threads, 1) lora_w4_kernel(const __grid_con
                 if (++stage == stages) { stage = 0; phase ^= 1; }
             }
             // expand K-steps: no weights to convert, only this quadrant's arrive
-            for (int h = 0; h < 2 && ok; ++h) {
+            for (int h = 0; h < 2 && ok && w.expand; ++h) {
                 if (w.g.nrows[h] == 0 || w.g.adapter[h] == 0) continue;
                 for (int kr = 0; kr < p.k_lora_blocks; ++kr) {
                     if ((stage & 1) == par) {
@@ -487,13 +521,33 @@ __global__ void __launch_bounds__(kW4Threads, 1) lora_w4_kernel(const __grid_con
         int chunk = 0;
         int it = 0;
         for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++it) {
-            const W4Unit w = w4_unit<FT>(p, groups, u);
+            const W4Unit w = w4_unit<FT, SPLIT>(p, groups, u);
             int ok = 1;
             if (lane == 0) ok = wait_bounded(smem_addr(tfull), it & 1, abort_flag, p.status, limit, true);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             ok = epilogue_bar_and(ok);   // the four warps leave together (they share barriers)
             if (!ok) break;
             tc_fence_after();
+            // K parts: every part but the last to arrive stores its fp32 sums; the last waits until
+            // all of them are stored and adds the k_split sums in part order, its own from registers
+            const int S = SPLIT ? p.k_split : 1;
+            bool store_part = false;
+            unsigned long long* ctr = nullptr;
+            if (SPLIT) {
+                ctr = p.split_ctr + 2 * (size_t)w.block;
+                if (issuer) {
+                    const unsigned long long old = atomicAdd(ctr, 1ull);
+                    const unsigned long long s64 = (unsigned long long)S;
+                    int role = old % s64 == s64 - 1 ? 0 : 1;
+                    if (role == 0 && !wait_count64(ctr + 1, (old / s64 + 1) * (s64 - 1), abort_flag, p.status, limit))
+                        role = 2;
+                    *ticket = role;
+                }
+                epilogue_bar_sync();
+                const int role = *ticket;
+                if (role == 2) break;    // the wait ran out: the CTA is aborting
+                store_part = role == 1;
+            }
             // FT = 1: token tile h at accumulator columns 128 h; FT = 2 (one token tile): feature
             // tile f at accumulator columns 128 f. The accumulator is released right after the
             // unit's last tensor-memory load, before that chunk's stores.
@@ -515,6 +569,44 @@ __global__ void __launch_bounds__(kW4Threads, 1) lora_w4_kernel(const __grid_con
                         mbar_arrive(smem_addr(tempty));
                     }
                     const int m = rows - c < 32 ? rows - c : 32;
+                    if (SPLIT) {
+                        // partial sums of part q: row t, feature n at partials[(q * part_rows + t) * d_out + n]
+                        const size_t t0 = (size_t)(w.g.row0[h] + c);
+                        if (store_part) {
+                            if (n_ok) {
+                                float* pp = p.partials + ((size_t)w.part * p.part_rows + t0) * p.d_out + n;
+#pragma unroll
+                                for (int t = 0; t < 32; ++t)
+                                    if (t < m) __stcg(pp + (size_t)t * p.d_out, __uint_as_float(v[t]));
+                            }
+                            continue;
+                        }
+                        // the sum in part order, eight tokens at a time; rows past m and features past
+                        // d_out read row t0 / feature 0 of a slot (in range; those sums are never stored)
+                        const float* pbase = p.partials + t0 * p.d_out + (n_ok ? n : 0);
+#pragma unroll
+                        for (int g8 = 0; g8 < 32; g8 += 8) {
+                            float acc[8];
+#pragma unroll
+                            for (int qq = 0; qq < kMaxKSplit; ++qq) {
+                                if (qq >= S) break;
+                                float tv[8];
+                                if (qq == w.part) {
+#pragma unroll
+                                    for (int t = 0; t < 8; ++t) tv[t] = __uint_as_float(v[g8 + t]);
+                                } else {
+                                    const float* pq = pbase + (size_t)qq * p.part_rows * p.d_out;
+#pragma unroll
+                                    for (int t = 0; t < 8; ++t)
+                                        tv[t] = __ldcg(pq + (size_t)(g8 + t < m ? g8 + t : 0) * p.d_out);
+                                }
+#pragma unroll
+                                for (int t = 0; t < 8; ++t) acc[t] = qq == 0 ? tv[t] : acc[t] + tv[t];
+                            }
+#pragma unroll
+                            for (int t = 0; t < 8; ++t) v[g8 + t] = __float_as_uint(acc[t]);
+                        }
+                    }
                     if (m == 32) {
                         uint8_t* buf = y_stage + (size_t)(chunk & 1) * kYStageBytes;
                         __nv_bfloat16* sb = reinterpret_cast<__nv_bfloat16*>(buf) + 32 * q + lane;
@@ -536,6 +628,15 @@ __global__ void __launch_bounds__(kW4Threads, 1) lora_w4_kernel(const __grid_con
                         for (int t = 0; t < 32; ++t)
                             if (t < m) col[(size_t)t * p.d_out] = __float2bfloat16_rn(__uint_as_float(v[t]));
                     }
+                }
+            }
+            if (store_part) {
+                // every thread's partial sums are stored before the last part may read them
+                __threadfence();
+                epilogue_bar_sync();
+                if (issuer) {
+                    __threadfence();
+                    atomicAdd(ctr + 1, 1ull);
                 }
             }
         }
@@ -560,10 +661,25 @@ size_t w4_smem_bytes(int stages, int pstages, int x_stage_bytes, int ft) {
 }
 
 cudaError_t w4_prepare_device() {
-    cudaError_t e = cudaFuncSetAttribute(dev::lora_w4_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kSmemLimit);
-    if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(dev::lora_w4_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+    cudaError_t e;
+    if ((e = cudaFuncSetAttribute(dev::lora_w4_kernel<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  kSmemLimit)) != cudaSuccess ||
+        (e = cudaFuncSetAttribute(dev::lora_w4_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  kSmemLimit)) != cudaSuccess ||
+        (e = cudaFuncSetAttribute(dev::lora_w4_kernel<2, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  kSmemLimit)) != cudaSuccess)
+        return e;
+    return cudaFuncSetAttribute(dev::lora_w4_kernel<2, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+}
+
+// Cooperative launches can be switched off for a profiler (LORA_LINEAR_NONCOOPERATIVE=1), as for
+// the bf16 kernel: Nsight Compute runs one kernel at a time, so the grid is co-resident anyway.
+static bool w4_cooperative_launches() {
+    static const bool on = [] {
+        const char* v = getenv("LORA_LINEAR_NONCOOPERATIVE");
+        return !(v && v[0] == '1');
+    }();
+    return on;
 }
 
 cudaError_t launch_w4(const W4Params& p, int grid, cudaStream_t stream) {
@@ -575,12 +691,31 @@ cudaError_t launch_w4(const W4Params& p, int grid, cudaStream_t stream) {
         p.stages < 2 || p.stages * 32 * ft > 256 || (p.stages & 1) || p.pstages < 2 || (p.x_stage_bytes & 1023) ||
         p.x_stage_bytes < 16384 || p.x_stage_bytes > (int)dev::kXStageMaxBytes || (ft == 2 && p.n_ntiles * 256 < p.d_out))
         return cudaErrorInvalidValue;
+    // K parts: every part a whole number of packed boxes (4 K-steps), the last one keeping at least one
+    if (p.k_split > 1 && (p.k_chunk < 4 || (p.k_chunk & 3) || (p.k_split - 1) * p.k_chunk >= p.k_main_blocks ||
+                          !p.partials || !p.split_ctr || p.part_rows < 1))
+        return cudaErrorInvalidValue;
     const size_t smem = w4_smem_bytes(p.stages, p.pstages, p.x_stage_bytes, ft);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(kW4Threads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    if (p.k_split > 1 && w4_cooperative_launches()) {
+        // the last part of a block waits for the block's other parts on other CTAs: a cooperative
+        // launch starts only when its whole grid can be resident
+        attr[0].id = cudaLaunchAttributeCooperative;
+        attr[0].val.cooperative = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    const bool split = p.k_split > 1;
     if (ft == 2)
-        dev::lora_w4_kernel<2><<<grid, kW4Threads, smem, stream>>>(p);
-    else
-        dev::lora_w4_kernel<1><<<grid, kW4Threads, smem, stream>>>(p);
-    return cudaGetLastError();
+        return split ? cudaLaunchKernelEx(&cfg, dev::lora_w4_kernel<2, true>, p)
+                     : cudaLaunchKernelEx(&cfg, dev::lora_w4_kernel<2, false>, p);
+    return split ? cudaLaunchKernelEx(&cfg, dev::lora_w4_kernel<1, true>, p)
+                 : cudaLaunchKernelEx(&cfg, dev::lora_w4_kernel<1, false>, p);
 }
 
 }  // namespace lora

@@ -50,6 +50,16 @@ struct W4Params {
     int tokens_fastest;              // unit order: 1 = token groups fastest, 0 = feature tiles fastest
     int feature_tiles;               // 128-feature tiles per unit: 1, or 2 for one token tile of at
                                      // most 128 rows with no adapter rows (tm_wq / tm_ws boxes 128 x FT)
+    // K parts (k_split > 1): every (token group, feature tile) block runs as k_split units over
+    // parts of the base K-steps (k_chunk each, a multiple of 4; the last part takes the rest and
+    // the expand); every part but the last to finish stores its fp32 sums in `partials`, the last
+    // adds the k_split sums in part order and stores Y. Counters only grow (64-bit): the k-th
+    // launch's arrivals at a block are k_split k .. k_split k + k_split - 1.
+    int k_split;
+    int k_chunk;
+    float* partials;                 // part q, row t, feature n at [(q * part_rows + t) * d_out + n]
+    int part_rows;
+    unsigned long long* split_ctr;   // per block: {parts arrived, partial sums stored}
     int debug_stall;
 };
 

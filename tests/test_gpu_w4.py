@@ -302,3 +302,114 @@ def test_w4_repack_rejects_bad_arguments(dev):
     assert lib.lora_linear_w4_repack(p + 1, p + 1, 8, None) == L.LORA_EINVAL  # misaligned
     assert lib.lora_linear_w4_repack(p, p + 4, 32, None) == L.LORA_EINVAL    # partial overlap
     assert lib.lora_linear_w4_repack(p, p, 0, None) == L.LORA_OK             # nothing to do
+
+
+# --------------------------------------------------------------------------- K parts (4-bit base)
+
+@pytest.mark.parametrize("parts", [1, 2, 3, 4])
+@pytest.mark.parametrize("T", [17, 48, 128])
+def test_w4_k_parts_match_oracle(dev, parts, T):
+    # decode batches (one token tile, no adapter rows) with the base's K-steps in 1..4 parts
+    # (2,048 inputs: 32 K-steps, parts of 8 or more); d_out 520 leaves a feature-tile tail
+    from mixed_lora_projection_gb300 import _lib as L
+    lens = [T // 2, T - T // 2] if T > 1 else [1]
+    off = [0] + np.cumsum(lens).tolist()
+    ids = [0] * len(lens)
+    w = Workload("w4kp", 18, T, 2048, 520, 32, tuple(off), tuple(ids))
+    inp = make_inputs(w, dev)
+    q, sc = make_w4_base(w, dev)
+    kq = _kq(q)
+    with _ll(w) as ll:
+        ll.set_option(L.OPT_W4_K_SPLIT, parts)
+        y1 = ll.forward_w4(inp.x, off, ids, kq, sc, inp.a, inp.b, inp.scales).clone()
+        y2 = ll.forward_w4(inp.x, off, ids, kq, sc, inp.a, inp.b, inp.scales)
+        torch.cuda.synchronize()
+        assert ll.status() == 0
+    assert torch.equal(y1, y2)                      # the same sum whichever part finishes last
+    assert rel_err(y1, _oracle(inp, q, sc, off, ids)) <= TOL
+
+
+def test_w4_k_parts_rows_do_not_depend_on_the_batch(dev):
+    # a decode-sized handle (at most 128 rows) of a narrow projection splits K by itself; the 48
+    # base rows alone and as the first rows of a 100-row batch with adapter rows (an expand on the
+    # last part) give the same bits, and the expand rows match the oracle
+    from mixed_lora_projection_gb300 import launch_shape
+    lens, ids = [8] * 6 + [52], [0] * 6 + [1]
+    off = [0] + np.cumsum(lens).tolist()
+    w = Workload("w4kpinv", 19, 128, 6144, 1024, 64, tuple(off), tuple(ids), scales=(0.75,))
+    inp = make_inputs(w, dev, x_rows=100)
+    q, sc = make_w4_base(w, dev)
+    kq = _kq(q)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    s = launch_shape(6144, 1024, 64, sms, 100, off, ids, w4=True)
+    assert s["fused_units"] == 8 * 4           # 8 one-tile units, K in 4 parts
+    with _ll(w) as ll:
+        full = ll.forward_w4(inp.x, off, ids, kq, sc, inp.a, inp.b, inp.scales).clone()
+        alone = ll.forward_w4(inp.x[:48], off[:7], ids[:6], kq, sc, inp.a, inp.b, inp.scales)
+        torch.cuda.synchronize()
+        assert ll.status() == 0
+    assert torch.equal(full[:48], alone)
+    assert rel_err(full, _oracle(inp, q, sc, off, ids)) <= TOL
+
+
+@pytest.mark.parametrize("name", ["decode_o", "decode_down"])
+def test_w4_k_parts_full_size_decode(dev, name):
+    # the 48-row decode batch of the o and down projections at full size: 40 one-tile units, K
+    # in 3 parts (120 units), sampled rows against the oracle
+    from mixed_lora_projection_gb300 import launch_shape
+    w = WORKLOADS[name]
+    off, ids = list(w.seg_offsets), list(w.seg_ids)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    assert launch_shape(w.d_in, w.d_out, w.rank, sms, w.T, off, ids, w4=True)["fused_units"] == 40 * 3
+    inp = make_inputs(w, dev)
+    q, sc = make_w4_base(w, dev)
+    with _ll(w) as ll:
+        y = ll.forward_w4(inp.x, off, ids, _kq(q), sc, inp.a, inp.b, inp.scales)
+        torch.cuda.synchronize()
+        assert ll.status() == 0
+    rows = sample_rows(w.T, off, ids, n_random=16, seed=8)
+    assert rel_err(y[torch.as_tensor(rows, device=dev)], _oracle(inp, q, sc, off, ids, rows)) <= TOL
+
+
+def test_w4_k_parts_graph_replays_and_timeout(dev):
+    # K parts across CUDA-graph replays (the block counters only grow, so replays need no reset);
+    # then every wait running out (20 ms) reports LORA_ETIMEOUT, the status reset also resets the
+    # counters, and the next call is correct
+    from mixed_lora_projection_gb300 import LoraLinear, _lib as L
+    T = 48
+    off, ids = [0, 24, 48], [0, 0]
+    w = Workload("w4kpg", 20, T, 2048, 768, 16, tuple(off), tuple(ids))
+    inp = make_inputs(w, dev)
+    q, sc = make_w4_base(w, dev)
+    kq = _kq(q)
+    with LoraLinear(2048, 768, 16, T, 4, 0) as ll:
+        ll.set_option(L.OPT_W4_K_SPLIT, 3)
+        ref = ll.forward_w4(inp.x, off, ids, kq, sc, inp.a, inp.b, inp.scales).clone()
+        y = torch.zeros_like(ref)
+        s = torch.cuda.Stream(dev)
+        s.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(s):
+            ll.forward_w4(inp.x, off, ids, kq, sc, inp.a, inp.b, inp.scales, y=y)
+        torch.cuda.current_stream(dev).wait_stream(s)
+        torch.cuda.synchronize()
+        y.zero_()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            ll.forward_w4(inp.x, off, ids, kq, sc, inp.a, inp.b, inp.scales, y=y)
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        assert ll.status() == 0
+        assert torch.equal(y, ref)
+        ll.set_option(L.OPT_WAIT_LIMIT_US, 20000)
+        ll.set_option(L.OPT_DEBUG_STALL, 1)
+        ll.forward_w4(inp.x, off, ids, kq, sc, inp.a, inp.b, inp.scales)
+        torch.cuda.synchronize()
+        assert ll.status(reset=True) == L.LORA_ETIMEOUT
+        ll.set_option(L.OPT_DEBUG_STALL, 0)
+        ll.set_option(L.OPT_WAIT_LIMIT_US, 4000000)
+        y2 = ll.forward_w4(inp.x, off, ids, kq, sc, inp.a, inp.b, inp.scales)
+        torch.cuda.synchronize()
+        assert ll.status() == 0
+    assert torch.equal(y2, ref)
+    assert rel_err(ref, _oracle(inp, q, sc, off, ids)) <= TOL
