@@ -180,9 +180,9 @@ CUresult encode_2d(lora_linear* h, CUtensorMap* m, const void* ptr, uint64_t inn
 }
 
 // Deepest ring that fits the opt-in shared memory, for `b_rows` B rows per CTA.
-int stages_for(int b_rows, int bk, int a_rows = kTileM) {
+int stages_for(int b_rows, int bk, int a_rows = kTileM, int yt = 0) {
     int s = kMaxStages;
-    while (s > 2 && gemm_smem_bytes(b_rows, s, bk, a_rows) > (size_t)kSmemLimit) --s;
+    while (s > 2 && gemm_smem_bytes(b_rows, s, bk, a_rows, yt) > (size_t)kSmemLimit) --s;
     return s;
 }
 
@@ -532,7 +532,7 @@ Shape choose_shape(lora_linear* h, const Plan& plan, bool allow_yt = true) {
         sh.bk = kTileK;
         sh.a_rows = kTileM;
         sh.n_ntiles = ceil_div(h->d_out, 2 * kTileM);
-        sh.stages = stages_for(std::max(sh.yt_rows, sh.shrink_n / 2), sh.bk, kTileM);
+        sh.stages = stages_for(std::max(sh.yt_rows, sh.shrink_n / 2), sh.bk, kTileM, 1);
         sh.m_fastest = 0;
     }
     return sh;

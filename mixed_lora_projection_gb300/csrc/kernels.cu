@@ -176,23 +176,33 @@ __device__ __forceinline__ int yt_token(int c, int h, int rows) {
 }
 
 // Epilogue of a token-column unit: this thread's TMEM lane is output feature f and each
-// accumulator column a token row. Each store of a warp writes 32 neighbouring features of one
-// token row (64 bytes).
-__device__ __forceinline__ void yt_store(const GemmParams& p, uint32_t taddr, int f) {
+// accumulator column a token row. Each 32-column chunk goes through the warp's 2 KB buffer
+// ([32 tokens][32 features] bf16, written one token column per thread) and leaves as 16-byte
+// stores: thread l writes 8 features of token row (l + 32 i) / 4, so a warp's store covers 8
+// token rows of 64 bytes.
+__device__ __forceinline__ void yt_store(const GemmParams& p, uint32_t taddr, int f0, int lane, uint8_t* stage) {
     const int h = p.yt_h, rows = p.yt_rows, n = 2 * p.yt_rows, T = p.yt_tokens;
-    const bool f_ok = f < p.d_out;
-    __nv_bfloat16* col = reinterpret_cast<__nv_bfloat16*>(p.y) + f;
+    __nv_bfloat16* sb = reinterpret_cast<__nv_bfloat16*>(stage);
     for (int c = 0; c < n; c += 32) {
         uint32_t v[32];
         const bool two = c + 16 < n;  // n is a multiple of 16
         tmem_ld16(taddr + (uint32_t)c, v);
         if (two) tmem_ld16(taddr + (uint32_t)c + 16, v + 16);
         tmem_ld_wait();
+        __syncwarp();                 // the buffer's previous chunk has been read by every lane
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            if (i < 16 || two) {
-                const int t = yt_token(c + i, h, rows);
-                if (f_ok && t < T) col[(size_t)t * p.d_out] = __float2bfloat16_rn(__uint_as_float(v[i]));
+        for (int t = 0; t < 32; ++t) sb[t * 32 + lane] = __float2bfloat16_rn(__uint_as_float(v[t]));
+        __syncwarp();
+        const int m = two ? 32 : 16;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int k = lane + 32 * i;      // 16-byte piece k: token column k / 4, features 8 (k % 4) ..
+            const int tc = k >> 2, seg = k & 3;
+            const int tok = yt_token(c + tc, h, rows);
+            const int f = f0 + 8 * seg;
+            if (tc < m && tok < T && f < p.d_out) {
+                const uint4 val = *reinterpret_cast<const uint4*>(stage + (size_t)k * 16);
+                *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.y) + (size_t)tok * p.d_out + f) = val;
             }
         }
     }
@@ -217,7 +227,9 @@ __global__ void __launch_bounds__(YT ? kThreadsYt : kThreads, 1) lora_gemm_kerne
     const int n_acc = (YT && 2 * p.yt_rows > kAccCols) ? 1 : 2;
     uint8_t* a_ring = base;
     uint8_t* b_ring = a_ring + (size_t)stages * kStageA;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(b_ring + (size_t)stages * b_stage_bytes);
+    // token-column units: the epilogue warps' transposing buffers (2 KB each) follow the rings
+    uint8_t* yt_stage = b_ring + (size_t)stages * b_stage_bytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(yt_stage + (YT ? kYtStageBytes : 0));
     uint64_t* full = bars;
     uint64_t* empty = full + stages;
     uint64_t* tfull = empty + stages;
@@ -520,7 +532,7 @@ __global__ void __launch_bounds__(YT ? kThreadsYt : kThreads, 1) lora_gemm_kerne
             }
             const uint32_t taddr = tmem_base + (uint32_t)(acc * kAccCols) + lane_off;
             if (YT && !w.shrink) {
-                yt_store(p, taddr, w.n0 + rank * kTileM + r_local);
+                yt_store(p, taddr, w.n0 + rank * kTileM + q * 32, lane, yt_stage + (size_t)q * 2048);
             } else {
                 const int row = w.tile.row0 + r_local;
                 const bool row_ok = r_local < w.tile.nrows;
@@ -691,9 +703,9 @@ cudaError_t w4_repack(const void* src, void* dst, long long n_words, int grid, c
     return cudaGetLastError();
 }
 
-size_t gemm_smem_bytes(int b_tile_rows, int stages, int bk, int a_rows) {
+size_t gemm_smem_bytes(int b_tile_rows, int stages, int bk, int a_rows, int yt) {
     return 1024 + (size_t)stages * ((size_t)a_rows * bk * 2 + (size_t)b_tile_rows * bk * 2) +
-           8 * (2 * (size_t)stages + 5) + 16;
+           (yt ? (size_t)kYtStageBytes : 0) + 8 * (2 * (size_t)stages + 5) + 16;
 }
 
 template <int BK, int CG, bool YT = false>
@@ -734,7 +746,7 @@ static void launch_config(const GemmParams& p, int grid, cudaStream_t stream, cu
     *cfg = cudaLaunchConfig_t{};
     cfg->gridDim = dim3(grid, 1, 1);
     cfg->blockDim = dim3(p.yt ? kThreadsYt : kThreads, 1, 1);
-    cfg->dynamicSmemBytes = gemm_smem_bytes(b_rows, p.stages, p.bk, p.a_rows ? p.a_rows : kTileM);
+    cfg->dynamicSmemBytes = gemm_smem_bytes(b_rows, p.stages, p.bk, p.a_rows ? p.a_rows : kTileM, p.yt);
     cfg->stream = stream;
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = p.cluster_size;

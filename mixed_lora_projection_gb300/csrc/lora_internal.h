@@ -18,6 +18,7 @@ constexpr int kMaxStages = 16;
 constexpr int kSmemLimit = 232448;                     // opt-in dynamic shared memory per CTA (227 KB)
 constexpr int kThreads = 192;        // warp 0 TMA, warp 1 MMA + TMEM owner, warps 2..5 epilogue
 constexpr int kThreadsYt = 224;      // token-column units: warp 6 issues the second MMA of each K16 step
+constexpr int kYtStageBytes = 4 * 32 * 32 * 2;  // token-column epilogue: 32 tokens x 32 features bf16 per warp
 constexpr int kEpilogueThreads = 128;
 constexpr int kW4Group = 128;        // input features per scale of a 4-bit base
 // Work lists this small travel inside the kernel parameters (no upload copy per call).
@@ -154,7 +155,7 @@ int plan_segments(const int32_t* seg_offsets, const int32_t* seg_ids, int n_seg,
                   int n_adapters, Plan* plan);
 
 // kernels.cu
-size_t gemm_smem_bytes(int b_tile_rows, int stages, int bk, int a_rows = kTileM);
+size_t gemm_smem_bytes(int b_tile_rows, int stages, int bk, int a_rows = kTileM, int yt = 0);
 cudaError_t gemm_prepare_device();           // sets the opt-in smem limit on the current device
 cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t stream);
 int gemm_max_clusters(const GemmParams& p);  // co-resident clusters of this launch shape
