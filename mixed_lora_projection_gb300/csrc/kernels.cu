@@ -42,6 +42,15 @@
 // both CTAs' stages and accumulators (multicast); both epilogues release the even CTA's
 // accumulator barrier.
 //
+// Token-column units (YT, an instantiation of their own, SM pairs): for batches of at most 512
+// rows on one adapter, a unit computes a block of Y^T instead: 256 output features (W rows as the
+// A operand, 128 per CTA) for every token row of the batch (X rows as the B operand, half of them
+// per CTA), so W is read once and no row tile is padded. Past 128 token rows per CTA each 16-wide
+// K step takes a second MMA over the remaining rows, issued by warp 6 beside warp 1's first (one
+// warp waits ~80 cycles between MMAs whatever their width). The epilogue maps accumulator
+// columns back to token rows through a per-warp shared-memory buffer. The sums keep their order,
+// so the bits equal those of row tiles.
+//
 // Every mbarrier wait is bounded by a wall-clock limit; a wait that runs out sets bit 0
 // of the status word and a CTA-wide abort flag, and all roles leave their loops, wait
 // (bounded) for their own copies and MMAs in flight, free TMEM and return.
@@ -209,7 +218,8 @@ __device__ __forceinline__ void yt_store(const GemmParams& p, uint32_t taddr, in
 }
 
 template <int BK, int CG, bool YT>
-__global__ void __launch_bounds__(YT ? kThreadsYt : kThreads, 1) lora_gemm_kernel(const __grid_constant__ GemmParams p) {
+__global__ void __launch_bounds__(YT ? kThreadsYt : kThreads, 1)
+    lora_gemm_kernel(const __grid_constant__ GemmParams p) {
     static_assert(!YT || (CG == 2 && BK == 64), "token-column units run on SM pairs with 64-wide K-steps");
     // A stage: the tile's rows of X (or U) for this K-step; a batch of one short tile loads
     // only its rows (a_rows < 128), and the MMA's remaining A rows read unrelated shared memory
