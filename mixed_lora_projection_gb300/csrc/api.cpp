@@ -671,7 +671,8 @@ W4Shape w4_shape(const lora_linear* h, const std::vector<W4Group>& groups, int T
     // a batch of one token tile of at most 128 rows and no adapter rows (a decode step) runs two
     // feature tiles per unit when that still gives most SMs a unit (gate_up: 136 units); narrower
     // projections keep one tile per unit, twice as many units (qkv 96, o and down 40)
-    const bool one_tile = n == 1 && groups[0].nrows[1] == 0 && groups[0].nrows[0] <= kTileM && groups[0].adapter[0] == 0;
+    const bool one_tile =
+        n == 1 && groups[0].nrows[1] == 0 && groups[0].nrows[0] <= kTileM && groups[0].adapter[0] == 0;
     w.feature_tiles = (one_tile && 4 * ceil_div(h->d_out, 2 * kW4TileM) >= 3 * usable_sms(h)) ? 2 : 1;
     w.n_ntiles = ceil_div(h->d_out, kW4TileM * w.feature_tiles);
     // unit order: token groups fastest when the packed base is too large to stay in L2 beside

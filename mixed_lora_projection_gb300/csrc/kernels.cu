@@ -614,10 +614,14 @@ __global__ void __launch_bounds__(YT ? kThreadsYt : kThreads, 1)
                         for (int h = 0; h < 4; ++h) {
                             if ((h < 2 || two) && c + 8 * h < n_out) {
                                 uint4 o;
-                                o.x = pack_bf16x2(__uint_as_float(v[8 * h + 0]) * scale, __uint_as_float(v[8 * h + 1]) * scale);
-                                o.y = pack_bf16x2(__uint_as_float(v[8 * h + 2]) * scale, __uint_as_float(v[8 * h + 3]) * scale);
-                                o.z = pack_bf16x2(__uint_as_float(v[8 * h + 4]) * scale, __uint_as_float(v[8 * h + 5]) * scale);
-                                o.w = pack_bf16x2(__uint_as_float(v[8 * h + 6]) * scale, __uint_as_float(v[8 * h + 7]) * scale);
+                                o.x = pack_bf16x2(__uint_as_float(v[8 * h + 0]) * scale,
+                                                  __uint_as_float(v[8 * h + 1]) * scale);
+                                o.y = pack_bf16x2(__uint_as_float(v[8 * h + 2]) * scale,
+                                                  __uint_as_float(v[8 * h + 3]) * scale);
+                                o.z = pack_bf16x2(__uint_as_float(v[8 * h + 4]) * scale,
+                                                  __uint_as_float(v[8 * h + 5]) * scale);
+                                o.w = pack_bf16x2(__uint_as_float(v[8 * h + 6]) * scale,
+                                                  __uint_as_float(v[8 * h + 7]) * scale);
                                 *reinterpret_cast<uint4*>(out + c + 8 * h) = o;
                             }
                         }
