@@ -413,3 +413,25 @@ def test_w4_k_parts_graph_replays_and_timeout(dev):
         assert ll.status() == 0
     assert torch.equal(y2, ref)
     assert rel_err(ref, _oracle(inp, q, sc, off, ids)) <= TOL
+
+
+def test_w4_k_parts_with_several_token_groups(dev):
+    # a decode-sized batch on three adapters and base rows: four planner tiles in two token groups,
+    # each block's K in 2 parts with the expand on the last; against the oracle, and repeated calls
+    # give the same bits
+    from mixed_lora_projection_gb300 import _lib as L
+    lens, ids = [20, 30, 10, 40, 20], [1, 2, 0, 3, 1]
+    off = [0] + np.cumsum(lens).tolist()
+    w = Workload("w4kpg2", 21, off[-1], 2048, 640, 32, tuple(off), tuple(ids), n_adapters=3,
+                 scales=(0.5, -1.0, 1.5))
+    inp = make_inputs(w, dev)
+    q, sc = make_w4_base(w, dev)
+    kq = _kq(q)
+    with _ll(w) as ll:
+        ll.set_option(L.OPT_W4_K_SPLIT, 2)
+        y1 = ll.forward_w4(inp.x, off, ids, kq, sc, inp.a, inp.b, inp.scales).clone()
+        y2 = ll.forward_w4(inp.x, off, ids, kq, sc, inp.a, inp.b, inp.scales)
+        torch.cuda.synchronize()
+        assert ll.status() == 0
+    assert torch.equal(y1, y2)
+    assert rel_err(y1, _oracle(inp, q, sc, off, ids)) <= TOL
