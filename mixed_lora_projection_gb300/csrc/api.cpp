@@ -202,10 +202,13 @@ CUresult encode_u8_sw128(lora_linear* h, CUtensorMap* m, const void* ptr, uint64
 // Token groups of the 4-bit base kernel: consecutive planner tiles in pairs.
 std::vector<W4Group> make_w4_groups(const std::vector<Tile>& fused) {
     std::vector<W4Group> g;
-    for (size_t i = 0; i < fused.size(); i += 2) {
+    // a batch of exactly three tiles whose last has at most kW4TailRows rows (a 300-row decision
+    // beside chat rows) is one group: each weight tile is dequantised once for all of it
+    const size_t per = (fused.size() == 3 && fused[2].nrows <= kW4TailRows) ? 3 : 2;
+    for (size_t i = 0; i < fused.size(); i += per) {
         W4Group w;
         memset(&w, 0, sizeof(w));
-        for (int k = 0; k < 2 && i + k < fused.size(); ++k) {
+        for (size_t k = 0; k < per && i + k < fused.size(); ++k) {
             w.row0[k] = fused[i + k].row0;
             w.nrows[k] = fused[i + k].nrows;
             w.adapter[k] = fused[i + k].adapter;
@@ -663,6 +666,7 @@ int ensure_w4_split_buffers(lora_linear* h) {
 // Launch shape of the 4-bit kernel for a call's token groups (host logic only).
 struct W4Shape {
     int feature_tiles = 1, n_ntiles = 0, tokens_fastest = 0, x_stage_bytes = 0, stages = 4, pstages = 2;
+    int tail_rows = 0;   // rows of the third token tile's X box (a group of three tiles), else 0
 };
 
 W4Shape w4_shape(const lora_linear* h, const std::vector<W4Group>& groups, int T) {
@@ -682,9 +686,13 @@ W4Shape w4_shape(const lora_linear* h, const std::vector<W4Group>& groups, int T
     w.tokens_fastest = h->raster == 1   ? 1
                        : h->raster == 2 ? 0
                                         : (n > 1 && packed_bytes > 32e6 && x_bytes <= 64e6) ? 1 : 0;
-    // X stages: two token tiles (and the expand's U + B_a boxes), or one tile when FT = 2; the
-    // packed ring takes the rest of shared memory
+    // X stages: two token tiles (and the expand's U + B_a boxes), or one tile when FT = 2, or
+    // two tiles and a third tile's rows; the packed ring takes the rest of shared memory
     w.x_stage_bytes = w.feature_tiles == 2 ? kTileM * 128 : 2 * kTileM * 128;
+    if (n == 1 && groups[0].nrows[2] > 0) {
+        w.tail_rows = ceil_div(groups[0].nrows[2], 16) * 16;
+        w.x_stage_bytes += w.tail_rows * 128;
+    }
     while (w.pstages < 8 &&
            w4_smem_bytes(w.stages, w.pstages + 1, w.x_stage_bytes, w.feature_tiles) <= (size_t)kSmemLimit)
         ++w.pstages;
@@ -1212,6 +1220,10 @@ int forward_impl(lora_linear* h, const void* x, int T, const int32_t* seg_offset
     if (w4) {
         q.tm_x = p.tm_x;
         q.feature_tiles = w4s.feature_tiles;
+        q.tail_rows = w4s.tail_rows;
+        if (w4s.tail_rows &&
+            encode_2d(h, &q.tm_x3, x, h->d_in, T, 64, (uint32_t)w4s.tail_rows) != CUDA_SUCCESS)
+            return LORA_ECUDA;
         const uint32_t q_box = (uint32_t)(kW4TileM * q.feature_tiles);
         if (encode_u8_sw128(h, &q.tm_wq, Wq, (uint64_t)h->d_in / 2, h->d_out, q_box) != CUDA_SUCCESS ||
             encode_plain_2d(h, &q.tm_ws, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Ws, h->d_out,
@@ -1315,9 +1327,10 @@ int forward_impl(lora_linear* h, const void* x, int T, const int32_t* seg_offset
         }
         if (timing) cudaEventRecord(rec.ev[1], stream);
         for (const W4Group& g : w4_groups)
-            for (int k = 0; k < 2; ++k)
+            for (int k = 0; k < 3; ++k)
                 if (g.adapter[k] < 0 || g.adapter[k] > n_used || g.nrows[k] < 0 || g.row0[k] < 0 ||
-                    g.row0[k] + g.nrows[k] > T || g.nrows[k] > kTileM || (k == 0 && g.nrows[0] == 0))
+                    g.row0[k] + g.nrows[k] > T || g.nrows[k] > kTileM || (k == 0 && g.nrows[0] == 0) ||
+                    (k == 2 && g.nrows[2] > 0 && (g.nrows[1] == 0 || g.nrows[2] > w4s.tail_rows)))
                     return LORA_EINVAL;
         q.tm_u = p.tm_u;
         q.y = y;

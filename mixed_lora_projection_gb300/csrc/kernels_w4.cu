@@ -48,7 +48,7 @@ namespace dev {
 
 namespace {
 
-constexpr uint32_t kXStageMaxBytes = 256 * 128;   // B operand: up to 256 token rows x 64 bf16
+constexpr uint32_t kXStageMaxBytes = (256 + kW4TailRows) * 128;   // B operand: up to 256 + 96 token rows x 64 bf16
 constexpr uint32_t kQStageBytes = 128 * kW4PackBytes;   // packed rows of 4 K-steps
 constexpr uint32_t kSStageBytes = 2 * 128 * 2;          // two scale groups of 128 features
 constexpr uint32_t kAccCols4 = 256;               // accumulator columns (tokens)
@@ -111,6 +111,7 @@ struct W4Unit {
     W4Group g;
     int n0;          // first output feature
     int n;           // MMA N of the base K-steps (tokens, multiple of 16)
+    int n2;          // N of the second MMA (the third token tile's rows), 0 without one
     int kb0, kend;   // base K-steps [kb0, kend) of this unit
     int part;        // K part (0 .. k_split - 1), 0 without parts
     int block;       // (token group, feature tile) block: its split counters
@@ -130,7 +131,12 @@ __device__ __forceinline__ W4Unit w4_unit(const W4Params& p, const W4Group* grou
     const int gi = w4_group_of(p, v);
     r.g = groups[gi];
     r.n0 = w4_ntile_of(p, v) * kW4TileM * FT;
-    r.n = r.g.nrows[1] > 0 ? 128 + ((r.g.nrows[1] + 15) & ~15) : ((r.g.nrows[0] + 15) & ~15);
+    // token tile h at accumulator columns 128 h: a third tile makes the first MMA cover both
+    // of the first two tiles whole
+    r.n = r.g.nrows[2] > 0   ? 256
+          : r.g.nrows[1] > 0 ? 128 + ((r.g.nrows[1] + 15) & ~15)
+                             : ((r.g.nrows[0] + 15) & ~15);
+    r.n2 = r.g.nrows[2] > 0 ? ((r.g.nrows[2] + 15) & ~15) : 0;
     return r;
 }
 
@@ -191,8 +197,10 @@ __global__ void __launch_bounds__(kW4Threads, 1) lora_w4_kernel(const __grid_con
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    // MMA warps: one per feature tile of a unit, each commits every stage, accumulator and drain
-    constexpr uint32_t kIssuers = FT;
+    // MMA warps (one per feature tile of a unit, or two with a third token tile): each commits
+    // every stage, accumulator and drain
+    const bool mma2 = FT == 2 || p.tail_rows > 0;
+    const uint32_t kIssuers = mma2 ? 2u : 1u;
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
             mbar_init(smem_addr(&full[s]), 1 + kW4ConvertWarps / 2);
@@ -213,7 +221,8 @@ __global__ void __launch_bounds__(kW4Threads, 1) lora_w4_kernel(const __grid_con
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    const uint32_t tmem_a = tmem_base + kAccCols4;  // A stages: columns 256 + 32 FT s
+    // A stages after the accumulators: columns 256 + 32 FT s, or 384 + 32 s past a third token tile
+    const uint32_t tmem_a = tmem_base + (FT == 1 && p.tail_rows ? 3u * 128u : kAccCols4);
 
     const int n_units = p.n_groups * p.n_ntiles * (SPLIT ? p.k_split : 1);
     const uint64_t limit = p.wait_limit_ns;
@@ -236,21 +245,25 @@ __global__ void __launch_bounds__(kW4Threads, 1) lora_w4_kernel(const __grid_con
             bool ok = true;
             for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
                 const W4Unit w = w4_unit<FT, SPLIT>(p, groups, u);
-                const int ntile = w.g.nrows[1] > 0 ? 2 : 1;
+                const int ntile = w.g.nrows[2] > 0 ? 3 : w.g.nrows[1] > 0 ? 2 : 1;
+                // tiles 0 and 1: 128-row boxes; a third tile: its own box of tail_rows rows
+                const uint32_t x_bytes = (ntile < 3 ? (uint32_t)ntile : 2u) * 16384u +
+                                         (ntile == 3 ? (uint32_t)p.tail_rows * 128u : 0u);
                 for (int kb = w.kb0; kb < w.kend; ++kb) {
                     if (!wait_warp(smem_addr(&empty[stage]), phase ^ 1, abort_flag, p.status, limit)) {
                         ok = false;
                         break;
                     }
                     const uint32_t fb = smem_addr(&full[stage]);
-                    mbar_arrive_expect_tx(fb, (uint32_t)ntile * 16384u, issuer);
+                    mbar_arrive_expect_tx(fb, x_bytes, issuer);
                     const uint32_t xs = smem_addr(x_ring + (size_t)stage * x_stage);
                     for (int h = 0; h < ntile; ++h)
-                        tma_load_2d<1>(xs + (uint32_t)h * 16384u, &p.tm_x, fb, kb * 64, w.g.row0[h], issuer);
+                        tma_load_2d<1>(xs + (uint32_t)h * 16384u, h < 2 ? &p.tm_x : &p.tm_x3, fb, kb * 64,
+                                       w.g.row0[h], issuer);
                     ++issued;
                     if (++stage == stages) { stage = 0; phase ^= 1; }
                 }
-                for (int h = 0; h < 2 && ok && w.expand; ++h) {
+                for (int h = 0; h < 3 && ok && w.expand; ++h) {
                     const int a = w.g.adapter[h];
                     if (w.g.nrows[h] == 0 || a == 0) continue;
                     const CUtensorMap* bm = &bmaps[a - 1];
@@ -319,12 +332,13 @@ __global__ void __launch_bounds__(kW4Threads, 1) lora_w4_kernel(const __grid_con
                                  limit, false);
             }
         }
-    } else if (warp == 1 || (FT == 2 && warp == 15)) {
+    } else if (warp == 1 || (mma2 && warp == 15)) {
         // ------------------------------------------------------------ MMA issuers
-        // Warp 1 issues feature tile 0's MMAs (and the expand's), warp 15 tile 1's; both walk
+        // Warp 1 issues feature tile 0's MMAs (and the expand's), warp 15 tile 1's, or with
+        // three token tiles warp 1 the first two tiles' MMA and warp 15 the third's; both walk
         // every stage and commit it.
         const uint32_t issuer = lane == 0 ? 1u : 0u;
-        const int my_tile = (FT == 2 && warp == 15) ? 1 : 0;
+        const int my_tile = (mma2 && warp == 15) ? 1 : 0;
         int stage = 0;
         uint32_t phase = 0;
         int it = 0;
@@ -340,6 +354,7 @@ __global__ void __launch_bounds__(kW4Threads, 1) lora_w4_kernel(const __grid_con
             // wait) does not complete before the MMAs it issued earlier have, so each wait
             // costs a drain of the tensor pipe; eight MMAs per wait hide it where four do not.
             const uint32_t idesc = instr_desc_bf16(kW4TileM, w.n);
+            const uint32_t idesc2 = instr_desc_bf16(kW4TileM, w.n2 ? w.n2 : 16);
             // a part's K-steps are even in number (k_chunk % 4 == 0, k_main_blocks even: d_in % 128 == 0)
             for (int kb = w.kb0; kb < w.kend; kb += 2) {
                 int st1 = stage + 1;
@@ -355,11 +370,27 @@ __global__ void __launch_bounds__(kW4Threads, 1) lora_w4_kernel(const __grid_con
                 for (int j = 0; j < 2; ++j) {
                     const int st = j ? st1 : stage;
                     const uint64_t bd = smem_desc<64>(smem_addr(x_ring + (size_t)st * x_stage));
-                    const int f = my_tile;
+                    if (FT == 2) {
+                        const int f = my_tile;
 #pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        mma_tmem_a(tmem_base + (uint32_t)(128 * f), tmem_a + kAStageCols * st + (uint32_t)(32 * f + 8 * k),
-                                   bd + (uint64_t)(2 * k), idesc, (kb > w.kb0 || j > 0 || k > 0) ? 1u : 0u, issuer);
+                        for (int k = 0; k < 4; ++k)
+                            mma_tmem_a(tmem_base + (uint32_t)(128 * f),
+                                       tmem_a + kAStageCols * st + (uint32_t)(32 * f + 8 * k), bd + (uint64_t)(2 * k),
+                                       idesc, (kb > w.kb0 || j > 0 || k > 0) ? 1u : 0u, issuer);
+                    } else if (my_tile == 0) {
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            mma_tmem_a(tmem_base, tmem_a + kAStageCols * st + (uint32_t)(8 * k), bd + (uint64_t)(2 * k),
+                                       idesc, (kb > w.kb0 || j > 0 || k > 0) ? 1u : 0u, issuer);
+                    } else if (w.n2) {
+                        // the third token tile: its rows follow the first two 16 KB boxes; its
+                        // accumulator columns follow theirs
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            mma_tmem_a(tmem_base + 256u, tmem_a + kAStageCols * st + (uint32_t)(8 * k),
+                                       bd + (uint64_t)((32768 >> 4) + 2 * k), idesc2,
+                                       (kb > w.kb0 || j > 0 || k > 0) ? 1u : 0u, issuer);
+                    }
                     mma_commit<1>(smem_addr(&empty[st]), issuer);
                 }
                 stage = st1 + 1;
@@ -367,7 +398,7 @@ __global__ void __launch_bounds__(kW4Threads, 1) lora_w4_kernel(const __grid_con
                 if (stage == stages) { stage = 0; phase ^= 1; }
             }
             const uint32_t idesc_e = instr_desc_bf16(kW4TileM, 128);
-            for (int h = 0; h < 2 && ok && w.expand; ++h) {
+            for (int h = 0; h < 3 && ok && w.expand; ++h) {
                 if (w.g.nrows[h] == 0 || w.g.adapter[h] == 0) continue;
                 for (int kr = 0; kr < p.k_lora_blocks; kr += 2) {
                     const int ns = kr + 1 < p.k_lora_blocks ? 2 : 1;
@@ -493,7 +524,7 @@ __global__ void __launch_bounds__(kW4Threads, 1) lora_w4_kernel(const __grid_con
                 if (++stage == stages) { stage = 0; phase ^= 1; }
             }
             // expand K-steps: no weights to convert, only this quadrant's arrive
-            for (int h = 0; h < 2 && ok && w.expand; ++h) {
+            for (int h = 0; h < 3 && ok && w.expand; ++h) {
                 if (w.g.nrows[h] == 0 || w.g.adapter[h] == 0) continue;
                 for (int kr = 0; kr < p.k_lora_blocks; ++kr) {
                     if ((stage & 1) == par) {
@@ -548,11 +579,11 @@ __global__ void __launch_bounds__(kW4Threads, 1) lora_w4_kernel(const __grid_con
                 if (role == 2) break;    // the wait ran out: the CTA is aborting
                 store_part = role == 1;
             }
-            // FT = 1: token tile h at accumulator columns 128 h; FT = 2 (one token tile): feature
+            // FT = 1: token tile h (up to three) at accumulator columns 128 h; FT = 2 (one token tile): feature
             // tile f at accumulator columns 128 f. The accumulator is released right after the
             // unit's last tensor-memory load, before that chunk's stores.
-            const int last_hf = FT == 1 ? (w.g.nrows[1] > 0 ? 1 : 0) : 1;
-            for (int hf = 0; hf < 2; ++hf) {
+            const int last_hf = FT == 1 ? (w.g.nrows[2] > 0 ? 2 : w.g.nrows[1] > 0 ? 1 : 0) : 1;
+            for (int hf = 0; hf < (FT == 1 ? 3 : 2); ++hf) {
                 const int h = FT == 1 ? hf : 0;
                 const int n_tile = w.n0 + (FT == 1 ? 0 : kW4TileM * hf);
                 const int n = n_tile + 32 * q + lane;
@@ -688,8 +719,13 @@ cudaError_t launch_w4(const W4Params& p, int grid, cudaStream_t stream) {
     // with FT = 1, the expand's U and B_a boxes of 16 KB each)
     const int ft = p.feature_tiles;
     if ((ft != 1 && ft != 2) || w4_smem_bytes(p.stages, p.pstages, p.x_stage_bytes, ft) > (size_t)kSmemLimit ||
-        p.stages < 2 || p.stages * 32 * ft > 256 || (p.stages & 1) || p.pstages < 2 || (p.x_stage_bytes & 1023) ||
+        p.stages < 2 || p.stages * 32 * ft > (p.tail_rows ? 128 : 256) || (p.stages & 1) || p.pstages < 2 ||
+        (p.x_stage_bytes & 1023) ||
         p.x_stage_bytes < 16384 || p.x_stage_bytes > (int)dev::kXStageMaxBytes || (ft == 2 && p.n_ntiles * 256 < p.d_out))
+        return cudaErrorInvalidValue;
+    // a third token tile (FT = 1): its X box of at most kW4TailRows rows after the first two
+    if (p.tail_rows && (ft != 1 || p.tail_rows > kW4TailRows || (p.tail_rows & 15) ||
+                        p.x_stage_bytes < 32768 + p.tail_rows * 128))
         return cudaErrorInvalidValue;
     // K parts: every part a whole number of packed boxes (4 K-steps), the last one keeping at least one
     if (p.k_split > 1 && (p.k_chunk < 4 || (p.k_chunk & 3) || (p.k_split - 1) * p.k_chunk >= p.k_main_blocks ||

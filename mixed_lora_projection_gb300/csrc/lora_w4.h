@@ -9,19 +9,25 @@ namespace lora {
 
 // 4-bit base kernel (transposed tile: output features on the MMA's M side, tokens on N).
 // A token group is one or two consecutive planner tiles (each <= 128 rows and one adapter);
-// its X rows form the B operand of up to 256 columns. Units = groups x output tiles of 128
-// features, in the order W4Params::tokens_fastest selects.
+// its X rows form the B operand of up to 256 columns. A batch of exactly three tiles whose last
+// one has at most kW4TailRows rows is one group of three: the third tile's rows (its own X box)
+// are the B operand of a second MMA per 16-wide K step, so each weight tile is dequantised once
+// for the whole batch. Units = groups x output tiles of 128 features, in the order
+// W4Params::tokens_fastest selects.
 constexpr int kW4TileM = 128;         // output features per unit (TMEM lanes)
 constexpr int kW4Threads = 512;       // warp 0 TMA (X, U, B_a), 1 MMA, 2..5 epilogue,
                                       // 6..13 dequantise into TMEM, 14 TMA of the packed base,
-                                      // 15 the second feature tile's MMAs (two tiles per unit)
+                                      // 15 the second MMA of a K16 step: the second feature
+                                      // tile's (two feature tiles per unit) or the third token
+                                      // tile's (three token tiles per group)
+constexpr int kW4TailRows = 96;       // most rows of the third token tile of a group
 constexpr int kW4ConvertWarps = 8;
 constexpr int kW4AStages = 8;         // most ring stages (TMEM A stages of 32 columns each)
 constexpr int kW4InlineGroups = 48;
 constexpr int kW4PackBytes = 128;     // packed bytes per row per TMA box (4 K-steps of 64)
 
 struct W4Group {
-    int32_t row0[2], nrows[2], adapter[2];  // second tile absent when nrows[1] == 0
+    int32_t row0[3], nrows[3], adapter[3];  // a tile is absent when its nrows is 0
 };
 
 struct W4Params {
@@ -29,6 +35,7 @@ struct W4Params {
     W4Group inline_groups[kW4InlineGroups];
     int inline_wl;
     CUtensorMap tm_x;                // X [T, d_in] bf16, box 64 x 128, 128-byte swizzle
+    CUtensorMap tm_x3;               // X, box 64 x tail_rows: the third token tile of a group
     CUtensorMap tm_u;                // U [u_rows, rank] bf16, box 64 x 128, 128-byte swizzle
     CUtensorMap tm_wq;               // packed base [d_out, d_in/2] u8 (kernel layout), box 128 x 128, swizzled
     CUtensorMap tm_ws;               // scales [d_in/128, d_out] bf16, box 128 x 2
@@ -50,6 +57,8 @@ struct W4Params {
     int tokens_fastest;              // unit order: 1 = token groups fastest, 0 = feature tiles fastest
     int feature_tiles;               // 128-feature tiles per unit: 1, or 2 for one token tile of at
                                      // most 128 rows with no adapter rows (tm_wq / tm_ws boxes 128 x FT)
+    int tail_rows;                   // FT = 1: rows of the third token tile's X box (a multiple of 16,
+                                     // <= kW4TailRows) when the call's group has three tiles, else 0
     // K parts (k_split > 1): every (token group, feature tile) block runs as k_split units over
     // parts of the base K-steps (k_chunk each, a multiple of 4; the last part takes the rest and
     // the expand); every part but the last to finish stores its fp32 sums in `partials`, the last

@@ -294,11 +294,12 @@ def test_host_chunk_schedule(lib, T):
 
 
 # the 4-bit kernel's shape: two feature tiles per unit for a decode batch (one token tile, no
-# adapter rows); token groups fastest where the packed base exceeds 32 MB and X fits in 64 MB
+# adapter rows); token groups fastest where the packed base exceeds 32 MB and X fits in 64 MB;
+# one group of three tiles for the near-ridge batch (128 + 128 + 92 rows)
 W4_SHAPES = {
     # name: (output columns per unit, unit order, token groups)
     "prefill_16k": (128, 0, 64), "mixed_batch": (128, 1, 17), "mixed_8x300": (128, 1, 10),
-    "prefix_tail_1552": (128, 1, 7), "mixed_near_ridge": (128, 1, 2), "mixed_decode": (256, 0, 1),
+    "prefix_tail_1552": (128, 1, 7), "mixed_near_ridge": (128, 0, 1), "mixed_decode": (256, 0, 1),
     "prefill_32k": (128, 0, 128),
 }
 

@@ -435,3 +435,30 @@ def test_w4_k_parts_with_several_token_groups(dev):
         assert ll.status() == 0
     assert torch.equal(y1, y2)
     assert rel_err(y1, _oracle(inp, q, sc, off, ids)) <= TOL
+
+
+@pytest.mark.parametrize("case", [([128, 128, 92], [1, 1, 1]), ([50, 78, 128, 60], [0, 1, 2, 3]),
+                                  ([128, 100, 28, 40], [0, 2, 2, 0])])
+def test_w4_three_token_tiles_in_one_group(dev, case):
+    # a batch of three tiles whose last has at most 96 rows runs as one token group (the third
+    # tile's rows the B operand of a second MMA, its expand the group's third): against the oracle,
+    # and its first 128 rows bitwise equal to the same rows in a batch of their own
+    from mixed_lora_projection_gb300 import launch_shape
+    lens, ids = case
+    off = [0] + np.cumsum(lens).tolist()
+    T = off[-1]
+    w = Workload("w4t3", 22, T, 1024, 768, 32, tuple(off), tuple(ids), n_adapters=3, scales=(0.5, -1.0, 1.5))
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    assert launch_shape(1024, 768, 32, sms, T, off, ids, w4=True)["fused_units"] == 768 // 128
+    inp = make_inputs(w, dev)
+    q, sc = make_w4_base(w, dev)
+    kq = _kq(q)
+    with _ll(w) as ll:
+        y = ll.forward_w4(inp.x, off, ids, kq, sc, inp.a, inp.b, inp.scales).clone()
+        off1 = [o for o in off if o <= 128] + ([] if 128 in off else [128])   # the first 128 rows
+        ids1 = ids[:len(off1) - 1]
+        y1 = ll.forward_w4(inp.x[:128], off1, ids1, kq, sc, inp.a, inp.b, inp.scales)
+        torch.cuda.synchronize()
+        assert ll.status() == 0
+    assert rel_err(y, _oracle(inp, q, sc, off, ids)) <= TOL
+    assert torch.equal(y[:128], y1)
