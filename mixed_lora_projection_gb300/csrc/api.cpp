@@ -1093,10 +1093,23 @@ int forward_impl(lora_linear* h, const void* x, int T, const int32_t* seg_offset
     Shape sh = choose_shape(h, plan, !w4);
     // 4-bit base: the shrink pass runs on the bf16 kernel (64-wide K-steps), then the 4-bit
     // kernel runs the base and expand passes over token groups
+    int shrink_rank_tiles = 1;
     if (w4) {
         // the 4-bit kernel reads X and U through the same maps with 128-row boxes
         sh.bk = 64;
         sh.a_rows = kTileM;
+        // its shrink is a launch of its own: spread over rank tiles (multiples of 32 columns) so
+        // that a few shrink groups still find most SMs (48 + 300 rows: 3 groups x 4 tiles of 64);
+        // each U column is the same whole-K sum
+        const int groups = (int)(sh.shrink_groups.size() / sh.cs);
+        if (groups > 0 && h->k_split <= 1) {
+            const int room = std::max(1, usable_sms(h) / sh.cs / groups);
+            const int width = std::max(32, ceil_div(ceil_div(h->rank, std::min(room, 8)), 32) * 32);
+            if (width < sh.shrink_n) {
+                shrink_rank_tiles = ceil_div(h->rank, width);
+                sh.shrink_n = width;
+            }
+        }
         sh.stages = stages_for(std::max(sh.tile_n, sh.shrink_n) / sh.cs, sh.bk);
     }
     const std::vector<W4Group> w4_groups = w4 ? make_w4_groups(plan.fused) : std::vector<W4Group>();
@@ -1321,7 +1334,8 @@ int forward_impl(lora_linear* h, const void* x, int T, const int32_t* seg_offset
         if (nsg > 0) {
             GemmParams sp = p;
             sp.n_fused = 0;
-            if (launch_gemm(sp, std::min(nsg, slots) * cs, stream) != cudaSuccess) return LORA_ECUDA;
+            sp.shrink_ntiles = shrink_rank_tiles;
+            if (launch_gemm(sp, std::min(nsg * shrink_rank_tiles, slots) * cs, stream) != cudaSuccess) return LORA_ECUDA;
             ++h->launches;
             rec.has_shrink = true;
         }

@@ -128,14 +128,16 @@ __device__ __forceinline__ Unit decode_unit(const GemmParams& p, const WorkList&
     r.part = u - v0 * S;
     r.kb0 = r.part * p.k_chunk;
     r.kmain = r.part == S - 1 ? p.k_main_blocks - r.kb0 : p.k_chunk;
-    if (v0 < p.n_shrink) {
-        r.tile = wl.shrink[v0 * cs + rank];
+    const int srt = p.shrink_ntiles > 1 ? p.shrink_ntiles : 1;   // rank tiles per shrink group
+    if (v0 < p.n_shrink * srt) {
+        const int g = v0 / srt;
+        r.tile = wl.shrink[g * cs + rank];
         r.shrink = 1;
         r.tile_index = r.tile.fused_index;
-        r.n0 = 0;
+        r.n0 = (v0 - g * srt) * p.shrink_n;
         r.n = p.shrink_n;
         r.nk = r.kmain;
-        r.slot = p.shrink_slot0 + v0 * cs + rank;
+        r.slot = p.shrink_slot0 + g * cs + rank;
         r.pchunk = p.u_chunk0;
     } else if (YT) {
         // token-column unit: 256 output features (128 per CTA) for every token row
@@ -277,7 +279,8 @@ __global__ void __launch_bounds__(YT ? kThreadsYt : kThreads, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    const int n_units = (p.n_shrink + p.n_fused * p.n_ntiles) * (p.k_split > 1 ? p.k_split : 1);
+    const int n_units = (p.n_shrink * (p.shrink_ntiles > 1 ? p.shrink_ntiles : 1) + p.n_fused * p.n_ntiles) *
+                        (p.k_split > 1 ? p.k_split : 1);
     const uint64_t limit = p.wait_limit_ns;
     const WorkList wl = resolve_work_list(p);
     // the next call's kernel may start on the SMs this one leaves, and stream its first W tiles
@@ -552,8 +555,8 @@ __global__ void __launch_bounds__(YT ? kThreadsYt : kThreads, 1)
                 if (w.shrink) {
                     const int a = row_ok ? row_adapter(wl.seg_off, wl.seg_id, p.n_seg, row) : 0;
                     scale = (a == w.tile.adapter) ? wl.scales[w.tile.adapter - 1] : 0.0f;
-                    out = reinterpret_cast<__nv_bfloat16*>(p.u) + (size_t)row * p.rank;
-                    n_out = p.rank;
+                    out = reinterpret_cast<__nv_bfloat16*>(p.u) + (size_t)row * p.rank + w.n0;
+                    n_out = p.rank - w.n0;
                 } else {
                     out = reinterpret_cast<__nv_bfloat16*>(p.y) + (size_t)row * p.d_out + w.n0;
                     n_out = p.d_out - w.n0;
@@ -795,6 +798,9 @@ static cudaError_t dispatch(const GemmParams& p, F&& f) {
 }
 
 cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t stream) {
+    // rank tiles only in a launch of shrink units alone, without ready flags or K parts
+    if (p.shrink_ntiles > 1 && (p.n_fused || p.flags || p.k_split > 1 || p.shrink_n < 16 || (p.shrink_n & 15)))
+        return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[3];
     launch_config(p, grid, stream, &cfg, attr);

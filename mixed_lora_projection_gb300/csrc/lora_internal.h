@@ -124,6 +124,9 @@ struct GemmParams {
     // - yt_h)) into the columns after them. The launch runs n_ntiles such units (n_fused = 1).
     // Every token row names the same adapter, yt_adapter (0: none, no expand); the expand reads U
     // through tm_u, whose box is then yt_rows rows.
+    // Shrink units over rank tiles (a launch of shrink units alone, without ready flags or K
+    // parts): every shrink group runs shrink_ntiles units of shrink_n rank columns each.
+    int shrink_ntiles;               // 0 or 1: one unit over the whole rank
     int yt;
     int yt_tokens;                   // T: token rows stored
     int yt_rows;                     // token rows per CTA per stage (a multiple of 8, <= 256)
