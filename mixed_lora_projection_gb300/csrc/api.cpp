@@ -200,11 +200,12 @@ CUresult encode_u8_sw128(lora_linear* h, CUtensorMap* m, const void* ptr, uint64
 }
 
 // Token groups of the 4-bit base kernel: consecutive planner tiles in pairs.
-std::vector<W4Group> make_w4_groups(const std::vector<Tile>& fused) {
+std::vector<W4Group> make_w4_groups(const std::vector<Tile>& fused, bool allow_three = true) {
     std::vector<W4Group> g;
     // a batch of exactly three tiles whose last has at most kW4TailRows rows (a 300-row decision
-    // beside chat rows) is one group: each weight tile is dequantised once for all of it
-    const size_t per = (fused.size() == 3 && fused[2].nrows <= kW4TailRows) ? 3 : 2;
+    // beside chat rows) is one group: each weight tile is dequantised once for all of it (not on
+    // handles that split the 4-bit K-steps)
+    const size_t per = (allow_three && fused.size() == 3 && fused[2].nrows <= kW4TailRows) ? 3 : 2;
     for (size_t i = 0; i < fused.size(); i += per) {
         W4Group w;
         memset(&w, 0, sizeof(w));
@@ -1112,7 +1113,8 @@ int forward_impl(lora_linear* h, const void* x, int T, const int32_t* seg_offset
         }
         sh.stages = stages_for(std::max(sh.tile_n, sh.shrink_n) / sh.cs, sh.bk);
     }
-    const std::vector<W4Group> w4_groups = w4 ? make_w4_groups(plan.fused) : std::vector<W4Group>();
+    const std::vector<W4Group> w4_groups =
+        w4 ? make_w4_groups(plan.fused, h->w4_k_split <= 1) : std::vector<W4Group>();
     const int n_w4g = (int)w4_groups.size();
     const W4Shape w4s = w4 ? w4_shape(h, w4_groups, T) : W4Shape();
     const bool w4_inline = n_used <= kInlineAdapters && n_w4g <= kW4InlineGroups;
@@ -1651,7 +1653,7 @@ int lora_linear_shape(int d_in, int d_out, int rank, int num_sms, int T, const i
     const Shape sh = choose_shape(&h, plan, !w4);
     if (w4) {
         // the 4-bit kernel over token groups; the shrink runs as the bf16 kernel's shrink units
-        const std::vector<W4Group> groups = make_w4_groups(plan.fused);
+        const std::vector<W4Group> groups = make_w4_groups(plan.fused, h.w4_k_split <= 1);
         const W4Shape ws = w4_shape(&h, groups, T);
         if (cluster) *cluster = 1;
         if (tile_n) *tile_n = kW4TileM * ws.feature_tiles;

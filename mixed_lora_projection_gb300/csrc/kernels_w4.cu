@@ -118,7 +118,7 @@ struct W4Unit {
     bool expand;     // runs the expand's K-steps (the last part)
 };
 
-template <int FT, bool SPLIT>
+template <int FT, bool SPLIT, bool TAIL>
 __device__ __forceinline__ W4Unit w4_unit(const W4Params& p, const W4Group* groups, int u) {
     W4Unit r;
     const int S = SPLIT ? p.k_split : 1;
@@ -133,10 +133,11 @@ __device__ __forceinline__ W4Unit w4_unit(const W4Params& p, const W4Group* grou
     r.n0 = w4_ntile_of(p, v) * kW4TileM * FT;
     // token tile h at accumulator columns 128 h: a third tile makes the first MMA cover both
     // of the first two tiles whole
-    r.n = r.g.nrows[2] > 0   ? 256
+    const bool third = TAIL && r.g.nrows[2] > 0;
+    r.n = third              ? 256
           : r.g.nrows[1] > 0 ? 128 + ((r.g.nrows[1] + 15) & ~15)
                              : ((r.g.nrows[0] + 15) & ~15);
-    r.n2 = r.g.nrows[2] > 0 ? ((r.g.nrows[2] + 15) & ~15) : 0;
+    r.n2 = third ? ((r.g.nrows[2] + 15) & ~15) : 0;
     return r;
 }
 
@@ -164,8 +165,9 @@ static __device__ __noinline__ bool wait_count64(const unsigned long long* count
 // with no adapter rows (decode steps): the unit's two tiles share each K-step's X stage, barrier
 // round trips and ring slots, which halves the K-steps an SM runs in sequence. Tensor memory
 // then holds two 128-column accumulators (tile f at column 128 f) and A stages of 64 columns.
-template <int FT, bool SPLIT>
+template <int FT, bool SPLIT, bool TAIL>
 __global__ void __launch_bounds__(kW4Threads, 1) lora_w4_kernel(const __grid_constant__ W4Params p) {
+    static_assert(!TAIL || FT == 1, "a third token tile only with one feature tile per unit");
     static_assert(FT == 1 || FT == 2, "one or two feature tiles per unit");
     constexpr uint32_t kQStage = FT * kQStageBytes;    // packed rows of the unit's feature tiles
     constexpr uint32_t kSStage = FT * kSStageBytes;    // their scales (two groups of 128 inputs)
@@ -199,8 +201,8 @@ __global__ void __launch_bounds__(kW4Threads, 1) lora_w4_kernel(const __grid_con
 
     // MMA warps (one per feature tile of a unit, or two with a third token tile): each commits
     // every stage, accumulator and drain
-    const bool mma2 = FT == 2 || p.tail_rows > 0;
-    const uint32_t kIssuers = mma2 ? 2u : 1u;
+    constexpr bool mma2 = FT == 2 || TAIL;
+    constexpr uint32_t kIssuers = mma2 ? 2u : 1u;
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
             mbar_init(smem_addr(&full[s]), 1 + kW4ConvertWarps / 2);
@@ -222,7 +224,7 @@ __global__ void __launch_bounds__(kW4Threads, 1) lora_w4_kernel(const __grid_con
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     // A stages after the accumulators: columns 256 + 32 FT s, or 384 + 32 s past a third token tile
-    const uint32_t tmem_a = tmem_base + (FT == 1 && p.tail_rows ? 3u * 128u : kAccCols4);
+    const uint32_t tmem_a = tmem_base + (TAIL ? 3u * 128u : kAccCols4);
 
     const int n_units = p.n_groups * p.n_ntiles * (SPLIT ? p.k_split : 1);
     const uint64_t limit = p.wait_limit_ns;
@@ -244,8 +246,8 @@ __global__ void __launch_bounds__(kW4Threads, 1) lora_w4_kernel(const __grid_con
             int acquired = -1;
             bool ok = true;
             for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-                const W4Unit w = w4_unit<FT, SPLIT>(p, groups, u);
-                const int ntile = w.g.nrows[2] > 0 ? 3 : w.g.nrows[1] > 0 ? 2 : 1;
+                const W4Unit w = w4_unit<FT, SPLIT, TAIL>(p, groups, u);
+                const int ntile = (TAIL && w.g.nrows[2] > 0) ? 3 : w.g.nrows[1] > 0 ? 2 : 1;
                 // tiles 0 and 1: 128-row boxes; a third tile: its own box of tail_rows rows
                 const uint32_t x_bytes = (ntile < 3 ? (uint32_t)ntile : 2u) * 16384u +
                                          (ntile == 3 ? (uint32_t)p.tail_rows * 128u : 0u);
@@ -263,7 +265,7 @@ __global__ void __launch_bounds__(kW4Threads, 1) lora_w4_kernel(const __grid_con
                     ++issued;
                     if (++stage == stages) { stage = 0; phase ^= 1; }
                 }
-                for (int h = 0; h < 3 && ok && w.expand; ++h) {
+                for (int h = 0; h < (TAIL ? 3 : 2) && ok && w.expand; ++h) {
                     const int a = w.g.adapter[h];
                     if (w.g.nrows[h] == 0 || a == 0) continue;
                     const CUtensorMap* bm = &bmaps[a - 1];
@@ -308,7 +310,7 @@ __global__ void __launch_bounds__(kW4Threads, 1) lora_w4_kernel(const __grid_con
             long long issued = 0;
             bool ok = true;
             for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-                const W4Unit w = w4_unit<FT, SPLIT>(p, groups, u);
+                const W4Unit w = w4_unit<FT, SPLIT, TAIL>(p, groups, u);
                 const int n0 = w.n0;
                 // packed boxes of 4 K-steps; part boundaries are multiples of 4 K-steps
                 for (int pb = w.kb0 >> 2; pb < ((w.kend + 3) >> 2); ++pb) {
@@ -344,7 +346,7 @@ __global__ void __launch_bounds__(kW4Threads, 1) lora_w4_kernel(const __grid_con
         int it = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++it) {
-            const W4Unit w = w4_unit<FT, SPLIT>(p, groups, u);
+            const W4Unit w = w4_unit<FT, SPLIT, TAIL>(p, groups, u);
             if (!wait_warp(smem_addr(tempty), (it & 1) ^ 1, abort_flag, p.status, limit)) {
                 ok = false;
                 break;
@@ -377,7 +379,7 @@ __global__ void __launch_bounds__(kW4Threads, 1) lora_w4_kernel(const __grid_con
                             mma_tmem_a(tmem_base + (uint32_t)(128 * f),
                                        tmem_a + kAStageCols * st + (uint32_t)(32 * f + 8 * k), bd + (uint64_t)(2 * k),
                                        idesc, (kb > w.kb0 || j > 0 || k > 0) ? 1u : 0u, issuer);
-                    } else if (my_tile == 0) {
+                    } else if (!TAIL || my_tile == 0) {
 #pragma unroll
                         for (int k = 0; k < 4; ++k)
                             mma_tmem_a(tmem_base, tmem_a + kAStageCols * st + (uint32_t)(8 * k), bd + (uint64_t)(2 * k),
@@ -398,7 +400,7 @@ __global__ void __launch_bounds__(kW4Threads, 1) lora_w4_kernel(const __grid_con
                 if (stage == stages) { stage = 0; phase ^= 1; }
             }
             const uint32_t idesc_e = instr_desc_bf16(kW4TileM, 128);
-            for (int h = 0; h < 3 && ok && w.expand; ++h) {
+            for (int h = 0; h < (TAIL ? 3 : 2) && ok && w.expand; ++h) {
                 if (w.g.nrows[h] == 0 || w.g.adapter[h] == 0) continue;
                 for (int kr = 0; kr < p.k_lora_blocks; kr += 2) {
                     const int ns = kr + 1 < p.k_lora_blocks ? 2 : 1;
@@ -460,7 +462,7 @@ __global__ void __launch_bounds__(kW4Threads, 1) lora_w4_kernel(const __grid_con
         uint32_t pph = 0, phase = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-            const W4Unit w = w4_unit<FT, SPLIT>(p, groups, u);
+            const W4Unit w = w4_unit<FT, SPLIT, TAIL>(p, groups, u);
             for (int kb = w.kb0; kb < w.kend; ++kb) {
                 if ((kb & 3) == 0 &&
                     !wait_warp(smem_addr(&pfull[ps]), pph, abort_flag, p.status, limit)) {
@@ -524,7 +526,7 @@ __global__ void __launch_bounds__(kW4Threads, 1) lora_w4_kernel(const __grid_con
                 if (++stage == stages) { stage = 0; phase ^= 1; }
             }
             // expand K-steps: no weights to convert, only this quadrant's arrive
-            for (int h = 0; h < 3 && ok && w.expand; ++h) {
+            for (int h = 0; h < (TAIL ? 3 : 2) && ok && w.expand; ++h) {
                 if (w.g.nrows[h] == 0 || w.g.adapter[h] == 0) continue;
                 for (int kr = 0; kr < p.k_lora_blocks; ++kr) {
                     if ((stage & 1) == par) {
@@ -552,7 +554,7 @@ __global__ void __launch_bounds__(kW4Threads, 1) lora_w4_kernel(const __grid_con
         int chunk = 0;
         int it = 0;
         for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++it) {
-            const W4Unit w = w4_unit<FT, SPLIT>(p, groups, u);
+            const W4Unit w = w4_unit<FT, SPLIT, TAIL>(p, groups, u);
             int ok = 1;
             if (lane == 0) ok = wait_bounded(smem_addr(tfull), it & 1, abort_flag, p.status, limit, true);
             ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -582,8 +584,8 @@ __global__ void __launch_bounds__(kW4Threads, 1) lora_w4_kernel(const __grid_con
             // FT = 1: token tile h (up to three) at accumulator columns 128 h; FT = 2 (one token tile): feature
             // tile f at accumulator columns 128 f. The accumulator is released right after the
             // unit's last tensor-memory load, before that chunk's stores.
-            const int last_hf = FT == 1 ? (w.g.nrows[2] > 0 ? 2 : w.g.nrows[1] > 0 ? 1 : 0) : 1;
-            for (int hf = 0; hf < (FT == 1 ? 3 : 2); ++hf) {
+            const int last_hf = FT == 1 ? ((TAIL && w.g.nrows[2] > 0) ? 2 : w.g.nrows[1] > 0 ? 1 : 0) : 1;
+            for (int hf = 0; hf < (TAIL ? 3 : 2); ++hf) {
                 const int h = FT == 1 ? hf : 0;
                 const int n_tile = w.n0 + (FT == 1 ? 0 : kW4TileM * hf);
                 const int n = n_tile + 32 * q + lane;
@@ -691,16 +693,18 @@ size_t w4_smem_bytes(int stages, int pstages, int x_stage_bytes, int ft) {
            8 * (2 * (size_t)stages + 2 * (size_t)pstages + 3) + 16;
 }
 
+template <int FT, bool SPLIT, bool TAIL>
+static cudaError_t w4_smem_attr() {
+    return cudaFuncSetAttribute(dev::lora_w4_kernel<FT, SPLIT, TAIL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kSmemLimit);
+}
+
 cudaError_t w4_prepare_device() {
     cudaError_t e;
-    if ((e = cudaFuncSetAttribute(dev::lora_w4_kernel<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  kSmemLimit)) != cudaSuccess ||
-        (e = cudaFuncSetAttribute(dev::lora_w4_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  kSmemLimit)) != cudaSuccess ||
-        (e = cudaFuncSetAttribute(dev::lora_w4_kernel<2, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  kSmemLimit)) != cudaSuccess)
+    if ((e = w4_smem_attr<1, false, false>()) != cudaSuccess || (e = w4_smem_attr<1, true, false>()) != cudaSuccess ||
+        (e = w4_smem_attr<1, false, true>()) != cudaSuccess || (e = w4_smem_attr<2, false, false>()) != cudaSuccess)
         return e;
-    return cudaFuncSetAttribute(dev::lora_w4_kernel<2, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+    return w4_smem_attr<2, true, false>();
 }
 
 // Cooperative launches can be switched off for a profiler (LORA_LINEAR_NONCOOPERATIVE=1), as for
@@ -724,7 +728,7 @@ cudaError_t launch_w4(const W4Params& p, int grid, cudaStream_t stream) {
         p.x_stage_bytes < 16384 || p.x_stage_bytes > (int)dev::kXStageMaxBytes || (ft == 2 && p.n_ntiles * 256 < p.d_out))
         return cudaErrorInvalidValue;
     // a third token tile (FT = 1): its X box of at most kW4TailRows rows after the first two
-    if (p.tail_rows && (ft != 1 || p.tail_rows > kW4TailRows || (p.tail_rows & 15) ||
+    if (p.tail_rows && (ft != 1 || p.k_split > 1 || p.tail_rows > kW4TailRows || (p.tail_rows & 15) ||
                         p.x_stage_bytes < 32768 + p.tail_rows * 128))
         return cudaErrorInvalidValue;
     // K parts: every part a whole number of packed boxes (4 K-steps), the last one keeping at least one
@@ -748,10 +752,11 @@ cudaError_t launch_w4(const W4Params& p, int grid, cudaStream_t stream) {
     }
     const bool split = p.k_split > 1;
     if (ft == 2)
-        return split ? cudaLaunchKernelEx(&cfg, dev::lora_w4_kernel<2, true>, p)
-                     : cudaLaunchKernelEx(&cfg, dev::lora_w4_kernel<2, false>, p);
-    return split ? cudaLaunchKernelEx(&cfg, dev::lora_w4_kernel<1, true>, p)
-                 : cudaLaunchKernelEx(&cfg, dev::lora_w4_kernel<1, false>, p);
+        return split ? cudaLaunchKernelEx(&cfg, dev::lora_w4_kernel<2, true, false>, p)
+                     : cudaLaunchKernelEx(&cfg, dev::lora_w4_kernel<2, false, false>, p);
+    if (p.tail_rows) return cudaLaunchKernelEx(&cfg, dev::lora_w4_kernel<1, false, true>, p);
+    return split ? cudaLaunchKernelEx(&cfg, dev::lora_w4_kernel<1, true, false>, p)
+                 : cudaLaunchKernelEx(&cfg, dev::lora_w4_kernel<1, false, false>, p);
 }
 
 }  // namespace lora
