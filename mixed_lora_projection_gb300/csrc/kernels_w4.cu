@@ -30,7 +30,11 @@
 //               10..13 the odd ones) for the 32 features of lane quadrant w % 4, packed
 //               ring -> TMEM, and counts itself in on the stage's full barrier;
 //   warp 14     TMA of the packed base and its scales (4 K-steps per box) into their ring;
-//   warp 15     with two feature tiles per unit: the second tile's MMAs (see warp 1).
+//   warp 15     with two feature tiles per unit: the second tile's MMAs (see warp 1); with three
+//               token tiles in a group: the third tile's MMAs (its rows the B operand, its
+//               accumulator at columns 256 ..).
+// Instantiations: FT (feature tiles per unit), SPLIT (K parts), TAIL (a third token tile); the
+// code of each option stays out of the others' instantiations, where it cost registers and time.
 // Every wait is bounded as in the bf16 kernel (status word, abort flag, orderly exit).
 #include <cuda.h>
 #include <cuda_bf16.h>
