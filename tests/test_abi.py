@@ -316,6 +316,21 @@ def test_w4_launch_shape_choices(lib, name):
     assert (s["shrink_units"] == 0) == (w.adapter_rows == 0)
 
 
+def test_w4_decode_shapes_fill_the_gpu(lib):
+    # 48-row decode batches on the 4-bit base: gate_up keeps two feature tiles per unit (136 units),
+    # qkv runs one tile per unit (96 units), o and down one tile per unit with K in 3 parts (40 x 3
+    # units) on a decode-sized handle; a handle for more than 128 rows never splits
+    from mixed_lora_projection_gb300 import launch_shape
+    from mixed_lora_projection_gb300.synth import WORKLOADS
+    want = {"decode_gate_up": (256, 136), "decode_qkv": (128, 96), "decode_o": (128, 120), "decode_down": (128, 120)}
+    for name, (cols, units) in want.items():
+        w = WORKLOADS[name]
+        s = launch_shape(w.d_in, w.d_out, w.rank, 152, w.T, w.seg_offsets, w.seg_ids, w4=True)
+        assert (s["tile_n"], s["fused_units"]) == (cols, units), (name, s)
+    s = launch_shape(6144, 5120, 256, 152, 129, (0, 129), (0,), w4=True)
+    assert s["fused_units"] == 40          # one token group of two tiles, whole K
+
+
 def test_w4_launch_shape_rejects_d_in_not_multiple_of_128(lib):
     from mixed_lora_projection_gb300 import LoraError, launch_shape
     with pytest.raises(LoraError):
