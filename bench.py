@@ -317,6 +317,8 @@ def run_ours(args, rank, world, dist):
                 handles[key].set_option(L.OPT_PDL, 1)
             if args.token_columns:
                 handles[key].set_option(L.OPT_TOKEN_COLUMNS, args.token_columns)
+            if args.wide_tiles:
+                handles[key].set_option(L.OPT_WIDE_TILES, args.wide_tiles)
             if args.raster:
                 mode, _, group = args.raster.partition(":")
                 handles[key].set_option(L.OPT_RASTER, int(mode))
@@ -474,6 +476,7 @@ def run_ours(args, rank, world, dist):
                    **({"k_split": args.k_split} if args.k_split else {}),
                    **({"pdl": True} if args.pdl else {}),
                    **({"token_columns": args.token_columns} if args.token_columns else {}),
+                   **({"wide_tiles": args.wide_tiles} if args.wide_tiles else {}),
                    "base": "int4 (symmetric, group 128, bf16 scales)" if args.w4 else "bf16", "T": w0.T, "d_in": w0.d_in if len(items) == 1 else "per projection",
                    "d_out": w0.d_out if len(items) == 1 else "per projection", "rank": w0.rank,
                    "segments": len(w0.seg_ids), "adapter_rows": w0.adapter_rows, "calls_per_step": len(items),
@@ -655,6 +658,8 @@ def main():
     ap.add_argument("--token-columns", type=int, default=0, choices=[0, 1, 2], help="token-column units (the "
                     "library's option: 0 = when the shape model expects them sooner, 1 = never, 2 = whenever the "
                     "batch allows)")
+    ap.add_argument("--wide-tiles", type=int, default=0, choices=[0, 1], help="wide row tiles (the library's "
+                    "option: 0 = when the shape model expects them sooner, 1 = never)")
     ap.add_argument("--graph", action="store_true", help="time the steps as CUDA-graph replays (each call's "
                     "work list must travel in the kernel parameters, e.g. the 24-layer sweep)")
     args = ap.parse_args()

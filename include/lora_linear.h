@@ -219,7 +219,9 @@ int lora_linear_validate(int d_in, int d_out, int rank, int max_tokens, int max_
 
 /* Tunables and diagnostics (tests, benchmarks). */
 enum {
-    LORA_OPT_TILE_N = 1,        /* force the output-tile width (multiple of 16, 16..256); 0 = auto */
+    LORA_OPT_TILE_N = 1,        /* force the output-tile width (multiple of 16, 16..256; 272..512 runs
+                                   wide row tiles on SM pairs of the bf16 base with whole K, see
+                                   LORA_OPT_WIDE_TILES, else 256); 0 = auto */
     LORA_OPT_WAIT_LIMIT_US = 2, /* bound of every in-kernel wait, microseconds (default 4,000,000) */
     LORA_OPT_DEBUG_STALL = 3,   /* 1 = the load warp never issues: every wait runs out (tests only) */
     LORA_OPT_TIMING = 4,        /* 1 = record CUDA events around each kernel launch */
@@ -262,13 +264,18 @@ enum {
                                    and no 128-row tile is padded. 0 (default) = when the launch-shape model
                                    expects them to finish sooner, 1 = never, 2 = whenever the batch allows
                                    them. Does not change any result */
-    LORA_OPT_W4_K_SPLIT = 18    /* 4-bit base: 0 = the handle's own choice (made at create: decode-sized
+    LORA_OPT_W4_K_SPLIT = 18,   /* 4-bit base: 0 = the handle's own choice (made at create: decode-sized
                                    handles of at most 128 rows whose one-tile units would leave most SMs
                                    idle split K in 2 to 4 parts), 1 = whole K, 2..4 = K in that many parts
                                    (each a multiple of 4 K-steps, at least 8; fewer where K is too short).
                                    Every part but the last to finish stores its fp32 sums, the last adds
                                    them in part order before the bf16 rounding. Changes the summation for
                                    later calls; may allocate (LORA_ENOMEM) */
+    LORA_OPT_WIDE_TILES = 19    /* bf16 base, SM pairs, whole K: wide row tiles of 288 to 320 output columns
+                                   (each 16-wide K step a second MMA over the columns past 256, one
+                                   accumulator per unit), so that a projection's units fill whole waves of
+                                   SM pairs. 0 (default) = when the launch-shape model expects them to
+                                   finish sooner, 1 = never. Does not change any result */
 };
 
 /* lora_linear_set_option -- set one option above. Returns LORA_OK or LORA_EINVAL. */

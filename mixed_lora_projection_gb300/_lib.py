@@ -50,7 +50,7 @@ LORA_OK, LORA_EINVAL, LORA_ENOMEM, LORA_ECUDA, LORA_ETIMEOUT, LORA_EUNSUPPORTED,
 (OPT_TILE_N, OPT_WAIT_LIMIT_US, OPT_DEBUG_STALL, OPT_TIMING, OPT_RASTER, OPT_TWO_LAUNCH, OPT_CLUSTER,
  OPT_RASTER_GROUP, _OPT_RETIRED_9, OPT_TILE_K, OPT_INLINE_WORK_LIST, OPT_MMA_GROUP,
  OPT_DEBUG_PUBLISH_DELAY_US, OPT_K_SPLIT, OPT_MAX_CTAS, OPT_PDL,
- OPT_TOKEN_COLUMNS, OPT_W4_K_SPLIT) = 1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 11, 12, 13, 14, 15, 16, 17, 18
+ OPT_TOKEN_COLUMNS, OPT_W4_K_SPLIT, OPT_WIDE_TILES) = 1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 11, 12, 13, 14, 15, 16, 17, 18, 19
 
 
 def load():

@@ -83,6 +83,7 @@ struct lora_linear {
     int max_ctas = 0;           // LORA_OPT_MAX_CTAS: at most this many CTAs per launch (0 = one per SM)
     int pdl = 0;                // LORA_OPT_PDL: launches without ready flags may start early
     int yt_mode = 0;            // LORA_OPT_TOKEN_COLUMNS: 0 = auto, 1 = never, 2 = whenever a batch allows
+    int wide_mode = 0;          // LORA_OPT_WIDE_TILES: 0 = auto, 1 = never
     // 4-bit base K parts: chosen once per handle like k_split
     int w4_k_split = 1;         // 1..4: every 4-bit block runs as that many units over parts of K
     int w4_k_split_opt = 0;     // LORA_OPT_W4_K_SPLIT: 0 = the handle's own choice
@@ -344,7 +345,20 @@ int max_clusters(lora_linear* h, const GemmParams& p) {
 // lands only half of B per SM and its cost falls less than proportionally with N (the A tile
 // and the per-step barrier round trips stay): fitted to 16k-prefill units of 256, 224 and 192
 // columns, which cost 1 : 0.954 : 0.862 per unit.
+//
+// Wide row tiles (SM pairs, 288 to 320 columns) add a second MMA per 16-wide K step over the
+// columns past 256, which costs ~50-90 cycles whatever its width (the tensor pipe's floor per
+// instruction), and hold all of TMEM in one accumulator: measured per unit against a 256-column
+// unit on 2,048-row projections, 1.31x (down, 17,408 -> 5,120) to 1.51x (o, 6,144 -> 5,120) for
+// 12-25% more columns. They pay where they take a wave off a projection whose units do not fill
+// their last wave (down at 2,048 rows: 160 units of 256 columns on 76 SM pairs, 3 waves; 149 of
+// 288, 2 waves: 271 -> 237 us). kWideKstepFactor is the per-K-step cost against a 256-column
+// unit that reproduces the measured choices (down and o: 288; qkv, gate_up, the prefills: not).
+constexpr double kWideKstepFactor = 1.32;
+constexpr int kMinAutoWideTileN = 288, kMaxAutoWideTileN = 320;
+
 double kstep_cycles(int cs, int n) {
+    if (cs > 1 && n > kMaxTileN) return kWideKstepFactor * kstep_cycles(2, kMaxTileN);
     if (cs > 1) return 300.0 + 1.58 * n;
     const double mma = 4.0 * std::max(n / 2.0, 48.0) + 130.0;
     const double fill = (kTileM + (double)n) * kTileK * 2.0 / 61.0;
@@ -438,10 +452,18 @@ double yt_makespan(const lora_linear* h, const Plan& plan, int slots) {
     return *std::max_element(load.begin(), load.end());
 }
 
+// On SM pairs a tile narrower than 256 columns replaces the best 256-column or wide one only when
+// the model expects it at least this much sooner: narrow pair tiles measured slower than the model
+// expects on 2,048-row projections (o: 192 columns 103.8 us against 95.5 us for 256, where the
+// model expected 192 to finish 10% sooner), while where they win the model expects more (qkv:
+// 224 columns, 7% expected, 3-7% measured).
+constexpr double kNarrowPairMargin = 0.05;
+
 // The launch shape (SM pair or single CTA, output-tile width) the makespan model expects to
-// finish a plan soonest with K in `k_split` parts; cs / tn nonzero fix that choice. Returns the
-// expected makespan.
-double search_shape(const lora_linear* h, const Plan& plan, int cs, int tn, int k_split, int* out_cs, int* out_tn) {
+// finish a plan soonest with K in `k_split` parts; cs / tn nonzero fix that choice; `wide` lets SM
+// pairs weigh wide row tiles. Returns the expected makespan.
+double search_shape(const lora_linear* h, const Plan& plan, int cs, int tn, int k_split, int* out_cs, int* out_tn,
+                    bool wide = false) {
     const int nf = (int)plan.fused.size();
     const int shrink_n = ceil_div(h->rank, 16) * 16;
     const bool small_batch = (long long)nf * kTileM <= 384;
@@ -461,36 +483,59 @@ double search_shape(const lora_linear* h, const Plan& plan, int cs, int tn, int 
             if (best < 0 || m < best) { best = m; best_cs = c; best_tn = t; }
             continue;
         }
-        for (int t = kMaxTileN; t >= 128; t -= 16) {
-            if (tn && t != tn) continue;
-            const double m = makespan(h, fg, sg, c, t, shrink_n, slots, k_split);
-            if (best < 0 || m < best * 0.999) { best = m; best_cs = c; best_tn = t; }
+        if (tn) {
+            const double m = makespan(h, fg, sg, c, tn, shrink_n, slots, k_split);
+            if (best < 0 || m < best * 0.999) { best = m; best_cs = c; best_tn = tn; }
+            continue;
         }
+        // 256 columns, then (SM pairs) the wide tiles, then the narrower ones
+        double wide_best = -1;
+        int wide_tn = kMaxTileN;
+        for (int t = kMaxTileN; t <= (c == 2 && wide ? kMaxAutoWideTileN : kMaxTileN); t += 16) {
+            if (t > kMaxTileN && t < kMinAutoWideTileN) continue;
+            const double m = makespan(h, fg, sg, c, t, shrink_n, slots, k_split);
+            if (wide_best < 0 || m < wide_best * 0.999) { wide_best = m; wide_tn = t; }
+        }
+        double c_best = wide_best;
+        int c_tn = wide_tn;
+        const double bar = c == 2 ? (1.0 - kNarrowPairMargin) * wide_best : wide_best;
+        for (int t = kMaxTileN - 16; t >= 128; t -= 16) {
+            const double m = makespan(h, fg, sg, c, t, shrink_n, slots, k_split);
+            if (m < bar && m < c_best * 0.999) { c_best = m; c_tn = t; }
+        }
+        if (best < 0 || c_best < best * 0.999) { best = c_best; best_cs = c; best_tn = c_tn; }
     }
     *out_cs = best_cs;
     *out_tn = best_tn;
     return best;
 }
 
-Shape choose_shape(lora_linear* h, const Plan& plan, bool allow_yt = true) {
+Shape choose_shape(lora_linear* h, const Plan& plan, bool bf16 = true) {
     Shape sh;
     const int nf = (int)plan.fused.size();
     sh.shrink_n = ceil_div(h->rank, 16) * 16;
     sh.bk = h->tile_k ? h->tile_k : 64;
     const bool small_batch = (long long)nf * kTileM <= 384;
     int cs = h->cluster, tn = h->force_tile_n;
+    // wide row tiles (past 256 columns) run on SM pairs of the bf16 kernel with whole K per unit
+    if (tn > kMaxTileN) {
+        if (!bf16 || cs == 1 || h->k_split > 1 || (h->tile_k && h->tile_k != kTileK)) tn = kMaxTileN;
+        else cs = 2;
+    }
     // K halves: whole 256-column blocks (narrower ones gained nothing where halves were measured)
     if (h->k_split > 1 && !small_batch && !tn) tn = kMaxTileN;
-    const bool yt_ok = allow_yt && yt_allowed(h, plan);
+    const bool yt_ok = bf16 && yt_allowed(h, plan);
     int yt = 0;
     if (!cs || !tn || yt_ok) {
         const int cs0 = cs, tn0 = tn;
         if (small_batch && !cs) cs = 1;
-        // plan signature: tile count and each tile's adapter / row count
+        // plan signature: tile count and each tile's adapter / row count, then the options that
+        // fix or restrict the choice, each mixed in on its own
         uint64_t key = 1469598103934665603ull ^ (uint64_t)nf;
         for (const Tile& t : plan.fused) key = (key ^ (uint64_t)(t.adapter * 131 + t.nrows)) * 1099511628211ull;
-        key ^= ((uint64_t)cs << 56) ^ ((uint64_t)tn << 40) ^ ((uint64_t)h->k_split << 32) ^
-               ((uint64_t)(yt_ok ? 1 + h->yt_mode : 0) << 48);
+        for (const int v : {cs, tn, h->k_split, yt_ok ? 1 + h->yt_mode : 0, h->wide_mode, h->tile_k, h->max_ctas,
+                            bf16 ? 1 : 0})
+            key = (key ^ (uint64_t)(uint32_t)v) * 1099511628211ull;
         auto it = h->shape_cache.find(key);
         if (it != h->shape_cache.end()) {
             yt = (int)(it->second >> 31);
@@ -498,7 +543,9 @@ Shape choose_shape(lora_linear* h, const Plan& plan, bool allow_yt = true) {
             tn = (int)(it->second & 0xFFFF);
         } else {
             double m = 0.0;
-            if (!cs || !tn) m = search_shape(h, plan, cs, tn, h->k_split, &cs, &tn);
+            // wide row tiles: bf16 base, whole K, 64-wide K-steps
+            const bool wide = bf16 && h->wide_mode != 1 && h->k_split <= 1 && (!h->tile_k || h->tile_k == kTileK);
+            if (!cs || !tn) m = search_shape(h, plan, cs, tn, h->k_split, &cs, &tn, wide);
             if (yt_ok) {
                 // token-column units when asked for, or, for batches of more than one row tile,
                 // when the calibrated models expect them to finish sooner
@@ -882,7 +929,7 @@ int lora_linear_set_option(lora_linear* h, int option, long long value) {
     if (!h) return LORA_EINVAL;
     switch (option) {
         case LORA_OPT_TILE_N:
-            if (value != 0 && (value < 16 || value > kMaxTileN || value % 16)) return LORA_EINVAL;
+            if (value != 0 && (value < 16 || value > kMaxWideTileN || value % 16)) return LORA_EINVAL;
             h->force_tile_n = (int)value;
             return LORA_OK;
         case LORA_OPT_WAIT_LIMIT_US:
@@ -937,6 +984,10 @@ int lora_linear_set_option(lora_linear* h, int option, long long value) {
         case LORA_OPT_TOKEN_COLUMNS:
             if (value < 0 || value > 2) return LORA_EINVAL;
             h->yt_mode = (int)value;
+            return LORA_OK;
+        case LORA_OPT_WIDE_TILES:
+            if (value < 0 || value > 1) return LORA_EINVAL;
+            h->wide_mode = (int)value;
             return LORA_OK;
         case LORA_OPT_W4_K_SPLIT: {
             if (value < 0 || value > 4) return LORA_EINVAL;

@@ -42,14 +42,22 @@
 // both CTAs' stages and accumulators (multicast); both epilogues release the even CTA's
 // accumulator barrier.
 //
-// Token-column units (YT, an instantiation of their own, SM pairs): for batches of at most 512
-// rows on one adapter, a unit computes a block of Y^T instead: 256 output features (W rows as the
-// A operand, 128 per CTA) for every token row of the batch (X rows as the B operand, half of them
-// per CTA), so W is read once and no row tile is padded. Past 128 token rows per CTA each 16-wide
-// K step takes a second MMA over the remaining rows, issued by warp 6 beside warp 1's first (one
-// warp waits ~80 cycles between MMAs whatever their width). The epilogue maps accumulator
-// columns back to token rows through a per-warp shared-memory buffer. The sums keep their order,
-// so the bits equal those of row tiles.
+// Two unit forms wider than one MMA (SM pairs, 224 threads, each an instantiation of its own, so
+// that neither changes the code of the others): each 16-wide K step takes a second MMA over the B
+// stage rows past the first MMA's, issued by warp 6 beside warp 1's first (one warp waits ~80
+// cycles between MMAs whatever their width), into the accumulator columns after the first MMA's;
+// one accumulator of up to 512 columns, so a unit's epilogue no longer overlaps the next unit's
+// MMAs.
+//   token-column units (FORM 1, p.yt): for batches of at most 512 rows on one adapter, a unit computes a
+//     block of Y^T: 256 output features (W rows as the A operand, 128 per CTA) for every token row
+//     of the batch (X rows as the B operand, half of them per CTA), so W is read once and no row
+//     tile is padded; the epilogue maps accumulator columns back to token rows through a per-warp
+//     shared-memory buffer;
+//   wide row tiles (FORM 2, tile_n of 272 to 512 columns): 256-row units as on SM pairs, with more output
+//     columns per unit, so that a projection's units fill whole waves of SM pairs (2,048 rows of
+//     a 5,120-column projection: 152 units of 272 columns, two waves, instead of 160 of 256).
+// The sums keep their order whatever the unit's shape, so the bits equal those of 256-column
+// row tiles.
 //
 // Every mbarrier wait is bounded by a wall-clock limit; a wait that runs out sets bit 0
 // of the status word and a CTA-wide abort flag, and all roles leave their loops, wait
@@ -177,10 +185,12 @@ __device__ __forceinline__ Unit decode_unit(const GemmParams& p, const WorkList&
     return r;
 }
 
-// Token row of accumulator column c of a token-column unit: the first MMA's columns [0, 2 h)
-// hold stage rows [0, h) of the even CTA (tokens 0 ..) then of the odd CTA (tokens rows ..); the
-// second MMA's columns hold stage rows [h, rows) of the even CTA, then of the odd CTA.
-__device__ __forceinline__ int yt_token(int c, int h, int rows) {
+// Row of the pair's B stages (the even CTA's `rows` rows, then the odd CTA's) that accumulator
+// column c of a two-MMA unit multiplies: the first MMA's columns [0, 2 h) hold stage rows [0, h)
+// of the even CTA, then of the odd CTA; the second MMA's columns hold stage rows [h, rows) of the
+// even CTA, then of the odd CTA. It is the token row of a token-column unit and the output
+// column (from the unit's first) of a wide row tile.
+__device__ __forceinline__ int pair_b_row(int c, int h, int rows) {
     if (c < 2 * h) return c < h ? c : rows + c - h;
     const int cc = c - 2 * h, h1 = rows - h;
     return cc < h1 ? h + cc : rows + h + cc - h1;
@@ -209,7 +219,7 @@ __device__ __forceinline__ void yt_store(const GemmParams& p, uint32_t taddr, in
         for (int i = 0; i < 4; ++i) {
             const int k = lane + 32 * i;      // 16-byte piece k: token column k / 4, features 8 (k % 4) ..
             const int tc = k >> 2, seg = k & 3;
-            const int tok = yt_token(c + tc, h, rows);
+            const int tok = pair_b_row(c + tc, h, rows);
             const int f = f0 + 8 * seg;
             if (tc < m && tok < T && f < p.d_out) {
                 const uint4 val = *reinterpret_cast<const uint4*>(stage + (size_t)k * 16);
@@ -219,10 +229,13 @@ __device__ __forceinline__ void yt_store(const GemmParams& p, uint32_t taddr, in
     }
 }
 
-template <int BK, int CG, bool YT>
-__global__ void __launch_bounds__(YT ? kThreadsYt : kThreads, 1)
+// FORM: kFormRows (row tiles), kFormTokenColumns, kFormWideRows (see the file header).
+template <int BK, int CG, int FORM>
+__global__ void __launch_bounds__(FORM != kFormRows ? kThreadsWide : kThreads, 1)
     lora_gemm_kernel(const __grid_constant__ GemmParams p) {
-    static_assert(!YT || (CG == 2 && BK == 64), "token-column units run on SM pairs with 64-wide K-steps");
+    constexpr bool YT = FORM == kFormTokenColumns;   // token-column units
+    constexpr bool WIDE = FORM != kFormRows;         // two MMAs per K16 step, two MMA warps
+    static_assert(!WIDE || (CG == 2 && BK == 64), "two-MMA units run on SM pairs with 64-wide K-steps");
     // A stage: the tile's rows of X (or U) for this K-step; a batch of one short tile loads
     // only its rows (a_rows < 128), and the MMA's remaining A rows read unrelated shared memory
     // whose output rows are never stored
@@ -235,8 +248,8 @@ __global__ void __launch_bounds__(YT ? kThreadsYt : kThreads, 1)
     // this CTA's B rows per stage: output-tile rows of W, rows of A_a, or token rows
     const int b_rows = YT ? max(p.yt_rows, p.shrink_n / CG) : (p.tile_n > p.shrink_n ? p.tile_n : p.shrink_n) / CG;
     const uint32_t b_stage_bytes = (uint32_t)b_rows * BK * 2;
-    // token-column units wider than one accumulator take all of TMEM: one accumulator at a time
-    const int n_acc = (YT && 2 * p.yt_rows > kAccCols) ? 1 : 2;
+    // units wider than one accumulator take all of TMEM: one accumulator at a time
+    const int n_acc = (WIDE && (YT ? 2 * p.yt_rows : p.tile_n) > kAccCols) ? 1 : 2;
     uint8_t* a_ring = base;
     uint8_t* b_ring = a_ring + (size_t)stages * kStageA;
     // token-column units: the epilogue warps' transposing buffers (2 KB each) follow the rings
@@ -257,8 +270,8 @@ __global__ void __launch_bounds__(YT ? kThreadsYt : kThreads, 1)
     const int group = (int)blockIdx.x / CG;        // cluster index
     const int n_groups = (int)gridDim.x / CG;
 
-    // token-column units: two MMA warps (1 and 6) commit every stage, accumulator and drain
-    constexpr uint32_t kIssuers = YT ? 2 : 1;
+    // two-MMA units: two MMA warps (1 and 6) commit every stage, accumulator and drain
+    constexpr uint32_t kIssuers = WIDE ? 2 : 1;
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
             mbar_init(smem_addr(&full[s]), 1);
@@ -418,15 +431,15 @@ __global__ void __launch_bounds__(YT ? kThreadsYt : kThreads, 1)
                 }
             }
         }
-    } else if (warp == 1 || (YT && warp == 6)) {
+    } else if (warp == 1 || (WIDE && warp == 6)) {
         // ------------------------------------------------------------ MMA issuer (even CTA)
-        // The whole warp runs the loop (converged); lane 0 issues the MMAs and commits. With
-        // token-column units warp 6 issues each K16 step's second MMA (the stage rows past the
-        // first yt_h) beside warp 1's first: one warp waits ~80 cycles between MMAs whatever their
+        // The whole warp runs the loop (converged); lane 0 issues the MMAs and commits. In the
+        // two-MMA instantiations warp 6 issues each K16 step's second MMA (the B stage rows past the
+        // first MMA's) beside warp 1's first: one warp waits ~80 cycles between MMAs whatever their
         // width, two warps keep the tensor pipe fed with both. Both commit every stage and
         // accumulator (the barriers count two arrivals).
         const uint32_t issuer = lane == 0 ? 1u : 0u;
-        const bool second = YT && warp == 6;
+        const bool second = WIDE && warp == 6;
         if (p.pdl) griddep_wait();
         if (leader) {
             int stage = 0;
@@ -435,12 +448,24 @@ __global__ void __launch_bounds__(YT ? kThreadsYt : kThreads, 1)
             bool ok = true;
             for (int u = group; u < n_units && ok; u += n_groups, ++it) {
                 const Unit w = decode_unit<YT>(p, wl, u, rank);
-                const uint32_t idesc = instr_desc_bf16(kTileM * CG, w.n);
-                // token-column units past 128 token rows per CTA: a second MMA per 16-wide K-step
-                // over the stage's remaining token rows, into the accumulator columns after the first's
-                const bool mma2 = YT && !w.shrink && p.yt_rows > p.yt_h;
-                const uint32_t idesc2 = instr_desc_bf16(kTileM * CG, 2 * (p.yt_rows - p.yt_h));
-                const uint64_t b_off2 = (uint64_t)((p.yt_h * BK * 2) >> 4);
+                // two-MMA units: the first MMA takes B stage rows [0, r1) of each CTA (N = n1), a
+                // second, when n2 > 0, the rest (N = n2) into the accumulator columns after the
+                // first's: token-column units past yt_h token rows per CTA, row tiles past 256 columns
+                int n1 = w.n, n2 = 0, r1 = 0;
+                if (WIDE && !w.shrink) {
+                    if (YT) {
+                        n2 = 2 * (p.yt_rows - p.yt_h);
+                        r1 = p.yt_h;
+                    } else if (w.n > kAccCols) {
+                        n1 = kAccCols;
+                        n2 = w.n - kAccCols;
+                        r1 = kAccCols / CG;
+                    }
+                }
+                const uint32_t idesc = instr_desc_bf16(kTileM * CG, n1);
+                const bool mma2 = n2 > 0;
+                const uint32_t idesc2 = instr_desc_bf16(kTileM * CG, mma2 ? n2 : 16);
+                const uint64_t b_off2 = (uint64_t)((r1 * BK * 2) >> 4);
                 const int acc = it % n_acc;
                 if (!wait_warp(smem_addr(&tempty[acc]), ((it / n_acc) & 1) ^ 1, abort_flag, p.status, limit)) {
                     ok = false;
@@ -477,8 +502,8 @@ __global__ void __launch_bounds__(YT ? kThreadsYt : kThreads, 1)
                         } else if (mma2) {
 #pragma unroll
                             for (int k = 0; k < BK / 16; ++k) {
-                                // the stage rows past the first yt_h (whole 1024-byte swizzle atoms)
-                                mma_bf16<CG>(d + (uint32_t)w.n, ad + (uint64_t)(2 * k),
+                                // the stage rows past the first r1 (whole 1024-byte swizzle atoms)
+                                mma_bf16<CG>(d + (uint32_t)n1, ad + (uint64_t)(2 * k),
                                              bd + b_off2 + (uint64_t)(2 * k), idesc2,
                                              (kb + j > 0 || k > 0) ? 1u : 0u, issuer);
                             }
@@ -565,6 +590,7 @@ __global__ void __launch_bounds__(YT ? kThreadsYt : kThreads, 1)
                 // part_base[(q * part_chunks + j) * part_rows]
                 const size_t part_stride = (size_t)p.part_chunks * p.part_rows;    // one part's slot
                 float4* part = split ? p.partials + (size_t)w.pchunk * p.part_rows + row : nullptr;
+                const bool wide_tile = FORM == kFormWideRows && !w.shrink && w.n > kAccCols;
                 for (int c = 0; c < w.n; c += 32) {
                     uint32_t v[32];
                     const bool two = c + 16 < w.n;  // w.n is a multiple of 16
@@ -615,7 +641,10 @@ __global__ void __launch_bounds__(YT ? kThreadsYt : kThreads, 1)
                     if (row_ok && !first) {
 #pragma unroll
                         for (int h = 0; h < 4; ++h) {
-                            if ((h < 2 || two) && c + 8 * h < n_out) {
+                            // a wide row tile's accumulator columns follow its B stage rows
+                            // (boundaries at multiples of 8 columns)
+                            const int col = wide_tile ? pair_b_row(c + 8 * h, kAccCols / CG, w.n / CG) : c + 8 * h;
+                            if ((h < 2 || two) && col < n_out) {
                                 uint4 o;
                                 o.x = pack_bf16x2(__uint_as_float(v[8 * h + 0]) * scale,
                                                   __uint_as_float(v[8 * h + 1]) * scale);
@@ -625,7 +654,7 @@ __global__ void __launch_bounds__(YT ? kThreadsYt : kThreads, 1)
                                                   __uint_as_float(v[8 * h + 5]) * scale);
                                 o.w = pack_bf16x2(__uint_as_float(v[8 * h + 6]) * scale,
                                                   __uint_as_float(v[8 * h + 7]) * scale);
-                                *reinterpret_cast<uint4*>(out + c + 8 * h) = o;
+                                *reinterpret_cast<uint4*>(out + col) = o;
                             }
                         }
                     }
@@ -725,9 +754,9 @@ size_t gemm_smem_bytes(int b_tile_rows, int stages, int bk, int a_rows, int yt) 
            (yt ? (size_t)kYtStageBytes : 0) + 8 * (2 * (size_t)stages + 5) + 16;
 }
 
-template <int BK, int CG, bool YT = false>
+template <int BK, int CG, int FORM = kFormRows>
 static cudaError_t set_smem_attr() {
-    return cudaFuncSetAttribute(dev::lora_gemm_kernel<BK, CG, YT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    return cudaFuncSetAttribute(dev::lora_gemm_kernel<BK, CG, FORM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 kSmemLimit);
 }
 
@@ -735,7 +764,8 @@ cudaError_t gemm_prepare_device() {
     cudaError_t e;
     if ((e = set_smem_attr<64, 1>()) != cudaSuccess) return e;
     if ((e = set_smem_attr<64, 2>()) != cudaSuccess) return e;
-    if ((e = set_smem_attr<64, 2, true>()) != cudaSuccess) return e;
+    if ((e = set_smem_attr<64, 2, kFormTokenColumns>()) != cudaSuccess) return e;
+    if ((e = set_smem_attr<64, 2, kFormWideRows>()) != cudaSuccess) return e;
     if ((e = set_smem_attr<32, 1>()) != cudaSuccess) return e;
     return set_smem_attr<32, 2>();
 }
@@ -752,6 +782,11 @@ static bool cooperative_launches() {
     return on;
 }
 
+// Launches of a two-MMA instantiation: token-column units and row tiles wider than 256 columns.
+bool gemm_wide(const GemmParams& p) {
+    return p.yt || p.tile_n > kAccCols;
+}
+
 int gemm_b_rows(const GemmParams& p) {
     if (p.yt) return p.yt_rows > p.shrink_n / p.cluster_size ? p.yt_rows : p.shrink_n / p.cluster_size;
     return (p.tile_n > p.shrink_n ? p.tile_n : p.shrink_n) / p.cluster_size;
@@ -762,7 +797,7 @@ static void launch_config(const GemmParams& p, int grid, cudaStream_t stream, cu
     const int b_rows = gemm_b_rows(p);
     *cfg = cudaLaunchConfig_t{};
     cfg->gridDim = dim3(grid, 1, 1);
-    cfg->blockDim = dim3(p.yt ? kThreadsYt : kThreads, 1, 1);
+    cfg->blockDim = dim3(gemm_wide(p) ? kThreadsWide : kThreads, 1, 1);
     cfg->dynamicSmemBytes = gemm_smem_bytes(b_rows, p.stages, p.bk, p.a_rows ? p.a_rows : kTileM, p.yt);
     cfg->stream = stream;
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -789,17 +824,23 @@ static void launch_config(const GemmParams& p, int grid, cudaStream_t stream, cu
 
 template <typename F>
 static cudaError_t dispatch(const GemmParams& p, F&& f) {
-    if (p.yt) return p.bk == 64 && p.cluster_size == 2 ? f(dev::lora_gemm_kernel<64, 2, true>) : cudaErrorInvalidValue;
-    if (p.bk == 64 && p.cluster_size == 1) return f(dev::lora_gemm_kernel<64, 1, false>);
-    if (p.bk == 64 && p.cluster_size == 2) return f(dev::lora_gemm_kernel<64, 2, false>);
-    if (p.bk == 32 && p.cluster_size == 1) return f(dev::lora_gemm_kernel<32, 1, false>);
-    if (p.bk == 32 && p.cluster_size == 2) return f(dev::lora_gemm_kernel<32, 2, false>);
+    const bool pair64 = p.bk == 64 && p.cluster_size == 2;
+    if (p.yt) return pair64 ? f(dev::lora_gemm_kernel<64, 2, kFormTokenColumns>) : cudaErrorInvalidValue;
+    if (p.tile_n > kAccCols) return pair64 ? f(dev::lora_gemm_kernel<64, 2, kFormWideRows>) : cudaErrorInvalidValue;
+    if (p.bk == 64 && p.cluster_size == 1) return f(dev::lora_gemm_kernel<64, 1, kFormRows>);
+    if (pair64) return f(dev::lora_gemm_kernel<64, 2, kFormRows>);
+    if (p.bk == 32 && p.cluster_size == 1) return f(dev::lora_gemm_kernel<32, 1, kFormRows>);
+    if (p.bk == 32 && p.cluster_size == 2) return f(dev::lora_gemm_kernel<32, 2, kFormRows>);
     return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t stream) {
     // rank tiles only in a launch of shrink units alone, without ready flags or K parts
     if (p.shrink_ntiles > 1 && (p.n_fused || p.flags || p.k_split > 1 || p.shrink_n < 16 || (p.shrink_n & 15)))
+        return cudaErrorInvalidValue;
+    // wide row tiles: whole K per unit, a multiple of 16 columns, at most two 256-column MMAs
+    if (!p.yt && p.tile_n > kAccCols &&
+        (p.k_split > 1 || p.tile_n > kMaxWideTileN || (p.tile_n & 15) || (p.a_rows && p.a_rows != kTileM)))
         return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[3];

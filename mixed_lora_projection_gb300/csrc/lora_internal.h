@@ -12,12 +12,16 @@ namespace lora {
 constexpr int kTileM = 128;          // rows per tile = tcgen05 M (cta_group::1)
 constexpr int kTileK = 64;           // default K per pipeline stage: one 128-byte swizzle row of bf16
 constexpr int kMaxTileN = 256;       // widest output tile = one TMEM accumulator (256 fp32 columns)
+constexpr int kMaxWideTileN = 512;   // widest row tile of the two-MMA instantiation (one 512-column accumulator)
 constexpr int kAccCols = 256;        // TMEM columns per accumulator; two accumulators per CTA
 constexpr int kStageBytesA = kTileM * kTileK * 2;      // 16 KB at K = 64
 constexpr int kMaxStages = 16;
 constexpr int kSmemLimit = 232448;                     // opt-in dynamic shared memory per CTA (227 KB)
 constexpr int kThreads = 192;        // warp 0 TMA, warp 1 MMA + TMEM owner, warps 2..5 epilogue
-constexpr int kThreadsYt = 224;      // token-column units: warp 6 issues the second MMA of each K16 step
+constexpr int kThreadsWide = 224;    // two-MMA units: warp 6 issues the second MMA of each K16 step
+// Unit forms of the bf16 kernel, one instantiation each: row tiles (up to 256 output columns),
+// token-column units (blocks of Y^T), wide row tiles (272 to 512 output columns, SM pairs)
+constexpr int kFormRows = 0, kFormTokenColumns = 1, kFormWideRows = 2;
 constexpr int kYtStageBytes = 4 * 32 * 32 * 2;  // token-column epilogue: 32 tokens x 32 features bf16 per warp
 constexpr int kEpilogueThreads = 128;
 constexpr int kW4Group = 128;        // input features per scale of a 4-bit base
@@ -82,7 +86,9 @@ struct GemmParams {
     int n_shrink;                    // shrink groups (tiles = cluster_size x groups)
     int n_fused;                     // fused row groups
     int n_ntiles;                    // output-column tiles of the fused units
-    int tile_n;                      // fused output-tile width (multiple of 16, <= 256)
+    int tile_n;                      // fused output-tile width (multiple of 16, <= 256; on SM pairs with
+                                     // whole K per unit up to 512: wide row tiles, whose 16-wide K
+                                     // steps take a second MMA over the B rows past 128 per CTA)
     int shrink_n;                    // shrink output-tile width = rank rounded up to 16
     int stages;
     int m_fastest;                   // 1: row tiles first, 0: column tiles first, 2: column-tile groups
@@ -163,6 +169,7 @@ cudaError_t gemm_prepare_device();           // sets the opt-in smem limit on th
 cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t stream);
 int gemm_max_clusters(const GemmParams& p);  // co-resident clusters of this launch shape
 int gemm_b_rows(const GemmParams& p);        // B rows of one CTA's pipeline stage
+bool gemm_wide(const GemmParams& p);         // the launch runs the two-MMA instantiation
 cudaError_t w4_repack(const void* src, void* dst, long long n_words, int grid, cudaStream_t stream);
 
 }  // namespace lora

@@ -169,8 +169,8 @@ def test_create_without_a_gpu_reports_no_device(lib):
 SHAPES = {
     "prefill_16k": (2, 256, 2), "prefill_32k": (2, 256, 2), "mixed_batch": (2, 256, 1),
     "mixed_8x300": (2, 256, 1), "prefix_tail_1552": (2, 256, 1), "mixed_decode": (1, 240, None),
-    "mixed_near_ridge": (2, 256, 3), "sweep_qkv": (2, 224, None), "sweep_o": (2, 192, None),
-    "sweep_gate_up": (2, 256, None), "sweep_down": (2, 192, None),
+    "mixed_near_ridge": (2, 256, 3), "sweep_qkv": (2, 224, None), "sweep_o": (2, 288, None),
+    "sweep_gate_up": (2, 256, None), "sweep_down": (2, 288, None),
 }
 # K halves chosen by a handle of max_tokens = the workload's rows: none of the configured
 # workloads (their batches are past the small-batch path, or their K is 5,120)
