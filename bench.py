@@ -198,10 +198,12 @@ def _l2_note(items, n_copies, w4=False):
     return f"X ({xb / 1e6:.1f} MB) fits in L2; {wdesc}, larger than L2 together"
 
 
-def _rooflines(items, w4, fused_flops, avg_fused_ms, traffic, peak_burst, hbm, src, shrink_n):
+def _rooflines(items, w4, fused_flops, avg_fused_ms, traffic, peak_burst, hbm, src, shrink_n, peak_sust=None):
     """(binding roof, other roof) of the timed kernel: the tensor roof (algorithmic FLOPs against
     the measured bf16 burst) and the HBM roof (algorithmic bytes against the measured copy
-    bandwidth); the one that takes longer at its peak binds."""
+    bandwidth); the one that takes longer at its peak binds. The tensor roof also gives the
+    fraction of the measured sustained bf16 rate (cuBLAS back to back for seconds, at the power
+    limit), the figure for lines whose timed region runs long enough to reach that limit."""
     alg = sum(_alg_bytes(w, w4) for w, _, _ in items)
     kernel = ("lora_w4_kernel (4-bit base + expand; shrink on lora_gemm_kernel before it)" if w4
               else "lora_gemm_kernel (shrink + base + expand, one launch per call)" if not shrink_n
@@ -212,6 +214,9 @@ def _rooflines(items, w4, fused_flops, avg_fused_ms, traffic, peak_burst, hbm, s
               "unit": "TFLOP/s", "frac": round(achieved_tf / peak_burst, 4) if achieved_tf else None,
               "traffic": traffic, "peak_source": f"{src} bf16 burst", "kernel": kernel,
               "algorithmic_flops_per_step": fused_flops}
+    if peak_sust:
+        tensor["peak_sustained"] = peak_sust
+        tensor["frac_of_sustained"] = round(achieved_tf / peak_sust, 4) if achieved_tf else None
     mem = {"bound": "hbm", "achieved": round(achieved_gbs, 1) if achieved_gbs else None, "peak": hbm,
            "unit": "GB/s", "frac": round(achieved_gbs / hbm, 4) if achieved_gbs else None, "traffic": traffic,
            "peak_source": f"{src} copy bandwidth", "kernel": kernel, "algorithmic_bytes_per_step": alg}
@@ -463,7 +468,8 @@ def run_ours(args, rank, world, dist):
     achieved = fused_flops / (avg_fused_ms * 1e-3) / 1e12 if avg_fused_ms else None
     traffic = _profiled_traffic(args.workload + ("+w4" if args.w4 else ""))
     w0 = items[0][0]
-    roof, roof_other = _rooflines(items, args.w4, fused_flops, avg_fused_ms, traffic, peak_burst, hbm, src, shrink_n)
+    roof, roof_other = _rooflines(items, args.w4, fused_flops, avg_fused_ms, traffic, peak_burst, hbm, src, shrink_n,
+                                  peak_sust)
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
