@@ -350,12 +350,18 @@ int max_clusters(lora_linear* h, const GemmParams& p) {
 // columns past 256, which costs ~50-90 cycles whatever its width (the tensor pipe's floor per
 // instruction), and hold all of TMEM in one accumulator: measured per unit against a 256-column
 // unit on 2,048-row projections, 1.31x (down, 17,408 -> 5,120) to 1.51x (o, 6,144 -> 5,120) for
-// 12-25% more columns. They pay where they take a wave off a projection whose units do not fill
-// their last wave (down at 2,048 rows: 160 units of 256 columns on 76 SM pairs, 3 waves; 149 of
-// 288, 2 waves: 271 -> 237 us). kWideKstepFactor is the per-K-step cost against a 256-column
-// unit that reproduces the measured choices (down and o: 288; qkv, gate_up, the prefills: not).
+// 12-25% more columns. They pay where they take a wave off a projection whose 256-column units
+// leave the last wave of SM pairs at most half full (down at 2,048 rows: 160 units of 256 columns
+// on 76 SM pairs, 3 waves, the last 17% full; 149 of 288, 2 waves: 271 -> 237 us; at 1,024 rows
+// o and down 0.71x and 0.75x of the narrow tiles chosen before; o at 2,176 rows 0.92x), and are
+// weighed only there: with the last wave 68% full (o, 3,456 rows) the model would expect 1% from
+// them, o's measured 1.51x loses it. kWideKstepFactor is the per-K-step cost against a 256-column
+// unit that reproduces the measured choices. Relative to the unit, the second MMA and the exposed
+// epilogue cost more the shorter its K: on projections of 80 K-steps (d_in 5,120) wide units took
+// 1.37-1.49x (qkv at 336 columns 177 against 172 us at 224; gate_up at 288-512 columns 490-555
+// against 431 us at 256), so they are weighed only from kMinWideKSteps K-steps on.
 constexpr double kWideKstepFactor = 1.32;
-constexpr int kMinAutoWideTileN = 288, kMaxAutoWideTileN = 320;
+constexpr int kMinAutoWideTileN = 288, kMaxAutoWideTileN = 320, kMinWideKSteps = 96;
 
 double kstep_cycles(int cs, int n) {
     if (cs > 1 && n > kMaxTileN) return kWideKstepFactor * kstep_cycles(2, kMaxTileN);
@@ -452,13 +458,6 @@ double yt_makespan(const lora_linear* h, const Plan& plan, int slots) {
     return *std::max_element(load.begin(), load.end());
 }
 
-// On SM pairs a tile narrower than 256 columns replaces the best 256-column or wide one only when
-// the model expects it at least this much sooner: narrow pair tiles measured slower than the model
-// expects on 2,048-row projections (o: 192 columns 103.8 us against 95.5 us for 256, where the
-// model expected 192 to finish 10% sooner), while where they win the model expects more (qkv:
-// 224 columns, 7% expected, 3-7% measured).
-constexpr double kNarrowPairMargin = 0.05;
-
 // The launch shape (SM pair or single CTA, output-tile width) the makespan model expects to
 // finish a plan soonest with K in `k_split` parts; cs / tn nonzero fix that choice; `wide` lets SM
 // pairs weigh wide row tiles. Returns the expected makespan.
@@ -488,22 +487,20 @@ double search_shape(const lora_linear* h, const Plan& plan, int cs, int tn, int 
             if (best < 0 || m < best * 0.999) { best = m; best_cs = c; best_tn = tn; }
             continue;
         }
-        // 256 columns, then (SM pairs) the wide tiles, then the narrower ones
-        double wide_best = -1;
-        int wide_tn = kMaxTileN;
-        for (int t = kMaxTileN; t <= (c == 2 && wide ? kMaxAutoWideTileN : kMaxTileN); t += 16) {
+        // 256 columns, then (SM pairs) the wide tiles, then the narrower ones; a tie goes to the
+        // earlier. Wide tiles are weighed where 256-column units leave the last wave of SM pairs at
+        // most half full (their gains were measured there: 2,048 rows of o and down 17%, 1,024
+        // rows 8%, 2,176 rows of o 43%)
+        const long long u256 = (long long)(fg.size() / c) * ceil_div(h->d_out, kMaxTileN) + (long long)(sg.size() / c);
+        const double last = (double)(u256 % slots) / slots;
+        const bool wide_here = c == 2 && wide && last > 0.0 && last <= 0.5;
+        const int t_max = wide_here ? kMaxAutoWideTileN : kMaxTileN;
+        for (int i = 0; i <= (t_max - kMaxTileN) / 16 + (kMaxTileN - 128) / 16; ++i) {
+            const int t = i <= (t_max - kMaxTileN) / 16 ? kMaxTileN + 16 * i : kMaxTileN - 16 * (i - (t_max - kMaxTileN) / 16);
             if (t > kMaxTileN && t < kMinAutoWideTileN) continue;
             const double m = makespan(h, fg, sg, c, t, shrink_n, slots, k_split);
-            if (wide_best < 0 || m < wide_best * 0.999) { wide_best = m; wide_tn = t; }
+            if (best < 0 || m < best * 0.999) { best = m; best_cs = c; best_tn = t; }
         }
-        double c_best = wide_best;
-        int c_tn = wide_tn;
-        const double bar = c == 2 ? (1.0 - kNarrowPairMargin) * wide_best : wide_best;
-        for (int t = kMaxTileN - 16; t >= 128; t -= 16) {
-            const double m = makespan(h, fg, sg, c, t, shrink_n, slots, k_split);
-            if (m < bar && m < c_best * 0.999) { c_best = m; c_tn = t; }
-        }
-        if (best < 0 || c_best < best * 0.999) { best = c_best; best_cs = c; best_tn = c_tn; }
     }
     *out_cs = best_cs;
     *out_tn = best_tn;
@@ -543,8 +540,9 @@ Shape choose_shape(lora_linear* h, const Plan& plan, bool bf16 = true) {
             tn = (int)(it->second & 0xFFFF);
         } else {
             double m = 0.0;
-            // wide row tiles: bf16 base, whole K, 64-wide K-steps
-            const bool wide = bf16 && h->wide_mode != 1 && h->k_split <= 1 && (!h->tile_k || h->tile_k == kTileK);
+            // wide row tiles: bf16 base, whole K of at least kMinWideKSteps 64-wide K-steps
+            const bool wide = bf16 && h->wide_mode != 1 && h->k_split <= 1 && (!h->tile_k || h->tile_k == kTileK) &&
+                              ceil_div(h->d_in, kTileK) >= kMinWideKSteps;
             if (!cs || !tn) m = search_shape(h, plan, cs, tn, h->k_split, &cs, &tn, wide);
             if (yt_ok) {
                 // token-column units when asked for, or, for batches of more than one row tile,

@@ -260,6 +260,31 @@ def test_token_column_rule(lib):
     assert order(5120, 12288, 400, (0, 400), (0,)) == 3 and order(5120, 12288, 448, (0, 48, 448), (0, 1)) == 3
 
 
+def test_wide_tile_rule(lib):
+    from mixed_lora_projection_gb300 import launch_shape
+
+    def shape(d_in, d_out, T, off, ids):
+        s = launch_shape(d_in, d_out, 256, 152, T, off, ids)
+        return s["cluster"], s["tile_n"]
+    # o and down (K of 96 and 272 steps of 64) with half their rows on an adapter, where 256-column
+    # units leave the last wave of 76 SM pairs at most half full, take wide row tiles (the shapes
+    # measured): 1,024 rows (80 units + shrink, 8% of a second wave), 2,048 rows (17% of a third)
+    # -> 288 columns; 2,176 rows (43%) -> 320; 1,024 rows also without adapter rows or all on one
+    for d_in in (6144, 17408):
+        for T, tn in ((1024, 288), (2048, 288), (2176, 320)):
+            assert shape(d_in, 5120, T, (0, T // 2, T), (0, 1)) == (2, tn), (d_in, T)
+        for off, ids in (((0, 1024), (0,)), ((0, 1024), (1,))):
+            assert shape(d_in, 5120, 1024, off, ids) == (2, 288), (d_in, ids)
+    # not: a last wave more than half full (3,456 base rows: 68%), K of 80 steps (qkv, gate_up,
+    # the 16k prefill's 5,120 -> 5,120), decode-sized batches (single CTAs)
+    for d_in in (6144, 17408):
+        assert shape(d_in, 5120, 3456, (0, 3456), (0,))[1] <= 256
+        assert shape(d_in, 5120, 48, (0, 48), (0,))[0] == 1
+    for d_out in (12288, 34816, 5120):
+        for T in (1024, 2048, 2176, 4096, 16384):
+            assert shape(5120, d_out, T, (0, T // 2, T), (0, 1))[1] <= 256, (d_out, T)
+
+
 def test_launch_shape_of_an_empty_batch_and_bad_arguments(lib):
     from mixed_lora_projection_gb300 import LoraError, launch_shape
     assert launch_shape(256, 512, 16, 152, 0, [0], [])["fused_units"] == 0
