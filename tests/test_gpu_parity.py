@@ -374,11 +374,12 @@ def test_invalid_call_leaves_output_untouched(dev):
         assert ll.timing(1)[2] == 0
 
 
-@pytest.mark.parametrize("name", ["tiny", "mixed_batch", "sweep_qkv_multi", "prefix_tail_1552"])
+@pytest.mark.parametrize("name", ["tiny", "mixed_batch", "sweep_qkv_multi", "prefix_tail_1552", "sweep_down"])
 def test_host_buffers_path_matches_device_path(dev, name):
     # the host-buffer entry point pipelines row chunks (from 2,048 rows) over copy and compute
     # streams; each chunk is planned on its own rows, and a row's sums do not depend on the
-    # batch it is in, so the result is the device path's bit for bit
+    # batch it is in, so the result is the device path's bit for bit (sweep_down: the device call
+    # runs 288-column wide row tiles, its chunks narrower ones)
     w = WORKLOADS[name]
     inp = make_inputs(w, dev)
     x_host = inp.x.cpu().pin_memory()
