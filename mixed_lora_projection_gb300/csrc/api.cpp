@@ -487,17 +487,17 @@ double search_shape(const lora_linear* h, const Plan& plan, int cs, int tn, int 
             if (best < 0 || m < best * 0.999) { best = m; best_cs = c; best_tn = tn; }
             continue;
         }
-        // 256 columns, then (SM pairs) the wide tiles, then the narrower ones; a tie goes to the
-        // earlier. Wide tiles are weighed where 256-column units leave the last wave of SM pairs at
-        // most half full (their gains were measured there: 2,048 rows of o and down 17%, 1,024
-        // rows 8%, 2,176 rows of o 43%)
+        // Candidate widths in the order a tie goes to: 256 columns, then the wide tiles, then the
+        // narrower ones. Wide tiles are weighed on SM pairs where 256-column units leave the last
+        // wave at most half full (their gains were measured there: 2,048 rows of o and down 17%,
+        // 1,024 rows 8%, 2,176 rows of o 43%).
         const long long u256 = (long long)(fg.size() / c) * ceil_div(h->d_out, kMaxTileN) + (long long)(sg.size() / c);
         const double last = (double)(u256 % slots) / slots;
-        const bool wide_here = c == 2 && wide && last > 0.0 && last <= 0.5;
-        const int t_max = wide_here ? kMaxAutoWideTileN : kMaxTileN;
-        for (int i = 0; i <= (t_max - kMaxTileN) / 16 + (kMaxTileN - 128) / 16; ++i) {
-            const int t = i <= (t_max - kMaxTileN) / 16 ? kMaxTileN + 16 * i : kMaxTileN - 16 * (i - (t_max - kMaxTileN) / 16);
-            if (t > kMaxTileN && t < kMinAutoWideTileN) continue;
+        std::vector<int> widths{kMaxTileN};
+        if (c == 2 && wide && last > 0.0 && last <= 0.5)
+            for (int t = kMinAutoWideTileN; t <= kMaxAutoWideTileN; t += 16) widths.push_back(t);
+        for (int t = kMaxTileN - 16; t >= 128; t -= 16) widths.push_back(t);
+        for (const int t : widths) {
             const double m = makespan(h, fg, sg, c, t, shrink_n, slots, k_split);
             if (best < 0 || m < best * 0.999) { best = m; best_cs = c; best_tn = t; }
         }
