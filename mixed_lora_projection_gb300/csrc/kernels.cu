@@ -48,14 +48,16 @@
 // cycles between MMAs whatever their width), into the accumulator columns after the first MMA's;
 // one accumulator of up to 512 columns, so a unit's epilogue no longer overlaps the next unit's
 // MMAs.
-//   token-column units (FORM 1, p.yt): for batches of at most 512 rows on one adapter, a unit computes a
-//     block of Y^T: 256 output features (W rows as the A operand, 128 per CTA) for every token row
-//     of the batch (X rows as the B operand, half of them per CTA), so W is read once and no row
-//     tile is padded; the epilogue maps accumulator columns back to token rows through a per-warp
-//     shared-memory buffer;
-//   wide row tiles (FORM 2, tile_n of 272 to 512 columns): 256-row units as on SM pairs, with more output
-//     columns per unit, so that a projection's units fill whole waves of SM pairs (2,048 rows of
-//     a 5,120-column projection: 152 units of 272 columns, two waves, instead of 160 of 256).
+//   token-column units (FORM 1, p.yt): for batches of at most 512 rows on one adapter, a unit
+//     computes a block of Y^T: 256 output features (W rows as the A operand, 128 per CTA) for
+//     every token row of the batch (X rows as the B operand, half of them per CTA), so W is read
+//     once and no row tile is padded; the epilogue maps accumulator columns back to token rows
+//     through a per-warp shared-memory buffer;
+//   wide row tiles (FORM 2, tile_n of 272 to 512 columns): 256-row units as on SM pairs, with
+//     more output columns per unit, so that a projection's units fill whole waves of SM pairs
+//     (2,048 rows of a 5,120-column projection on 76 SM pairs: 144 units of 288 columns, two
+//     waves, instead of 160 of 256, three); the epilogue maps accumulator columns back to output
+//     columns in the order of the pair's B stage rows.
 // The sums keep their order whatever the unit's shape, so the bits equal those of 256-column
 // row tiles.
 //
