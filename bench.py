@@ -27,6 +27,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -51,19 +52,28 @@ def _peaks():
     return 1900.0, 1700.0, 6800.0, "fallback"
 
 
+def _code_only(text: str) -> str:
+    """Source text without its comments and blank lines: what the compiler reads (the device
+    sources hold no comment markers inside string literals)."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    lines = (line.split("//", 1)[0].rstrip() for line in text.splitlines())
+    return "\n".join(line for line in lines if line.strip())
+
+
 def _kernel_hash(w4: bool = False):
     """Hash of the code the GPU runs for the measured kernel: the device part of its source file
     (up to the end of its device namespace; the host launch code after it does not count), the
     device helpers and the parameter headers it compiles from (lora_internal.h, and lora_w4.h
-    for the 4-bit kernel)."""
+    for the 4-bit kernel), each without comments and blank lines, so that an edit of a comment
+    does not retire a capture of the same code."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "mixed_lora_projection_gb300", "csrc")
     with open(os.path.join(csrc, "kernels_w4.cu" if w4 else "kernels.cu")) as fh:
         text = fh.read()
-    h.update(text[:text.index("}  // namespace dev")].encode())
+    h.update(_code_only(text[:text.index("}  // namespace dev")]).encode())
     for f in ("dev_common.cuh", "lora_internal.h") + (("lora_w4.h",) if w4 else ()):
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(csrc, f)) as fh:
+            h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 
