@@ -200,3 +200,77 @@ def test_options_that_rule_out_wide_tiles(dev):
                 ll.set_option(opt, v)
     assert rel_err(y, oracle_full(inp, off, ids)) <= TOL
     assert rel_err(y256, oracle_full(inp, off, ids)) <= TOL
+
+
+@pytest.mark.parametrize("variant", ["raster1", "raster2", "raster3", "two_launch", "uploaded_list", "mma_group1",
+                                     "max_ctas100"])
+def test_wide_tiles_under_launch_options(dev, variant):
+    # 320-column wide tiles under every launch option that touches their path (unit orders, the
+    # shrink as its own launch, the work list uploaded instead of in the parameters, one stage per
+    # MMA wait, a cap of 100 SMs) give the bits of 256-column tiles; the plain call matches the oracle
+    from mixed_lora_projection_gb300 import _lib as L
+    T = 1536
+    off, ids = [0, 400, 1000, T], [0, 1, 2]
+    w = Workload("wide_opts", 47, T, 640, 2000, 64, tuple(off), tuple(ids), n_adapters=2, scales=(0.5, 1.5))
+    inp = make_inputs(w, dev)
+    with _ll(w) as ll:
+        ll.set_option(L.OPT_TILE_N, 256)
+        ref = run(ll, inp, off, ids).clone()
+        ll.set_option(L.OPT_TILE_N, 320)
+        plain = run(ll, inp, off, ids).clone()
+        if variant.startswith("raster"):
+            ll.set_option(L.OPT_RASTER, int(variant[-1]))
+            ll.set_option(L.OPT_RASTER_GROUP, 3)
+        elif variant == "two_launch":
+            ll.set_option(L.OPT_TWO_LAUNCH, 1)
+        elif variant == "uploaded_list":
+            ll.set_option(L.OPT_INLINE_WORK_LIST, 0)
+        elif variant == "mma_group1":
+            ll.set_option(L.OPT_MMA_GROUP, 1)
+        else:
+            ll.set_option(L.OPT_MAX_CTAS, 100)
+        assert _tile_n(ll, T, off, ids) == 320
+        y = run(ll, inp, off, ids)
+        torch.cuda.synchronize()
+        assert ll.status() == 0
+    assert torch.equal(plain, ref)
+    assert torch.equal(y, ref)
+    assert rel_err(plain, oracle_full(inp, off, ids)) <= TOL
+
+
+def test_two_wide_calls_side_by_side(dev):
+    # the 2,048-row down projection as one call (288-column wide tiles on every SM pair), and as two
+    # calls of 1,024 rows on two streams capped to 76 SMs each (wide tiles too): the same bits
+    from mixed_lora_projection_gb300 import LoraLinear, _lib as L
+    w = WORKLOADS["sweep_down"]
+    inp = make_inputs(w, dev)
+    off, ids = list(w.seg_offsets), list(w.seg_ids)
+    y = torch.empty((w.T, w.d_out), dtype=torch.bfloat16, device=dev)
+    main = torch.cuda.current_stream(dev)
+    sa, sb = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    # rows 0..1023 and 1024..2047 in the batch's own segments
+    cut = 1024
+    oa, ia, ob, ib = [0], [], [0], []
+    for k in range(len(ids)):
+        lo, hi = off[k], off[k + 1]
+        if lo < cut:
+            oa.append(min(hi, cut)); ia.append(ids[k])
+        if hi > cut:
+            ob.append(hi - max(lo, cut) + ob[-1]); ib.append(ids[k])
+    with LoraLinear(w.d_in, w.d_out, w.rank, w.T, 16, 0) as one, \
+            LoraLinear(w.d_in, w.d_out, w.rank, cut, 16, 0) as ha, LoraLinear(w.d_in, w.d_out, w.rank, cut, 16, 0) as hb:
+        assert _tile_n(one, w.T, off, ids) == 288
+        ref = run(one, inp, off, ids).clone()
+        for h in (ha, hb):
+            h.set_option(L.OPT_MAX_CTAS, 76)
+            h.set_option(L.OPT_TILE_N, 288)
+        for _ in range(3):
+            sa.wait_stream(main)
+            sb.wait_stream(main)
+            ha.forward(inp.x[:cut], oa, ia, inp.w, inp.a, inp.b, inp.scales, y=y[:cut], stream=sa)
+            hb.forward(inp.x[cut:], ob, ib, inp.w, inp.a, inp.b, inp.scales, y=y[cut:], stream=sb)
+            main.wait_stream(sa)
+            main.wait_stream(sb)
+        torch.cuda.synchronize()
+        assert ha.status() == 0 and hb.status() == 0
+    assert torch.equal(y, ref)
